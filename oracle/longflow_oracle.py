@@ -82,20 +82,18 @@ def choose_victim(scores: np.ndarray, pos: np.ndarray, next_pos: int, window: in
     Pre-Allocation and In-Place Eviction", step 2).
 
     Candidates are slots whose position is older than the protected window,
-    pos_i < next_pos - window.  Exact ties go to the lowest slot index.
+    pos_i < next_pos - window.  They are sorted by score with a stable sort, so
+    equal scores stay in slot order and an exact tie goes to the lowest slot.
     Returns (victim slot, lowest score, second-lowest score or inf).
     """
     scores = np.asarray(scores, np.float64)
-    cand = [i for i in range(len(scores)) if pos[i] < next_pos - window]
-    if not cand:
+    cand = np.flatnonzero(np.asarray(pos) < next_pos - window)
+    if cand.size == 0:
         raise ValueError("no eviction candidate: window covers every cached slot")
-    best = cand[0]
-    for i in cand[1:]:
-        if scores[i] < scores[best]:          # strict: an equal score keeps the lower slot
-            best = i
-    rest = sorted(scores[i] for i in cand if i != best)
-    second = rest[0] if rest else math.inf
-    return best, float(scores[best]), float(second)
+    order = cand[np.argsort(scores[cand], kind="stable")]
+    best = int(order[0])
+    second = float(scores[order[1]]) if order.size > 1 else math.inf
+    return best, float(scores[best]), second
 
 
 @dataclass

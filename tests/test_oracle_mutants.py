@@ -33,9 +33,11 @@ MUTANTS = {
         "return np.asarray(alpha_cached, np.float64).max(axis=0) *"),
     "score_index_shift": ("longflow_scores(alpha[:, :n], self.vnorm[:n])",
                           "longflow_scores(alpha[:, 1:], self.vnorm[:n])"),
-    "argmax_not_argmin": ("if scores[i] < scores[best]:", "if scores[i] > scores[best]:"),
-    "ties_to_highest": ("if scores[i] < scores[best]:", "if scores[i] <= scores[best]:"),
-    "window_off_by_one": ("if pos[i] < next_pos - window]", "if pos[i] <= next_pos - window]"),
+    "argmax_not_argmin": ('np.argsort(scores[cand], kind="stable")',
+                          'np.argsort(-scores[cand], kind="stable")'),
+    "ties_to_highest": ("cand = np.flatnonzero(np.asarray(pos) < next_pos - window)",
+                        "cand = np.flatnonzero(np.asarray(pos) < next_pos - window)[::-1]"),
+    "window_off_by_one": ("np.asarray(pos) < next_pos - window", "np.asarray(pos) <= next_pos - window"),
     "vnorm_l2": ("self.vnorm[slot] = np.abs(np.asarray(v, np.float64)).sum()",
                  "self.vnorm[slot] = np.sqrt((np.asarray(v, np.float64) ** 2).sum())"),
     "fill_wrong_slot": ("written = n            # initial fill: next free slot",
