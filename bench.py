@@ -1,0 +1,465 @@
+"""Benchmark of the LongFlow fused decode step (attention + score + eviction).
+
+One *step* = one decode token for every layer and sequence of the workload
+(layers x batch "units", one lf_decode_step launch per layer).  The metric is
+units per second ("fused decode steps/s (batch x layers)") and the achieved
+HBM bandwidth of the decode kernel against the measured copy peak.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle on the host cores (the reference
+arm: a deliberately slow, plain implementation of the same step).
+
+Multi-GPU: every rank runs an independent replica (the path has no exchange
+step); the time is the max over ranks and the value the units of all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused decode steps/s (batch·layers) and achieved HBM GB/s vs ~8 TB/s peak"
+UNIT = "units/s (unit = one (layer, sequence) decode step)"
+NOMINAL_HBM_GBS = 8000.0
+
+
+# ---------------------------------------------------------------------------
+# byte model (algorithmic bytes of one (layer, sequence) unit)
+# ---------------------------------------------------------------------------
+
+def unit_bytes(wl, n_slots: int, evict: bool = True, writes_slot: bool = True) -> int:
+    """K and V of the n occupied slots, their ||v||_1 and positions, q read,
+    out written, k_new / v_new read, and (when a slot is written) the new
+    token's K, V, ||v||_1, position plus the evicted index."""
+    e = wl.elem_bytes
+    hkv, hq, d = wl.kv_heads, wl.q_heads, wl.head_dim
+    b = 2 * hkv * n_slots * d * e + 8 * hkv * n_slots
+    b += 2 * hq * d * e + 2 * hkv * d * e
+    b += 4 * hkv  # evicted slot index
+    if writes_slot:
+        b += 2 * hkv * d * e + 8 * hkv
+    return b
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host cores (CPU baseline and reference arm)
+# ---------------------------------------------------------------------------
+
+def _oracle_worker(args):
+    """Run OracleSequence steps of one (layer, sequence) for `seconds` (or `steps`)."""
+    wl_name, overrides, seed, seconds, steps = args
+    import numpy as np
+    sys.path.insert(0, ROOT)
+    import oracle
+    from synth.workloads import get_workload
+    wl = get_workload(wl_name).scaled(**overrides)
+    rng = np.random.default_rng(seed)
+    seq = oracle.OracleSequence(wl.kv_heads, wl.q_heads, wl.budget, wl.head_dim, wl.budget,
+                                wl.window, evict=True)
+    P = wl.budget  # steady state: the buffer is full, every step evicts
+    k = rng.standard_normal((wl.kv_heads, P, wl.head_dim))
+    v = rng.standard_normal((wl.kv_heads, P, wl.head_dim))
+    seq.prefill(k, v)
+    q = rng.standard_normal((wl.q_heads, wl.head_dim))
+    done = 0
+    t0 = time.perf_counter()
+    while True:
+        q = wl.rho * q + 0.44 * rng.standard_normal(q.shape)
+        seq.step(q, rng.standard_normal((wl.kv_heads, wl.head_dim)),
+                 rng.standard_normal((wl.kv_heads, wl.head_dim)))
+        done += 1
+        el = time.perf_counter() - t0
+        if (steps and done >= steps) or (not steps and el >= seconds):
+            return done, el
+
+
+def run_oracle(wl_name: str, workers: int, seconds: float = 0.0, steps: int = 0):
+    import multiprocessing as mp
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"  # one core per worker process: `cores` is exact
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(workers) as pool:
+        res = pool.map(_oracle_worker, [(wl_name, {}, 1000 + i, seconds, steps)
+                                        for i in range(workers)])
+    units = sum(r[0] for r in res)
+    wall = max(r[1] for r in res)
+    return units, wall
+
+
+def cpu_baseline(wl_name: str, seconds: float):
+    cores = os.cpu_count() or 1
+    units, wall = run_oracle(wl_name, cores, seconds=seconds)
+    return {"value": units / wall, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{cores} spawn workers x ~{seconds:.0f} s each of fp64 oracle steps of one "
+                      f"{wl_name}-shaped (layer, sequence) at steady state (full buffer, every "
+                      f"step evicts); {units} units total"}
+
+
+def bench_reference(args):
+    """--impl reference: the oracle as the reference arm on the host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    cores = os.cpu_count() or 1
+    t_all = time.perf_counter()
+    # warm-up: W oracle steps per worker, untimed
+    if args.warmup:
+        run_oracle(args.workload, cores, steps=args.warmup)
+    units, wall = run_oracle(args.workload, cores, steps=args.steps)
+    value = units / wall
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "impl": "reference",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000.0 * wall / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"each of {cores} spawn workers runs {args.steps} fp64 "
+                                       f"oracle steps of one {args.workload}-shaped (layer, "
+                                       f"sequence) at steady state"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "wall_s": time.perf_counter() - t_all}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+
+def build_cache(wl, torch, lf, stream_mod, seed, evict=True, capacity=None, layers=None,
+                cluster=0, stages=0):
+    L = wl.layers if layers is None else layers
+    cap = capacity or wl.budget
+    cache = lf.LFCache(L, wl.batch, wl.kv_heads, wl.q_heads, wl.head_dim, cap, wl.window,
+                       dtype=wl.dtype, evict=evict, cluster=cluster, stages=stages)
+    gen = stream_mod.InputStream(wl, seed=seed, device="cuda", layers=list(range(L)))
+    for l in range(L):
+        k, v, lens = gen.prompt(l)
+        lens = [min(P, cap) for P in lens]
+        cache.prefill(l, k, v, lens)
+        del k, v
+    torch.cuda.synchronize()
+    return cache, gen
+
+
+def pregenerate(gen, steps, torch):
+    """Inputs of `steps` decode steps, resident in HBM: list of (q, k, v) per layer."""
+    out = []
+    for _ in range(steps):
+        qs, ks, vs = gen.next_step()
+        out.append((qs, ks, vs))
+    torch.cuda.synchronize()
+    return out
+
+
+def time_steps(cache, inputs, outs, evs, torch, graph: bool):
+    """Run len(inputs) steps; return elapsed ms measured with CUDA events."""
+    L = len(outs)
+    stream = torch.cuda.current_stream()
+
+    def launch_all():
+        for (qs, ks, vs) in inputs:
+            for l in range(L):
+                cache.decode_step(l, qs[l], ks[l], vs[l], outs[l], evs[l])
+
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            launch_all()
+        torch.cuda.synchronize()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(torch.cuda.current_stream())
+        g.replay()
+        end.record(torch.cuda.current_stream())
+        end.synchronize()
+        ms = start.elapsed_time(end)
+        del g
+        return ms
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    launch_all()
+    end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end)
+
+
+def bench_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from decode_kv_cache_gb300 import longflow as lf
+    from synth import workloads as stream_mod
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    from decode_kv_cache_gb300 import build as _b
+    if rank == 0 or world == 1:
+        _b.build()
+    if world > 1:
+        dist.barrier()
+    lf.load_library()
+
+    wl = stream_mod.get_workload(args.workload)
+    if args.layers:
+        wl = wl.scaled(layers=args.layers)
+    peak, peak_kind = load_peaks()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(x: float) -> float:
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    # ---- eviction on, steady state (cache pre-filled to the budget) ----
+    cache, gen = build_cache(wl, torch, lf, stream_mod, seed=rank, cluster=args.cluster,
+                             stages=args.stages)
+    L = wl.layers
+    outs = [torch.empty(wl.batch, wl.q_heads, wl.head_dim, dtype=cache.dtype, device="cuda")
+            for _ in range(L)]
+    evs = [torch.empty(wl.batch, wl.kv_heads, dtype=torch.int32, device="cuda") for _ in range(L)]
+    warm = pregenerate(gen, args.warmup, torch)
+    timed = pregenerate(gen, args.steps, torch)
+    time_steps(cache, warm, outs, evs, torch, graph=False)  # W untimed warm-up steps
+    del warm
+    if cache.check() != 0:
+        raise RuntimeError("device error during warm-up")
+    clocks = ClockSampler(local)
+    barrier()
+    clocks.start()
+    ms = time_steps(cache, timed, outs, evs, torch, graph=not args.eager)
+    barrier()
+    clk = clocks.stop()
+    ms = max_over_ranks(ms)
+    bits = cache.check()
+    if bits:
+        raise RuntimeError(f"device error word {bits} after the timed region")
+    units = wl.batch * L * args.steps
+    value = world * units / (ms / 1000.0)
+    launches = L * args.steps
+    b_unit = unit_bytes(wl, wl.budget)
+    bytes_per_launch = b_unit * wl.batch
+    achieved = bytes_per_launch / (ms / 1000.0 / launches) / 1e9
+    lay = cache.layout
+
+    # ---- e2e: host buffers, copies inside the timed region ----
+    e2e_steps = min(args.steps, args.e2e_steps)
+    host_in = []
+    for (qs, ks, vs) in timed[:e2e_steps]:
+        host_in.append(([t.cpu().pin_memory() for t in qs], [t.cpu().pin_memory() for t in ks],
+                        [t.cpu().pin_memory() for t in vs]))
+    dev_q = [torch.empty_like(t) for t in timed[0][0]]
+    dev_k = [torch.empty_like(t) for t in timed[0][1]]
+    dev_v = [torch.empty_like(t) for t in timed[0][2]]
+    host_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+    host_ev = [torch.empty(e.shape, dtype=e.dtype).pin_memory() for e in evs]
+    del timed
+    h2d = sum(t.numel() * t.element_size() for grp in host_in[0] for t in grp)
+    d2h = sum(t.numel() * t.element_size() for t in host_out + host_ev)
+    barrier()
+    st = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for (qs, ks, vs) in host_in:
+        for l in range(L):
+            dev_q[l].copy_(qs[l], non_blocking=True)
+            dev_k[l].copy_(ks[l], non_blocking=True)
+            dev_v[l].copy_(vs[l], non_blocking=True)
+            cache.decode_step(l, dev_q[l], dev_k[l], dev_v[l], outs[l], evs[l])
+            host_out[l].copy_(outs[l], non_blocking=True)
+            host_ev[l].copy_(evs[l], non_blocking=True)
+    e1.record(st)
+    e1.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1))
+    e2e_value = world * wl.batch * L * e2e_steps / (e2e_ms / 1000.0)
+    cache.close()
+    del cache, gen, host_in
+    torch.cuda.empty_cache()
+
+    # ---- eviction off: the same kernel over the full-length KV (read only) ----
+    full = None
+    if args.full_kv and wl.full_kv_capacity:
+        cap = wl.full_kv_capacity
+        fl = min(L, args.full_kv_layers)
+        wl_full = wl.scaled(prefill=cap, layers=fl)
+        need = 2 * fl * wl.batch * wl.kv_heads * cap * wl.head_dim * wl.elem_bytes
+        free = torch.cuda.mem_get_info()[0]
+        if need * 1.3 < free:
+            cfull, gfull = build_cache(wl_full, torch, lf, stream_mod, seed=rank + 100, evict=False,
+                                       capacity=cap, layers=fl)
+            outs_f = outs[:fl]
+            evs_f = evs[:fl]
+            fsteps = max(4, args.steps // 4)
+            warm = pregenerate(gfull, args.warmup, torch)
+            time_steps(cfull, warm, outs_f, evs_f, torch, graph=False)
+            del warm
+            tin = pregenerate(gfull, fsteps, torch)
+            barrier()
+            fms = max_over_ranks(time_steps(cfull, tin, outs_f, evs_f, torch,
+                                            graph=not args.eager))
+            fb = unit_bytes(wl_full, cap, writes_slot=False) * wl.batch
+            full = {"value": world * wl.batch * fl * fsteps / (fms / 1000.0), "unit": UNIT,
+                    "layers": fl, "steps": fsteps, "capacity": cap,
+                    "ms_per_layer_step": fms / (fl * fsteps),
+                    "achieved_gbs": fb / (fms / 1000.0 / (fl * fsteps)) / 1e9}
+            cfull.close()
+            del tin
+        else:
+            full = {"skipped": f"needs {need / 1e9:.1f} GB, {free / 1e9:.1f} GB free"}
+
+    if rank != 0:
+        return 0
+    cpu = None
+    if not args.no_cpu_baseline:
+        cpu = cpu_baseline(args.workload, args.cpu_seconds)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if
+        wl.dtype == "bf16" else "f32", "data": "synthetic",
+        "config": {"workload": wl.name, "layers": L, "batch": wl.batch, "q_heads": wl.q_heads,
+                   "kv_heads": wl.kv_heads, "head_dim": wl.head_dim, "budget": wl.budget,
+                   "window": wl.window, "state": "steady (pre-filled to the budget, every step "
+                   "evicts)", "l2": "inputs larger than L2: each layer's slab is "
+                   f"{wl.batch * wl.kv_heads * lay.slot_stride * wl.head_dim * 2 * wl.elem_bytes / 1e6:.0f} MB",
+                   "cluster": lay.cluster, "stages": lay.stages,
+                   "launch": "eager" if args.eager else "CUDA graph of all timed steps",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind,
+                     "frac_of_nominal_8000": achieved / NOMINAL_HBM_GBS,
+                     "traffic": None, "kernel": "decode_step_kernel<bf16,128,4>",
+                     "bytes_per_launch": bytes_per_launch,
+                     "timing": "timed region / launches (includes launch gaps)"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "full_kv": full,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=128)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="qwen3-8b-steady")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--layers", type=int, default=0, help="override the layer count")
+    ap.add_argument("--cluster", type=int, default=0)
+    ap.add_argument("--stages", type=int, default=0)
+    ap.add_argument("--eager", action="store_true", help="launch eagerly instead of a CUDA graph")
+    ap.add_argument("--e2e-steps", type=int, default=32)
+    ap.add_argument("--full-kv", dest="full_kv", action="store_true", default=True)
+    ap.add_argument("--no-full-kv", dest="full_kv", action="store_false")
+    ap.add_argument("--full-kv-layers", type=int, default=8)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return bench_reference(args)
+    return bench_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,457 @@
+// C ABI of the LongFlow fused decode step: cache creation, prefill, decode,
+// error checks and the slab layout.  Declarations and semantics are in
+// include/longflow.h.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <climits>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+
+#include "lf_decode.cuh"
+#include "lf_kernels.h"
+#include "longflow.h"
+
+struct lf_cache {
+  int layers, batch, kv_heads, q_heads, head_dim, capacity, slot_stride, window;
+  int dtype, evict, cluster, stages, chunk, smem, device;
+  size_t elem_bytes;
+  void* K;
+  void* V;
+  float* vnorm;
+  int32_t* pos;
+  int32_t* count;
+  int32_t* next_pos;
+  int32_t* budget;
+  int32_t* err;
+  int32_t* plen;  // [layers][batch] prompt lengths uploaded by lf_prefill_fill
+  void* small;    // one allocation holding vnorm..plen
+  lf::KernelEntry kern;
+};
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  const int code = (e == cudaErrorMemoryAllocation) ? LF_ERR_OOM : LF_ERR_CUDA;
+  (void)cudaGetLastError();  // clear a non-sticky error
+  return fail(code, "%s: %s", what, cudaGetErrorString(e));
+}
+
+inline size_t round_up(size_t x, size_t m) { return (x + m - 1) / m * m; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Largest CTA count per cluster the launch can keep resident at least once.
+bool cluster_fits(const void* fn, int cluster, int kv_heads, int batch, int smem) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cluster, kv_heads, batch);
+  cfg.blockDim = dim3(lf::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  return n > 0;
+}
+
+void destroy_memory(lf_cache* c) {
+  if (c->K) cudaFree(c->K);
+  if (c->V) cudaFree(c->V);
+  if (c->small) cudaFree(c->small);
+  c->K = c->V = c->small = nullptr;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* lf_last_error(void) { return g_last_error.c_str(); }
+
+int lf_abi_version(void) { return LF_ABI_VERSION; }
+
+lf_cache* lf_cache_create(int layers, int batch, int kv_heads, int q_heads, int head_dim,
+                          int budget, int window) {
+  return lf_cache_create_ex(layers, batch, kv_heads, q_heads, head_dim, budget, window, nullptr);
+}
+
+lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, int head_dim,
+                             int capacity, int window, const lf_config* cfg) {
+  g_last_error.clear();
+  lf_config def = {LF_BF16, 1, nullptr, 0, 0};
+  const lf_config c = cfg ? *cfg : def;
+  if (layers < 1 || batch < 1 || kv_heads < 1 || q_heads < 1 || capacity < 1 || window < 0) {
+    fail(LF_ERR_ARG, "layers, batch, heads and capacity must be >= 1 and window >= 0");
+    return nullptr;
+  }
+  if (batch > 65535 || kv_heads > 65535) {
+    fail(LF_ERR_ARG, "batch and kv_heads must be <= 65535");
+    return nullptr;
+  }
+  if (q_heads % kv_heads != 0) {
+    fail(LF_ERR_ARG, "q_heads (%d) must be a multiple of kv_heads (%d)", q_heads, kv_heads);
+    return nullptr;
+  }
+  if (c.dtype != LF_BF16 && c.dtype != LF_F32) {
+    fail(LF_ERR_ARG, "dtype must be LF_BF16 or LF_F32");
+    return nullptr;
+  }
+  if (c.evict != 0 && c.evict != 1) {
+    fail(LF_ERR_ARG, "evict must be 0 or 1");
+    return nullptr;
+  }
+  if (c.cluster != 0 && (c.cluster < 1 || c.cluster > lf::kMaxCluster ||
+                         (c.cluster & (c.cluster - 1)) != 0)) {
+    fail(LF_ERR_ARG, "cluster must be 0 (auto) or a power of two <= %d", lf::kMaxCluster);
+    return nullptr;
+  }
+  if (c.stages != 0 && (c.stages < 2 || c.stages > lf::kMaxStages)) {
+    fail(LF_ERR_ARG, "stages must be 0 (auto) or in [2, %d]", lf::kMaxStages);
+    return nullptr;
+  }
+  const int group = q_heads / kv_heads;
+  lf::KernelEntry kern;
+  const bool found = (c.dtype == LF_BF16) ? lf::find_kernels_bf16(head_dim, group, &kern)
+                                          : lf::find_kernels_f32(head_dim, group, &kern);
+  if (!found) {
+    fail(LF_ERR_UNSUPPORTED, "no kernel for head_dim %d and group size %d (built: head_dim "
+         "16/32/64/128, group 1/2/4/8)", head_dim, group);
+    return nullptr;
+  }
+  // Per-sequence budgets.
+  int min_budget = capacity;
+  if (c.budgets) {
+    for (int b = 0; b < batch; ++b) {
+      if (c.budgets[b] < 1 || c.budgets[b] > capacity) {
+        fail(LF_ERR_ARG, "budget[%d] = %d outside [1, capacity %d]", b, c.budgets[b], capacity);
+        return nullptr;
+      }
+      min_budget = std::min(min_budget, (int)c.budgets[b]);
+    }
+  }
+  if (c.evict && window >= min_budget) {
+    fail(LF_ERR_ARG, "window (%d) must be smaller than every budget (min %d)", window, min_budget);
+    return nullptr;
+  }
+  if (capacity > INT_MAX / 2) {
+    fail(LF_ERR_ARG, "capacity too large");
+    return nullptr;
+  }
+
+  int device = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) {
+    cuda_fail(e, "cudaGetDevice");
+    return nullptr;
+  }
+  int num_sms = 0, max_optin = 0;
+  if ((e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, device)) != cudaSuccess ||
+      (e = cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device)) !=
+          cudaSuccess) {
+    cuda_fail(e, "cudaDeviceGetAttribute");
+    return nullptr;
+  }
+  if ((e = cudaFuncSetAttribute(kern.decode, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                max_optin)) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(kern.decode, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) !=
+          cudaSuccess) {
+    cuda_fail(e, "cudaFuncSetAttribute");
+    return nullptr;
+  }
+
+  // Launch shape: a cluster of C CTAs splits each unit's slots.  Prefer the
+  // smallest C that gives at least 8 CTAs per SM over the grid, with at least
+  // 128 slots per CTA; the caller may force C and the ring depth.
+  const int units = batch * kv_heads;
+  const int stages = c.stages ? c.stages : 4;
+  int cluster = c.cluster;
+  if (cluster == 0) {
+    cluster = 1;
+    while (cluster < lf::kMaxCluster && (long long)units * cluster < 8LL * num_sms &&
+           (capacity + 2 * cluster - 1) / (2 * cluster) >= 128)
+      cluster *= 2;
+  }
+  int chunk = 0, smem = 0;
+  for (;;) {
+    chunk = (int)round_up((size_t)((capacity + cluster - 1) / cluster), 4);
+    smem = kern.smem_bytes(stages, chunk);
+    if (smem <= max_optin && cluster_fits(kern.decode, cluster, kv_heads, batch, smem)) break;
+    if (c.cluster != 0 || cluster >= lf::kMaxCluster) {
+      fail(LF_ERR_UNSUPPORTED, "launch does not fit: cluster %d, %d stages, %d slots per CTA need "
+           "%d bytes of shared memory (max %d)", cluster, stages, chunk, smem, max_optin);
+      return nullptr;
+    }
+    cluster *= 2;
+  }
+
+  lf_cache* cache = new (std::nothrow) lf_cache();
+  if (!cache) {
+    fail(LF_ERR_OOM, "host allocation failed");
+    return nullptr;
+  }
+  cache->layers = layers;
+  cache->batch = batch;
+  cache->kv_heads = kv_heads;
+  cache->q_heads = q_heads;
+  cache->head_dim = head_dim;
+  cache->capacity = capacity;
+  cache->slot_stride = (int)round_up((size_t)capacity, 32);
+  cache->window = window;
+  cache->dtype = c.dtype;
+  cache->evict = c.evict;
+  cache->cluster = cluster;
+  cache->stages = stages;
+  cache->chunk = chunk;
+  cache->smem = smem;
+  cache->device = device;
+  cache->elem_bytes = (size_t)kern.elem_bytes;
+  cache->kern = kern;
+
+  const size_t n_units = (size_t)layers * batch * kv_heads;
+  const size_t n_slots = n_units * cache->slot_stride;
+  const size_t kv_bytes = n_slots * head_dim * cache->elem_bytes;
+  // small block: vnorm, pos [n_slots]; count, next_pos [n_units]; budget [batch];
+  // err [1]; plen [layers*batch] -- each piece 256-byte aligned.
+  size_t off_vnorm = 0;
+  size_t off_pos = round_up(off_vnorm + n_slots * 4, 256);
+  size_t off_count = round_up(off_pos + n_slots * 4, 256);
+  size_t off_next = round_up(off_count + n_units * 4, 256);
+  size_t off_budget = round_up(off_next + n_units * 4, 256);
+  size_t off_err = round_up(off_budget + (size_t)batch * 4, 256);
+  size_t off_plen = round_up(off_err + 4, 256);
+  size_t small_bytes = round_up(off_plen + (size_t)layers * batch * 4, 256);
+
+  if ((e = cudaMalloc(&cache->K, kv_bytes)) != cudaSuccess ||
+      (e = cudaMalloc(&cache->V, kv_bytes)) != cudaSuccess ||
+      (e = cudaMalloc(&cache->small, small_bytes)) != cudaSuccess) {
+    cuda_fail(e, "cudaMalloc of the slab");
+    destroy_memory(cache);
+    delete cache;
+    return nullptr;
+  }
+  char* s = static_cast<char*>(cache->small);
+  cache->vnorm = reinterpret_cast<float*>(s + off_vnorm);
+  cache->pos = reinterpret_cast<int32_t*>(s + off_pos);
+  cache->count = reinterpret_cast<int32_t*>(s + off_count);
+  cache->next_pos = reinterpret_cast<int32_t*>(s + off_next);
+  cache->budget = reinterpret_cast<int32_t*>(s + off_budget);
+  cache->err = reinterpret_cast<int32_t*>(s + off_err);
+  cache->plen = reinterpret_cast<int32_t*>(s + off_plen);
+
+  // Empty state: no occupied slot, positions -1, ||v||_1 0, K/V zero.
+  int32_t* hb = new (std::nothrow) int32_t[batch];
+  if (!hb) {
+    fail(LF_ERR_OOM, "host allocation failed");
+    destroy_memory(cache);
+    delete cache;
+    return nullptr;
+  }
+  for (int b = 0; b < batch; ++b) hb[b] = c.budgets ? c.budgets[b] : capacity;
+  if ((e = cudaMemset(cache->small, 0, small_bytes)) != cudaSuccess ||
+      (e = cudaMemset(cache->pos, 0xff, n_slots * 4)) != cudaSuccess ||
+      (e = cudaMemset(cache->K, 0, kv_bytes)) != cudaSuccess ||
+      (e = cudaMemset(cache->V, 0, kv_bytes)) != cudaSuccess ||
+      (e = cudaMemcpy(cache->budget, hb, (size_t)batch * 4, cudaMemcpyHostToDevice)) !=
+          cudaSuccess ||
+      (e = cudaDeviceSynchronize()) != cudaSuccess) {
+    delete[] hb;
+    cuda_fail(e, "initialising the slab");
+    destroy_memory(cache);
+    delete cache;
+    return nullptr;
+  }
+  delete[] hb;
+  return cache;
+}
+
+int lf_cache_destroy(lf_cache* cache) {
+  g_last_error.clear();
+  if (!cache) return LF_OK;
+  destroy_memory(cache);
+  delete cache;
+  return LF_OK;
+}
+
+int lf_prefill_fill(lf_cache* cache, int layer, const void* k, const void* v,
+                    const int32_t* prompt_len, int max_prompt, lf_stream_t stream) {
+  g_last_error.clear();
+  if (!cache) return fail(LF_ERR_ARG, "null cache");
+  if (layer < 0 || layer >= cache->layers)
+    return fail(LF_ERR_ARG, "layer %d outside [0, %d)", layer, cache->layers);
+  if (!prompt_len) return fail(LF_ERR_ARG, "null prompt_len");
+  if (max_prompt < 0) return fail(LF_ERR_ARG, "max_prompt < 0");
+  int longest = 0;
+  for (int b = 0; b < cache->batch; ++b) {
+    const int P = prompt_len[b];
+    if (P < 0 || P > max_prompt)
+      return fail(LF_ERR_ARG, "prompt_len[%d] = %d outside [0, max_prompt %d]", b, P, max_prompt);
+    longest = std::max(longest, P);
+  }
+  // Limits need the budgets, which live on the device; the host mirror below
+  // is read back only here, outside any step.
+  int32_t* hb = new (std::nothrow) int32_t[cache->batch];
+  if (!hb) return fail(LF_ERR_OOM, "host allocation failed");
+  cudaError_t e = cudaMemcpy(hb, cache->budget, (size_t)cache->batch * 4, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) {
+    delete[] hb;
+    return cuda_fail(e, "reading budgets");
+  }
+  for (int b = 0; b < cache->batch; ++b) {
+    const int limit = cache->evict ? hb[b] : cache->capacity;
+    if (prompt_len[b] > limit) {
+      delete[] hb;
+      return fail(LF_ERR_ARG, "prompt_len[%d] = %d exceeds the buffer (%d); feed the rest "
+                  "through lf_decode_step", b, prompt_len[b], limit);
+    }
+  }
+  delete[] hb;
+  if (longest > 0 && (!k || !v)) return fail(LF_ERR_ARG, "null k or v");
+  if (longest > 0 && (!aligned16(k) || !aligned16(v)))
+    return fail(LF_ERR_ARG, "k and v must be 16-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t* dplen = cache->plen + (size_t)layer * cache->batch;
+  if ((e = cudaMemcpyAsync(dplen, prompt_len, (size_t)cache->batch * 4, cudaMemcpyHostToDevice,
+                           st)) != cudaSuccess)
+    return cuda_fail(e, "uploading prompt lengths");
+  const size_t layer_units = (size_t)cache->batch * cache->kv_heads;
+  const size_t layer_slots = layer_units * cache->slot_stride;
+  lf::PrefillArgs a;
+  a.k = k;
+  a.v = v;
+  a.plen = dplen;
+  a.K = static_cast<char*>(cache->K) + layer * layer_slots * cache->head_dim * cache->elem_bytes;
+  a.V = static_cast<char*>(cache->V) + layer * layer_slots * cache->head_dim * cache->elem_bytes;
+  a.vnorm = cache->vnorm + layer * layer_slots;
+  a.pos = cache->pos + layer * layer_slots;
+  a.count = cache->count + layer * layer_units;
+  a.next_pos = cache->next_pos + layer * layer_units;
+  a.kv_heads = cache->kv_heads;
+  a.max_prompt = max_prompt;
+  a.slot_stride = cache->slot_stride;
+  void* args[] = {&a};
+  e = cudaLaunchKernel(cache->kern.prefill, dim3(cache->kv_heads, cache->batch, 1),
+                       dim3(lf::kThreads, 1, 1), args, 0, st);
+  if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+  return LF_OK;
+}
+
+int lf_decode_step(lf_cache* cache, int layer, const void* q, const void* k_new,
+                   const void* v_new, void* out, int32_t* evicted_slot, lf_stream_t stream) {
+  if (!cache) return fail(LF_ERR_ARG, "null cache");
+  if (layer < 0 || layer >= cache->layers)
+    return fail(LF_ERR_ARG, "layer %d outside [0, %d)", layer, cache->layers);
+  if (!q || !k_new || !v_new || !out || !evicted_slot)
+    return fail(LF_ERR_ARG, "null q, k_new, v_new, out or evicted_slot");
+  if (!aligned16(q)) return fail(LF_ERR_ARG, "q must be 16-byte aligned");
+  const size_t layer_units = (size_t)cache->batch * cache->kv_heads;
+  const size_t layer_slots = layer_units * cache->slot_stride;
+  lf::DecodeArgs a;
+  a.q = q;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.out = out;
+  a.evicted = evicted_slot;
+  a.K = static_cast<char*>(cache->K) + layer * layer_slots * cache->head_dim * cache->elem_bytes;
+  a.V = static_cast<char*>(cache->V) + layer * layer_slots * cache->head_dim * cache->elem_bytes;
+  a.vnorm = cache->vnorm + layer * layer_slots;
+  a.pos = cache->pos + layer * layer_slots;
+  a.count = cache->count + layer * layer_units;
+  a.next_pos = cache->next_pos + layer * layer_units;
+  a.budget = cache->budget;
+  a.err = cache->err;
+  a.kv_heads = cache->kv_heads;
+  a.q_heads = cache->q_heads;
+  a.slot_stride = cache->slot_stride;
+  a.capacity = cache->capacity;
+  a.window = cache->window;
+  a.chunk = cache->chunk;
+  a.stages = cache->stages;
+  a.evict = cache->evict;
+  a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)cache->head_dim));
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cache->cluster, cache->kv_heads, cache->batch);
+  cfg.blockDim = dim3(lf::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = cache->smem;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cache->cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void* args[] = {&a};
+  cudaError_t e = cudaLaunchKernelExC(&cfg, cache->kern.decode, args);
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  return LF_OK;
+}
+
+int lf_cache_check(lf_cache* cache, lf_stream_t stream, int32_t* bits) {
+  g_last_error.clear();
+  if (bits) *bits = 0;
+  if (!cache) return fail(LF_ERR_ARG, "null cache");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t word = 0;
+  cudaError_t e;
+  if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  if ((e = cudaMemcpy(&word, cache->err, 4, cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e, "reading the error word");
+  if ((e = cudaMemset(cache->err, 0, 4)) != cudaSuccess ||
+      (e = cudaDeviceSynchronize()) != cudaSuccess)
+    return cuda_fail(e, "clearing the error word");
+  if (bits) *bits = word;
+  if (word != 0) return fail(LF_ERR_DEVICE, "device error word 0x%x", (unsigned)word);
+  return LF_OK;
+}
+
+int lf_cache_layout(const lf_cache* cache, lf_layout* out) {
+  g_last_error.clear();
+  if (!cache || !out) return fail(LF_ERR_ARG, "null cache or layout");
+  out->layers = cache->layers;
+  out->batch = cache->batch;
+  out->kv_heads = cache->kv_heads;
+  out->q_heads = cache->q_heads;
+  out->head_dim = cache->head_dim;
+  out->capacity = cache->capacity;
+  out->slot_stride = cache->slot_stride;
+  out->window = cache->window;
+  out->dtype = cache->dtype;
+  out->evict = cache->evict;
+  out->cluster = cache->cluster;
+  out->stages = cache->stages;
+  out->k = cache->K;
+  out->v = cache->V;
+  out->vnorm = cache->vnorm;
+  out->pos = cache->pos;
+  out->count = cache->count;
+  out->next_pos = cache->next_pos;
+  out->budget = cache->budget;
+  out->err = cache->err;
+  return LF_OK;
+}
+
+}  // extern "C"

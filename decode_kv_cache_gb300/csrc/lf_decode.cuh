@@ -1,0 +1,549 @@
+// The LongFlow fused decode step (attention + zero-cost score + in-place
+// eviction) and the prefill kernel, for sm_103a.
+//
+// One launch handles one layer for every (sequence, KV head) unit.  A
+// thread-block cluster of C CTAs owns one unit; CTA `rank` streams the slots
+// [rank*chunk, (rank+1)*chunk) of that unit:
+//
+//   phase A  K tiles (+ ||v||_1 and positions) arrive through a ring of
+//            1-D bulk TMA copies into shared memory; each warp computes the
+//            G query heads' logits of its slots and keeps them in shared
+//            memory (they are needed again for the exact score);
+//   softmax  the CTA's local max m_h and p_{h,i} = 2^(s_{h,i} - m_h), l_h;
+//   phase B  V tiles arrive through the same ring; o_h += p_{h,i} v_i;
+//   combine  the cluster exchanges (m_h, l_h) and the partial outputs through
+//            distributed shared memory, adds the new token as one more key,
+//            writes out_h, and scores every unprotected slot exactly:
+//            score_i = ||v_i||_1 * sum_h p_{h,i} 2^(m_h - M_h) / L_h;
+//   evict    the leader CTA takes the lowest (score, slot) over the cluster
+//            and overwrites that slot with the new token in place.
+//
+// Logits are kept pre-multiplied by log2(e) so every exponential is an exp2.
+// No global scratch is used, no CTA waits on another CTA except through the
+// hardware cluster barrier, and every mbarrier wait is bounded.
+#pragma once
+
+#include <cooperative_groups.h>
+#include <limits.h>
+#include <math.h>
+
+#include "lf_device.cuh"
+#include "longflow.h"
+
+namespace lf {
+namespace cg = cooperative_groups;
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kTile = 32;        // slots per staged tile
+constexpr int kMaxCluster = 16;
+constexpr int kMaxStages = 16;
+constexpr int kMaxGroup = 8;
+
+struct DecodeArgs {
+  const void* q;       // [batch][q_heads][D]
+  const void* k_new;   // [batch][kv_heads][D]
+  const void* v_new;   // [batch][kv_heads][D]
+  void* out;           // [batch][q_heads][D]
+  int32_t* evicted;    // [batch][kv_heads]
+  void* K;             // this layer's [batch][kv_heads][slot_stride][D]
+  void* V;
+  float* vnorm;        // this layer's [batch][kv_heads][slot_stride]
+  int32_t* pos;
+  int32_t* count;      // this layer's [batch][kv_heads]
+  int32_t* next_pos;
+  const int32_t* budget;  // [batch]
+  int32_t* err;
+  int kv_heads, q_heads, slot_stride, capacity, window, chunk, stages, evict;
+  float scale_log2;    // log2(e) / sqrt(D)
+};
+
+// Shared-memory plan, shared by the host (launch size) and the kernel.
+template <typename T, int D, int G>
+struct DecodePlan {
+  static constexpr int kStageData = kTile * D * (int)sizeof(T);
+  static constexpr int kStageBytes = kStageData + 2 * kTile * 4;  // + ||v||_1, pos
+  static constexpr int kPvTpr = D / 4;               // threads per V row (4 elements each)
+  static constexpr int kPvGroups = kThreads / kPvTpr;
+  static constexpr int kPvBufBytes = kPvGroups * G * D * 4;
+  // fixed header
+  static constexpr int kOffBars = 0;                  // kMaxStages mbarriers
+  static constexpr int kOffStats = 128;               // 6 x kMaxGroup floats
+  static constexpr int kOffBest = kOffStats + 6 * kMaxGroup * 4;  // kMaxCluster (score, slot, flag)
+  static constexpr int kOffRed = kOffBest + 3 * kMaxCluster * 4;  // kWarps x kMaxGroup floats + ints
+  static constexpr int kOffDecision = kOffRed + 2 * kWarps * kMaxGroup * 4;
+  static constexpr int kHeader = 2048;
+  static_assert(kOffDecision + 16 <= kHeader, "header overflow");
+  static constexpr int kOffOpart = kHeader;           // G x D floats
+  static constexpr int kOffRing = (kOffOpart + G * D * 4 + 127) / 128 * 128;
+
+  __host__ __device__ static constexpr int ring_bytes(int stages) {
+    return ((stages * kStageBytes > kPvBufBytes ? stages * kStageBytes : kPvBufBytes) + 127) / 128 *
+           128;
+  }
+  __host__ __device__ static constexpr int off_logits(int stages) {
+    return kOffRing + ring_bytes(stages);
+  }
+  __host__ __device__ static constexpr int off_weights(int stages, int chunk) {
+    return off_logits(stages) + chunk * G * 4;
+  }
+  __host__ __device__ static constexpr int smem_bytes(int stages, int chunk) {
+    return off_weights(stages, chunk) + chunk * 4;
+  }
+};
+
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeArgs a) {
+  using P = DecodePlan<T, D, G>;
+  constexpr int V = ElemTraits<T>::kPer16B;  // elements per 16-byte chunk
+  constexpr int NC = D / V;                  // chunks per row
+  constexpr int LPS = NC < 8 ? NC : 8;       // lanes sharing one slot's dot product
+  constexpr int CPL = NC / LPS;              // chunks per lane
+  constexpr int SPW = 32 / LPS;              // slots per warp pass
+  constexpr int SPP = kWarps * SPW;          // slots per CTA pass
+  static_assert(NC % LPS == 0 && 32 % LPS == 0, "bad row split");
+  static_assert(G <= kWarps && G <= kMaxGroup, "group too large");
+
+  cg::cluster_group cluster = cg::this_cluster();
+  const int C = (int)cluster.num_blocks();
+  const int rank = (int)cluster.block_rank();
+  const int g = blockIdx.y;
+  const int b = blockIdx.z;
+  const int unit = b * a.kv_heads + g;
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const int S = a.stages;
+
+  extern __shared__ __align__(1024) unsigned char smem[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P::kOffBars);
+  float* m_loc = reinterpret_cast<float*>(smem + P::kOffStats);
+  float* l_loc = m_loc + kMaxGroup;
+  float* s_new = l_loc + kMaxGroup;
+  float* cmul = s_new + kMaxGroup;
+  float* m_glb = cmul + kMaxGroup;
+  float* l_glb = m_glb + kMaxGroup;
+  float* best_s = reinterpret_cast<float*>(smem + P::kOffBest);
+  int* best_i = reinterpret_cast<int*>(best_s + kMaxCluster);
+  int* fail_in = best_i + kMaxCluster;
+  float* red = reinterpret_cast<float*>(smem + P::kOffRed);
+  int* red_i = reinterpret_cast<int*>(red + kWarps * kMaxGroup);
+  int* decision = reinterpret_cast<int*>(smem + P::kOffDecision);
+  float* o_part = reinterpret_cast<float*>(smem + P::kOffOpart);
+  unsigned char* ring = smem + P::kOffRing;
+  float* lg = reinterpret_cast<float*>(smem + P::off_logits(S));
+  float* wv = reinterpret_cast<float*>(smem + P::off_weights(S, a.chunk));
+
+  const int n = a.count[unit];
+  const int p = a.next_pos[unit];
+  const int bud = a.budget[b];
+  const bool state_ok = (n >= 0 && n <= a.capacity && p >= n);
+  const bool evicting = state_ok && a.evict && n >= bud;
+  const int s0 = rank * a.chunk;
+  const int s1 = state_ok ? min(s0 + a.chunk, n) : s0;
+  const int rows = max(0, s1 - s0);
+  const int ntile = (rows + kTile - 1) / kTile;
+  const int total = 2 * ntile;  // K tiles then V tiles through one ring
+
+  const size_t ubase = (size_t)unit * a.slot_stride;
+  const T* Ku = reinterpret_cast<const T*>(a.K) + ubase * D;
+  const T* Vu = reinterpret_cast<const T*>(a.V) + ubase * D;
+  const float* vnu = a.vnorm + ubase;
+  const int32_t* posu = a.pos + ubase;
+  const T* qg = reinterpret_cast<const T*>(a.q) + ((size_t)b * a.q_heads + (size_t)g * G) * D;
+  const T* kn = reinterpret_cast<const T*>(a.k_new) + (size_t)unit * D;
+  const T* vn = reinterpret_cast<const T*>(a.v_new) + (size_t)unit * D;
+
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+    fence_mbar_init();
+  }
+  if (tid < kMaxCluster) {
+    best_s[tid] = INFINITY;
+    best_i[tid] = INT_MAX;
+    fail_in[tid] = 0;
+  }
+  __syncthreads();
+
+  const uint64_t policy = l2_evict_first_policy();
+  auto issue = [&](int t) {
+    const int st = t % S;
+    const bool isK = t < ntile;
+    const int j = isK ? t : t - ntile;
+    const int r0 = s0 + j * kTile;
+    const int r = min(kTile, s1 - r0);
+    unsigned char* dst = ring + (size_t)st * P::kStageBytes;
+    const uint32_t data_bytes = (uint32_t)(r * D * (int)sizeof(T));
+    // ||v||_1 and pos are 4-byte fields: copy whole 16-byte groups (the slab's
+    // slot stride is a multiple of 32, so this stays inside the unit).
+    const uint32_t small_bytes = isK ? (uint32_t)(((r + 3) & ~3) * 4) : 0u;
+    mbar_arrive_expect_tx(&bars[st], data_bytes + 2u * small_bytes);
+    bulk_g2s(dst, (isK ? Ku : Vu) + (size_t)r0 * D, data_bytes, &bars[st], policy);
+    if (isK) {
+      bulk_g2s(dst + P::kStageData, vnu + r0, small_bytes, &bars[st], policy);
+      bulk_g2s(dst + P::kStageData + kTile * 4, posu + r0, small_bytes, &bars[st], policy);
+    }
+  };
+  int issued = 0;
+  if (tid == 0) {
+    issued = min(S, total);
+    for (int t = 0; t < issued; ++t) issue(t);
+  }
+
+  // This lane's slice of the group's queries, pre-scaled by log2(e)/sqrt(D).
+  const int sub = lane % LPS;
+  const int rsl = lane / LPS;
+  float qr[G][CPL * V];
+#pragma unroll
+  for (int h = 0; h < G; ++h)
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) {
+      load16_f32(qg + (size_t)h * D + (sub + LPS * c) * V, &qr[h][c * V]);
+#pragma unroll
+      for (int v = 0; v < V; ++v) qr[h][c * V + v] *= a.scale_log2;
+    }
+
+  const int plim = p - a.window;  // a slot is a candidate iff pos < plim
+  const int pv_e0 = (tid % P::kPvTpr) * 4;
+  const int pv_grp = tid / P::kPvTpr;
+  float pv[G][4];
+#pragma unroll
+  for (int h = 0; h < G; ++h)
+#pragma unroll
+    for (int v = 0; v < 4; ++v) pv[h][v] = 0.f;
+
+  bool failed = false;
+  int t_stop = total;
+  for (int t = 0; t < total; ++t) {
+    const int st = t % S;
+    bool ok = mbar_wait_bounded(&bars[st], (uint32_t)((t / S) & 1));
+    ok = __all_sync(0xffffffffu, ok);
+    const unsigned char* stage = ring + (size_t)st * P::kStageBytes;
+    const bool isK = t < ntile;
+    const int j = isK ? t : t - ntile;
+    const int off = j * kTile;
+    const int r = min(kTile, rows - off);
+    if (ok && isK) {
+      const T* Kt = reinterpret_cast<const T*>(stage);
+#pragma unroll
+      for (int ps = 0; ps < kTile; ps += SPP) {
+        const int rr = ps + warp * SPW + rsl;
+        float acc[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) acc[h] = 0.f;
+        if (rr < r) {
+#pragma unroll
+          for (int c = 0; c < CPL; ++c) {
+            float x[V];
+            load16_f32(Kt + (size_t)rr * D + (sub + LPS * c) * V, x);
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+#pragma unroll
+              for (int v = 0; v < V; ++v) acc[h] = fmaf(qr[h][c * V + v], x[v], acc[h]);
+          }
+        }
+#pragma unroll
+        for (int o = 1; o < LPS; o <<= 1)
+#pragma unroll
+          for (int h = 0; h < G; ++h) acc[h] += __shfl_xor_sync(0xffffffffu, acc[h], o);
+        if (rr < r) {
+#pragma unroll
+          for (int h = 0; h < G; ++h)
+            if (sub == h % LPS) lg[(size_t)(off + rr) * G + h] = acc[h];
+        }
+      }
+      const float* vn_t = reinterpret_cast<const float*>(stage + P::kStageData);
+      const int32_t* pos_t = reinterpret_cast<const int32_t*>(stage + P::kStageData + kTile * 4);
+      if (tid < r) wv[off + tid] = (pos_t[tid] < plim) ? vn_t[tid] : -1.0f;
+    } else if (ok) {
+      const T* Vt = reinterpret_cast<const T*>(stage);
+      for (int rr = pv_grp; rr < r; rr += P::kPvGroups) {
+        float x[4];
+        load4_f32(Vt + (size_t)rr * D + pv_e0, x);
+        const float* pp = lg + (size_t)(off + rr) * G;
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float ph = pp[h];
+#pragma unroll
+          for (int v = 0; v < 4; ++v) pv[h][v] = fmaf(ph, x[v], pv[h][v]);
+        }
+      }
+    }
+    failed = failed || !ok;
+    if (__syncthreads_or(failed)) {  // uniform: every thread leaves together
+      t_stop = t;
+      break;
+    }
+    if (tid == 0 && t + S < total) {
+      issue(t + S);
+      issued = t + S + 1;
+    }
+    if (t == ntile - 1) {
+      // Local softmax statistics over this CTA's slots: m_h, p = 2^(s - m_h), l_h.
+      float mx[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) mx[h] = -INFINITY;
+      for (int i = tid; i < rows; i += kThreads)
+#pragma unroll
+        for (int h = 0; h < G; ++h) mx[h] = fmaxf(mx[h], lg[(size_t)i * G + h]);
+#pragma unroll
+      for (int h = 0; h < G; ++h) mx[h] = warp_max(mx[h]);
+      if (lane == 0)
+#pragma unroll
+        for (int h = 0; h < G; ++h) red[warp * kMaxGroup + h] = mx[h];
+      __syncthreads();
+      if (tid < G) {
+        float m = -INFINITY;
+        for (int w = 0; w < kWarps; ++w) m = fmaxf(m, red[w * kMaxGroup + tid]);
+        m_loc[tid] = m;
+      }
+      __syncthreads();
+      float sm[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) sm[h] = 0.f;
+      for (int i = tid; i < rows; i += kThreads)
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float e = exp2f(lg[(size_t)i * G + h] - m_loc[h]);
+          lg[(size_t)i * G + h] = e;
+          sm[h] += e;
+        }
+#pragma unroll
+      for (int h = 0; h < G; ++h) sm[h] = warp_sum(sm[h]);
+      if (lane == 0)
+#pragma unroll
+        for (int h = 0; h < G; ++h) red[warp * kMaxGroup + h] = sm[h];
+      __syncthreads();
+      if (tid < G) {
+        float s = 0.f;
+        for (int w = 0; w < kWarps; ++w) s += red[w * kMaxGroup + tid];
+        l_loc[tid] = s;
+      }
+      __syncthreads();
+    }
+  }
+  const bool aborted = (t_stop < total);
+  if (aborted && tid == 0) {
+    // Retire every copy still in flight into our shared memory, then report.
+    for (int t = t_stop; t < issued; ++t)
+      (void)mbar_wait_bounded(&bars[t % S], (uint32_t)((t / S) & 1));
+    atomicOr(a.err, LF_DEVERR_TIMEOUT);
+  }
+  if (rows == 0 || aborted) {
+    if (tid < G) {
+      m_loc[tid] = -INFINITY;
+      l_loc[tid] = 0.f;
+    }
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+      for (int v = 0; v < 4; ++v) pv[h][v] = 0.f;
+  }
+
+  // Reduce the partial outputs of the P.V thread groups (the ring is idle now).
+  float* pvbuf = reinterpret_cast<float*>(ring);
+  __syncthreads();
+#pragma unroll
+  for (int h = 0; h < G; ++h)
+#pragma unroll
+    for (int v = 0; v < 4; ++v) pvbuf[((size_t)pv_grp * G + h) * D + pv_e0 + v] = pv[h][v];
+  __syncthreads();
+  for (int idx = tid; idx < G * D; idx += kThreads) {
+    float s = 0.f;
+    for (int grp = 0; grp < P::kPvGroups; ++grp) s += pvbuf[(size_t)grp * G * D + idx];
+    o_part[idx] = s;
+  }
+  // The new token's logits, computed redundantly by every CTA of the cluster.
+  if (warp < G) {
+    float s = 0.f;
+    for (int e = lane; e < D; e += 32) s = fmaf(to_f32(qg[(size_t)warp * D + e]), to_f32(kn[e]), s);
+    s = warp_sum(s);
+    if (lane == 0) s_new[warp] = s * a.scale_log2;
+  }
+  // #1: every CTA has started (DSMEM may be touched from here on) and its
+  // m_loc, l_loc and o_part are visible to the cluster.
+  cluster.sync();
+  if (tid == 0 && aborted) *cluster.map_shared_rank(&fail_in[rank], 0) = 1;
+
+  if (tid < G) {
+    const int h = tid;
+    float M = s_new[h];
+    for (int r = 0; r < C; ++r) M = fmaxf(M, *cluster.map_shared_rank(&m_loc[h], r));
+    float L = exp2f(s_new[h] - M);
+    for (int r = 0; r < C; ++r) {
+      const float mr = *cluster.map_shared_rank(&m_loc[h], r);
+      if (mr != -INFINITY) L += *cluster.map_shared_rank(&l_loc[h], r) * exp2f(mr - M);
+    }
+    m_glb[h] = M;
+    l_glb[h] = L;
+    cmul[h] = (m_loc[h] != -INFINITY) ? exp2f(m_loc[h] - M) / L : 0.f;
+    if (!(isfinite(M) && isfinite(L) && L > 0.f)) atomicOr(a.err, LF_DEVERR_NONFINITE);
+  }
+  __syncthreads();
+
+  // Output: the cluster's threads share the G x D elements.
+  {
+    T* og = reinterpret_cast<T*>(a.out) + ((size_t)b * a.q_heads + (size_t)g * G) * D;
+    for (int idx = rank * kThreads + tid; idx < G * D; idx += C * kThreads) {
+      const int h = idx / D;
+      const int e = idx - h * D;
+      float acc = exp2f(s_new[h] - m_glb[h]) * to_f32(vn[e]);
+      for (int r = 0; r < C; ++r) {
+        const float mr = *cluster.map_shared_rank(&m_loc[h], r);
+        if (mr != -INFINITY) acc += *cluster.map_shared_rank(&o_part[idx], r) * exp2f(mr - m_glb[h]);
+      }
+      from_f32(acc / l_glb[h], &og[(size_t)h * D + e]);
+    }
+  }
+
+  // Exact LongFlow scores of this CTA's candidates and their (score, slot) minimum.
+  float bs = INFINITY;
+  int bi = INT_MAX;
+  if (evicting && !aborted) {
+    for (int i = tid; i < rows; i += kThreads) {
+      const float w = wv[i];
+      if (w >= 0.f) {
+        float acc = 0.f;
+#pragma unroll
+        for (int h = 0; h < G; ++h) acc = fmaf(lg[(size_t)i * G + h], cmul[h], acc);
+        const float sc = w * acc;
+        if (better(sc, s0 + i, bs, bi)) {
+          bs = sc;
+          bi = s0 + i;
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float os = __shfl_xor_sync(0xffffffffu, bs, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    if (better(os, oi, bs, bi)) {
+      bs = os;
+      bi = oi;
+    }
+  }
+  if (lane == 0) {
+    red[warp] = bs;
+    red_i[warp] = bi;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    for (int w = 1; w < kWarps; ++w)
+      if (better(red[w], red_i[w], bs, bi)) {
+        bs = red[w];
+        bi = red_i[w];
+      }
+    *cluster.map_shared_rank(&best_s[rank], 0) = bs;
+    *cluster.map_shared_rank(&best_i[rank], 0) = bi;
+  }
+  cluster.sync();  // #2: all slot reads of the step are done; minima are at the leader
+  if (rank != 0) return;
+
+  if (tid == 0) {
+    bool any_fail = false;
+    for (int r = 0; r < C; ++r) any_fail = any_fail || fail_in[r] != 0;
+    int victim = -1;
+    if (evicting) {
+      float fs = INFINITY;
+      int fi = INT_MAX;
+      for (int r = 0; r < C; ++r)
+        if (better(best_s[r], best_i[r], fs, fi)) {
+          fs = best_s[r];
+          fi = best_i[r];
+        }
+      if (fi != INT_MAX) victim = fi;
+      else if (!any_fail) atomicOr(a.err, LF_DEVERR_STATE);  // no candidate
+    }
+    const int limit = a.evict ? bud : a.capacity;
+    int slot = evicting ? victim : (n < limit ? n : -1);
+    if (!state_ok) atomicOr(a.err, LF_DEVERR_STATE);
+    if (any_fail || !state_ok) {
+      slot = -1;
+      victim = -1;
+    }
+    decision[0] = slot;
+    decision[1] = victim;
+    a.evicted[unit] = victim;
+    if (state_ok && !any_fail) {
+      if (!evicting && slot >= 0) a.count[unit] = n + 1;
+      a.next_pos[unit] = p + 1;
+    }
+  }
+  __syncthreads();
+  const int slot = decision[0];
+  if (slot >= 0) {
+    // In-place overwrite of one slot: K, V, ||v||_1 (fp32, from the stored value), position.
+    T* Kd = reinterpret_cast<T*>(a.K) + (ubase + slot) * D;
+    T* Vd = reinterpret_cast<T*>(a.V) + (ubase + slot) * D;
+    for (int e = tid; e < D; e += kThreads) {
+      Kd[e] = kn[e];
+      Vd[e] = vn[e];
+    }
+    if (warp == 0) {
+      float s = 0.f;
+      for (int e = lane; e < D; e += 32) s += fabsf(to_f32(vn[e]));
+      s = warp_sum(s);
+      if (lane == 0) {
+        a.vnorm[ubase + slot] = s;
+        a.pos[ubase + slot] = p;
+      }
+    }
+  }
+}
+
+// ---- prefill ----------------------------------------------------------------
+
+struct PrefillArgs {
+  const void* k;          // [batch][kv_heads][max_prompt][D]
+  const void* v;
+  const int32_t* plen;    // [batch]
+  void* K;                // this layer's slab
+  void* V;
+  float* vnorm;
+  int32_t* pos;
+  int32_t* count;
+  int32_t* next_pos;
+  int kv_heads, max_prompt, slot_stride;
+};
+
+// grid (kv_heads, batch); one CTA copies one unit's prompt rows.
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads) prefill_kernel(const PrefillArgs a) {
+  const int g = blockIdx.x;
+  const int b = blockIdx.y;
+  const int unit = b * a.kv_heads + g;
+  const int P = a.plen[b];
+  const size_t src0 = (size_t)unit * a.max_prompt * D;
+  const size_t dst0 = (size_t)unit * a.slot_stride * D;
+  // Rows 0..P-1 are contiguous on both sides: copy them as 16-byte words.
+  const size_t words = (size_t)P * D * sizeof(T) / 16;
+  const uint4* ks = reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(a.k) + src0);
+  const uint4* vs = reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(a.v) + src0);
+  uint4* kd = reinterpret_cast<uint4*>(reinterpret_cast<T*>(a.K) + dst0);
+  uint4* vd = reinterpret_cast<uint4*>(reinterpret_cast<T*>(a.V) + dst0);
+  for (size_t w = threadIdx.x; w < words; w += kThreads) {
+    kd[w] = ks[w];
+    vd[w] = vs[w];
+  }
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const T* vrow0 = reinterpret_cast<const T*>(a.v) + src0;
+  const size_t ubase = (size_t)unit * a.slot_stride;
+  for (int i = warp; i < a.slot_stride; i += kWarps) {
+    float s = 0.f;
+    if (i < P)
+      for (int e = lane; e < D; e += 32) s += fabsf(to_f32(vrow0[(size_t)i * D + e]));
+    s = warp_sum(s);
+    if (lane == 0) {
+      a.vnorm[ubase + i] = (i < P) ? s : 0.f;
+      a.pos[ubase + i] = (i < P) ? i : -1;
+    }
+  }
+  if (threadIdx.x == 0) {
+    a.count[unit] = P;
+    a.next_pos[unit] = P;
+  }
+}
+
+}  // namespace lf

@@ -1,0 +1,172 @@
+/*
+ * longflow.h -- C ABI of the LongFlow fused decode step on a static KV slab.
+ *
+ * The operation (one call = one layer, every sequence of the batch):
+ *
+ *   for every sequence b and KV head g, with the G = q_heads / kv_heads query
+ *   heads h in g's group (query head h reads KV head floor(h / G)):
+ *     s_{h,i}  = (q_h . k_i) / sqrt(d)   over the n cached slots i and the new token
+ *     alpha    = softmax_i(s_{h,i})      (the new token attends to itself)
+ *     out_h    = sum_i alpha_{h,i} v_i
+ *       -- "LongFlow Guide: KV Cache Compression for Reasoning AI", section
+ *          "Mathematical Derivation of the LongFlow Score", alpha_{t,i} and o_t;
+ *     score_i  = ||v_i||_1 * sum_{h in group} alpha_{h,i}
+ *       -- same section, Score_LongFlow(i) = ||c_{t,i}||_1 = alpha_{t,i} ||v_i||_1,
+ *          and "LongFlow: Efficient KV Cache Compression for Reasoning M"
+ *          (gist.science summary), section 2.1, LongFlowScore(t_i) = alpha_i^t ||v_i||_1;
+ *     if n < budget_b:   the new token takes slot n           (initial fill)
+ *     else:              victim e = argmin score_i over slots whose position is
+ *                        older than the protected window (pos_i < p - window),
+ *                        exact ties to the lowest slot; the new token's K, V,
+ *                        ||v||_1 and position overwrite slot e in place
+ *       -- guide, section "Static Memory Pre-Allocation and In-Place Eviction",
+ *          steps 1-3; summary, section 2.3 "Static KV Cache" / "Fused Kernel".
+ *
+ * Storage: one static slab per cache, allocated once by lf_cache_create*,
+ * never grown, moved or compacted.  All per-step work is stream-ordered and
+ * asynchronous: no call below synchronises the host except lf_cache_check,
+ * lf_prefill_fill's upload of the host prompt lengths, and create/destroy.
+ *
+ * Threading: a cache may be used from any host thread, but calls touching the
+ * same layer must be ordered by the caller (same stream, or events).
+ * Device: every call must run with the device that was current at create.
+ *
+ * Errors: functions return LF_OK (0) or a negative lf_status and set a
+ * thread-local message (lf_last_error).  Conditions detected on the device
+ * (non-finite inputs, corrupted state, an expired bounded wait) are OR-ed
+ * into a per-cache error word read and cleared by lf_cache_check.  No kernel
+ * traps or waits without a bound.
+ */
+#ifndef LONGFLOW_H_
+#define LONGFLOW_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define LF_ABI_VERSION 1
+
+typedef struct lf_cache lf_cache; /* opaque; owns the slab */
+
+/* A cudaStream_t passed as a plain pointer; NULL is the legacy default stream. */
+typedef void* lf_stream_t;
+
+typedef enum lf_status {
+  LF_OK = 0,
+  LF_ERR_ARG = -1,         /* invalid argument (shape, range, null pointer) */
+  LF_ERR_OOM = -2,         /* device allocation failed */
+  LF_ERR_CUDA = -3,        /* a CUDA runtime call or launch failed */
+  LF_ERR_DEVICE = -5,      /* lf_cache_check: the device error word was set */
+  LF_ERR_UNSUPPORTED = -7  /* valid but not built (head_dim, group size, smem) */
+} lf_status;
+
+typedef enum lf_dtype { LF_BF16 = 0, LF_F32 = 1 } lf_dtype;
+
+/* Bits of the device error word (lf_cache_check). */
+#define LF_DEVERR_NONFINITE 1 /* a softmax max/denominator was not finite */
+#define LF_DEVERR_STATE 2     /* no eviction candidate / count out of range */
+#define LF_DEVERR_TIMEOUT 4   /* a bounded on-chip wait expired; step skipped */
+
+typedef struct lf_config {
+  int dtype;              /* LF_BF16 or LF_F32: type of q, K, V, k_new, v_new, out */
+  int evict;              /* 1: LongFlow eviction; 0: full KV -- append until the
+                             capacity, then read only (no scores, no writes) */
+  const int32_t* budgets; /* host [batch] per-sequence budgets (each <= capacity and
+                             > window when evicting), or NULL: every budget = capacity */
+  int cluster;            /* CTAs that split one KV head's slots (1,2,4,8,16); 0 = auto */
+  int stages;             /* depth of the shared-memory staging ring (2..16); 0 = auto */
+} lf_config;
+
+/*
+ * Create a cache of `layers` independent layers for `batch` sequences with
+ * kv_heads KV heads of dimension head_dim, q_heads query heads (a multiple of
+ * kv_heads), `budget` slots per (layer, sequence, KV head) and a protected
+ * window of the `window` most recent positions (0 <= window < budget).
+ * Storage is bf16, eviction on.  Returns NULL on error (see lf_last_error).
+ * Supported: head_dim in {16, 32, 64, 128}; q_heads / kv_heads in {1, 2, 4, 8}.
+ */
+lf_cache* lf_cache_create(int layers, int batch, int kv_heads, int q_heads, int head_dim,
+                          int budget, int window);
+
+/* Same with explicit dtype / eviction mode / ragged budgets / launch shape.
+ * `capacity` is the slot count of every slab unit (the largest budget when
+ * evicting; the full-KV length when not).  cfg may be NULL (bf16, evict). */
+lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, int head_dim,
+                             int capacity, int window, const lf_config* cfg);
+
+/* Free the slab and the handle.  NULL is accepted (no-op).  Returns LF_OK. */
+int lf_cache_destroy(lf_cache* cache);
+
+/*
+ * Initial fill of one layer (guide, "Static Memory Pre-Allocation and
+ * In-Place Eviction", step 1): sequence b's first prompt_len[b] tokens take
+ * slots 0..prompt_len[b]-1 with positions 0..prompt_len[b]-1; ||v||_1 is
+ * computed in fp32 from the stored values; the occupied count and the next
+ * position become prompt_len[b].  Slots past the prompt are marked empty.
+ *   k, v        device, [batch][kv_heads][max_prompt][head_dim], cache dtype,
+ *               contiguous, 16-byte aligned, caller-owned
+ *   prompt_len  HOST [batch], 0 <= prompt_len[b] <= max_prompt and <= that
+ *               sequence's budget (capacity when eviction is off); longer
+ *               prompts are fed through lf_decode_step by the caller
+ * The host lengths are uploaded before the call returns.  Stream-ordered.
+ */
+int lf_prefill_fill(lf_cache* cache, int layer, const void* k, const void* v,
+                    const int32_t* prompt_len, int max_prompt, lf_stream_t stream);
+
+/*
+ * One fused decode step of one layer for every sequence (see the top of the
+ * file).  All buffers are caller-owned, contiguous device memory that must
+ * stay valid until the stream reaches the call:
+ *   q             [batch][q_heads][head_dim]   cache dtype
+ *   k_new, v_new  [batch][kv_heads][head_dim]  cache dtype (the token's stored values)
+ *   out           [batch][q_heads][head_dim]   cache dtype (fp32 accumulation, RNE rounding)
+ *   evicted_slot  [batch][kv_heads] int32: the slot overwritten, or -1 in the fill
+ *                 phase and in eviction-off mode
+ * Asynchronous; no host synchronisation; allocates nothing; capturable in a
+ * CUDA graph.  Returns LF_ERR_ARG / LF_ERR_CUDA on a bad call or launch.
+ */
+int lf_decode_step(lf_cache* cache, int layer, const void* q, const void* k_new,
+                   const void* v_new, void* out, int32_t* evicted_slot, lf_stream_t stream);
+
+/* Synchronise `stream`, read and clear the device error word.  *bits (may be
+ * NULL) receives the LF_DEVERR_* bits.  Returns LF_ERR_DEVICE if any was set. */
+int lf_cache_check(lf_cache* cache, lf_stream_t stream, int32_t* bits);
+
+/* Device pointers and shape of the slab, for inspection, snapshots and
+ * restores by the caller (stream-ordered with the caller's own copies).
+ * Element (layer l, sequence b, KV head g, slot s) of k/v starts at
+ * ((((l * batch + b) * kv_heads + g) * slot_stride + s) * head_dim); vnorm and
+ * pos use the same index without head_dim; count / next_pos are indexed
+ * [(l * batch + b) * kv_heads + g]; budget is [batch]. */
+typedef struct lf_layout {
+  int layers, batch, kv_heads, q_heads, head_dim;
+  int capacity;     /* usable slots per unit */
+  int slot_stride;  /* allocated slots per unit (capacity rounded up) */
+  int window, dtype, evict;
+  int cluster, stages; /* launch shape of lf_decode_step */
+  void* k;          /* cache dtype */
+  void* v;          /* cache dtype */
+  float* vnorm;     /* fp32 ||v||_1 of each slot, written at insert */
+  int32_t* pos;     /* token position of each slot, -1 when empty */
+  int32_t* count;   /* occupied slots */
+  int32_t* next_pos;/* position of the next token */
+  int32_t* budget;  /* per-sequence budget */
+  int32_t* err;     /* device error word */
+} lf_layout;
+
+int lf_cache_layout(const lf_cache* cache, lf_layout* out);
+
+/* Message of the last failed call on this thread ("" if none). */
+const char* lf_last_error(void);
+
+/* LF_ABI_VERSION of the loaded library. */
+int lf_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LONGFLOW_H_ */

@@ -1,0 +1,122 @@
+"""CUDA path vs the fp64 oracle, element by element on the same seeded inputs.
+
+Small cases run every unit through the oracle.  The large workloads run one or
+two layers at their full per-layer size (batch, heads, budget, window: the
+launch configuration the benchmark times) and replay a sample of units.
+"""
+import numpy as np
+import pytest
+import torch
+
+from gpu_harness import ParityRun
+from synth.workloads import WORKLOADS, InputStream
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(wl, steps, **kw):
+    run = ParityRun(wl, **kw)
+    try:
+        run.run(steps)
+        run.compare_state()
+        run.check_invariants()
+        run.stats.assert_ok()
+        return run.stats
+    finally:
+        run.close()
+
+
+@pytest.mark.parametrize("cluster", [0, 2, 4])
+def test_tiny_fp32_full_workload(cluster):
+    """The tiny fp32 workload end to end (8-token prompt, 64 steps: 24 fill, 40 evict)."""
+    st = _run(WORKLOADS["tiny-fp32"], 64, cluster=cluster)
+    assert st.evictions == 40
+
+
+def test_qwen3_06b_shape_two_layers():
+    wl = WORKLOADS["qwen3-0.6b"]
+    sample = [(li, b, g) for li in range(2) for b in (0, 3, 7) for g in (0, 5)]
+    st = _run(wl, 600, layers=(0, 13), sample=sample)
+    assert st.evictions > 0
+
+
+def test_r1_llama_shape_fill_phase():
+    """Prompt 512 of budget 3276: the first steps of the fill phase at full size."""
+    wl = WORKLOADS["r1-llama-8b"]
+    _run(wl, 40, layers=(5,), sample=[(0, 0, 0), (0, 31, 7), (0, 17, 3)])
+
+
+def test_r1_llama_shape_eviction_phase():
+    """Same launch shape with the prompt near the budget, so steps evict."""
+    wl = WORKLOADS["r1-llama-8b"].scaled(prefill=3240)
+    st = _run(wl, 160, layers=(2,), sample=[(0, 0, 0), (0, 13, 6), (0, 31, 7)])
+    assert st.evictions >= 3 * 120
+
+
+def test_qwen3_8b_steady_state():
+    wl = WORKLOADS["qwen3-8b-steady"]
+    st = _run(wl, 120, layers=(0,), sample=[(0, 0, 0), (0, 63, 7), (0, 40, 2)])
+    assert st.evictions == 3 * 120
+
+
+def test_full_kv_read_only():
+    """Eviction off at the full 16384-token capacity: every step attends over
+    all slots plus the new token and writes nothing."""
+    wl = WORKLOADS["qwen3-8b-steady"].scaled(prefill=16384, batch=16)
+    st = _run(wl, 12, layers=(0,), sample=[(0, 0, 0), (0, 15, 7)], evict=False, capacity=16384)
+    assert st.evictions == 0
+
+
+def test_ragged_serving_shape():
+    wl = WORKLOADS["ragged-serving"]
+    budgets = InputStream(wl, seed=0, device="cpu", layers=[0]).budgets  # same seeded draw
+    # one sampled sequence per budget value
+    picks = []
+    for B in sorted(set(budgets)):
+        b = budgets.index(B)
+        picks += [(0, b, 0), (0, b, 7)]
+    st = _run(wl, 300, layers=(0,), sample=picks)
+    assert st.unit_steps == 300 * len(picks)
+
+
+@pytest.mark.parametrize("case", [
+    # name, overrides, capacity, cluster
+    ("g1_d64_empty_start_ragged_tail", dict(q_heads=4, kv_heads=4, head_dim=64, budget=37,
+                                            window=3, prefill=0, batch=3), None, 4),
+    ("g8_d32_f32_single_candidate", dict(q_heads=8, kv_heads=1, head_dim=32, budget=100,
+                                         window=99, prefill=100, batch=2, dtype="f32"), None, 0),
+    ("g4_d128_sparse_cluster16", dict(q_heads=8, kv_heads=2, head_dim=128, budget=130,
+                                      window=5, prefill=120, batch=2), None, 16),
+    ("g2_d16_window0", dict(q_heads=4, kv_heads=2, head_dim=16, budget=64, window=0,
+                            prefill=64, batch=2), None, 2),
+    ("g4_d128_f32", dict(q_heads=8, kv_heads=2, head_dim=128, budget=200, window=8,
+                         prefill=150, batch=2, dtype="f32"), None, 0),
+], ids=lambda c: c[0])
+def test_edge_cases(case):
+    name, over, cap, cluster = case
+    wl = WORKLOADS["qwen3-0.6b"].scaled(layers=1, steps=80, v_lognormal_sigma=0.5, **over)
+    _run(wl, 80, cluster=cluster, capacity=cap)
+
+
+@pytest.mark.parametrize("cluster,stages", [(1, 4), (2, 2), (4, 8), (8, 3), (16, 16)])
+def test_launch_shapes_agree(cluster, stages):
+    """Every cluster size and ring depth gives the oracle's results."""
+    wl = WORKLOADS["r1-llama-8b"].scaled(batch=2, prefill=3200)
+    _run(wl, 100, cluster=cluster, stages=stages, sample=[(0, 0, 0), (0, 1, 5)])
+
+
+def test_nonfinite_query_sets_error_word():
+    from decode_kv_cache_gb300.longflow import LF_DEVERR_NONFINITE, LFCache
+    wl = WORKLOADS["tiny-fp32"]
+    c = LFCache(1, 1, 1, 2, 16, 32, 4, dtype="f32")
+    k = torch.randn(1, 1, 8, 16, device="cuda")
+    c.prefill(0, k, k.clone(), [8])
+    q = torch.randn(1, 2, 16, device="cuda")
+    kn = torch.randn(1, 1, 16, device="cuda")
+    c.decode_step(0, q, kn, kn.clone())
+    assert c.check() == 0
+    q[0, 1, 3] = float("nan")
+    c.decode_step(0, q, kn, kn.clone())
+    assert c.check() & LF_DEVERR_NONFINITE
+    assert c.check() == 0  # cleared by the read
+    c.close()
