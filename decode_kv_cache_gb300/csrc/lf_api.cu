@@ -1,6 +1,7 @@
 // C ABI of the LongFlow fused decode step: cache creation, prefill, decode,
 // error checks and the slab layout.  Declarations and semantics are in
 // include/longflow.h.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -12,7 +13,7 @@
 #include <new>
 #include <string>
 
-#include "lf_decode.cuh"
+#include "lf_decode_tc.cuh"
 #include "lf_kernels.h"
 #include "longflow.h"
 
@@ -31,6 +32,9 @@ struct lf_cache {
   int32_t* plen;  // [layers][batch] prompt lengths uploaded by lf_prefill_fill
   void* small;    // one allocation holding vnorm..plen
   lf::KernelEntry kern;
+  int threads;    // CTA size of the decode kernel
+  int grid_y;     // tensor-core path: resident clusters (persistent grid)
+  CUtensorMap tmaps[4];  // tensor-core path: K and V as 2-D [rows][head_dim], two box heights
 };
 
 namespace {
@@ -57,11 +61,11 @@ inline size_t round_up(size_t x, size_t m) { return (x + m - 1) / m * m; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Largest CTA count per cluster the launch can keep resident at least once.
-bool cluster_fits(const void* fn, int cluster, int kv_heads, int batch, int smem) {
+// How many clusters of this shape can be resident at once (0: none).
+int active_clusters(const void* fn, int cluster, int grid_y, int grid_z, int smem, int threads) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(cluster, kv_heads, batch);
-  cfg.blockDim = dim3(lf::kThreads, 1, 1);
+  cfg.gridDim = dim3(cluster, grid_y, grid_z);
+  cfg.blockDim = dim3(threads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -73,9 +77,41 @@ bool cluster_fits(const void* fn, int cluster, int kv_heads, int batch, int smem
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
     (void)cudaGetLastError();
-    return false;
+    return 0;
   }
-  return n > 0;
+  return n;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// K and V slabs as 2-D tensors [rows = every slot of every unit][head_dim]
+// (bf16), read in boxes of 64 columns x {64, 16} rows with the 128-byte
+// swizzle the tensor-core descriptors expect.
+int encode_tensor_maps(lf_cache* c, size_t n_rows) {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                   cudaEnableDefault, &q);
+  if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+    return fail(LF_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  if (n_rows >= (1ull << 31)) return fail(LF_ERR_UNSUPPORTED, "slab has too many rows for TMA");
+  EncodeTiledFn encode = reinterpret_cast<EncodeTiledFn>(fn);
+  const cuuint64_t dims[2] = {(cuuint64_t)c->head_dim, (cuuint64_t)n_rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)c->head_dim * 2};
+  const cuuint32_t estr[2] = {1, 1};
+  void* bases[4] = {c->K, c->K, c->V, c->V};
+  const cuuint32_t heights[4] = {64, 16, 64, 16};
+  for (int i = 0; i < 4; ++i) {
+    const cuuint32_t box[2] = {64, heights[i]};
+    CUresult r = encode(&c->tmaps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, bases[i], dims, strides,
+                        box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(LF_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  }
+  return LF_OK;
 }
 
 void destroy_memory(lf_cache* c) {
@@ -101,7 +137,7 @@ lf_cache* lf_cache_create(int layers, int batch, int kv_heads, int q_heads, int 
 lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, int head_dim,
                              int capacity, int window, const lf_config* cfg) {
   g_last_error.clear();
-  lf_config def = {LF_BF16, 1, nullptr, 0, 0};
+  lf_config def = {LF_BF16, 1, nullptr, 0, 0, LF_KERNEL_AUTO};
   const lf_config c = cfg ? *cfg : def;
   if (layers < 1 || batch < 1 || kv_heads < 1 || q_heads < 1 || capacity < 1 || window < 0) {
     fail(LF_ERR_ARG, "layers, batch, heads and capacity must be >= 1 and window >= 0");
@@ -132,10 +168,23 @@ lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, i
     fail(LF_ERR_ARG, "stages must be 0 (auto) or in [2, %d]", lf::kMaxStages);
     return nullptr;
   }
+  if (c.kernel < LF_KERNEL_AUTO || c.kernel > LF_KERNEL_TENSOR_CORE) {
+    fail(LF_ERR_ARG, "kernel must be LF_KERNEL_AUTO, LF_KERNEL_SIMT or LF_KERNEL_TENSOR_CORE");
+    return nullptr;
+  }
   const int group = q_heads / kv_heads;
   lf::KernelEntry kern;
-  const bool found = (c.dtype == LF_BF16) ? lf::find_kernels_bf16(head_dim, group, &kern)
-                                          : lf::find_kernels_f32(head_dim, group, &kern);
+  bool found = false;
+  if (c.dtype == LF_BF16 && c.kernel != LF_KERNEL_SIMT)
+    found = lf::find_kernels_tc(head_dim, group, &kern);
+  if (!found && c.kernel == LF_KERNEL_TENSOR_CORE) {
+    fail(LF_ERR_UNSUPPORTED, "the tensor-core kernel needs bf16 storage, head_dim 128 and group "
+         "size 1/2/4/8");
+    return nullptr;
+  }
+  if (!found)
+    found = (c.dtype == LF_BF16) ? lf::find_kernels_bf16(head_dim, group, &kern)
+                                 : lf::find_kernels_f32(head_dim, group, &kern);
   if (!found) {
     fail(LF_ERR_UNSUPPORTED, "no kernel for head_dim %d and group size %d (built: head_dim "
          "16/32/64/128, group 1/2/4/8)", head_dim, group);
@@ -167,8 +216,10 @@ lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, i
     cuda_fail(e, "cudaGetDevice");
     return nullptr;
   }
-  int num_sms = 0, max_optin = 0;
-  if ((e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, device)) != cudaSuccess ||
+  int num_sms = 0, max_optin = 0, max_sm_smem = 0;
+  if ((e = cudaDeviceGetAttribute(&max_sm_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor,
+                                  device)) != cudaSuccess ||
+      (e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, device)) != cudaSuccess ||
       (e = cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device)) !=
           cudaSuccess) {
     cuda_fail(e, "cudaDeviceGetAttribute");
@@ -182,23 +233,41 @@ lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, i
     return nullptr;
   }
 
-  // Launch shape: a cluster of C CTAs splits each unit's slots.  Prefer the
-  // smallest C that gives at least 8 CTAs per SM over the grid, with at least
-  // 128 slots per CTA; the caller may force C and the ring depth.
+  // Launch shape.  CUDA-core kernel: one cluster of C CTAs per unit; prefer
+  // the smallest C giving at least 8 CTAs per SM with >= 128 slots per CTA.
+  // Tensor-core kernel: persistent, one CTA per SM; prefer the smallest C
+  // whose per-CTA chunk fits next to a ring of `stages` 32 KB tiles.  The
+  // caller may force C and the ring depth.
+  const bool tc = (kern.kind == lf::kTensorCore);
+  const int threads = tc ? lf::kTcThreads : lf::kThreads;
   const int units = batch * kv_heads;
-  const int stages = c.stages ? c.stages : 4;
+  const int stages = c.stages ? c.stages : (tc ? 3 : 4);
   int cluster = c.cluster;
   if (cluster == 0) {
     cluster = 1;
-    while (cluster < lf::kMaxCluster && (long long)units * cluster < 8LL * num_sms &&
-           (capacity + 2 * cluster - 1) / (2 * cluster) >= 128)
-      cluster *= 2;
+    if (!tc)
+      while (cluster < lf::kMaxCluster && (long long)units * cluster < 8LL * num_sms &&
+             (capacity + 2 * cluster - 1) / (2 * cluster) >= 128)
+        cluster *= 2;
   }
-  int chunk = 0, smem = 0;
+  int chunk = 0, smem = 0, grid_y = 0;
   for (;;) {
     chunk = (int)round_up((size_t)((capacity + cluster - 1) / cluster), 4);
-    smem = kern.smem_bytes(stages, chunk);
-    if (smem <= max_optin && cluster_fits(kern.decode, cluster, kv_heads, batch, smem)) break;
+    smem = kern.smem_bytes(stages, chunk, cluster);
+    // The tensor-core kernel takes all of an SM's tensor memory: ask for more
+    // than half of its shared memory so that never two CTAs share an SM.
+    if (tc) smem = std::max(smem, max_sm_smem / 2 + 1024);
+    int fits = 0;
+    if (smem <= max_optin) {
+      if (tc) {
+        fits = active_clusters(kern.decode, cluster, 1, 1, smem, threads);
+        grid_y = std::min(fits, units);
+        if (fits > 0 && (units + grid_y - 1) / grid_y > lf::kTcMaxItems) fits = 0;
+      } else {
+        fits = active_clusters(kern.decode, cluster, kv_heads, batch, smem, threads);
+      }
+    }
+    if (fits > 0) break;
     if (c.cluster != 0 || cluster >= lf::kMaxCluster) {
       fail(LF_ERR_UNSUPPORTED, "launch does not fit: cluster %d, %d stages, %d slots per CTA need "
            "%d bytes of shared memory (max %d)", cluster, stages, chunk, smem, max_optin);
@@ -229,6 +298,8 @@ lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, i
   cache->device = device;
   cache->elem_bytes = (size_t)kern.elem_bytes;
   cache->kern = kern;
+  cache->threads = threads;
+  cache->grid_y = grid_y;
 
   const size_t n_units = (size_t)layers * batch * kv_heads;
   const size_t n_slots = n_units * cache->slot_stride;
@@ -284,6 +355,14 @@ lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, i
     return nullptr;
   }
   delete[] hb;
+  if (tc) {
+    const int code = encode_tensor_maps(cache, n_slots);
+    if (code != LF_OK) {
+      destroy_memory(cache);
+      delete cache;
+      return nullptr;
+    }
+  }
   return cache;
 }
 
@@ -382,6 +461,7 @@ int lf_decode_step(lf_cache* cache, int layer, const void* q, const void* k_new,
   a.next_pos = cache->next_pos + layer * layer_units;
   a.budget = cache->budget;
   a.err = cache->err;
+  a.batch = cache->batch;
   a.kv_heads = cache->kv_heads;
   a.q_heads = cache->q_heads;
   a.slot_stride = cache->slot_stride;
@@ -393,8 +473,10 @@ int lf_decode_step(lf_cache* cache, int layer, const void* q, const void* k_new,
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)cache->head_dim));
 
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(cache->cluster, cache->kv_heads, cache->batch);
-  cfg.blockDim = dim3(lf::kThreads, 1, 1);
+  cfg.gridDim = (cache->kern.kind == lf::kTensorCore)
+                    ? dim3(cache->cluster, cache->grid_y, 1)
+                    : dim3(cache->cluster, cache->kv_heads, cache->batch);
+  cfg.blockDim = dim3(cache->threads, 1, 1);
   cfg.dynamicSmemBytes = cache->smem;
   cfg.stream = static_cast<cudaStream_t>(stream);
   cudaLaunchAttribute attr[1];
@@ -404,8 +486,21 @@ int lf_decode_step(lf_cache* cache, int layer, const void* q, const void* k_new,
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  void* args[] = {&a};
-  cudaError_t e = cudaLaunchKernelExC(&cfg, cache->kern.decode, args);
+  cudaError_t e;
+  if (cache->kern.kind == lf::kTensorCore) {
+    lf::TcArgs ta;
+    ta.k64 = cache->tmaps[0];
+    ta.k16 = cache->tmaps[1];
+    ta.v64 = cache->tmaps[2];
+    ta.v16 = cache->tmaps[3];
+    ta.a = a;
+    ta.row_base = (int)(layer * layer_slots);
+    void* args[] = {&ta};
+    e = cudaLaunchKernelExC(&cfg, cache->kern.decode, args);
+  } else {
+    void* args[] = {&a};
+    e = cudaLaunchKernelExC(&cfg, cache->kern.decode, args);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return LF_OK;
 }
@@ -443,6 +538,7 @@ int lf_cache_layout(const lf_cache* cache, lf_layout* out) {
   out->evict = cache->evict;
   out->cluster = cache->cluster;
   out->stages = cache->stages;
+  out->kernel = cache->kern.kind == lf::kTensorCore ? LF_KERNEL_TENSOR_CORE : LF_KERNEL_SIMT;
   out->k = cache->K;
   out->v = cache->V;
   out->vnorm = cache->vnorm;

@@ -54,7 +54,7 @@ struct DecodeArgs {
   int32_t* next_pos;
   const int32_t* budget;  // [batch]
   int32_t* err;
-  int kv_heads, q_heads, slot_stride, capacity, window, chunk, stages, evict;
+  int batch, kv_heads, q_heads, slot_stride, capacity, window, chunk, stages, evict;
   float scale_log2;    // log2(e) / sqrt(D)
 };
 
@@ -92,8 +92,183 @@ struct DecodePlan {
   }
 };
 
+// Shared-memory pieces the cluster combine reads and writes.
+struct CombineSmem {
+  float* m_loc;   // [kMaxGroup] this CTA's max logit per head (log2 domain)
+  float* l_loc;   // [kMaxGroup] sum of 2^(s - m_loc) over this CTA's slots
+  float* s_new;   // [kMaxGroup] the new token's logit per head
+  float* cmul;    // [kMaxGroup] 2^(m_loc - M) / L per head
+  float* m_glb;   // [kMaxGroup] M: max over the cluster and the new token
+  float* l_glb;   // [kMaxGroup] L: softmax denominator over the unit
+  float* best_s;  // [kMaxCluster] per-rank lowest score (leader's copy is filled)
+  int* best_i;    // [kMaxCluster] per-rank victim slot
+  int* fail_in;   // [kMaxCluster] per-rank abort flags
+  float* red;     // [kWarps * kMaxGroup] reduction scratch
+  int* red_i;     // [kWarps * kMaxGroup]
+  int* decision;  // [2] slot written, victim
+  float* o_part;  // [G][D] this CTA's unnormalised output, relative to m_loc
+  const float* p; // [rows][G] 2^(s - m_loc) of this CTA's slots
+  const float* w; // [rows] ||v||_1 of candidates, -1 for protected slots
+};
+
+// Cluster-wide combine of one unit: merge (m, l) and the partial outputs over
+// DSMEM, add the new token as one more key, write out, score every candidate
+// exactly, and let the leader CTA overwrite the lowest-scored slot.  Called by
+// all NT threads of every CTA of the cluster.
+template <typename T, int D, int G, int NT>
+__device__ __forceinline__ void combine_and_evict(
+    const DecodeArgs& a, cg::cluster_group& cluster, const CombineSmem& sm, int C, int rank, int b,
+    int g, int unit, size_t ubase, int n, int p, int bud, bool state_ok, bool evicting, int s0,
+    int rows, bool aborted, const T* qg, const T* kn, const T* vn) {
+  constexpr int NW = NT / 32;
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  // The new token's logits, computed redundantly by every CTA of the cluster.
+  for (int h = warp; h < G; h += NW) {
+    float s = 0.f;
+    for (int e = lane; e < D; e += 32) s = fmaf(to_f32(qg[(size_t)h * D + e]), to_f32(kn[e]), s);
+    s = warp_sum(s);
+    if (lane == 0) sm.s_new[h] = s * a.scale_log2;
+  }
+  // #1: every CTA has started (DSMEM may be touched from here on) and its
+  // m_loc, l_loc and o_part are visible to the cluster.
+  cluster.sync();
+  if (tid == 0 && aborted) *cluster.map_shared_rank(&sm.fail_in[rank], 0) = 1;
+
+  if (tid < G) {
+    const int h = tid;
+    float M = sm.s_new[h];
+    for (int r = 0; r < C; ++r) M = fmaxf(M, *cluster.map_shared_rank(&sm.m_loc[h], r));
+    float L = exp2f(sm.s_new[h] - M);
+    for (int r = 0; r < C; ++r) {
+      const float mr = *cluster.map_shared_rank(&sm.m_loc[h], r);
+      if (mr != -INFINITY) L += *cluster.map_shared_rank(&sm.l_loc[h], r) * exp2f(mr - M);
+    }
+    sm.m_glb[h] = M;
+    sm.l_glb[h] = L;
+    sm.cmul[h] = (sm.m_loc[h] != -INFINITY) ? exp2f(sm.m_loc[h] - M) / L : 0.f;
+    if (!(isfinite(M) && isfinite(L) && L > 0.f)) atomicOr(a.err, LF_DEVERR_NONFINITE);
+  }
+  __syncthreads();
+
+  // Output: the cluster's threads share the G x D elements.
+  {
+    T* og = reinterpret_cast<T*>(a.out) + ((size_t)b * a.q_heads + (size_t)g * G) * D;
+    for (int idx = rank * NT + tid; idx < G * D; idx += C * NT) {
+      const int h = idx / D;
+      const int e = idx - h * D;
+      float acc = exp2f(sm.s_new[h] - sm.m_glb[h]) * to_f32(vn[e]);
+      for (int r = 0; r < C; ++r) {
+        const float mr = *cluster.map_shared_rank(&sm.m_loc[h], r);
+        if (mr != -INFINITY)
+          acc += *cluster.map_shared_rank(&sm.o_part[idx], r) * exp2f(mr - sm.m_glb[h]);
+      }
+      from_f32(acc / sm.l_glb[h], &og[(size_t)h * D + e]);
+    }
+  }
+
+  // Exact LongFlow scores of this CTA's candidates and their (score, slot) minimum.
+  float bs = INFINITY;
+  int bi = INT_MAX;
+  if (evicting && !aborted) {
+    float cm[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) cm[h] = sm.cmul[h];
+    for (int i = tid; i < rows; i += NT) {
+      const float w = sm.w[i];
+      if (w >= 0.f) {
+        float acc = 0.f;
+#pragma unroll
+        for (int h = 0; h < G; ++h) acc = fmaf(sm.p[(size_t)i * G + h], cm[h], acc);
+        const float sc = w * acc;
+        if (better(sc, s0 + i, bs, bi)) {
+          bs = sc;
+          bi = s0 + i;
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float os = __shfl_xor_sync(0xffffffffu, bs, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    if (better(os, oi, bs, bi)) {
+      bs = os;
+      bi = oi;
+    }
+  }
+  if (lane == 0) {
+    sm.red[warp] = bs;
+    sm.red_i[warp] = bi;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    for (int w = 1; w < NW; ++w)
+      if (better(sm.red[w], sm.red_i[w], bs, bi)) {
+        bs = sm.red[w];
+        bi = sm.red_i[w];
+      }
+    *cluster.map_shared_rank(&sm.best_s[rank], 0) = bs;
+    *cluster.map_shared_rank(&sm.best_i[rank], 0) = bi;
+  }
+  cluster.sync();  // #2: all slot reads of the step are done; minima are at the leader
+  if (rank != 0) return;
+
+  if (tid == 0) {
+    bool any_fail = false;
+    for (int r = 0; r < C; ++r) any_fail = any_fail || sm.fail_in[r] != 0;
+    int victim = -1;
+    if (evicting) {
+      float fs = INFINITY;
+      int fi = INT_MAX;
+      for (int r = 0; r < C; ++r)
+        if (better(sm.best_s[r], sm.best_i[r], fs, fi)) {
+          fs = sm.best_s[r];
+          fi = sm.best_i[r];
+        }
+      if (fi != INT_MAX) victim = fi;
+      else if (!any_fail) atomicOr(a.err, LF_DEVERR_STATE);  // no candidate
+    }
+    const int limit = a.evict ? bud : a.capacity;
+    int slot = evicting ? victim : (n < limit ? n : -1);
+    if (!state_ok) atomicOr(a.err, LF_DEVERR_STATE);
+    if (any_fail || !state_ok) {
+      slot = -1;
+      victim = -1;
+    }
+    sm.decision[0] = slot;
+    sm.decision[1] = victim;
+    a.evicted[unit] = victim;
+    if (state_ok && !any_fail) {
+      if (!evicting && slot >= 0) a.count[unit] = n + 1;
+      a.next_pos[unit] = p + 1;
+    }
+  }
+  __syncthreads();
+  const int slot = sm.decision[0];
+  if (slot >= 0) {
+    // In-place overwrite of one slot: K, V, ||v||_1 (fp32, from the stored value), position.
+    T* Kd = reinterpret_cast<T*>(a.K) + (ubase + slot) * D;
+    T* Vd = reinterpret_cast<T*>(a.V) + (ubase + slot) * D;
+    for (int e = tid; e < D; e += NT) {
+      Kd[e] = kn[e];
+      Vd[e] = vn[e];
+    }
+    if (warp == 0) {
+      float s = 0.f;
+      for (int e = lane; e < D; e += 32) s += fabsf(to_f32(vn[e]));
+      s = warp_sum(s);
+      if (lane == 0) {
+        a.vnorm[ubase + slot] = s;
+        a.pos[ubase + slot] = p;
+      }
+    }
+  }
+}
+
 template <typename T, int D, int G>
-__global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) decode_step_simt_kernel(const DecodeArgs a) {
   using P = DecodePlan<T, D, G>;
   constexpr int V = ElemTraits<T>::kPer16B;  // elements per 16-byte chunk
   constexpr int NC = D / V;                  // chunks per row
@@ -353,143 +528,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
     for (int grp = 0; grp < P::kPvGroups; ++grp) s += pvbuf[(size_t)grp * G * D + idx];
     o_part[idx] = s;
   }
-  // The new token's logits, computed redundantly by every CTA of the cluster.
-  if (warp < G) {
-    float s = 0.f;
-    for (int e = lane; e < D; e += 32) s = fmaf(to_f32(qg[(size_t)warp * D + e]), to_f32(kn[e]), s);
-    s = warp_sum(s);
-    if (lane == 0) s_new[warp] = s * a.scale_log2;
-  }
-  // #1: every CTA has started (DSMEM may be touched from here on) and its
-  // m_loc, l_loc and o_part are visible to the cluster.
-  cluster.sync();
-  if (tid == 0 && aborted) *cluster.map_shared_rank(&fail_in[rank], 0) = 1;
-
-  if (tid < G) {
-    const int h = tid;
-    float M = s_new[h];
-    for (int r = 0; r < C; ++r) M = fmaxf(M, *cluster.map_shared_rank(&m_loc[h], r));
-    float L = exp2f(s_new[h] - M);
-    for (int r = 0; r < C; ++r) {
-      const float mr = *cluster.map_shared_rank(&m_loc[h], r);
-      if (mr != -INFINITY) L += *cluster.map_shared_rank(&l_loc[h], r) * exp2f(mr - M);
-    }
-    m_glb[h] = M;
-    l_glb[h] = L;
-    cmul[h] = (m_loc[h] != -INFINITY) ? exp2f(m_loc[h] - M) / L : 0.f;
-    if (!(isfinite(M) && isfinite(L) && L > 0.f)) atomicOr(a.err, LF_DEVERR_NONFINITE);
-  }
-  __syncthreads();
-
-  // Output: the cluster's threads share the G x D elements.
-  {
-    T* og = reinterpret_cast<T*>(a.out) + ((size_t)b * a.q_heads + (size_t)g * G) * D;
-    for (int idx = rank * kThreads + tid; idx < G * D; idx += C * kThreads) {
-      const int h = idx / D;
-      const int e = idx - h * D;
-      float acc = exp2f(s_new[h] - m_glb[h]) * to_f32(vn[e]);
-      for (int r = 0; r < C; ++r) {
-        const float mr = *cluster.map_shared_rank(&m_loc[h], r);
-        if (mr != -INFINITY) acc += *cluster.map_shared_rank(&o_part[idx], r) * exp2f(mr - m_glb[h]);
-      }
-      from_f32(acc / l_glb[h], &og[(size_t)h * D + e]);
-    }
-  }
-
-  // Exact LongFlow scores of this CTA's candidates and their (score, slot) minimum.
-  float bs = INFINITY;
-  int bi = INT_MAX;
-  if (evicting && !aborted) {
-    for (int i = tid; i < rows; i += kThreads) {
-      const float w = wv[i];
-      if (w >= 0.f) {
-        float acc = 0.f;
-#pragma unroll
-        for (int h = 0; h < G; ++h) acc = fmaf(lg[(size_t)i * G + h], cmul[h], acc);
-        const float sc = w * acc;
-        if (better(sc, s0 + i, bs, bi)) {
-          bs = sc;
-          bi = s0 + i;
-        }
-      }
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float os = __shfl_xor_sync(0xffffffffu, bs, o);
-    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-    if (better(os, oi, bs, bi)) {
-      bs = os;
-      bi = oi;
-    }
-  }
-  if (lane == 0) {
-    red[warp] = bs;
-    red_i[warp] = bi;
-  }
-  __syncthreads();
-  if (tid == 0) {
-    for (int w = 1; w < kWarps; ++w)
-      if (better(red[w], red_i[w], bs, bi)) {
-        bs = red[w];
-        bi = red_i[w];
-      }
-    *cluster.map_shared_rank(&best_s[rank], 0) = bs;
-    *cluster.map_shared_rank(&best_i[rank], 0) = bi;
-  }
-  cluster.sync();  // #2: all slot reads of the step are done; minima are at the leader
-  if (rank != 0) return;
-
-  if (tid == 0) {
-    bool any_fail = false;
-    for (int r = 0; r < C; ++r) any_fail = any_fail || fail_in[r] != 0;
-    int victim = -1;
-    if (evicting) {
-      float fs = INFINITY;
-      int fi = INT_MAX;
-      for (int r = 0; r < C; ++r)
-        if (better(best_s[r], best_i[r], fs, fi)) {
-          fs = best_s[r];
-          fi = best_i[r];
-        }
-      if (fi != INT_MAX) victim = fi;
-      else if (!any_fail) atomicOr(a.err, LF_DEVERR_STATE);  // no candidate
-    }
-    const int limit = a.evict ? bud : a.capacity;
-    int slot = evicting ? victim : (n < limit ? n : -1);
-    if (!state_ok) atomicOr(a.err, LF_DEVERR_STATE);
-    if (any_fail || !state_ok) {
-      slot = -1;
-      victim = -1;
-    }
-    decision[0] = slot;
-    decision[1] = victim;
-    a.evicted[unit] = victim;
-    if (state_ok && !any_fail) {
-      if (!evicting && slot >= 0) a.count[unit] = n + 1;
-      a.next_pos[unit] = p + 1;
-    }
-  }
-  __syncthreads();
-  const int slot = decision[0];
-  if (slot >= 0) {
-    // In-place overwrite of one slot: K, V, ||v||_1 (fp32, from the stored value), position.
-    T* Kd = reinterpret_cast<T*>(a.K) + (ubase + slot) * D;
-    T* Vd = reinterpret_cast<T*>(a.V) + (ubase + slot) * D;
-    for (int e = tid; e < D; e += kThreads) {
-      Kd[e] = kn[e];
-      Vd[e] = vn[e];
-    }
-    if (warp == 0) {
-      float s = 0.f;
-      for (int e = lane; e < D; e += 32) s += fabsf(to_f32(vn[e]));
-      s = warp_sum(s);
-      if (lane == 0) {
-        a.vnorm[ubase + slot] = s;
-        a.pos[ubase + slot] = p;
-      }
-    }
-  }
+  CombineSmem cs{m_loc, l_loc, s_new, cmul, m_glb, l_glb, best_s, best_i, fail_in, red, red_i,
+                 decision, o_part, lg, wv};
+  combine_and_evict<T, D, G, kThreads>(a, cluster, cs, C, rank, b, g, unit, ubase, n, p, bud,
+                                       state_ok, evicting, s0, rows, aborted, qg, kn, vn);
 }
 
 // ---- prefill ----------------------------------------------------------------

@@ -1,0 +1,833 @@
+// The LongFlow fused decode step on the 5th-generation tensor cores (tcgen05):
+// a persistent, warp-specialised kernel for bf16 storage, head_dim 128 and
+// group size G <= 8.
+//
+// Work decomposition.  A thread-block cluster of C CTAs walks a list of
+// (sequence, KV head) units: cluster j takes units j, j + NC, j + 2 NC, ...
+// (NC clusters are resident, one CTA per SM).  CTA `rank` owns the slots
+// [rank*chunk, (rank+1)*chunk) of every unit it visits.
+//
+// Per unit, both contractions run as tcgen05.mma with fp32 accumulators in
+// tensor memory:
+//   phase A  S^T[slot][h] = K[slot][:] . q_h     M = 128 slots, N = 16 (G heads,
+//            A = K tile (K-major), B = q         zero-padded), K = d: 8 MMAs / tile
+//   phase B  O^T[e][c]   = sum_slot V[slot][e] P^T[c][slot]
+//            A = V tile (MN-major), B = P^T      M = 128 = d, N = 16, K = 128 slots
+//            rows c < G hold bf16(p_h), rows G+h hold bf16(p_h - bf16(p_h)), so
+//            O = O_hi + O_lo carries p to ~16 significant bits.
+// The softmax runs in two passes over the CTA's slots: all logits first (kept
+// in shared memory, needed again for the exact score), then p = 2^(s - m)
+// with the CTA's exact max m, so nothing is rescaled.
+//
+// Warp roles (256 threads):
+//   warp 4  producer: a ring of 2-D tensor-TMA copies (K then V tiles of
+//           128 slots x 256 bytes, 128-byte swizzle) that runs ahead across
+//           units, waiting only for stages the tensor cores have read;
+//   warp 5  MMA: writes the q operand and issues every tcgen05.mma;
+//   warps 0-3  epilogue (thread i <-> TMEM lane i): logits, softmax
+//           statistics, P^T and the output accumulator of one unit, then a
+//           hand-off of double-buffered state to
+//   warps 6-7  tail: the exchange, exact scores, and the leader's output and
+//           eviction of that unit, while warps 0-3 go on with the next unit.
+// Exchange (no cluster barrier inside the loop, so no other warp stops for
+// it): every CTA sends its (m_h, l_h) to all CTAs of the
+// cluster with st.async into an mbarrier-counted slot; each CTA then knows
+// the unit's max M_h and denominator L_h, scores its own candidates exactly,
+//   score_i = ||v_i||_1 * sum_h p_{h,i} 2^(m_h - M_h) / L_h,
+// and sends its partial output and its lowest (score, slot) to the unit's
+// leader CTA (rank = item mod C), which adds the new token as one more key,
+// writes the output, and overwrites the victim slot in place.
+// Every wait is bounded; on expiry the step is skipped and LF_DEVERR_TIMEOUT
+// is raised.
+#pragma once
+
+#include <cuda.h>
+
+#include "lf_decode.cuh"
+
+namespace lf {
+
+constexpr int kTcCompute = 128;   // epilogue threads: warps 0-3, TMEM lanes 0..127
+constexpr int kTcProducerWarp = 4;
+constexpr int kTcMmaWarp = 5;
+constexpr int kTcTailWarp0 = 6;   // tail warps 6 and 7
+constexpr int kTcTail = 64;
+constexpr int kTcThreads = 256;
+constexpr int kTcTile = 128;      // slots per tile (the MMA M of phase A)
+constexpr int kTcSBufs = 16;      // logit accumulators in flight between MMA and epilogue
+constexpr int kTcLookahead = 2;   // K tiles of the next unit issued before V of this one
+constexpr int kTcPBufs = 4;       // P^T tiles in flight between the compute warps and MMA
+// kTcSBufs x 16 columns of S + 16 columns of O, rounded to a power of two.  All
+// 512 columns of the SM: the host sizes shared memory so that exactly one CTA
+// is resident per SM, so the allocation never waits.
+constexpr int kTcTmemCols = 512;
+constexpr int kTcMaxItems = 512;  // units one cluster may visit in one launch
+
+struct TcArgs {
+  CUtensorMap k64, k16, v64, v16;  // 2-D views [rows][128] of K and V, boxes {64,64} / {64,16}
+  DecodeArgs a;
+  int row_base;                    // tensor row of this layer's first slot
+};
+
+template <int G>
+struct TcPlan {
+  static constexpr int D = 128;
+  static constexpr int kBlock = kTcTile * 128;  // [128 rows][64 bf16], swizzled: 16 KB
+  static constexpr int kStage = 2 * kBlock;     // one K or V tile: 32 KB
+  static constexpr int kQBytes = 2 * 16 * 128;  // q^T operand [16][128], 2 blocks
+  static constexpr int kPTile = 2 * 16 * 128;   // P^T operand of one tile [16][128 slots]
+  static constexpr int kFinBytes = G * D * 4 + 16;  // one CTA's partial output + (score, slot)
+  // header: barriers, statistics, reductions, exchange slots, unit metadata
+  static constexpr int kOffBars = 0;     // 112 mbarriers
+  static constexpr int kOffStats = 896;  // m_loc[2], l_loc[2], s_new[2], cmul, m_glb, l_glb
+  static constexpr int kOffRed = kOffStats + 9 * kMaxGroup * 4;
+  static constexpr int kOffMisc = kOffRed + 4 * kMaxGroup * 4 + 16;
+  static constexpr int kOffStatIn = 2048;                    // [2][kMaxCluster][2G] floats
+  static constexpr int kOffItems = kOffStatIn + 2 * kMaxCluster * 2 * kMaxGroup * 4;
+  static constexpr int kOffOpart = kOffItems + kTcMaxItems * 8;  // [2][G][D]
+  static_assert(kOffMisc + 64 <= kOffStatIn, "header overflow");
+  static_assert(16 + 16 + 2 * kTcSBufs + 2 * kTcPBufs + 14 <= kOffStats / 8, "too many barriers");
+  static constexpr int kOffQ = (kOffOpart + 2 * G * D * 4 + 1023) / 1024 * 1024;  // [2] buffers
+  static constexpr int kOffRing = kOffQ + 2 * kQBytes;
+
+  __host__ __device__ static constexpr int off_p(int stages) { return kOffRing + stages * kStage; }
+  __host__ __device__ static constexpr int off_fin(int stages) {
+    return off_p(stages) + kTcPBufs * kPTile;
+  }
+  __host__ __device__ static constexpr int off_lg(int stages, int cluster) {
+    return off_fin(stages) + cluster * kFinBytes;
+  }
+  __host__ __device__ static constexpr int vn_bytes(int chunk) { return (chunk + 3) / 4 * 16; }
+  __host__ __device__ static constexpr int off_vn(int stages, int chunk, int cluster) {
+    return (off_lg(stages, cluster) + 2 * chunk * G * 4 + 15) / 16 * 16;  // lg[2]
+  }
+  // vn[2], pos[2] (raw, from the slab) then w[2] (candidate weights), each vn_bytes(chunk)
+  __host__ __device__ static constexpr int smem_bytes(int stages, int chunk, int cluster) {
+    return off_vn(stages, chunk, cluster) + 6 * vn_bytes(chunk) + 1024;  // + alignment slack
+  }
+};
+
+template <int G>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    decode_step_tc_kernel(const __grid_constant__ TcArgs ta) {
+  constexpr int D = 128;
+  using P = TcPlan<G>;
+  using T = __nv_bfloat16;
+  static_assert(2 * G <= 16, "group too large for N = 16");
+  static_assert(D == kTcCompute, "one compute thread per output element / TMEM lane");
+  const DecodeArgs& a = ta.a;
+
+  cg::cluster_group cluster = cg::this_cluster();
+  const int C = (int)cluster.num_blocks();
+  const int rank = (int)cluster.block_rank();
+  const int NC = (int)gridDim.y;
+  const int j = (int)blockIdx.y;
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const int S = a.stages;
+  const int chunk = a.chunk;
+  const int units = a.batch * a.kv_heads;
+  const int nitems = (j < units) ? (units - j + NC - 1) / NC : 0;
+  const int s0 = rank * chunk;
+
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // The 128-byte swizzle phase of TMA writes and MMA reads follows address
+  // bits 7-9: start the carve-up on a 1024-byte boundary (1 KB is reserved).
+  unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P::kOffBars);
+  uint64_t* full = bars;                   // [16] stage landed
+  uint64_t* empty = bars + 16;             // [16] stage read by the tensor cores
+  uint64_t* sfull = bars + 32;             // [kTcSBufs] logits ready in TMEM
+  uint64_t* sfree = sfull + kTcSBufs;      // [kTcSBufs] logits read by the compute warps
+  uint64_t* pready = sfree + kTcSBufs;     // [kTcPBufs] P^T tile written
+  uint64_t* pfree = pready + kTcPBufs;     // [kTcPBufs] P^T tile read by the tensor cores
+  uint64_t* ofull = pfree + kTcPBufs;      // output accumulator complete
+  uint64_t* aux = ofull + 1;               // [2] ||v||_1 and positions landed
+  uint64_t* auxfree = aux + 2;             // [2] ... read by the epilogue warps
+  uint64_t* statb = auxfree + 2;           // [2] all CTAs' (m, l) arrived
+  uint64_t* finb = statb + 2;              // all CTAs' partial outputs arrived (leader)
+  uint64_t* qfree = finb + 1;              // [2] q operand buffer read by the tensor cores
+  uint64_t* handoff = qfree + 2;           // [2] epilogue -> tail: a unit's state is ready
+  uint64_t* taildone = handoff + 2;        // [2] tail -> epilogue: that state is consumed
+  uint64_t* drain = taildone + 2;          // every MMA complete
+  float* m_loc = reinterpret_cast<float*>(smem + P::kOffStats);  // [2][kMaxGroup]
+  float* l_loc = m_loc + 2 * kMaxGroup;                          // [2][kMaxGroup]
+  float* s_new = l_loc + 2 * kMaxGroup;                          // [2][kMaxGroup]
+  float* cmul = s_new + 2 * kMaxGroup;
+  float* m_glb = cmul + kMaxGroup;
+  float* l_glb = m_glb + kMaxGroup;
+  float* red = reinterpret_cast<float*>(smem + P::kOffRed);  // epilogue: [4][kMaxGroup]
+  float* red_t = red + 4 * kMaxGroup;                        // tail: [2] scores
+  int* red_ti = reinterpret_cast<int*>(red_t + 2);           // tail: [2] slots
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + P::kOffMisc);
+  int* decision = reinterpret_cast<int*>(smem + P::kOffMisc + 8);
+  volatile int* fail_any = reinterpret_cast<volatile int*>(smem + P::kOffMisc + 16);
+  volatile int* uflag = reinterpret_cast<volatile int*>(smem + P::kOffMisc + 24);  // [2]
+  float* stat_in = reinterpret_cast<float*>(smem + P::kOffStatIn);  // [2][C][2G]
+  int* items = reinterpret_cast<int*>(smem + P::kOffItems);         // [nitems][2] (n, p)
+  float* opbase = reinterpret_cast<float*>(smem + P::kOffOpart);     // [2][G][D]
+  unsigned char* qbuf = smem + P::kOffQ;
+  unsigned char* ring = smem + P::kOffRing;
+  unsigned char* ptile = smem + P::off_p(S);      // [kTcPBufs] P^T tiles
+  unsigned char* fin_in = smem + P::off_fin(S);   // [C][kFinBytes]
+  float* lgbase = reinterpret_cast<float*>(smem + P::off_lg(S, C));  // [2][chunk][G]
+  unsigned char* vnbase = smem + P::off_vn(S, chunk, C);
+
+  // ---- set-up ---------------------------------------------------------------
+  // Occupancy and position of every unit this cluster visits, read once: the
+  // leaders update them during the launch, every role must see the old values.
+  for (int k = tid; k < nitems; k += kTcThreads) {
+    const int u = j + k * NC;
+    items[2 * k] = a.count[u];
+    items[2 * k + 1] = a.next_pos[u];
+  }
+  if (tid == kTcProducerWarp * 32) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int i = 0; i < kTcSBufs; ++i) {
+      mbar_init(&sfull[i], 1);
+      mbar_init(&sfree[i], 4);
+    }
+    mbar_init(ofull, 1);
+    mbar_init(finb, 1);
+    for (int i = 0; i < kTcPBufs; ++i) {
+      mbar_init(&pready[i], 4);
+      mbar_init(&pfree[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&aux[i], 1);
+      mbar_init(&auxfree[i], 4);   // the four epilogue warps
+      mbar_init(&statb[i], 1);
+      mbar_init(&qfree[i], 1);
+      mbar_init(&handoff[i], 4);   // the four epilogue warps
+      mbar_init(&taildone[i], 2);  // the two tail warps
+    }
+    mbar_init(drain, 1);
+    fence_mbar_init();
+  }
+  if (tid == 0) *fail_any = 0;
+  // Operand buffers start at zero (padding rows of q^T and P^T stay zero).
+  {
+    uint4* z = reinterpret_cast<uint4*>(qbuf);
+    for (int i = tid; i < 2 * P::kQBytes / 16; i += kTcThreads) z[i] = make_uint4(0, 0, 0, 0);
+    z = reinterpret_cast<uint4*>(ptile);
+    for (int i = tid; i < kTcPBufs * P::kPTile / 16; i += kTcThreads) z[i] = make_uint4(0, 0, 0, 0);
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, kTcTmemCols);
+    tmem_relinquish();
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  // Every CTA of the cluster has started: shared memory may be addressed remotely.
+  cluster.sync();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tO = tmem + 16 * kTcSBufs;
+
+  auto unit_rows = [&](int k, int& n, int& p, bool& ok) {
+    n = items[2 * k];
+    p = items[2 * k + 1];
+    ok = (n >= 0 && n <= a.capacity && p >= n);
+    const int s1 = ok ? min(s0 + chunk, n) : s0;
+    return max(0, s1 - s0);
+  };
+
+  // Tile order through the ring, shared by the producer and the MMA warp.  For
+  // the non-empty units u0, u1, ... of this CTA:
+  //   K(u0), then for each x: K(u_{x+1})[0, L), V(u_x), K(u_{x+1})[L, end)
+  // with L = min(tiles, kTcLookahead): the next unit's first logits are computed
+  // while the epilogue warps finish the softmax of u_x, so the tensor cores and
+  // the TMA stream do not wait for it.  L stays below the accumulator count,
+  // which the epilogue frees before it needs V(u_x).  A pending
+  // V(u_x) is issued on its own as soon as the walk reaches unit u_x + 2
+  // (empty units in between): the producer then waits for the tail warps to be
+  // done with u_x, which needs V(u_x) -- so every wait looks strictly back.
+  if (warp == kTcProducerWarp) {
+    // ---- producer: the ring of K / V tiles and the per-unit ||v||_1, pos ----------
+    if (lane == 0) {
+      const uint64_t pol = l2_evict_first_policy();
+      bool fail = false;
+      int tt = 0;  // tiles produced
+      // Issue tiles [t0, t1) of unit k (K when isK) into the ring.
+      auto emit = [&](int k, int rows, bool isK, int t0, int t1) {
+        const int u = j + k * NC;
+        const int unit_row = ta.row_base + u * a.slot_stride + s0;
+        const void* m64 = isK ? (const void*)&ta.k64 : (const void*)&ta.v64;
+        const void* m16 = isK ? (const void*)&ta.k16 : (const void*)&ta.v16;
+        for (int t = t0; t < t1 && !fail; ++t, ++tt) {
+          const int st = tt % S;
+          if (tt >= S && !mbar_wait_bounded(&empty[st], (uint32_t)(((tt / S) - 1) & 1))) {
+            fail = true;
+            break;
+          }
+          const int r0 = t * kTcTile;
+          const int rr = (min(kTcTile, rows - r0) + 15) & ~15;  // 16-row granules
+          unsigned char* dst = ring + (size_t)st * P::kStage;
+          mbar_arrive_expect_tx(&full[st], (uint32_t)(rr * D * 2));
+          for (int blk = 0; blk < 2; ++blk) {
+            int ro = 0;
+            for (; ro + 64 <= rr; ro += 64)
+              tma_load_2d(dst + blk * P::kBlock + ro * 128, m64, blk * 64, unit_row + r0 + ro,
+                          &full[st], pol);
+            for (; ro < rr; ro += 16)
+              tma_load_2d(dst + blk * P::kBlock + ro * 128, m16, blk * 64, unit_row + r0 + ro,
+                          &full[st], pol);
+          }
+        }
+      };
+      int prev = -1, prev_rows = 0;
+      for (int k = 0; k < nitems && !fail; ++k) {
+        if (prev >= 0 && prev <= k - 2) {
+          emit(prev, prev_rows, false, 0, (prev_rows + kTcTile - 1) / kTcTile);
+          prev = -1;
+        }
+        int n, p;
+        bool ok;
+        const int rows = unit_rows(k, n, p, ok);
+        const int u = j + k * NC;
+        const size_t ubase = (size_t)u * a.slot_stride;
+        const int b2 = k & 1;
+        if (k >= 2 && !mbar_wait_bounded(&auxfree[b2], (uint32_t)(((k >> 1) - 1) & 1))) {
+          fail = true;
+          break;
+        }
+        if (rows > 0) {
+          const uint32_t small = (uint32_t)(((rows + 3) & ~3) * 4);
+          unsigned char* vdst = vnbase + b2 * P::vn_bytes(chunk);
+          unsigned char* pdst = vnbase + (2 + b2) * P::vn_bytes(chunk);
+          mbar_arrive_expect_tx(&aux[b2], 2u * small);
+          bulk_g2s(vdst, a.vnorm + ubase + s0, small, &aux[b2], pol);
+          bulk_g2s(pdst, a.pos + ubase + s0, small, &aux[b2], pol);
+        } else {
+          mbar_arrive(&aux[b2]);
+          continue;
+        }
+        const int ntile = (rows + kTcTile - 1) / kTcTile;
+        if (prev < 0) {
+          emit(k, rows, true, 0, ntile);
+        } else {
+          const int L = min(ntile, kTcLookahead);
+          const int pnt = (prev_rows + kTcTile - 1) / kTcTile;
+          emit(k, rows, true, 0, L);
+          emit(prev, prev_rows, false, 0, pnt);
+          emit(k, rows, true, L, ntile);
+        }
+        prev = k;
+        prev_rows = rows;
+      }
+      if (prev >= 0 && !fail) emit(prev, prev_rows, false, 0, (prev_rows + kTcTile - 1) / kTcTile);
+      // Every copy issued lands before the CTA may exit.
+      for (int t = max(0, tt - S); t < tt; ++t)
+        (void)mbar_wait_bounded(&full[t % S], (uint32_t)((t / S) & 1));
+      if (fail) {
+        *fail_any = 1;
+        atomicOr(a.err, LF_DEVERR_TIMEOUT);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kTcMmaWarp) {
+    // ---- MMA warp: the q operand (all lanes) and every tcgen05.mma (lane 0) --------
+    constexpr uint32_t kIdA = idesc_bf16_f32(128, 16, false, false);
+    constexpr uint32_t kIdB = idesc_bf16_f32(128, 16, true, false);
+    bool fail = false;
+    int tt = 0, kt = 0, pt = 0, nn = 0;  // tiles, K tiles, P^T tiles, non-empty units
+    int nq[2] = {0, 0};
+    // K tiles [t0, t1) of a unit: S^T = K . q^T into the next free logit accumulator.
+    auto mma_k = [&](int t0, int t1, uint32_t qaddr) {
+      for (int t = t0; t < t1 && !fail; ++t, ++tt, ++kt) {
+        const int st = tt % S;
+        const int buf = kt % kTcSBufs;
+        if (!mbar_wait_bounded(&full[st], (uint32_t)((tt / S) & 1)) ||
+            (kt >= kTcSBufs &&
+             !mbar_wait_bounded(&sfree[buf], (uint32_t)(((kt / kTcSBufs) - 1) & 1)))) {
+          fail = true;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sbase = smem_u32(ring + (size_t)st * P::kStage);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t ko = (uint32_t)((kk >> 2) * P::kBlock + (kk & 3) * 32);
+          const uint32_t qo = (uint32_t)((kk >> 2) * 2048 + (kk & 3) * 32);
+          tc_mma_bf16(tmem + 16 * buf, sw128_desc(sbase + ko, 16, 1024),
+                      sw128_desc(qaddr + qo, 16, 1024), kIdA, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(&sfull[buf]);
+        tc_commit(&empty[st]);
+      }
+    };
+    // All V tiles of a unit: O^T += V^T . P^T, then signal the output.
+    auto mma_v = [&](int rows) {
+      const int ntile = (rows + kTcTile - 1) / kTcTile;
+      for (int vt = 0; vt < ntile && !fail; ++vt, ++tt, ++pt) {
+        const int st = tt % S;
+        const int pb = pt % kTcPBufs;
+        if (!mbar_wait_bounded(&pready[pb], (uint32_t)((pt / kTcPBufs) & 1)) ||
+            !mbar_wait_bounded(&full[st], (uint32_t)((tt / S) & 1))) {
+          fail = true;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sbase = smem_u32(ring + (size_t)st * P::kStage);
+        const int ksteps = (min(kTcTile, rows - vt * kTcTile) + 15) >> 4;
+        const uint32_t pbase = smem_u32(ptile + (size_t)pb * P::kPTile);
+        for (int jj = 0; jj < ksteps; ++jj) {
+          const uint32_t po = (uint32_t)((jj >> 2) * 2048 + (jj & 3) * 32);
+          tc_mma_bf16(tO, sw128_desc(sbase + jj * 2048, P::kBlock, 1024),
+                      sw128_desc(pbase + po, 16, 1024), kIdB, (vt > 0 || jj > 0) ? 1u : 0u);
+        }
+        tc_commit(&empty[st]);
+        tc_commit(&pfree[pb]);
+      }
+      tc_commit(ofull);
+    };
+    int prev = -1, prev_rows = 0;
+    for (int k = 0; k < nitems && !fail; ++k) {
+      if (prev >= 0 && prev <= k - 2) {  // same flush rule as the producer
+        if (lane == 0) mma_v(prev_rows);
+        prev = -1;
+        fail = __shfl_sync(0xffffffffu, fail ? 1 : 0, 0) != 0;
+        if (fail) break;
+      }
+      int n, p;
+      bool ok;
+      const int rows = unit_rows(k, n, p, ok);
+      if (rows == 0) continue;
+      const int ntile = (rows + kTcTile - 1) / kTcTile;
+      const int u = j + k * NC;
+      const int b = u / a.kv_heads;
+      const int g = u - b * a.kv_heads;
+      const int qb = nn & 1;
+      unsigned char* qdst = qbuf + qb * P::kQBytes;
+      // The buffer's previous contents (two units ago) must have been read.
+      bool okq = true;
+      if (lane == 0 && nq[qb] > 0)
+        okq = mbar_wait_bounded(&qfree[qb], (uint32_t)((nq[qb] - 1) & 1));
+      if (__shfl_sync(0xffffffffu, okq ? 1 : 0, 0) == 0) {
+        fail = true;
+        break;
+      }
+      // q^T rows h < G: the group's queries (16-byte chunks, 128-byte swizzle).
+      const T* qg = reinterpret_cast<const T*>(a.q) + ((size_t)b * a.q_heads + (size_t)g * G) * D;
+      for (int c = lane; c < G * 16; c += 32) {
+        const int h = c >> 4;
+        const int ch = c & 15;
+        const uint4 v = *reinterpret_cast<const uint4*>(qg + (size_t)h * D + ch * 8);
+        *reinterpret_cast<uint4*>(qdst + (ch >> 3) * 2048 + h * 128 + (((ch & 7) ^ (h & 7)) << 4)) =
+            v;
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        const uint32_t qaddr = smem_u32(qdst);
+        if (prev < 0) {
+          mma_k(0, ntile, qaddr);
+        } else {
+          const int L = min(ntile, kTcLookahead);
+          mma_k(0, L, qaddr);
+          mma_v(prev_rows);
+          mma_k(L, ntile, qaddr);
+        }
+        tc_commit(&qfree[qb]);
+      }
+      nq[qb] += 1;
+      nn += 1;
+      prev = k;
+      prev_rows = rows;
+      fail = __shfl_sync(0xffffffffu, fail ? 1 : 0, 0) != 0;
+    }
+    if (lane == 0 && prev >= 0 && !fail) mma_v(prev_rows);
+    if (lane == 0) {
+      // Every MMA issued completes before tensor memory is released.
+      tc_commit(drain);
+      (void)mbar_wait_bounded(drain, 0);
+      if (fail) {
+        *fail_any = 1;
+        atomicOr(a.err, LF_DEVERR_TIMEOUT);
+      }
+    }
+    __syncwarp();
+  } else if (warp < kTcTailWarp0) {
+    // ---- epilogue warps 0-3 (thread i <-> TMEM lane i) ---------------------------
+    int kt = 0, ne = 0, pt = 0;
+    for (int k = 0; k < nitems; ++k) {
+      int n, p;
+      bool state_ok;
+      const int rows = unit_rows(k, n, p, state_ok);
+      const int ntile = (rows + kTcTile - 1) / kTcTile;
+      const int b2 = k & 1;
+      float* lg = lgbase + (size_t)b2 * chunk * G;
+      float* o_part = opbase + (size_t)b2 * G * D;
+      const float* vn_s = reinterpret_cast<const float*>(vnbase + b2 * P::vn_bytes(chunk));
+      const int32_t* pos_s =
+          reinterpret_cast<const int32_t*>(vnbase + (2 + b2) * P::vn_bytes(chunk));
+      float* w_s = reinterpret_cast<float*>(vnbase + (4 + b2) * P::vn_bytes(chunk));
+      const int plim = p - a.window;  // a slot is a candidate iff pos < plim
+
+      // The tail warps must be done with this parity's buffers (unit k - 2).
+      bool bad = false;
+      if (k >= 2)
+        bad = !__all_sync(0xffffffffu, mbar_wait_bounded(&taildone[b2],
+                                                         (uint32_t)(((k >> 1) - 1) & 1)));
+      bad = bad || !__all_sync(0xffffffffu,
+                               mbar_wait_bounded(&aux[b2], (uint32_t)((k >> 1) & 1)));
+
+      // Phase A epilogue: logits of this CTA's slots, their max, candidate weights.
+      float mx[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) mx[h] = -INFINITY;
+      for (int t = 0; t < ntile && !bad; ++t, ++kt) {
+        const int buf = kt % kTcSBufs;
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait_bounded(&sfull[buf], (uint32_t)((kt / kTcSBufs) & 1)))) {
+          bad = true;
+          break;
+        }
+        tc_fence_after();
+        float acc[8];
+        tmem_ld8(tmem + 16 * buf + ((uint32_t)(warp * 32) << 16), acc);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sfree[buf]);
+        const int i = t * kTcTile + tid;
+        if (i < rows) {
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            const float s = acc[h] * a.scale_log2;
+            lg[(size_t)i * G + h] = s;
+            mx[h] = fmaxf(mx[h], s);
+          }
+          w_s[i] = (pos_s[i] < plim) ? vn_s[i] : -1.0f;
+        }
+      }
+      const bool any_bad = named_bar_or(1, kTcCompute, bad);
+      // The raw ||v||_1 / positions buffer may be refilled for unit k + 2.
+      if (lane == 0) mbar_arrive(&auxfree[b2]);
+      bool bad2 = false;
+      if (rows > 0 && !any_bad) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) mx[h] = warp_max(mx[h]);
+        if (lane == 0)
+#pragma unroll
+          for (int h = 0; h < G; ++h) red[warp * kMaxGroup + h] = mx[h];
+        named_bar_sync(1, kTcCompute);
+        float ml[G], sm[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          float m = -INFINITY;
+          for (int w = 0; w < 4; ++w) m = fmaxf(m, red[w * kMaxGroup + h]);
+          ml[h] = m;
+          sm[h] = 0.f;
+        }
+        // p = 2^(s - m) (kept in fp32 for the score) and the bf16 hi/lo P^T operand,
+        // ahead of the MMAs in a ring of kTcPBufs tiles; slots past `rows` are zero.
+        for (int vt = 0; vt < ntile; ++vt, ++pt) {
+          const int pb = pt % kTcPBufs;
+          if (pt >= kTcPBufs &&
+              !__all_sync(0xffffffffu, mbar_wait_bounded(&pfree[pb],
+                                                         (uint32_t)(((pt / kTcPBufs) - 1) & 1)))) {
+            bad2 = true;  // the MMA warp stopped; it reports the error
+            break;
+          }
+          const int i = vt * kTcTile + tid;
+          unsigned char* ptb = ptile + (size_t)pb * P::kPTile + ((tid >> 6) & 1) * 2048;
+          const int c = tid & 63;
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            float pv = 0.f;
+            if (i < rows) {
+              pv = exp2f(lg[(size_t)i * G + h] - ml[h]);
+              lg[(size_t)i * G + h] = pv;
+              sm[h] += pv;
+            }
+            const T hi = __float2bfloat16_rn(pv);
+            const T lo = __float2bfloat16_rn(pv - __bfloat162float(hi));
+            *reinterpret_cast<T*>(ptb + sw128_offset(h, c)) = hi;
+            *reinterpret_cast<T*>(ptb + sw128_offset(G + h, c)) = lo;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&pready[pb]);
+        }
+#pragma unroll
+        for (int h = 0; h < G; ++h) sm[h] = warp_sum(sm[h]);
+        named_bar_sync(1, kTcCompute);  // every warp has read red[] (the maxima)
+        if (lane == 0)
+#pragma unroll
+          for (int h = 0; h < G; ++h) red[warp * kMaxGroup + h] = sm[h];
+        named_bar_sync(1, kTcCompute);
+        if (tid < G) {
+          float sl = 0.f;
+          for (int w = 0; w < 4; ++w) sl += red[w * kMaxGroup + tid];
+          m_loc[b2 * kMaxGroup + tid] = ml[tid];
+          l_loc[b2 * kMaxGroup + tid] = sl;
+        }
+        // The output accumulator: thread e <-> TMEM lane e <-> output element e.
+        if (!bad2 && __all_sync(0xffffffffu, mbar_wait_bounded(ofull, (uint32_t)(ne & 1)))) {
+          tc_fence_after();
+          float o[16];
+          tmem_ld16(tO + ((uint32_t)(warp * 32) << 16), o);
+          tmem_wait_ld();
+          tc_fence_before();
+#pragma unroll
+          for (int h = 0; h < G; ++h) o_part[h * D + tid] = o[h] + o[G + h];
+        } else {
+          bad2 = true;
+        }
+      }
+      if (rows > 0) ne += 1;
+      const bool failed = any_bad || named_bar_or(1, kTcCompute, bad2);
+      if (rows == 0 || failed) {
+        if (tid < G) {
+          m_loc[b2 * kMaxGroup + tid] = -INFINITY;
+          l_loc[b2 * kMaxGroup + tid] = 0.f;
+        }
+#pragma unroll
+        for (int h = 0; h < G; ++h) o_part[h * D + tid] = 0.f;
+      }
+      if (tid == 0) uflag[b2] = failed ? 1 : 0;
+      if (failed && tid == 0) {
+        *fail_any = 1;
+        atomicOr(a.err, LF_DEVERR_TIMEOUT);
+      }
+      // Hand the unit over to the tail warps (release of the writes above).
+      named_bar_sync(1, kTcCompute);
+      if (lane == 0) mbar_arrive(&handoff[b2]);
+    }
+  } else {
+    // ---- tail warps 6-7: exchange, exact scores, leader's output and eviction -----
+    const int tt_id = tid - kTcTailWarp0 * 32;  // 0..63
+    const int twarp = tt_id >> 5;
+    for (int k = 0; k < nitems; ++k) {
+      int n, p;
+      bool state_ok;
+      const int rows = unit_rows(k, n, p, state_ok);
+      const int u = j + k * NC;
+      const int b = u / a.kv_heads;
+      const int g = u - b * a.kv_heads;
+      const int bud = a.budget[b];
+      const bool evicting = state_ok && a.evict && n >= bud;
+      const int b2 = k & 1;
+      const float* lg = lgbase + (size_t)b2 * chunk * G;
+      const float* o_part = opbase + (size_t)b2 * G * D;
+      const float* w_s = reinterpret_cast<const float*>(vnbase + (4 + b2) * P::vn_bytes(chunk));
+      const size_t ubase = (size_t)u * a.slot_stride;
+      const T* qg = reinterpret_cast<const T*>(a.q) + ((size_t)b * a.q_heads + (size_t)g * G) * D;
+      const T* kn = reinterpret_cast<const T*>(a.k_new) + (size_t)u * D;
+      const T* vn = reinterpret_cast<const T*>(a.v_new) + (size_t)u * D;
+      float* snw = s_new + b2 * kMaxGroup;
+      const float* mlc = m_loc + b2 * kMaxGroup;
+      const float* llc = l_loc + b2 * kMaxGroup;
+
+      // The new token's logits (every CTA computes them), before the hand-off wait.
+      for (int h = twarp; h < G; h += 2) {
+        float s = 0.f;
+        for (int e = lane; e < D; e += 32)
+          s = fmaf(to_f32(qg[(size_t)h * D + e]), to_f32(kn[e]), s);
+        s = warp_sum(s);
+        if (lane == 0) snw[h] = s * a.scale_log2;
+      }
+      const bool got_unit = __all_sync(
+          0xffffffffu, mbar_wait_bounded(&handoff[b2], (uint32_t)((k >> 1) & 1)));
+      named_bar_sync(2, kTcTail);
+      const bool unit_failed = !got_unit || uflag[b2] != 0;
+
+      // Exchange 1: every CTA's (m_h, l_h) to every CTA of the cluster.
+      float* sin = stat_in + (size_t)b2 * kMaxCluster * 2 * kMaxGroup;
+      if (tt_id == 0) {
+        mbar_arrive_expect_tx(&statb[b2], (uint32_t)(C * 2 * kMaxGroup * 4));
+        const uint32_t src = smem_u32(sin + (size_t)rank * 2 * kMaxGroup);
+        const uint32_t bar = smem_u32(&statb[b2]);
+        uint32_t v[2 * kMaxGroup];
+#pragma unroll
+        for (int h = 0; h < kMaxGroup; ++h) {
+          v[h] = __float_as_uint(h < G ? mlc[h] : -INFINITY);
+          v[kMaxGroup + h] = __float_as_uint(h < G ? llc[h] : 0.f);
+        }
+        for (int r = 0; r < C; ++r) {
+          const uint32_t ra = mapa_u32(src, (uint32_t)r);
+          const uint32_t rb = mapa_u32(bar, (uint32_t)r);
+#pragma unroll
+          for (int q4 = 0; q4 < 2 * kMaxGroup; q4 += 4)
+            st_async_v4(ra + q4 * 4, v[q4], v[q4 + 1], v[q4 + 2], v[q4 + 3], rb);
+        }
+      }
+      const bool got_stats = __all_sync(
+          0xffffffffu, mbar_wait_cluster_bounded(&statb[b2], (uint32_t)((k >> 1) & 1)));
+      if (tt_id < G) {
+        const int h = tt_id;
+        float M = snw[h];
+        for (int r = 0; r < C; ++r) M = fmaxf(M, sin[r * 2 * kMaxGroup + h]);
+        float L = exp2f(snw[h] - M);
+        for (int r = 0; r < C; ++r) {
+          const float mr = sin[r * 2 * kMaxGroup + h];
+          if (mr != -INFINITY) L += sin[r * 2 * kMaxGroup + kMaxGroup + h] * exp2f(mr - M);
+        }
+        m_glb[h] = M;
+        l_glb[h] = L;
+        cmul[h] = (mlc[h] != -INFINITY) ? exp2f(mlc[h] - M) / L : 0.f;
+        if (!(isfinite(M) && isfinite(L) && L > 0.f)) atomicOr(a.err, LF_DEVERR_NONFINITE);
+      }
+      const bool stats_ok = !named_bar_or(2, kTcTail, !got_stats);
+      if (!stats_ok && tt_id == 0) {
+        *fail_any = 1;
+        atomicOr(a.err, LF_DEVERR_TIMEOUT);
+      }
+
+      // Exact LongFlow scores of this CTA's candidates and their (score, slot) minimum.
+      float bs = INFINITY;
+      int bi = INT_MAX;
+      if (evicting && !unit_failed && stats_ok) {
+        float cm[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) cm[h] = cmul[h];
+        for (int i = tt_id; i < rows; i += kTcTail) {
+          const float w = w_s[i];
+          if (w >= 0.f) {
+            float acc = 0.f;
+#pragma unroll
+            for (int h = 0; h < G; ++h) acc = fmaf(lg[(size_t)i * G + h], cm[h], acc);
+            const float sc = w * acc;
+            if (better(sc, s0 + i, bs, bi)) {
+              bs = sc;
+              bi = s0 + i;
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float os = __shfl_xor_sync(0xffffffffu, bs, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (better(os, oi, bs, bi)) {
+          bs = os;
+          bi = oi;
+        }
+      }
+      if (lane == 0) {
+        red_t[twarp] = bs;
+        red_ti[twarp] = bi;
+      }
+      named_bar_sync(2, kTcTail);
+
+      // Exchange 2: partial output and lowest (score, slot) to the unit's leader.
+      // One receive buffer suffices: a peer can send the leader's next unit only
+      // after the leader has sent its own statistics for it, i.e. finished this one.
+      const int leader = k % C;
+      unsigned char* fin = fin_in;
+      if (rank == leader && tt_id == 0) mbar_arrive_expect_tx(finb, (uint32_t)(C * P::kFinBytes));
+      {
+        const uint32_t dst = mapa_u32(smem_u32(fin + (size_t)rank * P::kFinBytes), (uint32_t)leader);
+        const uint32_t rb = mapa_u32(smem_u32(finb), (uint32_t)leader);
+        for (int c = tt_id; c < G * D / 4; c += kTcTail) {
+          const uint4 v = *reinterpret_cast<const uint4*>(o_part + c * 4);
+          st_async_v4(dst + c * 16, v.x, v.y, v.z, v.w, rb);
+        }
+        if (tt_id == 0) {
+          if (better(red_t[1], red_ti[1], bs, bi)) {
+            bs = red_t[1];
+            bi = red_ti[1];
+          }
+          const uint32_t flag = (unit_failed || !stats_ok || *fail_any) ? 1u : 0u;
+          st_async_v4(dst + G * D * 4, __float_as_uint(bs), (uint32_t)bi, flag, 0u, rb);
+        }
+      }
+      if (rank == leader) {
+        const bool got = __all_sync(0xffffffffu,
+                                    mbar_wait_cluster_bounded(finb, (uint32_t)((k / C) & 1)));
+        const bool all_got = !named_bar_or(2, kTcTail, !got);
+        // Output: the new token + every CTA's partial output, in rank order.
+        if (all_got && stats_ok) {
+          T* og = reinterpret_cast<T*>(a.out) + ((size_t)b * a.q_heads + (size_t)g * G) * D;
+          for (int idx = tt_id; idx < G * D; idx += kTcTail) {
+            const int h = idx / D;
+            const int e = idx - h * D;
+            float acc = exp2f(snw[h] - m_glb[h]) * to_f32(vn[e]);
+            for (int r = 0; r < C; ++r) {
+              const float mr = sin[r * 2 * kMaxGroup + h];
+              if (mr != -INFINITY)
+                acc += reinterpret_cast<const float*>(fin + (size_t)r * P::kFinBytes)[idx] *
+                       exp2f(mr - m_glb[h]);
+            }
+            from_f32(acc / l_glb[h], &og[(size_t)h * D + e]);
+          }
+        }
+        if (tt_id == 0) {
+          bool any_fail = !all_got || !stats_ok;
+          float fs = INFINITY;
+          int fi = INT_MAX;
+          for (int r = 0; r < C; ++r) {
+            const uint32_t* tail =
+                reinterpret_cast<const uint32_t*>(fin + (size_t)r * P::kFinBytes + G * D * 4);
+            any_fail = any_fail || tail[2] != 0;
+            const float rs = __uint_as_float(tail[0]);
+            const int ri = (int)tail[1];
+            if (better(rs, ri, fs, fi)) {
+              fs = rs;
+              fi = ri;
+            }
+          }
+          int victim = -1;
+          if (evicting) {
+            if (fi != INT_MAX) victim = fi;
+            else if (!any_fail) atomicOr(a.err, LF_DEVERR_STATE);  // no candidate
+          }
+          const int limit = a.evict ? bud : a.capacity;
+          int slot = evicting ? victim : (n < limit ? n : -1);
+          if (!state_ok) atomicOr(a.err, LF_DEVERR_STATE);
+          if (any_fail || !state_ok) {
+            slot = -1;
+            victim = -1;
+          }
+          decision[0] = slot;
+          a.evicted[u] = victim;
+          if (state_ok && !any_fail) {
+            if (!evicting && slot >= 0) a.count[u] = n + 1;
+            a.next_pos[u] = p + 1;
+          }
+        }
+        named_bar_sync(2, kTcTail);
+        const int slot = decision[0];
+        if (slot >= 0) {
+          // In-place overwrite: K, V, ||v||_1 (fp32, from the stored value), position.
+          T* Kd = reinterpret_cast<T*>(a.K) + (ubase + slot) * D;
+          T* Vd = reinterpret_cast<T*>(a.V) + (ubase + slot) * D;
+          for (int e = tt_id; e < D; e += kTcTail) {
+            Kd[e] = kn[e];
+            Vd[e] = vn[e];
+          }
+          if (twarp == 0) {
+            float sl = 0.f;
+            for (int e = lane; e < D; e += 32) sl += fabsf(to_f32(vn[e]));
+            sl = warp_sum(sl);
+            if (lane == 0) {
+              a.vnorm[ubase + slot] = sl;
+              a.pos[ubase + slot] = p;
+            }
+          }
+        }
+      }
+      // Release this parity's buffers (logits, partial output, statistics).
+      named_bar_sync(2, kTcTail);
+      if (lane == 0) mbar_arrive(&taildone[b2]);
+    }
+  }
+
+  // ---- teardown ---------------------------------------------------------------
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTcTmemCols);
+  }
+  // No CTA leaves while a peer may still address its shared memory.
+  cluster.sync();
+}
+
+}  // namespace lf

@@ -6,13 +6,13 @@ namespace lf {
 namespace {
 
 template <int D, int G>
-int smem_bytes_bf16(int stages, int chunk) {
+int smem_bytes_bf16(int stages, int chunk, int /*cluster*/) {
   return DecodePlan<__nv_bfloat16, D, G>::smem_bytes(stages, chunk);
 }
 
 template <int D, int G>
 bool fill(KernelEntry* e) {
-  e->decode = reinterpret_cast<const void*>(&decode_step_kernel<__nv_bfloat16, D, G>);
+  e->decode = reinterpret_cast<const void*>(&decode_step_simt_kernel<__nv_bfloat16, D, G>);
   e->prefill = reinterpret_cast<const void*>(&prefill_kernel<__nv_bfloat16, D>);
   e->smem_bytes = &smem_bytes_bf16<D, G>;
   e->head_dim = D;

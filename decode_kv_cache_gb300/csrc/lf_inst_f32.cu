@@ -6,13 +6,13 @@ namespace lf {
 namespace {
 
 template <int D, int G>
-int smem_bytes_f32(int stages, int chunk) {
+int smem_bytes_f32(int stages, int chunk, int /*cluster*/) {
   return DecodePlan<float, D, G>::smem_bytes(stages, chunk);
 }
 
 template <int D, int G>
 bool fill(KernelEntry* e) {
-  e->decode = reinterpret_cast<const void*>(&decode_step_kernel<float, D, G>);
+  e->decode = reinterpret_cast<const void*>(&decode_step_simt_kernel<float, D, G>);
   e->prefill = reinterpret_cast<const void*>(&prefill_kernel<float, D>);
   e->smem_bytes = &smem_bytes_f32<D, G>;
   e->head_dim = D;

@@ -3,15 +3,20 @@
 
 namespace lf {
 
+enum KernelKind { kSimt = 0, kTensorCore = 1 };
+
 struct KernelEntry {
-  const void* decode = nullptr;   // __global__ void(DecodeArgs)
+  int kind = kSimt;               // kSimt: decode(DecodeArgs); kTensorCore: decode(TcArgs)
+  const void* decode = nullptr;
   const void* prefill = nullptr;  // __global__ void(PrefillArgs)
-  int (*smem_bytes)(int stages, int chunk) = nullptr;
+  int (*smem_bytes)(int stages, int chunk, int cluster) = nullptr;
   int head_dim = 0, group = 0, elem_bytes = 0;
 };
 
 // Defined in one translation unit per element type.
 bool find_kernels_bf16(int head_dim, int group, KernelEntry* out);
 bool find_kernels_f32(int head_dim, int group, KernelEntry* out);
+// tcgen05 path: bf16 storage, head_dim 128, group 1/2/4/8.
+bool find_kernels_tc(int head_dim, int group, KernelEntry* out);
 
 }  // namespace lf

@@ -19,7 +19,8 @@ import torch
 
 __all__ = [
     "LF_OK", "LF_ERR_ARG", "LF_ERR_OOM", "LF_ERR_CUDA", "LF_ERR_DEVICE", "LF_ERR_UNSUPPORTED",
-    "LF_BF16", "LF_F32", "LF_DEVERR_NONFINITE", "LF_DEVERR_STATE", "LF_DEVERR_TIMEOUT",
+    "LF_BF16", "LF_F32", "LF_KERNEL_AUTO", "LF_KERNEL_SIMT", "LF_KERNEL_TENSOR_CORE",
+    "LF_DEVERR_NONFINITE", "LF_DEVERR_STATE", "LF_DEVERR_TIMEOUT",
     "LFError", "LFConfig", "LFLayout", "load_library", "library_path",
     "lf_cache_create", "lf_cache_create_ex", "lf_cache_destroy", "lf_prefill_fill",
     "lf_decode_step", "lf_cache_check", "lf_cache_layout", "lf_last_error", "lf_abi_version",
@@ -28,6 +29,8 @@ __all__ = [
 
 LF_OK, LF_ERR_ARG, LF_ERR_OOM, LF_ERR_CUDA, LF_ERR_DEVICE, LF_ERR_UNSUPPORTED = 0, -1, -2, -3, -5, -7
 LF_BF16, LF_F32 = 0, 1
+LF_KERNEL_AUTO, LF_KERNEL_SIMT, LF_KERNEL_TENSOR_CORE = 0, 1, 2
+_KERNEL = {"auto": LF_KERNEL_AUTO, "simt": LF_KERNEL_SIMT, "tc": LF_KERNEL_TENSOR_CORE}
 LF_DEVERR_NONFINITE, LF_DEVERR_STATE, LF_DEVERR_TIMEOUT = 1, 2, 4
 
 _DTYPE = {"bf16": LF_BF16, "f32": LF_F32}
@@ -43,13 +46,13 @@ class LFError(RuntimeError):
 class LFConfig(ctypes.Structure):
     _fields_ = [("dtype", ctypes.c_int), ("evict", ctypes.c_int),
                 ("budgets", ctypes.POINTER(ctypes.c_int32)), ("cluster", ctypes.c_int),
-                ("stages", ctypes.c_int)]
+                ("stages", ctypes.c_int), ("kernel", ctypes.c_int)]
 
 
 class LFLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "layers", "batch", "kv_heads", "q_heads", "head_dim", "capacity", "slot_stride",
-        "window", "dtype", "evict", "cluster", "stages")] + [
+        "window", "dtype", "evict", "cluster", "stages", "kernel")] + [
         ("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("vnorm", ctypes.c_void_p),
         ("pos", ctypes.c_void_p), ("count", ctypes.c_void_p), ("next_pos", ctypes.c_void_p),
         ("budget", ctypes.c_void_p), ("err", ctypes.c_void_p)]
@@ -137,7 +140,7 @@ def lf_cache_create(layers, batch, kv_heads, q_heads, head_dim, budget, window) 
 
 def lf_cache_create_ex(layers, batch, kv_heads, q_heads, head_dim, capacity, window,
                        dtype="bf16", evict=True, budgets: Optional[Sequence[int]] = None,
-                       cluster=0, stages=0) -> int:
+                       cluster=0, stages=0, kernel="auto") -> int:
     cfg = LFConfig()
     cfg.dtype = _DTYPE[dtype] if isinstance(dtype, str) else int(dtype)
     cfg.evict = int(bool(evict))
@@ -147,6 +150,7 @@ def lf_cache_create_ex(layers, batch, kv_heads, q_heads, head_dim, capacity, win
         cfg.budgets = ctypes.cast(arr, ctypes.POINTER(ctypes.c_int32))
     cfg.cluster = int(cluster)
     cfg.stages = int(stages)
+    cfg.kernel = _KERNEL[kernel] if isinstance(kernel, str) else int(kernel)
     h = load_library().lf_cache_create_ex(layers, batch, kv_heads, q_heads, head_dim, capacity,
                                           window, ctypes.byref(cfg))
     if not h:
@@ -203,12 +207,14 @@ class LFCache:
     """One LongFlow cache (owns the C handle).  Sizes as in ``lf_cache_create_ex``."""
 
     def __init__(self, layers, batch, kv_heads, q_heads, head_dim, capacity, window,
-                 dtype="bf16", evict=True, budgets=None, cluster=0, stages=0, device=None):
+                 dtype="bf16", evict=True, budgets=None, cluster=0, stages=0, kernel="auto",
+                 device=None):
         self.device = torch.device("cuda", torch.cuda.current_device() if device is None
                                    else torch.device(device).index or 0)
         with torch.cuda.device(self.device):
             self.handle = lf_cache_create_ex(layers, batch, kv_heads, q_heads, head_dim, capacity,
-                                             window, dtype, evict, budgets, cluster, stages)
+                                             window, dtype, evict, budgets, cluster, stages,
+                                             kernel)
         self.layout = lf_cache_layout(self.handle)
         self.dtype = _TORCH_DTYPE[self.layout.dtype]
         self.layers, self.batch = layers, batch

@@ -65,6 +65,13 @@ typedef enum lf_status {
 
 typedef enum lf_dtype { LF_BF16 = 0, LF_F32 = 1 } lf_dtype;
 
+/* Which decode kernel to build the cache for. */
+typedef enum lf_kernel {
+  LF_KERNEL_AUTO = 0,        /* tensor cores where supported, else CUDA cores */
+  LF_KERNEL_SIMT = 1,        /* CUDA-core dot products (every dtype / head_dim) */
+  LF_KERNEL_TENSOR_CORE = 2  /* tcgen05 MMAs: bf16, head_dim 128, group 1/2/4/8 */
+} lf_kernel;
+
 /* Bits of the device error word (lf_cache_check). */
 #define LF_DEVERR_NONFINITE 1 /* a softmax max/denominator was not finite */
 #define LF_DEVERR_STATE 2     /* no eviction candidate / count out of range */
@@ -78,6 +85,7 @@ typedef struct lf_config {
                              > window when evicting), or NULL: every budget = capacity */
   int cluster;            /* CTAs that split one KV head's slots (1,2,4,8,16); 0 = auto */
   int stages;             /* depth of the shared-memory staging ring (2..16); 0 = auto */
+  int kernel;             /* lf_kernel; LF_KERNEL_AUTO by default */
 } lf_config;
 
 /*
@@ -147,6 +155,7 @@ typedef struct lf_layout {
   int slot_stride;  /* allocated slots per unit (capacity rounded up) */
   int window, dtype, evict;
   int cluster, stages; /* launch shape of lf_decode_step */
+  int kernel;          /* LF_KERNEL_SIMT or LF_KERNEL_TENSOR_CORE */
   void* k;          /* cache dtype */
   void* v;          /* cache dtype */
   float* vnorm;     /* fp32 ||v||_1 of each slot, written at insert */

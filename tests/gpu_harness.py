@@ -73,7 +73,7 @@ class ParityRun:
     def __init__(self, wl: Workload, layers: Sequence[int] = (0,), seed: int = 0,
                  sample: Optional[Sequence[Tuple[int, int, int]]] = None, cluster: int = 0,
                  stages: int = 0, evict: bool = True, capacity: Optional[int] = None,
-                 budgets: Optional[Sequence[int]] = None, device="cuda"):
+                 budgets: Optional[Sequence[int]] = None, device="cuda", kernel: str = "auto"):
         self.wl = wl
         self.layers = list(layers)
         self.stream = InputStream(wl, seed=seed, device=device, layers=self.layers)
@@ -85,7 +85,7 @@ class ParityRun:
         self.cache = LFCache(len(self.layers), wl.batch, wl.kv_heads, wl.q_heads, wl.head_dim,
                              cap, wl.window, dtype=wl.dtype, evict=evict,
                              budgets=self.budgets if evict else None, cluster=cluster,
-                             stages=stages)
+                             stages=stages, kernel=kernel)
         if sample is None:
             sample = [(li, b, g) for li in range(len(self.layers)) for b in range(wl.batch)
                       for g in range(wl.kv_heads)]

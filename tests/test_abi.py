@@ -48,7 +48,8 @@ def test_abi_version_matches_header(lib):
 def test_constants_match_header():
     text = _header()
     for name in ["LF_OK", "LF_ERR_ARG", "LF_ERR_OOM", "LF_ERR_CUDA", "LF_ERR_DEVICE",
-                 "LF_ERR_UNSUPPORTED", "LF_BF16", "LF_F32"]:
+                 "LF_ERR_UNSUPPORTED", "LF_BF16", "LF_F32", "LF_KERNEL_AUTO", "LF_KERNEL_SIMT",
+                 "LF_KERNEL_TENSOR_CORE"]:
         m = re.search(rf"\b{name}\s*=\s*(-?\d+)", text)
         assert m and int(m.group(1)) == getattr(lf, name), name
     for name in ["LF_DEVERR_NONFINITE", "LF_DEVERR_STATE", "LF_DEVERR_TIMEOUT"]:

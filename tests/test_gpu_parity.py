@@ -98,11 +98,40 @@ def test_edge_cases(case):
     _run(wl, 80, cluster=cluster, capacity=cap)
 
 
-@pytest.mark.parametrize("cluster,stages", [(1, 4), (2, 2), (4, 8), (8, 3), (16, 16)])
-def test_launch_shapes_agree(cluster, stages):
-    """Every cluster size and ring depth gives the oracle's results."""
-    wl = WORKLOADS["r1-llama-8b"].scaled(batch=2, prefill=3200)
-    _run(wl, 100, cluster=cluster, stages=stages, sample=[(0, 0, 0), (0, 1, 5)])
+@pytest.mark.parametrize("kernel,cluster,stages", [
+    ("simt", 1, 4), ("simt", 2, 2), ("simt", 4, 8), ("simt", 8, 3), ("simt", 16, 16),
+    ("tc", 1, 2), ("tc", 2, 2), ("tc", 4, 3), ("tc", 8, 4), ("tc", 16, 3)])
+def test_launch_shapes_agree(kernel, cluster, stages):
+    """Both kernels, every cluster size and ring depth give the oracle's results."""
+    # cluster 1 keeps every slot of a unit in one CTA: use a budget that fits
+    budget = 1500 if cluster == 1 else 3276
+    wl = WORKLOADS["r1-llama-8b"].scaled(batch=2, budget=budget, prefill=budget - 76)
+    _run(wl, 100, cluster=cluster, stages=stages, kernel=kernel, sample=[(0, 0, 0), (0, 1, 5)])
+
+
+@pytest.mark.parametrize("case", [
+    # name, overrides, cluster: tensor-core kernel (bf16, d = 128) edge cases
+    ("g1_empty_start", dict(q_heads=3, kv_heads=3, budget=37, window=3, prefill=0, batch=2), 4),
+    ("g2_multi_tile_ragged", dict(q_heads=4, kv_heads=2, budget=300, window=6, prefill=290,
+                                  batch=2), 1),
+    ("g8_single_candidate", dict(q_heads=8, kv_heads=1, budget=140, window=139, prefill=140,
+                                 batch=2), 2),
+    ("g4_sparse_cluster16", dict(q_heads=8, kv_heads=2, budget=130, window=5, prefill=120,
+                                 batch=2), 16),
+    ("g4_tail_of_one", dict(q_heads=8, kv_heads=2, budget=129, window=2, prefill=129,
+                            batch=2), 1),
+], ids=lambda c: c[0])
+def test_tensor_core_edge_cases(case):
+    name, over, cluster = case
+    wl = WORKLOADS["r1-llama-8b"].scaled(layers=1, v_lognormal_sigma=0.5, **over)
+    _run(wl, 60, cluster=cluster, kernel="tc")
+
+
+def test_simt_kernel_full_size_eviction():
+    """The CUDA-core kernel at the full r1-llama-8b launch shape."""
+    wl = WORKLOADS["r1-llama-8b"].scaled(prefill=3240)
+    st = _run(wl, 80, layers=(1,), kernel="simt", sample=[(0, 4, 1), (0, 30, 6)])
+    assert st.evictions >= 2 * 40
 
 
 def test_nonfinite_query_sets_error_word():
