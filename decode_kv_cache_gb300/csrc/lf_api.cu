@@ -123,6 +123,8 @@ void destroy_memory(lf_cache* c) {
 
 }  // namespace
 
+void lf::set_last_error(const std::string& msg) { g_last_error = msg; }
+
 extern "C" {
 
 const char* lf_last_error(void) { return g_last_error.c_str(); }

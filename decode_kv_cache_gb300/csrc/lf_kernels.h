@@ -1,7 +1,12 @@
 // Internal table of compiled decode/prefill kernel instantiations.
 #pragma once
 
+#include <string>
+
 namespace lf {
+
+// Message returned by lf_last_error() on this thread.
+void set_last_error(const std::string& msg);
 
 enum KernelKind { kSimt = 0, kTensorCore = 1 };
 

@@ -1,0 +1,128 @@
+// lf_prefill_fill_noalloc: the prefill step for callers that cannot allocate
+// device memory (see include/longflow.h).
+//
+// The prefill kernel reads each sequence's prompt length from device memory.
+// lf_prefill_fill keeps those lengths in memory that lf_cache_create_ex
+// allocated; this entry point instead uses a fixed array compiled into the
+// library, so a caller that owns the slab memory itself can run the prefill
+// without any allocation.  The array is shared by every call on a device and
+// keeps the last call's contents (the call overwrites the first `batch`
+// entries before the kernel reads them); calls whose kernels overlap on the
+// GPU race on it.
+#include <cuda_runtime.h>
+
+#include <mutex>
+#include <string>
+
+#include "lf_decode.cuh"
+#include "lf_kernels.h"
+#include "longflow.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+// One prompt length per sequence: 64 KB on every device that loads the library.
+__device__ __align__(256) int32_t g_prompt_len_scratch[LF_NOALLOC_MAX_BATCH];
+
+std::mutex g_setup_mutex;
+int32_t* g_scratch_ptr[kMaxDevices] = {nullptr};
+
+int noalloc_fail(int code, const std::string& msg) {
+  lf::set_last_error(msg);
+  return code;
+}
+
+// Device address of the scratch array on the current device (set up once per
+// device, with that device current).
+int scratch_address(int32_t** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return noalloc_fail(LF_ERR_CUDA, cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return noalloc_fail(LF_ERR_ARG, "device index too large");
+  std::lock_guard<std::mutex> lock(g_setup_mutex);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_prompt_len_scratch);
+    if (e != cudaSuccess || !p) {
+      (void)cudaGetLastError();
+      return noalloc_fail(LF_ERR_CUDA, std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e));
+    }
+    g_scratch_ptr[dev] = static_cast<int32_t*>(p);
+  }
+  *out = g_scratch_ptr[dev];
+  return LF_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" int lf_prefill_fill_noalloc(const lf_layout* dst, int layer, const void* k,
+                                       const void* v, const int32_t* prompt_len, int max_prompt,
+                                       lf_stream_t stream) {
+  if (!dst) return noalloc_fail(LF_ERR_ARG, "null destination layout");
+  if (!dst->k || !dst->v || !dst->vnorm || !dst->pos || !dst->count || !dst->next_pos)
+    return noalloc_fail(LF_ERR_ARG, "destination layout has a null pointer");
+  if (layer < 0 || layer >= dst->layers) return noalloc_fail(LF_ERR_ARG, "layer out of range");
+  if (dst->batch < 1 || dst->kv_heads < 1 || dst->capacity < 1 ||
+      dst->slot_stride < dst->capacity || dst->slot_stride % 4 != 0)
+    return noalloc_fail(LF_ERR_ARG, "invalid destination shape");
+  if (dst->batch > LF_NOALLOC_MAX_BATCH)
+    return noalloc_fail(LF_ERR_ARG, "batch " + std::to_string(dst->batch) +
+                                        " exceeds LF_NOALLOC_MAX_BATCH (" +
+                                        std::to_string(LF_NOALLOC_MAX_BATCH) + ")");
+  if (!prompt_len || max_prompt < 0) return noalloc_fail(LF_ERR_ARG, "bad prompt lengths");
+  int longest = 0;
+  for (int b = 0; b < dst->batch; ++b) {
+    const int P = prompt_len[b];
+    if (P < 0 || P > max_prompt || P > dst->capacity)
+      return noalloc_fail(LF_ERR_ARG, "prompt_len[" + std::to_string(b) + "] = " +
+                                          std::to_string(P) + " outside [0, min(max_prompt, capacity)]");
+    if (P > longest) longest = P;
+  }
+  if (longest > 0 && (!k || !v || !aligned16(k) || !aligned16(v)))
+    return noalloc_fail(LF_ERR_ARG, "k and v must be non-null and 16-byte aligned");
+  if (!aligned16(dst->k) || !aligned16(dst->v))
+    return noalloc_fail(LF_ERR_ARG, "destination K and V must be 16-byte aligned");
+  lf::KernelEntry kern;
+  const bool found = (dst->dtype == LF_BF16) ? lf::find_kernels_bf16(dst->head_dim, 1, &kern)
+                     : (dst->dtype == LF_F32) ? lf::find_kernels_f32(dst->head_dim, 1, &kern)
+                                              : false;
+  if (!found) return noalloc_fail(LF_ERR_UNSUPPORTED, "unsupported dtype or head_dim");
+
+  int32_t* plen = nullptr;
+  int rc = scratch_address(&plen);
+  if (rc != LF_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(plen, prompt_len, (size_t)dst->batch * 4,
+                                  cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return noalloc_fail(LF_ERR_CUDA, std::string("uploading prompt lengths: ") + cudaGetErrorString(e));
+  }
+  const size_t layer_units = (size_t)dst->batch * dst->kv_heads;
+  const size_t layer_slots = layer_units * dst->slot_stride;
+  const size_t elem = (size_t)kern.elem_bytes;
+  lf::PrefillArgs a;
+  a.k = k;
+  a.v = v;
+  a.plen = plen;
+  a.K = static_cast<char*>(dst->k) + layer * layer_slots * dst->head_dim * elem;
+  a.V = static_cast<char*>(dst->v) + layer * layer_slots * dst->head_dim * elem;
+  a.vnorm = dst->vnorm + layer * layer_slots;
+  a.pos = dst->pos + layer * layer_slots;
+  a.count = dst->count + layer * layer_units;
+  a.next_pos = dst->next_pos + layer * layer_units;
+  a.kv_heads = dst->kv_heads;
+  a.max_prompt = max_prompt;
+  a.slot_stride = dst->slot_stride;
+  void* args[] = {&a};
+  e = cudaLaunchKernel(kern.prefill, dim3(dst->kv_heads, dst->batch, 1), dim3(lf::kThreads, 1, 1),
+                       args, 0, st);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return noalloc_fail(LF_ERR_CUDA, std::string("prefill launch: ") + cudaGetErrorString(e));
+  }
+  return LF_OK;
+}

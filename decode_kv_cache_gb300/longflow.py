@@ -24,6 +24,7 @@ __all__ = [
     "LFError", "LFConfig", "LFLayout", "load_library", "library_path",
     "lf_cache_create", "lf_cache_create_ex", "lf_cache_destroy", "lf_prefill_fill",
     "lf_decode_step", "lf_cache_check", "lf_cache_layout", "lf_last_error", "lf_abi_version",
+    "lf_prefill_fill_noalloc",
     "LFCache",
 ]
 
@@ -95,6 +96,9 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.lf_last_error.argtypes = []
     lib.lf_abi_version.restype = I
     lib.lf_abi_version.argtypes = []
+    lib.lf_prefill_fill_noalloc.restype = I
+    lib.lf_prefill_fill_noalloc.argtypes = [ctypes.POINTER(LFLayout), I, VP, VP,
+                                            ctypes.POINTER(ctypes.c_int32), I, VP]
     _lib = lib
     return lib
 
@@ -180,6 +184,13 @@ def lf_cache_check(handle, stream=None) -> int:
     if code not in (LF_OK, LF_ERR_DEVICE):
         raise LFError(code, lf_last_error())
     return int(bits.value)
+
+
+def lf_prefill_fill_noalloc(dst: LFLayout, layer, k, v, prompt_len: Sequence[int], max_prompt,
+                            stream=None) -> int:
+    arr = (ctypes.c_int32 * len(prompt_len))(*[int(x) for x in prompt_len])
+    return _check(load_library().lf_prefill_fill_noalloc(ctypes.byref(dst), layer, _ptr(k), _ptr(v),
+                                                         arr, int(max_prompt), _stream(stream)))
 
 
 def lf_cache_layout(handle) -> LFLayout:

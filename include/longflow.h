@@ -168,6 +168,36 @@ typedef struct lf_layout {
 
 int lf_cache_layout(const lf_cache* cache, lf_layout* out);
 
+/*
+ * Prefill without any device allocation.  (No counterpart on the pages: this
+ * is an integration entry point, not part of the method.)
+ *
+ * For callers that cannot call cudaMalloc at the point where they prefill:
+ * an engine that reserves all device memory up front and hands out slices of
+ * its own pool, code running where an allocation's implicit device
+ * synchronisation is not allowed, or a runtime without access to the CUDA
+ * allocator.  Such a caller owns the slab itself and describes it with an
+ * lf_layout (k, v, vnorm, pos, count, next_pos, and layers, batch, kv_heads,
+ * head_dim, capacity, slot_stride, dtype; the other fields are ignored), laid
+ * out exactly as lf_cache_layout documents.  The operation, argument meaning
+ * and error behaviour are those of lf_prefill_fill, except that prompt
+ * lengths are checked against `capacity` (the caller keeps its budgets).
+ *
+ * The prompt lengths travel to the GPU through a fixed array compiled into
+ * the library (LF_NOALLOC_MAX_BATCH int32 entries, held by every GPU that
+ * loads the library until the process exits); batches larger than that are
+ * rejected with LF_ERR_ARG.  The array is shared by every call on a device and
+ * keeps the last call's contents (each call overwrites the entries it reads),
+ * so calls whose work overlaps on the GPU (different streams, no ordering)
+ * race on it.  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  Nothing is allocated: no cudaMalloc, no
+ * cudaFree, no allocating library routine.
+ */
+#define LF_NOALLOC_MAX_BATCH 16384
+int lf_prefill_fill_noalloc(const lf_layout* dst, int layer, const void* k, const void* v,
+                            const int32_t* prompt_len, int max_prompt, lf_stream_t stream);
+
 /* Message of the last failed call on this thread ("" if none). */
 const char* lf_last_error(void);
 
