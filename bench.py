@@ -52,6 +52,57 @@ def unit_bytes(wl, n_slots: int, evict: bool = True, writes_slot: bool = True) -
     return b
 
 
+KERNEL_SOURCES = ["lf_decode_tc.cuh", "lf_decode.cuh", "lf_device.cuh"]
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_step_tc_qwen3-8b-steady.md")
+
+
+def kernel_source_hash() -> str:
+    """sha256 over the decode kernels' sources: ties a stored ncu traffic figure
+    to the exact code it was measured on."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "decode_kv_cache_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def stored_traffic(workload: str, batch: int):
+    """DRAM bytes (read + write) per decode launch from the committed ncu
+    summary, if it was taken on this workload and on the current kernel source;
+    else None."""
+    try:
+        text = open(PROFILE_SUMMARY).read()
+    except OSError:
+        return None
+    vals = {}
+    for line in text.splitlines():
+        if ":" in line and line.strip().startswith("- `"):
+            key, _, val = line.strip()[3:].partition("`:")
+            vals[key.strip()] = val.strip().strip("`")
+    try:
+        if (vals.get("kernel_source_sha256") != kernel_source_hash() or
+                vals.get("workload") != workload or int(vals.get("batch", -1)) != batch):
+            return None
+        return int(vals["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def aggregate(ms_local: float, units_local: int, dist=None):
+    """Whole-job throughput of independent replicas: the slowest rank's time
+    and the units of all ranks (max / sum over the process group)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return ms_local, units_local
+    import torch
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([ms_local], dtype=torch.float64, device=dev)
+    u = torch.tensor([units_local], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), int(u.item())
+
+
 def load_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -299,11 +350,7 @@ def bench_ours(args):
         torch.cuda.synchronize()
 
     def max_over_ranks(x: float) -> float:
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return aggregate(x, 0, dist)[0]
 
     # ---- eviction on, steady state (cache pre-filled to the budget) ----
     cache, gen = build_cache(wl, torch, lf, stream_mod, seed=rank, cluster=args.cluster,
@@ -324,12 +371,11 @@ def bench_ours(args):
     ms = time_steps(cache, timed, outs, evs, torch, graph=not args.eager)
     barrier()
     clk = clocks.stop()
-    ms = max_over_ranks(ms)
     bits = cache.check()
     if bits:
         raise RuntimeError(f"device error word {bits} after the timed region")
-    units = wl.batch * L * args.steps
-    value = world * units / (ms / 1000.0)
+    ms, all_units = aggregate(ms, wl.batch * L * args.steps, dist)
+    value = all_units / (ms / 1000.0)
     launches = L * args.steps
     b_unit = unit_bytes(wl, wl.budget)
     bytes_per_launch = b_unit * wl.batch
@@ -422,7 +468,9 @@ def bench_ours(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
                      "frac_of_nominal_8000": achieved / NOMINAL_HBM_GBS,
-                     "traffic": None, "kernel": "decode_step_kernel<bf16,128,4>",
+                     "traffic": stored_traffic(wl.name, wl.batch),
+                     "kernel": (f"decode_step_tc_kernel<{wl.group}>" if lay.kernel == 2 else
+                                f"decode_step_simt_kernel<{wl.dtype},{wl.head_dim},{wl.group}>"),
                      "bytes_per_launch": bytes_per_launch,
                      "timing": "timed region / launches (includes launch gaps)"},
         "cpu_baseline": cpu,
