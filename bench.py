@@ -264,12 +264,15 @@ def build_cache(wl, torch, lf, stream_mod, seed, evict=True, capacity=None, laye
                 cluster=0, stages=0):
     L = wl.layers if layers is None else layers
     cap = capacity or wl.budget
-    cache = lf.LFCache(L, wl.batch, wl.kv_heads, wl.q_heads, wl.head_dim, cap, wl.window,
-                       dtype=wl.dtype, evict=evict, cluster=cluster, stages=stages)
     gen = stream_mod.InputStream(wl, seed=seed, device="cuda", layers=list(range(L)))
+    budgets = gen.budgets if (evict and wl.ragged) else None
+    cache = lf.LFCache(L, wl.batch, wl.kv_heads, wl.q_heads, wl.head_dim, cap, wl.window,
+                       dtype=wl.dtype, evict=evict, budgets=budgets, cluster=cluster,
+                       stages=stages)
     for l in range(L):
         k, v, lens = gen.prompt(l)
-        lens = [min(P, cap) for P in lens]
+        # prompt tokens past a sequence's budget would arrive as decode steps
+        lens = [min(P, budgets[b] if budgets else cap) for b, P in enumerate(lens)]
         cache.prefill(l, k, v, lens)
         del k, v
     torch.cuda.synchronize()
@@ -365,6 +368,7 @@ def bench_ours(args):
     del warm
     if cache.check() != 0:
         raise RuntimeError("device error during warm-up")
+    occ_start = cache.views()["count"][0, :, 0].cpu().tolist()  # occupied slots per sequence
     clocks = ClockSampler(local)
     barrier()
     clocks.start()
@@ -377,8 +381,11 @@ def bench_ours(args):
     ms, all_units = aggregate(ms, wl.batch * L * args.steps, dist)
     value = all_units / (ms / 1000.0)
     launches = L * args.steps
-    b_unit = unit_bytes(wl, wl.budget)
-    bytes_per_launch = b_unit * wl.batch
+    # algorithmic bytes per launch: the mean occupancy over the timed steps (the
+    # start and end counts; steady workloads stay at the budget throughout)
+    occ_end = cache.views()["count"][0, :, 0].cpu().tolist()
+    bytes_per_launch = sum((unit_bytes(wl, int(a)) + unit_bytes(wl, int(e))) // 2
+                           for a, e in zip(occ_start, occ_end))
     achieved = bytes_per_launch / (ms / 1000.0 / launches) / 1e9
     lay = cache.layout
 
@@ -459,8 +466,9 @@ def bench_ours(args):
         wl.dtype == "bf16" else "f32", "data": "synthetic",
         "config": {"workload": wl.name, "layers": L, "batch": wl.batch, "q_heads": wl.q_heads,
                    "kv_heads": wl.kv_heads, "head_dim": wl.head_dim, "budget": wl.budget,
-                   "window": wl.window, "state": "steady (pre-filled to the budget, every step "
-                   "evicts)", "l2": "inputs larger than L2: each layer's slab is "
+                   "window": wl.window, "state": ("steady (pre-filled to the budget, every step "
+                   "evicts)" if wl.prefill >= wl.budget else f"prompt {wl.prefill}, timed from "
+                   "the start of generation"), "l2": "inputs larger than L2: each layer's slab is "
                    f"{wl.batch * wl.kv_heads * lay.slot_stride * wl.head_dim * 2 * wl.elem_bytes / 1e6:.0f} MB",
                    "cluster": lay.cluster, "stages": lay.stages,
                    "launch": "eager" if args.eager else "CUDA graph of all timed steps",

@@ -255,7 +255,7 @@ lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, i
   int chunk = 0, smem = 0, grid_y = 0;
   for (;;) {
     chunk = (int)round_up((size_t)((capacity + cluster - 1) / cluster), 4);
-    smem = kern.smem_bytes(stages, chunk, cluster);
+    smem = kern.smem_bytes(stages, chunk, cluster, c.evict);
     // The tensor-core kernel takes all of an SM's tensor memory: ask for more
     // than half of its shared memory so that never two CTAs share an SM.
     if (tc) smem = std::max(smem, max_sm_smem / 2 + 1024);
@@ -481,13 +481,17 @@ int lf_decode_step(lf_cache* cache, int layer, const void* q, const void* k_new,
   cfg.blockDim = dim3(cache->threads, 1, 1);
   cfg.dynamicSmemBytes = cache->smem;
   cfg.stream = static_cast<cudaStream_t>(stream);
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = cache->cluster;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // Tensor-core kernel: programmatic dependent launch (its prologue overlaps the
+  // previous grid; it waits for that grid before touching global memory).
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = (cache->kern.kind == lf::kTensorCore) ? 2 : 1;
   cudaError_t e;
   if (cache->kern.kind == lf::kTensorCore) {
     lf::TcArgs ta;

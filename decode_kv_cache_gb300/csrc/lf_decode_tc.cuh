@@ -98,12 +98,17 @@ struct TcPlan {
     return off_fin(stages) + cluster * kFinBytes;
   }
   __host__ __device__ static constexpr int vn_bytes(int chunk) { return (chunk + 3) / 4 * 16; }
-  __host__ __device__ static constexpr int off_vn(int stages, int chunk, int cluster) {
-    return (off_lg(stages, cluster) + 2 * chunk * G * 4 + 15) / 16 * 16;  // lg[2]
+  // Eviction needs two logit buffers (the tail warps score unit k while the
+  // epilogue fills unit k+1) and the ||v||_1 / position / weight buffers; the
+  // read-only full-KV mode needs one logit buffer and none of the others.
+  __host__ __device__ static constexpr int off_vn(int stages, int chunk, int cluster, int evict) {
+    return (off_lg(stages, cluster) + (evict ? 2 : 1) * chunk * G * 4 + 15) / 16 * 16;
   }
   // vn[2], pos[2] (raw, from the slab) then w[2] (candidate weights), each vn_bytes(chunk)
-  __host__ __device__ static constexpr int smem_bytes(int stages, int chunk, int cluster) {
-    return off_vn(stages, chunk, cluster) + 6 * vn_bytes(chunk) + 1024;  // + alignment slack
+  __host__ __device__ static constexpr int smem_bytes(int stages, int chunk, int cluster,
+                                                      int evict) {
+    return off_vn(stages, chunk, cluster, evict) + (evict ? 6 * vn_bytes(chunk) : 0) +
+           1024;  // + alignment slack
   }
 };
 
@@ -172,16 +177,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   unsigned char* ptile = smem + P::off_p(S);      // [kTcPBufs] P^T tiles
   unsigned char* fin_in = smem + P::off_fin(S);   // [C][kFinBytes]
   float* lgbase = reinterpret_cast<float*>(smem + P::off_lg(S, C));  // [2][chunk][G]
-  unsigned char* vnbase = smem + P::off_vn(S, chunk, C);
+  unsigned char* vnbase = smem + P::off_vn(S, chunk, C, a.evict);
+  const int lgpar = a.evict ? 1 : 0;  // logit buffers alternate only when scores are needed
 
   // ---- set-up ---------------------------------------------------------------
-  // Occupancy and position of every unit this cluster visits, read once: the
-  // leaders update them during the launch, every role must see the old values.
-  for (int k = tid; k < nitems; k += kTcThreads) {
-    const int u = j + k * NC;
-    items[2 * k] = a.count[u];
-    items[2 * k + 1] = a.next_pos[u];
-  }
+  // Everything up to griddepcontrol.wait touches only this CTA's own shared and
+  // tensor memory, so with programmatic dependent launch it overlaps the tail
+  // of the previous launch on the stream.
   if (tid == kTcProducerWarp * 32) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
@@ -219,6 +221,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == 0) {
     tmem_alloc(tmem_slot, kTcTmemCols);
     tmem_relinquish();
+  }
+  // Global memory from here on: wait until the previous grid on the stream has
+  // completed and its writes are visible (this kernel never lets a dependent
+  // grid pass its own wait early, so back-to-back steps of one layer stay ordered).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // Occupancy and position of every unit this cluster visits, read once: the
+  // leaders update them during the launch, every role must see the old values.
+  for (int k = tid; k < nitems; k += kTcThreads) {
+    const int u = j + k * NC;
+    items[2 * k] = a.count[u];
+    items[2 * k + 1] = a.next_pos[u];
   }
   fence_proxy_async_smem();
   tc_fence_before();
@@ -296,7 +309,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           fail = true;
           break;
         }
-        if (rows > 0) {
+        if (rows > 0 && a.evict) {
           const uint32_t small = (uint32_t)(((rows + 3) & ~3) * 4);
           unsigned char* vdst = vnbase + b2 * P::vn_bytes(chunk);
           unsigned char* pdst = vnbase + (2 + b2) * P::vn_bytes(chunk);
@@ -304,9 +317,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           bulk_g2s(vdst, a.vnorm + ubase + s0, small, &aux[b2], pol);
           bulk_g2s(pdst, a.pos + ubase + s0, small, &aux[b2], pol);
         } else {
-          mbar_arrive(&aux[b2]);
-          continue;
+          mbar_arrive(&aux[b2]);  // nothing to load: complete the phase
         }
+        if (rows == 0) continue;
         const int ntile = (rows + kTcTile - 1) / kTcTile;
         if (prev < 0) {
           emit(k, rows, true, 0, ntile);
@@ -461,7 +474,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int rows = unit_rows(k, n, p, state_ok);
       const int ntile = (rows + kTcTile - 1) / kTcTile;
       const int b2 = k & 1;
-      float* lg = lgbase + (size_t)b2 * chunk * G;
+      float* lg = lgbase + (size_t)(b2 & lgpar) * chunk * G;
       float* o_part = opbase + (size_t)b2 * G * D;
       const float* vn_s = reinterpret_cast<const float*>(vnbase + b2 * P::vn_bytes(chunk));
       const int32_t* pos_s =
@@ -503,7 +516,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             lg[(size_t)i * G + h] = s;
             mx[h] = fmaxf(mx[h], s);
           }
-          w_s[i] = (pos_s[i] < plim) ? vn_s[i] : -1.0f;
+          if (lgpar) w_s[i] = (pos_s[i] < plim) ? vn_s[i] : -1.0f;
         }
       }
       const bool any_bad = named_bar_or(1, kTcCompute, bad);
@@ -614,7 +627,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int bud = a.budget[b];
       const bool evicting = state_ok && a.evict && n >= bud;
       const int b2 = k & 1;
-      const float* lg = lgbase + (size_t)b2 * chunk * G;
+      const float* lg = lgbase + (size_t)(b2 & lgpar) * chunk * G;
       const float* o_part = opbase + (size_t)b2 * G * D;
       const float* w_s = reinterpret_cast<const float*>(vnbase + (4 + b2) * P::vn_bytes(chunk));
       const size_t ubase = (size_t)u * a.slot_stride;

@@ -6,7 +6,7 @@ namespace lf {
 namespace {
 
 template <int D, int G>
-int smem_bytes_bf16(int stages, int chunk, int /*cluster*/) {
+int smem_bytes_bf16(int stages, int chunk, int /*cluster*/, int /*evict*/) {
   return DecodePlan<__nv_bfloat16, D, G>::smem_bytes(stages, chunk);
 }
 

@@ -6,7 +6,7 @@ namespace lf {
 namespace {
 
 template <int D, int G>
-int smem_bytes_f32(int stages, int chunk, int /*cluster*/) {
+int smem_bytes_f32(int stages, int chunk, int /*cluster*/, int /*evict*/) {
   return DecodePlan<float, D, G>::smem_bytes(stages, chunk);
 }
 

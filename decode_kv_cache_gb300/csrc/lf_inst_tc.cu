@@ -6,8 +6,8 @@ namespace lf {
 namespace {
 
 template <int G>
-int smem_bytes_tc(int stages, int chunk, int cluster) {
-  return TcPlan<G>::smem_bytes(stages, chunk, cluster);
+int smem_bytes_tc(int stages, int chunk, int cluster, int evict) {
+  return TcPlan<G>::smem_bytes(stages, chunk, cluster, evict);
 }
 
 template <int G>

@@ -14,7 +14,7 @@ struct KernelEntry {
   int kind = kSimt;               // kSimt: decode(DecodeArgs); kTensorCore: decode(TcArgs)
   const void* decode = nullptr;
   const void* prefill = nullptr;  // __global__ void(PrefillArgs)
-  int (*smem_bytes)(int stages, int chunk, int cluster) = nullptr;
+  int (*smem_bytes)(int stages, int chunk, int cluster, int evict) = nullptr;
   int head_dim = 0, group = 0, elem_bytes = 0;
 };
 
