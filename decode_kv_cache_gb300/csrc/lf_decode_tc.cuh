@@ -134,7 +134,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int chunk = a.chunk;
   const int units = a.batch * a.kv_heads;
   const int nitems = (j < units) ? (units - j + NC - 1) / NC : 0;
-  const int s0 = rank * chunk;
 
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // The 128-byte swizzle phase of TMA writes and MMA reads follows address
@@ -242,12 +241,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const uint32_t tO = tmem + 16 * kTcSBufs;
 
-  auto unit_rows = [&](int k, int& n, int& p, bool& ok) {
+  // This CTA's share of unit k: the occupied slots are split evenly over the
+  // cluster (in multiples of 4), so a partly filled unit keeps every CTA busy.
+  // Returns the slot count and sets `base`, the first slot.
+  auto unit_rows = [&](int k, int& n, int& p, bool& ok, int& base) {
     n = items[2 * k];
     p = items[2 * k + 1];
     ok = (n >= 0 && n <= a.capacity && p >= n);
-    const int s1 = ok ? min(s0 + chunk, n) : s0;
-    return max(0, s1 - s0);
+    const int per = ((n + C - 1) / C + 3) & ~3;  // <= chunk since n <= capacity
+    base = rank * per;
+    return ok ? max(0, min(per, n - base)) : 0;
   };
 
   // Tile order through the ring, shared by the producer and the MMA warp.  For
@@ -267,9 +270,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       bool fail = false;
       int tt = 0;  // tiles produced
       // Issue tiles [t0, t1) of unit k (K when isK) into the ring.
-      auto emit = [&](int k, int rows, bool isK, int t0, int t1) {
+      auto emit = [&](int k, int rows, int base, bool isK, int t0, int t1) {
         const int u = j + k * NC;
-        const int unit_row = ta.row_base + u * a.slot_stride + s0;
+        const int unit_row = ta.row_base + u * a.slot_stride + base;
         const void* m64 = isK ? (const void*)&ta.k64 : (const void*)&ta.v64;
         const void* m16 = isK ? (const void*)&ta.k16 : (const void*)&ta.v16;
         for (int t = t0; t < t1 && !fail; ++t, ++tt) {
@@ -293,15 +296,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
       };
-      int prev = -1, prev_rows = 0;
+      int prev = -1, prev_rows = 0, prev_base = 0;
       for (int k = 0; k < nitems && !fail; ++k) {
         if (prev >= 0 && prev <= k - 2) {
-          emit(prev, prev_rows, false, 0, (prev_rows + kTcTile - 1) / kTcTile);
+          emit(prev, prev_rows, prev_base, false, 0, (prev_rows + kTcTile - 1) / kTcTile);
           prev = -1;
         }
-        int n, p;
+        int n, p, base;
         bool ok;
-        const int rows = unit_rows(k, n, p, ok);
+        const int rows = unit_rows(k, n, p, ok, base);
         const int u = j + k * NC;
         const size_t ubase = (size_t)u * a.slot_stride;
         const int b2 = k & 1;
@@ -314,26 +317,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           unsigned char* vdst = vnbase + b2 * P::vn_bytes(chunk);
           unsigned char* pdst = vnbase + (2 + b2) * P::vn_bytes(chunk);
           mbar_arrive_expect_tx(&aux[b2], 2u * small);
-          bulk_g2s(vdst, a.vnorm + ubase + s0, small, &aux[b2], pol);
-          bulk_g2s(pdst, a.pos + ubase + s0, small, &aux[b2], pol);
+          bulk_g2s(vdst, a.vnorm + ubase + base, small, &aux[b2], pol);
+          bulk_g2s(pdst, a.pos + ubase + base, small, &aux[b2], pol);
         } else {
           mbar_arrive(&aux[b2]);  // nothing to load: complete the phase
         }
         if (rows == 0) continue;
         const int ntile = (rows + kTcTile - 1) / kTcTile;
         if (prev < 0) {
-          emit(k, rows, true, 0, ntile);
+          emit(k, rows, base, true, 0, ntile);
         } else {
           const int L = min(ntile, kTcLookahead);
           const int pnt = (prev_rows + kTcTile - 1) / kTcTile;
-          emit(k, rows, true, 0, L);
-          emit(prev, prev_rows, false, 0, pnt);
-          emit(k, rows, true, L, ntile);
+          emit(k, rows, base, true, 0, L);
+          emit(prev, prev_rows, prev_base, false, 0, pnt);
+          emit(k, rows, base, true, L, ntile);
         }
         prev = k;
         prev_rows = rows;
+        prev_base = base;
       }
-      if (prev >= 0 && !fail) emit(prev, prev_rows, false, 0, (prev_rows + kTcTile - 1) / kTcTile);
+      if (prev >= 0 && !fail)
+        emit(prev, prev_rows, prev_base, false, 0, (prev_rows + kTcTile - 1) / kTcTile);
       // Every copy issued lands before the CTA may exit.
       for (int t = max(0, tt - S); t < tt; ++t)
         (void)mbar_wait_bounded(&full[t % S], (uint32_t)((t / S) & 1));
@@ -407,9 +412,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         fail = __shfl_sync(0xffffffffu, fail ? 1 : 0, 0) != 0;
         if (fail) break;
       }
-      int n, p;
+      int n, p, base;
       bool ok;
-      const int rows = unit_rows(k, n, p, ok);
+      const int rows = unit_rows(k, n, p, ok, base);
       if (rows == 0) continue;
       const int ntile = (rows + kTcTile - 1) / kTcTile;
       const int u = j + k * NC;
@@ -469,9 +474,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ---- epilogue warps 0-3 (thread i <-> TMEM lane i) ---------------------------
     int kt = 0, ne = 0, pt = 0;
     for (int k = 0; k < nitems; ++k) {
-      int n, p;
+      int n, p, base;
       bool state_ok;
-      const int rows = unit_rows(k, n, p, state_ok);
+      const int rows = unit_rows(k, n, p, state_ok, base);
       const int ntile = (rows + kTcTile - 1) / kTcTile;
       const int b2 = k & 1;
       float* lg = lgbase + (size_t)(b2 & lgpar) * chunk * G;
@@ -618,9 +623,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int tt_id = tid - kTcTailWarp0 * 32;  // 0..63
     const int twarp = tt_id >> 5;
     for (int k = 0; k < nitems; ++k) {
-      int n, p;
+      int n, p, base;
       bool state_ok;
-      const int rows = unit_rows(k, n, p, state_ok);
+      const int rows = unit_rows(k, n, p, state_ok, base);
       const int u = j + k * NC;
       const int b = u / a.kv_heads;
       const int g = u - b * a.kv_heads;
@@ -707,9 +712,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
             for (int h = 0; h < G; ++h) acc = fmaf(lg[(size_t)i * G + h], cm[h], acc);
             const float sc = w * acc;
-            if (better(sc, s0 + i, bs, bi)) {
+            if (better(sc, base + i, bs, bi)) {
               bs = sc;
-              bi = s0 + i;
+              bi = base + i;
             }
           }
         }
