@@ -3,8 +3,8 @@
 TEST INFRASTRUCTURE ONLY: imported by tests/, __graft_entry__.smoke() and the
 CPU-baseline / reference leg of bench.py.  The product path never imports it.
 """
-from .longflow_oracle import (OracleSequence, OracleUnit, StepResult, attention,
-                              choose_victim, longflow_scores)
+from .longflow_oracle import (OracleSequence, OracleUnit, Policy, StepResult, attention,
+                              choose_victim, group_step, longflow_scores, value_norm)
 
-__all__ = ["OracleSequence", "OracleUnit", "StepResult", "attention", "choose_victim",
-           "longflow_scores"]
+__all__ = ["OracleSequence", "OracleUnit", "Policy", "StepResult", "attention", "choose_victim",
+           "group_step", "longflow_scores", "value_norm"]

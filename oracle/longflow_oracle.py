@@ -32,17 +32,40 @@ Readings where the pages are silent or ambiguous (each listed in the design doc):
 * The W most recent cached positions (pos >= p - W, p = the new token's
   position) are never evicted; exact score ties go to the lowest slot index.
 * Softmax scale 1/sqrt(d).  The cached ||v||_1 is taken from the stored value.
+
+Policy variants (``Policy``), each a plain reading of a passage:
+
+* ``norm=2``: the score uses ||v_i||_2 -- the guide defines the importance as
+  "the l1-norm or l2-norm" of c_{t,i} ("Mathematical Derivation ...").
+* ``sinks=s``: positions 0..s-1 are never evicted -- the guide's reference step
+  ("End-to-End Implementation") protects its first sink_size slots.
+* ``deferred=True``: the order of the guide's reference step and of its fused
+  kernel's step 4 ("the physical slot index to be overwritten in the next
+  iteration"): the new token is first written into the slot chosen at the
+  previous step (or the next free slot while filling), the query attends over
+  the buffer, and the lowest-score slot outside the window becomes the slot
+  the next token overwrites.  The window then counts the new token: slots with
+  pos >= p + 1 - W are protected (W >= 1 keeps the new token itself).
+* ``scope="layer"``: one victim per (layer, sequence), shared by all KV heads,
+  scored by the sum over every query head -- the guide's reference step sums
+  |c| over heads and feature dimensions.
+* ``score="h2o"``: cumulative attention mass -- the comparison the guide draws
+  with H2O ("cumulative attention statistics", "Cumulative Attention Mass").
+  Each slot keeps the sum of the attention weights its token has received
+  (over the group's query heads) at every decode step since it entered the
+  buffer, its own entry step included; a prompt token starts at zero.  The
+  victim is the lowest such sum among the candidates.
 """
 from __future__ import annotations
 
 import math
 from dataclasses import dataclass
-from typing import Optional
+from typing import List, Optional, Sequence
 
 import numpy as np
 
-__all__ = ["attention", "longflow_scores", "choose_victim", "OracleUnit", "StepResult",
-           "OracleSequence"]
+__all__ = ["attention", "value_norm", "longflow_scores", "choose_victim", "Policy",
+           "OracleUnit", "StepResult", "OracleSequence"]
 
 
 def attention(q: np.ndarray, keys: np.ndarray, values: np.ndarray, scale: float):
@@ -65,6 +88,16 @@ def attention(q: np.ndarray, keys: np.ndarray, values: np.ndarray, scale: float)
     return alpha, out
 
 
+def value_norm(v: np.ndarray, norm: int = 1) -> float:
+    """||v||_1 (default) or ||v||_2 of one stored value vector."""
+    v = np.asarray(v, np.float64)
+    if norm == 1:
+        return float(np.abs(v).sum())
+    if norm == 2:
+        return float(math.sqrt((v * v).sum()))
+    raise ValueError("norm must be 1 or 2")
+
+
 def longflow_scores(alpha_cached: np.ndarray, vnorm1: np.ndarray) -> np.ndarray:
     """LongFlow score of every cached slot of one KV head.
 
@@ -77,40 +110,66 @@ def longflow_scores(alpha_cached: np.ndarray, vnorm1: np.ndarray) -> np.ndarray:
     return np.asarray(alpha_cached, np.float64).sum(axis=0) * np.asarray(vnorm1, np.float64)
 
 
-def choose_victim(scores: np.ndarray, pos: np.ndarray, next_pos: int, window: int):
+def choose_victim(scores: np.ndarray, pos: np.ndarray, next_pos: int, window: int,
+                  sinks: int = 0):
     """Lowest-score slot among the candidates (guide, "Static Memory
     Pre-Allocation and In-Place Eviction", step 2).
 
     Candidates are slots whose position is older than the protected window,
-    pos_i < next_pos - window.  They are sorted by score with a stable sort, so
-    equal scores stay in slot order and an exact tie goes to the lowest slot.
+    pos_i < next_pos - window, and not one of the first `sinks` positions.
+    They are sorted by score with a stable sort, so equal scores stay in slot
+    order and an exact tie goes to the lowest slot.
     Returns (victim slot, lowest score, second-lowest score or inf).
     """
     scores = np.asarray(scores, np.float64)
-    cand = np.flatnonzero(np.asarray(pos) < next_pos - window)
+    pos = np.asarray(pos)
+    cand = np.flatnonzero((pos < next_pos - window) & (pos >= sinks))
     if cand.size == 0:
-        raise ValueError("no eviction candidate: window covers every cached slot")
+        raise ValueError("no eviction candidate: window and sinks cover every cached slot")
     order = cand[np.argsort(scores[cand], kind="stable")]
     best = int(order[0])
     second = float(scores[order[1]]) if order.size > 1 else math.inf
     return best, float(scores[best]), second
 
 
+@dataclass(frozen=True)
+class Policy:
+    """How a cache scores and evicts (the defaults are the method as read here)."""
+    score: str = "longflow"   # "longflow": alpha * ||v||; "h2o": cumulative attention
+    norm: int = 1             # norm of v in the LongFlow score: 1 or 2
+    sinks: int = 0            # positions < sinks are never evicted
+    deferred: bool = False    # pick now, overwrite with the next token
+    scope: str = "kv_head"    # "kv_head": a victim per KV head; "layer": one per sequence
+
+    def validate(self):
+        if self.score not in ("longflow", "h2o"):
+            raise ValueError("score must be 'longflow' or 'h2o'")
+        if self.norm not in (1, 2):
+            raise ValueError("norm must be 1 or 2")
+        if self.sinks < 0:
+            raise ValueError("sinks must be >= 0")
+        if self.scope not in ("kv_head", "layer"):
+            raise ValueError("scope must be 'kv_head' or 'layer'")
+
+
 @dataclass
 class StepResult:
     out: np.ndarray          # [G][d] attention output of the group's query heads
-    evicted: int             # overwritten slot, or -1 (fill phase / eviction off)
+    evicted: int             # slot whose token left the buffer this step, or -1
     written: int             # slot the new token went to, or -1 (read-only full cache)
-    alpha: np.ndarray        # [G][n+1] weights over cached slots then the new token
-    scores: Optional[np.ndarray]  # [n] LongFlow scores when an eviction happened
-    lowest: float            # lowest candidate score (nan when no eviction)
-    second: float            # second-lowest candidate score (nan when no eviction)
+    alpha: np.ndarray        # [G][m] weights (same step: n cached then the new token;
+                             #         deferred: the buffer's n slots, new token included)
+    scores: Optional[np.ndarray]  # [n] the scores a victim was chosen from this step
+    lowest: float            # lowest candidate score (nan when nothing was chosen)
+    second: float            # second-lowest candidate score (nan when nothing was chosen)
+    chosen: int = -1         # victim chosen this step (same step: == evicted;
+                             # deferred: the slot the next token overwrites)
 
     @property
     def rel_gap(self) -> float:
-        """(second - lowest) / second: how far the victim is from a tie."""
-        if not (self.evicted >= 0) or not math.isfinite(self.second) or self.second <= 0:
-            return math.inf if self.evicted >= 0 else math.nan
+        """(second - lowest) / second: how far the chosen victim is from a tie."""
+        if not (self.chosen >= 0) or not math.isfinite(self.second) or self.second <= 0:
+            return math.inf if self.chosen >= 0 else math.nan
         return (self.second - self.lowest) / self.second
 
 
@@ -119,22 +178,32 @@ class OracleUnit:
 
     State (summary, section 2.3 "Static KV Cache"; guide, "Static Memory
     Pre-Allocation and In-Place Eviction"): K/V [capacity][d], the cached
-    ||v||_1 per slot, the token position per slot, the occupied count n and the
-    next token position p.  Nothing is ever moved or compacted.
+    ||v|| per slot, the token position per slot, the occupied count n and the
+    next token position p; with the H2O score, the accumulated attention per
+    slot; when deferred, the slot the next token overwrites.  Nothing is ever
+    moved or compacted.
     """
 
     def __init__(self, capacity: int, head_dim: int, budget: int, window: int,
-                 evict: bool = True):
+                 evict: bool = True, policy: Optional[Policy] = None):
+        policy = policy or Policy()
+        policy.validate()
         if not (0 < budget <= capacity):
             raise ValueError("need 0 < budget <= capacity")
-        if evict and not (0 <= window < budget):
-            raise ValueError("need 0 <= window < budget")
+        if evict:
+            if not (0 <= window and window + policy.sinks < budget):
+                raise ValueError("need 0 <= window and window + sinks < budget")
+            if policy.deferred and window < 1:
+                raise ValueError("deferred eviction needs window >= 1")
         self.capacity, self.d, self.budget, self.window = capacity, head_dim, budget, window
         self.evict = evict
+        self.policy = policy
         self.K = np.zeros((capacity, head_dim))
         self.V = np.zeros((capacity, head_dim))
         self.vnorm = np.zeros(capacity)
         self.pos = np.full(capacity, -1, dtype=np.int64)
+        self.acc = np.zeros(capacity)   # H2O: attention received so far
+        self.pending = -1               # deferred: slot the next token overwrites
         self.n = 0
         self.p = 0
 
@@ -142,20 +211,29 @@ class OracleUnit:
     def scale(self) -> float:
         return 1.0 / math.sqrt(self.d)
 
+    @property
+    def limit(self) -> int:
+        return self.budget if self.evict else self.capacity
+
     def _write(self, slot: int, k, v, position: int):
         # In-place overwrite of one slot (guide, step 3 "Direct In-Place Overwrite").
         self.K[slot] = k
         self.V[slot] = v
-        self.vnorm[slot] = np.abs(np.asarray(v, np.float64)).sum()
+        self.vnorm[slot] = value_norm(v, self.policy.norm)
         self.pos[slot] = position
+        self.acc[slot] = 0.0
 
     def prefill(self, k: np.ndarray, v: np.ndarray):
         """Initial fill: prompt tokens take slots 0..P-1 in order (guide, step 1).
 
-        k, v [P][d] with P <= budget (eviction on) or <= capacity (eviction off).
+        k, v [P][d] with P <= budget (eviction on; < budget when deferred, so
+        that the step that fills the buffer picks the first victim) or
+        <= capacity (eviction off).
         """
         P = len(k)
-        limit = self.budget if self.evict else self.capacity
+        limit = self.limit
+        if self.evict and self.policy.deferred:
+            limit -= 1
         if P > limit:
             raise ValueError("prompt longer than the buffer")
         for i in range(P):
@@ -163,42 +241,120 @@ class OracleUnit:
         self.n = P
         self.p = P
 
+    def slot_scores(self, alpha_slots: np.ndarray, n: int) -> np.ndarray:
+        """This unit's score of each of its n slots (alpha over those slots)."""
+        if self.policy.score == "h2o":
+            return self.acc[:n].copy()
+        return longflow_scores(alpha_slots, self.vnorm[:n])
+
     def step(self, q: np.ndarray, k_new: np.ndarray, v_new: np.ndarray) -> StepResult:
         """One decode step for this unit; q [G][d], k_new/v_new [d]."""
-        n = self.n
-        keys = np.vstack([self.K[:n], np.asarray(k_new, np.float64)[None]])
-        values = np.vstack([self.V[:n], np.asarray(v_new, np.float64)[None]])
-        alpha, out = attention(q, keys, values, self.scale)
-        scores, lowest, second = None, math.nan, math.nan
-        evicted = -1
-        if self.evict and n >= self.budget:
-            scores = longflow_scores(alpha[:, :n], self.vnorm[:n])
-            evicted, lowest, second = choose_victim(scores, self.pos[:n], self.p, self.window)
-            written = evicted
-        elif n < (self.budget if self.evict else self.capacity):
-            written = n            # initial fill: next free slot
-            self.n = n + 1
-        else:
-            written = -1           # eviction off and the buffer is full: read-only
-        if written >= 0:
-            self._write(written, k_new, v_new, self.p)
-        self.p += 1
-        return StepResult(out=out, evicted=evicted, written=written, alpha=alpha,
-                          scores=scores, lowest=lowest, second=second)
+        if self.policy.scope != "kv_head" and self.evict:
+            raise ValueError("a layer-wide victim needs OracleSequence")
+        return group_step([self], [q], [k_new], [v_new])[0]
 
     def snapshot(self):
         return (self.K.copy(), self.V.copy(), self.vnorm.copy(), self.pos.copy(), self.n, self.p)
+
+
+def group_step(units: Sequence[OracleUnit], qs, k_news, v_news) -> List[StepResult]:
+    """One decode step of units that share one eviction decision.
+
+    With the per-KV-head scope the group is one unit; with the layer scope it is
+    every KV head of the sequence, and a slot's score is the sum of the units'
+    scores for it.  Returns one StepResult per unit.
+    """
+    u0 = units[0]
+    pol = u0.policy
+    n, p = u0.n, u0.p
+    for u in units:
+        if (u.n, u.p) != (n, p) or u.pending != u0.pending:
+            raise ValueError("units of one group must share occupancy and positions")
+    if pol.deferred and u0.evict:
+        return _deferred_group_step(units, qs, k_news, v_news)
+
+    # Same-step order: attend over the n cached slots plus the new token, update
+    # the accumulated attention, pick the victim among the cached slots, write.
+    alphas, outs = [], []
+    for u, q, kn, vn in zip(units, qs, k_news, v_news):
+        keys = np.vstack([u.K[:n], np.asarray(kn, np.float64)[None]])
+        values = np.vstack([u.V[:n], np.asarray(vn, np.float64)[None]])
+        alpha, out = attention(q, keys, values, u.scale)
+        if pol.score == "h2o":
+            u.acc[:n] += alpha[:, :n].sum(axis=0)
+        alphas.append(alpha)
+        outs.append(out)
+    scores, lowest, second = None, math.nan, math.nan
+    evicted = -1
+    if u0.evict and n >= u0.budget:
+        scores = sum(u.slot_scores(a[:, :n], n) for u, a in zip(units, alphas))
+        evicted, lowest, second = choose_victim(scores, u0.pos[:n], p, u0.window, pol.sinks)
+        written = evicted
+    elif n < u0.limit:
+        written = n            # initial fill: next free slot
+        for u in units:
+            u.n = n + 1
+    else:
+        written = -1           # eviction off and the buffer is full: read-only
+    results = []
+    for u, kn, vn, a, out in zip(units, k_news, v_news, alphas, outs):
+        if written >= 0:
+            u._write(written, kn, vn, p)
+            if pol.score == "h2o":
+                u.acc[written] = a[:, n].sum()   # the new token's own weight
+        u.p = p + 1
+        results.append(StepResult(out=out, evicted=evicted, written=written, alpha=a,
+                                  scores=scores, lowest=lowest, second=second, chosen=evicted))
+    return results
+
+
+def _deferred_group_step(units, qs, k_news, v_news) -> List[StepResult]:
+    """Deferred order: write the new token into the next free slot or the slot
+    chosen at the previous step, attend over the buffer, and once the buffer is
+    full choose the slot the next token overwrites."""
+    u0 = units[0]
+    pol = u0.policy
+    n, p = u0.n, u0.p
+    if n < u0.budget:
+        written, evicted, n_after = n, -1, n + 1
+    else:
+        if u0.pending < 0:
+            raise ValueError("full buffer without a chosen slot")
+        written, evicted, n_after = u0.pending, u0.pending, n
+    alphas, outs = [], []
+    for u, q, kn, vn in zip(units, qs, k_news, v_news):
+        u._write(written, kn, vn, p)
+        u.n = n_after
+        alpha, out = attention(q, u.K[:n_after], u.V[:n_after], u.scale)
+        if pol.score == "h2o":
+            u.acc[:n_after] += alpha.sum(axis=0)
+        alphas.append(alpha)
+        outs.append(out)
+    scores, lowest, second = None, math.nan, math.nan
+    chosen = -1
+    if n_after >= u0.budget:
+        scores = sum(u.slot_scores(a, n_after) for u, a in zip(units, alphas))
+        chosen, lowest, second = choose_victim(scores, u0.pos[:n_after], p + 1, u0.window,
+                                               pol.sinks)
+    results = []
+    for u, a, out in zip(units, alphas, outs):
+        u.pending = chosen
+        u.p = p + 1
+        results.append(StepResult(out=out, evicted=evicted, written=written, alpha=a,
+                                  scores=scores, lowest=lowest, second=second, chosen=chosen))
+    return results
 
 
 class OracleSequence:
     """All KV heads of one (layer, sequence): q [H_q][d] -> out [H_q][d]."""
 
     def __init__(self, kv_heads: int, q_heads: int, capacity: int, head_dim: int,
-                 budget: int, window: int, evict: bool = True):
+                 budget: int, window: int, evict: bool = True, policy: Optional[Policy] = None):
         if q_heads % kv_heads:
             raise ValueError("q_heads must be a multiple of kv_heads")
         self.G = q_heads // kv_heads
-        self.units = [OracleUnit(capacity, head_dim, budget, window, evict)
+        self.policy = policy or Policy()
+        self.units = [OracleUnit(capacity, head_dim, budget, window, evict, self.policy)
                       for _ in range(kv_heads)]
 
     def prefill(self, k: np.ndarray, v: np.ndarray):
@@ -208,10 +364,10 @@ class OracleSequence:
 
     def step(self, q: np.ndarray, k_new: np.ndarray, v_new: np.ndarray):
         """q [H_q][d], k_new/v_new [H_kv][d] -> (out [H_q][d], [StepResult per KV head])."""
-        results = []
-        outs = []
-        for g, u in enumerate(self.units):
-            r = u.step(q[g * self.G:(g + 1) * self.G], k_new[g], v_new[g])
-            results.append(r)
-            outs.append(r.out)
-        return np.vstack(outs), results
+        qs = [q[g * self.G:(g + 1) * self.G] for g in range(len(self.units))]
+        if self.policy.scope == "layer":
+            results = group_step(self.units, qs, k_new, v_new)
+        else:
+            results = [group_step([u], [qs[g]], [k_new[g]], [v_new[g]])[0]
+                       for g, u in enumerate(self.units)]
+        return np.vstack([r.out for r in results]), results

@@ -318,6 +318,208 @@ def check_eviction_off_full_cache(orc):
     assert after[5] == before[5] + 1
 
 
+# ---------------------------------------------------------------------------
+# Policy variants (guide, "Mathematical Derivation ..." -- the l1 or l2 norm;
+# "End-to-End Implementation" -- sinks, a layer-wide score, the victim written
+# at the next step; "The Long-Output Reasoning Crisis" and the comparison table
+# -- H2O's cumulative attention)
+# ---------------------------------------------------------------------------
+
+def _policy_run(orc, policy, rng, G, d, B, W, steps, prompt, hkv=1):
+    """Drive an OracleSequence; yield (state before, q, k_new, v_new, results) per step."""
+    seq = orc.OracleSequence(hkv, hkv * G, B, d, B, W, True, policy)
+    seq.prefill(rng.standard_normal((hkv, prompt, d)),
+                rng.standard_normal((hkv, prompt, d)) * np.exp(0.5 * rng.standard_normal((hkv, prompt, 1))))
+    for _ in range(steps):
+        q = rng.standard_normal((hkv * G, d))
+        kn = rng.standard_normal((hkv, d))
+        vn = rng.standard_normal((hkv, d)) * np.exp(0.5 * rng.standard_normal((hkv, 1)))
+        before = [(u.K[:u.n].copy(), u.V[:u.n].copy(), u.pos[:u.n].copy(), u.n, u.p)
+                  for u in seq.units]
+        _, res = seq.step(q, kn, vn)
+        yield seq, before, q, kn, vn, res
+
+
+def check_l2_norm_and_sinks_against_library(orc):
+    """norm = 2 and s sinks: every victim is the lowest sum_h alpha_{h,i} ||v_i||_2
+    (weights from SDPA, norm from numpy) among slots with s <= pos < p - W; the
+    first s positions are never evicted."""
+    rng = np.random.default_rng(RNG_SEED + 12)
+    for G, d, B, W, s in [(1, 8, 12, 2, 3), (2, 16, 16, 4, 4)]:
+        pol = orc.Policy(norm=2, sinks=s)
+        evictions = 0
+        for seq, before, q, kn, vn, res in _policy_run(orc, pol, rng, G, d, B, W, 50, B - 3):
+            K0, V0, pos0, n0, p0 = before[0]
+            r = res[0]
+            if n0 < B:
+                continue
+            keys = np.vstack([K0, kn[0][None]])
+            alpha = sdpa_weights(q, np.broadcast_to(keys, (G,) + keys.shape))
+            score = alpha[:, :n0].sum(axis=0) * np.linalg.norm(V0, axis=1)
+            cand = np.nonzero((pos0 < p0 - W) & (pos0 >= s))[0]
+            assert r.evicted == cand[np.argmin(score[cand])], (r.evicted, cand)
+            assert np.allclose(r.scores, score, rtol=1e-10, atol=1e-300)
+            assert pos0[r.evicted] >= s
+            evictions += 1
+        assert evictions > 20
+        assert sorted(seq.units[0].pos[seq.units[0].pos < s].tolist()) == list(range(s))
+
+
+def check_deferred_equals_same_step_one_slot_larger(orc):
+    """Choosing the victim at step t and overwriting it at t + 1 with a buffer of
+    B + 1 and a window of W + 1 (the new token counts) attends over exactly the
+    tokens that same-step eviction with B slots and window W attends over, and
+    drops the same tokens: outputs agree to rounding and victims by position.
+    Holds for every score, norm, sink count and scope."""
+    rng = np.random.default_rng(RNG_SEED + 13)
+    for score, norm, sinks, scope, hkv in [("longflow", 1, 0, "kv_head", 1),
+                                           ("longflow", 2, 2, "kv_head", 2),
+                                           ("h2o", 1, 1, "kv_head", 1),
+                                           ("longflow", 1, 1, "layer", 2),
+                                           ("h2o", 1, 0, "layer", 3)]:
+        G, d, B, W, P = 2, 8, 10, 2, 6
+        same = orc.OracleSequence(hkv, hkv * G, B, d, B, W, True,
+                                  orc.Policy(score=score, norm=norm, sinks=sinks, scope=scope))
+        defer = orc.OracleSequence(hkv, hkv * G, B + 1, d, B + 1, W + 1, True,
+                                   orc.Policy(score=score, norm=norm, sinks=sinks, scope=scope,
+                                              deferred=True))
+        k = rng.standard_normal((hkv, P, d))
+        v = rng.standard_normal((hkv, P, d))
+        same.prefill(k, v)
+        defer.prefill(k, v)
+        dropped = 0
+        for t in range(40):
+            q = rng.standard_normal((hkv * G, d))
+            kn = rng.standard_normal((hkv, d))
+            vn = rng.standard_normal((hkv, d))
+            o1, r1 = same.step(q, kn, vn)
+            o2, r2 = defer.step(q, kn, vn)
+            assert np.allclose(o1, o2, rtol=1e-12, atol=1e-13), (score, t, np.abs(o1 - o2).max())
+            for g in range(hkv):
+                assert (r1[g].evicted >= 0) == (r2[g].chosen >= 0), (score, t)
+            # the token same-step eviction dropped is the one deferred eviction marked
+            for g in range(hkv):
+                if r2[g].chosen >= 0:
+                    marked = defer.units[g].pos[r2[g].chosen]
+                    live = set(same.units[g].pos[:same.units[g].n].tolist())
+                    live_d = set(defer.units[g].pos[:defer.units[g].n].tolist()) - {marked}
+                    assert live == live_d, (score, t)
+                    dropped += 1
+        assert dropped > 20
+
+
+def check_deferred_order(orc):
+    """Deferred: the slot chosen at step t is the slot written at step t + 1
+    (guide, fused kernel step 4), the new token is attended from the buffer
+    (weights sum to one over n slots), never chosen in its own step, and the
+    first victim is chosen by the step that fills the buffer."""
+    rng = np.random.default_rng(RNG_SEED + 14)
+    G, d, B, W = 2, 8, 9, 1
+    pol = orc.Policy(deferred=True, sinks=2)
+    prev_chosen = None
+    for seq, before, q, kn, vn, res in _policy_run(orc, pol, rng, G, d, B, W, 30, 5):
+        r = res[0]
+        u = seq.units[0]
+        n0 = before[0][3]
+        assert np.allclose(r.alpha.sum(axis=1), 1.0, atol=1e-12)
+        assert r.alpha.shape[1] == u.n
+        if n0 < B:
+            assert r.written == n0 and r.evicted == -1
+        else:
+            assert r.written == prev_chosen and r.evicted == prev_chosen
+        if u.n == B:
+            assert r.chosen >= 0 and r.chosen != r.written
+            assert u.pos[r.chosen] >= 2
+        else:
+            assert r.chosen == -1
+        prev_chosen = r.chosen
+
+
+def check_layer_scope(orc):
+    """One victim per sequence: (a) it is the lowest sum over every query head of
+    alpha_{h,i} ||v_{kv(h),i}||_1 (weights from SDPA); (b) all KV heads keep the
+    same positions; (c) with identical KV heads it equals the per-head victim."""
+    rng = np.random.default_rng(RNG_SEED + 15)
+    G, d, B, W, hkv = 2, 8, 12, 2, 3
+    evictions = 0
+    for seq, before, q, kn, vn, res in _policy_run(orc, orc.Policy(scope="layer"), rng, G, d, B,
+                                                   W, 40, 8, hkv=hkv):
+        n0, p0 = before[0][3], before[0][4]
+        if n0 < B:
+            continue
+        score = np.zeros(n0)
+        for g in range(hkv):
+            K0, V0 = before[g][0], before[g][1]
+            keys = np.vstack([K0, kn[g][None]])
+            alpha = sdpa_weights(q[g * G:(g + 1) * G], np.broadcast_to(keys, (G,) + keys.shape))
+            score += alpha[:, :n0].sum(axis=0) * np.abs(V0).sum(axis=1)
+        cand = np.nonzero(before[0][2] < p0 - W)[0]
+        expect = cand[np.argmin(score[cand])]
+        assert all(r.evicted == expect for r in res), ([r.evicted for r in res], expect)
+        for u in seq.units[1:]:
+            assert np.array_equal(u.pos, seq.units[0].pos)
+        evictions += 1
+    assert evictions > 20
+    # (c) identical heads: the summed score is hkv times each head's
+    same = orc.OracleSequence(hkv, hkv * G, B, d, B, W, True, orc.Policy(scope="layer"))
+    per = orc.OracleSequence(1, G, B, d, B, W, True)
+    k = rng.standard_normal((1, B, d))
+    v = rng.standard_normal((1, B, d))
+    same.prefill(np.repeat(k, hkv, 0), np.repeat(v, hkv, 0))
+    per.prefill(k, v)
+    for _ in range(15):
+        q = rng.standard_normal((G, d))
+        kn = rng.standard_normal((1, d))
+        vn = rng.standard_normal((1, d))
+        _, r_all = same.step(np.tile(q, (hkv, 1)), np.repeat(kn, hkv, 0), np.repeat(vn, hkv, 0))
+        _, r_one = per.step(q, kn, vn)
+        assert r_all[0].evicted == r_one[0].evicted
+
+
+def check_h2o_accumulates_library_weights(orc):
+    """H2O: each slot's accumulator is the sum of the SDPA weights (over the
+    group's heads) its token received at every step since it entered, its own
+    entry step included, prompt tokens from zero; the victim is the lowest
+    accumulator among the candidates."""
+    rng = np.random.default_rng(RNG_SEED + 16)
+    G, d, B, W = 2, 8, 10, 2
+    mass = {}   # token position -> accumulated weight
+    evictions = 0
+    for seq, before, q, kn, vn, res in _policy_run(orc, orc.Policy(score="h2o"), rng, G, d, B,
+                                                   W, 60, 7):
+        K0, V0, pos0, n0, p0 = before[0]
+        r = res[0]
+        keys = np.vstack([K0, kn[0][None]])
+        alpha = sdpa_weights(q, np.broadcast_to(keys, (G,) + keys.shape)).sum(axis=0)
+        for i in range(n0):
+            mass[int(pos0[i])] = mass.get(int(pos0[i]), 0.0) + alpha[i]
+        mass[p0] = alpha[n0]
+        if n0 >= B:
+            cand = np.nonzero(pos0 < p0 - W)[0]
+            acc = np.array([mass[int(x)] for x in pos0])
+            assert r.evicted == cand[np.argmin(acc[cand])], (r.evicted, cand)
+            evictions += 1
+        u = seq.units[0]
+        expect = np.array([mass[int(x)] for x in u.pos[:u.n]])
+        assert np.allclose(u.acc[:u.n], expect, rtol=1e-12, atol=1e-15)
+    assert evictions > 40
+
+
+def check_h2o_zero_query_closed_form(orc):
+    """H2O with q = 0 on a full prompt: weights are uniform, so a token's mass
+    is proportional to the steps it has been cached.  Prompt tokens tie until a
+    decode token leaves the window; from then on the victim is the decode token
+    cached W + 1 steps earlier.  Exact ties go to the lowest slot, so the victim
+    of eviction step t is slot t mod (W + 1)."""
+    rng = np.random.default_rng(RNG_SEED + 17)
+    for B, W, G in [(9, 2, 1), (12, 3, 2)]:
+        u = orc.OracleUnit(B, 4, B, W, True, orc.Policy(score="h2o"))
+        u.prefill(rng.standard_normal((B, 4)), rng.standard_normal((B, 4)))
+        for t in range(30):
+            r = u.step(np.zeros((G, 4)), rng.standard_normal(4), rng.standard_normal(4))
+            assert r.evicted == t % (W + 1), (B, W, t, r.evicted)
+
+
 ALL_CHECKS = [
     check_weights_sum_to_one,
     check_gqa_output_matches_library,
@@ -331,4 +533,10 @@ ALL_CHECKS = [
     check_cap_and_window_invariants,
     check_fill_then_evict_slots,
     check_eviction_off_full_cache,
+    check_l2_norm_and_sinks_against_library,
+    check_deferred_equals_same_step_one_slot_larger,
+    check_deferred_order,
+    check_layer_scope,
+    check_h2o_accumulates_library_weights,
+    check_h2o_zero_query_closed_form,
 ]

@@ -18,8 +18,8 @@ ORACLE_SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file
 
 MUTANTS = {
     "new_token_not_attended": (
-        "keys = np.vstack([self.K[:n], np.asarray(k_new, np.float64)[None]])",
-        "keys = np.vstack([self.K[:n], 0.0 * np.asarray(k_new, np.float64)[None]])"),
+        "keys = np.vstack([u.K[:n], np.asarray(kn, np.float64)[None]])",
+        "keys = np.vstack([u.K[:n], 0.0 * np.asarray(kn, np.float64)[None]])"),
     "scale_1_over_d": ("return 1.0 / math.sqrt(self.d)", "return 1.0 / self.d"),
     "logit_sign": ("logits = (q @ keys.T) * scale", "logits = -(q @ keys.T) * scale"),
     "softmax_wrong_axis": ("alpha = w / w.sum(axis=1, keepdims=True)",
@@ -31,20 +31,38 @@ MUTANTS = {
     "score_max_over_heads": (
         "return np.asarray(alpha_cached, np.float64).sum(axis=0) *",
         "return np.asarray(alpha_cached, np.float64).max(axis=0) *"),
-    "score_index_shift": ("longflow_scores(alpha[:, :n], self.vnorm[:n])",
-                          "longflow_scores(alpha[:, 1:], self.vnorm[:n])"),
+    "score_index_shift": ("u.slot_scores(a[:, :n], n)", "u.slot_scores(a[:, 1:], n)"),
     "argmax_not_argmin": ('np.argsort(scores[cand], kind="stable")',
                           'np.argsort(-scores[cand], kind="stable")'),
-    "ties_to_highest": ("cand = np.flatnonzero(np.asarray(pos) < next_pos - window)",
-                        "cand = np.flatnonzero(np.asarray(pos) < next_pos - window)[::-1]"),
-    "window_off_by_one": ("np.asarray(pos) < next_pos - window", "np.asarray(pos) <= next_pos - window"),
-    "vnorm_l2": ("self.vnorm[slot] = np.abs(np.asarray(v, np.float64)).sum()",
-                 "self.vnorm[slot] = np.sqrt((np.asarray(v, np.float64) ** 2).sum())"),
+    "ties_to_highest": ("cand = np.flatnonzero((pos < next_pos - window) & (pos >= sinks))",
+                        "cand = np.flatnonzero((pos < next_pos - window) & (pos >= sinks))[::-1]"),
+    "window_off_by_one": ("(pos < next_pos - window)", "(pos <= next_pos - window)"),
+    "vnorm_l2": ("self.vnorm[slot] = value_norm(v, self.policy.norm)",
+                 "self.vnorm[slot] = value_norm(v, 2)"),
     "fill_wrong_slot": ("written = n            # initial fill: next free slot",
-                        "written = (n + 1) % self.capacity"),
-    "position_off_by_one": ("self._write(written, k_new, v_new, self.p)",
-                            "self._write(written, k_new, v_new, self.p + 1)"),
-    "no_write_on_evict": ("            written = evicted\n", "            written = -1\n"),
+                        "written = (n + 1) % u0.capacity"),
+    "position_off_by_one": ("u._write(written, kn, vn, p)", "u._write(written, kn, vn, p + 1)"),
+    "no_write_on_evict": ("        written = evicted\n", "        written = -1\n"),
+    # policy variants
+    "sinks_ignored": ("& (pos >= sinks)", "& (pos >= 0)"),
+    "sinks_off_by_one": ("& (pos >= sinks)", "& (pos > sinks)"),
+    "l2_without_sqrt": ("return float(math.sqrt((v * v).sum()))", "return float((v * v).sum())"),
+    "l2_is_l1": ("if norm == 1:", "if norm in (1, 2):"),
+    "deferred_window_excludes_new": ("p + 1, u0.window,", "p, u0.window,"),
+    "deferred_attends_before_write": (
+        "        u._write(written, kn, vn, p)\n        u.n = n_after\n",
+        "        u.n = n_after\n"),
+    "deferred_choice_not_carried": ("        u.pending = chosen\n", "        u.pending = -1 if chosen < 0 else 0\n"),
+    "layer_scope_first_head_only": (
+        "scores = sum(u.slot_scores(a[:, :n], n) for u, a in zip(units, alphas))",
+        "scores = units[0].slot_scores(alphas[0][:, :n], n)"),
+    "layer_scope_is_per_head": ('if self.policy.scope == "layer":', "if False:"),
+    "h2o_no_self_weight": ("u.acc[written] = a[:, n].sum()   # the new token's own weight",
+                           "u.acc[written] = 0.0"),
+    "h2o_not_accumulated": ("u.acc[:n] += alpha[:, :n].sum(axis=0)",
+                            "u.acc[:n] = alpha[:, :n].sum(axis=0)"),
+    "h2o_scores_are_longflow": ('if self.policy.score == "h2o":\n            return',
+                                'if False:\n            return'),
 }
 
 
@@ -72,7 +90,7 @@ def test_pins_catch_mutant(name):
         for check in oracle_pins.ALL_CHECKS:
             try:
                 check(mod)
-            except (AssertionError, ValueError, IndexError) as e:
+            except (AssertionError, ValueError, IndexError, KeyError):
                 caught.append(check.__name__)
     finally:
         sys.modules.pop(mod.__name__, None)
