@@ -38,10 +38,12 @@ NOMINAL_HBM_GBS = 8000.0
 # byte model (algorithmic bytes of one (layer, sequence) unit)
 # ---------------------------------------------------------------------------
 
-def unit_bytes(wl, n_slots: int, evict: bool = True, writes_slot: bool = True) -> int:
+def unit_bytes(wl, n_slots: int, evict: bool = True, writes_slot: bool = True,
+               h2o: bool = False) -> int:
     """K and V of the n occupied slots, their ||v||_1 and positions, q read,
     out written, k_new / v_new read, and (when a slot is written) the new
-    token's K, V, ||v||_1, position plus the evicted index."""
+    token's K, V, ||v||_1, position plus the evicted index.  The H2O score
+    reads each slot's accumulator instead of its ||v|| and writes it back."""
     e = wl.elem_bytes
     hkv, hq, d = wl.kv_heads, wl.q_heads, wl.head_dim
     b = 2 * hkv * n_slots * d * e + 8 * hkv * n_slots
@@ -49,7 +51,20 @@ def unit_bytes(wl, n_slots: int, evict: bool = True, writes_slot: bool = True) -
     b += 4 * hkv  # evicted slot index
     if writes_slot:
         b += 2 * hkv * d * e + 8 * hkv
+    if h2o:
+        b += 4 * hkv * n_slots + (4 * hkv if writes_slot else 0)
     return b
+
+
+# Policy variants timed beside the default method (name -> LFCache keywords).
+POLICY_VARIANTS = {
+    "l2_sinks4": dict(norm=2, sinks=4),
+    "deferred": dict(deferred=True),
+    "layer_scope": dict(scope="layer"),
+    "h2o": dict(score="h2o"),
+    # the guide listing's choices together (window 1: only the new token protected)
+    "listing": dict(sinks=4, deferred=True, scope="layer"),
+}
 
 
 KERNEL_SOURCES = ["lf_decode_tc.cuh", "lf_decode.cuh", "lf_device.cuh"]
@@ -261,18 +276,22 @@ def bench_reference(args):
 # ---------------------------------------------------------------------------
 
 def build_cache(wl, torch, lf, stream_mod, seed, evict=True, capacity=None, layers=None,
-                cluster=0, stages=0):
+                cluster=0, stages=0, policy=None):
     L = wl.layers if layers is None else layers
     cap = capacity or wl.budget
+    policy = policy or {}
     gen = stream_mod.InputStream(wl, seed=seed, device="cuda", layers=list(range(L)))
     budgets = gen.budgets if (evict and wl.ragged) else None
     cache = lf.LFCache(L, wl.batch, wl.kv_heads, wl.q_heads, wl.head_dim, cap, wl.window,
                        dtype=wl.dtype, evict=evict, budgets=budgets, cluster=cluster,
-                       stages=stages)
+                       stages=stages, **policy)
+    # deferred eviction keeps one slot free in the prompt (the step that fills
+    # the buffer chooses the first victim)
+    spare = 1 if (evict and policy.get("deferred")) else 0
     for l in range(L):
         k, v, lens = gen.prompt(l)
         # prompt tokens past a sequence's budget would arrive as decode steps
-        lens = [min(P, budgets[b] if budgets else cap) for b, P in enumerate(lens)]
+        lens = [min(P, (budgets[b] if budgets else cap) - spare) for b, P in enumerate(lens)]
         cache.prefill(l, k, v, lens)
         del k, v
     torch.cuda.synchronize()
@@ -454,6 +473,37 @@ def bench_ours(args):
         else:
             full = {"skipped": f"needs {need / 1e9:.1f} GB, {free / 1e9:.1f} GB free"}
 
+    # ---- policy variants on the same workload (fewer layers) ----
+    policies = None
+    if args.policies and wl.prefill >= wl.budget and not wl.ragged:
+        policies = {}
+        pl = min(L, args.policy_layers)
+        psteps = max(8, args.steps // 4)
+        for name, kw in POLICY_VARIANTS.items():
+            wl_p = wl.scaled(layers=pl, window=1) if name == "listing" else wl.scaled(layers=pl)
+            cp, gp = build_cache(wl_p, torch, lf, stream_mod, seed=rank + 200, layers=pl,
+                                 cluster=args.cluster, stages=args.stages, policy=kw)
+            warm = pregenerate(gp, args.warmup, torch)
+            time_steps(cp, warm, outs[:pl], evs[:pl], torch, graph=False)
+            del warm
+            tin = pregenerate(gp, psteps, torch)
+            barrier()
+            pms = max_over_ranks(time_steps(cp, tin, outs[:pl], evs[:pl], torch,
+                                            graph=not args.eager))
+            if cp.check() != 0:
+                raise RuntimeError(f"device error in the {name} variant")
+            pb = unit_bytes(wl_p, wl_p.budget, h2o=(kw.get("score") == "h2o")) * wl.batch
+            per_launch = pms / 1000.0 / (pl * psteps)
+            policies[name] = {
+                "policy": kw, "value": world * wl.batch * pl * psteps / (pms / 1000.0),
+                "unit": UNIT, "layers": pl, "steps": psteps,
+                "launches_per_layer_step": 2 if kw.get("scope") == "layer" else 1,
+                "bytes_per_layer_step": pb, "achieved_gbs": pb / per_launch / 1e9,
+                "frac_of_peak": pb / per_launch / 1e9 / peak}
+            cp.close()
+            del cp, gp, tin
+            torch.cuda.empty_cache()
+
     if rank != 0:
         return 0
     cpu = None
@@ -487,6 +537,7 @@ def bench_ours(args):
         "gpu_launches": launches,
         "clocks": clk,
         "full_kv": full,
+        "policy_variants": policies,
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -508,6 +559,9 @@ def main():
     ap.add_argument("--no-full-kv", dest="full_kv", action="store_false")
     ap.add_argument("--full-kv-layers", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-policies", dest="policies", action="store_false", default=True,
+                    help="skip timing the policy variants")
+    ap.add_argument("--policy-layers", type=int, default=8)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args()
     if args.warmup < 3:

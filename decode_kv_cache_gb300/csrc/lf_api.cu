@@ -20,6 +20,8 @@
 struct lf_cache {
   int layers, batch, kv_heads, q_heads, head_dim, capacity, slot_stride, window;
   int dtype, evict, cluster, stages, chunk, smem, device;
+  int score, norm, sinks, deferred, scope;  // the policy (zero when eviction is off, but norm)
+  int items;      // tensor-core path: units one cluster may visit per launch
   size_t elem_bytes;
   void* K;
   void* V;
@@ -30,7 +32,12 @@ struct lf_cache {
   int32_t* budget;
   int32_t* err;
   int32_t* plen;  // [layers][batch] prompt lengths uploaded by lf_prefill_fill
-  void* small;    // one allocation holding vnorm..plen
+  float* acc;     // H2O: attention mass per slot, else null
+  int32_t* pending;   // deferred: chosen slot per unit, else null
+  float* lw_score;    // layer scope: one layer's per-slot scores, else null
+  int32_t* lw_req;    // layer scope: [batch][kv_heads] requests, else null
+  float* lw_anew;     // layer scope: [batch][kv_heads] new tokens' attention mass
+  void* small;    // one allocation holding vnorm..lw_anew
   lf::KernelEntry kern;
   int threads;    // CTA size of the decode kernel
   int grid_y;     // tensor-core path: resident clusters (persistent grid)
@@ -139,8 +146,9 @@ lf_cache* lf_cache_create(int layers, int batch, int kv_heads, int q_heads, int 
 lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, int head_dim,
                              int capacity, int window, const lf_config* cfg) {
   g_last_error.clear();
-  lf_config def = {LF_BF16, 1, nullptr, 0, 0, LF_KERNEL_AUTO};
-  const lf_config c = cfg ? *cfg : def;
+  lf_config def = {LF_BF16, 1, nullptr, 0, 0, LF_KERNEL_AUTO, LF_SCORE_LONGFLOW, 1, 0, 0,
+                   LF_SCOPE_KV_HEAD};
+  lf_config c = cfg ? *cfg : def;
   if (layers < 1 || batch < 1 || kv_heads < 1 || q_heads < 1 || capacity < 1 || window < 0) {
     fail(LF_ERR_ARG, "layers, batch, heads and capacity must be >= 1 and window >= 0");
     return nullptr;
@@ -174,6 +182,19 @@ lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, i
     fail(LF_ERR_ARG, "kernel must be LF_KERNEL_AUTO, LF_KERNEL_SIMT or LF_KERNEL_TENSOR_CORE");
     return nullptr;
   }
+  if (c.norm == 0) c.norm = 1;
+  if ((c.score != LF_SCORE_LONGFLOW && c.score != LF_SCORE_H2O) || (c.norm != 1 && c.norm != 2) ||
+      c.sinks < 0 || (c.deferred != 0 && c.deferred != 1) ||
+      (c.scope != LF_SCOPE_KV_HEAD && c.scope != LF_SCOPE_LAYER)) {
+    fail(LF_ERR_ARG, "policy: score must be LF_SCORE_LONGFLOW or LF_SCORE_H2O, norm 1 or 2, "
+         "sinks >= 0, deferred 0 or 1, scope LF_SCOPE_KV_HEAD or LF_SCOPE_LAYER");
+    return nullptr;
+  }
+  if (!c.evict) {  // nothing is ever evicted: the policy has nothing to decide
+    c.score = LF_SCORE_LONGFLOW;
+    c.sinks = c.deferred = 0;
+    c.scope = LF_SCOPE_KV_HEAD;
+  }
   const int group = q_heads / kv_heads;
   lf::KernelEntry kern;
   bool found = false;
@@ -203,8 +224,13 @@ lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, i
       min_budget = std::min(min_budget, (int)c.budgets[b]);
     }
   }
-  if (c.evict && window >= min_budget) {
-    fail(LF_ERR_ARG, "window (%d) must be smaller than every budget (min %d)", window, min_budget);
+  if (c.evict && window + c.sinks >= min_budget) {
+    fail(LF_ERR_ARG, "window + sinks (%d + %d) must be smaller than every budget (min %d)", window,
+         c.sinks, min_budget);
+    return nullptr;
+  }
+  if (c.evict && c.deferred && window < 1) {
+    fail(LF_ERR_ARG, "deferred eviction needs window >= 1 (the new token is protected)");
     return nullptr;
   }
   if (capacity > INT_MAX / 2) {
@@ -252,22 +278,34 @@ lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, i
              (capacity + 2 * cluster - 1) / (2 * cluster) >= 128)
         cluster *= 2;
   }
-  int chunk = 0, smem = 0, grid_y = 0;
+  int chunk = 0, smem = 0, grid_y = 0, items = 0;
   for (;;) {
     chunk = (int)round_up((size_t)((capacity + cluster - 1) / cluster), 4);
-    smem = kern.smem_bytes(stages, chunk, cluster, c.evict);
-    // The tensor-core kernel takes all of an SM's tensor memory: ask for more
-    // than half of its shared memory so that never two CTAs share an SM.
-    if (tc) smem = std::max(smem, max_sm_smem / 2 + 1024);
     int fits = 0;
-    if (smem <= max_optin) {
-      if (tc) {
-        fits = active_clusters(kern.decode, cluster, 1, 1, smem, threads);
+    if (tc) {
+      // The persistent grid visits ceil(units / resident clusters) units per
+      // cluster; its item table is sized for that.  Start from the most
+      // clusters the SMs could hold and grow the table if fewer are resident.
+      const int most = std::max(1, num_sms / cluster);
+      items = (units + most - 1) / most;
+      for (int pass = 0; pass < 4; ++pass) {
+        smem = kern.smem_bytes(stages, chunk, cluster, c.evict, items);
+        // The tensor-core kernel takes all of an SM's tensor memory: ask for more
+        // than half of its shared memory so that never two CTAs share an SM.
+        smem = std::max(smem, max_sm_smem / 2 + 1024);
+        fits = (smem <= max_optin) ? active_clusters(kern.decode, cluster, 1, 1, smem, threads) : 0;
+        if (fits <= 0) break;
         grid_y = std::min(fits, units);
-        if (fits > 0 && (units + grid_y - 1) / grid_y > lf::kTcMaxItems) fits = 0;
-      } else {
-        fits = active_clusters(kern.decode, cluster, kv_heads, batch, smem, threads);
+        const int need = (units + grid_y - 1) / grid_y;
+        if (need <= items) break;
+        items = need;
+        fits = 0;
       }
+      if (fits > 0 && items > lf::kTcMaxItems) fits = 0;
+    } else {
+      smem = kern.smem_bytes(stages, chunk, cluster, c.evict, 0);
+      if (smem <= max_optin)
+        fits = active_clusters(kern.decode, cluster, kv_heads, batch, smem, threads);
     }
     if (fits > 0) break;
     if (c.cluster != 0 || cluster >= lf::kMaxCluster) {
@@ -302,6 +340,12 @@ lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, i
   cache->kern = kern;
   cache->threads = threads;
   cache->grid_y = grid_y;
+  cache->items = items;
+  cache->score = c.score;
+  cache->norm = c.norm;
+  cache->sinks = c.sinks;
+  cache->deferred = c.deferred;
+  cache->scope = c.scope;
 
   const size_t n_units = (size_t)layers * batch * kv_heads;
   const size_t n_slots = n_units * cache->slot_stride;
@@ -315,7 +359,16 @@ lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, i
   size_t off_budget = round_up(off_next + n_units * 4, 256);
   size_t off_err = round_up(off_budget + (size_t)batch * 4, 256);
   size_t off_plen = round_up(off_err + 4, 256);
-  size_t small_bytes = round_up(off_plen + (size_t)layers * batch * 4, 256);
+  // policy state: acc [n_slots] (H2O); pending [n_units] (deferred); one layer's
+  // lw_score [slots], lw_req and lw_anew [units] (layer scope)
+  const size_t lunits = (size_t)batch * kv_heads;
+  const bool h2o = c.score == LF_SCORE_H2O, layer = c.scope == LF_SCOPE_LAYER;
+  size_t off_acc = round_up(off_plen + (size_t)layers * batch * 4, 256);
+  size_t off_pend = round_up(off_acc + (h2o ? n_slots * 4 : 0), 256);
+  size_t off_lws = round_up(off_pend + (c.deferred ? n_units * 4 : 0), 256);
+  size_t off_lwr = round_up(off_lws + (layer ? lunits * cache->slot_stride * 4 : 0), 256);
+  size_t off_lwa = round_up(off_lwr + (layer ? lunits * 4 : 0), 256);
+  size_t small_bytes = round_up(off_lwa + (layer ? lunits * 4 : 0), 256);
 
   if ((e = cudaMalloc(&cache->K, kv_bytes)) != cudaSuccess ||
       (e = cudaMalloc(&cache->V, kv_bytes)) != cudaSuccess ||
@@ -333,6 +386,11 @@ lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, i
   cache->budget = reinterpret_cast<int32_t*>(s + off_budget);
   cache->err = reinterpret_cast<int32_t*>(s + off_err);
   cache->plen = reinterpret_cast<int32_t*>(s + off_plen);
+  cache->acc = h2o ? reinterpret_cast<float*>(s + off_acc) : nullptr;
+  cache->pending = c.deferred ? reinterpret_cast<int32_t*>(s + off_pend) : nullptr;
+  cache->lw_score = layer ? reinterpret_cast<float*>(s + off_lws) : nullptr;
+  cache->lw_req = layer ? reinterpret_cast<int32_t*>(s + off_lwr) : nullptr;
+  cache->lw_anew = layer ? reinterpret_cast<float*>(s + off_lwa) : nullptr;
 
   // Empty state: no occupied slot, positions -1, ||v||_1 0, K/V zero.
   int32_t* hb = new (std::nothrow) int32_t[batch];
@@ -345,6 +403,7 @@ lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, i
   for (int b = 0; b < batch; ++b) hb[b] = c.budgets ? c.budgets[b] : capacity;
   if ((e = cudaMemset(cache->small, 0, small_bytes)) != cudaSuccess ||
       (e = cudaMemset(cache->pos, 0xff, n_slots * 4)) != cudaSuccess ||
+      (cache->pending && (e = cudaMemset(cache->pending, 0xff, n_units * 4)) != cudaSuccess) ||
       (e = cudaMemset(cache->K, 0, kv_bytes)) != cudaSuccess ||
       (e = cudaMemset(cache->V, 0, kv_bytes)) != cudaSuccess ||
       (e = cudaMemcpy(cache->budget, hb, (size_t)batch * 4, cudaMemcpyHostToDevice)) !=
@@ -401,11 +460,13 @@ int lf_prefill_fill(lf_cache* cache, int layer, const void* k, const void* v,
     return cuda_fail(e, "reading budgets");
   }
   for (int b = 0; b < cache->batch; ++b) {
-    const int limit = cache->evict ? hb[b] : cache->capacity;
+    // deferred: the step that fills the buffer chooses the first victim
+    const int limit = cache->evict ? hb[b] - (cache->deferred ? 1 : 0) : cache->capacity;
     if (prompt_len[b] > limit) {
       delete[] hb;
-      return fail(LF_ERR_ARG, "prompt_len[%d] = %d exceeds the buffer (%d); feed the rest "
-                  "through lf_decode_step", b, prompt_len[b], limit);
+      return fail(LF_ERR_ARG, "prompt_len[%d] = %d exceeds the buffer (%d%s); feed the rest "
+                  "through lf_decode_step", b, prompt_len[b], limit,
+                  cache->deferred ? ": budget - 1 in deferred mode" : "");
     }
   }
   delete[] hb;
@@ -429,9 +490,12 @@ int lf_prefill_fill(lf_cache* cache, int layer, const void* k, const void* v,
   a.pos = cache->pos + layer * layer_slots;
   a.count = cache->count + layer * layer_units;
   a.next_pos = cache->next_pos + layer * layer_units;
+  a.acc = cache->acc ? cache->acc + layer * layer_slots : nullptr;
+  a.pending = cache->pending ? cache->pending + layer * layer_units : nullptr;
   a.kv_heads = cache->kv_heads;
   a.max_prompt = max_prompt;
   a.slot_stride = cache->slot_stride;
+  a.norm = cache->norm;
   void* args[] = {&a};
   e = cudaLaunchKernel(cache->kern.prefill, dim3(cache->kv_heads, cache->batch, 1),
                        dim3(lf::kThreads, 1, 1), args, 0, st);
@@ -463,6 +527,16 @@ int lf_decode_step(lf_cache* cache, int layer, const void* q, const void* k_new,
   a.next_pos = cache->next_pos + layer * layer_units;
   a.budget = cache->budget;
   a.err = cache->err;
+  a.acc = cache->acc ? cache->acc + layer * layer_slots : nullptr;
+  a.pending = cache->pending ? cache->pending + layer * layer_units : nullptr;
+  a.lw_score = cache->lw_score;  // one layer's scratch, reused by every layer
+  a.lw_req = cache->lw_req;
+  a.lw_anew = cache->lw_anew;
+  a.score = cache->score;
+  a.norm = cache->norm;
+  a.sinks = cache->sinks;
+  a.deferred = cache->deferred;
+  a.scope = cache->scope;
   a.batch = cache->batch;
   a.kv_heads = cache->kv_heads;
   a.q_heads = cache->q_heads;
@@ -501,6 +575,7 @@ int lf_decode_step(lf_cache* cache, int layer, const void* q, const void* k_new,
     ta.v16 = cache->tmaps[3];
     ta.a = a;
     ta.row_base = (int)(layer * layer_slots);
+    ta.max_items = cache->items;
     void* args[] = {&ta};
     e = cudaLaunchKernelExC(&cfg, cache->kern.decode, args);
   } else {
@@ -508,6 +583,13 @@ int lf_decode_step(lf_cache* cache, int layer, const void* q, const void* k_new,
     e = cudaLaunchKernelExC(&cfg, cache->kern.decode, args);
   }
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  if (cache->scope == LF_SCOPE_LAYER) {
+    // The shared victim of every sequence, once all its KV heads have scored.
+    void* args[] = {&a};
+    e = cudaLaunchKernel(cache->kern.select, dim3(cache->batch, 1, 1), dim3(lf::kThreads, 1, 1),
+                         args, 0, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "layer-scope selection launch");
+  }
   return LF_OK;
 }
 
@@ -553,6 +635,13 @@ int lf_cache_layout(const lf_cache* cache, lf_layout* out) {
   out->next_pos = cache->next_pos;
   out->budget = cache->budget;
   out->err = cache->err;
+  out->score = cache->score;
+  out->norm = cache->norm;
+  out->sinks = cache->sinks;
+  out->deferred = cache->deferred;
+  out->scope = cache->scope;
+  out->acc = cache->acc;
+  out->pending = cache->pending;
   return LF_OK;
 }
 

@@ -54,9 +54,144 @@ struct DecodeArgs {
   int32_t* next_pos;
   const int32_t* budget;  // [batch]
   int32_t* err;
+  float* acc;          // H2O: this layer's attention mass per slot (as vnorm), else null
+  int32_t* pending;    // deferred: this layer's chosen slot per unit (as count), else null
+  float* lw_score;     // layer scope: one layer's per-slot scores (as vnorm), else null
+  int32_t* lw_req;     // layer scope: [batch][kv_heads] 1 = scores written this step
+  float* lw_anew;      // layer scope: [batch][kv_heads] the new token's attention mass
   int batch, kv_heads, q_heads, slot_stride, capacity, window, chunk, stages, evict;
+  int score, norm, sinks, deferred, scope;  // the policy (lf_config)
   float scale_log2;    // log2(e) / sqrt(D)
 };
+
+// ---- eviction rules shared by every decode kernel ------------------------------
+//
+// Per unit, from its occupancy n, next position p, budget and (deferred) the
+// slot chosen at the previous step:
+//   same step   attend over the n cached slots + the new token; once n >= budget
+//               choose among slots with sinks <= pos < p - W and write the new
+//               token there, else append at slot n;
+//   deferred    the new token takes slot n while n < budget, else the slot chosen
+//               before (`excl`: its old token is neither attended nor a
+//               candidate); once the buffer is full after the write, choose among
+//               slots with sinks <= pos < p + 1 - W the slot the next token takes.
+struct UnitRule {
+  bool full;      // n >= budget with eviction on: this step replaces a token
+  bool choosing;  // a victim is chosen this step
+  int plim;       // a slot is a candidate iff sinks <= pos < plim (and not excl)
+  int excl;       // slot whose old token is dropped before attention (deferred), or -1
+};
+
+__device__ __forceinline__ UnitRule unit_rule(const DecodeArgs& a, int n, int p, int pend,
+                                              int bud, bool state_ok) {
+  UnitRule r;
+  r.full = state_ok && a.evict && n >= bud;
+  if (a.deferred && a.evict) {
+    r.choosing = state_ok && n + 1 >= bud;
+    r.plim = p + 1 - a.window;
+    r.excl = r.full ? pend : -1;
+  } else {
+    r.choosing = r.full;
+    r.plim = p - a.window;
+    r.excl = -1;
+  }
+  return r;
+}
+
+// Candidate weights carry the candidate flag in the sign bit, so that a slot
+// that is not a candidate still carries its value (the H2O accumulator must be
+// written back for every slot, and it may be +0).
+__device__ __forceinline__ float flag_protected(float x) {
+  return __int_as_float(__float_as_int(x) | (int)0x80000000);
+}
+__device__ __forceinline__ bool is_candidate(float w) { return __float_as_int(w) >= 0; }
+
+// ||v|| of one stored value row, by one warp (fp32, lane-strided then a tree).
+template <typename T, int D>
+__device__ __forceinline__ float warp_value_norm(const T* v, int norm, int lane) {
+  float s = 0.f;
+  if (norm == 2) {
+    for (int e = lane; e < D; e += 32) {
+      const float x = to_f32(v[e]);
+      s = fmaf(x, x, s);
+    }
+    return sqrtf(warp_sum(s));
+  }
+  for (int e = lane; e < D; e += 32) s += fabsf(to_f32(v[e]));
+  return warp_sum(s);
+}
+
+// The unit leader's decision once the cluster's lowest (score, slot) is known
+// (`fi`, INT_MAX if none): the slot the new token takes (-1: none) and the slot
+// reported as evicted, with the unit's bookkeeping written to global memory
+// (count, next position, the deferred choice, the layer-scope request).
+struct LeaderOut {
+  int slot;
+  int evicted;
+};
+
+__device__ __forceinline__ LeaderOut leader_decide(const DecodeArgs& a, int unit, int n, int p,
+                                                   int pend, int bud, bool state_ok,
+                                                   bool any_fail, const UnitRule& r, int fi,
+                                                   float anew) {
+  const bool layer = a.evict && a.scope == LF_SCOPE_LAYER;
+  const bool deferred = a.evict && a.deferred;
+  int chosen = -1;
+  if (r.choosing && !layer) {
+    if (fi != INT_MAX) chosen = fi;
+    else if (!any_fail) atomicOr(a.err, LF_DEVERR_STATE);  // no candidate
+  }
+  int slot = -1, evicted = -1;
+  if (deferred) {
+    slot = r.full ? pend : n;
+    evicted = r.full ? pend : -1;
+    if (r.full && pend < 0) {  // a full buffer without a chosen slot
+      if (!any_fail) atomicOr(a.err, LF_DEVERR_STATE);
+      slot = evicted = -1;
+    }
+  } else if (r.full) {
+    slot = evicted = layer ? -1 : chosen;  // layer scope: the selection kernel writes
+  } else {
+    slot = (n < (a.evict ? bud : a.capacity)) ? n : -1;
+  }
+  if (!state_ok) atomicOr(a.err, LF_DEVERR_STATE);
+  if (any_fail || !state_ok) slot = evicted = -1;
+  a.evicted[unit] = evicted;
+  if (state_ok && !any_fail) {
+    if (!r.full && slot >= 0) a.count[unit] = n + 1;
+    a.next_pos[unit] = p + 1;
+    if (deferred && !layer && r.choosing) a.pending[unit] = chosen;
+    if (layer) {
+      a.lw_req[unit] = r.choosing ? n + 1 : 0;  // slots scored, + 1
+      a.lw_anew[unit] = anew;
+    }
+  }
+  return {slot, evicted};
+}
+
+// In-place overwrite of one slot (guide, "Static Memory Pre-Allocation and
+// In-Place Eviction", step 3): K, V, ||v|| (fp32, from the stored value), the
+// position and, with the H2O score, the new token's own attention mass.  Called
+// by `nthreads` threads numbered `tid`; threads 0..31 form one warp.
+template <typename T, int D>
+__device__ __forceinline__ void write_slot(const DecodeArgs& a, size_t ubase, int slot,
+                                           const T* kn, const T* vn, int p, float anew, int tid,
+                                           int nthreads) {
+  T* Kd = reinterpret_cast<T*>(a.K) + (ubase + slot) * D;
+  T* Vd = reinterpret_cast<T*>(a.V) + (ubase + slot) * D;
+  for (int e = tid; e < D; e += nthreads) {
+    Kd[e] = kn[e];
+    Vd[e] = vn[e];
+  }
+  if (tid < 32) {
+    const float nv = warp_value_norm<T, D>(vn, a.norm, tid);
+    if (tid == 0) {
+      a.vnorm[ubase + slot] = nv;
+      a.pos[ubase + slot] = p;
+      if (a.acc) a.acc[ubase + slot] = anew;
+    }
+  }
+}
 
 // Shared-memory plan, shared by the host (launch size) and the kernel.
 template <typename T, int D, int G>
@@ -108,7 +243,8 @@ struct CombineSmem {
   int* decision;  // [2] slot written, victim
   float* o_part;  // [G][D] this CTA's unnormalised output, relative to m_loc
   const float* p; // [rows][G] 2^(s - m_loc) of this CTA's slots
-  const float* w; // [rows] ||v||_1 of candidates, -1 for protected slots
+  const float* w; // [rows] ||v|| (H2O: the accumulator) of each slot, sign bit set
+                  // when the slot is not a candidate
 };
 
 // Cluster-wide combine of one unit: merge (m, l) and the partial outputs over
@@ -118,8 +254,8 @@ struct CombineSmem {
 template <typename T, int D, int G, int NT>
 __device__ __forceinline__ void combine_and_evict(
     const DecodeArgs& a, cg::cluster_group& cluster, const CombineSmem& sm, int C, int rank, int b,
-    int g, int unit, size_t ubase, int n, int p, int bud, bool state_ok, bool evicting, int s0,
-    int rows, bool aborted, const T* qg, const T* kn, const T* vn) {
+    int g, int unit, size_t ubase, int n, int p, int pend, int bud, bool state_ok,
+    const UnitRule& rl, int s0, int rows, bool aborted, const T* qg, const T* kn, const T* vn) {
   constexpr int NW = NT / 32;
   const int tid = threadIdx.x;
   const int lane = tid & 31;
@@ -168,23 +304,39 @@ __device__ __forceinline__ void combine_and_evict(
     }
   }
 
-  // Exact LongFlow scores of this CTA's candidates and their (score, slot) minimum.
+  // Exact scores of this CTA's slots and the lowest (score, slot) of its
+  // candidates.  LongFlow: ||v_i|| sum_h alpha_{h,i}.  H2O: the slot's
+  // accumulator plus this step's sum_h alpha_{h,i}, written back for every slot
+  // but the dropped one before cluster barrier #2 (the leader overwrites the
+  // written slot after it).  Layer scope: every score goes to the scratch for
+  // the selection kernel.
+  const bool h2o = a.evict && a.score == LF_SCORE_H2O;
+  const bool layer = a.evict && a.scope == LF_SCOPE_LAYER;
   float bs = INFINITY;
   int bi = INT_MAX;
-  if (evicting && !aborted) {
+  if ((rl.choosing || h2o) && !aborted) {
     float cm[G];
 #pragma unroll
     for (int h = 0; h < G; ++h) cm[h] = sm.cmul[h];
     for (int i = tid; i < rows; i += NT) {
+      const int slot = s0 + i;
+      if (slot == rl.excl) {
+        if (layer && rl.choosing) a.lw_score[ubase + slot] = INFINITY;
+        continue;
+      }
       const float w = sm.w[i];
-      if (w >= 0.f) {
-        float acc = 0.f;
+      const float val = fabsf(w);
+      float as = 0.f;
 #pragma unroll
-        for (int h = 0; h < G; ++h) acc = fmaf(sm.p[(size_t)i * G + h], cm[h], acc);
-        const float sc = w * acc;
-        if (better(sc, s0 + i, bs, bi)) {
+      for (int h = 0; h < G; ++h) as = fmaf(sm.p[(size_t)i * G + h], cm[h], as);
+      const float sc = h2o ? val + as : val * as;
+      if (h2o) a.acc[ubase + slot] = sc;
+      if (rl.choosing) {
+        if (layer) {
+          a.lw_score[ubase + slot] = is_candidate(w) ? sc : INFINITY;
+        } else if (is_candidate(w) && better(sc, slot, bs, bi)) {
           bs = sc;
-          bi = s0 + i;
+          bi = slot;
         }
       }
     }
@@ -215,56 +367,25 @@ __device__ __forceinline__ void combine_and_evict(
   cluster.sync();  // #2: all slot reads of the step are done; minima are at the leader
   if (rank != 0) return;
 
+  float anew = 0.f;  // the new token's attention mass (tid 0)
   if (tid == 0) {
     bool any_fail = false;
     for (int r = 0; r < C; ++r) any_fail = any_fail || sm.fail_in[r] != 0;
-    int victim = -1;
-    if (evicting) {
-      float fs = INFINITY;
-      int fi = INT_MAX;
-      for (int r = 0; r < C; ++r)
-        if (better(sm.best_s[r], sm.best_i[r], fs, fi)) {
-          fs = sm.best_s[r];
-          fi = sm.best_i[r];
-        }
-      if (fi != INT_MAX) victim = fi;
-      else if (!any_fail) atomicOr(a.err, LF_DEVERR_STATE);  // no candidate
-    }
-    const int limit = a.evict ? bud : a.capacity;
-    int slot = evicting ? victim : (n < limit ? n : -1);
-    if (!state_ok) atomicOr(a.err, LF_DEVERR_STATE);
-    if (any_fail || !state_ok) {
-      slot = -1;
-      victim = -1;
-    }
-    sm.decision[0] = slot;
-    sm.decision[1] = victim;
-    a.evicted[unit] = victim;
-    if (state_ok && !any_fail) {
-      if (!evicting && slot >= 0) a.count[unit] = n + 1;
-      a.next_pos[unit] = p + 1;
-    }
+    float fs = INFINITY;
+    int fi = INT_MAX;
+    for (int r = 0; r < C; ++r)
+      if (better(sm.best_s[r], sm.best_i[r], fs, fi)) {
+        fs = sm.best_s[r];
+        fi = sm.best_i[r];
+      }
+#pragma unroll
+    for (int h = 0; h < G; ++h) anew += exp2f(sm.s_new[h] - sm.m_glb[h]) / sm.l_glb[h];
+    const LeaderOut d = leader_decide(a, unit, n, p, pend, bud, state_ok, any_fail, rl, fi, anew);
+    sm.decision[0] = d.slot;
   }
   __syncthreads();
   const int slot = sm.decision[0];
-  if (slot >= 0) {
-    // In-place overwrite of one slot: K, V, ||v||_1 (fp32, from the stored value), position.
-    T* Kd = reinterpret_cast<T*>(a.K) + (ubase + slot) * D;
-    T* Vd = reinterpret_cast<T*>(a.V) + (ubase + slot) * D;
-    for (int e = tid; e < D; e += NT) {
-      Kd[e] = kn[e];
-      Vd[e] = vn[e];
-    }
-    if (warp == 0) {
-      float s = 0.f;
-      for (int e = lane; e < D; e += 32) s += fabsf(to_f32(vn[e]));
-      s = warp_sum(s);
-      if (lane == 0) {
-        a.vnorm[ubase + slot] = s;
-        a.pos[ubase + slot] = p;
-      }
-    }
-  }
+  if (slot >= 0) write_slot<T, D>(a, ubase, slot, kn, vn, p, anew, tid, NT);
 }
 
 template <typename T, int D, int G>
@@ -312,8 +433,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_simt_kernel(const Dec
   const int n = a.count[unit];
   const int p = a.next_pos[unit];
   const int bud = a.budget[b];
+  // Read before the leader may update it (after cluster barrier #2).
+  const int pend = (a.evict && a.deferred) ? a.pending[unit] : -1;
   const bool state_ok = (n >= 0 && n <= a.capacity && p >= n);
-  const bool evicting = state_ok && a.evict && n >= bud;
+  const UnitRule rl = unit_rule(a, n, p, pend, bud, state_ok);
   const int s0 = rank * a.chunk;
   const int s1 = state_ok ? min(s0 + a.chunk, n) : s0;
   const int rows = max(0, s1 - s0);
@@ -323,7 +446,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_simt_kernel(const Dec
   const size_t ubase = (size_t)unit * a.slot_stride;
   const T* Ku = reinterpret_cast<const T*>(a.K) + ubase * D;
   const T* Vu = reinterpret_cast<const T*>(a.V) + ubase * D;
-  const float* vnu = a.vnorm + ubase;
+  // ||v|| per slot, or the H2O accumulator: the value a candidate is scored from
+  const float* vnu = (a.evict && a.score == LF_SCORE_H2O) ? a.acc + ubase : a.vnorm + ubase;
   const int32_t* posu = a.pos + ubase;
   const T* qg = reinterpret_cast<const T*>(a.q) + ((size_t)b * a.q_heads + (size_t)g * G) * D;
   const T* kn = reinterpret_cast<const T*>(a.k_new) + (size_t)unit * D;
@@ -378,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_simt_kernel(const Dec
       for (int v = 0; v < V; ++v) qr[h][c * V + v] *= a.scale_log2;
     }
 
-  const int plim = p - a.window;  // a slot is a candidate iff pos < plim
+  const int plim = rl.plim;  // a slot is a candidate iff sinks <= pos < plim (and not excl)
   const int pv_e0 = (tid % P::kPvTpr) * 4;
   const int pv_grp = tid / P::kPvTpr;
   float pv[G][4];
@@ -424,12 +548,17 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_simt_kernel(const Dec
         if (rr < r) {
 #pragma unroll
           for (int h = 0; h < G; ++h)
-            if (sub == h % LPS) lg[(size_t)(off + rr) * G + h] = acc[h];
+            if (sub == h % LPS)
+              lg[(size_t)(off + rr) * G + h] = (s0 + off + rr == rl.excl) ? -INFINITY : acc[h];
         }
       }
       const float* vn_t = reinterpret_cast<const float*>(stage + P::kStageData);
       const int32_t* pos_t = reinterpret_cast<const int32_t*>(stage + P::kStageData + kTile * 4);
-      if (tid < r) wv[off + tid] = (pos_t[tid] < plim) ? vn_t[tid] : -1.0f;
+      if (tid < r) {
+        const int ps = pos_t[tid];
+        const bool cand = (s0 + off + tid != rl.excl) && ps < plim && ps >= a.sinks;
+        wv[off + tid] = cand ? vn_t[tid] : flag_protected(vn_t[tid]);
+      }
     } else if (ok) {
       const T* Vt = reinterpret_cast<const T*>(stage);
       for (int rr = pv_grp; rr < r; rr += P::kPvGroups) {
@@ -479,7 +608,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_simt_kernel(const Dec
       for (int i = tid; i < rows; i += kThreads)
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-          const float e = exp2f(lg[(size_t)i * G + h] - m_loc[h]);
+          const float x = lg[(size_t)i * G + h];
+          const float e = (x == -INFINITY) ? 0.f : exp2f(x - m_loc[h]);  // dropped slot
           lg[(size_t)i * G + h] = e;
           sm[h] += e;
         }
@@ -530,8 +660,89 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_simt_kernel(const Dec
   }
   CombineSmem cs{m_loc, l_loc, s_new, cmul, m_glb, l_glb, best_s, best_i, fail_in, red, red_i,
                  decision, o_part, lg, wv};
-  combine_and_evict<T, D, G, kThreads>(a, cluster, cs, C, rank, b, g, unit, ubase, n, p, bud,
-                                       state_ok, evicting, s0, rows, aborted, qg, kn, vn);
+  combine_and_evict<T, D, G, kThreads>(a, cluster, cs, C, rank, b, g, unit, ubase, n, p, pend,
+                                       bud, state_ok, rl, s0, rows, aborted, qg, kn, vn);
+}
+
+// ---- layer scope: the shared victim ------------------------------------------
+
+// After the attention kernel of a step, one CTA per sequence adds its KV heads'
+// per-slot scores (+inf for slots that are not candidates), takes the lowest
+// (ties to the lowest slot), and either records it as the slot the next token
+// takes (deferred) or writes every KV head's new token into it.
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads) select_layer_kernel(const DecodeArgs a) {
+  __shared__ float rs[kWarps];
+  __shared__ int ri[kWarps];
+  __shared__ int pick;
+  const int b = blockIdx.x;
+  const int u0 = b * a.kv_heads;
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  // Every KV head's attention kernel leaves the same request: the slots it
+  // scored, + 1 (0: nothing to choose this step).
+  const int req = a.lw_req[u0];
+  bool same = true;
+  for (int g = 1; g < a.kv_heads; ++g) same = same && a.lw_req[u0 + g] == req;
+  if (req == 0 && same) return;
+  __syncthreads();  // every thread has read the requests
+  if (!same || req < 2) {
+    if (tid == 0) atomicOr(a.err, LF_DEVERR_STATE);
+    for (int g = tid; g < a.kv_heads; g += kThreads) a.lw_req[u0 + g] = 0;
+    return;
+  }
+  const int scored = req - 1;
+  float bs = INFINITY;
+  int bi = INT_MAX;
+  for (int i = tid; i < scored; i += kThreads) {
+    float sc = 0.f;
+    for (int g = 0; g < a.kv_heads; ++g) sc += a.lw_score[(size_t)(u0 + g) * a.slot_stride + i];
+    if (sc < INFINITY && better(sc, i, bs, bi)) {
+      bs = sc;
+      bi = i;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float os = __shfl_xor_sync(0xffffffffu, bs, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    if (better(os, oi, bs, bi)) {
+      bs = os;
+      bi = oi;
+    }
+  }
+  if (lane == 0) {
+    rs[warp] = bs;
+    ri[warp] = bi;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    for (int w = 1; w < kWarps; ++w)
+      if (better(rs[w], ri[w], bs, bi)) {
+        bs = rs[w];
+        bi = ri[w];
+      }
+    pick = (bi == INT_MAX) ? -1 : bi;
+    if (pick < 0) atomicOr(a.err, LF_DEVERR_STATE);  // no candidate
+  }
+  __syncthreads();
+  const int e = pick;
+  if (a.deferred) {
+    for (int g = tid; g < a.kv_heads; g += kThreads) a.pending[u0 + g] = e;
+  } else {
+    for (int g = warp; g < a.kv_heads; g += kWarps) {
+      const int u = u0 + g;
+      if (e >= 0) {
+        const size_t ubase = (size_t)u * a.slot_stride;
+        const T* kn = reinterpret_cast<const T*>(a.k_new) + (size_t)u * D;
+        const T* vn = reinterpret_cast<const T*>(a.v_new) + (size_t)u * D;
+        write_slot<T, D>(a, ubase, e, kn, vn, a.next_pos[u] - 1, a.lw_anew[u], lane, 32);
+      }
+      if (lane == 0) a.evicted[u] = e;
+    }
+  }
+  for (int g = tid; g < a.kv_heads; g += kThreads) a.lw_req[u0 + g] = 0;
 }
 
 // ---- prefill ----------------------------------------------------------------
@@ -546,7 +757,9 @@ struct PrefillArgs {
   int32_t* pos;
   int32_t* count;
   int32_t* next_pos;
-  int kv_heads, max_prompt, slot_stride;
+  float* acc;             // H2O accumulators (zeroed), or null
+  int32_t* pending;       // deferred choice (set to -1), or null
+  int kv_heads, max_prompt, slot_stride, norm;
 };
 
 // grid (kv_heads, batch); one CTA copies one unit's prompt rows.
@@ -573,18 +786,17 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(const PrefillArgs a) 
   const T* vrow0 = reinterpret_cast<const T*>(a.v) + src0;
   const size_t ubase = (size_t)unit * a.slot_stride;
   for (int i = warp; i < a.slot_stride; i += kWarps) {
-    float s = 0.f;
-    if (i < P)
-      for (int e = lane; e < D; e += 32) s += fabsf(to_f32(vrow0[(size_t)i * D + e]));
-    s = warp_sum(s);
+    const float nv = (i < P) ? warp_value_norm<T, D>(vrow0 + (size_t)i * D, a.norm, lane) : 0.f;
     if (lane == 0) {
-      a.vnorm[ubase + i] = (i < P) ? s : 0.f;
+      a.vnorm[ubase + i] = nv;
       a.pos[ubase + i] = (i < P) ? i : -1;
+      if (a.acc) a.acc[ubase + i] = 0.f;
     }
   }
   if (threadIdx.x == 0) {
     a.count[unit] = P;
     a.next_pos[unit] = P;
+    if (a.pending) a.pending[unit] = -1;
   }
 }
 

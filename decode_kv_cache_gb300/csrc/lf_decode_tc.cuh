@@ -67,6 +67,7 @@ struct TcArgs {
   CUtensorMap k64, k16, v64, v16;  // 2-D views [rows][128] of K and V, boxes {64,64} / {64,16}
   DecodeArgs a;
   int row_base;                    // tensor row of this layer's first slot
+  int max_items;                   // units one cluster may visit (sizes the item table)
 };
 
 template <int G>
@@ -83,8 +84,7 @@ struct TcPlan {
   static constexpr int kOffRed = kOffStats + 9 * kMaxGroup * 4;
   static constexpr int kOffMisc = kOffRed + 4 * kMaxGroup * 4 + 16;
   static constexpr int kOffStatIn = 2048;                    // [2][kMaxCluster][2G] floats
-  static constexpr int kOffItems = kOffStatIn + 2 * kMaxCluster * 2 * kMaxGroup * 4;
-  static constexpr int kOffOpart = kOffItems + kTcMaxItems * 8;  // [2][G][D]
+  static constexpr int kOffOpart = kOffStatIn + 2 * kMaxCluster * 2 * kMaxGroup * 4;  // [2][G][D]
   static_assert(kOffMisc + 64 <= kOffStatIn, "header overflow");
   static_assert(16 + 16 + 2 * kTcSBufs + 2 * kTcPBufs + 14 <= kOffStats / 8, "too many barriers");
   static constexpr int kOffQ = (kOffOpart + 2 * G * D * 4 + 1023) / 1024 * 1024;  // [2] buffers
@@ -104,11 +104,15 @@ struct TcPlan {
   __host__ __device__ static constexpr int off_vn(int stages, int chunk, int cluster, int evict) {
     return (off_lg(stages, cluster) + (evict ? 2 : 1) * chunk * G * 4 + 15) / 16 * 16;
   }
-  // vn[2], pos[2] (raw, from the slab) then w[2] (candidate weights), each vn_bytes(chunk)
+  // vn[2], pos[2] (raw, from the slab) then w[2] (candidate weights), each vn_bytes(chunk);
+  // then the item table: (count, next position, deferred choice, -) per unit visited.
+  __host__ __device__ static constexpr int off_items(int stages, int chunk, int cluster,
+                                                     int evict) {
+    return off_vn(stages, chunk, cluster, evict) + (evict ? 6 * vn_bytes(chunk) : 0);
+  }
   __host__ __device__ static constexpr int smem_bytes(int stages, int chunk, int cluster,
-                                                      int evict) {
-    return off_vn(stages, chunk, cluster, evict) + (evict ? 6 * vn_bytes(chunk) : 0) +
-           1024;  // + alignment slack
+                                                      int evict, int items) {
+    return off_items(stages, chunk, cluster, evict) + items * 16 + 1024;  // + alignment slack
   }
 };
 
@@ -134,6 +138,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int chunk = a.chunk;
   const int units = a.batch * a.kv_heads;
   const int nitems = (j < units) ? (units - j + NC - 1) / NC : 0;
+  if (nitems > ta.max_items) {  // the host sized the item table for fewer units
+    if (threadIdx.x == 0 && cg::this_cluster().block_rank() == 0) atomicOr(ta.a.err, LF_DEVERR_STATE);
+    return;
+  }
 
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // The 128-byte swizzle phase of TMA writes and MMA reads follows address
@@ -169,7 +177,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   volatile int* fail_any = reinterpret_cast<volatile int*>(smem + P::kOffMisc + 16);
   volatile int* uflag = reinterpret_cast<volatile int*>(smem + P::kOffMisc + 24);  // [2]
   float* stat_in = reinterpret_cast<float*>(smem + P::kOffStatIn);  // [2][C][2G]
-  int* items = reinterpret_cast<int*>(smem + P::kOffItems);         // [nitems][2] (n, p)
+  int* items = reinterpret_cast<int*>(smem + P::off_items(S, chunk, C, a.evict));  // [nitems][4]
   float* opbase = reinterpret_cast<float*>(smem + P::kOffOpart);     // [2][G][D]
   unsigned char* qbuf = smem + P::kOffQ;
   unsigned char* ring = smem + P::kOffRing;
@@ -229,8 +237,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // leaders update them during the launch, every role must see the old values.
   for (int k = tid; k < nitems; k += kTcThreads) {
     const int u = j + k * NC;
-    items[2 * k] = a.count[u];
-    items[2 * k + 1] = a.next_pos[u];
+    items[4 * k] = a.count[u];
+    items[4 * k + 1] = a.next_pos[u];
+    items[4 * k + 2] = (a.evict && a.deferred) ? a.pending[u] : -1;
   }
   fence_proxy_async_smem();
   tc_fence_before();
@@ -245,8 +254,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // cluster (in multiples of 4), so a partly filled unit keeps every CTA busy.
   // Returns the slot count and sets `base`, the first slot.
   auto unit_rows = [&](int k, int& n, int& p, bool& ok, int& base) {
-    n = items[2 * k];
-    p = items[2 * k + 1];
+    n = items[4 * k];
+    p = items[4 * k + 1];
     ok = (n >= 0 && n <= a.capacity && p >= n);
     const int per = ((n + C - 1) / C + 3) & ~3;  // <= chunk since n <= capacity
     base = rank * per;
@@ -317,7 +326,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           unsigned char* vdst = vnbase + b2 * P::vn_bytes(chunk);
           unsigned char* pdst = vnbase + (2 + b2) * P::vn_bytes(chunk);
           mbar_arrive_expect_tx(&aux[b2], 2u * small);
-          bulk_g2s(vdst, a.vnorm + ubase + base, small, &aux[b2], pol);
+          bulk_g2s(vdst, (a.score == LF_SCORE_H2O ? a.acc : a.vnorm) + ubase + base, small,
+                   &aux[b2], pol);
           bulk_g2s(pdst, a.pos + ubase + base, small, &aux[b2], pol);
         } else {
           mbar_arrive(&aux[b2]);  // nothing to load: complete the phase
@@ -485,7 +495,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int32_t* pos_s =
           reinterpret_cast<const int32_t*>(vnbase + (2 + b2) * P::vn_bytes(chunk));
       float* w_s = reinterpret_cast<float*>(vnbase + (4 + b2) * P::vn_bytes(chunk));
-      const int plim = p - a.window;  // a slot is a candidate iff pos < plim
+      const int bud = a.budget[(j + k * NC) / a.kv_heads];
+      const UnitRule rl = unit_rule(a, n, p, items[4 * k + 2], bud, state_ok);
+      const int plim = rl.plim;  // a slot is a candidate iff sinks <= pos < plim (and not excl)
+      const int excl = rl.excl - base;  // this CTA's row of the dropped slot (deferred)
 
       // The tail warps must be done with this parity's buffers (unit k - 2).
       bool bad = false;
@@ -515,13 +528,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) mbar_arrive(&sfree[buf]);
         const int i = t * kTcTile + tid;
         if (i < rows) {
+          const bool dropped = (i == excl);
 #pragma unroll
           for (int h = 0; h < G; ++h) {
-            const float s = acc[h] * a.scale_log2;
+            const float s = dropped ? -INFINITY : acc[h] * a.scale_log2;
             lg[(size_t)i * G + h] = s;
             mx[h] = fmaxf(mx[h], s);
           }
-          if (lgpar) w_s[i] = (pos_s[i] < plim) ? vn_s[i] : -1.0f;
+          if (lgpar) {
+            const int ps = pos_s[i];
+            const bool cand = !dropped && ps < plim && ps >= a.sinks;
+            w_s[i] = cand ? vn_s[i] : flag_protected(vn_s[i]);
+          }
         }
       }
       const bool any_bad = named_bar_or(1, kTcCompute, bad);
@@ -560,7 +578,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           for (int h = 0; h < G; ++h) {
             float pv = 0.f;
             if (i < rows) {
-              pv = exp2f(lg[(size_t)i * G + h] - ml[h]);
+              const float x = lg[(size_t)i * G + h];
+              pv = (x == -INFINITY) ? 0.f : exp2f(x - ml[h]);  // the dropped slot: 0
               lg[(size_t)i * G + h] = pv;
               sm[h] += pv;
             }
@@ -630,7 +649,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int b = u / a.kv_heads;
       const int g = u - b * a.kv_heads;
       const int bud = a.budget[b];
-      const bool evicting = state_ok && a.evict && n >= bud;
+      const int pend = items[4 * k + 2];
+      const UnitRule rl = unit_rule(a, n, p, pend, bud, state_ok);
+      const bool h2o = a.evict && a.score == LF_SCORE_H2O;
+      const bool layer = a.evict && a.scope == LF_SCOPE_LAYER;
       const int b2 = k & 1;
       const float* lg = lgbase + (size_t)(b2 & lgpar) * chunk * G;
       const float* o_part = opbase + (size_t)b2 * G * D;
@@ -698,24 +720,36 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         atomicOr(a.err, LF_DEVERR_TIMEOUT);
       }
 
-      // Exact LongFlow scores of this CTA's candidates and their (score, slot) minimum.
+      // Exact scores of this CTA's slots and the lowest (score, slot) of its
+      // candidates.  LongFlow: ||v_i|| sum_h alpha_{h,i}.  H2O: the slot's
+      // accumulator plus this step's sum_h alpha_{h,i}.  Layer scope: every score
+      // goes to the scratch for the selection kernel, and the H2O accumulators
+      // are written back here.
       float bs = INFINITY;
       int bi = INT_MAX;
-      if (evicting && !unit_failed && stats_ok) {
+      const bool scoring = (rl.choosing || h2o) && !unit_failed && stats_ok;
+      if (scoring) {
         float cm[G];
 #pragma unroll
         for (int h = 0; h < G; ++h) cm[h] = cmul[h];
         for (int i = tt_id; i < rows; i += kTcTail) {
+          const int slot = base + i;
+          if (slot == rl.excl) {
+            if (layer && rl.choosing) a.lw_score[ubase + slot] = INFINITY;
+            continue;
+          }
           const float w = w_s[i];
-          if (w >= 0.f) {
-            float acc = 0.f;
+          const float val = fabsf(w);
+          float as = 0.f;
 #pragma unroll
-            for (int h = 0; h < G; ++h) acc = fmaf(lg[(size_t)i * G + h], cm[h], acc);
-            const float sc = w * acc;
-            if (better(sc, base + i, bs, bi)) {
-              bs = sc;
-              bi = base + i;
-            }
+          for (int h = 0; h < G; ++h) as = fmaf(lg[(size_t)i * G + h], cm[h], as);
+          const float sc = h2o ? val + as : val * as;
+          if (layer) {
+            if (h2o) a.acc[ubase + slot] = sc;
+            if (rl.choosing) a.lw_score[ubase + slot] = is_candidate(w) ? sc : INFINITY;
+          } else if (rl.choosing && is_candidate(w) && better(sc, slot, bs, bi)) {
+            bs = sc;
+            bi = slot;
           }
         }
       }
@@ -733,6 +767,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         red_ti[twarp] = bi;
       }
       named_bar_sync(2, kTcTail);
+      // H2O, per-KV-head scope: write back the accumulators of this CTA's slots
+      // except the dropped slot and the CTA's lowest candidate.  The leader
+      // writes that one (it may be the victim, which takes the new token's), so
+      // no slot has two writers.
+      if (scoring && h2o && !layer) {
+        int ci = red_ti[0];
+        float cs = red_t[0];
+        if (better(red_t[1], red_ti[1], cs, ci)) ci = red_ti[1];
+        float cm[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) cm[h] = cmul[h];
+        for (int i = tt_id; i < rows; i += kTcTail) {
+          const int slot = base + i;
+          if (slot == rl.excl || slot == ci) continue;
+          float as = 0.f;
+#pragma unroll
+          for (int h = 0; h < G; ++h) as = fmaf(lg[(size_t)i * G + h], cm[h], as);
+          a.acc[ubase + slot] = fabsf(w_s[i]) + as;
+        }
+      }
 
       // Exchange 2: partial output and lowest (score, slot) to the unit's leader.
       // One receive buffer suffices: a peer can send the leader's next unit only
@@ -776,6 +830,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             from_f32(acc / l_glb[h], &og[(size_t)h * D + e]);
           }
         }
+        float anew = 0.f;  // the new token's attention mass (tt_id 0)
         if (tt_id == 0) {
           bool any_fail = !all_got || !stats_ok;
           float fs = INFINITY;
@@ -791,45 +846,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               fi = ri;
             }
           }
-          int victim = -1;
-          if (evicting) {
-            if (fi != INT_MAX) victim = fi;
-            else if (!any_fail) atomicOr(a.err, LF_DEVERR_STATE);  // no candidate
-          }
-          const int limit = a.evict ? bud : a.capacity;
-          int slot = evicting ? victim : (n < limit ? n : -1);
-          if (!state_ok) atomicOr(a.err, LF_DEVERR_STATE);
-          if (any_fail || !state_ok) {
-            slot = -1;
-            victim = -1;
-          }
-          decision[0] = slot;
-          a.evicted[u] = victim;
-          if (state_ok && !any_fail) {
-            if (!evicting && slot >= 0) a.count[u] = n + 1;
-            a.next_pos[u] = p + 1;
-          }
+#pragma unroll
+          for (int h = 0; h < G; ++h) anew += exp2f(snw[h] - m_glb[h]) / l_glb[h];
+          const LeaderOut d = leader_decide(a, u, n, p, pend, bud, state_ok, any_fail, rl, fi, anew);
+          decision[0] = d.slot;
+          // H2O: the accumulators of the CTAs' lowest candidates (their scores),
+          // except the slot the new token takes.
+          if (h2o && !layer && state_ok && !any_fail)
+            for (int r = 0; r < C; ++r) {
+              const uint32_t* tail =
+                  reinterpret_cast<const uint32_t*>(fin + (size_t)r * P::kFinBytes + G * D * 4);
+              const int ri = (int)tail[1];
+              if (ri != INT_MAX && ri != d.slot) a.acc[ubase + ri] = __uint_as_float(tail[0]);
+            }
         }
         named_bar_sync(2, kTcTail);
         const int slot = decision[0];
-        if (slot >= 0) {
-          // In-place overwrite: K, V, ||v||_1 (fp32, from the stored value), position.
-          T* Kd = reinterpret_cast<T*>(a.K) + (ubase + slot) * D;
-          T* Vd = reinterpret_cast<T*>(a.V) + (ubase + slot) * D;
-          for (int e = tt_id; e < D; e += kTcTail) {
-            Kd[e] = kn[e];
-            Vd[e] = vn[e];
-          }
-          if (twarp == 0) {
-            float sl = 0.f;
-            for (int e = lane; e < D; e += 32) sl += fabsf(to_f32(vn[e]));
-            sl = warp_sum(sl);
-            if (lane == 0) {
-              a.vnorm[ubase + slot] = sl;
-              a.pos[ubase + slot] = p;
-            }
-          }
-        }
+        if (slot >= 0) write_slot<T, D>(a, ubase, slot, kn, vn, p, anew, tt_id, kTcTail);
       }
       // Release this parity's buffers (logits, partial output, statistics).
       named_bar_sync(2, kTcTail);

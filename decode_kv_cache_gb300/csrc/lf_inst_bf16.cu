@@ -6,7 +6,7 @@ namespace lf {
 namespace {
 
 template <int D, int G>
-int smem_bytes_bf16(int stages, int chunk, int /*cluster*/, int /*evict*/) {
+int smem_bytes_bf16(int stages, int chunk, int /*cluster*/, int /*evict*/, int /*items*/) {
   return DecodePlan<__nv_bfloat16, D, G>::smem_bytes(stages, chunk);
 }
 
@@ -14,6 +14,7 @@ template <int D, int G>
 bool fill(KernelEntry* e) {
   e->decode = reinterpret_cast<const void*>(&decode_step_simt_kernel<__nv_bfloat16, D, G>);
   e->prefill = reinterpret_cast<const void*>(&prefill_kernel<__nv_bfloat16, D>);
+  e->select = reinterpret_cast<const void*>(&select_layer_kernel<__nv_bfloat16, D>);
   e->smem_bytes = &smem_bytes_bf16<D, G>;
   e->head_dim = D;
   e->group = G;

@@ -6,8 +6,8 @@ namespace lf {
 namespace {
 
 template <int G>
-int smem_bytes_tc(int stages, int chunk, int cluster, int evict) {
-  return TcPlan<G>::smem_bytes(stages, chunk, cluster, evict);
+int smem_bytes_tc(int stages, int chunk, int cluster, int evict, int items) {
+  return TcPlan<G>::smem_bytes(stages, chunk, cluster, evict, items);
 }
 
 template <int G>
@@ -15,6 +15,7 @@ bool fill(KernelEntry* e) {
   e->kind = kTensorCore;
   e->decode = reinterpret_cast<const void*>(&decode_step_tc_kernel<G>);
   e->prefill = reinterpret_cast<const void*>(&prefill_kernel<__nv_bfloat16, 128>);
+  e->select = reinterpret_cast<const void*>(&select_layer_kernel<__nv_bfloat16, 128>);
   e->smem_bytes = &smem_bytes_tc<G>;
   e->head_dim = 128;
   e->group = G;

@@ -14,7 +14,10 @@ struct KernelEntry {
   int kind = kSimt;               // kSimt: decode(DecodeArgs); kTensorCore: decode(TcArgs)
   const void* decode = nullptr;
   const void* prefill = nullptr;  // __global__ void(PrefillArgs)
-  int (*smem_bytes)(int stages, int chunk, int cluster, int evict) = nullptr;
+  const void* select = nullptr;   // __global__ void(DecodeArgs): layer-scope victim
+  // Dynamic shared memory of one decode CTA; `items` bounds the units one
+  // cluster visits per launch (tensor-core kernel only).
+  int (*smem_bytes)(int stages, int chunk, int cluster, int evict, int items) = nullptr;
   int head_dim = 0, group = 0, elem_bytes = 0;
 };
 

@@ -65,6 +65,8 @@ extern "C" int lf_prefill_fill_noalloc(const lf_layout* dst, int layer, const vo
   if (!dst->k || !dst->v || !dst->vnorm || !dst->pos || !dst->count || !dst->next_pos)
     return noalloc_fail(LF_ERR_ARG, "destination layout has a null pointer");
   if (layer < 0 || layer >= dst->layers) return noalloc_fail(LF_ERR_ARG, "layer out of range");
+  if (dst->norm != 0 && dst->norm != 1 && dst->norm != 2)
+    return noalloc_fail(LF_ERR_ARG, "norm must be 0 (l1), 1 or 2");
   if (dst->batch < 1 || dst->kv_heads < 1 || dst->capacity < 1 ||
       dst->slot_stride < dst->capacity || dst->slot_stride % 4 != 0)
     return noalloc_fail(LF_ERR_ARG, "invalid destination shape");
@@ -114,9 +116,12 @@ extern "C" int lf_prefill_fill_noalloc(const lf_layout* dst, int layer, const vo
   a.pos = dst->pos + layer * layer_slots;
   a.count = dst->count + layer * layer_units;
   a.next_pos = dst->next_pos + layer * layer_units;
+  a.acc = dst->acc ? dst->acc + layer * layer_slots : nullptr;
+  a.pending = dst->pending ? dst->pending + layer * layer_units : nullptr;
   a.kv_heads = dst->kv_heads;
   a.max_prompt = max_prompt;
   a.slot_stride = dst->slot_stride;
+  a.norm = (dst->norm == 2) ? 2 : 1;
   void* args[] = {&a};
   e = cudaLaunchKernel(kern.prefill, dim3(dst->kv_heads, dst->batch, 1), dim3(lf::kThreads, 1, 1),
                        args, 0, st);

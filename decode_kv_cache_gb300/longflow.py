@@ -32,6 +32,10 @@ LF_OK, LF_ERR_ARG, LF_ERR_OOM, LF_ERR_CUDA, LF_ERR_DEVICE, LF_ERR_UNSUPPORTED = 
 LF_BF16, LF_F32 = 0, 1
 LF_KERNEL_AUTO, LF_KERNEL_SIMT, LF_KERNEL_TENSOR_CORE = 0, 1, 2
 _KERNEL = {"auto": LF_KERNEL_AUTO, "simt": LF_KERNEL_SIMT, "tc": LF_KERNEL_TENSOR_CORE}
+LF_SCORE_LONGFLOW, LF_SCORE_H2O = 0, 1
+_SCORE = {"longflow": LF_SCORE_LONGFLOW, "h2o": LF_SCORE_H2O}
+LF_SCOPE_KV_HEAD, LF_SCOPE_LAYER = 0, 1
+_SCOPE = {"kv_head": LF_SCOPE_KV_HEAD, "layer": LF_SCOPE_LAYER}
 LF_DEVERR_NONFINITE, LF_DEVERR_STATE, LF_DEVERR_TIMEOUT = 1, 2, 4
 
 _DTYPE = {"bf16": LF_BF16, "f32": LF_F32}
@@ -47,7 +51,9 @@ class LFError(RuntimeError):
 class LFConfig(ctypes.Structure):
     _fields_ = [("dtype", ctypes.c_int), ("evict", ctypes.c_int),
                 ("budgets", ctypes.POINTER(ctypes.c_int32)), ("cluster", ctypes.c_int),
-                ("stages", ctypes.c_int), ("kernel", ctypes.c_int)]
+                ("stages", ctypes.c_int), ("kernel", ctypes.c_int),
+                ("score", ctypes.c_int), ("norm", ctypes.c_int), ("sinks", ctypes.c_int),
+                ("deferred", ctypes.c_int), ("scope", ctypes.c_int)]
 
 
 class LFLayout(ctypes.Structure):
@@ -56,7 +62,9 @@ class LFLayout(ctypes.Structure):
         "window", "dtype", "evict", "cluster", "stages", "kernel")] + [
         ("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("vnorm", ctypes.c_void_p),
         ("pos", ctypes.c_void_p), ("count", ctypes.c_void_p), ("next_pos", ctypes.c_void_p),
-        ("budget", ctypes.c_void_p), ("err", ctypes.c_void_p)]
+        ("budget", ctypes.c_void_p), ("err", ctypes.c_void_p)] + [
+        (n, ctypes.c_int) for n in ("score", "norm", "sinks", "deferred", "scope")] + [
+        ("acc", ctypes.c_void_p), ("pending", ctypes.c_void_p)]
 
 
 _lib: Optional[ctypes.CDLL] = None
@@ -144,7 +152,8 @@ def lf_cache_create(layers, batch, kv_heads, q_heads, head_dim, budget, window) 
 
 def lf_cache_create_ex(layers, batch, kv_heads, q_heads, head_dim, capacity, window,
                        dtype="bf16", evict=True, budgets: Optional[Sequence[int]] = None,
-                       cluster=0, stages=0, kernel="auto") -> int:
+                       cluster=0, stages=0, kernel="auto", score="longflow", norm=1, sinks=0,
+                       deferred=False, scope="kv_head") -> int:
     cfg = LFConfig()
     cfg.dtype = _DTYPE[dtype] if isinstance(dtype, str) else int(dtype)
     cfg.evict = int(bool(evict))
@@ -155,6 +164,11 @@ def lf_cache_create_ex(layers, batch, kv_heads, q_heads, head_dim, capacity, win
     cfg.cluster = int(cluster)
     cfg.stages = int(stages)
     cfg.kernel = _KERNEL[kernel] if isinstance(kernel, str) else int(kernel)
+    cfg.score = _SCORE[score] if isinstance(score, str) else int(score)
+    cfg.norm = int(norm)
+    cfg.sinks = int(sinks)
+    cfg.deferred = int(bool(deferred))
+    cfg.scope = _SCOPE[scope] if isinstance(scope, str) else int(scope)
     h = load_library().lf_cache_create_ex(layers, batch, kv_heads, q_heads, head_dim, capacity,
                                           window, ctypes.byref(cfg))
     if not h:
@@ -219,13 +233,14 @@ class LFCache:
 
     def __init__(self, layers, batch, kv_heads, q_heads, head_dim, capacity, window,
                  dtype="bf16", evict=True, budgets=None, cluster=0, stages=0, kernel="auto",
-                 device=None):
+                 device=None, score="longflow", norm=1, sinks=0, deferred=False,
+                 scope="kv_head"):
         self.device = torch.device("cuda", torch.cuda.current_device() if device is None
                                    else torch.device(device).index or 0)
         with torch.cuda.device(self.device):
             self.handle = lf_cache_create_ex(layers, batch, kv_heads, q_heads, head_dim, capacity,
                                              window, dtype, evict, budgets, cluster, stages,
-                                             kernel)
+                                             kernel, score, norm, sinks, deferred, scope)
         self.layout = lf_cache_layout(self.handle)
         self.dtype = _TORCH_DTYPE[self.layout.dtype]
         self.layers, self.batch = layers, batch
@@ -282,7 +297,8 @@ class LFCache:
 
     def views(self):
         """Torch tensors aliasing the slab (no copy): k, v [L][b][H_kv][stride][d],
-        vnorm, pos [L][b][H_kv][stride], count, next_pos [L][b][H_kv], budget [b]."""
+        vnorm, pos [L][b][H_kv][stride], count, next_pos [L][b][H_kv], budget [b];
+        acc [L][b][H_kv][stride] (H2O) and pending [L][b][H_kv] (deferred), else None."""
         lay = self.layout
         L, b, g, s, d = lay.layers, lay.batch, lay.kv_heads, lay.slot_stride, lay.head_dim
         if self.dtype == torch.bfloat16:
@@ -298,4 +314,8 @@ class LFCache:
             "count": _view(lay.count, (L, b, g), torch.int32, self.device),
             "next_pos": _view(lay.next_pos, (L, b, g), torch.int32, self.device),
             "budget": _view(lay.budget, (b,), torch.int32, self.device),
+            "acc": (_view(lay.acc, (L, b, g, s), torch.float32, self.device)
+                    if lay.acc else None),
+            "pending": (_view(lay.pending, (L, b, g), torch.int32, self.device)
+                        if lay.pending else None),
         }

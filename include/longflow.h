@@ -22,6 +22,29 @@
  *       -- guide, section "Static Memory Pre-Allocation and In-Place Eviction",
  *          steps 1-3; summary, section 2.3 "Static KV Cache" / "Fused Kernel".
  *
+ * Policy variants (lf_config; the defaults are the operation above):
+ *   norm = 2       score_i = ||v_i||_2 * sum_h alpha_{h,i}: the guide, same section,
+ *                  defines the importance as the "l1-norm or l2-norm" of c_{t,i};
+ *   sinks = s      positions 0..s-1 are never evicted (the guide's reference step,
+ *                  section "End-to-End Implementation", protects its first
+ *                  sink_size slots);
+ *   deferred = 1   the order of that reference step and of the fused kernel's step 4
+ *                  ("the physical slot index to be overwritten in the next
+ *                  iteration"): the new token first takes the next free slot, or
+ *                  the slot chosen at the previous step, and is attended from the
+ *                  buffer; once the buffer is full the lowest-score slot with
+ *                  pos_i < p + 1 - window becomes the slot the next token takes
+ *                  (window >= 1 protects the new token itself);
+ *   scope = LF_SCOPE_LAYER  one victim per (layer, sequence) shared by all KV heads,
+ *                  scored by the sum over every query head (the reference step sums
+ *                  |c| over heads and feature dimensions);
+ *   score = LF_SCORE_H2O    score_i = the attention mass slot i's token has received,
+ *                  summed over the group's query heads and over every decode step
+ *                  since it entered the buffer, its entry step included (prompt
+ *                  tokens start at 0) -- the cumulative statistic the guide
+ *                  attributes to H2O ("The Long-Output Reasoning Crisis" and the
+ *                  comparison table, "Cumulative Attention Mass").
+ *
  * Storage: one static slab per cache, allocated once by lf_cache_create*,
  * never grown, moved or compacted.  All per-step work is stream-ordered and
  * asynchronous: no call below synchronises the host except lf_cache_check,
@@ -47,7 +70,7 @@
 extern "C" {
 #endif
 
-#define LF_ABI_VERSION 1
+#define LF_ABI_VERSION 2
 
 typedef struct lf_cache lf_cache; /* opaque; owns the slab */
 
@@ -72,6 +95,18 @@ typedef enum lf_kernel {
   LF_KERNEL_TENSOR_CORE = 2  /* tcgen05 MMAs: bf16, head_dim 128, group 1/2/4/8 */
 } lf_kernel;
 
+/* How slots are scored for eviction. */
+typedef enum lf_score {
+  LF_SCORE_LONGFLOW = 0, /* alpha_i * ||v_i|| over the current step's weights */
+  LF_SCORE_H2O = 1       /* cumulative attention mass (one fp32 accumulator per slot) */
+} lf_score;
+
+/* Which heads share one eviction decision. */
+typedef enum lf_scope {
+  LF_SCOPE_KV_HEAD = 0, /* every KV head evicts its own slot (scores summed over its group) */
+  LF_SCOPE_LAYER = 1    /* one slot per (layer, sequence), scores summed over all heads */
+} lf_scope;
+
 /* Bits of the device error word (lf_cache_check). */
 #define LF_DEVERR_NONFINITE 1 /* a softmax max/denominator was not finite */
 #define LF_DEVERR_STATE 2     /* no eviction candidate / count out of range */
@@ -86,6 +121,14 @@ typedef struct lf_config {
   int cluster;            /* CTAs that split one KV head's slots (1,2,4,8,16); 0 = auto */
   int stages;             /* depth of the shared-memory staging ring (2..16); 0 = auto */
   int kernel;             /* lf_kernel; LF_KERNEL_AUTO by default */
+  /* Policy variants (see the top of the file); 0 everywhere is the default method.
+   * Ignored when evict = 0, except norm, which sets what vnorm holds. */
+  int score;              /* lf_score */
+  int norm;               /* 1 (or 0) = ||v||_1, 2 = ||v||_2 */
+  int sinks;              /* >= 0; window + sinks < every budget */
+  int deferred;           /* 0 = victim chosen and overwritten in the same step,
+                             1 = chosen now, overwritten by the next token (window >= 1) */
+  int scope;              /* lf_scope */
 } lf_config;
 
 /*
@@ -93,7 +136,8 @@ typedef struct lf_config {
  * kv_heads KV heads of dimension head_dim, q_heads query heads (a multiple of
  * kv_heads), `budget` slots per (layer, sequence, KV head) and a protected
  * window of the `window` most recent positions (0 <= window < budget).
- * Storage is bf16, eviction on.  Returns NULL on error (see lf_last_error).
+ * Storage is bf16, eviction on, the default policy.  Returns NULL on error (see
+ * lf_last_error).
  * Supported: head_dim in {16, 32, 64, 128}; q_heads / kv_heads in {1, 2, 4, 8}.
  */
 lf_cache* lf_cache_create(int layers, int batch, int kv_heads, int q_heads, int head_dim,
@@ -101,7 +145,10 @@ lf_cache* lf_cache_create(int layers, int batch, int kv_heads, int q_heads, int 
 
 /* Same with explicit dtype / eviction mode / ragged budgets / launch shape.
  * `capacity` is the slot count of every slab unit (the largest budget when
- * evicting; the full-KV length when not).  cfg may be NULL (bf16, evict). */
+ * evicting; the full-KV length when not).  cfg may be NULL (bf16, evict, the
+ * default policy).  The H2O score adds one fp32 per slot, the deferred mode one
+ * int32 per unit and the layer scope a one-layer scratch of one fp32 per slot;
+ * all are allocated here. */
 lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, int head_dim,
                              int capacity, int window, const lf_config* cfg);
 
@@ -111,14 +158,17 @@ int lf_cache_destroy(lf_cache* cache);
 /*
  * Initial fill of one layer (guide, "Static Memory Pre-Allocation and
  * In-Place Eviction", step 1): sequence b's first prompt_len[b] tokens take
- * slots 0..prompt_len[b]-1 with positions 0..prompt_len[b]-1; ||v||_1 is
- * computed in fp32 from the stored values; the occupied count and the next
- * position become prompt_len[b].  Slots past the prompt are marked empty.
+ * slots 0..prompt_len[b]-1 with positions 0..prompt_len[b]-1; ||v||_1 (||v||_2
+ * with norm 2) is computed in fp32 from the stored values; the occupied count
+ * and the next position become prompt_len[b].  Slots past the prompt are
+ * marked empty.  H2O accumulators start at 0; no deferred victim is chosen.
  *   k, v        device, [batch][kv_heads][max_prompt][head_dim], cache dtype,
  *               contiguous, 16-byte aligned, caller-owned
  *   prompt_len  HOST [batch], 0 <= prompt_len[b] <= max_prompt and <= that
- *               sequence's budget (capacity when eviction is off); longer
- *               prompts are fed through lf_decode_step by the caller
+ *               sequence's budget (capacity when eviction is off; below the
+ *               budget in deferred mode, so that the step which fills the
+ *               buffer chooses the first victim); longer prompts are fed
+ *               through lf_decode_step by the caller
  * The host lengths are uploaded before the call returns.  Stream-ordered.
  */
 int lf_prefill_fill(lf_cache* cache, int layer, const void* k, const void* v,
@@ -131,10 +181,13 @@ int lf_prefill_fill(lf_cache* cache, int layer, const void* k, const void* v,
  *   q             [batch][q_heads][head_dim]   cache dtype
  *   k_new, v_new  [batch][kv_heads][head_dim]  cache dtype (the token's stored values)
  *   out           [batch][q_heads][head_dim]   cache dtype (fp32 accumulation, RNE rounding)
- *   evicted_slot  [batch][kv_heads] int32: the slot overwritten, or -1 in the fill
- *                 phase and in eviction-off mode
+ *   evicted_slot  [batch][kv_heads] int32: the slot whose token left the buffer this
+ *                 step (and took the new token), or -1 in the fill phase and in
+ *                 eviction-off mode
  * Asynchronous; no host synchronisation; allocates nothing; capturable in a
  * CUDA graph.  Returns LF_ERR_ARG / LF_ERR_CUDA on a bad call or launch.
+ * With the layer scope a step is two launches (the attention kernel, then a
+ * per-sequence selection of the shared victim).
  */
 int lf_decode_step(lf_cache* cache, int layer, const void* q, const void* k_new,
                    const void* v_new, void* out, int32_t* evicted_slot, lf_stream_t stream);
@@ -158,12 +211,17 @@ typedef struct lf_layout {
   int kernel;          /* LF_KERNEL_SIMT or LF_KERNEL_TENSOR_CORE */
   void* k;          /* cache dtype */
   void* v;          /* cache dtype */
-  float* vnorm;     /* fp32 ||v||_1 of each slot, written at insert */
+  float* vnorm;     /* fp32 ||v||_1 (||v||_2 with norm 2) of each slot, written at insert */
   int32_t* pos;     /* token position of each slot, -1 when empty */
   int32_t* count;   /* occupied slots */
   int32_t* next_pos;/* position of the next token */
   int32_t* budget;  /* per-sequence budget */
   int32_t* err;     /* device error word */
+  int score, norm, sinks, deferred, scope; /* the policy (lf_config) */
+  float* acc;       /* LF_SCORE_H2O: fp32 attention mass per slot (same index as
+                       vnorm), else NULL */
+  int32_t* pending; /* deferred: the slot the next token takes, per unit (same index
+                       as count; -1 = none chosen), else NULL */
 } lf_layout;
 
 int lf_cache_layout(const lf_cache* cache, lf_layout* out);
@@ -178,8 +236,9 @@ int lf_cache_layout(const lf_cache* cache, lf_layout* out);
  * synchronisation is not allowed, or a runtime without access to the CUDA
  * allocator.  Such a caller owns the slab itself and describes it with an
  * lf_layout (k, v, vnorm, pos, count, next_pos, and layers, batch, kv_heads,
- * head_dim, capacity, slot_stride, dtype; the other fields are ignored), laid
- * out exactly as lf_cache_layout documents.  The operation, argument meaning
+ * head_dim, capacity, slot_stride, dtype, norm; acc and pending when not
+ * NULL; the other fields are ignored), laid out exactly as lf_cache_layout
+ * documents.  The operation, argument meaning
  * and error behaviour are those of lf_prefill_fill, except that prompt
  * lengths are checked against `capacity` (the caller keeps its budgets).
  *

@@ -15,7 +15,14 @@ Comparison rules:
 * outputs: fp32 storage -- |x - y| <= 1e-5 * max(|y|, max |y| of that head);
   bf16 storage -- |x - y| <= 2e-2 + 1e-2 |y| (fp32 accumulation on the GPU);
 * after the run, every sampled unit's slab state equals the oracle's: K, V and
-  positions exactly, ||v||_1 to fp32 rounding, count and next position.
+  positions exactly, ||v||_1 to fp32 rounding, count and next position; with
+  the H2O score the accumulators to fp32 accumulation (rtol 1e-4), and when
+  deferred the chosen slot exactly.
+
+Policy variants: with the deferred order the slot chosen at a step is compared
+through the cache's `pending` state (near-tie rule as above) and the slot the
+step overwrote exactly; with the layer scope the oracle replays every KV head of
+a sampled sequence as one group sharing one victim.
 """
 from __future__ import annotations
 
@@ -73,25 +80,42 @@ class ParityRun:
     def __init__(self, wl: Workload, layers: Sequence[int] = (0,), seed: int = 0,
                  sample: Optional[Sequence[Tuple[int, int, int]]] = None, cluster: int = 0,
                  stages: int = 0, evict: bool = True, capacity: Optional[int] = None,
-                 budgets: Optional[Sequence[int]] = None, device="cuda", kernel: str = "auto"):
+                 budgets: Optional[Sequence[int]] = None, device="cuda", kernel: str = "auto",
+                 policy: Optional["oracle.Policy"] = None):
         self.wl = wl
         self.layers = list(layers)
+        self.policy = pol = policy or oracle.Policy()
         self.stream = InputStream(wl, seed=seed, device=device, layers=self.layers)
         self.budgets = list(budgets) if budgets is not None else list(self.stream.budgets)
         cap = capacity if capacity is not None else max(self.budgets)
         self.capacity = cap
         self.evict = evict
+        self.deferred = evict and pol.deferred
+        self.h2o = evict and pol.score == "h2o"
         self.G = wl.q_heads // wl.kv_heads
         self.cache = LFCache(len(self.layers), wl.batch, wl.kv_heads, wl.q_heads, wl.head_dim,
                              cap, wl.window, dtype=wl.dtype, evict=evict,
                              budgets=self.budgets if evict else None, cluster=cluster,
-                             stages=stages, kernel=kernel)
+                             stages=stages, kernel=kernel, score=pol.score, norm=pol.norm,
+                             sinks=pol.sinks, deferred=pol.deferred, scope=pol.scope)
         if sample is None:
             sample = [(li, b, g) for li in range(len(self.layers)) for b in range(wl.batch)
                       for g in range(wl.kv_heads)]
-        self.sample = list(sample)
+        layer_scope = evict and pol.scope == "layer"
+        if layer_scope:   # a sampled sequence brings all its KV heads
+            sample = [(li, b, g) for (li, b) in sorted({(x[0], x[1]) for x in sample})
+                      for g in range(wl.kv_heads)]
+        self.sample = sorted(set(sample))
+        self.groups = {}
+        for (li, b, g) in self.sample:
+            self.groups.setdefault((li, b) if layer_scope else (li, b, g), []).append((li, b, g))
         self.units = {}
-        limit = lambda b: self.budgets[b] if evict else cap
+
+        def limit(b):
+            if not evict:
+                return cap
+            return self.budgets[b] - (1 if self.deferred else 0)
+
         for li, l in enumerate(self.layers):
             k, v, lens = self.stream.prompt(l)
             lens = [min(P, limit(b)) for b, P in enumerate(lens)]
@@ -100,7 +124,7 @@ class ParityRun:
                 if sli != li:
                     continue
                 u = oracle.OracleUnit(cap, wl.head_dim, self.budgets[b] if evict else cap,
-                                      wl.window, evict)
+                                      wl.window, evict, pol)
                 P = lens[b]
                 u.prefill(to64(k[b, g, :P]), to64(v[b, g, :P]))
                 self.units[(li, b, g)] = u
@@ -112,23 +136,36 @@ class ParityRun:
                    for _ in self.layers]
         self.views = self.cache.views()
         self.stats = ParityStats()
-        self._pos_before = {}
 
     def close(self):
         self.cache.close()
 
-    def _was_candidate(self, li, b, g, slot, u: oracle.OracleUnit) -> bool:
-        # u has already advanced one step: its p is the new token's position + 1
-        return bool(self._pos_before[(li, b, g)][slot] < (u.p - 1) - self.wl.window)
-
-    def _resync(self, li, b, g, u: oracle.OracleUnit):
+    def _resync(self, members):
+        """Write the oracle's state of these units over the GPU's."""
         vw = self.views
         dt = self.cache.dtype
         cap = self.capacity
-        vw["k"][li, b, g, :cap] = torch.from_numpy(u.K).to(dt).to(vw["k"].device)
-        vw["v"][li, b, g, :cap] = torch.from_numpy(u.V).to(dt).to(vw["v"].device)
-        vw["vnorm"][li, b, g, :cap] = torch.from_numpy(u.vnorm).to(torch.float32).to(vw["k"].device)
-        vw["pos"][li, b, g, :cap] = torch.from_numpy(u.pos).to(torch.int32).to(vw["k"].device)
+        for (li, b, g) in members:
+            u = self.units[(li, b, g)]
+            dev = vw["k"].device
+            vw["k"][li, b, g, :cap] = torch.from_numpy(u.K).to(dt).to(dev)
+            vw["v"][li, b, g, :cap] = torch.from_numpy(u.V).to(dt).to(dev)
+            vw["vnorm"][li, b, g, :cap] = torch.from_numpy(u.vnorm).to(torch.float32).to(dev)
+            vw["pos"][li, b, g, :cap] = torch.from_numpy(u.pos).to(torch.int32).to(dev)
+            if self.h2o:
+                vw["acc"][li, b, g, :cap] = torch.from_numpy(u.acc).to(torch.float32).to(dev)
+            if self.deferred:
+                vw["pending"][li, b, g] = int(u.pending)
+
+    def _candidate(self, u: oracle.OracleUnit, pos_before, slot: int) -> bool:
+        """Was `slot` a candidate at the step the oracle unit just took?"""
+        pol, W = self.policy, self.wl.window
+        p = u.p - 1                     # the step's token position
+        if self.deferred:               # after the write; the window counts the new token
+            ps = u.pos[slot]
+            return bool(pol.sinks <= ps < p + 1 - W)
+        ps = pos_before[slot]
+        return bool(pol.sinks <= ps < p - W)
 
     def step(self, check: bool = True):
         qs, ks, vs = self.stream.next_step()
@@ -148,37 +185,49 @@ class ParityRun:
             gi = torch.tensor([g for _, g in idx], device=qs[li].device)
             qg = qs[li].view(self.wl.batch, self.wl.kv_heads, G, self.wl.head_dim)[bi, gi]
             og = self.out[li].view(self.wl.batch, self.wl.kv_heads, G, self.wl.head_dim)[bi, gi]
-            host[li] = (idx, to64(qg), to64(ks[li][bi, gi]), to64(vs[li][bi, gi]), to64(og),
-                        self.ev[li][bi, gi].cpu().numpy())
-        for li, (idx, q, k, v, o, ev) in host.items():
-            for j, (b, g) in enumerate(idx):
-                u = self.units[(li, b, g)]
-                self._pos_before[(li, b, g)] = u.pos.copy()
-                r = u.step(q[j], k[j], v[j])
-                self.stats.unit_steps += 1
+            pend = (self.views["pending"][li][bi, gi].cpu().numpy() if self.deferred else None)
+            host[li] = ({bg: j for j, bg in enumerate(idx)}, to64(qg), to64(ks[li][bi, gi]),
+                        to64(vs[li][bi, gi]), to64(og), self.ev[li][bi, gi].cpu().numpy(), pend)
+        for key, members in self.groups.items():
+            li = members[0][0]
+            jmap, q, k, v, o, ev, pend = host[li]
+            js = [jmap[(b, g)] for (_, b, g) in members]
+            units = [self.units[m] for m in members]
+            pos_before = [u.pos.copy() for u in units]
+            res = oracle.group_step(units, [q[j] for j in js], [k[j] for j in js],
+                                    [v[j] for j in js])
+            self.stats.unit_steps += len(units)
+            for m, j, r in zip(members, js, res):
                 viol = out_violation(o[j], r.out, self.wl.dtype)
                 if viol > self.stats.max_out_violation:
                     self.stats.max_out_violation = viol
-                    self.stats.worst_out = (self.stats.steps, li, b, g, viol)
-                if r.evicted >= 0:
-                    self.stats.evictions += 1
-                near = (r.rel_gap <= NEAR_TIE) or (r.evicted >= 0 and r.second < TINY_SCORE)
-                if near:
-                    self.stats.near_ties += 1
-                e_gpu = int(ev[j])
-                if e_gpu != r.evicted:
-                    # A different pick is acceptable only at a near-tie, and only
-                    # if the GPU's slot was a candidate within the tie band.
-                    ok_pick = (near and r.scores is not None and 0 <= e_gpu < len(r.scores)
-                               and self._was_candidate(li, b, g, e_gpu, u)
-                               and r.scores[e_gpu] <= r.lowest * (1 + 2 * NEAR_TIE) + TINY_SCORE)
-                    if ok_pick:
-                        self.stats.resyncs += 1
-                        self._resync(li, b, g, u)
-                    else:
+                    self.stats.worst_out = (self.stats.steps,) + m + (viol,)
+            r0 = res[0]
+            if r0.evicted >= 0:
+                self.stats.evictions += len(units)
+            # The slot the GPU chose this step (same step: the one it overwrote;
+            # deferred: its pending choice), and what the step overwrote.
+            gpu_chosen = [int(pend[j]) if self.deferred else int(ev[j]) for j in js]
+            if self.deferred:
+                for m, j, r in zip(members, js, res):
+                    if int(ev[j]) != r.evicted:
                         self.stats.hard_mismatches.append(
-                            (self.stats.steps, li, b, g, e_gpu, r.evicted, r.rel_gap))
-                        self._resync(li, b, g, u)
+                            (self.stats.steps,) + m + (int(ev[j]), r.evicted, "overwritten"))
+            near = (r0.rel_gap <= NEAR_TIE) or (r0.chosen >= 0 and r0.second < TINY_SCORE)
+            if near:
+                self.stats.near_ties += 1
+            if any(c != r0.chosen for c in gpu_chosen):
+                e_gpu = gpu_chosen[0]
+                ok_pick = (near and r0.scores is not None and all(c == e_gpu for c in gpu_chosen)
+                           and 0 <= e_gpu < len(r0.scores)
+                           and self._candidate(units[0], pos_before[0], e_gpu)
+                           and r0.scores[e_gpu] <= r0.lowest * (1 + 2 * NEAR_TIE) + TINY_SCORE)
+                if ok_pick:
+                    self.stats.resyncs += 1
+                else:
+                    self.stats.hard_mismatches.append(
+                        (self.stats.steps,) + members[0] + (e_gpu, r0.chosen, r0.rel_gap))
+                self._resync(members)
 
     def run(self, steps: int, check_every: int = 1) -> ParityStats:
         for t in range(steps):
@@ -189,7 +238,6 @@ class ParityRun:
     def compare_state(self):
         """Sampled units' slab state against the oracle's."""
         vw = self.views
-        cap = self.capacity
         for (li, b, g), u in self.units.items():
             n = u.n
             k = to64(vw["k"][li, b, g, :n])
@@ -207,18 +255,29 @@ class ParityRun:
             if not (np.array_equal(k, u.K[:n]) and np.array_equal(v, u.V[:n])):
                 self.stats.state_errors.append(f"{tag}: K/V differ")
             if not np.allclose(vn, u.vnorm[:n], rtol=2e-6, atol=1e-6):
-                self.stats.state_errors.append(f"{tag}: ||v||_1 differs "
+                self.stats.state_errors.append(f"{tag}: ||v|| differs "
                                                f"{np.abs(vn - u.vnorm[:n]).max()}")
+            if self.h2o:
+                acc = vw["acc"][li, b, g, :n].cpu().numpy().astype(np.float64)
+                if not np.allclose(acc, u.acc[:n], rtol=1e-4, atol=1e-7):
+                    self.stats.state_errors.append(f"{tag}: H2O accumulators differ "
+                                                   f"{np.abs(acc - u.acc[:n]).max()}")
+            if self.deferred and int(vw["pending"][li, b, g]) != u.pending:
+                self.stats.state_errors.append(
+                    f"{tag}: pending {int(vw['pending'][li, b, g])} vs {u.pending}")
         return self.stats
 
     def check_invariants(self):
         """Every unit (sampled or not): count within its buffer, the occupied
-        positions unique, and the W most recent positions present."""
+        positions unique, the W most recent positions and the sinks present,
+        the deferred choice outside both; with the layer scope every KV head of
+        a sequence holds the same positions."""
         vw = self.views
         cnt = vw["count"].cpu().numpy()
         nxt = vw["next_pos"].cpu().numpy()
         pos = vw["pos"].cpu().numpy()
-        W = self.wl.window
+        pend = vw["pending"].cpu().numpy() if self.deferred else None
+        W, S = self.wl.window, self.policy.sinks
         for li in range(len(self.layers)):
             for b in range(self.wl.batch):
                 lim = self.budgets[b] if self.evict else self.capacity
@@ -234,4 +293,13 @@ class ParityRun:
                         recent = np.arange(max(0, p - W), p)
                         if not np.isin(recent, live).all():
                             self.stats.state_errors.append(f"({li},{b},{g}): window lost")
+                        if not np.isin(np.arange(min(S, p)), live).all():
+                            self.stats.state_errors.append(f"({li},{b},{g}): sink lost")
+                    if self.deferred and n == lim:
+                        e = int(pend[li, b, g])
+                        if not (0 <= e < n and S <= pos[li, b, g, e] < p - W):
+                            self.stats.state_errors.append(f"({li},{b},{g}): bad pending {e}")
+                    if self.evict and self.policy.scope == "layer" and g > 0:
+                        if not np.array_equal(live, pos[li, b, 0, :n]):
+                            self.stats.state_errors.append(f"({li},{b}): heads disagree")
         return self.stats

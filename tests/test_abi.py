@@ -49,7 +49,8 @@ def test_constants_match_header():
     text = _header()
     for name in ["LF_OK", "LF_ERR_ARG", "LF_ERR_OOM", "LF_ERR_CUDA", "LF_ERR_DEVICE",
                  "LF_ERR_UNSUPPORTED", "LF_BF16", "LF_F32", "LF_KERNEL_AUTO", "LF_KERNEL_SIMT",
-                 "LF_KERNEL_TENSOR_CORE"]:
+                 "LF_KERNEL_TENSOR_CORE", "LF_SCORE_LONGFLOW", "LF_SCORE_H2O", "LF_SCOPE_KV_HEAD",
+                 "LF_SCOPE_LAYER"]:
         m = re.search(rf"\b{name}\s*=\s*(-?\d+)", text)
         assert m and int(m.group(1)) == getattr(lf, name), name
     for name in ["LF_DEVERR_NONFINITE", "LF_DEVERR_STATE", "LF_DEVERR_TIMEOUT"]:
@@ -94,7 +95,7 @@ def test_header_is_plain_c_and_structs_match_binding(tmp_path):
     ((1, 1, 1, 1, 128, 64, -1), "window >= 0"),
     ((1, 1, 8, 32, 96, 64, 4), "no kernel for head_dim 96"),
     ((1, 1, 2, 6, 128, 64, 4), "group size 3"),
-    ((1, 1, 1, 1, 128, 8, 8), "window (8) must be smaller"),
+    ((1, 1, 1, 1, 128, 8, 8), "window + sinks (8 + 0) must be smaller"),
 ])
 def test_argument_errors_need_no_gpu(lib, args, msg):
     h = lib.lf_cache_create(*args)
@@ -111,6 +112,24 @@ def test_bad_config_fields(lib):
         lf.lf_cache_create_ex(1, 2, 1, 1, 128, 64, 4, budgets=[64, 65])
     with pytest.raises(lf.LFError, match="window"):
         lf.lf_cache_create_ex(1, 2, 1, 1, 128, 64, 8, budgets=[64, 8])
+
+
+def test_bad_policy_fields(lib):
+    """The policy variants are checked on the host before any CUDA call."""
+    with pytest.raises(lf.LFError, match="policy"):
+        lf.lf_cache_create_ex(1, 1, 1, 1, 128, 64, 4, score=2)
+    with pytest.raises(lf.LFError, match="policy"):
+        lf.lf_cache_create_ex(1, 1, 1, 1, 128, 64, 4, norm=3)
+    with pytest.raises(lf.LFError, match="policy"):
+        lf.lf_cache_create_ex(1, 1, 1, 1, 128, 64, 4, sinks=-1)
+    with pytest.raises(lf.LFError, match="policy"):
+        lf.lf_cache_create_ex(1, 1, 1, 1, 128, 64, 4, scope=5)
+    # the window and the sinks together must leave a candidate in every buffer
+    with pytest.raises(lf.LFError, match=r"window \+ sinks \(4 \+ 4\)"):
+        lf.lf_cache_create_ex(1, 2, 1, 1, 128, 64, 4, budgets=[64, 8], sinks=4)
+    # deferred eviction protects the new token through the window
+    with pytest.raises(lf.LFError, match="window >= 1"):
+        lf.lf_cache_create_ex(1, 1, 1, 1, 128, 64, 0, deferred=True)
 
 
 def test_null_handles(lib):
