@@ -19,7 +19,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "liblongflow.so")
 
-SOURCES = ["lf_api.cu", "lf_inst_bf16.cu", "lf_inst_f32.cu", "lf_inst_tc.cu", "lf_noalloc.cu"]
+SOURCES = ["lf_api.cu", "lf_inst_bf16.cu", "lf_inst_f32.cu", "lf_inst_tc.cu", "lf_noalloc.cu",
+           "lf_rkv.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 

@@ -15,12 +15,16 @@
 
 #include "lf_decode_tc.cuh"
 #include "lf_kernels.h"
+#include "lf_rkv.h"
 #include "longflow.h"
 
 struct lf_cache {
   int layers, batch, kv_heads, q_heads, head_dim, capacity, slot_stride, window;
   int dtype, evict, cluster, stages, chunk, smem, device;
-  int score, norm, sinks, deferred, scope;  // the policy (zero when eviction is off, but norm)
+  int score, norm, sinks, deferred, scope;  // the policy (zero unless LongFlow eviction, but norm)
+  int kevict;     // what the decode kernels do: 1 LongFlow eviction, 0 append (off and R-KV)
+  int rkv_buffer, rkv_alpha, rkv_beta;      // R-KV parameters (evict = LF_EVICT_RKV)
+  float rkv_lambda, rkv_tau;
   int items;      // tensor-core path: units one cluster may visit per launch
   size_t elem_bytes;
   void* K;
@@ -147,7 +151,7 @@ lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, i
                              int capacity, int window, const lf_config* cfg) {
   g_last_error.clear();
   lf_config def = {LF_BF16, 1, nullptr, 0, 0, LF_KERNEL_AUTO, LF_SCORE_LONGFLOW, 1, 0, 0,
-                   LF_SCOPE_KV_HEAD};
+                   LF_SCOPE_KV_HEAD, 0, 0, 0, 0.f, 0.f};
   lf_config c = cfg ? *cfg : def;
   if (layers < 1 || batch < 1 || kv_heads < 1 || q_heads < 1 || capacity < 1 || window < 0) {
     fail(LF_ERR_ARG, "layers, batch, heads and capacity must be >= 1 and window >= 0");
@@ -165,10 +169,11 @@ lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, i
     fail(LF_ERR_ARG, "dtype must be LF_BF16 or LF_F32");
     return nullptr;
   }
-  if (c.evict != 0 && c.evict != 1) {
-    fail(LF_ERR_ARG, "evict must be 0 or 1");
+  if (c.evict < LF_EVICT_OFF || c.evict > LF_EVICT_RKV) {
+    fail(LF_ERR_ARG, "evict must be LF_EVICT_OFF, LF_EVICT_LONGFLOW or LF_EVICT_RKV");
     return nullptr;
   }
+  const bool rkv = c.evict == LF_EVICT_RKV;
   if (c.cluster != 0 && (c.cluster < 1 || c.cluster > lf::kMaxCluster ||
                          (c.cluster & (c.cluster - 1)) != 0)) {
     fail(LF_ERR_ARG, "cluster must be 0 (auto) or a power of two <= %d", lf::kMaxCluster);
@@ -190,10 +195,34 @@ lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, i
          "sinks >= 0, deferred 0 or 1, scope LF_SCOPE_KV_HEAD or LF_SCOPE_LAYER");
     return nullptr;
   }
-  if (!c.evict) {  // nothing is ever evicted: the policy has nothing to decide
+  if (c.evict != LF_EVICT_LONGFLOW) {  // no LongFlow eviction: the policy has nothing to decide
     c.score = LF_SCORE_LONGFLOW;
     c.sinks = c.deferred = 0;
     c.scope = LF_SCOPE_KV_HEAD;
+  }
+  const int kevict = (c.evict == LF_EVICT_LONGFLOW) ? 1 : 0;
+  if (rkv) {  // the README's defaults, then the limits of the compression kernel
+    if (c.rkv_buffer == 0) c.rkv_buffer = 128;
+    if (c.rkv_alpha == 0) c.rkv_alpha = 8;
+    if (c.rkv_beta == 0) c.rkv_beta = 1;
+    if (c.rkv_lambda == 0.f) c.rkv_lambda = 0.1f;
+    if (c.rkv_tau == 0.f) c.rkv_tau = 0.9f;
+    const int grp = q_heads / kv_heads;
+    if (c.dtype != LF_BF16 || head_dim != 128 || (grp != 1 && grp != 2 && grp != 4 && grp != 8)) {
+      fail(LF_ERR_UNSUPPORTED, "R-KV compression is built for bf16, head_dim 128, group 1/2/4/8");
+      return nullptr;
+    }
+    if (c.budgets) {
+      fail(LF_ERR_ARG, "R-KV takes no per-sequence budgets");
+      return nullptr;
+    }
+    if (capacity > lf::kRkvMaxSlots || c.rkv_buffer < 1 || c.rkv_alpha < 1 || c.rkv_beta < 1 ||
+        capacity - c.rkv_buffer <= c.rkv_alpha || c.rkv_alpha * grp > 64 ||
+        !(c.rkv_lambda > 0.f && c.rkv_lambda <= 1.f) || !(c.rkv_tau > 0.f && c.rkv_tau <= 1.f)) {
+      fail(LF_ERR_ARG, "R-KV: need capacity <= %d, buffer >= 1, alpha < capacity - buffer, "
+           "alpha * group <= 64, beta >= 1, lambda and tau in (0, 1]", lf::kRkvMaxSlots);
+      return nullptr;
+    }
   }
   const int group = q_heads / kv_heads;
   lf::KernelEntry kern;
@@ -224,12 +253,12 @@ lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, i
       min_budget = std::min(min_budget, (int)c.budgets[b]);
     }
   }
-  if (c.evict && window + c.sinks >= min_budget) {
+  if (kevict && window + c.sinks >= min_budget) {
     fail(LF_ERR_ARG, "window + sinks (%d + %d) must be smaller than every budget (min %d)", window,
          c.sinks, min_budget);
     return nullptr;
   }
-  if (c.evict && c.deferred && window < 1) {
+  if (kevict && c.deferred && window < 1) {
     fail(LF_ERR_ARG, "deferred eviction needs window >= 1 (the new token is protected)");
     return nullptr;
   }
@@ -289,7 +318,7 @@ lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, i
       const int most = std::max(1, num_sms / cluster);
       items = (units + most - 1) / most;
       for (int pass = 0; pass < 4; ++pass) {
-        smem = kern.smem_bytes(stages, chunk, cluster, c.evict, items);
+        smem = kern.smem_bytes(stages, chunk, cluster, kevict, items);
         // The tensor-core kernel takes all of an SM's tensor memory: ask for more
         // than half of its shared memory so that never two CTAs share an SM.
         smem = std::max(smem, max_sm_smem / 2 + 1024);
@@ -303,7 +332,7 @@ lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, i
       }
       if (fits > 0 && items > lf::kTcMaxItems) fits = 0;
     } else {
-      smem = kern.smem_bytes(stages, chunk, cluster, c.evict, 0);
+      smem = kern.smem_bytes(stages, chunk, cluster, kevict, 0);
       if (smem <= max_optin)
         fits = active_clusters(kern.decode, cluster, kv_heads, batch, smem, threads);
     }
@@ -331,6 +360,12 @@ lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, i
   cache->window = window;
   cache->dtype = c.dtype;
   cache->evict = c.evict;
+  cache->kevict = kevict;
+  cache->rkv_buffer = c.rkv_buffer;
+  cache->rkv_alpha = c.rkv_alpha;
+  cache->rkv_beta = c.rkv_beta;
+  cache->rkv_lambda = c.rkv_lambda;
+  cache->rkv_tau = c.rkv_tau;
   cache->cluster = cluster;
   cache->stages = stages;
   cache->chunk = chunk;
@@ -400,7 +435,8 @@ lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, i
     delete cache;
     return nullptr;
   }
-  for (int b = 0; b < batch; ++b) hb[b] = c.budgets ? c.budgets[b] : capacity;
+  for (int b = 0; b < batch; ++b)
+    hb[b] = c.budgets ? c.budgets[b] : (rkv ? capacity - c.rkv_buffer : capacity);
   if ((e = cudaMemset(cache->small, 0, small_bytes)) != cudaSuccess ||
       (e = cudaMemset(cache->pos, 0xff, n_slots * 4)) != cudaSuccess ||
       (cache->pending && (e = cudaMemset(cache->pending, 0xff, n_units * 4)) != cudaSuccess) ||
@@ -416,7 +452,17 @@ lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, i
     return nullptr;
   }
   delete[] hb;
-  if (tc) {
+  if (rkv) {
+    e = cudaFuncSetAttribute(lf::find_rkv_kernel(group), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             lf::rkv_smem_bytes());
+    if (e != cudaSuccess) {
+      cuda_fail(e, "cudaFuncSetAttribute (R-KV compression)");
+      destroy_memory(cache);
+      delete cache;
+      return nullptr;
+    }
+  }
+  if (tc || rkv) {
     const int code = encode_tensor_maps(cache, n_slots);
     if (code != LF_OK) {
       destroy_memory(cache);
@@ -461,7 +507,7 @@ int lf_prefill_fill(lf_cache* cache, int layer, const void* k, const void* v,
   }
   for (int b = 0; b < cache->batch; ++b) {
     // deferred: the step that fills the buffer chooses the first victim
-    const int limit = cache->evict ? hb[b] - (cache->deferred ? 1 : 0) : cache->capacity;
+    const int limit = cache->kevict ? hb[b] - (cache->deferred ? 1 : 0) : cache->capacity;
     if (prompt_len[b] > limit) {
       delete[] hb;
       return fail(LF_ERR_ARG, "prompt_len[%d] = %d exceeds the buffer (%d%s); feed the rest "
@@ -545,7 +591,8 @@ int lf_decode_step(lf_cache* cache, int layer, const void* q, const void* k_new,
   a.window = cache->window;
   a.chunk = cache->chunk;
   a.stages = cache->stages;
-  a.evict = cache->evict;
+  a.evict = cache->kevict;
+  a.strict = (cache->evict == LF_EVICT_RKV) ? 1 : 0;
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)cache->head_dim));
 
   cudaLaunchConfig_t cfg = {};
@@ -590,6 +637,43 @@ int lf_decode_step(lf_cache* cache, int layer, const void* q, const void* k_new,
                          args, 0, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "layer-scope selection launch");
   }
+  return LF_OK;
+}
+
+int lf_rkv_compress(lf_cache* cache, int layer, const void* q_obs, lf_stream_t stream) {
+  if (!cache) return fail(LF_ERR_ARG, "null cache");
+  if (cache->evict != LF_EVICT_RKV) return fail(LF_ERR_ARG, "not an R-KV cache (evict != LF_EVICT_RKV)");
+  if (layer < 0 || layer >= cache->layers)
+    return fail(LF_ERR_ARG, "layer %d outside [0, %d)", layer, cache->layers);
+  if (!q_obs || !aligned16(q_obs)) return fail(LF_ERR_ARG, "q_obs must be non-null and 16-byte aligned");
+  const int group = cache->q_heads / cache->kv_heads;
+  const size_t layer_units = (size_t)cache->batch * cache->kv_heads;
+  const size_t layer_slots = layer_units * cache->slot_stride;
+  lf::RkvArgs ra;
+  ra.kmap = cache->tmaps[0];
+  ra.q_obs = static_cast<const __nv_bfloat16*>(q_obs);
+  ra.K = static_cast<__nv_bfloat16*>(cache->K) + layer * layer_slots * cache->head_dim;
+  ra.V = static_cast<__nv_bfloat16*>(cache->V) + layer * layer_slots * cache->head_dim;
+  ra.vnorm = cache->vnorm + layer * layer_slots;
+  ra.pos = cache->pos + layer * layer_slots;
+  ra.count = cache->count + layer * layer_units;
+  ra.next_pos = cache->next_pos + layer * layer_units;
+  ra.err = cache->err;
+  ra.kv_heads = cache->kv_heads;
+  ra.q_heads = cache->q_heads;
+  ra.slot_stride = cache->slot_stride;
+  ra.budget = cache->capacity - cache->rkv_buffer;
+  ra.alpha = cache->rkv_alpha;
+  ra.beta = cache->rkv_beta;
+  ra.row_base = (int)(layer * layer_slots);
+  ra.lam = cache->rkv_lambda;
+  ra.tau = cache->rkv_tau;
+  ra.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)cache->head_dim));
+  void* args[] = {&ra};
+  cudaError_t e = cudaLaunchKernel(lf::find_rkv_kernel(group), dim3((unsigned)layer_units, 1, 1),
+                                   dim3(256, 1, 1), args, lf::rkv_smem_bytes(),
+                                   static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "R-KV compression launch");
   return LF_OK;
 }
 
@@ -642,6 +726,11 @@ int lf_cache_layout(const lf_cache* cache, lf_layout* out) {
   out->scope = cache->scope;
   out->acc = cache->acc;
   out->pending = cache->pending;
+  out->rkv_buffer = cache->rkv_buffer;
+  out->rkv_alpha = cache->rkv_alpha;
+  out->rkv_beta = cache->rkv_beta;
+  out->rkv_lambda = cache->rkv_lambda;
+  out->rkv_tau = cache->rkv_tau;
   return LF_OK;
 }
 

@@ -61,6 +61,7 @@ struct DecodeArgs {
   float* lw_anew;      // layer scope: [batch][kv_heads] the new token's attention mass
   int batch, kv_heads, q_heads, slot_stride, capacity, window, chunk, stages, evict;
   int score, norm, sinks, deferred, scope;  // the policy (lf_config)
+  int strict;          // a step on a full slab is an error (R-KV: compress first)
   float scale_log2;    // log2(e) / sqrt(D)
 };
 
@@ -153,6 +154,7 @@ __device__ __forceinline__ LeaderOut leader_decide(const DecodeArgs& a, int unit
     slot = evicted = layer ? -1 : chosen;  // layer scope: the selection kernel writes
   } else {
     slot = (n < (a.evict ? bud : a.capacity)) ? n : -1;
+    if (slot < 0 && a.strict && state_ok && !any_fail) atomicOr(a.err, LF_DEVERR_STATE);
   }
   if (!state_ok) atomicOr(a.err, LF_DEVERR_STATE);
   if (any_fail || !state_ok) slot = evicted = -1;

@@ -32,6 +32,8 @@ LF_OK, LF_ERR_ARG, LF_ERR_OOM, LF_ERR_CUDA, LF_ERR_DEVICE, LF_ERR_UNSUPPORTED = 
 LF_BF16, LF_F32 = 0, 1
 LF_KERNEL_AUTO, LF_KERNEL_SIMT, LF_KERNEL_TENSOR_CORE = 0, 1, 2
 _KERNEL = {"auto": LF_KERNEL_AUTO, "simt": LF_KERNEL_SIMT, "tc": LF_KERNEL_TENSOR_CORE}
+LF_EVICT_OFF, LF_EVICT_LONGFLOW, LF_EVICT_RKV = 0, 1, 2
+_EVICT = {"off": LF_EVICT_OFF, "longflow": LF_EVICT_LONGFLOW, "rkv": LF_EVICT_RKV}
 LF_SCORE_LONGFLOW, LF_SCORE_H2O = 0, 1
 _SCORE = {"longflow": LF_SCORE_LONGFLOW, "h2o": LF_SCORE_H2O}
 LF_SCOPE_KV_HEAD, LF_SCOPE_LAYER = 0, 1
@@ -53,7 +55,9 @@ class LFConfig(ctypes.Structure):
                 ("budgets", ctypes.POINTER(ctypes.c_int32)), ("cluster", ctypes.c_int),
                 ("stages", ctypes.c_int), ("kernel", ctypes.c_int),
                 ("score", ctypes.c_int), ("norm", ctypes.c_int), ("sinks", ctypes.c_int),
-                ("deferred", ctypes.c_int), ("scope", ctypes.c_int)]
+                ("deferred", ctypes.c_int), ("scope", ctypes.c_int),
+                ("rkv_buffer", ctypes.c_int), ("rkv_alpha", ctypes.c_int), ("rkv_beta", ctypes.c_int),
+                ("rkv_lambda", ctypes.c_float), ("rkv_tau", ctypes.c_float)]
 
 
 class LFLayout(ctypes.Structure):
@@ -64,7 +68,9 @@ class LFLayout(ctypes.Structure):
         ("pos", ctypes.c_void_p), ("count", ctypes.c_void_p), ("next_pos", ctypes.c_void_p),
         ("budget", ctypes.c_void_p), ("err", ctypes.c_void_p)] + [
         (n, ctypes.c_int) for n in ("score", "norm", "sinks", "deferred", "scope")] + [
-        ("acc", ctypes.c_void_p), ("pending", ctypes.c_void_p)]
+        ("acc", ctypes.c_void_p), ("pending", ctypes.c_void_p)] + [
+        (n, ctypes.c_int) for n in ("rkv_buffer", "rkv_alpha", "rkv_beta")] + [
+        ("rkv_lambda", ctypes.c_float), ("rkv_tau", ctypes.c_float)]
 
 
 _lib: Optional[ctypes.CDLL] = None
@@ -104,6 +110,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.lf_last_error.argtypes = []
     lib.lf_abi_version.restype = I
     lib.lf_abi_version.argtypes = []
+    lib.lf_rkv_compress.restype = I
+    lib.lf_rkv_compress.argtypes = [P, I, VP, VP]
     lib.lf_prefill_fill_noalloc.restype = I
     lib.lf_prefill_fill_noalloc.argtypes = [ctypes.POINTER(LFLayout), I, VP, VP,
                                             ctypes.POINTER(ctypes.c_int32), I, VP]
@@ -153,10 +161,11 @@ def lf_cache_create(layers, batch, kv_heads, q_heads, head_dim, budget, window) 
 def lf_cache_create_ex(layers, batch, kv_heads, q_heads, head_dim, capacity, window,
                        dtype="bf16", evict=True, budgets: Optional[Sequence[int]] = None,
                        cluster=0, stages=0, kernel="auto", score="longflow", norm=1, sinks=0,
-                       deferred=False, scope="kv_head") -> int:
+                       deferred=False, scope="kv_head", rkv_buffer=0, rkv_alpha=0, rkv_beta=0,
+                       rkv_lambda=0.0, rkv_tau=0.0) -> int:
     cfg = LFConfig()
     cfg.dtype = _DTYPE[dtype] if isinstance(dtype, str) else int(dtype)
-    cfg.evict = int(bool(evict))
+    cfg.evict = _EVICT[evict] if isinstance(evict, str) else int(evict)
     arr = None
     if budgets is not None:
         arr = (ctypes.c_int32 * len(budgets))(*[int(x) for x in budgets])
@@ -169,6 +178,8 @@ def lf_cache_create_ex(layers, batch, kv_heads, q_heads, head_dim, capacity, win
     cfg.sinks = int(sinks)
     cfg.deferred = int(bool(deferred))
     cfg.scope = _SCOPE[scope] if isinstance(scope, str) else int(scope)
+    cfg.rkv_buffer, cfg.rkv_alpha, cfg.rkv_beta = int(rkv_buffer), int(rkv_alpha), int(rkv_beta)
+    cfg.rkv_lambda, cfg.rkv_tau = float(rkv_lambda), float(rkv_tau)
     h = load_library().lf_cache_create_ex(layers, batch, kv_heads, q_heads, head_dim, capacity,
                                           window, ctypes.byref(cfg))
     if not h:
@@ -207,6 +218,10 @@ def lf_prefill_fill_noalloc(dst: LFLayout, layer, k, v, prompt_len: Sequence[int
                                                          arr, int(max_prompt), _stream(stream)))
 
 
+def lf_rkv_compress(handle, layer, q_obs, stream=None) -> int:
+    return _check(load_library().lf_rkv_compress(handle, layer, _ptr(q_obs), _stream(stream)))
+
+
 def lf_cache_layout(handle) -> LFLayout:
     lay = LFLayout()
     _check(load_library().lf_cache_layout(handle, ctypes.byref(lay)))
@@ -234,18 +249,19 @@ class LFCache:
     def __init__(self, layers, batch, kv_heads, q_heads, head_dim, capacity, window,
                  dtype="bf16", evict=True, budgets=None, cluster=0, stages=0, kernel="auto",
                  device=None, score="longflow", norm=1, sinks=0, deferred=False,
-                 scope="kv_head"):
+                 scope="kv_head", **rkv):
         self.device = torch.device("cuda", torch.cuda.current_device() if device is None
                                    else torch.device(device).index or 0)
         with torch.cuda.device(self.device):
             self.handle = lf_cache_create_ex(layers, batch, kv_heads, q_heads, head_dim, capacity,
                                              window, dtype, evict, budgets, cluster, stages,
-                                             kernel, score, norm, sinks, deferred, scope)
+                                             kernel, score, norm, sinks, deferred, scope, **rkv)
         self.layout = lf_cache_layout(self.handle)
         self.dtype = _TORCH_DTYPE[self.layout.dtype]
         self.layers, self.batch = layers, batch
         self.kv_heads, self.q_heads, self.head_dim = kv_heads, q_heads, head_dim
-        self.capacity, self.window, self.evict = capacity, window, bool(evict)
+        self.capacity, self.window = capacity, window
+        self.evict = self.layout.evict != LF_EVICT_OFF
 
     def close(self):
         if getattr(self, "handle", None):
@@ -291,6 +307,12 @@ class LFCache:
         self._expect(evicted, (b, hkv), "evicted", torch.int32)
         lf_decode_step(self.handle, layer, q, k_new, v_new, out, evicted, stream)
         return out, evicted
+
+    def rkv_compress(self, layer, q_obs, stream=None):
+        """R-KV compression of one layer; q_obs [batch][rkv_alpha][q_heads][head_dim]."""
+        lay = self.layout
+        self._expect(q_obs, (self.batch, lay.rkv_alpha, self.q_heads, self.head_dim), "q_obs")
+        lf_rkv_compress(self.handle, layer, q_obs, stream)
 
     def check(self, stream=None) -> int:
         return lf_cache_check(self.handle, stream)

@@ -88,6 +88,14 @@ typedef enum lf_status {
 
 typedef enum lf_dtype { LF_BF16 = 0, LF_F32 = 1 } lf_dtype;
 
+/* What makes room in the cache (lf_config.evict). */
+typedef enum lf_evict {
+  LF_EVICT_OFF = 0,       /* full KV: append until the capacity, then read only */
+  LF_EVICT_LONGFLOW = 1,  /* LongFlow: every step past the budget evicts one slot */
+  LF_EVICT_RKV = 2        /* R-KV: append into a staging buffer; lf_rkv_compress
+                             brings the cache back to its budget */
+} lf_evict;
+
 /* Which decode kernel to build the cache for. */
 typedef enum lf_kernel {
   LF_KERNEL_AUTO = 0,        /* tensor cores where supported, else CUDA cores */
@@ -114,8 +122,8 @@ typedef enum lf_scope {
 
 typedef struct lf_config {
   int dtype;              /* LF_BF16 or LF_F32: type of q, K, V, k_new, v_new, out */
-  int evict;              /* 1: LongFlow eviction; 0: full KV -- append until the
-                             capacity, then read only (no scores, no writes) */
+  int evict;              /* lf_evict: 1 LongFlow eviction; 0 full KV -- append until the
+                             capacity, then read only (no scores, no writes); 2 R-KV */
   const int32_t* budgets; /* host [batch] per-sequence budgets (each <= capacity and
                              > window when evicting), or NULL: every budget = capacity */
   int cluster;            /* CTAs that split one KV head's slots (1,2,4,8,16); 0 = auto */
@@ -129,6 +137,15 @@ typedef struct lf_config {
   int deferred;           /* 0 = victim chosen and overwritten in the same step,
                              1 = chosen now, overwritten by the next token (window >= 1) */
   int scope;              /* lf_scope */
+  /* R-KV (evict = LF_EVICT_RKV; 0 = the README's default): `capacity` is the
+   * retained budget plus the staging buffer.  bf16, head_dim 128, capacity <= 4096,
+   * rkv_alpha * (q_heads / kv_heads) <= 64, no per-sequence budgets. */
+  int rkv_buffer;         /* staging slots B_buffer (128) */
+  int rkv_alpha;          /* observation queries, always-kept newest tokens (8) */
+  int rkv_beta;           /* near-duplicates kept among the most recent (1) */
+  float rkv_lambda;       /* importance / redundancy trade-off in (0, 1] (0.1) */
+  float rkv_tau;          /* key cosine at or above which tokens are near-duplicates,
+                             in (0, 1] (0.9) */
 } lf_config;
 
 /*
@@ -192,6 +209,27 @@ int lf_prefill_fill(lf_cache* cache, int layer, const void* k, const void* v,
 int lf_decode_step(lf_cache* cache, int layer, const void* q, const void* k_new,
                    const void* v_new, void* out, int32_t* evicted_slot, lf_stream_t stream);
 
+/*
+ * R-KV's compression step ("GitHub - Zefan-Cai/R-KV", section "Method", stages
+ * 2-4) for one layer of an LF_EVICT_RKV cache: every (sequence, KV head) holding
+ * more than budget = capacity - rkv_buffer tokens is cut back to the budget.
+ *   importance  I_i = mean over the rkv_alpha observation queries q_obs and the
+ *               head's query group of their softmax weight on token i (softmax
+ *               over every cached token, scale 1/sqrt(d));
+ *   redundancy  R_i = 1 if at least rkv_beta later tokens have key cosine
+ *               >= rkv_tau with token i, else 0;
+ *   Z_i = rkv_lambda I_i - (1 - rkv_lambda) R_i; the rkv_alpha latest tokens
+ *   stay, then the highest Z (equal Z: the later token) up to the budget.
+ * The slab stays static: kept buffer tokens move into the freed slots below the
+ * budget, in slot order.  Call it when the buffer is full (decode steps on a
+ * full slab do not store the token and raise LF_DEVERR_STATE).
+ *   q_obs  device, [batch][rkv_alpha][q_heads][head_dim] bf16: the queries of
+ *          the rkv_alpha latest decode steps, any order, caller-owned
+ * Stream-ordered, asynchronous, allocates nothing.  LF_ERR_ARG if the cache is
+ * not an R-KV cache.
+ */
+int lf_rkv_compress(lf_cache* cache, int layer, const void* q_obs, lf_stream_t stream);
+
 /* Synchronise `stream`, read and clear the device error word.  *bits (may be
  * NULL) receives the LF_DEVERR_* bits.  Returns LF_ERR_DEVICE if any was set. */
 int lf_cache_check(lf_cache* cache, lf_stream_t stream, int32_t* bits);
@@ -222,6 +260,8 @@ typedef struct lf_layout {
                        vnorm), else NULL */
   int32_t* pending; /* deferred: the slot the next token takes, per unit (same index
                        as count; -1 = none chosen), else NULL */
+  int rkv_buffer, rkv_alpha, rkv_beta; /* R-KV parameters (evict = LF_EVICT_RKV) */
+  float rkv_lambda, rkv_tau;
 } lf_layout;
 
 int lf_cache_layout(const lf_cache* cache, lf_layout* out);

@@ -56,6 +56,19 @@ class Workload:
     rho_range: Tuple[float, float] = (0.0, 0.0)
     reset_every: int = 0     # fresh N(0,1) query every `reset_every` steps (0: never)
     full_kv_capacity: int = 0  # capacity of the eviction-off full-KV comparison (0: none)
+    # Near-duplicate keys: with probability dup_prob a token's key is one of
+    # dup_bank seeded pattern vectors of its (layer, KV head) plus relative noise
+    # dup_noise, so tokens sharing a pattern are near-duplicates of each other.
+    dup_prob: float = 0.0
+    dup_bank: int = 64
+    dup_noise: float = 0.02
+    # R-KV compression (0: not an R-KV workload): staging buffer, observation
+    # queries, lambda, cosine threshold and near-duplicates kept.
+    rkv_buffer: int = 0
+    rkv_alpha: int = 8
+    rkv_lambda: float = 0.1
+    rkv_tau: float = 0.9
+    rkv_beta: int = 1
 
     @property
     def group(self) -> int:
@@ -97,6 +110,14 @@ WORKLOADS = {
         budget=3276, window=32, prefill=2048, steps=8192, dtype="bf16",
         ragged=True, budget_choices=(512, 1024, 2048, 3276), prompt_range=(64, 2048),
         rho_range=(0.6, 0.98), reset_every=1000),
+    # R-KV, the pages' baseline, on the R1-Llama-8B geometry: 3276 retained slots
+    # plus a 128-token staging buffer, compressed whenever the buffer is full;
+    # 5% of tokens are near-duplicates of a per-head pattern (repeated
+    # reasoning), the redundancy R-KV removes.  Prefilled to the budget.
+    "rkv-r1-llama-8b": Workload(
+        name="rkv-r1-llama-8b", layers=32, batch=32, q_heads=32, kv_heads=8, head_dim=128,
+        budget=3276, window=0, prefill=3276, steps=16384, dtype="bf16",
+        rho=0.9, innovation=0.44, v_lognormal_sigma=0.5, dup_prob=0.05, rkv_buffer=128),
 }
 
 
@@ -112,7 +133,7 @@ def torch_dtype(dtype: str) -> torch.dtype:
 
 
 # Purposes keep independent draws in independent streams.
-_PURPOSE = {"seq": 1, "q0": 2, "step": 3, "prompt": 4, "sinkdir": 5}
+_PURPOSE = {"seq": 1, "q0": 2, "step": 3, "prompt": 4, "sinkdir": 5, "dupbank": 6}
 
 
 def _gen(seed: int, purpose: str, layer: int, device) -> torch.Generator:
@@ -163,7 +184,12 @@ class InputStream:
         self._gstep = {l: _gen(seed, "step", l, self.device) for l in self.layer_ids}
         self._q = {}
         self._sink_u = {}
+        self._bank = {}
         for l in self.layer_ids:
+            if wl.dup_prob > 0:
+                gb = _gen(seed, "dupbank", l, self.device)
+                self._bank[l] = torch.randn(wl.kv_heads, wl.dup_bank, d, generator=gb,
+                                            device=self.device)
             g0 = _gen(seed, "q0", l, self.device)
             self._q[l] = torch.randn(b, hq, d, generator=g0, device=self.device)
             if wl.sink_prob > 0:
@@ -187,6 +213,15 @@ class InputStream:
                        < wl.sink_prob).to(torch.float32)
             shift = wl.sink_sigmas * math.sqrt(wl.head_dim) * self._sink_u[layer]
             k = k + is_sink * shift.view(1, wl.kv_heads, 1, wl.head_dim)
+        if wl.dup_prob > 0:
+            is_dup = (torch.rand(wl.batch, wl.kv_heads, n, 1, generator=g, device=self.device)
+                      < wl.dup_prob)
+            pick = torch.randint(0, wl.dup_bank, (wl.batch, wl.kv_heads, n), generator=g,
+                                 device=self.device)
+            bank = self._bank[layer]                                   # [H_kv][bank][d]
+            pattern = torch.stack([bank[h][pick[:, h]] for h in range(wl.kv_heads)], dim=1)
+            noise = torch.randn(shape, generator=g, device=self.device)
+            k = torch.where(is_dup, pattern + wl.dup_noise * noise, k)
         return k, v
 
     def prompt(self, layer: int):

@@ -50,7 +50,7 @@ def test_constants_match_header():
     for name in ["LF_OK", "LF_ERR_ARG", "LF_ERR_OOM", "LF_ERR_CUDA", "LF_ERR_DEVICE",
                  "LF_ERR_UNSUPPORTED", "LF_BF16", "LF_F32", "LF_KERNEL_AUTO", "LF_KERNEL_SIMT",
                  "LF_KERNEL_TENSOR_CORE", "LF_SCORE_LONGFLOW", "LF_SCORE_H2O", "LF_SCOPE_KV_HEAD",
-                 "LF_SCOPE_LAYER"]:
+                 "LF_SCOPE_LAYER", "LF_EVICT_OFF", "LF_EVICT_LONGFLOW", "LF_EVICT_RKV"]:
         m = re.search(rf"\b{name}\s*=\s*(-?\d+)", text)
         assert m and int(m.group(1)) == getattr(lf, name), name
     for name in ["LF_DEVERR_NONFINITE", "LF_DEVERR_STATE", "LF_DEVERR_TIMEOUT"]:
@@ -130,6 +130,23 @@ def test_bad_policy_fields(lib):
     # deferred eviction protects the new token through the window
     with pytest.raises(lf.LFError, match="window >= 1"):
         lf.lf_cache_create_ex(1, 1, 1, 1, 128, 64, 0, deferred=True)
+
+
+def test_bad_rkv_fields(lib):
+    """R-KV mode: the compression kernel's limits are checked on the host."""
+    with pytest.raises(lf.LFError, match="bf16, head_dim 128"):
+        lf.lf_cache_create_ex(1, 1, 2, 8, 128, 400, 0, dtype="f32", evict="rkv")
+    with pytest.raises(lf.LFError, match="no per-sequence budgets"):
+        lf.lf_cache_create_ex(1, 2, 2, 8, 128, 400, 0, evict="rkv", budgets=[300, 300])
+    with pytest.raises(lf.LFError, match="capacity <= 4096"):
+        lf.lf_cache_create_ex(1, 1, 2, 8, 128, 5000, 0, evict="rkv")
+    with pytest.raises(lf.LFError, match="alpha \\* group <= 64"):
+        lf.lf_cache_create_ex(1, 1, 1, 8, 128, 400, 0, evict="rkv", rkv_alpha=9)
+    with pytest.raises(lf.LFError, match="lambda and tau"):
+        lf.lf_cache_create_ex(1, 1, 2, 8, 128, 400, 0, evict="rkv", rkv_lambda=1.5)
+    with pytest.raises(lf.LFError, match="evict must be"):
+        lf.lf_cache_create_ex(1, 1, 2, 8, 128, 400, 0, evict=3)
+    assert lib.lf_rkv_compress(None, 0, None, None) == lf.LF_ERR_ARG
 
 
 def test_null_handles(lib):
