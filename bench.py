@@ -339,6 +339,87 @@ def time_steps(cache, inputs, outs, evs, torch, graph: bool):
     return start.elapsed_time(end)
 
 
+def bench_rkv(args, torch, lf, stream_mod, peak, longflow_units_per_s):
+    """R-KV's cycle on rkv-r1-llama-8b: `buffer` decode steps that append into
+    the staging buffer, then one compression per layer (lf_rkv_compress).
+    Returns amortised units/s, the decode and compression rates, and the ratio
+    to LongFlow's units/s on the same head geometry and budget."""
+    wl = stream_mod.get_workload("rkv-r1-llama-8b")
+    L = min(wl.layers, args.rkv_layers)
+    wl = wl.scaled(layers=L)
+    B, buf, alpha = wl.budget, wl.rkv_buffer, wl.rkv_alpha
+    cap = B + buf
+    gen = stream_mod.InputStream(wl, seed=300, device="cuda", layers=list(range(L)))
+    cache = lf.LFCache(L, wl.batch, wl.kv_heads, wl.q_heads, wl.head_dim, cap, 0, dtype=wl.dtype,
+                       evict="rkv", rkv_buffer=buf, rkv_alpha=alpha, rkv_beta=wl.rkv_beta,
+                       rkv_lambda=wl.rkv_lambda, rkv_tau=wl.rkv_tau)
+    for l in range(L):
+        k, v, lens = gen.prompt(l)
+        cache.prefill(l, k, v, [min(P, cap) for P in lens])
+        del k, v
+    outs = [torch.empty(wl.batch, wl.q_heads, wl.head_dim, dtype=cache.dtype, device="cuda")
+            for _ in range(L)]
+    evs = [torch.empty(wl.batch, wl.kv_heads, dtype=torch.int32, device="cuda") for _ in range(L)]
+
+    def cycle_inputs():
+        steps = pregenerate(gen, buf, torch)
+        # observation queries of the last alpha steps, per layer: [b][alpha][H_q][d]
+        qobs = [torch.stack([steps[t][0][l] for t in range(buf - alpha, buf)], dim=1).contiguous()
+                for l in range(L)]
+        return steps, qobs
+
+    st = torch.cuda.current_stream()
+    # one untimed cycle (the first compression after the prompt), then a timed one
+    steps, qobs = cycle_inputs()
+    time_steps(cache, steps, outs, evs, torch, graph=False)
+    for l in range(L):
+        cache.rkv_compress(l, qobs[l])
+    if cache.check() != 0:
+        raise RuntimeError("device error in the R-KV warm-up cycle")
+    steps, qobs = cycle_inputs()
+    torch.cuda.synchronize()
+    dec_ms = time_steps(cache, steps, outs, evs, torch, graph=not args.eager)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for l in range(L):
+        cache.rkv_compress(l, qobs[l])
+    e1.record(st)
+    e1.synchronize()
+    comp_ms = e0.elapsed_time(e1)
+    bits = cache.check()
+    if bits:
+        raise RuntimeError(f"device error word {bits} in the R-KV cycle")
+    counts = cache.views()["count"].cpu()
+    cache.close()
+    del cache, gen, steps, qobs
+    torch.cuda.empty_cache()
+    units = wl.batch * L * buf
+    # decode bytes: occupancy grows from B to B + buf - 1 over the cycle
+    dec_bytes = sum(unit_bytes(wl, B + t) for t in range(buf)) * wl.batch * L
+    # compression: the key dot products of the blocks J >= I plus two importance passes
+    n = cap
+    nb = (n + 127) // 128
+    qn = (alpha * wl.group + 15) // 16 * 16
+    flops_unit = nb * (nb + 1) // 2 * 2 * 128 * 128 * 128 + 2 * nb * 2 * 128 * qn * 128
+    comp_units = wl.batch * wl.kv_heads * L
+    value = units / ((dec_ms + comp_ms) / 1000.0)
+    return {
+        "workload": wl.name, "layers": L, "batch": wl.batch, "budget": B, "buffer": buf,
+        "alpha": alpha, "lambda": wl.rkv_lambda, "tau": wl.rkv_tau, "beta": wl.rkv_beta,
+        "value": value, "unit": UNIT,
+        "cycle": f"{buf} decode steps + 1 compression per layer",
+        "decode_units_per_s": units / (dec_ms / 1000.0),
+        "decode_achieved_gbs": dec_bytes / (dec_ms / 1000.0) / 1e9,
+        "decode_frac_of_peak": dec_bytes / (dec_ms / 1000.0) / 1e9 / peak,
+        "compress_ms_per_layer": comp_ms / L,
+        "compress_share_of_cycle": comp_ms / (dec_ms + comp_ms),
+        "compress_tensor_tflops": flops_unit * comp_units / (comp_ms / 1000.0) / 1e12,
+        "counts_after": [int(counts.min()), int(counts.max())],
+        "longflow_units_per_s_same_geometry": longflow_units_per_s,
+        "longflow_over_rkv": longflow_units_per_s / value,
+    }
+
+
 def bench_ours(args):
     import torch
     import torch.distributed as dist
@@ -504,6 +585,11 @@ def bench_ours(args):
             del cp, gp, tin
             torch.cuda.empty_cache()
 
+    # ---- R-KV, the pages' baseline, on its own workload (fewer layers) ----
+    rkv = None
+    if args.rkv and rank == 0:
+        rkv = bench_rkv(args, torch, lf, stream_mod, peak, value)
+
     if rank != 0:
         return 0
     cpu = None
@@ -538,6 +624,7 @@ def bench_ours(args):
         "clocks": clk,
         "full_kv": full,
         "policy_variants": policies,
+        "rkv": rkv,
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -562,6 +649,9 @@ def main():
     ap.add_argument("--no-policies", dest="policies", action="store_false", default=True,
                     help="skip timing the policy variants")
     ap.add_argument("--policy-layers", type=int, default=8)
+    ap.add_argument("--no-rkv", dest="rkv", action="store_false", default=True,
+                    help="skip the R-KV baseline leg")
+    ap.add_argument("--rkv-layers", type=int, default=4)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args()
     if args.warmup < 3:
