@@ -21,7 +21,7 @@ head with its group of G query heads), in float64 on the exact stored values:
   overwrite -- guide, section "Static Memory Pre-Allocation and In-Place
   Eviction", steps 1-3; summary, section 2.3 "Static KV Cache".
 
-Readings where the pages are silent or ambiguous (each listed in the design doc):
+Readings where the pages are silent or ambiguous:
 
 * GQA: query head h reads KV head floor(h / G); each KV head keeps its own
   slots and evicts its own victim, scored by the sum over its G query heads.

@@ -21,7 +21,7 @@ Compression (R-KV)", the four-stage table) describes one compression step:
 Defaults from the same README ("Default Hyper-parameters"): B_buffer = 128,
 alpha = 8, lambda = 0.1.
 
-Readings where the README is silent (each listed in the design doc):
+Readings where the README is silent:
 
 * one cache unit = one (layer, sequence, KV head), as for LongFlow; the
   observation queries are the group's G query heads at each of the alpha most
