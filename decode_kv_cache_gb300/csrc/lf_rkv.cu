@@ -16,9 +16,11 @@
 //           observation query's softmax over all tokens;
 //   pass 2  per 128-token row block I: importance of its tokens, then the key
 //           dot products K_I . K_J^T (M = N = 128) for every J >= I, streamed
-//           through a 3-stage TMA ring into two TMEM accumulators; each pair
-//           (i, j) is looked at once and a near-duplicate pair counts for the
-//           older token.  The B x B cosine matrix never leaves the chip;
+//           through a 3-stage TMA ring into three TMEM accumulators (the MMAs
+//           run two blocks ahead; each warp hands an accumulator back as soon
+//           as it has loaded it); each pair (i, j) is looked at once and a
+//           near-duplicate pair counts for the older token.  The B x B cosine
+//           matrix never leaves the chip;
 //   select  a bitonic sort of (Z, position) keys, observation tokens first;
 //   move    kept buffer tokens into the freed retained slots.
 // Every wait is bounded; on expiry the unit is left as it was and
@@ -45,7 +47,8 @@ constexpr int kRkQRows = 64;                // observation query rows (alpha * G
 constexpr int kRkQBlock = kRkQRows * 128;   // one 64-column half of the query operand: 8 KB
 
 // Shared-memory plan (offsets from a 1024-byte aligned base).
-constexpr int kOffBars = 0;        // full[3], afull, impfull, accfull[2]
+constexpr int kOffBars = 0;        // full[3], afull, impfull, accfull[3], accfree[3]
+constexpr int kRkAcc = 3;          // key dot-product accumulators, 128 TMEM columns each
 constexpr int kOffTmem = 128;
 constexpr int kOffMisc = 144;      // [0] fail flag, [1] move count, [2] list length check
 constexpr int kOffStats = 256;     // m[64], l[64]
@@ -89,7 +92,8 @@ __global__ void __launch_bounds__(kRkThreads, 1) rkv_compress_kernel(const __gri
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kOffBars);
   uint64_t* afull = full + 3;
   uint64_t* impfull = full + 4;
-  uint64_t* accfull = full + 5;   // [2]
+  uint64_t* accfull = full + 5;   // [3] MMAs of a block complete
+  uint64_t* accfree = full + 8;   // [3] every warp has loaded the block
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmem);
   volatile int* misc = reinterpret_cast<volatile int*>(smem + kOffMisc);
   float* m_col = reinterpret_cast<float*>(smem + kOffStats);
@@ -115,7 +119,8 @@ __global__ void __launch_bounds__(kRkThreads, 1) rkv_compress_kernel(const __gri
 
   // ---- set-up: barriers, tensor memory, positions, 1/||k||, the query operand --
   if (tid == 0) {
-    for (int i = 0; i < 7; ++i) mbar_init(&full[i], 1);
+    for (int i = 0; i < 8; ++i) mbar_init(&full[i], 1);
+    for (int i = 0; i < kRkAcc; ++i) mbar_init(&accfree[i], kRkThreads / 32);
     fence_mbar_init();
     misc[0] = 0;
   }
@@ -124,19 +129,11 @@ __global__ void __launch_bounds__(kRkThreads, 1) rkv_compress_kernel(const __gri
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
-  const T* Ku = ra.K + ubase * D;
   for (int i = tid; i < kRkvMaxSlots; i += kRkThreads) {
     pos_s[i] = (i < n) ? ra.pos[ubase + i] : INT_MIN;
     cnt_s[i] = 0;
     z_s[i] = 0.f;
-    if (i >= n) inv_s[i] = 0.f;
-  }
-  // 1/||k_i|| of the occupied slots (0 for a zero key: never similar), a warp per row
-  for (int i = warp; i < n; i += kRkThreads / 32) {
-    float x[4];
-    load4_f32(Ku + (size_t)i * D + lane * 4, x);
-    const float ss = warp_sum(x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3]);
-    if (lane == 0) inv_s[i] = (ss > 0.f) ? rsqrtf(ss) : 0.f;
+    inv_s[i] = 0.f;   // ||k_i||^2 accumulates here in pass 1, then becomes 1/||k_i||
   }
   // the observation queries as the B operand: row j*G + h = query head g*G + h
   // of observation j; rows >= QN stay zero
@@ -152,22 +149,14 @@ __global__ void __launch_bounds__(kRkThreads, 1) rkv_compress_kernel(const __gri
     *reinterpret_cast<uint4*>(qop + (ch >> 3) * kRkQBlock + r * 128 + (((ch & 7) ^ (r & 7)) << 4)) = v;
   }
   __syncthreads();
-  // smallest norm of every 32-slot chunk (for the quick rejection below)
-  if (tid < kRkvMaxSlots / 32) {
-    float mn = INFINITY;
-    for (int c = 0; c < 32; ++c) {
-      const float iv = inv_s[tid * 32 + c];
-      if (iv > 0.f) mn = fminf(mn, 1.f / iv);
-    }
-    nmin[tid] = mn;
-  }
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tm = *tmem_slot;
-  const uint32_t t_imp = tm + 256;   // importance logits, QN16 <= 64 columns
-  const uint64_t pol = l2_evict_first_policy();
+  const uint32_t t_imp = tm + kRkAcc * 128;   // importance logits, QN16 <= 64 columns
+  // K tiles are read again for every row block: ask L2 to keep them
+  const uint64_t pol = l2_evict_last_policy();
   const int row0 = ra.row_base + (int)ubase;
   const uint32_t id_imp = idesc_bf16_f32(128, QN16, false, false);
   const uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
@@ -228,6 +217,25 @@ __global__ void __launch_bounds__(kRkThreads, 1) rkv_compress_kernel(const __gri
     float s[32];
     ok = a_tile_logits(I, s);
     if (!ok) break;
+    {
+      // ||k||^2 of this thread's token, d-half `half`, from the tile in shared memory
+      // (row r of the 64-column block at r * 128 bytes, 16-byte chunks swizzled by r mod 8)
+      const int r = quarter * 32 + lane;
+      const int row = I * kRkTile + r;
+      const unsigned char* rp = abuf + half * kRkBlock + r * 128;
+      float ss = 0.f;
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        const uint4 w = *reinterpret_cast<const uint4*>(rp + ((ch ^ (r & 7)) << 4));
+        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&w);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __bfloat1622float2(h2[e]);
+          ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
+        }
+      }
+      if (row < n) atomicAdd(&inv_s[row], ss);
+    }
 #pragma unroll
     for (int c = 0; c < 32; ++c) {
       const float wm = warp_max(s[c]);
@@ -254,6 +262,24 @@ __global__ void __launch_bounds__(kRkThreads, 1) rkv_compress_kernel(const __gri
     }
     __syncthreads();
   }
+
+  // 1/||k_i|| (0 for a zero key: never similar), and the smallest ||k|| of every
+  // 32-slot chunk for the quick rejection below
+  __syncthreads();
+  for (int i = tid; i < n; i += kRkThreads) {
+    const float ss = inv_s[i];
+    inv_s[i] = (ss > 0.f) ? rsqrtf(ss) : 0.f;
+  }
+  __syncthreads();
+  if (tid < kRkvMaxSlots / 32) {
+    float mn = INFINITY;
+    for (int c = 0; c < 32; ++c) {
+      const float iv = inv_s[tid * 32 + c];
+      if (iv > 0.f) mn = fminf(mn, 1.f / iv);
+    }
+    nmin[tid] = mn;
+  }
+  __syncthreads();
 
   // ---- pass 2: importance, then near-duplicate counts over blocks J >= I ---------
   int tglob = 0;   // K tiles through the ring so far
@@ -282,27 +308,37 @@ __global__ void __launch_bounds__(kRkThreads, 1) rkv_compress_kernel(const __gri
         load_tile(ring + ((tglob + q) % kRkStages) * kRkStage, I + q, &full[(tglob + q) % kRkStages]);
       issued = tglob + min(kRkStages, njb);
     }
-    auto mma_s = [&](int t) -> bool {   // K_I . K_J^T of ring tile t into accumulator t & 1
+    auto mma_s = [&](int t) -> bool {   // K_I . K_J^T of ring tile t into accumulator t % 3
       const int st = t % kRkStages;
+      const int acc = t % kRkAcc;
       if (!mbar_wait_bounded(&full[st], (uint32_t)((t / kRkStages) & 1))) return false;
+      // the accumulator's previous block (tile t - 3) has been loaded by every warp
+      if (t >= kRkAcc && !mbar_wait_bounded(&accfree[acc], (uint32_t)(((t / kRkAcc) - 1) & 1)))
+        return false;
       tc_fence_after();
       const uint32_t a0 = smem_u32(abuf), b0 = smem_u32(ring + st * kRkStage);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
-        tc_mma_bf16(tm + (uint32_t)((t & 1) * 128),
+        tc_mma_bf16(tm + (uint32_t)(acc * 128),
                     sw128_desc(a0 + (kk >> 2) * kRkBlock + (kk & 3) * 32, 16, 1024),
                     sw128_desc(b0 + (kk >> 2) * kRkBlock + (kk & 3) * 32, 16, 1024), id_s,
                     kk > 0 ? 1u : 0u);
-      tc_commit(&accfull[t & 1]);
+      tc_commit(&accfull[acc]);
       return true;
     };
-    if (tid == 0 && !mma_s(tglob)) misc[0] = 1;
+    // the first two blocks' MMAs (the MMAs then run two blocks ahead of the epilogue)
+    if (tid == 0) {
+      if (!mma_s(tglob)) misc[0] = 1;
+      if (njb > 1 && !misc[0] && !mma_s(tglob + 1)) misc[0] = 1;
+    }
     for (int J = I; J < nb; ++J) {
       const int t = tglob + (J - I);
-      if (tid == 0 && J + 1 < nb && !misc[0] && !mma_s(t + 1)) misc[0] = 1;
-      bool got = (misc[0] == 0) && mbar_wait_bounded(&accfull[t & 1], (uint32_t)((t >> 1) & 1));
-      got = __syncthreads_and(got);
-      if (!got) {
+      const int acc = t % kRkAcc;
+      if (tid == 0 && J + 2 < nb && !misc[0] && !mma_s(t + 2)) misc[0] = 1;
+      const bool got = (misc[0] == 0) &&
+                       mbar_wait_bounded(&accfull[acc], (uint32_t)((t / kRkAcc) & 1));
+      if (!__all_sync(0xffffffffu, got)) {
+        misc[0] = 1;
         ok = false;
         break;
       }
@@ -313,12 +349,15 @@ __global__ void __launch_bounds__(kRkThreads, 1) rkv_compress_kernel(const __gri
         issued = t + kRkStages + 1;
       }
       // columns 64*half .. +63 of block J: both warp-collective loads first, then
-      // each thread's own (divergent) tests
+      // hand the accumulator back, then each thread's own (divergent) tests
       float v[2][32];
       __syncwarp();
-      tmem_ld32(tm + (uint32_t)((t & 1) * 128) + lanes + (uint32_t)(half * 64), v[0]);
-      tmem_ld32(tm + (uint32_t)((t & 1) * 128) + lanes + (uint32_t)(half * 64 + 32), v[1]);
+      tmem_ld32(tm + (uint32_t)(acc * 128) + lanes + (uint32_t)(half * 64), v[0]);
+      tmem_ld32(tm + (uint32_t)(acc * 128) + lanes + (uint32_t)(half * 64 + 32), v[1]);
       tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&accfree[acc]);
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         const int j0 = J * kRkTile + half * 64 + cc * 32;   // first column token
@@ -337,9 +376,9 @@ __global__ void __launch_bounds__(kRkThreads, 1) rkv_compress_kernel(const __gri
           }
         }
       }
-      tc_fence_before();
-      __syncthreads();
     }
+    // every warp is through this row block (and every accumulator it used is free)
+    ok = __syncthreads_and(ok && misc[0] == 0);
     tglob += njb;
     if (!ok) break;
     if (row < n && cnt) atomicAdd(&cnt_s[row], cnt);
@@ -397,13 +436,21 @@ __global__ void __launch_bounds__(kRkThreads, 1) rkv_compress_kernel(const __gri
     // ---- move: kept buffer tokens into the freed retained slots, in slot order ----
     int* freed = reinterpret_cast<int*>(ring);                  // reuse the ring
     int* movers = freed + kRkvMaxSlots;
-    if (tid == 0) {
+    if (warp == 0) {   // ballot scans: freed retained slots and kept buffer slots, in order
       int nf = 0, nm = 0;
-      for (int s = 0; s < ra.budget; ++s)
-        if (!cnt_s[s]) freed[nf++] = s;
-      for (int s = ra.budget; s < n; ++s)
-        if (cnt_s[s]) movers[nm++] = s;
-      misc[1] = (nf == nm) ? nm : -1;
+      for (int s0 = 0; s0 < n; s0 += 32) {
+        const int sl = s0 + lane;
+        const bool is_freed = sl < ra.budget && !cnt_s[sl];
+        const bool is_mover = sl >= ra.budget && sl < n && cnt_s[sl];
+        const unsigned fb = __ballot_sync(0xffffffffu, is_freed);
+        const unsigned mb = __ballot_sync(0xffffffffu, is_mover);
+        const unsigned below = (1u << lane) - 1u;
+        if (is_freed) freed[nf + __popc(fb & below)] = sl;
+        if (is_mover) movers[nm + __popc(mb & below)] = sl;
+        nf += __popc(fb);
+        nm += __popc(mb);
+      }
+      if (lane == 0) misc[1] = (nf == nm) ? nm : -1;
     }
     __syncthreads();
     const int nmove = misc[1];
