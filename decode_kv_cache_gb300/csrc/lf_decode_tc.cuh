@@ -240,6 +240,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     items[4 * k] = a.count[u];
     items[4 * k + 1] = a.next_pos[u];
     items[4 * k + 2] = (a.evict && a.deferred) ? a.pending[u] : -1;
+    items[4 * k + 3] = a.budget[u / a.kv_heads];
   }
   fence_proxy_async_smem();
   tc_fence_before();
@@ -414,6 +415,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       tc_commit(ofull);
     };
+    // The group's queries of unit item kk, 16-byte chunk c = lane + 32 i, loaded
+    // into registers one unit ahead: the load's latency then passes while this
+    // warp issues the previous unit's MMAs instead of holding up the ring.
+    constexpr int kQChunks = (G * 16 + 31) / 32;
+    uint4 qreg[kQChunks];
+    int qreg_item = -1;
+    auto load_q = [&](int kk) {
+      const int uu = j + kk * NC;
+      const int bb = uu / a.kv_heads;
+      const int gg = uu - bb * a.kv_heads;
+      const T* qsrc =
+          reinterpret_cast<const T*>(a.q) + ((size_t)bb * a.q_heads + (size_t)gg * G) * D;
+#pragma unroll
+      for (int i = 0; i < kQChunks; ++i) {
+        const int c = lane + 32 * i;
+        if (c < G * 16)
+          qreg[i] = *reinterpret_cast<const uint4*>(qsrc + (size_t)(c >> 4) * D + (c & 15) * 8);
+      }
+      qreg_item = kk;
+    };
+    if (nitems > 0) load_q(0);
     int prev = -1, prev_rows = 0;
     for (int k = 0; k < nitems && !fail; ++k) {
       if (prev >= 0 && prev <= k - 2) {  // same flush rule as the producer
@@ -427,9 +449,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int rows = unit_rows(k, n, p, ok, base);
       if (rows == 0) continue;
       const int ntile = (rows + kTcTile - 1) / kTcTile;
-      const int u = j + k * NC;
-      const int b = u / a.kv_heads;
-      const int g = u - b * a.kv_heads;
       const int qb = nn & 1;
       unsigned char* qdst = qbuf + qb * P::kQBytes;
       // The buffer's previous contents (two units ago) must have been read.
@@ -441,16 +460,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         break;
       }
       // q^T rows h < G: the group's queries (16-byte chunks, 128-byte swizzle).
-      const T* qg = reinterpret_cast<const T*>(a.q) + ((size_t)b * a.q_heads + (size_t)g * G) * D;
-      for (int c = lane; c < G * 16; c += 32) {
-        const int h = c >> 4;
-        const int ch = c & 15;
-        const uint4 v = *reinterpret_cast<const uint4*>(qg + (size_t)h * D + ch * 8);
-        *reinterpret_cast<uint4*>(qdst + (ch >> 3) * 2048 + h * 128 + (((ch & 7) ^ (h & 7)) << 4)) =
-            v;
+      if (qreg_item != k) load_q(k);   // not fetched ahead (an empty unit came between)
+#pragma unroll
+      for (int i = 0; i < kQChunks; ++i) {
+        const int c = lane + 32 * i;
+        if (c < G * 16) {
+          const int h = c >> 4;
+          const int ch = c & 15;
+          *reinterpret_cast<uint4*>(qdst + (ch >> 3) * 2048 + h * 128 + (((ch & 7) ^ (h & 7)) << 4)) =
+              qreg[i];
+        }
       }
       fence_proxy_async_smem();
       __syncwarp();
+      if (k + 1 < nitems) load_q(k + 1);   // the next unit's queries, in the background
       if (lane == 0) {
         const uint32_t qaddr = smem_u32(qdst);
         if (prev < 0) {
@@ -495,7 +518,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int32_t* pos_s =
           reinterpret_cast<const int32_t*>(vnbase + (2 + b2) * P::vn_bytes(chunk));
       float* w_s = reinterpret_cast<float*>(vnbase + (4 + b2) * P::vn_bytes(chunk));
-      const int bud = a.budget[(j + k * NC) / a.kv_heads];
+      const int bud = items[4 * k + 3];
       const UnitRule rl = unit_rule(a, n, p, items[4 * k + 2], bud, state_ok);
       const int plim = rl.plim;  // a slot is a candidate iff sinks <= pos < plim (and not excl)
       const int excl = rl.excl - base;  // this CTA's row of the dropped slot (deferred)
@@ -648,7 +671,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int u = j + k * NC;
       const int b = u / a.kv_heads;
       const int g = u - b * a.kv_heads;
-      const int bud = a.budget[b];
+      const int bud = items[4 * k + 3];
       const int pend = items[4 * k + 2];
       const UnitRule rl = unit_rule(a, n, p, pend, bud, state_ok);
       const bool h2o = a.evict && a.score == LF_SCORE_H2O;
