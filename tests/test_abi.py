@@ -164,3 +164,17 @@ def test_create_without_gpu_fails_cleanly(lib):
     h = lib.lf_cache_create(1, 1, 1, 2, 16, 32, 4)
     assert not h
     assert lf.lf_last_error()  # a CUDA error message, no crash
+
+
+def test_stored_traffic_needs_the_measured_kernel(tmp_path, monkeypatch):
+    """bench.py reports the ncu traffic of the decode kernel only while the
+    committed summary was measured on the current kernel sources."""
+    import bench
+    good = bench.stored_traffic("qwen3-8b-steady", 64)
+    text = open(bench.PROFILE_SUMMARY).read()
+    stale = tmp_path / "summary.md"
+    stale.write_text(text.replace(bench.kernel_source_hash(), "0" * 64))
+    monkeypatch.setattr(bench, "PROFILE_SUMMARY", str(stale))
+    assert bench.stored_traffic("qwen3-8b-steady", 64) is None
+    assert good is None or good > 0
+    assert bench.stored_traffic("ragged-serving", 64) is None

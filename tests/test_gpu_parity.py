@@ -59,6 +59,14 @@ def test_qwen3_8b_steady_state():
     assert st.evictions == 3 * 120
 
 
+def test_qwen3_8b_steady_long_run():
+    """600 steps of the benchmark's layer launch (every step evicts): no drift
+    between the fp32 GPU path and the fp64 oracle over many evictions."""
+    wl = WORKLOADS["qwen3-8b-steady"]
+    st = _run(wl, 600, layers=(0,), sample=[(0, 1, 3), (0, 62, 0)])
+    assert st.evictions == 2 * 600
+
+
 def test_full_kv_read_only():
     """Eviction off at the full 16384-token capacity: every step attends over
     all slots plus the new token and writes nothing."""

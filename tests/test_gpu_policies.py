@@ -81,3 +81,26 @@ def test_eviction_off_ignores_policy():
     wl, cluster = _small("tc")
     _run(wl, 30, cluster=cluster, kernel="tc", evict=False, capacity=512,
          policy=oracle.Policy(norm=2))
+
+
+def test_h2o_full_size_long():
+    """The H2O accumulators of a qwen3-8b-steady layer over 300 steps: fp32 on
+    the GPU stays within 1e-4 relative of the fp64 sums, victims exact outside
+    near-ties."""
+    wl = WORKLOADS["qwen3-8b-steady"]
+    st = _run(wl, 300, layers=(0,), sample=[(0, 5, 1), (0, 50, 6)], policy=POLICIES["h2o"])
+    assert st.evictions == 2 * 300
+
+
+def test_policy_ragged_deferred_sinks():
+    """Per-sequence budgets 512..3276 with the deferred victim and 4 sinks."""
+    from synth.workloads import InputStream
+    wl = WORKLOADS["ragged-serving"]
+    budgets = InputStream(wl, seed=0, device="cpu", layers=[0]).budgets
+    picks = []
+    for B in sorted(set(budgets)):
+        b = budgets.index(B)
+        picks += [(0, b, 0), (0, b, 5)]
+    st = _run(wl, 150, layers=(0,), sample=picks,
+              policy=oracle.Policy(deferred=True, sinks=4))
+    assert st.unit_steps == 150 * len(picks)
