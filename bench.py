@@ -490,37 +490,87 @@ def bench_ours(args):
     lay = cache.layout
 
     # ---- e2e: host buffers, copies inside the timed region ----
+    # Each step's inputs (every layer's q, k_new, v_new) sit in one pinned host
+    # buffer and go up in one copy; each step's results (out, evicted) come back
+    # in one copy.  Copies run on their own streams, two steps in flight: the
+    # upload of step s+1 and the download of step s-1 overlap step s's kernels.
     e2e_steps = min(args.steps, args.e2e_steps)
+    shapes_in = [(t.shape, t.dtype) for grp in timed[0] for t in grp]
+    shapes_out = [(o.shape, o.dtype) for o in outs] + [(e.shape, e.dtype) for e in evs]
+
+    def nbytes(shape, dtype):
+        return math.prod(shape) * torch.empty((), dtype=dtype).element_size()
+
+    h2d = sum(nbytes(*sd) for sd in shapes_in)
+    d2h = sum(nbytes(*sd) for sd in shapes_out)
+
+    def carve(flat, shapes):
+        views, off = [], 0
+        for shape, dtype in shapes:
+            nb = nbytes(shape, dtype)
+            views.append(flat[off:off + nb].view(dtype).view(shape))
+            off += (nb + 255) // 256 * 256
+        return views
+
+    def padded(shapes):
+        return sum((nbytes(*sd) + 255) // 256 * 256 for sd in shapes)
+
     host_in = []
     for (qs, ks, vs) in timed[:e2e_steps]:
-        host_in.append(([t.cpu().pin_memory() for t in qs], [t.cpu().pin_memory() for t in ks],
-                        [t.cpu().pin_memory() for t in vs]))
-    dev_q = [torch.empty_like(t) for t in timed[0][0]]
-    dev_k = [torch.empty_like(t) for t in timed[0][1]]
-    dev_v = [torch.empty_like(t) for t in timed[0][2]]
-    host_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
-    host_ev = [torch.empty(e.shape, dtype=e.dtype).pin_memory() for e in evs]
+        flat = torch.empty(padded(shapes_in), dtype=torch.uint8).pin_memory()
+        for dst, src in zip(carve(flat, shapes_in), list(qs) + list(ks) + list(vs)):
+            dst.copy_(src.cpu())
+        host_in.append(flat)
     del timed
-    h2d = sum(t.numel() * t.element_size() for grp in host_in[0] for t in grp)
-    d2h = sum(t.numel() * t.element_size() for t in host_out + host_ev)
+    dev_in = [torch.empty(padded(shapes_in), dtype=torch.uint8, device="cuda") for _ in range(2)]
+    dev_out = [torch.empty(padded(shapes_out), dtype=torch.uint8, device="cuda") for _ in range(2)]
+    host_out = [torch.empty(padded(shapes_out), dtype=torch.uint8).pin_memory() for _ in range(2)]
+    in_views = [carve(b, shapes_in) for b in dev_in]
+    out_views = [carve(b, shapes_out) for b in dev_out]
     barrier()
-    st = torch.cuda.current_stream()
+    comp = torch.cuda.current_stream()
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def ev():
+        return torch.cuda.Event()
+
+    uploaded = [ev() for _ in range(e2e_steps)]
+    computed = [ev() for _ in range(e2e_steps)]
+    downloaded = [ev() for _ in range(e2e_steps)]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(st)
-    for (qs, ks, vs) in host_in:
+    e0.record(comp)
+
+    def upload(s):
+        up.wait_event(e0)
+        if s >= 2:
+            up.wait_event(computed[s - 2])        # the kernels of step s-2 read this buffer
+        with torch.cuda.stream(up):
+            dev_in[s % 2].copy_(host_in[s], non_blocking=True)
+        uploaded[s].record(up)
+
+    upload(0)
+    for s in range(e2e_steps):
+        if s + 1 < e2e_steps:
+            upload(s + 1)
+        comp.wait_event(uploaded[s])
+        if s >= 2:
+            comp.wait_event(downloaded[s - 2])    # step s-2's results have left this buffer
+        v = in_views[s % 2]
+        o = out_views[s % 2]
         for l in range(L):
-            dev_q[l].copy_(qs[l], non_blocking=True)
-            dev_k[l].copy_(ks[l], non_blocking=True)
-            dev_v[l].copy_(vs[l], non_blocking=True)
-            cache.decode_step(l, dev_q[l], dev_k[l], dev_v[l], outs[l], evs[l])
-            host_out[l].copy_(outs[l], non_blocking=True)
-            host_ev[l].copy_(evs[l], non_blocking=True)
-    e1.record(st)
+            cache.decode_step(l, v[l], v[L + l], v[2 * L + l], o[l], o[L + l])
+        computed[s].record(comp)
+        down.wait_event(computed[s])
+        with torch.cuda.stream(down):
+            host_out[s % 2].copy_(dev_out[s % 2], non_blocking=True)
+        downloaded[s].record(down)
+    comp.wait_event(downloaded[e2e_steps - 1])
+    e1.record(comp)
     e1.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1))
     e2e_value = world * wl.batch * L * e2e_steps / (e2e_ms / 1000.0)
     cache.close()
-    del cache, gen, host_in
+    del cache, gen, host_in, dev_in, dev_out, host_out, in_views, out_views
     torch.cuda.empty_cache()
 
     # ---- eviction off: the same kernel over the full-length KV (read only) ----
