@@ -671,7 +671,7 @@ int lf_rkv_compress(lf_cache* cache, int layer, const void* q_obs, lf_stream_t s
   ra.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)cache->head_dim));
   void* args[] = {&ra};
   cudaError_t e = cudaLaunchKernel(lf::find_rkv_kernel(group), dim3((unsigned)layer_units, 1, 1),
-                                   dim3(256, 1, 1), args, lf::rkv_smem_bytes(),
+                                   dim3((unsigned)lf::rkv_threads(), 1, 1), args, lf::rkv_smem_bytes(),
                                    static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "R-KV compression launch");
   return LF_OK;

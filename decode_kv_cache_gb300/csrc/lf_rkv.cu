@@ -10,18 +10,24 @@
 // keeps the alpha latest tokens and the best-scoring others up to the budget,
 // and (static slab) moves the kept buffer tokens into the freed slots.
 //
-// One CTA per (sequence, KV head) unit, n <= 4096 cached tokens:
-//   pass 1  per 128-token tile, S = K_tile . Q_obs^T on the tensor cores
-//           (M = 128, N = alpha * G padded to 16); online max / sum of every
-//           observation query's softmax over all tokens;
-//   pass 2  per 128-token row block I: importance of its tokens, then the key
-//           dot products K_I . K_J^T (M = N = 128) for every J >= I, streamed
-//           through a 3-stage TMA ring into three TMEM accumulators (the MMAs
-//           run two blocks ahead; each warp hands an accumulator back as soon
-//           as it has loaded it); each pair (i, j) is looked at once and a
-//           near-duplicate pair counts for the older token.  The B x B cosine
-//           matrix never leaves the chip;
-//   select  a bitonic sort of (Z, position) keys, observation tokens first;
+// One CTA per (sequence, KV head) unit, n <= 4096 cached tokens, with the
+// warps split by role: a producer warp streams K tiles through a 3-stage TMA
+// ring, an MMA warp issues every tcgen05.mma, and eight epilogue warps read
+// the accumulators (thread <-> token row, each warp half of the columns).
+//   pass 1  per 128-token tile, S = K_tile . Q_obs^T (M = 128, N = alpha * G
+//           padded to 16) into one of two TMEM accumulators; every epilogue
+//           thread keeps an online max / sum per observation query over its own
+//           rows, and ||k||^2 of its row from the tile in shared memory; the
+//           rows are merged once at the end;
+//   pass 2  per 128-token row block I (held in its own buffer): importance of
+//           its tokens, then the key dot products K_I . K_J^T (M = N = 128) for
+//           every J >= I, the column tiles streamed through the ring into three
+//           TMEM accumulators; a stage is refilled as soon as its MMAs
+//           complete, so the stream runs ahead of the epilogue; each pair
+//           (i, j) is looked at once and a near-duplicate pair counts for the
+//           older token.  The B x B cosine matrix never leaves the chip;
+//   select  a radix select of the (Z, position) keys for the budget-th largest,
+//           observation tokens first;
 //   move    kept buffer tokens into the freed retained slots.
 // Every wait is bounded; on expiry the unit is left as it was and
 // LF_DEVERR_TIMEOUT is raised.
@@ -38,23 +44,29 @@ namespace lf {
 
 namespace {
 
-constexpr int kRkThreads = 256;
+constexpr int kRkEpiWarps = 8;               // epilogue warps 0-7
+constexpr int kRkEpi = kRkEpiWarps * 32;
+constexpr int kRkProducerWarp = 8;
+constexpr int kRkMmaWarp = 9;
+constexpr int kRkThreads = 320;
 constexpr int kRkTile = 128;
 constexpr int kRkStages = 3;
 constexpr int kRkStage = kRkTile * 256;     // one K tile [128 rows][128 d] bf16: 32 KB
 constexpr int kRkBlock = kRkTile * 128;     // one 64-column half of it: 16 KB
 constexpr int kRkQRows = 64;                // observation query rows (alpha * G <= 64)
 constexpr int kRkQBlock = kRkQRows * 128;   // one 64-column half of the query operand: 8 KB
+constexpr int kRkAcc = 3;                   // key dot-product accumulators, 128 TMEM columns each
+constexpr int kRkImpCol = kRkAcc * 128;     // two importance accumulators, 64 columns each
+constexpr int kRkPrefetch = 6;              // ring tiles requested into L2 ahead of their load
 
 // Shared-memory plan (offsets from a 1024-byte aligned base).
-constexpr int kOffBars = 0;        // full[3], afull, impfull, accfull[3], accfree[3]
-constexpr int kRkAcc = 3;          // key dot-product accumulators, 128 TMEM columns each
-constexpr int kOffTmem = 128;
-constexpr int kOffMisc = 144;      // [0] fail flag, [1] move count, [2] list length check
-constexpr int kOffStats = 256;     // m[64], l[64]
+constexpr int kOffBars = 0;        // 19 mbarriers (see the kernel)
+constexpr int kOffTmem = 256;
+constexpr int kOffMisc = 272;      // [0] fail flag, [1] move count
+constexpr int kOffStats = 512;     // m[64], l[64]
 constexpr int kOffRed = 1024;      // [4 quarters][64 columns][2]
 constexpr int kOffNmin = 3072;     // per 32-slot chunk: smallest ||k|| (128 chunks)
-constexpr int kOffA = 4096;
+constexpr int kOffA = 4096;        // the row block of pass 2
 constexpr int kOffRing = kOffA + kRkStage;
 constexpr int kOffQ = kOffRing + kRkStages * kRkStage;
 constexpr int kOffPos = kOffQ + 2 * kRkQBlock;
@@ -63,6 +75,7 @@ constexpr int kOffCnt = kOffInv + kRkvMaxSlots * 4;
 constexpr int kOffZ = kOffCnt + kRkvMaxSlots * 4;
 constexpr int kSmem = kOffZ + kRkvMaxSlots * 4 + 1024;  // + alignment slack
 static_assert(kOffA % 1024 == 0 && kOffRing % 1024 == 0 && kOffQ % 1024 == 0, "alignment");
+static_assert(kOffMisc + 16 <= kOffStats && kOffStats + 2 * kRkQRows * 4 <= kOffRed, "header");
 // the sort reuses the ring: 64-bit keys then 16-bit slot indices
 static_assert(kRkvMaxSlots * 10 <= kRkStages * kRkStage, "sort space");
 
@@ -81,19 +94,24 @@ __global__ void __launch_bounds__(kRkThreads, 1) rkv_compress_kernel(const __gri
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
-  const int quarter = warp & 3;     // TMEM lanes 32*quarter .. +31
-  const int half = warp >> 2;       // which half of the accumulator's columns
+  const int quarter = warp & 3;     // epilogue: TMEM lanes 32*quarter .. +31
+  const int half = (warp >> 2) & 1;  // epilogue: which half of the accumulator's columns
   const int QN = ra.alpha * G;      // observation query rows
   const int QN16 = (QN + 15) & ~15;
   const size_t ubase = (size_t)unit * ra.slot_stride;
 
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kOffBars);
-  uint64_t* afull = full + 3;
-  uint64_t* impfull = full + 4;
-  uint64_t* accfull = full + 5;   // [3] MMAs of a block complete
-  uint64_t* accfree = full + 8;   // [3] every warp has loaded the block
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBars);
+  uint64_t* full = bars;            // [3] ring stage landed
+  uint64_t* empty = bars + 3;       // [3] ring stage read (pass 1: by the epilogue; pass 2: MMAs)
+  uint64_t* afull = bars + 6;       // row block landed
+  uint64_t* afree = bars + 7;       // every MMA reading the row block complete
+  uint64_t* impfull = bars + 8;     // [2] importance logits ready
+  uint64_t* impfree = bars + 10;    // [2] ... loaded by every epilogue warp
+  uint64_t* accfull = bars + 12;    // [3] key dot products of a block ready
+  uint64_t* accfree = bars + 15;    // [3] ... loaded by every epilogue warp
+  uint64_t* drain = bars + 18;      // every MMA complete
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmem);
   volatile int* misc = reinterpret_cast<volatile int*>(smem + kOffMisc);
   float* m_col = reinterpret_cast<float*>(smem + kOffStats);
@@ -117,10 +135,10 @@ __global__ void __launch_bounds__(kRkThreads, 1) rkv_compress_kernel(const __gri
   const int nb = (n + kRkTile - 1) / kRkTile;
   const int pnext = ra.next_pos[unit];
 
-  // ---- set-up: barriers, tensor memory, positions, 1/||k||, the query operand --
+  // ---- set-up: barriers, tensor memory, positions, the query operand -------------
   if (tid == 0) {
-    for (int i = 0; i < 8; ++i) mbar_init(&full[i], 1);
-    for (int i = 0; i < kRkAcc; ++i) mbar_init(&accfree[i], kRkThreads / 32);
+    for (int i = 0; i < 19; ++i)   // impfree, accfree: one arrival per epilogue warp
+      mbar_init(&bars[i], ((i >= 10 && i < 12) || (i >= 15 && i < 18)) ? kRkEpiWarps : 1);
     fence_mbar_init();
     misc[0] = 0;
   }
@@ -154,18 +172,10 @@ __global__ void __launch_bounds__(kRkThreads, 1) rkv_compress_kernel(const __gri
   __syncthreads();
   tc_fence_after();
   const uint32_t tm = *tmem_slot;
-  const uint32_t t_imp = tm + kRkAcc * 128;   // importance logits, QN16 <= 64 columns
+  const int row0 = ra.row_base + (int)ubase;
+
   // K tiles are read again for every row block: ask L2 to keep them
   const uint64_t pol = l2_evict_last_policy();
-  const int row0 = ra.row_base + (int)ubase;
-  const uint32_t id_imp = idesc_bf16_f32(128, QN16, false, false);
-  const uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
-  const uint32_t lanes = (uint32_t)(quarter * 32) << 16;
-  bool ok = true;
-  int n_a = 0, n_imp = 0;   // uses of the A-tile and importance barriers
-  int issued = 0;           // ring tiles requested (thread 0)
-
-  // Load K tile t (rows 128 t ..) into dst, counted on bar (thread 0).
   auto load_tile = [&](unsigned char* dst, int t, uint64_t* bar) {
     mbar_arrive_expect_tx(bar, (uint32_t)kRkStage);
     for (int blk = 0; blk < 2; ++blk)
@@ -173,265 +183,408 @@ __global__ void __launch_bounds__(kRkThreads, 1) rkv_compress_kernel(const __gri
         tma_load_2d(dst + blk * kRkBlock + ro * 128, &ra.kmap, blk * 64, row0 + t * kRkTile + ro,
                     bar, pol);
   };
-  // Importance logits of the A tile into t_imp (thread 0).
-  auto mma_imp = [&]() {
-    const uint32_t a0 = smem_u32(abuf), q0 = smem_u32(qop);
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk)
-      tc_mma_bf16(t_imp, sw128_desc(a0 + (kk >> 2) * kRkBlock + (kk & 3) * 32, 16, 1024),
-                  sw128_desc(q0 + (kk >> 2) * kRkQBlock + (kk & 3) * 32, 16, 1024), id_imp,
-                  kk > 0 ? 1u : 0u);
-    tc_commit(impfull);
-  };
-  // Row block I of A: load it and compute its importance logits (all threads);
-  // returns this thread's 32 logits (columns 32*half ..) scaled to log2 units.
-  auto a_tile_logits = [&](int I, float* s) -> bool {
-    if (tid == 0) load_tile(abuf, I, afull);
-    bool got = mbar_wait_bounded(afull, (uint32_t)(n_a & 1));
-    ++n_a;
-    if (tid == 0 && got) {
-      tc_fence_after();
-      mma_imp();
-    }
-    got = got && mbar_wait_bounded(impfull, (uint32_t)(n_imp & 1));
-    ++n_imp;
-    got = __syncthreads_and(got);
-    if (!got) return false;
-    tc_fence_after();
-    __syncwarp();  // tcgen05.ld is warp-collective
-    tmem_ld32(t_imp + lanes + (uint32_t)(half * 32), s);
-    tmem_wait_ld();
-    const int row = I * kRkTile + quarter * 32 + lane;
-#pragma unroll
-    for (int c = 0; c < 32; ++c)
-      s[c] = (row < n && half * 32 + c < QN) ? s[c] * ra.scale_log2 : -INFINITY;
-    return true;
-  };
 
-  // ---- pass 1: every observation query's max and softmax denominator ------------
-  if (tid < kRkQRows) {
-    m_col[tid] = -INFINITY;
-    l_col[tid] = 0.f;
-  }
-  for (int I = 0; I < nb && ok; ++I) {
-    float s[32];
-    ok = a_tile_logits(I, s);
-    if (!ok) break;
-    {
-      // ||k||^2 of this thread's token, d-half `half`, from the tile in shared memory
-      // (row r of the 64-column block at r * 128 bytes, 16-byte chunks swizzled by r mod 8)
-      const int r = quarter * 32 + lane;
-      const int row = I * kRkTile + r;
-      const unsigned char* rp = abuf + half * kRkBlock + r * 128;
-      float ss = 0.f;
+  if (warp == kRkProducerWarp) {
+    // ---- producer: the ring's tile sequence, pass 1 tiles 0..nb-1, then for
+    // each row block I the column tiles I+1..nb-1.  The ring is latency-bound
+    // (the tiles mostly come from L2), so every tile is also requested into L2
+    // kRkPrefetch places ahead of its load. ---------------------------------------
+    if (lane == 0) {
+      // walks the sequence: returns the next tile index, or -1 at the end
+      struct Walk {
+        int k, I, J;
+      };
+      auto next = [&](Walk& w) -> int {
+        if (w.k < nb) return w.k++;
+        for (;;) {
+          if (w.I >= nb) return -1;
+          if (w.J < nb) return w.J++;
+          ++w.I;
+          w.J = w.I + 1;
+        }
+      };
+      Walk ahead{0, 0, 1};
+      for (int q = 0; q < kRkPrefetch; ++q) {
+        const int t = next(ahead);
+        if (t < 0) break;
+        for (int ro = 0; ro < kRkTile; ro += 64)
+          for (int blk = 0; blk < 2; ++blk)
+            tma_prefetch_l2_2d(&ra.kmap, blk * 64, row0 + t * kRkTile + ro);
+      }
+      Walk cur{0, 0, 1};
+      int tt = 0;       // ring tiles issued
+      for (int t = next(cur); t >= 0; t = next(cur), ++tt) {
+        const int st = tt % kRkStages;
+        if (tt >= kRkStages &&
+            (misc[0] || !mbar_wait_bounded(&empty[st], (uint32_t)(((tt / kRkStages) - 1) & 1)))) {
+          misc[0] = 1;
+          break;
+        }
+        load_tile(ring + st * kRkStage, t, &full[st]);
+        const int tp = next(ahead);
+        if (tp >= 0)
+          for (int ro = 0; ro < kRkTile; ro += 64)
+            for (int blk = 0; blk < 2; ++blk)
+              tma_prefetch_l2_2d(&ra.kmap, blk * 64, row0 + tp * kRkTile + ro);
+      }
+      // every copy issued lands before the CTA may exit
+      for (int t = max(0, tt - kRkStages); t < tt; ++t)
+        (void)mbar_wait_bounded(&full[t % kRkStages], (uint32_t)((t / kRkStages) & 1));
+    }
+    __syncwarp();
+  } else if (warp == kRkMmaWarp) {
+    // ---- MMA warp (lane 0): the same tile order as the producer; it also loads
+    // each row block into its own buffer once the previous block's MMAs are done,
+    // so the producer's stream runs on across row blocks --------------------------
+    if (lane == 0) {
+      const uint32_t id_imp = idesc_bf16_f32(128, QN16, false, false);
+      const uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
+      const uint32_t q0 = smem_u32(qop);
+      bool fail = false;
+      int rt = 0;   // ring tiles consumed
+      int it = 0;   // importance accumulators used
+      int at = 0;   // key dot-product accumulators used
+      int na = 0;   // row blocks requested
+      auto wait = [&](uint64_t* bar, uint32_t parity) {
+        if (!fail && (misc[0] || !mbar_wait_bounded(bar, parity))) fail = true;
+        return !fail;
+      };
+      // S = tile . Q^T into importance accumulator it % 2
+      auto mma_imp = [&](uint32_t a0) {
+        const int ib = it & 1;
+        if (it >= 2 && !wait(&impfree[ib], (uint32_t)(((it >> 1) - 1) & 1))) return;
+        tc_fence_after();
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        const uint4 w = *reinterpret_cast<const uint4*>(rp + ((ch ^ (r & 7)) << 4));
-        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&w);
+        for (int kk = 0; kk < D / 16; ++kk)
+          tc_mma_bf16(tm + (uint32_t)(kRkImpCol + ib * 64),
+                      sw128_desc(a0 + (kk >> 2) * kRkBlock + (kk & 3) * 32, 16, 1024),
+                      sw128_desc(q0 + (kk >> 2) * kRkQBlock + (kk & 3) * 32, 16, 1024), id_imp,
+                      kk > 0 ? 1u : 0u);
+        tc_commit(&impfull[ib]);
+        ++it;
+      };
+      // row block 0 is not used in pass 1: request it now
+      load_tile(abuf, 0, afull);
+      na = 1;
+      // pass 1: the stage is released by the epilogue (it also reads ||k|| there)
+      for (int t = 0; t < nb && !fail; ++t) {
+        const int st = rt % kRkStages;
+        if (!wait(&full[st], (uint32_t)((rt / kRkStages) & 1))) break;
+        tc_fence_after();
+        mma_imp(smem_u32(ring + st * kRkStage));
+        ++rt;
+      }
+      // pass 2
+      const uint32_t a0 = smem_u32(abuf);
+      for (int I = 0; I < nb && !fail; ++I) {
+        if (!wait(afull, (uint32_t)(I & 1))) break;
+        tc_fence_after();
+        mma_imp(a0);
+        for (int J = I; J < nb && !fail; ++J) {
+          const int acc = at % kRkAcc;
+          if (at >= kRkAcc && !wait(&accfree[acc], (uint32_t)(((at / kRkAcc) - 1) & 1))) break;
+          int st = -1;
+          uint32_t b0 = a0;   // the diagonal block: K_I . K_I^T
+          if (J > I) {
+            st = rt % kRkStages;
+            if (!wait(&full[st], (uint32_t)((rt / kRkStages) & 1))) break;
+            b0 = smem_u32(ring + st * kRkStage);
+          }
+          tc_fence_after();
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 f = __bfloat1622float2(h2[e]);
-          ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
+          for (int kk = 0; kk < D / 16; ++kk)
+            tc_mma_bf16(tm + (uint32_t)(acc * 128),
+                        sw128_desc(a0 + (kk >> 2) * kRkBlock + (kk & 3) * 32, 16, 1024),
+                        sw128_desc(b0 + (kk >> 2) * kRkBlock + (kk & 3) * 32, 16, 1024), id_s,
+                        kk > 0 ? 1u : 0u);
+          tc_commit(&accfull[acc]);
+          if (st >= 0) {
+            tc_commit(&empty[st]);
+            ++rt;
+          }
+          ++at;
+        }
+        // the next row block goes into the buffer once these MMAs have read it
+        if (!fail && I + 1 < nb) {
+          tc_commit(afree);
+          if (!wait(afree, (uint32_t)(I & 1))) break;
+          load_tile(abuf, I + 1, afull);
+          ++na;
         }
       }
-      if (row < n) atomicAdd(&inv_s[row], ss);
+      if (fail) misc[0] = 1;
+      // every MMA issued completes before tensor memory is released, and the
+      // last row block requested lands before the CTA may exit
+      tc_commit(drain);
+      (void)mbar_wait_bounded(drain, 0);
+      (void)mbar_wait_bounded(afull, (uint32_t)((na - 1) & 1));
     }
-#pragma unroll
-    for (int c = 0; c < 32; ++c) {
-      const float wm = warp_max(s[c]);
-      const float e = (s[c] == -INFINITY) ? 0.f : exp2f(s[c] - wm);
-      const float ws = warp_sum(e);
-      if (lane == 0) {
-        red[(quarter * kRkQRows + half * 32 + c) * 2] = wm;
-        red[(quarter * kRkQRows + half * 32 + c) * 2 + 1] = ws;
+    __syncwarp();
+  } else {
+    // ---- epilogue warps 0-7 ------------------------------------------------------
+    const int r = quarter * 32 + lane;              // this thread's row of a tile
+    const uint32_t lanes = (uint32_t)(quarter * 32) << 16;
+    bool bad = false;                               // this warp gave up waiting
+    auto wait = [&](uint64_t* bar, uint32_t parity) {
+      if (!bad && (misc[0] || !__all_sync(0xffffffffu, mbar_wait_bounded(bar, parity)))) {
+        bad = true;
+        if (lane == 0) misc[0] = 1;
       }
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (tid < QN) {
-      float m = m_col[tid], l = l_col[tid];
-      for (int q = 0; q < 4; ++q) {
-        const float bm = red[(q * kRkQRows + tid) * 2], bl = red[(q * kRkQRows + tid) * 2 + 1];
-        if (bm == -INFINITY) continue;
-        const float mn = fmaxf(m, bm);
-        l = (m == -INFINITY ? 0.f : l * exp2f(m - mn)) + bl * exp2f(bm - mn);
-        m = mn;
-      }
-      m_col[tid] = m;
-      l_col[tid] = l;
-    }
-    __syncthreads();
-  }
-
-  // 1/||k_i|| (0 for a zero key: never similar), and the smallest ||k|| of every
-  // 32-slot chunk for the quick rejection below
-  __syncthreads();
-  for (int i = tid; i < n; i += kRkThreads) {
-    const float ss = inv_s[i];
-    inv_s[i] = (ss > 0.f) ? rsqrtf(ss) : 0.f;
-  }
-  __syncthreads();
-  if (tid < kRkvMaxSlots / 32) {
-    float mn = INFINITY;
-    for (int c = 0; c < 32; ++c) {
-      const float iv = inv_s[tid * 32 + c];
-      if (iv > 0.f) mn = fminf(mn, 1.f / iv);
-    }
-    nmin[tid] = mn;
-  }
-  __syncthreads();
-
-  // ---- pass 2: importance, then near-duplicate counts over blocks J >= I ---------
-  int tglob = 0;   // K tiles through the ring so far
-  for (int I = 0; I < nb && ok; ++I) {
-    const int row = I * kRkTile + quarter * 32 + lane;   // this thread's token
-    {
-      float s[32];
-      ok = a_tile_logits(I, s);
-      if (!ok) break;
-      float part = 0.f;
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const int col = half * 32 + c;
-        if (col < QN && s[c] != -INFINITY) part += exp2f(s[c] - m_col[col]) / l_col[col];
-      }
-      if (row < n) atomicAdd(&z_s[row], part / (float)QN);
-    }
-    const float inv_i = (row < n) ? inv_s[row] : 0.f;
-    const float thr_i = (inv_i > 0.f) ? ra.tau / inv_i : INFINITY;   // tau * ||k_i||
-    const int pos_i = pos_s[min(row, kRkvMaxSlots - 1)];
-    int cnt = 0;
-    // prologue: the first tiles of this row block's column walk, and its first MMA
-    const int njb = nb - I;
-    if (tid == 0) {
-      for (int q = 0; q < kRkStages && q < njb; ++q)
-        load_tile(ring + ((tglob + q) % kRkStages) * kRkStage, I + q, &full[(tglob + q) % kRkStages]);
-      issued = tglob + min(kRkStages, njb);
-    }
-    auto mma_s = [&](int t) -> bool {   // K_I . K_J^T of ring tile t into accumulator t % 3
-      const int st = t % kRkStages;
-      const int acc = t % kRkAcc;
-      if (!mbar_wait_bounded(&full[st], (uint32_t)((t / kRkStages) & 1))) return false;
-      // the accumulator's previous block (tile t - 3) has been loaded by every warp
-      if (t >= kRkAcc && !mbar_wait_bounded(&accfree[acc], (uint32_t)(((t / kRkAcc) - 1) & 1)))
-        return false;
-      tc_fence_after();
-      const uint32_t a0 = smem_u32(abuf), b0 = smem_u32(ring + st * kRkStage);
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk)
-        tc_mma_bf16(tm + (uint32_t)(acc * 128),
-                    sw128_desc(a0 + (kk >> 2) * kRkBlock + (kk & 3) * 32, 16, 1024),
-                    sw128_desc(b0 + (kk >> 2) * kRkBlock + (kk & 3) * 32, 16, 1024), id_s,
-                    kk > 0 ? 1u : 0u);
-      tc_commit(&accfull[acc]);
-      return true;
+      return !bad;
     };
-    // the first two blocks' MMAs (the MMAs then run two blocks ahead of the epilogue)
-    if (tid == 0) {
-      if (!mma_s(tglob)) misc[0] = 1;
-      if (njb > 1 && !misc[0] && !mma_s(tglob + 1)) misc[0] = 1;
-    }
-    for (int J = I; J < nb; ++J) {
-      const int t = tglob + (J - I);
-      const int acc = t % kRkAcc;
-      if (tid == 0 && J + 2 < nb && !misc[0] && !mma_s(t + 2)) misc[0] = 1;
-      const bool got = (misc[0] == 0) &&
-                       mbar_wait_bounded(&accfull[acc], (uint32_t)((t / kRkAcc) & 1));
-      if (!__all_sync(0xffffffffu, got)) {
-        misc[0] = 1;
-        ok = false;
-        break;
-      }
+    // importance logits of accumulator it % 2 (32 columns from 32 * half),
+    // scaled to log2 units; -inf outside the tokens and the query rows
+    int it = 0;
+    auto imp_logits = [&](int row, float* s) -> bool {
+      const int ib = it & 1;
+      const bool got = wait(&impfull[ib], (uint32_t)((it >> 1) & 1));
+      ++it;
+      if (!got) return false;
       tc_fence_after();
-      // the stage of tile t is free again (its MMAs completed): refill it
-      if (tid == 0 && J + kRkStages < nb) {
-        load_tile(ring + (t % kRkStages) * kRkStage, J + kRkStages, &full[t % kRkStages]);
-        issued = t + kRkStages + 1;
-      }
-      // columns 64*half .. +63 of block J: both warp-collective loads first, then
-      // hand the accumulator back, then each thread's own (divergent) tests
-      float v[2][32];
-      __syncwarp();
-      tmem_ld32(tm + (uint32_t)(acc * 128) + lanes + (uint32_t)(half * 64), v[0]);
-      tmem_ld32(tm + (uint32_t)(acc * 128) + lanes + (uint32_t)(half * 64 + 32), v[1]);
+      __syncwarp();  // tcgen05.ld is warp-collective
+      tmem_ld32(tm + (uint32_t)(kRkImpCol + ib * 64) + lanes + (uint32_t)(half * 32), s);
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&accfree[acc]);
+      if (lane == 0) mbar_arrive(&impfree[ib]);
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const int j0 = J * kRkTile + half * 64 + cc * 32;   // first column token
-        float mx = -INFINITY;
+      for (int c = 0; c < 32; ++c)
+        s[c] = (row < n && half * 32 + c < QN) ? s[c] * ra.scale_log2 : -INFINITY;
+      return true;
+    };
+
+    // ---- pass 1: every observation query's max and softmax denominator, kept
+    // per thread over its own rows (online), and ||k||^2 --------------------------
+    float m[32], l[32];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) mx = fmaxf(mx, v[cc][c]);
-        // quick rejection: cos >= tau needs S_ij >= tau ||k_i|| ||k_j|| >= thr_i * min ||k_j||
-        if (mx < thr_i * nmin[j0 >> 5]) continue;
+    for (int c = 0; c < 32; ++c) {
+      m[c] = -INFINITY;
+      l[c] = 0.f;
+    }
+    for (int t = 0; t < nb; ++t) {
+      const int row = t * kRkTile + r;
+      const int st = t % kRkStages;
+      float s[32];
+      const bool got = imp_logits(row, s) && wait(&full[st], (uint32_t)((t / kRkStages) & 1));
+      if (got) {
+        // ||k||^2 of this thread's token, d-half `half`, from the tile in shared memory
+        // (row r of the 64-column block at r * 128 bytes, 16-byte chunks swizzled by r mod 8)
+        const unsigned char* rp = ring + st * kRkStage + half * kRkBlock + r * 128;
+        float ss = 0.f;
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          const uint4 w = *reinterpret_cast<const uint4*>(rp + ((ch ^ (r & 7)) << 4));
+          const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&w);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = __bfloat1622float2(h2[e]);
+            ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
+          }
+        }
+        if (row < n) atomicAdd(&inv_s[row], ss);
+      }
+      // every epilogue warp has read the stage (the MMAs on it completed before
+      // the logits were ready): hand it back to the producer
+      named_bar_sync(1, kRkEpi);
+      if (tid == 0 && !misc[0]) mbar_arrive(&empty[st]);
+      if (got) {
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
-          const int j = j0 + c;
-          const bool valid = row < n && j < n && (J != I || j > row);
-          if (valid && v[cc][c] * inv_s[j] >= thr_i) {
-            if (pos_s[j] > pos_i) ++cnt;                 // a later near-duplicate of i
-            else atomicAdd(&cnt_s[j], 1);                 // i is the later one: j is older
+          const float x = s[c];
+          const float mn = fmaxf(m[c], x);   // branch-free: every lane the same path
+          if (mn != -INFINITY) {
+            l[c] = l[c] * exp2f(m[c] - mn) + exp2f(x - mn);
+            m[c] = mn;
           }
         }
       }
     }
-    // every warp is through this row block (and every accumulator it used is free)
-    ok = __syncthreads_and(ok && misc[0] == 0);
-    tglob += njb;
-    if (!ok) break;
-    if (row < n && cnt) atomicAdd(&cnt_s[row], cnt);
-    __syncthreads();
-    // block I is final: Z_i = lambda I_i - (1 - lambda) R_i
-    if (half == 0 && row < n) {
-      const float red_i = (cnt_s[row] >= ra.beta) ? 1.f : 0.f;
-      z_s[row] = ra.lam * z_s[row] - (1.f - ra.lam) * red_i;
-    }
-  }
-  ok = __syncthreads_and(ok && misc[0] == 0);
-
-  // ---- selection: observation tokens first, then Z descending, ties to later ----
-  if (ok) {
-    int np2 = 256;
-    while (np2 < n) np2 <<= 1;
-    unsigned long long* key = reinterpret_cast<unsigned long long*>(ring);
-    uint16_t* idx = reinterpret_cast<uint16_t*>(ring + kRkvMaxSlots * 8);
-    for (int i = tid; i < np2; i += kRkThreads) {
-      if (i < n) {
-        const bool obs = pos_s[i] >= pnext - ra.alpha;
-        const uint32_t hi = obs ? 0xFFFFFFFFu : orderable(z_s[i]);
-        key[i] = ((unsigned long long)hi << 32) | (uint32_t)pos_s[i];
-      } else {
-        key[i] = 0ull;
+    // merge the rows: the 32 lanes of the warp, then the four quarters
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+      float mc = m[c], lc = l[c];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float mo = __shfl_xor_sync(0xffffffffu, mc, o);
+        const float lo = __shfl_xor_sync(0xffffffffu, lc, o);
+        const float mn = fmaxf(mc, mo);
+        if (mn != -INFINITY) {
+          lc = lc * exp2f(mc - mn) + lo * exp2f(mo - mn);
+          mc = mn;
+        }
       }
-      idx[i] = (uint16_t)i;
+      if (lane == 0) {
+        red[(quarter * kRkQRows + half * 32 + c) * 2] = mc;
+        red[(quarter * kRkQRows + half * 32 + c) * 2 + 1] = lc;
+      }
     }
-    __syncthreads();
-    // bitonic sort, descending
-    for (int kk = 2; kk <= np2; kk <<= 1) {
-      for (int jj = kk >> 1; jj > 0; jj >>= 1) {
-        for (int i = tid; i < np2; i += kRkThreads) {
-          const int ixj = i ^ jj;
-          if (ixj > i) {
-            const bool desc = (i & kk) == 0;
-            const unsigned long long a = key[i], c = key[ixj];
-            if (desc ? (a < c) : (a > c)) {
-              key[i] = c;
-              key[ixj] = a;
-              const uint16_t t = idx[i];
-              idx[i] = idx[ixj];
-              idx[ixj] = t;
+    named_bar_sync(1, kRkEpi);
+    if (tid < QN) {
+      float mc = -INFINITY, lc = 0.f;
+      for (int q = 0; q < 4; ++q) {
+        const float bm = red[(q * kRkQRows + tid) * 2], bl = red[(q * kRkQRows + tid) * 2 + 1];
+        if (bm == -INFINITY) continue;
+        const float mn = fmaxf(mc, bm);
+        lc = (mc == -INFINITY ? 0.f : lc * exp2f(mc - mn)) + bl * exp2f(bm - mn);
+        mc = mn;
+      }
+      m_col[tid] = mc;
+      l_col[tid] = lc;
+    }
+    // 1/||k_i|| (0 for a zero key: never similar), and the smallest ||k|| of every
+    // 32-slot chunk for the quick rejection below
+    for (int i = tid; i < n; i += kRkEpi) {
+      const float ss = inv_s[i];
+      inv_s[i] = (ss > 0.f) ? rsqrtf(ss) : 0.f;
+    }
+    named_bar_sync(1, kRkEpi);
+    if (tid < kRkvMaxSlots / 32) {
+      float mn = INFINITY;
+      for (int c = 0; c < 32; ++c) {
+        const float iv = inv_s[tid * 32 + c];
+        if (iv > 0.f) mn = fminf(mn, 1.f / iv);
+      }
+      nmin[tid] = mn;
+    }
+    named_bar_sync(1, kRkEpi);
+
+    // ---- pass 2: importance, then near-duplicate counts over blocks J >= I ---------
+    int at = 0;
+    for (int I = 0; I < nb; ++I) {
+      const int row = I * kRkTile + r;   // this thread's token
+      {
+        float s[32];
+        if (imp_logits(row, s)) {
+          float part = 0.f;
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int col = half * 32 + c;
+            if (col < QN && s[c] != -INFINITY) part += exp2f(s[c] - m_col[col]) / l_col[col];
+          }
+          if (row < n) atomicAdd(&z_s[row], part / (float)QN);
+        }
+      }
+      const float inv_i = (row < n) ? inv_s[row] : 0.f;
+      const float thr_i = (inv_i > 0.f) ? ra.tau / inv_i : INFINITY;   // tau * ||k_i||
+      const int pos_i = pos_s[min(row, kRkvMaxSlots - 1)];
+      int cnt = 0;
+      for (int J = I; J < nb; ++J, ++at) {
+        const int acc = at % kRkAcc;
+        if (!wait(&accfull[acc], (uint32_t)((at / kRkAcc) & 1))) continue;
+        tc_fence_after();
+        // columns 64*half .. +63 of block J: both warp-collective loads first, then
+        // hand the accumulator back, then each thread's own (divergent) tests
+        float v[2][32];
+        __syncwarp();
+        tmem_ld32(tm + (uint32_t)(acc * 128) + lanes + (uint32_t)(half * 64), v[0]);
+        tmem_ld32(tm + (uint32_t)(acc * 128) + lanes + (uint32_t)(half * 64 + 32), v[1]);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&accfree[acc]);
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const int j0 = J * kRkTile + half * 64 + cc * 32;   // first column token
+          float mx = -INFINITY;
+#pragma unroll
+          for (int c = 0; c < 32; ++c) mx = fmaxf(mx, v[cc][c]);
+          // quick rejection: cos >= tau needs S_ij >= tau ||k_i|| ||k_j|| >= thr_i * min ||k_j||
+          if (mx < thr_i * nmin[j0 >> 5]) continue;
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int j = j0 + c;
+            const bool valid = row < n && j < n && (J != I || j > row);
+            if (valid && v[cc][c] * inv_s[j] >= thr_i) {
+              if (pos_s[j] > pos_i) ++cnt;                 // a later near-duplicate of i
+              else atomicAdd(&cnt_s[j], 1);                 // i is the later one: j is older
             }
           }
         }
-        __syncthreads();
       }
+      if (row < n && cnt) atomicAdd(&cnt_s[row], cnt);
     }
-    // kept flags (reuse the counts)
-    for (int i = tid; i < kRkvMaxSlots; i += kRkThreads) cnt_s[i] = 0;
+  }
+  const bool ok = __syncthreads_and(misc[0] == 0);
+
+  // ---- selection: observation tokens first, then Z descending, ties to later ----
+  // Every token gets a unique 64-bit key (observation flag or orderable Z, then
+  // its position); the `budget` largest keys stay.  A radix select finds the
+  // m-th smallest key, m = n - budget, 8 bits per pass from the top: count the
+  // keys that share the prefix found so far by their next byte, then take the
+  // byte in which the remaining rank falls.  Tokens above that key are kept.
+  if (ok) {
+    // every count is in: Z_i = lambda I_i - (1 - lambda) R_i
+    for (int i = tid; i < n; i += kRkThreads)
+      z_s[i] = ra.lam * z_s[i] - (1.f - ra.lam) * ((cnt_s[i] >= ra.beta) ? 1.f : 0.f);
     __syncthreads();
-    for (int r = tid; r < ra.budget; r += kRkThreads) cnt_s[idx[r]] = 1;
+    unsigned long long* key = reinterpret_cast<unsigned long long*>(ring);   // [n]
+    int* hist = reinterpret_cast<int*>(ring + kRkvMaxSlots * 8);            // [256]
+    unsigned long long* sel_prefix = reinterpret_cast<unsigned long long*>(smem + kOffMisc + 16);
+    int* sel_rank = reinterpret_cast<int*>(smem + kOffMisc + 24);
+    for (int i = tid; i < n; i += kRkThreads) {
+      const bool obs = pos_s[i] >= pnext - ra.alpha;
+      const uint32_t hi = obs ? 0xFFFFFFFFu : orderable(z_s[i]);
+      key[i] = ((unsigned long long)hi << 32) | (uint32_t)pos_s[i];
+    }
+    if (tid == 0) {
+      *sel_prefix = 0ull;
+      *sel_rank = n - ra.budget;   // 1-based rank of the largest dropped key
+    }
+    const int nwalk = (n + kRkThreads - 1) / kRkThreads * kRkThreads;
+    for (int shift = 56; shift >= 0; shift -= 8) {
+      if (tid < 256) hist[tid] = 0;
+      __syncthreads();
+      const unsigned long long prefix = *sel_prefix;
+      const unsigned long long hmask = (shift == 56) ? 0ull : (~0ull << (shift + 8));
+      // warp-aggregated counts: lanes with the same byte add once
+      for (int i = tid; i < nwalk; i += kRkThreads) {
+        int digit = 256;
+        if (i < n) {
+          const unsigned long long k = key[i];
+          if ((k & hmask) == prefix) digit = (int)((k >> shift) & 255u);
+        }
+        const unsigned peers = __match_any_sync(0xffffffffu, digit);
+        if (digit < 256 && lane == __ffs(peers) - 1) atomicAdd(&hist[digit], __popc(peers));
+      }
+      __syncthreads();
+      if (warp == 0) {
+        // lane L holds bytes 8L .. 8L+7; find the byte where the rank falls
+        int c[8], sum = 0;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          c[q] = hist[lane * 8 + q];
+          sum += c[q];
+        }
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const int rank = *sel_rank;
+        const int excl = incl - sum;
+        if (rank > excl && rank <= incl) {
+          // the first of this lane's bytes at which the running count reaches the rank
+          int below = excl, qs = 7;
+          bool found = false;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            if (!found && below + c[q] >= rank) {
+              qs = q;
+              found = true;
+            } else if (!found) {
+              below += c[q];
+            }
+          }
+          *sel_prefix = prefix | ((unsigned long long)(lane * 8 + qs) << shift);
+          *sel_rank = rank - below;
+        }
+      }
+      __syncthreads();
+    }
+    // kept flags (reuse the counts): every key above the largest dropped one
+    const unsigned long long kcut = *sel_prefix;
+    for (int i = tid; i < kRkvMaxSlots; i += kRkThreads) cnt_s[i] = (i < n && key[i] > kcut) ? 1 : 0;
     __syncthreads();
     // ---- move: kept buffer tokens into the freed retained slots, in slot order ----
     int* freed = reinterpret_cast<int*>(ring);                  // reuse the ring
@@ -475,12 +628,9 @@ __global__ void __launch_bounds__(kRkThreads, 1) rkv_compress_kernel(const __gri
       if (tid == 0) ra.count[unit] = ra.budget;
     }
   } else if (tid == 0) {
-    // A wait ran out: leave the unit as it was, and let every copy this CTA
-    // requested land before its shared memory is released.
+    // A wait ran out: leave the unit as it was (the producer has waited for every
+    // copy it requested, the MMA warp for every MMA).
     atomicOr(ra.err, LF_DEVERR_TIMEOUT);
-    for (int t = max(0, issued - kRkStages); t < issued; ++t)
-      (void)mbar_wait_bounded(&full[t % kRkStages], (uint32_t)((t / kRkStages) & 1));
-    if (n_a > 0) (void)mbar_wait_bounded(afull, (uint32_t)((n_a - 1) & 1));
   }
 
   // ---- teardown ----------------------------------------------------------------
@@ -495,6 +645,8 @@ __global__ void __launch_bounds__(kRkThreads, 1) rkv_compress_kernel(const __gri
 }  // namespace
 
 int rkv_smem_bytes() { return kSmem; }
+
+int rkv_threads() { return kRkThreads; }
 
 const void* find_rkv_kernel(int group) {
   switch (group) {

@@ -23,8 +23,9 @@ struct RkvArgs {
   float lam, tau, scale_log2;     // lambda, cosine threshold, log2(e)/sqrt(128)
 };
 
-// Dynamic shared memory of one compression CTA.
+// Dynamic shared memory and threads of one compression CTA.
 int rkv_smem_bytes();
+int rkv_threads();
 // __global__ void(RkvArgs) for q_heads / kv_heads = group, or null.
 const void* find_rkv_kernel(int group);
 
