@@ -243,6 +243,16 @@ def cpu_baseline(wl_name: str, seconds: float):
                       f"step evicts); {units} units total"}
 
 
+def workload_config(wl, layers: int) -> dict:
+    """The workload keys of `config`, the same in both arms."""
+    return {"workload": wl.name, "layers": layers, "batch": wl.batch, "q_heads": wl.q_heads,
+            "kv_heads": wl.kv_heads, "head_dim": wl.head_dim, "budget": wl.budget,
+            "window": wl.window,
+            "state": ("steady (pre-filled to the budget, every step evicts)"
+                      if wl.prefill >= wl.budget else
+                      f"prompt {wl.prefill}, timed from the start of generation")}
+
+
 def bench_reference(args):
     """--impl reference: the oracle as the reference arm on the host cores."""
     rank = int(os.environ.get("RANK", "0"))
@@ -255,11 +265,15 @@ def bench_reference(args):
         run_oracle(args.workload, cores, steps=args.warmup)
     units, wall = run_oracle(args.workload, cores, steps=args.steps)
     value = units / wall
+    from synth import workloads as stream_mod
+    wl = stream_mod.get_workload(args.workload)
+    config = workload_config(wl, args.layers or wl.layers)
+    config["sample"] = "one (layer, sequence) unit per worker per step, at steady state"
     line = {"metric": METRIC, "value": value, "unit": UNIT, "impl": "reference",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1000.0 * wall / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload},
+            "config": config,
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": f"each of {cores} spawn workers runs {args.steps} fp64 "
                                        f"oracle steps of one {args.workload}-shaped (layer, "
@@ -650,11 +664,8 @@ def bench_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if
         wl.dtype == "bf16" else "f32", "data": "synthetic",
-        "config": {"workload": wl.name, "layers": L, "batch": wl.batch, "q_heads": wl.q_heads,
-                   "kv_heads": wl.kv_heads, "head_dim": wl.head_dim, "budget": wl.budget,
-                   "window": wl.window, "state": ("steady (pre-filled to the budget, every step "
-                   "evicts)" if wl.prefill >= wl.budget else f"prompt {wl.prefill}, timed from "
-                   "the start of generation"), "l2": "inputs larger than L2: each layer's slab is "
+        "config": {**workload_config(wl, L),
+                   "l2": "inputs larger than L2: each layer's slab is "
                    f"{wl.batch * wl.kv_heads * lay.slot_stride * wl.head_dim * 2 * wl.elem_bytes / 1e6:.0f} MB",
                    "cluster": lay.cluster, "stages": lay.stages,
                    "launch": "eager" if args.eager else "CUDA graph of all timed steps",
