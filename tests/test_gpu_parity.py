@@ -157,3 +157,19 @@ def test_nonfinite_query_sets_error_word():
     assert c.check() & LF_DEVERR_NONFINITE
     assert c.check() == 0  # cleared by the read
     c.close()
+
+
+@pytest.mark.parametrize("kernel,budget,cluster", [
+    ("simt", 1, 0), ("simt", 2, 2), ("tc", 1, 0), ("tc", 2, 2), ("tc", 3, 16)])
+def test_degenerate_budgets(kernel, budget, cluster):
+    """Budgets of 1-3 slots with window 0, batch 1: every step past the prompt
+    evicts one of a handful of candidates (budget 1: the only cached slot), and
+    most CTAs of a cluster own no slot at all."""
+    if kernel == "tc":
+        wl = WORKLOADS["r1-llama-8b"].scaled(layers=1, batch=1, q_heads=8, kv_heads=2,
+                                              budget=budget, window=0, prefill=1,
+                                              v_lognormal_sigma=0.5)
+    else:
+        wl = WORKLOADS["tiny-fp32"].scaled(budget=budget, window=0, prefill=1)
+    st = _run(wl, 40, cluster=cluster, kernel=kernel)
+    assert st.evictions == 40 * wl.kv_heads - (budget - 1) * wl.kv_heads
