@@ -235,12 +235,16 @@ def run_oracle(wl_name: str, workers: int, seconds: float = 0.0, steps: int = 0)
 
 
 def cpu_baseline(wl_name: str, seconds: float):
+    """The oracle on every host core (the reported value) and on one core."""
     cores = os.cpu_count() or 1
     units, wall = run_oracle(wl_name, cores, seconds=seconds)
+    one_units, one_wall = run_oracle(wl_name, 1, seconds=max(1.0, seconds / 3))
     return {"value": units / wall, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "single_core_value": one_units / one_wall,
             "sample": f"{cores} spawn workers x ~{seconds:.0f} s each of fp64 oracle steps of one "
                       f"{wl_name}-shaped (layer, sequence) at steady state (full buffer, every "
-                      f"step evicts); {units} units total"}
+                      f"step evicts); {units} units total. single_core_value: one worker, "
+                      f"~{max(1.0, seconds / 3):.0f} s, {one_units} units"}
 
 
 def workload_config(wl, layers: int) -> dict:
