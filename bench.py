@@ -118,6 +118,15 @@ def aggregate(ms_local: float, units_local: int, dist=None):
     return float(t.item()), int(u.item())
 
 
+def load_tensor_peak():
+    """Measured dense bf16 TFLOP/s (burst: the compression is timed on its own)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
 def load_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -432,6 +441,9 @@ def bench_rkv(args, torch, lf, stream_mod, peak, longflow_units_per_s):
         "compress_ms_per_layer": comp_ms / L,
         "compress_share_of_cycle": comp_ms / (dec_ms + comp_ms),
         "compress_tensor_tflops": flops_unit * comp_units / (comp_ms / 1000.0) / 1e12,
+        "compress_frac_of_tensor_peak": (flops_unit * comp_units / (comp_ms / 1000.0) / 1e12
+                                         / load_tensor_peak()[0]),
+        "tensor_peak_kind": load_tensor_peak()[1],
         "counts_after": [int(counts.min()), int(counts.max())],
         "longflow_units_per_s_same_geometry": longflow_units_per_s,
         "longflow_over_rkv": longflow_units_per_s / value,
