@@ -632,9 +632,20 @@ int lf_decode_step(lf_cache* cache, int layer, const void* q, const void* k_new,
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   if (cache->scope == LF_SCOPE_LAYER) {
     // The shared victim of every sequence, once all its KV heads have scored.
+    // Programmatic dependent launch: its CTAs are placed while the decode grid
+    // drains and wait for it in griddepcontrol.wait.
     void* args[] = {&a};
-    e = cudaLaunchKernel(cache->kern.select, dim3(cache->batch, 1, 1), dim3(lf::kThreads, 1, 1),
-                         args, 0, static_cast<cudaStream_t>(stream));
+    cudaLaunchConfig_t sc = {};
+    sc.gridDim = dim3(cache->batch, 1, 1);
+    sc.blockDim = dim3(lf::kSelThreads, 1, 1);
+    sc.dynamicSmemBytes = 0;
+    sc.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute sa[1];
+    sa[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    sa[0].val.programmaticStreamSerializationAllowed = 1;
+    sc.attrs = sa;
+    sc.numAttrs = 1;
+    e = cudaLaunchKernelExC(&sc, cache->kern.select, args);
     if (e != cudaSuccess) return cuda_fail(e, "layer-scope selection launch");
   }
   return LF_OK;

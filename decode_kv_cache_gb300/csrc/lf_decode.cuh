@@ -672,16 +672,22 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_simt_kernel(const Dec
 // per-slot scores (+inf for slots that are not candidates), takes the lowest
 // (ties to the lowest slot), and either records it as the slot the next token
 // takes (deferred) or writes every KV head's new token into it.
+constexpr int kSelThreads = 1024;
+constexpr int kSelWarps = kSelThreads / 32;
+
 template <typename T, int D>
-__global__ void __launch_bounds__(kThreads) select_layer_kernel(const DecodeArgs a) {
-  __shared__ float rs[kWarps];
-  __shared__ int ri[kWarps];
+__global__ void __launch_bounds__(kSelThreads) select_layer_kernel(const DecodeArgs a) {
+  __shared__ float rs[kSelWarps];
+  __shared__ int ri[kSelWarps];
   __shared__ int pick;
   const int b = blockIdx.x;
   const int u0 = b * a.kv_heads;
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
+  // Launched as a programmatic dependent of the decode grid: wait until that
+  // grid has completed and its writes are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // Every KV head's attention kernel leaves the same request: the slots it
   // scored, + 1 (0: nothing to choose this step).
   const int req = a.lw_req[u0];
@@ -691,18 +697,32 @@ __global__ void __launch_bounds__(kThreads) select_layer_kernel(const DecodeArgs
   __syncthreads();  // every thread has read the requests
   if (!same || req < 2) {
     if (tid == 0) atomicOr(a.err, LF_DEVERR_STATE);
-    for (int g = tid; g < a.kv_heads; g += kThreads) a.lw_req[u0 + g] = 0;
+    for (int g = tid; g < a.kv_heads; g += kSelThreads) a.lw_req[u0 + g] = 0;
     return;
   }
   const int scored = req - 1;
   float bs = INFINITY;
   int bi = INT_MAX;
-  for (int i = tid; i < scored; i += kThreads) {
-    float sc = 0.f;
-    for (int g = 0; g < a.kv_heads; ++g) sc += a.lw_score[(size_t)(u0 + g) * a.slot_stride + i];
-    if (sc < INFINITY && better(sc, i, bs, bi)) {
-      bs = sc;
-      bi = i;
+  // Four consecutive slots per thread and step, one 16-byte load per KV head
+  // (every scratch row starts on a 16-byte boundary: slot_stride is a multiple
+  // of 32); the heads are summed in order, slots past `scored` are skipped.
+  for (int i0 = 4 * tid; i0 < scored; i0 += 4 * kSelThreads) {
+    float sc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int g = 0; g < a.kv_heads; ++g) {
+      const float4 x =
+          *reinterpret_cast<const float4*>(a.lw_score + (size_t)(u0 + g) * a.slot_stride + i0);
+      sc[0] += x.x;
+      sc[1] += x.y;
+      sc[2] += x.z;
+      sc[3] += x.w;
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int i = i0 + q;
+      if (i < scored && sc[q] < INFINITY && better(sc[q], i, bs, bi)) {
+        bs = sc[q];
+        bi = i;
+      }
     }
   }
 #pragma unroll
@@ -720,7 +740,7 @@ __global__ void __launch_bounds__(kThreads) select_layer_kernel(const DecodeArgs
   }
   __syncthreads();
   if (tid == 0) {
-    for (int w = 1; w < kWarps; ++w)
+    for (int w = 1; w < kSelWarps; ++w)
       if (better(rs[w], ri[w], bs, bi)) {
         bs = rs[w];
         bi = ri[w];
@@ -731,9 +751,9 @@ __global__ void __launch_bounds__(kThreads) select_layer_kernel(const DecodeArgs
   __syncthreads();
   const int e = pick;
   if (a.deferred) {
-    for (int g = tid; g < a.kv_heads; g += kThreads) a.pending[u0 + g] = e;
+    for (int g = tid; g < a.kv_heads; g += kSelThreads) a.pending[u0 + g] = e;
   } else {
-    for (int g = warp; g < a.kv_heads; g += kWarps) {
+    for (int g = warp; g < a.kv_heads; g += kSelWarps) {
       const int u = u0 + g;
       if (e >= 0) {
         const size_t ubase = (size_t)u * a.slot_stride;
@@ -744,7 +764,7 @@ __global__ void __launch_bounds__(kThreads) select_layer_kernel(const DecodeArgs
       if (lane == 0) a.evicted[u] = e;
     }
   }
-  for (int g = tid; g < a.kv_heads; g += kThreads) a.lw_req[u0 + g] = 0;
+  for (int g = tid; g < a.kv_heads; g += kSelThreads) a.lw_req[u0 + g] = 0;
 }
 
 // ---- prefill ----------------------------------------------------------------
