@@ -51,7 +51,9 @@
  * lf_prefill_fill's upload of the host prompt lengths, and create/destroy.
  *
  * Threading: a cache may be used from any host thread, but calls touching the
- * same layer must be ordered by the caller (same stream, or events).
+ * same layer must be ordered by the caller (same stream, or events).  With
+ * scope = LF_SCOPE_LAYER every lf_decode_step of a cache must be ordered: the
+ * per-slot score scratch the selection reads is one layer's, reused by all.
  * Device: every call must run with the device that was current at create.
  *
  * Errors: functions return LF_OK (0) or a negative lf_status and set a
