@@ -366,11 +366,12 @@ def time_steps(cache, inputs, outs, evs, torch, graph: bool):
     return start.elapsed_time(end)
 
 
-def bench_rkv(args, torch, lf, stream_mod, peak, longflow_units_per_s):
+def bench_rkv(args, torch, lf, stream_mod, peak):
     """R-KV's cycle on rkv-r1-llama-8b: `buffer` decode steps that append into
     the staging buffer, then one compression per layer (lf_rkv_compress).
     Returns amortised units/s, the decode and compression rates, and the ratio
-    to LongFlow's units/s on the same head geometry and budget."""
+    to LongFlow measured on the same geometry (layers, batch, heads, budget,
+    steady state, the window of the r1-llama-8b configuration)."""
     wl = stream_mod.get_workload("rkv-r1-llama-8b")
     L = min(wl.layers, args.rkv_layers)
     wl = wl.scaled(layers=L)
@@ -421,6 +422,21 @@ def bench_rkv(args, torch, lf, stream_mod, peak, longflow_units_per_s):
     del cache, gen, steps, qobs
     torch.cuda.empty_cache()
     units = wl.batch * L * buf
+    # LongFlow on the same geometry: a cache at the same budget, filled to it, timed
+    # over the same number of decode steps (every step evicts)
+    lwl = wl.scaled(window=stream_mod.get_workload("r1-llama-8b").window, prefill=B)
+    lcache, lgen = build_cache(lwl, torch, lf, stream_mod, seed=301)
+    lwarm = pregenerate(lgen, 3, torch)
+    time_steps(lcache, lwarm, outs, evs, torch, graph=False)
+    del lwarm
+    lsteps = pregenerate(lgen, buf, torch)
+    lf_ms = time_steps(lcache, lsteps, outs, evs, torch, graph=not args.eager)
+    if lcache.check() != 0:
+        raise RuntimeError("device error in the LongFlow run on the R-KV geometry")
+    lcache.close()
+    del lcache, lgen, lsteps
+    torch.cuda.empty_cache()
+    longflow_units_per_s = units / (lf_ms / 1000.0)
     # decode bytes: occupancy grows from B to B + buf - 1 over the cycle
     dec_bytes = sum(unit_bytes(wl, B + t) for t in range(buf)) * wl.batch * L
     # compression: the key dot products of the blocks J >= I plus two importance passes
@@ -446,6 +462,8 @@ def bench_rkv(args, torch, lf, stream_mod, peak, longflow_units_per_s):
         "tensor_peak_kind": load_tensor_peak()[1],
         "counts_after": [int(counts.min()), int(counts.max())],
         "longflow_units_per_s_same_geometry": longflow_units_per_s,
+        "longflow_geometry": f"{L} layers, batch {wl.batch}, budget {B}, window {lwl.window}, "
+                             f"steady, {buf} steps",
         "longflow_over_rkv": longflow_units_per_s / value,
     }
 
@@ -668,7 +686,7 @@ def bench_ours(args):
     # ---- R-KV, the pages' baseline, on its own workload (fewer layers) ----
     rkv = None
     if args.rkv and rank == 0:
-        rkv = bench_rkv(args, torch, lf, stream_mod, peak, value)
+        rkv = bench_rkv(args, torch, lf, stream_mod, peak)
 
     if rank != 0:
         return 0
