@@ -45,6 +45,10 @@ struct lf_cache {
   lf::KernelEntry kern;
   int threads;    // CTA size of the decode kernel
   int grid_y;     // tensor-core path: resident clusters (persistent grid)
+  int split_rem;  // tensor-core path: last-round units shared by two clusters (0: none)
+  float* split_stat;  // ... their exchanges through global memory (see TcArgs)
+  float* split_fin;
+  int32_t* split_cnt;
   CUtensorMap tmaps[4];  // tensor-core path: K and V as 2-D [rows][head_dim], two box heights
 };
 
@@ -285,7 +289,13 @@ lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, i
   if ((e = cudaFuncSetAttribute(kern.decode, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 max_optin)) != cudaSuccess ||
       (e = cudaFuncSetAttribute(kern.decode, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) !=
-          cudaSuccess) {
+          cudaSuccess ||
+      (kern.decode_split &&
+       ((e = cudaFuncSetAttribute(kern.decode_split, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  max_optin)) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(kern.decode_split,
+                                  cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) !=
+            cudaSuccess))) {
     cuda_fail(e, "cudaFuncSetAttribute");
     return nullptr;
   }
@@ -376,6 +386,18 @@ lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, i
   cache->threads = threads;
   cache->grid_y = grid_y;
   cache->items = items;
+  // Split launches: when the units left over after the whole rounds fill at
+  // most half of the clusters, each of them is shared by two clusters (the
+  // last round then takes about half as long).  Only for the per-KV-head
+  // LongFlow score without the deferred order, and for the append modes.
+  if (tc) {
+    const int rem = units % grid_y;
+    const bool plain = !kevict || (c.score == LF_SCORE_LONGFLOW && c.scope == LF_SCOPE_KV_HEAD &&
+                                   !c.deferred);
+    if (rem > 0 && 2 * rem <= grid_y && 2 * cluster <= lf::kMaxSplitParts && plain &&
+        kern.decode_split)
+      cache->split_rem = rem;
+  }
   cache->score = c.score;
   cache->norm = c.norm;
   cache->sinks = c.sinks;
@@ -403,7 +425,13 @@ lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, i
   size_t off_lws = round_up(off_pend + (c.deferred ? n_units * 4 : 0), 256);
   size_t off_lwr = round_up(off_lws + (layer ? lunits * cache->slot_stride * 4 : 0), 256);
   size_t off_lwa = round_up(off_lwr + (layer ? lunits * 4 : 0), 256);
-  size_t small_bytes = round_up(off_lwa + (layer ? lunits * 4 : 0), 256);
+  // split launches: [rem][2C][2 kMaxGroup] statistics, [rem][2C][G d + 4] partial
+  // outputs, [rem][2] counters
+  const size_t nsp = (size_t)cache->split_rem * 2 * cluster;
+  size_t off_sst = round_up(off_lwa + (layer ? lunits * 4 : 0), 256);
+  size_t off_sfn = round_up(off_sst + nsp * 2 * lf::kMaxGroup * 4, 256);
+  size_t off_scn = round_up(off_sfn + nsp * ((size_t)group * head_dim + 4) * 4, 256);
+  size_t small_bytes = round_up(off_scn + (size_t)cache->split_rem * 2 * 4, 256);
 
   if ((e = cudaMalloc(&cache->K, kv_bytes)) != cudaSuccess ||
       (e = cudaMalloc(&cache->V, kv_bytes)) != cudaSuccess ||
@@ -426,6 +454,9 @@ lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, i
   cache->lw_score = layer ? reinterpret_cast<float*>(s + off_lws) : nullptr;
   cache->lw_req = layer ? reinterpret_cast<int32_t*>(s + off_lwr) : nullptr;
   cache->lw_anew = layer ? reinterpret_cast<float*>(s + off_lwa) : nullptr;
+  cache->split_stat = cache->split_rem ? reinterpret_cast<float*>(s + off_sst) : nullptr;
+  cache->split_fin = cache->split_rem ? reinterpret_cast<float*>(s + off_sfn) : nullptr;
+  cache->split_cnt = cache->split_rem ? reinterpret_cast<int32_t*>(s + off_scn) : nullptr;
 
   // Empty state: no occupied slot, positions -1, ||v||_1 0, K/V zero.
   int32_t* hb = new (std::nothrow) int32_t[batch];
@@ -623,8 +654,13 @@ int lf_decode_step(lf_cache* cache, int layer, const void* q, const void* k_new,
     ta.a = a;
     ta.row_base = (int)(layer * layer_slots);
     ta.max_items = cache->items;
+    ta.split_rem = cache->split_rem;
+    ta.split_stat = cache->split_stat;
+    ta.split_fin = cache->split_fin;
+    ta.split_cnt = cache->split_cnt;
     void* args[] = {&ta};
-    e = cudaLaunchKernelExC(&cfg, cache->kern.decode, args);
+    e = cudaLaunchKernelExC(&cfg, cache->split_rem ? cache->kern.decode_split : cache->kern.decode,
+                            args);
   } else {
     void* args[] = {&a};
     e = cudaLaunchKernelExC(&cfg, cache->kern.decode, args);

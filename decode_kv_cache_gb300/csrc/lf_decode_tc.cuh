@@ -68,7 +68,37 @@ struct TcArgs {
   DecodeArgs a;
   int row_base;                    // tensor row of this layer's first slot
   int max_items;                   // units one cluster may visit (sizes the item table)
+  // Split launches (kernel instantiated with kSplit): the units left over after
+  // the whole rounds are each shared by two clusters, which exchange through
+  // global memory (they are co-resident: the grid is persistent).
+  int split_rem;                   // units shared by two clusters (units mod clusters)
+  float* split_stat;               // [split_rem][2C][2 kMaxGroup]: each piece's (m_h, l_h)
+  float* split_fin;                // [split_rem][2C][G D + 4]: partial output, score, slot, flag
+  int* split_cnt;                  // [split_rem][2]: arrivals at the two exchanges
 };
+
+// Split launches: at most this many CTAs share a unit (clusters of 1 or 2).
+constexpr int kMaxSplitParts = 4;
+
+// Split launches: spin, with a bound, until another CTA of this persistent grid
+// (all of them are resident) has counted itself in.
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ bool wait_count_bounded(const int* cnt, int target) {
+  if (ld_acquire_gpu(cnt) >= target) return true;
+  const unsigned long long t0 = global_ns();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i) {
+      if (ld_acquire_gpu(cnt) >= target) return true;
+      __nanosleep(32);
+    }
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
 
 template <int G>
 struct TcPlan {
@@ -116,7 +146,7 @@ struct TcPlan {
   }
 };
 
-template <int G>
+template <int G, bool kSplit = false>
 __global__ void __launch_bounds__(kTcThreads, 1)
     decode_step_tc_kernel(const __grid_constant__ TcArgs ta) {
   constexpr int D = 128;
@@ -137,7 +167,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int S = a.stages;
   const int chunk = a.chunk;
   const int units = a.batch * a.kv_heads;
-  const int nitems = (j < units) ? (units - j + NC - 1) / NC : 0;
+  // Whole units: cluster j takes j, j + NC, ...  Split launches: after `rounds`
+  // whole rounds, cluster j < 2 split_rem takes half (j & 1) of unit
+  // rounds NC + j / 2 as its last item, shared with cluster j ^ 1.
+  const int rounds = kSplit ? (units - ta.split_rem) / NC : 0;
+  const bool has_piece = kSplit && j < 2 * ta.split_rem;
+  const int nitems = kSplit ? rounds + (has_piece ? 1 : 0)
+                            : ((j < units) ? (units - j + NC - 1) / NC : 0);
+  auto unit_of = [&](int k) { return (kSplit && k == rounds) ? rounds * NC + (j >> 1) : j + k * NC; };
+  auto is_piece = [&](int k) { return kSplit && k == rounds; };
   if (nitems > ta.max_items) {  // the host sized the item table for fewer units
     if (threadIdx.x == 0 && cg::this_cluster().block_rank() == 0) atomicOr(ta.a.err, LF_DEVERR_STATE);
     return;
@@ -176,6 +214,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   int* decision = reinterpret_cast<int*>(smem + P::kOffMisc + 8);
   volatile int* fail_any = reinterpret_cast<volatile int*>(smem + P::kOffMisc + 16);
   volatile int* uflag = reinterpret_cast<volatile int*>(smem + P::kOffMisc + 24);  // [2]
+  volatile int* split_flag = reinterpret_cast<volatile int*>(smem + P::kOffMisc + 40);
   float* stat_in = reinterpret_cast<float*>(smem + P::kOffStatIn);  // [2][C][2G]
   int* items = reinterpret_cast<int*>(smem + P::off_items(S, chunk, C, a.evict));  // [nitems][4]
   float* opbase = reinterpret_cast<float*>(smem + P::kOffOpart);     // [2][G][D]
@@ -236,7 +275,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // Occupancy and position of every unit this cluster visits, read once: the
   // leaders update them during the launch, every role must see the old values.
   for (int k = tid; k < nitems; k += kTcThreads) {
-    const int u = j + k * NC;
+    const int u = unit_of(k);
     items[4 * k] = a.count[u];
     items[4 * k + 1] = a.next_pos[u];
     items[4 * k + 2] = (a.evict && a.deferred) ? a.pending[u] : -1;
@@ -258,8 +297,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     n = items[4 * k];
     p = items[4 * k + 1];
     ok = (n >= 0 && n <= a.capacity && p >= n);
-    const int per = ((n + C - 1) / C + 3) & ~3;  // <= chunk since n <= capacity
-    base = rank * per;
+    // a split unit is shared by 2C CTAs: this cluster's half is the CTAs (j & 1) C ..
+    const int parts = is_piece(k) ? 2 * C : C;
+    const int sub = is_piece(k) ? (j & 1) * C + rank : rank;
+    const int per = ((n + parts - 1) / parts + 3) & ~3;  // <= chunk since n <= capacity
+    base = sub * per;
     return ok ? max(0, min(per, n - base)) : 0;
   };
 
@@ -281,7 +323,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       int tt = 0;  // tiles produced
       // Issue tiles [t0, t1) of unit k (K when isK) into the ring.
       auto emit = [&](int k, int rows, int base, bool isK, int t0, int t1) {
-        const int u = j + k * NC;
+        const int u = unit_of(k);
         const int unit_row = ta.row_base + u * a.slot_stride + base;
         const void* m64 = isK ? (const void*)&ta.k64 : (const void*)&ta.v64;
         const void* m16 = isK ? (const void*)&ta.k16 : (const void*)&ta.v16;
@@ -315,7 +357,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         int n, p, base;
         bool ok;
         const int rows = unit_rows(k, n, p, ok, base);
-        const int u = j + k * NC;
+        const int u = unit_of(k);
         const size_t ubase = (size_t)u * a.slot_stride;
         const int b2 = k & 1;
         if (k >= 2 && !mbar_wait_bounded(&auxfree[b2], (uint32_t)(((k >> 1) - 1) & 1))) {
@@ -422,7 +464,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint4 qreg[kQChunks];
     int qreg_item = -1;
     auto load_q = [&](int kk) {
-      const int uu = j + kk * NC;
+      const int uu = unit_of(kk);
       const int bb = uu / a.kv_heads;
       const int gg = uu - bb * a.kv_heads;
       const T* qsrc =
@@ -668,7 +710,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       int n, p, base;
       bool state_ok;
       const int rows = unit_rows(k, n, p, state_ok, base);
-      const int u = j + k * NC;
+      const int u = unit_of(k);
       const int b = u / a.kv_heads;
       const int g = u - b * a.kv_heads;
       const int bud = items[4 * k + 3];
@@ -700,6 +742,187 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           0xffffffffu, mbar_wait_bounded(&handoff[b2], (uint32_t)((k >> 1) & 1)));
       named_bar_sync(2, kTcTail);
       const bool unit_failed = !got_unit || uflag[b2] != 0;
+
+      if constexpr (kSplit) {
+        if (is_piece(k)) {
+          // ---- a unit shared with cluster j ^ 1 (its last item, and ours): both
+          // exchanges go through global memory, counted by atomics.  Only the
+          // per-KV-head LongFlow score and append modes are split (host). ----
+          const int su = j >> 1;              // shared unit
+          const int np = 2 * C;               // CTAs sharing it (<= kMaxSplitParts: host)
+          const int me = (j & 1) * C + rank;  // this CTA's piece; piece 0 leads
+          constexpr int kFinF = G * D + 4;    // floats per piece: output, score, slot, flag
+          int* cnt = ta.split_cnt + 2 * su;
+          float* gst = ta.split_stat + (size_t)su * np * 2 * kMaxGroup;
+          float* gfn = ta.split_fin + (size_t)su * np * kFinF;
+          float* sst = stat_in + (size_t)b2 * kMaxCluster * 2 * kMaxGroup;  // local copy
+          // Exchange 1: every piece's (m_h, l_h).
+          if (tt_id < 2 * kMaxGroup) {
+            const int h = tt_id % kMaxGroup;
+            gst[me * 2 * kMaxGroup + tt_id] =
+                tt_id < kMaxGroup ? (h < G ? mlc[h] : -INFINITY) : (h < G ? llc[h] : 0.f);
+          }
+          __threadfence();
+          named_bar_sync(2, kTcTail);
+          if (tt_id == 0) {
+            atomicAdd(cnt, 1);
+            split_flag[0] = wait_count_bounded(cnt, np) ? 1 : 0;
+            __threadfence();
+          }
+          named_bar_sync(2, kTcTail);
+          const bool got_stats = split_flag[0] != 0;
+          for (int i = tt_id; i < np * 2 * kMaxGroup; i += kTcTail) sst[i] = __ldcg(gst + i);
+          named_bar_sync(2, kTcTail);
+          if (tt_id < G) {
+            const int h = tt_id;
+            float M = snw[h];
+            for (int r = 0; r < np; ++r) M = fmaxf(M, sst[r * 2 * kMaxGroup + h]);
+            float L = exp2f(snw[h] - M);
+            for (int r = 0; r < np; ++r) {
+              const float mr = sst[r * 2 * kMaxGroup + h];
+              if (mr != -INFINITY) L += sst[r * 2 * kMaxGroup + kMaxGroup + h] * exp2f(mr - M);
+            }
+            m_glb[h] = M;
+            l_glb[h] = L;
+            cmul[h] = (mlc[h] != -INFINITY) ? exp2f(mlc[h] - M) / L : 0.f;
+            if (!(isfinite(M) && isfinite(L) && L > 0.f)) atomicOr(a.err, LF_DEVERR_NONFINITE);
+          }
+          const bool stats_ok = !named_bar_or(2, kTcTail, !got_stats);
+          if (!stats_ok && tt_id == 0) {
+            *fail_any = 1;
+            atomicOr(a.err, LF_DEVERR_TIMEOUT);
+          }
+          // Exact scores of this CTA's slots, its lowest candidate.
+          float bs = INFINITY;
+          int bi = INT_MAX;
+          if (rl.choosing && !unit_failed && stats_ok) {
+            float cm[G];
+#pragma unroll
+            for (int h = 0; h < G; ++h) cm[h] = cmul[h];
+            for (int i = tt_id; i < rows; i += kTcTail) {
+              const int slot = base + i;
+              if (slot == rl.excl) continue;
+              const float w = w_s[i];
+              float as = 0.f;
+#pragma unroll
+              for (int h = 0; h < G; ++h) as = fmaf(lg[(size_t)i * G + h], cm[h], as);
+              const float sc = fabsf(w) * as;
+              if (is_candidate(w) && better(sc, slot, bs, bi)) {
+                bs = sc;
+                bi = slot;
+              }
+            }
+          }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            const float os = __shfl_xor_sync(0xffffffffu, bs, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (better(os, oi, bs, bi)) {
+              bs = os;
+              bi = oi;
+            }
+          }
+          if (lane == 0) {
+            red_t[twarp] = bs;
+            red_ti[twarp] = bi;
+          }
+          named_bar_sync(2, kTcTail);
+          // Exchange 2: partial output, lowest (score, slot) and failure flag to piece 0.
+          for (int c = tt_id; c < G * D; c += kTcTail) gfn[(size_t)me * kFinF + c] = o_part[c];
+          if (tt_id == 0) {
+            float cs = red_t[0];
+            int ci = red_ti[0];
+            if (better(red_t[1], red_ti[1], cs, ci)) {
+              cs = red_t[1];
+              ci = red_ti[1];
+            }
+            const bool fl = unit_failed || !stats_ok || *fail_any;
+            gfn[(size_t)me * kFinF + G * D] = cs;
+            gfn[(size_t)me * kFinF + G * D + 1] = __int_as_float(ci);
+            gfn[(size_t)me * kFinF + G * D + 2] = fl ? 1.f : 0.f;
+          }
+          __threadfence();
+          named_bar_sync(2, kTcTail);
+          if (tt_id == 0) atomicAdd(cnt + 1, 1);
+          if (me == 0) {
+            if (tt_id == 0) {
+              split_flag[0] = wait_count_bounded(cnt + 1, np) ? 1 : 0;
+              __threadfence();
+            }
+            named_bar_sync(2, kTcTail);
+            const bool all_got = split_flag[0] != 0;
+            // Every piece's lowest (score, slot) and failure flag: one piece per
+            // lane of warp 0, loaded together, then reduced.
+            float fs = INFINITY;
+            int fi = INT_MAX;
+            bool any_fail = !all_got || !stats_ok;
+            if (twarp == 0) {
+              float rs = INFINITY, rf = 0.f;
+              int ri = INT_MAX;
+              if (lane < np) {
+                const float* tl = gfn + (size_t)lane * kFinF + G * D;
+                rs = __ldcg(tl);
+                ri = __float_as_int(__ldcg(tl + 1));
+                rf = __ldcg(tl + 2);
+              }
+              any_fail = any_fail || __any_sync(0xffffffffu, rf != 0.f);
+              fs = rs;
+              fi = ri;
+#pragma unroll
+              for (int o = 16; o > 0; o >>= 1) {
+                const float os = __shfl_xor_sync(0xffffffffu, fs, o);
+                const int oi = __shfl_xor_sync(0xffffffffu, fi, o);
+                if (better(os, oi, fs, fi)) {
+                  fs = os;
+                  fi = oi;
+                }
+              }
+            }
+            // Output: the new token + every piece's partial output, in piece order.
+            // Each thread's elements (tt_id + 64 i) of every piece are loaded at once.
+            if (all_got && stats_ok) {
+              constexpr int kEl = G * D / kTcTail;
+              T* og = reinterpret_cast<T*>(a.out) + ((size_t)b * a.q_heads + (size_t)g * G) * D;
+              float part[kEl][kMaxSplitParts];
+#pragma unroll
+              for (int i = 0; i < kEl; ++i)
+#pragma unroll
+                for (int r = 0; r < kMaxSplitParts; ++r)
+                  part[i][r] = (r < np) ? __ldcg(gfn + (size_t)r * kFinF + tt_id + i * kTcTail) : 0.f;
+#pragma unroll
+              for (int i = 0; i < kEl; ++i) {
+                const int idx = tt_id + i * kTcTail;
+                const int h = idx / D;
+                const int e = idx - h * D;
+                float acc = exp2f(snw[h] - m_glb[h]) * to_f32(vn[e]);
+#pragma unroll
+                for (int r = 0; r < kMaxSplitParts; ++r) {
+                  const float mr = (r < np) ? sst[r * 2 * kMaxGroup + h] : -INFINITY;
+                  if (mr != -INFINITY) acc += part[i][r] * exp2f(mr - m_glb[h]);
+                }
+                from_f32(acc / l_glb[h], &og[(size_t)h * D + e]);
+              }
+            }
+            float anew = 0.f;
+            if (tt_id == 0) {
+#pragma unroll
+              for (int h = 0; h < G; ++h) anew += exp2f(snw[h] - m_glb[h]) / l_glb[h];
+              const LeaderOut d =
+                  leader_decide(a, u, n, p, pend, bud, state_ok, any_fail, rl, fi, anew);
+              decision[0] = d.slot;
+              // every piece is through both exchanges: ready for the next launch
+              cnt[0] = 0;
+              cnt[1] = 0;
+            }
+            named_bar_sync(2, kTcTail);
+            const int slot = decision[0];
+            if (slot >= 0) write_slot<T, D>(a, ubase, slot, kn, vn, p, anew, tt_id, kTcTail);
+          }
+          named_bar_sync(2, kTcTail);
+          if (lane == 0) mbar_arrive(&taildone[b2]);
+          continue;
+        }
+      }
 
       // Exchange 1: every CTA's (m_h, l_h) to every CTA of the cluster.
       float* sin = stat_in + (size_t)b2 * kMaxCluster * 2 * kMaxGroup;

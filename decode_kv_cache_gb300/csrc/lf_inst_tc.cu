@@ -13,7 +13,8 @@ int smem_bytes_tc(int stages, int chunk, int cluster, int evict, int items) {
 template <int G>
 bool fill(KernelEntry* e) {
   e->kind = kTensorCore;
-  e->decode = reinterpret_cast<const void*>(&decode_step_tc_kernel<G>);
+  e->decode = reinterpret_cast<const void*>(&decode_step_tc_kernel<G, false>);
+  e->decode_split = reinterpret_cast<const void*>(&decode_step_tc_kernel<G, true>);
   e->prefill = reinterpret_cast<const void*>(&prefill_kernel<__nv_bfloat16, 128>);
   e->select = reinterpret_cast<const void*>(&select_layer_kernel<__nv_bfloat16, 128>);
   e->smem_bytes = &smem_bytes_tc<G>;

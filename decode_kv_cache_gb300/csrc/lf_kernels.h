@@ -13,6 +13,7 @@ enum KernelKind { kSimt = 0, kTensorCore = 1 };
 struct KernelEntry {
   int kind = kSimt;               // kSimt: decode(DecodeArgs); kTensorCore: decode(TcArgs)
   const void* decode = nullptr;
+  const void* decode_split = nullptr;  // kTensorCore: the split-launch instantiation
   const void* prefill = nullptr;  // __global__ void(PrefillArgs)
   const void* select = nullptr;   // __global__ void(DecodeArgs): layer-scope victim
   // Dynamic shared memory of one decode CTA; `items` bounds the units one
