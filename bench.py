@@ -418,6 +418,8 @@ def bench_rkv(args, torch, lf, stream_mod, peak):
     if bits:
         raise RuntimeError(f"device error word {bits} in the R-KV cycle")
     counts = cache.views()["count"].cpu()
+    rlay = cache.layout
+    rkv_shape = {"cluster": rlay.cluster, "stages": rlay.stages, "split_units": rlay.split_units}
     cache.close()
     del cache, gen, steps, qobs
     torch.cuda.empty_cache()
@@ -426,6 +428,8 @@ def bench_rkv(args, torch, lf, stream_mod, peak):
     # over the same number of decode steps (every step evicts)
     lwl = wl.scaled(window=stream_mod.get_workload("r1-llama-8b").window, prefill=B)
     lcache, lgen = build_cache(lwl, torch, lf, stream_mod, seed=301)
+    llay = lcache.layout
+    lf_shape = {"cluster": llay.cluster, "stages": llay.stages, "split_units": llay.split_units}
     lwarm = pregenerate(lgen, 3, torch)
     time_steps(lcache, lwarm, outs, evs, torch, graph=False)
     del lwarm
@@ -462,6 +466,7 @@ def bench_rkv(args, torch, lf, stream_mod, peak):
         "tensor_peak_kind": load_tensor_peak()[1],
         "counts_after": [int(counts.min()), int(counts.max())],
         "longflow_units_per_s_same_geometry": longflow_units_per_s,
+        "launch_shapes": {"rkv_decode": rkv_shape, "longflow": lf_shape},
         "longflow_geometry": f"{L} layers, batch {wl.batch}, budget {B}, window {lwl.window}, "
                              f"steady, {buf} steps",
         "longflow_over_rkv": longflow_units_per_s / value,
@@ -708,7 +713,8 @@ def bench_ours(args):
                      "frac": achieved / peak, "peak_kind": peak_kind,
                      "frac_of_nominal_8000": achieved / NOMINAL_HBM_GBS,
                      "traffic": stored_traffic(wl.name, wl.batch),
-                     "kernel": (f"decode_step_tc_kernel<{wl.group}>" if lay.kernel == 2 else
+                     "kernel": (f"decode_step_tc_kernel<{wl.group}, "
+                                f"{'true' if lay.split_units else 'false'}>" if lay.kernel == 2 else
                                 f"decode_step_simt_kernel<{wl.dtype},{wl.head_dim},{wl.group}>"),
                      "bytes_per_launch": bytes_per_launch,
                      "timing": "timed region / launches (includes launch gaps)"},

@@ -778,6 +778,7 @@ int lf_cache_layout(const lf_cache* cache, lf_layout* out) {
   out->rkv_beta = cache->rkv_beta;
   out->rkv_lambda = cache->rkv_lambda;
   out->rkv_tau = cache->rkv_tau;
+  out->split_units = cache->split_rem;
   return LF_OK;
 }
 

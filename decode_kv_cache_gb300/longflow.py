@@ -70,7 +70,8 @@ class LFLayout(ctypes.Structure):
         (n, ctypes.c_int) for n in ("score", "norm", "sinks", "deferred", "scope")] + [
         ("acc", ctypes.c_void_p), ("pending", ctypes.c_void_p)] + [
         (n, ctypes.c_int) for n in ("rkv_buffer", "rkv_alpha", "rkv_beta")] + [
-        ("rkv_lambda", ctypes.c_float), ("rkv_tau", ctypes.c_float)]
+        ("rkv_lambda", ctypes.c_float), ("rkv_tau", ctypes.c_float),
+        ("split_units", ctypes.c_int)]
 
 
 _lib: Optional[ctypes.CDLL] = None

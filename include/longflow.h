@@ -72,7 +72,7 @@
 extern "C" {
 #endif
 
-#define LF_ABI_VERSION 2
+#define LF_ABI_VERSION 3
 
 typedef struct lf_cache lf_cache; /* opaque; owns the slab */
 
@@ -264,6 +264,9 @@ typedef struct lf_layout {
                        as count; -1 = none chosen), else NULL */
   int rkv_buffer, rkv_alpha, rkv_beta; /* R-KV parameters (evict = LF_EVICT_RKV) */
   float rkv_lambda, rkv_tau;
+  int split_units;  /* tensor-core kernel: units of each step shared by two clusters
+                       (the last round's, when they fill at most half of the clusters);
+                       0 when no step is split */
 } lf_layout;
 
 int lf_cache_layout(const lf_cache* cache, lf_layout* out);

@@ -173,3 +173,29 @@ def test_degenerate_budgets(kernel, budget, cluster):
         wl = WORKLOADS["tiny-fp32"].scaled(budget=budget, window=0, prefill=1)
     st = _run(wl, 40, cluster=cluster, kernel=kernel)
     assert st.evictions == 40 * wl.kv_heads - (budget - 1) * wl.kv_heads
+
+
+def test_split_launch_choice():
+    """The last round is shared by two clusters exactly when its units fill at
+    most half of the resident clusters (one two-CTA cluster per two SMs at
+    budget 3276): batch 32 x 8 KV heads leaves 256 mod 76 = 28 units, batch 64
+    leaves 56 and is not split.  The parity tests at the r1-llama-8b shape run
+    through the split kernel."""
+    from decode_kv_cache_gb300.longflow import LFCache
+    clusters = torch.cuda.get_device_properties(0).multi_processor_count // 2
+    for batch in (32, 64):
+        cache = LFCache(1, batch, 8, 32, 128, 3276, 64)
+        try:
+            lay = cache.layout
+            assert lay.cluster == 2
+            rem = (batch * 8) % clusters
+            want = rem if 0 < rem and 2 * rem <= clusters else 0
+            assert lay.split_units == want, (batch, lay.split_units, want)
+        finally:
+            cache.close()
+    # the deferred order and the H2O score are never split
+    cache = LFCache(1, 32, 8, 32, 128, 3276, 64, deferred=True)
+    try:
+        assert cache.layout.split_units == 0
+    finally:
+        cache.close()
