@@ -120,7 +120,10 @@ typedef enum lf_scope {
 /* Bits of the device error word (lf_cache_check). */
 #define LF_DEVERR_NONFINITE 1 /* a softmax max/denominator was not finite */
 #define LF_DEVERR_STATE 2     /* no eviction candidate / count out of range */
-#define LF_DEVERR_TIMEOUT 4   /* a bounded on-chip wait expired; step skipped */
+#define LF_DEVERR_TIMEOUT 4   /* a bounded on-chip wait expired; step skipped.  After
+                                 it the step's outputs and the cache's contents are
+                                 unspecified (a split launch's exchange counters may be
+                                 left mid-count): restore the cache or recreate it */
 
 typedef struct lf_config {
   int dtype;              /* LF_BF16 or LF_F32: type of q, K, V, k_new, v_new, out */
