@@ -735,6 +735,9 @@ int lf_cache_check(lf_cache* cache, lf_stream_t stream, int32_t* bits) {
   if ((e = cudaMemcpy(&word, cache->err, 4, cudaMemcpyDeviceToHost)) != cudaSuccess)
     return cuda_fail(e, "reading the error word");
   if ((e = cudaMemset(cache->err, 0, 4)) != cudaSuccess ||
+      // an expired wait can leave a split launch's exchange counters mid-count
+      ((word & LF_DEVERR_TIMEOUT) && cache->split_cnt &&
+       (e = cudaMemset(cache->split_cnt, 0, (size_t)cache->split_rem * 2 * 4)) != cudaSuccess) ||
       (e = cudaDeviceSynchronize()) != cudaSuccess)
     return cuda_fail(e, "clearing the error word");
   if (bits) *bits = word;

@@ -122,8 +122,9 @@ typedef enum lf_scope {
 #define LF_DEVERR_STATE 2     /* no eviction candidate / count out of range */
 #define LF_DEVERR_TIMEOUT 4   /* a bounded on-chip wait expired; step skipped.  After
                                  it the step's outputs and the cache's contents are
-                                 unspecified (a split launch's exchange counters may be
-                                 left mid-count): restore the cache or recreate it */
+                                 unspecified: restore them (lf_cache_layout) or recreate
+                                 the cache; lf_cache_check also resets the internal
+                                 exchange counters of split launches */
 
 typedef struct lf_config {
   int dtype;              /* LF_BF16 or LF_F32: type of q, K, V, k_new, v_new, out */
