@@ -199,3 +199,15 @@ def test_split_launch_choice():
         assert cache.layout.split_units == 0
     finally:
         cache.close()
+
+
+def test_split_launch_transition_with_policy():
+    """r1-llama-8b's launch shape (256 units; 28 are shared by two clusters at
+    the steps where every sequence holds >= 3000 tokens): a prompt of 2990, so
+    the first 10 steps run unsplit and the rest split, here with the l2 norm
+    and 4 sinks; sampled units in the shared last round and in whole rounds."""
+    import oracle
+    wl = WORKLOADS["r1-llama-8b"].scaled(prefill=2990)
+    st = _run(wl, 60, layers=(1,), sample=[(0, 31, 7), (0, 29, 0), (0, 2, 3)],
+              policy=oracle.Policy(norm=2, sinks=4))
+    assert st.unit_steps == 60 * 3
