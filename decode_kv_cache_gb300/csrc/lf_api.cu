@@ -318,30 +318,24 @@ lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, i
   const int threads = tc ? lf::kTcThreads : lf::kThreads;
   const int units = batch * kv_heads;
   const int stages = c.stages ? c.stages : (tc ? 3 : 4);
-  int cluster = c.cluster;
-  if (cluster == 0) {
-    cluster = 1;
-    if (!tc)
-      while (cluster < lf::kMaxCluster && (long long)units * cluster < 8LL * num_sms &&
-             (capacity + 2 * cluster - 1) / (2 * cluster) >= 128)
-        cluster *= 2;
-  }
+  // The shared memory, resident clusters and item-table size of one cluster size;
+  // false if it does not fit.
   int chunk = 0, smem = 0, grid_y = 0, items = 0;
-  for (;;) {
-    chunk = (int)round_up((size_t)((capacity + cluster - 1) / cluster), 4);
+  auto try_shape = [&](int cl) -> bool {
+    chunk = (int)round_up((size_t)((capacity + cl - 1) / cl), 4);
     int fits = 0;
     if (tc) {
       // The persistent grid visits ceil(units / resident clusters) units per
       // cluster; its item table is sized for that.  Start from the most
       // clusters the SMs could hold and grow the table if fewer are resident.
-      const int most = std::max(1, num_sms / cluster);
+      const int most = std::max(1, num_sms / cl);
       items = (units + most - 1) / most;
       for (int pass = 0; pass < 4; ++pass) {
-        smem = kern.smem_bytes(stages, chunk, cluster, kevict, items);
+        smem = kern.smem_bytes(stages, chunk, cl, kevict, items);
         // The tensor-core kernel takes all of an SM's tensor memory: ask for more
         // than half of its shared memory so that never two CTAs share an SM.
         smem = std::max(smem, max_sm_smem / 2 + 1024);
-        fits = (smem <= max_optin) ? active_clusters(kern.decode, cluster, 1, 1, smem, threads) : 0;
+        fits = (smem <= max_optin) ? active_clusters(kern.decode, cl, 1, 1, smem, threads) : 0;
         if (fits <= 0) break;
         grid_y = std::min(fits, units);
         const int need = (units + grid_y - 1) / grid_y;
@@ -351,17 +345,55 @@ lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, i
       }
       if (fits > 0 && items > lf::kTcMaxItems) fits = 0;
     } else {
-      smem = kern.smem_bytes(stages, chunk, cluster, kevict, 0);
+      smem = kern.smem_bytes(stages, chunk, cl, kevict, 0);
       if (smem <= max_optin)
-        fits = active_clusters(kern.decode, cluster, kv_heads, batch, smem, threads);
+        fits = active_clusters(kern.decode, cl, kv_heads, batch, smem, threads);
     }
-    if (fits > 0) break;
+    return fits > 0;
+  };
+  int cluster = c.cluster;
+  if (cluster == 0) {
+    cluster = 1;
+    if (!tc)
+      while (cluster < lf::kMaxCluster && (long long)units * cluster < 8LL * num_sms &&
+             (capacity + 2 * cluster - 1) / (2 * cluster) >= 128)
+        cluster *= 2;
+  }
+  for (;;) {
+    if (try_shape(cluster)) break;
     if (c.cluster != 0 || cluster >= lf::kMaxCluster) {
       fail(LF_ERR_UNSUPPORTED, "launch does not fit: cluster %d, %d stages, %d slots per CTA need "
            "%d bytes of shared memory (max %d)", cluster, stages, chunk, smem, max_optin);
       return nullptr;
     }
     cluster *= 2;
+  }
+  if (tc && c.cluster == 0) {
+    // Tensor-core kernel: of the smallest cluster that fits and the next two,
+    // take the one with the least estimated time per launch: rounds of units per
+    // cluster x (K and V tiles per CTA x ~0.7 us + ~3 us per unit boundary).
+    // More CTAs per unit pay when the units do not fill the SMs (64 units of
+    // 512 slots: 2-CTA clusters 14.5 us, 1-CTA 16.8 us) and cost when they do.
+    auto cost = [&](int cl) {
+      const long long rounds = (units + grid_y - 1) / grid_y;
+      const long long tiles = 2LL * ((((capacity + cl - 1) / cl) + lf::kTcTile - 1) / lf::kTcTile);
+      return rounds * (7 * tiles + 30);
+    };
+    int best = cluster;
+    long long best_cost = cost(cluster);
+    for (int cl = cluster * 2; cl <= std::min(cluster * 4, lf::kMaxCluster); cl *= 2) {
+      if (!try_shape(cl)) continue;
+      const long long cc = cost(cl);
+      if (cc < best_cost) {
+        best = cl;
+        best_cost = cc;
+      }
+    }
+    cluster = best;
+    if (!try_shape(cluster)) {  // restore the chosen shape (it fitted above)
+      fail(LF_ERR_UNSUPPORTED, "launch shape changed while choosing it");
+      return nullptr;
+    }
   }
 
   lf_cache* cache = new (std::nothrow) lf_cache();
