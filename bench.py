@@ -498,6 +498,8 @@ def bench_ours(args):
     wl = stream_mod.get_workload(args.workload)
     if args.layers:
         wl = wl.scaled(layers=args.layers)
+    if args.steady and not wl.ragged:
+        wl = wl.scaled(prefill=wl.budget)
     peak, peak_kind = load_peaks()
 
     def barrier():
@@ -739,6 +741,9 @@ def main():
     ap.add_argument("--workload", default="qwen3-8b-steady")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--layers", type=int, default=0, help="override the layer count")
+    ap.add_argument("--steady", action="store_true",
+                    help="start with the cache filled to the budget (every step evicts) "
+                         "instead of from the workload's prompt")
     ap.add_argument("--cluster", type=int, default=0)
     ap.add_argument("--stages", type=int, default=0)
     ap.add_argument("--eager", action="store_true", help="launch eagerly instead of a CUDA graph")

@@ -688,6 +688,8 @@ __global__ void __launch_bounds__(kSelThreads) select_layer_kernel(const DecodeA
   // Launched as a programmatic dependent of the decode grid: wait until that
   // grid has completed and its writes are visible.
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // The next decode grid may be scheduled now; it still waits for this grid.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // Every KV head's attention kernel leaves the same request: the slots it
   // scored, + 1 (0: nothing to choose this step).
   const int req = a.lw_req[u0];

@@ -272,6 +272,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // completed and its writes are visible (this kernel never lets a dependent
   // grid pass its own wait early, so back-to-back steps of one layer stay ordered).
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // Let the next grid on the stream be scheduled now: its CTAs take SMs as this
+  // grid's CTAs exit and run their set-up there, but none of them passes its own
+  // griddepcontrol.wait before this whole grid has completed.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // Occupancy and position of every unit this cluster visits, read once: the
   // leaders update them during the launch, every role must see the old values.
   for (int k = tid; k < nitems; k += kTcThreads) {
