@@ -63,7 +63,7 @@ namespace {
 thread_local std::string g_last_error;
 
 // Split launches only once every sequence of the layer holds this many tokens.
-constexpr long long kSplitMinSlots = 3000;
+constexpr long long kSplitMinSlots = 2048;
 
 int fail(int code, const char* fmt, ...) {
   char buf[512];
@@ -430,8 +430,8 @@ lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, i
   cache->fill.assign((size_t)layers, 0);
   cache->fill_cap = kevict ? min_budget : capacity;   // append modes fill the slab
   // Split launches: when the units left over after the whole rounds fill at
-  // most half of the clusters, each of them is shared by two clusters (the
-  // last round then takes about half as long).  Only for the per-KV-head
+  // most half of the clusters, each of them is shared by two clusters, as the
+  // first item of both (the part-filled round then takes about half as long).  Only for the per-KV-head
   // LongFlow score without the deferred order, and for the append modes.
   if (tc) {
     const int rem = units % grid_y;
@@ -701,7 +701,8 @@ int lf_decode_step(lf_cache* cache, int layer, const void* q, const void* k_new,
     ta.row_base = (int)(layer * layer_slots);
     ta.max_items = cache->items;
     // the split kernel pays for its exchanges only when every unit is long (measured at
-    // batch 32: 4% faster at 3276 slots, 0.8% slower at 2560, 11% slower at ~580)
+    // batch 32 on 2-CTA clusters: 9% faster at 3276 slots, 7% at 2048 and 2560, even at
+    // 1664, 4-9% slower from 1408 down to 640)
     const bool split = cache->split_rem > 0 && cache->fill[layer] >= kSplitMinSlots;
     ta.split_rem = cache->split_rem;
     ta.split_stat = cache->split_stat;

@@ -167,15 +167,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int S = a.stages;
   const int chunk = a.chunk;
   const int units = a.batch * a.kv_heads;
-  // Whole units: cluster j takes j, j + NC, ...  Split launches: after `rounds`
-  // whole rounds, cluster j < 2 split_rem takes half (j & 1) of unit
-  // rounds NC + j / 2 as its last item, shared with cluster j ^ 1.
+  // Whole units: cluster j takes j, j + NC, ...  Split launches: `rounds` whole
+  // rounds, and cluster j < 2 split_rem first takes half (j & 1) of unit
+  // rounds NC + j / 2, shared with cluster j ^ 1.  The shared unit comes first
+  // so that both halves start together and its exchanges through L2 overlap
+  // the stream of the whole units after it.
   const int rounds = kSplit ? (units - ta.split_rem) / NC : 0;
   const bool has_piece = kSplit && j < 2 * ta.split_rem;
-  const int nitems = kSplit ? rounds + (has_piece ? 1 : 0)
+  const int pfirst = has_piece ? 1 : 0;  // items before the first whole unit
+  const int nitems = kSplit ? rounds + pfirst
                             : ((j < units) ? (units - j + NC - 1) / NC : 0);
-  auto unit_of = [&](int k) { return (kSplit && k == rounds) ? rounds * NC + (j >> 1) : j + k * NC; };
-  auto is_piece = [&](int k) { return kSplit && k == rounds; };
+  auto unit_of = [&](int k) {
+    return (has_piece && k == 0) ? rounds * NC + (j >> 1) : j + (k - pfirst) * NC;
+  };
+  auto is_piece = [&](int k) { return has_piece && k == 0; };
   if (nitems > ta.max_items) {  // the host sized the item table for fewer units
     if (threadIdx.x == 0 && cg::this_cluster().block_rank() == 0) atomicOr(ta.a.err, LF_DEVERR_STATE);
     return;
@@ -749,7 +754,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
       if constexpr (kSplit) {
         if (is_piece(k)) {
-          // ---- a unit shared with cluster j ^ 1 (its last item, and ours): both
+          // ---- a unit shared with cluster j ^ 1 (the first item of both): both
           // exchanges go through global memory, counted by atomics.  Only the
           // per-KV-head LongFlow score and append modes are split (host). ----
           const int su = j >> 1;              // shared unit
@@ -948,8 +953,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             st_async_v4(ra + q4 * 4, v[q4], v[q4 + 1], v[q4 + 2], v[q4 + 3], rb);
         }
       }
+      // statb[b2] completes once per whole unit of parity b2 (a shared unit,
+      // item 0, does not use it).
+      const uint32_t stat_phase = (uint32_t)(((k >> 1) - ((pfirst && b2 == 0) ? 1 : 0)) & 1);
       const bool got_stats = __all_sync(
-          0xffffffffu, mbar_wait_cluster_bounded(&statb[b2], (uint32_t)((k >> 1) & 1)));
+          0xffffffffu, mbar_wait_cluster_bounded(&statb[b2], stat_phase));
       if (tt_id < G) {
         const int h = tt_id;
         float M = snw[h];
@@ -1061,8 +1069,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
       if (rank == leader) {
-        const bool got = __all_sync(0xffffffffu,
-                                    mbar_wait_cluster_bounded(finb, (uint32_t)((k / C) & 1)));
+        // finb completes once per whole unit this CTA leads (not for a shared unit).
+        const uint32_t fin_phase = (uint32_t)(((k / C) - ((pfirst && leader == 0) ? 1 : 0)) & 1);
+        const bool got = __all_sync(0xffffffffu, mbar_wait_cluster_bounded(finb, fin_phase));
         const bool all_got = !named_bar_or(2, kTcTail, !got);
         // Output: the new token + every CTA's partial output, in rank order.
         if (all_got && stats_ok) {

@@ -268,9 +268,10 @@ typedef struct lf_layout {
                        as count; -1 = none chosen), else NULL */
   int rkv_buffer, rkv_alpha, rkv_beta; /* R-KV parameters (evict = LF_EVICT_RKV) */
   float rkv_lambda, rkv_tau;
-  int split_units;  /* tensor-core kernel: units shared by two clusters (the last
-                       round's, when they fill at most half of the clusters) at the
-                       steps where every sequence of the layer holds >= 3000 tokens,
+  int split_units;  /* tensor-core kernel: units shared by two clusters (those left
+                       after the whole rounds, when they fill at most half of the
+                       clusters) at the steps where every sequence of the layer holds
+                       >= 2048 tokens,
                        by the host's count of prompts and steps; 0: never split */
 } lf_layout;
 

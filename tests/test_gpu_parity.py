@@ -176,8 +176,8 @@ def test_degenerate_budgets(kernel, budget, cluster):
 
 
 def test_split_launch_choice():
-    """The last round is shared by two clusters exactly when its units fill at
-    most half of the resident clusters (one two-CTA cluster per two SMs at
+    """The units left after the whole rounds are shared by two clusters exactly
+    when they fill at most half of the resident clusters (one two-CTA cluster per two SMs at
     budget 3276): batch 32 x 8 KV heads leaves 256 mod 76 = 28 units, batch 64
     leaves 56 and is not split.  The parity tests at the r1-llama-8b shape run
     through the split kernel."""
@@ -203,11 +203,11 @@ def test_split_launch_choice():
 
 def test_split_launch_transition_with_policy():
     """r1-llama-8b's launch shape (256 units; 28 are shared by two clusters at
-    the steps where every sequence holds >= 3000 tokens): a prompt of 2990, so
+    the steps where every sequence holds >= 2048 tokens): a prompt of 2038, so
     the first 10 steps run unsplit and the rest split, here with the l2 norm
-    and 4 sinks; sampled units in the shared last round and in whole rounds."""
+    and 4 sinks; sampled units among the shared ones and in whole rounds."""
     import oracle
-    wl = WORKLOADS["r1-llama-8b"].scaled(prefill=2990)
+    wl = WORKLOADS["r1-llama-8b"].scaled(prefill=2038)
     st = _run(wl, 60, layers=(1,), sample=[(0, 31, 7), (0, 29, 0), (0, 2, 3)],
               policy=oracle.Policy(norm=2, sinks=4))
     assert st.unit_steps == 60 * 3
