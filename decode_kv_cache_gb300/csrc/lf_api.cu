@@ -834,6 +834,7 @@ int lf_cache_layout(const lf_cache* cache, lf_layout* out) {
   out->rkv_lambda = cache->rkv_lambda;
   out->rkv_tau = cache->rkv_tau;
   out->split_units = cache->split_rem;
+  out->split_cnt = cache->split_cnt;
   return LF_OK;
 }
 

@@ -71,7 +71,7 @@ class LFLayout(ctypes.Structure):
         ("acc", ctypes.c_void_p), ("pending", ctypes.c_void_p)] + [
         (n, ctypes.c_int) for n in ("rkv_buffer", "rkv_alpha", "rkv_beta")] + [
         ("rkv_lambda", ctypes.c_float), ("rkv_tau", ctypes.c_float),
-        ("split_units", ctypes.c_int)]
+        ("split_units", ctypes.c_int), ("split_cnt", ctypes.c_void_p)]
 
 
 _lib: Optional[ctypes.CDLL] = None
@@ -321,7 +321,8 @@ class LFCache:
     def views(self):
         """Torch tensors aliasing the slab (no copy): k, v [L][b][H_kv][stride][d],
         vnorm, pos [L][b][H_kv][stride], count, next_pos [L][b][H_kv], budget [b];
-        acc [L][b][H_kv][stride] (H2O) and pending [L][b][H_kv] (deferred), else None."""
+        acc [L][b][H_kv][stride] (H2O) and pending [L][b][H_kv] (deferred), else None;
+        split_cnt [split_units][2] (split launches), else None."""
         lay = self.layout
         L, b, g, s, d = lay.layers, lay.batch, lay.kv_heads, lay.slot_stride, lay.head_dim
         if self.dtype == torch.bfloat16:
@@ -341,4 +342,6 @@ class LFCache:
                     if lay.acc else None),
             "pending": (_view(lay.pending, (L, b, g), torch.int32, self.device)
                         if lay.pending else None),
+            "split_cnt": (_view(lay.split_cnt, (lay.split_units, 2), torch.int32, self.device)
+                          if lay.split_cnt else None),
         }

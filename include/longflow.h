@@ -72,7 +72,7 @@
 extern "C" {
 #endif
 
-#define LF_ABI_VERSION 3
+#define LF_ABI_VERSION 4
 
 typedef struct lf_cache lf_cache; /* opaque; owns the slab */
 
@@ -273,6 +273,10 @@ typedef struct lf_layout {
                        clusters) at the steps where every sequence of the layer holds
                        >= 2048 tokens,
                        by the host's count of prompts and steps; 0: never split */
+  int32_t* split_cnt; /* split launches: [split_units][2] arrival counts of a shared
+                       unit's two exchanges through global memory.  Zero between
+                       launches; lf_cache_check zeroes them after an expired wait.
+                       NULL when split_units is 0 */
 } lf_layout;
 
 int lf_cache_layout(const lf_cache* cache, lf_layout* out);

@@ -211,3 +211,57 @@ def test_split_launch_transition_with_policy():
     st = _run(wl, 60, layers=(1,), sample=[(0, 31, 7), (0, 29, 0), (0, 2, 3)],
               policy=oracle.Policy(norm=2, sinks=4))
     assert st.unit_steps == 60 * 3
+
+
+def test_split_exchange_timeout_recovers():
+    """A split launch whose exchange can never complete: the wait gives up after
+    its bound, the unit skips the step (state, count and position unchanged,
+    evicted = -1), LF_DEVERR_TIMEOUT is reported, lf_cache_check zeroes the
+    counters, and the context stays usable.  The failure is made on the host: the
+    first exchange's arrival count of shared unit 0 is set so low that the
+    arrivals never reach the target.  Batch 12 on 2-CTA clusters: 96 units on 76
+    clusters, the 20 left over shared.  Shared unit 0 is (sequence 9, KV head 4),
+    the first item of clusters 0 and 1.  A CTA whose wait ran out skips the rest
+    of its launch, so their second items, whole units 0 and 1, skip the step
+    too; every other unit matches the oracle."""
+    import time
+    from decode_kv_cache_gb300.longflow import LF_DEVERR_TIMEOUT
+    wl = WORKLOADS["r1-llama-8b"].scaled(layers=1, batch=12, prefill=3276)
+    nc = torch.cuda.get_device_properties(0).multi_processor_count // 2
+    units = wl.batch * wl.kv_heads
+    rounds, rem = divmod(units, nc)
+    assert rounds >= 1 and 0 < 2 * rem <= nc
+    bad = divmod(rounds * nc, wl.kv_heads)  # shared unit 0
+    skipped = [bad] + [divmod(j + r * nc, wl.kv_heads) for j in (0, 1) for r in range(rounds)]
+    sample = [(0, b, g) for b in range(wl.batch) for g in range(wl.kv_heads)
+              if (b, g) not in skipped]
+    run = ParityRun(wl, layers=(0,), sample=sample, cluster=2)
+    try:
+        lay = run.cache.layout
+        assert lay.cluster == 2 and lay.split_units == rem
+        run.run(3)
+        assert run.cache.check() == 0
+        vw = run.views
+        cnt = vw["split_cnt"]
+        assert int(cnt.abs().sum()) == 0
+        names = ("k", "v", "vnorm", "pos", "count", "next_pos")
+        before = {(bg, n): vw[n][0][bg].clone() for bg in skipped for n in names}
+        cnt[0, 0] = -(1 << 20)
+        torch.cuda.synchronize()
+        t0 = time.monotonic()
+        run.step(check=True)  # every sampled unit against the oracle as usual
+        bits = run.cache.check()
+        elapsed = time.monotonic() - t0
+        assert bits == LF_DEVERR_TIMEOUT, bits
+        assert elapsed < 30.0
+        assert int(cnt.abs().sum()) == 0
+        for (bg, n), t in before.items():
+            assert torch.equal(vw[n][0][bg], t), (bg, n)
+        for bg in skipped:
+            assert int(run.ev[0][bg]) == -1
+        run.run(4)
+        assert run.cache.check() == 0
+        run.compare_state()
+        run.stats.assert_ok()
+    finally:
+        run.close()
