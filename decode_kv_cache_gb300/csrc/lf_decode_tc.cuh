@@ -206,6 +206,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* handoff = qfree + 2;           // [2] epilogue -> tail: a unit's state is ready
   uint64_t* taildone = handoff + 2;        // [2] tail -> epilogue: that state is consumed
   uint64_t* drain = taildone + 2;          // every MMA complete
+  uint64_t* statrdy = drain + 1;           // [2] epilogue -> tail: (m, l), logits, weights
   float* m_loc = reinterpret_cast<float*>(smem + P::kOffStats);  // [2][kMaxGroup]
   float* l_loc = m_loc + 2 * kMaxGroup;                          // [2][kMaxGroup]
   float* s_new = l_loc + 2 * kMaxGroup;                          // [2][kMaxGroup]
@@ -257,6 +258,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&qfree[i], 1);
       mbar_init(&handoff[i], 4);   // the four epilogue warps
       mbar_init(&taildone[i], 2);  // the two tail warps
+      mbar_init(&statrdy[i], 1);
     }
     mbar_init(drain, 1);
     fence_mbar_init();
@@ -679,6 +681,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           m_loc[b2 * kMaxGroup + tid] = ml[tid];
           l_loc[b2 * kMaxGroup + tid] = sl;
         }
+        // This CTA's (m, l), logits and candidate weights are final: the tail
+        // warps exchange and score them while the unit's V tiles still stream.
+        __syncwarp();
+        if (tid == 0) mbar_arrive(&statrdy[b2]);
         // The output accumulator: thread e <-> TMEM lane e <-> output element e.
         if (!bad2 && __all_sync(0xffffffffu, mbar_wait_bounded(ofull, (uint32_t)(ne & 1)))) {
           tc_fence_after();
@@ -691,14 +697,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         } else {
           bad2 = true;
         }
-      }
-      if (rows > 0) ne += 1;
-      const bool failed = any_bad || named_bar_or(1, kTcCompute, bad2);
-      if (rows == 0 || failed) {
+      } else {
+        // Nothing of this unit here (or a wait ran out): no statistics.
         if (tid < G) {
           m_loc[b2 * kMaxGroup + tid] = -INFINITY;
           l_loc[b2 * kMaxGroup + tid] = 0.f;
         }
+        __syncwarp();
+        if (tid == 0) mbar_arrive(&statrdy[b2]);
+      }
+      if (rows > 0) ne += 1;
+      const bool failed = any_bad || named_bar_or(1, kTcCompute, bad2);
+      if (rows == 0 || failed) {
 #pragma unroll
         for (int h = 0; h < G; ++h) o_part[h * D + tid] = 0.f;
       }
@@ -739,7 +749,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const float* mlc = m_loc + b2 * kMaxGroup;
       const float* llc = l_loc + b2 * kMaxGroup;
 
-      // The new token's logits (every CTA computes them), before the hand-off wait.
+      // The new token's logits (every CTA computes them), before the waits.
       for (int h = twarp; h < G; h += 2) {
         float s = 0.f;
         for (int e = lane; e < D; e += 32)
@@ -747,10 +757,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         s = warp_sum(s);
         if (lane == 0) snw[h] = s * a.scale_log2;
       }
-      const bool got_unit = __all_sync(
-          0xffffffffu, mbar_wait_bounded(&handoff[b2], (uint32_t)((k >> 1) & 1)));
+      // This CTA's (m, l), logits and weights: exchanged and scored while the
+      // unit's V tiles still stream.
+      const bool got_loc = __all_sync(
+          0xffffffffu, mbar_wait_bounded(&statrdy[b2], (uint32_t)((k >> 1) & 1)));
       named_bar_sync(2, kTcTail);
-      const bool unit_failed = !got_unit || uflag[b2] != 0;
+      // The partial output and the unit's failure flag, once the output
+      // accumulator is read (the epilogue's hand-off).  Every tail thread calls it.
+      auto unit_handoff = [&]() -> bool {
+        const bool got = __all_sync(
+            0xffffffffu, mbar_wait_bounded(&handoff[b2], (uint32_t)((k >> 1) & 1)));
+        named_bar_sync(2, kTcTail);
+        return !got || !got_loc || uflag[b2] != 0;
+      };
 
       if constexpr (kSplit) {
         if (is_piece(k)) {
@@ -804,7 +823,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           // Exact scores of this CTA's slots, its lowest candidate.
           float bs = INFINITY;
           int bi = INT_MAX;
-          if (rl.choosing && !unit_failed && stats_ok) {
+          if (rl.choosing && got_loc && stats_ok) {
             float cm[G];
 #pragma unroll
             for (int h = 0; h < G; ++h) cm[h] = cmul[h];
@@ -836,6 +855,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             red_ti[twarp] = bi;
           }
           named_bar_sync(2, kTcTail);
+          const bool unit_failed = unit_handoff();
           // Exchange 2: partial output, lowest (score, slot) and failure flag to piece 0.
           for (int c = tt_id; c < G * D; c += kTcTail) gfn[(size_t)me * kFinF + c] = o_part[c];
           if (tt_id == 0) {
@@ -982,10 +1002,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // candidates.  LongFlow: ||v_i|| sum_h alpha_{h,i}.  H2O: the slot's
       // accumulator plus this step's sum_h alpha_{h,i}.  Layer scope: every score
       // goes to the scratch for the selection kernel, and the H2O accumulators
-      // are written back here.
+      // are written back here.  Scores that write nothing to global memory are
+      // taken before the hand-off; the others wait for it, so that a failed unit
+      // leaves its accumulators and the scratch alone.
+      const bool early = !h2o && !layer;
+      bool unit_failed = early ? false : unit_handoff();
       float bs = INFINITY;
       int bi = INT_MAX;
-      const bool scoring = (rl.choosing || h2o) && !unit_failed && stats_ok;
+      const bool scoring = (rl.choosing || h2o) && !unit_failed && got_loc && stats_ok;
       if (scoring) {
         float cm[G];
 #pragma unroll
@@ -1045,6 +1069,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           a.acc[ubase + slot] = fabsf(w_s[i]) + as;
         }
       }
+      if (early) unit_failed = unit_handoff();
 
       // Exchange 2: partial output and lowest (score, slot) to the unit's leader.
       // One receive buffer suffices: a peer can send the leader's next unit only
