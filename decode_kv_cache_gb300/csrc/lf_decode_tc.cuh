@@ -1002,10 +1002,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // candidates.  LongFlow: ||v_i|| sum_h alpha_{h,i}.  H2O: the slot's
       // accumulator plus this step's sum_h alpha_{h,i}.  Layer scope: every score
       // goes to the scratch for the selection kernel, and the H2O accumulators
-      // are written back here.  Scores that write nothing to global memory are
-      // taken before the hand-off; the others wait for it, so that a failed unit
-      // leaves its accumulators and the scratch alone.
-      const bool early = !h2o && !layer;
+      // are written back here.  The per-KV-head scores are taken before the
+      // hand-off; every write to global memory (the scratch, the accumulators)
+      // waits for it, so that a failed unit leaves them alone.
+      const bool early = !layer;
       bool unit_failed = early ? false : unit_handoff();
       float bs = INFINITY;
       int bi = INT_MAX;
@@ -1049,11 +1049,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         red_ti[twarp] = bi;
       }
       named_bar_sync(2, kTcTail);
+      if (early) unit_failed = unit_handoff();
       // H2O, per-KV-head scope: write back the accumulators of this CTA's slots
       // except the dropped slot and the CTA's lowest candidate.  The leader
       // writes that one (it may be the victim, which takes the new token's), so
       // no slot has two writers.
-      if (scoring && h2o && !layer) {
+      if (scoring && h2o && !layer && !unit_failed) {
         int ci = red_ti[0];
         float cs = red_t[0];
         if (better(red_t[1], red_ti[1], cs, ci)) ci = red_ti[1];
@@ -1069,7 +1070,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           a.acc[ubase + slot] = fabsf(w_s[i]) + as;
         }
       }
-      if (early) unit_failed = unit_handoff();
 
       // Exchange 2: partial output and lowest (score, slot) to the unit's leader.
       // One receive buffer suffices: a peer can send the leader's next unit only
