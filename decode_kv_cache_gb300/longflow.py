@@ -21,10 +21,12 @@ __all__ = [
     "LF_OK", "LF_ERR_ARG", "LF_ERR_OOM", "LF_ERR_CUDA", "LF_ERR_DEVICE", "LF_ERR_UNSUPPORTED",
     "LF_BF16", "LF_F32", "LF_KERNEL_AUTO", "LF_KERNEL_SIMT", "LF_KERNEL_TENSOR_CORE",
     "LF_DEVERR_NONFINITE", "LF_DEVERR_STATE", "LF_DEVERR_TIMEOUT",
+    "LF_EVICT_OFF", "LF_EVICT_LONGFLOW", "LF_EVICT_RKV", "LF_SCORE_LONGFLOW", "LF_SCORE_H2O",
+    "LF_SCOPE_KV_HEAD", "LF_SCOPE_LAYER",
     "LFError", "LFConfig", "LFLayout", "load_library", "library_path",
     "lf_cache_create", "lf_cache_create_ex", "lf_cache_destroy", "lf_prefill_fill",
     "lf_decode_step", "lf_cache_check", "lf_cache_layout", "lf_last_error", "lf_abi_version",
-    "lf_prefill_fill_noalloc",
+    "lf_prefill_fill_noalloc", "lf_rkv_compress",
     "LFCache",
 ]
 
