@@ -76,6 +76,9 @@ def test_full_kv_read_only():
 
 
 def test_ragged_serving_shape():
+    """Mixed budgets and prompts at full batch; 1100 steps cross the first
+    abrupt query reset (every 1000 steps) and the prompt overflow of the
+    sequences whose prompt exceeds their budget."""
     wl = WORKLOADS["ragged-serving"]
     budgets = InputStream(wl, seed=0, device="cpu", layers=[0]).budgets  # same seeded draw
     # one sampled sequence per budget value
@@ -83,8 +86,8 @@ def test_ragged_serving_shape():
     for B in sorted(set(budgets)):
         b = budgets.index(B)
         picks += [(0, b, 0), (0, b, 7)]
-    st = _run(wl, 300, layers=(0,), sample=picks)
-    assert st.unit_steps == 300 * len(picks)
+    st = _run(wl, 1100, layers=(0,), sample=picks)
+    assert st.unit_steps == 1100 * len(picks)
 
 
 @pytest.mark.parametrize("case", [
