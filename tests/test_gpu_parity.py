@@ -4,6 +4,8 @@ Small cases run every unit through the oracle.  The large workloads run one or
 two layers at their full per-layer size (batch, heads, budget, window: the
 launch configuration the benchmark times) and replay a sample of units.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -20,8 +22,15 @@ def _run(wl, steps, **kw):
         run.run(steps)
         run.compare_state()
         run.check_invariants()
-        run.stats.assert_ok()
-        return run.stats
+        st = run.stats
+        # one line per case (shown with pytest -s): the parity counts of the run
+        case = os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0]
+        print(f"\nparity {case}: {st.unit_steps} unit-steps, {st.evictions} evictions, "
+              f"{st.near_ties} near-ties, {st.resyncs} resyncs, "
+              f"{len(st.hard_mismatches)} mismatches, max output error "
+              f"{st.max_out_violation:.3f} of tolerance")
+        st.assert_ok()
+        return st
     finally:
         run.close()
 
