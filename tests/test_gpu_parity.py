@@ -62,6 +62,23 @@ def test_r1_llama_shape_eviction_phase():
     assert st.evictions >= 3 * 120
 
 
+def test_r1_llama_full_generation():
+    """The R1-Llama-8B-shaped workload end to end on one layer at full batch:
+    prompt 512, then all 16384 decode steps (2764 fill steps up to the 3276-slot
+    budget, then 13620 evicting steps), two sampled units replayed throughout."""
+    wl = WORKLOADS["r1-llama-8b"]
+    st = _run(wl, 16384, layers=(7,), sample=[(0, 0, 0), (0, 31, 7)])
+    assert st.evictions == 2 * (16384 - (3276 - 512))
+
+
+def test_qwen3_06b_full_generation():
+    """The Qwen3-0.6B-shaped workload end to end on one layer: prompt 256, all
+    4096 decode steps (256 fill, then evictions at budget 512)."""
+    wl = WORKLOADS["qwen3-0.6b"]
+    st = _run(wl, 4096, layers=(20,), sample=[(0, 2, 1), (0, 7, 6)])
+    assert st.evictions == 2 * (4096 - (512 - 256))
+
+
 def test_qwen3_8b_steady_state():
     wl = WORKLOADS["qwen3-8b-steady"]
     st = _run(wl, 120, layers=(0,), sample=[(0, 0, 0), (0, 63, 7), (0, 40, 2)])
