@@ -117,6 +117,9 @@ def check_deletion_identity(orc):
         o = r.out[0]
         for i in range(n):
             a = r.alpha[0, i]
+            # a softmax over n + 1 >= 2 finite logits puts every weight strictly
+            # inside (0, 1), so the identity's factor alpha / (1 - alpha) is finite
+            assert 0.0 < a < 1.0, (i, a)
             keep = [j for j in range(n + 1) if j != i]
             o_del = sdpa(q, keys[keep][None], vals[keep][None])[0]
             pred = a / (1 - a) * (o - vals[i])
