@@ -299,6 +299,36 @@ def check_fill_then_evict_slots(orc):
     assert u.n == B and u.p == 7
 
 
+def check_budget_below_capacity(orc):
+    """A per-sequence budget below the slab's capacity (the ragged serving
+    workload): the buffer fills to the budget, never further, and then every
+    step evicts among the budget's slots; the slots above the budget are never
+    written; a prompt longer than the budget is refused (guide, "Static Memory
+    Pre-Allocation and In-Place Eviction": the fixed budget B is the buffer)."""
+    rng = np.random.default_rng(RNG_SEED + 17)
+    cap, d, B, W = 12, 8, 7, 2
+    for deferred in (False, True):
+        pol = orc.Policy(deferred=deferred)
+        u = orc.OracleUnit(cap, d, B, W, True, pol)
+        u.prefill(rng.standard_normal((3, d)), rng.standard_normal((3, d)))
+        for t in range(30):
+            r = u.step(rng.standard_normal((1, d)), rng.standard_normal(d), rng.standard_normal(d))
+            assert u.n == min(B, 3 + t + 1), (deferred, t, u.n)
+            assert 0 <= r.written < B
+            if not deferred and 3 + t >= B:
+                assert 0 <= r.evicted < B
+        assert np.all(u.pos[B:] == -1) and not u.K[B:].any() and not u.V[B:].any()
+        assert sorted(u.pos[:B].tolist()) == sorted(set(u.pos[:B].tolist()))
+        long_prompt = B if deferred else B + 1
+        v = orc.OracleUnit(cap, d, B, W, True, pol)
+        try:
+            v.prefill(np.zeros((long_prompt, d)), np.zeros((long_prompt, d)))
+        except ValueError:
+            pass
+        else:
+            raise AssertionError("a prompt longer than the buffer was accepted")
+
+
 def check_eviction_off_full_cache(orc):
     """Eviction off: tokens append up to the capacity, then the cache is read
     only -- every step still attends over all cached slots plus the new token."""
@@ -535,6 +565,7 @@ ALL_CHECKS = [
     check_exact_tie_lowest_slot,
     check_cap_and_window_invariants,
     check_fill_then_evict_slots,
+    check_budget_below_capacity,
     check_eviction_off_full_cache,
     check_l2_norm_and_sinks_against_library,
     check_deferred_equals_same_step_one_slot_larger,

@@ -43,6 +43,10 @@ MUTANTS = {
                         "written = (n + 1) % u0.capacity"),
     "position_off_by_one": ("u._write(written, kn, vn, p)", "u._write(written, kn, vn, p + 1)"),
     "no_write_on_evict": ("        written = evicted\n", "        written = -1\n"),
+    "budget_ignored": ("if u0.evict and n >= u0.budget:", "if u0.evict and n >= u0.capacity:"),
+    "limit_is_capacity": ("return self.budget if self.evict else self.capacity",
+                          "return self.capacity"),
+    "deferred_budget_ignored": ("    if n < u0.budget:\n", "    if n < u0.capacity:\n"),
     # policy variants
     "sinks_ignored": ("& (pos >= sinks)", "& (pos >= 0)"),
     "sinks_off_by_one": ("& (pos >= sinks)", "& (pos > sinks)"),
