@@ -1,0 +1,254 @@
+"""A CPU model of the tensor-core decode kernel's four warp roles and their
+mbarriers (CPU only; no GPU involved).
+
+The kernel (decode_kv_cache_gb300/csrc/lf_decode_tc.cuh) runs, in every CTA,
+a producer warp (TMA tiles into a ring of S stages), an MMA warp, four
+epilogue warps and two tail warps.  They hand work to each other only through
+mbarriers: the tile ring (full / empty), the logit accumulators (sfull /
+sfree, 16 of them), the P^T tiles (pready / pfree, 4), the output accumulator
+(ofull), and the per-parity unit buffers (aux / auxfree, statrdy, handoff,
+taildone).  The ring order is shared by the producer and the MMA warp: K of
+the first non-empty unit, then for each next non-empty unit its first L K
+tiles, the V tiles of the unit before it, and its remaining K tiles.  A V
+block still pending when the walk reaches two units past it is issued alone
+first (the flush), because the producer's wait on the unit-2 buffers needs it.
+
+Here each role is a generator that performs the same arrivals and waits in the
+same order as its warp; a random scheduler interleaves them.  The model checks,
+over many seeded patterns of empty and non-empty units:
+  * liveness: every role finishes (no state where all remaining roles wait);
+  * no phase aliasing: a parity wait never sees its barrier two or more phases
+    past the phase it waits for (the hardware wait would then block or pass on
+    the wrong phase);
+  * the producer's ring order and the MMA warp's are the same tile for tile.
+Planting a mistake shows the checks bite: without the flush the model finds
+deadlocks (the epilogue waits for a unit's output whose V tiles the producer
+holds back), and a flush in the producer alone breaks the shared order.
+The exchanges between the CTAs of a cluster are left out: a single CTA's tail
+finds its peers' statistics at once.
+"""
+import random
+
+import pytest
+
+SBUFS, PBUFS = 16, 4     # logit accumulators and P^T tiles in flight (as in the kernel)
+TILE = 128
+
+
+def ntiles(rows):
+    return (rows + TILE - 1) // TILE
+
+
+def ring_order(rows, lookahead, flush):
+    """The tile order one role derives from the unit list: (kind, item, tile)."""
+    order, prev = [], None
+    for k, r in enumerate(rows):
+        if flush and prev is not None and prev <= k - 2:
+            order += [("V", prev, t) for t in range(ntiles(rows[prev]))]
+            prev = None
+        if r == 0:
+            continue
+        nt = ntiles(r)
+        if prev is None:
+            order += [("K", k, t) for t in range(nt)]
+        else:
+            L = min(nt, lookahead)
+            order += [("K", k, t) for t in range(L)]
+            order += [("V", prev, t) for t in range(ntiles(rows[prev]))]
+            order += [("K", k, t) for t in range(L, nt)]
+        prev = k
+    if prev is not None:
+        order += [("V", prev, t) for t in range(ntiles(rows[prev]))]
+    return order
+
+
+class Model:
+    def __init__(self, rows, stages, lookahead, producer_flush=True, mma_flush=True):
+        self.rows = rows
+        self.S = stages
+        self.L = lookahead
+        self.count = {}          # (barrier, slot) -> completed phases
+        self.produced = []       # ring order as issued by the producer
+        self.consumed = []       # ring order as consumed by the MMA warp
+        self.pflush, self.mflush = producer_flush, mma_flush
+
+    # -- barriers -------------------------------------------------------------
+    def arrive(self, name, slot=0):
+        key = (name, slot)
+        self.count[key] = self.count.get(key, 0) + 1
+
+    def done(self, wait):
+        name, slot, phase = wait
+        c = self.count.get((name, slot), 0)
+        assert c <= phase + 1, f"phase aliasing on {name}[{slot}]: {c} completions, waits for {phase}"
+        return c >= phase + 1
+
+    # -- roles (same arrivals and waits, in the same order, as the warps) -------
+    def producer(self):
+        S, tt = self.S, 0
+        order = ring_order(self.rows, self.L, self.pflush)
+        # split the order at the points where the producer handles each item
+        prev = None
+        plan = []                 # (item, tiles to flush first, tiles of the item)
+        o = 0
+        for k, r in enumerate(self.rows):
+            flush = []
+            if self.pflush and prev is not None and prev <= k - 2:
+                n = ntiles(self.rows[prev])
+                flush = order[o:o + n]
+                o += n
+                prev = None
+            own = []
+            if r > 0:
+                n = ntiles(r) + (ntiles(self.rows[prev]) if prev is not None else 0)
+                own = order[o:o + n]
+                o += n
+                prev = k
+            plan.append((k, flush, own))
+        tail = order[o:]
+
+        def emit(tiles):
+            nonlocal tt
+            for tile in tiles:
+                if tt >= S:
+                    yield ("empty", tt % S, tt // S - 1)
+                self.produced.append(tile)
+                self.arrive("full", tt % S)       # the TMA bytes land
+                tt += 1
+
+        for k, flush, own in plan:
+            yield from emit(flush)
+            if k >= 2:
+                yield ("auxfree", k & 1, (k >> 1) - 1)
+            self.arrive("aux", k & 1)             # ||v|| and positions of unit k
+            yield from emit(own)
+        yield from emit(tail)
+
+    def mma(self):
+        S = self.S
+        order = ring_order(self.rows, self.L, self.mflush)
+        tt = kt = pt = 0
+        for tile in order:
+            kind = tile[0]
+            if kind == "K":
+                yield ("full", tt % S, tt // S)
+                if kt >= SBUFS:
+                    yield ("sfree", kt % SBUFS, kt // SBUFS - 1)
+                self.consumed.append(tile)
+                self.arrive("sfull", kt % SBUFS)
+                self.arrive("empty", tt % S)
+                kt += 1
+            else:
+                yield ("pready", pt % PBUFS, pt // PBUFS)
+                yield ("full", tt % S, tt // S)
+                self.consumed.append(tile)
+                self.arrive("empty", tt % S)
+                self.arrive("pfree", pt % PBUFS)
+                pt += 1
+                item, t = tile[1], tile[2]
+                if t == ntiles(self.rows[item]) - 1:
+                    self.arrive("ofull")          # the unit's output accumulator is final
+            tt += 1
+
+    def epilogue(self):
+        kt = pt = ne = 0
+        for k, r in enumerate(self.rows):
+            if k >= 2:
+                yield ("taildone", k & 1, (k >> 1) - 1)
+            yield ("aux", k & 1, k >> 1)
+            for _ in range(ntiles(r)):
+                yield ("sfull", kt % SBUFS, kt // SBUFS)
+                self.arrive("sfree", kt % SBUFS)
+                kt += 1
+            self.arrive("auxfree", k & 1)
+            if r > 0:
+                for _ in range(ntiles(r)):
+                    if pt >= PBUFS:
+                        yield ("pfree", pt % PBUFS, pt // PBUFS - 1)
+                    self.arrive("pready", pt % PBUFS)
+                    pt += 1
+                self.arrive("statrdy", k & 1)
+                yield ("ofull", 0, ne)
+                ne += 1
+            else:
+                self.arrive("statrdy", k & 1)
+            self.arrive("handoff", k & 1)
+
+    def tail(self):
+        for k in range(len(self.rows)):
+            yield ("statrdy", k & 1, k >> 1)
+            yield ("handoff", k & 1, k >> 1)
+            self.arrive("taildone", k & 1)
+
+    # -- a random interleaving ---------------------------------------------------
+    def run(self, rng):
+        roles = {"producer": self.producer(), "mma": self.mma(), "epilogue": self.epilogue(),
+                 "tail": self.tail()}
+        waits = {}
+        for name, g in roles.items():
+            w = next(g, None)
+            if w is not None:
+                waits[name] = w
+        while waits:
+            ready = [n for n, w in waits.items() if self.done(w)]
+            if not ready:
+                return "deadlock", dict(waits)
+            n = rng.choice(ready)
+            w = next(roles[n], None)
+            if w is None:
+                del waits[n]
+            else:
+                waits[n] = w
+        return "done", None
+
+
+def random_rows(rng, n_items):
+    rows = []
+    for _ in range(n_items):
+        x = rng.random()
+        if x < 0.4:
+            rows.append(0)                               # empty: no share of this unit here
+        elif x < 0.6:
+            rows.append(rng.randint(1, TILE))            # one (ragged) tile
+        else:
+            rows.append(rng.randint(TILE + 1, 14 * TILE))
+    return rows
+
+
+@pytest.mark.parametrize("stages,lookahead", [(3, 2), (2, 1), (4, 3), (3, 8)])
+def test_kernel_protocol_is_live_and_alias_free(stages, lookahead):
+    rng = random.Random(1000 * stages + lookahead)
+    for trial in range(400):
+        rows = random_rows(rng, rng.randint(1, 12))
+        m = Model(rows, stages, lookahead)
+        status, waits = m.run(rng)
+        assert status == "done", (rows, waits)
+        assert m.produced == m.consumed == ring_order(rows, lookahead, True)
+        assert all(m.count.get(("handoff", b), 0) == (len(rows) + 1 - b) // 2 for b in (0, 1))
+
+
+def test_without_the_flush_a_unit_after_two_empty_ones_deadlocks():
+    rows = [300, 0, 0, 200]
+    status, waits = Model(rows, 3, 2, producer_flush=False, mma_flush=False).run(random.Random(0))
+    assert status == "deadlock"
+    # the epilogue waits for unit 0's output; the producer holds its V tiles back
+    assert waits["epilogue"][0] == "ofull" and waits["producer"][0] == "auxfree"
+    assert Model(rows, 3, 2).run(random.Random(0))[0] == "done"
+
+
+def test_without_the_flush_random_patterns_deadlock():
+    rng = random.Random(7)
+    found = 0
+    for _ in range(300):
+        rows = random_rows(rng, rng.randint(3, 12))
+        if Model(rows, 3, 2, producer_flush=False, mma_flush=False).run(rng)[0] == "deadlock":
+            found += 1
+    assert found > 0
+
+
+def test_flush_in_one_role_only_breaks_the_shared_order():
+    rows = [300, 0, 0, 200]
+    m = Model(rows, 3, 2, producer_flush=True, mma_flush=False)
+    status, _ = m.run(random.Random(0))
+    # the MMA warp reads a stage as the wrong tile (here: a V tile of unit 0 as K of unit 3)
+    assert any(p != c for p, c in zip(m.produced, m.consumed)) or status == "deadlock"
