@@ -24,8 +24,13 @@ over many seeded patterns of empty and non-empty units:
 Planting a mistake shows the checks bite: without the flush the model finds
 deadlocks (the epilogue waits for a unit's output whose V tiles the producer
 holds back), and a flush in the producer alone breaks the shared order.
-The exchanges between the CTAs of a cluster are left out: a single CTA's tail
-finds its peers' statistics at once.
+ClusterModel adds the exchanges between the CTAs of a cluster (clusters of 1,
+2 and 4; each CTA holds its share of every unit, possibly none): every CTA's
+(m, l) to every CTA, then its partial output to the unit's leader.  Each
+transfer checks that it lands in the phase it is meant for and that the
+receiving buffer is no longer read; a planted single statistics buffer fails
+that check.  The split launch's shared units (exchanges through global memory)
+are not modelled.
 """
 import random
 
@@ -63,23 +68,25 @@ def ring_order(rows, lookahead, flush):
 
 
 class Model:
-    def __init__(self, rows, stages, lookahead, producer_flush=True, mma_flush=True):
+    def __init__(self, rows, stages, lookahead, producer_flush=True, mma_flush=True,
+                 cta=0, count=None):
         self.rows = rows
         self.S = stages
         self.L = lookahead
-        self.count = {}          # (barrier, slot) -> completed phases
+        self.cta = cta
+        self.count = {} if count is None else count   # (cta, barrier, slot) -> completed phases
         self.produced = []       # ring order as issued by the producer
         self.consumed = []       # ring order as consumed by the MMA warp
         self.pflush, self.mflush = producer_flush, mma_flush
 
     # -- barriers -------------------------------------------------------------
     def arrive(self, name, slot=0):
-        key = (name, slot)
+        key = (self.cta, name, slot)
         self.count[key] = self.count.get(key, 0) + 1
 
     def done(self, wait):
         name, slot, phase = wait
-        c = self.count.get((name, slot), 0)
+        c = self.count.get((self.cta, name, slot), 0)
         assert c <= phase + 1, f"phase aliasing on {name}[{slot}]: {c} completions, waits for {phase}"
         return c >= phase + 1
 
@@ -202,6 +209,129 @@ class Model:
         return "done", None
 
 
+class TxBarrier:
+    """An mbarrier completed by its owner's arrive.expect_tx plus `senders`
+    remote st.async transfers.  A transfer must land in the phase it is meant
+    for: landing while the previous phase is still open would complete that one
+    with the wrong data."""
+
+    def __init__(self, senders):
+        self.senders = senders
+        self.completed = 0
+        self.landed = 0
+        self.armed = False
+
+    def _maybe_complete(self):
+        if self.armed and self.landed == self.senders:
+            self.completed += 1
+            self.landed, self.armed = 0, False
+
+    def arm(self, phase):
+        assert self.completed == phase and not self.armed, (self.completed, phase)
+        self.armed = True
+        self._maybe_complete()
+
+    def land(self, phase):
+        assert self.completed == phase, f"transfer for phase {phase} lands in phase {self.completed}"
+        self.landed += 1
+        assert self.landed <= self.senders
+        self._maybe_complete()
+
+
+class ClusterModel:
+    """C CTAs of one cluster walk the same unit list; CTA `rank` holds the
+    slots [rank*per, (rank+1)*per) of each unit (per = ceil(n/C) rounded up
+    to 4).  Besides the roles of every CTA, the tail warps run the two
+    exchanges: every CTA sends its (m, l) to every CTA (statb, one buffer per
+    unit parity), then its partial output to the unit's leader, rank k mod C
+    (finb, a single buffer).  Each transfer checks that the receiving buffer
+    is free: the receiver has finished the unit that last used it."""
+
+    def __init__(self, occupied, cluster, stages, lookahead, mistake=None):
+        self.n = occupied
+        self.C = cluster
+        self.mistake = mistake    # a planted protocol error (tests of the model itself)
+        self.count = {}
+        self.ctas = []
+        for r in range(cluster):
+            rows = []
+            for n in occupied:
+                per = ((n + cluster - 1) // cluster + 3) & ~3
+                rows.append(max(0, min(per, n - r * per)))
+            m = Model(rows, stages, lookahead, cta=r, count=self.count)
+            m.tail = self._tail_fn(m)
+            self.ctas.append(m)
+        self.statb = {(r, b): TxBarrier(cluster) for r in range(cluster) for b in (0, 1)}
+        self.finb = {r: TxBarrier(cluster) for r in range(cluster)}
+        self.stats_read = [-1] * cluster   # last unit whose statistics each CTA has read
+        self.tail_done = [0] * cluster     # units each CTA's tail has finished
+
+    def _tail_fn(self, m):
+        C, r = self.C, m.cta
+
+        def tail():
+            for k in range(len(self.n)):
+                b2 = k & 1
+                yield ("statrdy", b2, k >> 1)
+                # exchange 1: arm this parity's receive barrier, send (m, l) to all
+                if self.mistake == "one_statistics_buffer":
+                    sb, sp, gap = 0, k, 1      # (planted) one buffer for every unit
+                else:
+                    sb, sp, gap = b2, k >> 1, 2
+                self.statb[(r, sb)].arm(sp)
+                for dst in range(C):
+                    assert self.stats_read[dst] >= k - gap, "statistics buffer still in use"
+                    self.statb[(dst, sb)].land(sp)
+                yield ("statb", sb, sp)
+                self.stats_read[r] = k
+                yield ("handoff", b2, k >> 1)          # the partial output is read
+                # exchange 2: partial output and lowest candidate to the leader
+                leader = k % C
+                if r == leader:
+                    self.finb[r].arm(k // C)
+                assert k < C or self.tail_done[leader] >= k - C + 1, "output buffer still in use"
+                self.finb[leader].land(k // C)
+                if r == leader:
+                    yield ("finb", 0, k // C)
+                self.tail_done[r] += 1
+                m.arrive("taildone", b2)
+        return tail
+
+    def done(self, cta, wait):
+        name, slot, phase = wait
+        if name == "statb":
+            bar = self.statb[(cta, slot)]
+        elif name == "finb":
+            bar = self.finb[cta]
+        else:
+            return self.ctas[cta].done(wait)
+        assert bar.completed <= phase + 1
+        return bar.completed >= phase + 1
+
+    def run(self, rng):
+        roles = {}
+        for m in self.ctas:
+            for name, fn in (("producer", m.producer), ("mma", m.mma), ("epilogue", m.epilogue),
+                             ("tail", m.tail)):
+                roles[(m.cta, name)] = fn()
+        waits = {}
+        for key, g in roles.items():
+            w = next(g, None)
+            if w is not None:
+                waits[key] = w
+        while waits:
+            ready = [key for key, w in waits.items() if self.done(key[0], w)]
+            if not ready:
+                return "deadlock", dict(waits)
+            key = rng.choice(ready)
+            w = next(roles[key], None)
+            if w is None:
+                del waits[key]
+            else:
+                waits[key] = w
+        return "done", None
+
+
 def random_rows(rng, n_items):
     rows = []
     for _ in range(n_items):
@@ -224,7 +354,7 @@ def test_kernel_protocol_is_live_and_alias_free(stages, lookahead):
         status, waits = m.run(rng)
         assert status == "done", (rows, waits)
         assert m.produced == m.consumed == ring_order(rows, lookahead, True)
-        assert all(m.count.get(("handoff", b), 0) == (len(rows) + 1 - b) // 2 for b in (0, 1))
+        assert all(m.count.get((0, "handoff", b), 0) == (len(rows) + 1 - b) // 2 for b in (0, 1))
 
 
 def test_without_the_flush_a_unit_after_two_empty_ones_deadlocks():
@@ -252,3 +382,39 @@ def test_flush_in_one_role_only_breaks_the_shared_order():
     status, _ = m.run(random.Random(0))
     # the MMA warp reads a stage as the wrong tile (here: a V tile of unit 0 as K of unit 3)
     assert any(p != c for p, c in zip(m.produced, m.consumed)) or status == "deadlock"
+
+
+@pytest.mark.parametrize("cluster", [1, 2, 4])
+def test_cluster_exchanges_are_live_and_reuse_free_buffers(cluster):
+    """Units of every size, including ones that leave some CTAs of the cluster
+    without slots (fewer than C*4 occupied), under random interleavings of all
+    roles of all CTAs."""
+    rng = random.Random(31 + cluster)
+    for _ in range(250):
+        occupied = []
+        for _ in range(rng.randint(1, 10)):
+            x = rng.random()
+            occupied.append(0 if x < 0.15 else rng.randint(1, 4 * cluster) if x < 0.4
+                            else rng.randint(1, 3276))
+        m = ClusterModel(occupied, cluster, 3, 2)
+        status, waits = m.run(rng)
+        assert status == "done", (occupied, waits)
+        assert m.tail_done == [len(occupied)] * cluster
+        for c in m.ctas:
+            assert c.produced == c.consumed
+
+
+def test_cluster_model_catches_a_single_statistics_buffer():
+    """Planted: one statistics receive buffer instead of one per unit parity.
+    A CTA that has finished a unit's first exchange can then send the next
+    unit's statistics while a slower peer is still reading the previous ones."""
+    rng = random.Random(5)
+    caught = 0
+    for _ in range(200):
+        occupied = [rng.randint(1, 3276) for _ in range(rng.randint(3, 10))]
+        try:
+            ClusterModel(occupied, 2, 3, 2, mistake="one_statistics_buffer").run(rng)
+        except AssertionError as e:
+            assert "statistics buffer still in use" in str(e)
+            caught += 1
+    assert caught > 0
