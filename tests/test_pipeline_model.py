@@ -29,8 +29,9 @@ ClusterModel adds the exchanges between the CTAs of a cluster (clusters of 1,
 (m, l) to every CTA, then its partial output to the unit's leader.  Each
 transfer checks that it lands in the phase it is meant for and that the
 receiving buffer is no longer read; a planted single statistics buffer fails
-that check.  The split launch's shared units (exchanges through global memory)
-are not modelled.
+that check.  For split launches the model puts a shared unit first, exchanged
+through global memory (taken as immediate here: the other cluster is not
+modelled), and checks the whole units' corrected phase indices.
 """
 import random
 
@@ -247,10 +248,13 @@ class ClusterModel:
     (finb, a single buffer).  Each transfer checks that the receiving buffer
     is free: the receiver has finished the unit that last used it."""
 
-    def __init__(self, occupied, cluster, stages, lookahead, mistake=None):
+    def __init__(self, occupied, cluster, stages, lookahead, mistake=None, shared_first=False):
         self.n = occupied
         self.C = cluster
         self.mistake = mistake    # a planted protocol error (tests of the model itself)
+        # split launch: item 0 is a unit shared with another cluster, exchanged through
+        # global memory (modelled as immediate); it uses neither statb nor finb
+        self.shared = shared_first
         self.count = {}
         self.ctas = []
         for r in range(cluster):
@@ -273,11 +277,20 @@ class ClusterModel:
             for k in range(len(self.n)):
                 b2 = k & 1
                 yield ("statrdy", b2, k >> 1)
+                if self.shared and k == 0:
+                    yield ("handoff", 0, 0)
+                    self.stats_read[r] = 0
+                    self.tail_done[r] += 1
+                    m.arrive("taildone", 0)
+                    continue
+                # the shared item completed no statb / finb phase: the phase index of
+                # a whole unit counts only the whole units before it
+                fix = self.shared and self.mistake != "uncorrected_phases"
                 # exchange 1: arm this parity's receive barrier, send (m, l) to all
                 if self.mistake == "one_statistics_buffer":
                     sb, sp, gap = 0, k, 1      # (planted) one buffer for every unit
                 else:
-                    sb, sp, gap = b2, k >> 1, 2
+                    sb, sp, gap = b2, (k >> 1) - (1 if fix and b2 == 0 else 0), 2
                 self.statb[(r, sb)].arm(sp)
                 for dst in range(C):
                     assert self.stats_read[dst] >= k - gap, "statistics buffer still in use"
@@ -287,12 +300,13 @@ class ClusterModel:
                 yield ("handoff", b2, k >> 1)          # the partial output is read
                 # exchange 2: partial output and lowest candidate to the leader
                 leader = k % C
+                fp = k // C - (1 if fix and leader == 0 else 0)
                 if r == leader:
-                    self.finb[r].arm(k // C)
+                    self.finb[r].arm(fp)
                 assert k < C or self.tail_done[leader] >= k - C + 1, "output buffer still in use"
-                self.finb[leader].land(k // C)
+                self.finb[leader].land(fp)
                 if r == leader:
-                    yield ("finb", 0, k // C)
+                    yield ("finb", 0, fp)
                 self.tail_done[r] += 1
                 m.arrive("taildone", b2)
         return tail
@@ -418,3 +432,20 @@ def test_cluster_model_catches_a_single_statistics_buffer():
             assert "statistics buffer still in use" in str(e)
             caught += 1
     assert caught > 0
+
+
+@pytest.mark.parametrize("cluster", [1, 2])
+def test_split_launch_phase_indices(cluster):
+    """Split launches put a unit shared with another cluster first; it is
+    exchanged through global memory, so it completes no statb / finb phase.
+    The whole units' phase indices subtract it (the kernel's stat_phase and
+    fin_phase): the model runs clean with that correction, and without it a
+    transfer lands in the wrong phase."""
+    rng = random.Random(90 + cluster)
+    for _ in range(150):
+        occupied = [rng.randint(1, 3276) for _ in range(rng.randint(2, 9))]
+        m = ClusterModel(occupied, cluster, 3, 2, shared_first=True)
+        assert m.run(rng)[0] == "done", occupied
+    with pytest.raises(AssertionError):
+        ClusterModel([3276] * 5, cluster, 3, 2, shared_first=True,
+                     mistake="uncorrected_phases").run(random.Random(0))
