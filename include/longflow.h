@@ -24,13 +24,13 @@
  *
  * Policy variants (lf_config; the defaults are the operation above):
  *   norm = 2       score_i = ||v_i||_2 * sum_h alpha_{h,i}: the guide, same section,
- *                  defines the importance as the "l1-norm or l2-norm" of c_{t,i};
+ *                  lets the importance be either the l1 or the l2 norm of c_{t,i};
  *   sinks = s      positions 0..s-1 are never evicted (the guide's reference step,
  *                  section "End-to-End Implementation", protects its first
  *                  sink_size slots);
- *   deferred = 1   the order of that reference step and of the fused kernel's step 4
- *                  ("the physical slot index to be overwritten in the next
- *                  iteration"): the new token first takes the next free slot, or
+ *   deferred = 1   the order of that reference step and of the fused kernel's step 4,
+ *                  whose output is the slot that the following step overwrites:
+ *                  the new token first takes the next free slot, or
  *                  the slot chosen at the previous step, and is attended from the
  *                  buffer; once the buffer is full the lowest-score slot with
  *                  pos_i < p + 1 - window becomes the slot the next token takes
@@ -42,8 +42,8 @@
  *                  summed over the group's query heads and over every decode step
  *                  since it entered the buffer, its entry step included (prompt
  *                  tokens start at 0) -- the cumulative statistic the guide
- *                  attributes to H2O ("The Long-Output Reasoning Crisis" and the
- *                  comparison table, "Cumulative Attention Mass").
+ *                  attributes to H2O (section "The Long-Output Reasoning Crisis"
+ *                  and H2O's row of the comparison table).
  *
  * Storage: one static slab per cache, allocated once by lf_cache_create*,
  * never grown, moved or compacted.  All per-step work is stream-ordered and

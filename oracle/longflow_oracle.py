@@ -35,13 +35,13 @@ Readings where the pages are silent or ambiguous:
 
 Policy variants (``Policy``), each a plain reading of a passage:
 
-* ``norm=2``: the score uses ||v_i||_2 -- the guide defines the importance as
-  "the l1-norm or l2-norm" of c_{t,i} ("Mathematical Derivation ...").
+* ``norm=2``: the score uses ||v_i||_2 -- the guide lets the importance be
+  either the l1 or the l2 norm of c_{t,i} ("Mathematical Derivation ...").
 * ``sinks=s``: positions 0..s-1 are never evicted -- the guide's reference step
   ("End-to-End Implementation") protects its first sink_size slots.
 * ``deferred=True``: the order of the guide's reference step and of its fused
-  kernel's step 4 ("the physical slot index to be overwritten in the next
-  iteration"): the new token is first written into the slot chosen at the
+  kernel's step 4, whose output is the slot that the following step
+  overwrites: the new token is first written into the slot chosen at the
   previous step (or the next free slot while filling), the query attends over
   the buffer, and the lowest-score slot outside the window becomes the slot
   the next token overwrites.  The window then counts the new token: slots with
@@ -50,7 +50,9 @@ Policy variants (``Policy``), each a plain reading of a passage:
   scored by the sum over every query head -- the guide's reference step sums
   |c| over heads and feature dimensions.
 * ``score="h2o"``: cumulative attention mass -- the comparison the guide draws
-  with H2O ("cumulative attention statistics", "Cumulative Attention Mass").
+  with H2O, which scores tokens by the attention they have accumulated
+  (section "The Long-Output Reasoning Crisis" and H2O's row of the comparison
+  table).
   Each slot keeps the sum of the attention weights its token has received
   (over the group's query heads) at every decode step since it entered the
   buffer, its own entry step included; a prompt token starts at zero.  The

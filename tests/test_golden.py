@@ -4,7 +4,7 @@
 Validation Benchmark": 8 heads of dimension 64, a 1000-token budget, 2500
 decode steps with fresh standard-normal q, k and v, starting from an empty
 buffer.  The guide prints the number of finished steps and a final cache length
-of 1000, "strictly capped" at the budget.  The fixture in
+of 1000, which it says can never exceed the budget.  The fixture in
 tests/golden/guide_functional_validation.json holds those printed values.
 
 The run uses the guide listing's own choices (section "End-to-End
