@@ -29,9 +29,10 @@ Readings where the README is silent:
 * importance I_i = the mean over those alpha * G queries of their softmax
   weight on candidate i, the softmax taken over every candidate (scale
   1/sqrt(d));
-* "highly similar" means cosine >= tau; token i is redundant (R_i = 1) when at
-  least beta candidates with a later position are highly similar to it, else
-  R_i = 0.  The README gives no tau or beta: tau = 0.9, beta = 1 here;
+* two keys count as near-duplicates when their cosine is >= tau; token i is
+  redundant (R_i = 1) when at least beta candidates with a later position are
+  near-duplicates of it, else R_i = 0.  The README gives no tau or beta:
+  tau = 0.9, beta = 1 here;
 * the alpha most recent positions are the observation tokens and always stay;
   the other B_budget - alpha places go to the highest Z, exact ties to the
   more recent token;
