@@ -61,6 +61,13 @@ struct lf_cache {
 namespace {
 
 thread_local std::string g_last_error;
+thread_local int g_last_status = LF_OK;
+
+// A call starts with no recorded failure.
+void clear_last() {
+  g_last_error.clear();
+  g_last_status = LF_OK;
+}
 
 // Split launches only once every sequence of the layer holds this many tokens.
 constexpr long long kSplitMinSlots = 2048;
@@ -72,6 +79,7 @@ int fail(int code, const char* fmt, ...) {
   vsnprintf(buf, sizeof(buf), fmt, ap);
   va_end(ap);
   g_last_error = buf;
+  g_last_status = code;
   return code;
 }
 
@@ -147,11 +155,16 @@ void destroy_memory(lf_cache* c) {
 
 }  // namespace
 
-void lf::set_last_error(const std::string& msg) { g_last_error = msg; }
+void lf::set_last_error(int code, const std::string& msg) {
+  g_last_error = msg;
+  g_last_status = code;
+}
 
 extern "C" {
 
 const char* lf_last_error(void) { return g_last_error.c_str(); }
+
+int lf_last_status(void) { return g_last_status; }
 
 int lf_abi_version(void) { return LF_ABI_VERSION; }
 
@@ -162,7 +175,7 @@ lf_cache* lf_cache_create(int layers, int batch, int kv_heads, int q_heads, int 
 
 lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, int head_dim,
                              int capacity, int window, const lf_config* cfg) {
-  g_last_error.clear();
+  clear_last();
   lf_config def = {LF_BF16, 1, nullptr, 0, 0, LF_KERNEL_AUTO, LF_SCORE_LONGFLOW, 1, 0, 0,
                    LF_SCOPE_KV_HEAD, 0, 0, 0, 0.f, 0.f};
   lf_config c = cfg ? *cfg : def;
@@ -548,7 +561,7 @@ lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, i
 }
 
 int lf_cache_destroy(lf_cache* cache) {
-  g_last_error.clear();
+  clear_last();
   if (!cache) return LF_OK;
   destroy_memory(cache);
   delete cache;
@@ -557,7 +570,7 @@ int lf_cache_destroy(lf_cache* cache) {
 
 int lf_prefill_fill(lf_cache* cache, int layer, const void* k, const void* v,
                     const int32_t* prompt_len, int max_prompt, lf_stream_t stream) {
-  g_last_error.clear();
+  clear_last();
   if (!cache) return fail(LF_ERR_ARG, "null cache");
   if (layer < 0 || layer >= cache->layers)
     return fail(LF_ERR_ARG, "layer %d outside [0, %d)", layer, cache->layers);
@@ -777,7 +790,7 @@ int lf_rkv_compress(lf_cache* cache, int layer, const void* q_obs, lf_stream_t s
 }
 
 int lf_cache_check(lf_cache* cache, lf_stream_t stream, int32_t* bits) {
-  g_last_error.clear();
+  clear_last();
   if (bits) *bits = 0;
   if (!cache) return fail(LF_ERR_ARG, "null cache");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -798,7 +811,7 @@ int lf_cache_check(lf_cache* cache, lf_stream_t stream, int32_t* bits) {
 }
 
 int lf_cache_layout(const lf_cache* cache, lf_layout* out) {
-  g_last_error.clear();
+  clear_last();
   if (!cache || !out) return fail(LF_ERR_ARG, "null cache or layout");
   out->layers = cache->layers;
   out->batch = cache->batch;

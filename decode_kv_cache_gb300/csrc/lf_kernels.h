@@ -6,7 +6,7 @@
 namespace lf {
 
 // Message returned by lf_last_error() on this thread.
-void set_last_error(const std::string& msg);
+void set_last_error(int code, const std::string& msg);  // message and status
 
 enum KernelKind { kSimt = 0, kTensorCore = 1 };
 

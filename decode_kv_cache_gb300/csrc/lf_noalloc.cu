@@ -29,7 +29,7 @@ std::mutex g_setup_mutex;
 int32_t* g_scratch_ptr[kMaxDevices] = {nullptr};
 
 int noalloc_fail(int code, const std::string& msg) {
-  lf::set_last_error(msg);
+  lf::set_last_error(code, msg);
   return code;
 }
 

@@ -25,7 +25,8 @@ __all__ = [
     "LF_SCOPE_KV_HEAD", "LF_SCOPE_LAYER",
     "LFError", "LFConfig", "LFLayout", "load_library", "library_path",
     "lf_cache_create", "lf_cache_create_ex", "lf_cache_destroy", "lf_prefill_fill",
-    "lf_decode_step", "lf_cache_check", "lf_cache_layout", "lf_last_error", "lf_abi_version",
+    "lf_decode_step", "lf_cache_check", "lf_cache_layout", "lf_last_error", "lf_last_status",
+    "lf_abi_version",
     "lf_prefill_fill_noalloc", "lf_rkv_compress",
     "LFCache",
 ]
@@ -113,6 +114,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.lf_last_error.argtypes = []
     lib.lf_abi_version.restype = I
     lib.lf_abi_version.argtypes = []
+    lib.lf_last_status.restype = I
+    lib.lf_last_status.argtypes = []
     lib.lf_rkv_compress.restype = I
     lib.lf_rkv_compress.argtypes = [P, I, VP, VP]
     lib.lf_prefill_fill_noalloc.restype = I
@@ -126,6 +129,15 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
 
 def lf_last_error() -> str:
     return (load_library().lf_last_error() or b"").decode()
+
+
+def lf_last_status() -> int:
+    return load_library().lf_last_status()
+
+
+def _create_failed() -> "LFError":
+    """The error of a create call that returned NULL, with the library's status."""
+    return LFError(lf_last_status() or LF_ERR_ARG, lf_last_error())
 
 
 def lf_abi_version() -> int:
@@ -157,7 +169,7 @@ def _stream(stream) -> Optional[int]:
 def lf_cache_create(layers, batch, kv_heads, q_heads, head_dim, budget, window) -> int:
     h = load_library().lf_cache_create(layers, batch, kv_heads, q_heads, head_dim, budget, window)
     if not h:
-        raise LFError(LF_ERR_ARG, lf_last_error())
+        raise _create_failed()
     return h
 
 
@@ -186,7 +198,7 @@ def lf_cache_create_ex(layers, batch, kv_heads, q_heads, head_dim, capacity, win
     h = load_library().lf_cache_create_ex(layers, batch, kv_heads, q_heads, head_dim, capacity,
                                           window, ctypes.byref(cfg))
     if not h:
-        raise LFError(LF_ERR_ARG, lf_last_error())
+        raise _create_failed()
     return h
 
 

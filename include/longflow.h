@@ -72,7 +72,7 @@
 extern "C" {
 #endif
 
-#define LF_ABI_VERSION 4
+#define LF_ABI_VERSION 5
 
 typedef struct lf_cache lf_cache; /* opaque; owns the slab */
 
@@ -314,6 +314,14 @@ int lf_prefill_fill_noalloc(const lf_layout* dst, int layer, const void* k, cons
 
 /* Message of the last failed call on this thread ("" if none). */
 const char* lf_last_error(void);
+
+/* lf_status of the last failed call on this thread (LF_OK if none).  The way to
+ * learn why lf_cache_create / lf_cache_create_ex returned NULL: LF_ERR_ARG,
+ * LF_ERR_UNSUPPORTED, LF_ERR_OOM (the slab does not fit in device memory) or
+ * LF_ERR_CUDA.  It keeps its value until the next failure, or until one of
+ * lf_cache_create*, lf_cache_destroy, lf_prefill_fill, lf_cache_check and
+ * lf_cache_layout resets it (with the message) on entry. */
+int lf_last_status(void);
 
 /* LF_ABI_VERSION of the loaded library. */
 int lf_abi_version(void);

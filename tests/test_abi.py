@@ -178,3 +178,20 @@ def test_stored_traffic_needs_the_measured_kernel(tmp_path, monkeypatch):
     assert bench.stored_traffic("qwen3-8b-steady", 64) is None
     assert good is None or good > 0
     assert bench.stored_traffic("ragged-serving", 64) is None
+
+
+def test_last_status_tells_why_create_failed(lib):
+    """lf_cache_create* returns NULL on failure; lf_last_status says why."""
+    assert not lib.lf_cache_create(1, 1, 3, 4, 16, 32, 4)        # q_heads % kv_heads != 0
+    assert lf.lf_last_status() == lf.LF_ERR_ARG
+    with pytest.raises(lf.LFError) as e:
+        lf.lf_cache_create(1, 1, 1, 2, 16, 32, 40)               # window >= budget
+    assert e.value.code == lf.LF_ERR_ARG
+    # a call that resets the message resets the status too
+    assert lib.lf_cache_destroy(None) == lf.LF_OK
+    assert lf.lf_last_status() == lf.LF_OK and lf.lf_last_error() == ""
+    import torch
+    if not torch.cuda.is_available():
+        with pytest.raises(lf.LFError) as e:
+            lf.lf_cache_create(1, 1, 1, 2, 16, 32, 4)           # valid, but no device here
+        assert e.value.code == lf.LF_ERR_CUDA
