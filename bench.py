@@ -303,7 +303,7 @@ def bench_reference(args):
 # ---------------------------------------------------------------------------
 
 def build_cache(wl, torch, lf, stream_mod, seed, evict=True, capacity=None, layers=None,
-                cluster=0, stages=0, policy=None):
+                cluster=0, stages=0, policy=None, kernel="auto"):
     L = wl.layers if layers is None else layers
     cap = capacity or wl.budget
     policy = policy or {}
@@ -311,14 +311,15 @@ def build_cache(wl, torch, lf, stream_mod, seed, evict=True, capacity=None, laye
     budgets = gen.budgets if (evict and wl.ragged) else None
     cache = lf.LFCache(L, wl.batch, wl.kv_heads, wl.q_heads, wl.head_dim, cap, wl.window,
                        dtype=wl.dtype, evict=evict, budgets=budgets, cluster=cluster,
-                       stages=stages, **policy)
+                       stages=stages, kernel=kernel, **policy)
     # deferred eviction keeps one slot free in the prompt (the step that fills
     # the buffer chooses the first victim)
     spare = 1 if (evict and policy.get("deferred")) else 0
+    limits = [(budgets[b] if budgets else cap) - spare for b in range(wl.batch)]
     for l in range(L):
-        k, v, lens = gen.prompt(l)
-        # prompt tokens past a sequence's budget would arrive as decode steps
-        lens = [min(P, (budgets[b] if budgets else cap) - spare) for b, P in enumerate(lens)]
+        # prompt tokens past a sequence's budget come out of the stream as its
+        # first decode tokens (the batch advances in lock-step)
+        k, v, lens = gen.prompt_split(l, limits)
         cache.prefill(l, k, v, lens)
         del k, v
     torch.cuda.synchronize()
@@ -364,6 +365,61 @@ def time_steps(cache, inputs, outs, evs, torch, graph: bool):
     end.record(stream)
     end.synchronize()
     return start.elapsed_time(end)
+
+
+def bench_workload(args, torch, lf, stream_mod, peak, name, layers, steady, dist=None):
+    """One more workload timed like the headline: its own cache, W untimed
+    steps, then `args.steps` steps in one CUDA graph, from the start of
+    generation (or at steady state with `steady`).  Returns units/s, the
+    algorithmic GB/s of the decode launches, their fraction of the measured
+    copy peak, the launch shape and the occupancy the steps ran at."""
+    wl = stream_mod.get_workload(name)
+    wl = wl.scaled(layers=min(wl.layers, layers))
+    if steady:
+        wl = wl.scaled(prefill=wl.budget)
+    cache, gen = build_cache(wl, torch, lf, stream_mod, seed=400)
+    L = wl.layers
+    outs = [torch.empty(wl.batch, wl.q_heads, wl.head_dim, dtype=cache.dtype, device="cuda")
+            for _ in range(L)]
+    evs = [torch.empty(wl.batch, wl.kv_heads, dtype=torch.int32, device="cuda") for _ in range(L)]
+    overflow = gen.overflow_lengths(0)
+    warm = pregenerate(gen, args.warmup, torch)
+    timed = pregenerate(gen, args.steps, torch)
+    time_steps(cache, warm, outs, evs, torch, graph=False)
+    del warm
+    occ_start = cache.views()["count"][0, :, 0].cpu().tolist()
+    torch.cuda.synchronize()
+    ms = time_steps(cache, timed, outs, evs, torch, graph=not args.eager)
+    ms = aggregate(ms, 0, dist)[0]
+    bits = cache.check()
+    if bits:
+        raise RuntimeError(f"device error word {bits} in the {name} leg")
+    occ_end = cache.views()["count"][0, :, 0].cpu().tolist()
+    lay = cache.layout
+    launches = L * args.steps
+    bytes_per_launch = sum((unit_bytes(wl, int(a)) + unit_bytes(wl, int(e))) // 2
+                           for a, e in zip(occ_start, occ_end))
+    achieved = bytes_per_launch / (ms / 1000.0 / launches) / 1e9
+    world = dist.get_world_size() if (dist is not None and dist.is_initialized()) else 1
+    cache.close()
+    del cache, gen, timed
+    torch.cuda.empty_cache()
+    return {
+        "workload": name, "layers": L, "batch": wl.batch, "steps": args.steps,
+        "state": ("steady (pre-filled to the budget, every step evicts)" if steady else
+                  f"from the start of generation after step {args.warmup}"),
+        "value": world * wl.batch * L * args.steps / (ms / 1000.0), "unit": UNIT,
+        "ms_per_layer_step": ms / launches,
+        "achieved_gbs": achieved, "frac_of_peak": achieved / peak,
+        "frac_of_nominal_8000": achieved / NOMINAL_HBM_GBS,
+        "bytes_per_launch": bytes_per_launch,
+        "occupied_slots": {"start_mean": sum(occ_start) / len(occ_start),
+                           "end_mean": sum(occ_end) / len(occ_end)},
+        "prompt_remainder_steps": ({"sequences": sum(1 for x in overflow if x > 0),
+                                    "max": max(overflow)} if max(overflow) > 0 else None),
+        "launch_shape": {"cluster": lay.cluster, "stages": lay.stages,
+                         "split_units": lay.split_units},
+    }
 
 
 def bench_rkv(args, torch, lf, stream_mod, peak):
@@ -498,6 +554,8 @@ def bench_ours(args):
     wl = stream_mod.get_workload(args.workload)
     if args.layers:
         wl = wl.scaled(layers=args.layers)
+    if args.batch:
+        wl = wl.scaled(batch=args.batch)
     if args.steady and not wl.ragged:
         wl = wl.scaled(prefill=wl.budget)
     peak, peak_kind = load_peaks()
@@ -512,7 +570,7 @@ def bench_ours(args):
 
     # ---- eviction on, steady state (cache pre-filled to the budget) ----
     cache, gen = build_cache(wl, torch, lf, stream_mod, seed=rank, cluster=args.cluster,
-                             stages=args.stages)
+                             stages=args.stages, kernel=args.kernel)
     L = wl.layers
     outs = [torch.empty(wl.batch, wl.q_heads, wl.head_dim, dtype=cache.dtype, device="cuda")
             for _ in range(L)]
@@ -690,6 +748,15 @@ def bench_ours(args):
             del cp, gp, tin
             torch.cuda.empty_cache()
 
+    # ---- the other two timed workloads: batch 32 at budget 3276 (steady) and
+    # the ragged serving batch (from its prompts, remainders fed as steps) ----
+    others = {}
+    if args.other_workloads and not (args.layers or args.batch):
+        others["r1_llama_steady"] = bench_workload(args, torch, lf, stream_mod, peak,
+                                                   "r1-llama-8b", args.r1_layers, True, dist)
+        others["ragged"] = bench_workload(args, torch, lf, stream_mod, peak, "ragged-serving",
+                                          args.ragged_layers, False, dist)
+
     # ---- R-KV, the pages' baseline, on its own workload (fewer layers) ----
     rkv = None
     if args.rkv and rank == 0:
@@ -728,6 +795,7 @@ def bench_ours(args):
         "full_kv": full,
         "policy_variants": policies,
         "rkv": rkv,
+        **others,
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -741,6 +809,9 @@ def main():
     ap.add_argument("--workload", default="qwen3-8b-steady")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--layers", type=int, default=0, help="override the layer count")
+    ap.add_argument("--batch", type=int, default=0, help="override the batch (sequences)")
+    ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "tc"],
+                    help="decode kernel of the timed workload (auto: tensor cores where built)")
     ap.add_argument("--steady", action="store_true",
                     help="start with the cache filled to the budget (every step evicts) "
                          "instead of from the workload's prompt")
@@ -758,6 +829,10 @@ def main():
     ap.add_argument("--no-rkv", dest="rkv", action="store_false", default=True,
                     help="skip the R-KV baseline leg")
     ap.add_argument("--rkv-layers", type=int, default=4)
+    ap.add_argument("--no-other-workloads", dest="other_workloads", action="store_false",
+                    default=True, help="skip the r1-llama-8b steady and ragged legs")
+    ap.add_argument("--r1-layers", type=int, default=32)
+    ap.add_argument("--ragged-layers", type=int, default=8)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args()
     if args.warmup < 3:

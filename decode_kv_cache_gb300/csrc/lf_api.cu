@@ -160,6 +160,8 @@ void lf::set_last_error(int code, const std::string& msg) {
   g_last_status = code;
 }
 
+void lf::clear_last_error() { clear_last(); }
+
 extern "C" {
 
 const char* lf_last_error(void) { return g_last_error.c_str(); }

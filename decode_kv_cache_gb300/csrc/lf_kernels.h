@@ -7,6 +7,8 @@ namespace lf {
 
 // Message returned by lf_last_error() on this thread.
 void set_last_error(int code, const std::string& msg);  // message and status
+// A call starts with no recorded failure (status LF_OK, empty message).
+void clear_last_error();
 
 enum KernelKind { kSimt = 0, kTensorCore = 1 };
 

@@ -9,6 +9,7 @@
 // keeps the last call's contents (the call overwrites the first `batch`
 // entries before the kernel reads them); calls whose kernels overlap on the
 // GPU race on it.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -26,22 +27,61 @@ constexpr int kMaxDevices = 64;
 __device__ __align__(256) int32_t g_prompt_len_scratch[LF_NOALLOC_MAX_BATCH];
 
 std::mutex g_setup_mutex;
+// Per device: the array's address and the id of the CUDA context it was
+// looked up in.  A cudaDeviceReset in the process ends that context (the next
+// runtime call makes a new one, where the array may sit elsewhere), so the
+// address is looked up again whenever the current context's id differs.
 int32_t* g_scratch_ptr[kMaxDevices] = {nullptr};
+unsigned long long g_scratch_ctx[kMaxDevices] = {0};
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
 
 int noalloc_fail(int code, const std::string& msg) {
   lf::set_last_error(code, msg);
   return code;
 }
 
-// Device address of the scratch array on the current device (set up once per
-// device, with that device current).
+// Id of the current CUDA context (unique over the process's lifetime), or 0
+// if the driver does not tell.
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static bool looked_up = false;
+  if (!looked_up) {  // called with g_setup_mutex held
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(fn);
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(fn);
+    (void)cudaGetLastError();
+    looked_up = true;
+  }
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx ||
+      get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// Device address of the scratch array on the current device: looked up once
+// per device (and again after the device's context was replaced), with that
+// device current.
 int scratch_address(int32_t** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return noalloc_fail(LF_ERR_CUDA, cudaGetErrorString(e));
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return noalloc_fail(LF_ERR_CUDA, cudaGetErrorString(e));
+  }
   if (dev < 0 || dev >= kMaxDevices) return noalloc_fail(LF_ERR_ARG, "device index too large");
   std::lock_guard<std::mutex> lock(g_setup_mutex);
-  if (!g_scratch_ptr[dev]) {
+  if (!g_scratch_ptr[dev] || current_context_id() != g_scratch_ctx[dev]) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_prompt_len_scratch);
     if (e != cudaSuccess || !p) {
@@ -49,6 +89,9 @@ int scratch_address(int32_t** out) {
       return noalloc_fail(LF_ERR_CUDA, std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e));
     }
     g_scratch_ptr[dev] = static_cast<int32_t*>(p);
+    // read after the lookup, which makes the device's context current if the
+    // runtime had not yet
+    g_scratch_ctx[dev] = current_context_id();
   }
   *out = g_scratch_ptr[dev];
   return LF_OK;
@@ -61,6 +104,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 extern "C" int lf_prefill_fill_noalloc(const lf_layout* dst, int layer, const void* k,
                                        const void* v, const int32_t* prompt_len, int max_prompt,
                                        lf_stream_t stream) {
+  lf::clear_last_error();
   if (!dst) return noalloc_fail(LF_ERR_ARG, "null destination layout");
   if (!dst->k || !dst->v || !dst->vnorm || !dst->pos || !dst->count || !dst->next_pos)
     return noalloc_fail(LF_ERR_ARG, "destination layout has a null pointer");
@@ -75,12 +119,17 @@ extern "C" int lf_prefill_fill_noalloc(const lf_layout* dst, int layer, const vo
                                         " exceeds LF_NOALLOC_MAX_BATCH (" +
                                         std::to_string(LF_NOALLOC_MAX_BATCH) + ")");
   if (!prompt_len || max_prompt < 0) return noalloc_fail(LF_ERR_ARG, "bad prompt lengths");
+  // Deferred mode (a pending array): the step that fills the buffer chooses
+  // the first victim, so a prompt leaves at least one slot free.
+  const int limit = dst->pending ? dst->capacity - 1 : dst->capacity;
   int longest = 0;
   for (int b = 0; b < dst->batch; ++b) {
     const int P = prompt_len[b];
-    if (P < 0 || P > max_prompt || P > dst->capacity)
+    if (P < 0 || P > max_prompt || P > limit)
       return noalloc_fail(LF_ERR_ARG, "prompt_len[" + std::to_string(b) + "] = " +
-                                          std::to_string(P) + " outside [0, min(max_prompt, capacity)]");
+                                          std::to_string(P) + " outside [0, min(max_prompt, " +
+                                          (dst->pending ? "capacity - 1 (deferred mode))]"
+                                                        : "capacity)]"));
     if (P > longest) longest = P;
   }
   if (longest > 0 && (!k || !v || !aligned16(k) || !aligned16(v)))

@@ -295,7 +295,12 @@ int lf_cache_layout(const lf_cache* cache, lf_layout* out);
  * NULL; the other fields are ignored), laid out exactly as lf_cache_layout
  * documents.  The operation, argument meaning
  * and error behaviour are those of lf_prefill_fill, except that prompt
- * lengths are checked against `capacity` (the caller keeps its budgets).
+ * lengths are checked against `capacity` (the caller keeps its budgets):
+ * prompt_len[b] <= capacity, and <= capacity - 1 when `pending` is not NULL
+ * (deferred mode).  A caller whose budgets are below the capacity keeps
+ * prompt_len[b] <= budget, and <= budget - 1 in deferred mode, itself: a
+ * deferred buffer filled to its budget by the prompt reaches its next step
+ * without a chosen slot, and that step raises LF_DEVERR_STATE.
  *
  * The prompt lengths travel to the GPU through a fixed array compiled into
  * the library (LF_NOALLOC_MAX_BATCH int32 entries, held by every GPU that
@@ -305,8 +310,11 @@ int lf_cache_layout(const lf_cache* cache, lf_layout* out);
  * so calls whose work overlaps on the GPU (different streams, no ordering)
  * race on it.  The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture.  Nothing is allocated: no cudaMalloc, no
- * cudaFree, no allocating library routine.
+ * before any stream capture.  The address is looked up again after the
+ * device's CUDA context was replaced (a cudaDeviceReset in the process): the
+ * first call after the reset, too, should come before any stream capture.
+ * Nothing is allocated: no cudaMalloc, no cudaFree, no allocating library
+ * routine.
  */
 #define LF_NOALLOC_MAX_BATCH 16384
 int lf_prefill_fill_noalloc(const lf_layout* dst, int layer, const void* k, const void* v,
@@ -319,8 +327,8 @@ const char* lf_last_error(void);
  * learn why lf_cache_create / lf_cache_create_ex returned NULL: LF_ERR_ARG,
  * LF_ERR_UNSUPPORTED, LF_ERR_OOM (the slab does not fit in device memory) or
  * LF_ERR_CUDA.  It keeps its value until the next failure, or until one of
- * lf_cache_create*, lf_cache_destroy, lf_prefill_fill, lf_cache_check and
- * lf_cache_layout resets it (with the message) on entry. */
+ * lf_cache_create*, lf_cache_destroy, lf_prefill_fill, lf_prefill_fill_noalloc,
+ * lf_cache_check and lf_cache_layout resets it (with the message) on entry. */
 int lf_last_status(void);
 
 /* LF_ABI_VERSION of the loaded library. */

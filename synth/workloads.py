@@ -197,6 +197,9 @@ class InputStream:
                 u = torch.randn(wl.kv_heads, d, generator=gu, device=self.device)
                 self._sink_u[l] = u / u.norm(dim=-1, keepdim=True)
         self.t = 0  # decode steps drawn so far
+        # Prompt tokens past a sequence's buffer limit, fed as its next decode
+        # tokens (see prompt_split): layer -> (k [b][H_kv][n][d], v, lengths [b]).
+        self._overflow = {}
 
     # -- token K/V recipe shared by prompt and decode tokens -----------------
     def _tokens(self, g: torch.Generator, layer: int, n: int):
@@ -234,6 +237,42 @@ class InputStream:
         k, v = self._tokens(g, layer, pmax)
         return k.to(self.dtype).contiguous(), v.to(self.dtype).contiguous(), list(self.prompt_lens)
 
+    def prompt_split(self, layer: int, limits: Sequence[int]):
+        """Prompt of one layer cut at each sequence's buffer limit.
+
+        Returns (k, v, lens) like ``prompt`` with lens[b] = min(P_b, limits[b]):
+        the part that prefills the buffer.  The rest of a longer prompt,
+        positions limits[b] .. P_b - 1, is kept and comes out of ``next_step``
+        as that sequence's k_new / v_new for its first P_b - limits[b] decode
+        steps, each with the query the stream draws for that step.  The batch
+        advances in lock-step: sequences without such a remainder take drawn
+        tokens from the first step on.  Every step draws the same random
+        numbers either way, so the other sequences' streams are unchanged.
+        """
+        k, v, lens = self.prompt(layer)
+        cut = [min(P, int(lim)) for P, lim in zip(lens, limits)]
+        extra = [P - c for P, c in zip(lens, cut)]
+        if max(extra) > 0:
+            n = max(extra)
+            ok = torch.zeros(k.shape[0], k.shape[1], n, k.shape[3], dtype=k.dtype,
+                             device=k.device)
+            ov = torch.zeros_like(ok)
+            for b, (c, e) in enumerate(zip(cut, extra)):
+                if e > 0:
+                    ok[b, :, :e] = k[b, :, c:c + e]
+                    ov[b, :, :e] = v[b, :, c:c + e]
+            self._overflow[layer] = (ok, ov, torch.tensor(extra, device=self.device))
+        else:
+            self._overflow.pop(layer, None)
+        return k, v, cut
+
+    def overflow_lengths(self, layer: int) -> List[int]:
+        """Prompt tokens of each sequence still to be fed as decode tokens
+        (counted from the start of decoding)."""
+        if layer not in self._overflow:
+            return [0] * self.wl.batch
+        return self._overflow[layer][2].tolist()
+
     def next_step(self):
         """Advance one decode step for every drawn layer.
 
@@ -251,7 +290,16 @@ class InputStream:
             else:
                 self._q[l] = self._rho_t * self._q[l] + self._sig_t * eps
             k, v = self._tokens(g, l, 1)
+            k = k[:, :, 0].to(self.dtype)
+            v = v[:, :, 0].to(self.dtype)
+            if l in self._overflow:
+                ok, ov, extra = self._overflow[l]
+                i = self.t - 1
+                if i < ok.shape[2]:   # prompt tokens past the buffer come first
+                    use = (extra > i).view(-1, 1, 1)
+                    k = torch.where(use, ok[:, :, i], k)
+                    v = torch.where(use, ov[:, :, i], v)
             qs.append(self._q[l].to(self.dtype).contiguous())
-            ks.append(k[:, :, 0].to(self.dtype).contiguous())
-            vs.append(v[:, :, 0].to(self.dtype).contiguous())
+            ks.append(k.contiguous())
+            vs.append(v.contiguous())
         return qs, ks, vs

@@ -12,12 +12,20 @@ Comparison rules:
   counted and resynchronised: the oracle's state of that unit (K, V, ||v||_1,
   positions) is written over the GPU's through the slab layout, so both
   continue from the oracle's state;
+* an exact tie -- the oracle's two lowest candidate scores equal in fp64,
+  which takes identical stored values -- has one right answer, the lowest
+  tied slot (the tie rule), so there the slot must be bit-exact too: a
+  different pick is a mismatch, never a resync;
 * outputs: fp32 storage -- |x - y| <= 1e-5 * max(|y|, max |y| of that head);
   bf16 storage -- |x - y| <= 2e-2 + 1e-2 |y| (fp32 accumulation on the GPU);
 * after the run, every sampled unit's slab state equals the oracle's: K, V and
   positions exactly, ||v||_1 to fp32 rounding, count and next position; with
   the H2O score the accumulators to fp32 accumulation (rtol 1e-4), and when
   deferred the chosen slot exactly.
+
+Long prompts: a sequence's prompt tokens past its buffer are fed as its first
+decode tokens, each with the query the stream draws for that step
+(``InputStream.prompt_split``); the oracle receives the same tokens.
 
 Policy variants: with the deferred order the slot chosen at a step is compared
 through the cache's `pending` state (near-tie rule as above) and the slot the
@@ -58,6 +66,7 @@ class ParityStats:
     unit_steps: int = 0
     evictions: int = 0
     near_ties: int = 0
+    exact_ties: int = 0
     resyncs: int = 0
     hard_mismatches: List[Tuple] = field(default_factory=list)
     max_out_violation: float = 0.0
@@ -116,9 +125,10 @@ class ParityRun:
                 return cap
             return self.budgets[b] - (1 if self.deferred else 0)
 
+        self.overflow = []   # per layer: prompt tokens each sequence feeds as decode tokens
         for li, l in enumerate(self.layers):
-            k, v, lens = self.stream.prompt(l)
-            lens = [min(P, limit(b)) for b, P in enumerate(lens)]
+            k, v, lens = self.stream.prompt_split(l, [limit(b) for b in range(wl.batch)])
+            self.overflow.append(self.stream.overflow_lengths(l))
             self.cache.prefill(li, k, v, lens)
             for (sli, b, g) in self.sample:
                 if sli != li:
@@ -167,8 +177,37 @@ class ParityRun:
         ps = pos_before[slot]
         return bool(pol.sinks <= ps < p - W)
 
-    def step(self, check: bool = True):
+    def plant_tie(self, li: int, slots: Sequence[int], src: Optional[int] = None,
+                  scale: float = 0.05):
+        """Make `slots` of every unit of layer index `li` hold the same stored
+        key and value: slot `src`'s (default: the first of `slots`), with the
+        value scaled by `scale` so that a small ||v|| puts them at the bottom
+        of the LongFlow score.  The GPU slab and the oracle units get the same
+        bytes; each slot keeps its position."""
+        vw = self.views
+        src = slots[0] if src is None else src
+        sl = torch.tensor(list(slots), device=vw["k"].device)
+        krow = vw["k"][li, :, :, src].clone()
+        vrow = (vw["v"][li, :, :, src].float() * scale).to(self.cache.dtype)
+        norm = vrow.float().abs().sum(-1) if self.policy.norm == 1 else vrow.float().norm(dim=-1)
+        n_s = len(slots)
+        vw["k"][li][:, :, sl] = krow.unsqueeze(2).expand(-1, -1, n_s, -1)
+        vw["v"][li][:, :, sl] = vrow.unsqueeze(2).expand(-1, -1, n_s, -1)
+        vw["vnorm"][li][:, :, sl] = norm.unsqueeze(2).expand(-1, -1, n_s)
+        torch.cuda.synchronize()
+        for (sli, b, g), u in self.units.items():
+            if sli != li:
+                continue
+            kk, vv = to64(krow[b, g]), to64(vrow[b, g])
+            for s in slots:
+                u.K[s] = kk
+                u.V[s] = vv
+                u.vnorm[s] = oracle.value_norm(vv, self.policy.norm)
+
+    def step(self, check: bool = True, zero_query: bool = False):
         qs, ks, vs = self.stream.next_step()
+        if zero_query:   # every weight uniform: the score is ||v|| (or the H2O mass) alone
+            qs = [torch.zeros_like(q) for q in qs]
         for li in range(len(self.layers)):
             self.cache.decode_step(li, qs[li], ks[li], vs[li], self.out[li], self.ev[li])
         self.stats.steps += 1
@@ -213,11 +252,20 @@ class ParityRun:
                     if int(ev[j]) != r.evicted:
                         self.stats.hard_mismatches.append(
                             (self.stats.steps,) + m + (int(ev[j]), r.evicted, "overwritten"))
-            near = (r0.rel_gap <= NEAR_TIE) or (r0.chosen >= 0 and r0.second < TINY_SCORE)
+            exact = (r0.chosen >= 0 and r0.lowest == r0.second and r0.lowest >= TINY_SCORE)
+            near = not exact and ((r0.rel_gap <= NEAR_TIE) or
+                                  (r0.chosen >= 0 and r0.second < TINY_SCORE))
+            if exact:
+                self.stats.exact_ties += 1
             if near:
                 self.stats.near_ties += 1
             if any(c != r0.chosen for c in gpu_chosen):
                 e_gpu = gpu_chosen[0]
+                if exact:   # one right answer: the lowest tied slot
+                    self.stats.hard_mismatches.append(
+                        (self.stats.steps,) + members[0] + (e_gpu, r0.chosen, "exact tie"))
+                    self._resync(members)
+                    continue
                 ok_pick = (near and r0.scores is not None and all(c == e_gpu for c in gpu_chosen)
                            and 0 <= e_gpu < len(r0.scores)
                            and self._candidate(units[0], pos_before[0], e_gpu)
@@ -229,9 +277,9 @@ class ParityRun:
                         (self.stats.steps,) + members[0] + (e_gpu, r0.chosen, r0.rel_gap))
                 self._resync(members)
 
-    def run(self, steps: int, check_every: int = 1) -> ParityStats:
+    def run(self, steps: int, zero_query: bool = False) -> ParityStats:
         for t in range(steps):
-            self.step(check=True)
+            self.step(check=True, zero_query=zero_query)
         torch.cuda.synchronize()
         return self.stats
 

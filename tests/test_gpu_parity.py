@@ -102,18 +102,43 @@ def test_full_kv_read_only():
 
 
 def test_ragged_serving_shape():
-    """Mixed budgets and prompts at full batch; 1100 steps cross the first
-    abrupt query reset (every 1000 steps) and the prompt overflow of the
-    sequences whose prompt exceeds their budget."""
+    """Mixed budgets and prompts at full batch, 1100 steps.  A sequence whose
+    prompt is longer than its budget prefills the budget and feeds the rest of
+    its prompt as decode steps, each with the query drawn for that step, while
+    the batch advances in lock-step.  The sampled sequences include, per budget
+    value, the first one drawn, and sequences whose prompt remainder ends after
+    30, 109 and 996 steps or outlasts the run, so the run crosses the end of
+    the prompt remainder and the first abrupt query reset (every 1000 steps)."""
     wl = WORKLOADS["ragged-serving"]
-    budgets = InputStream(wl, seed=0, device="cpu", layers=[0]).budgets  # same seeded draw
-    # one sampled sequence per budget value
+    ins = InputStream(wl, seed=0, device="cpu", layers=[0])  # the same seeded draw
+    budgets, prompts = ins.budgets, ins.prompt_lens
     picks = []
-    for B in sorted(set(budgets)):
-        b = budgets.index(B)
+    seqs = [budgets.index(B) for B in sorted(set(budgets))]
+    extra = {b: P - B for b, (P, B) in enumerate(zip(prompts, budgets)) if P > B}
+    remainders = sorted(extra.values())
+    for want in (30, 109, 996):   # a remainder of about this length
+        seqs.append(min(extra, key=lambda b: abs(extra[b] - want)))
+    seqs.append(max(extra, key=extra.get))
+    for b in dict.fromkeys(seqs):
         picks += [(0, b, 0), (0, b, 7)]
-    st = _run(wl, 1100, layers=(0,), sample=picks)
-    assert st.unit_steps == 1100 * len(picks)
+    run = ParityRun(wl, layers=(0,), sample=picks)
+    try:
+        fed = run.overflow[0]
+        assert sum(0 < fed[b] < 1100 for b in seqs) >= 3 and max(fed) > 1100
+        assert fed == [max(0, P - B) for P, B in zip(prompts, budgets)]
+        assert remainders and min(remainders) > 0
+        run.run(1100)
+        run.compare_state()
+        run.check_invariants()
+        st = run.stats
+        print(f"\nparity ragged: {st.unit_steps} unit-steps, {st.evictions} evictions, "
+              f"{st.near_ties} near-ties, {st.resyncs} resyncs, "
+              f"{len(st.hard_mismatches)} mismatches, max output error "
+              f"{st.max_out_violation:.3f} of tolerance")
+        st.assert_ok()
+        assert st.unit_steps == 1100 * len(picks)
+    finally:
+        run.close()
 
 
 @pytest.mark.parametrize("case", [

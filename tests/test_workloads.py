@@ -84,3 +84,32 @@ def test_ragged_draws_and_query_resets():
         prev = q
     assert corr[999] > 0.6 and corr[1001] > 0.6      # AR(1) with rho in [0.6, 0.98]
     assert abs(corr[1000]) < 0.05                     # step 1000 draws a fresh query
+
+
+def test_prompt_remainder_fed_as_decode_tokens():
+    """A prompt longer than its sequence's buffer: the buffer takes its first
+    tokens, the rest come out as that sequence's next decode tokens in prompt
+    order (one per step, with the step's own query), then drawn tokens
+    follow; other sequences and the queries see the same draws as without
+    the cut."""
+    wl = WORKLOADS["ragged-serving"].scaled(batch=6, layers=1, prompt_range=(40, 90))
+    a = InputStream(wl, seed=5, layers=[0])
+    b = InputStream(wl, seed=5, layers=[0])
+    limits = [50, 100, 60, 10, 100, 45]
+    k, v, cut = a.prompt_split(0, limits)
+    kb, vb, lens = b.prompt(0)
+    assert torch.equal(k, kb) and lens == a.prompt_lens
+    assert cut == [min(P, m) for P, m in zip(lens, limits)]
+    extra = [P - c for P, c in zip(lens, cut)]
+    assert a.overflow_lengths(0) == extra and max(extra) > 0 and min(extra) == 0
+    for t in range(max(extra) + 2):
+        qa, ka, va = a.next_step()
+        qb, kb_t, vb_t = b.next_step()
+        assert torch.equal(qa[0], qb[0])
+        for s in range(wl.batch):
+            if t < extra[s]:   # the prompt's token at position cut + t
+                assert torch.equal(ka[0][s], k[s, :, cut[s] + t])
+                assert torch.equal(va[0][s], v[s, :, cut[s] + t])
+            else:              # a drawn token, the same as without the cut
+                assert torch.equal(ka[0][s], kb_t[0][s])
+                assert torch.equal(va[0][s], vb_t[0][s])
