@@ -388,6 +388,7 @@ def bench_workload(args, torch, lf, stream_mod, peak, name, layers, steady, dist
     time_steps(cache, warm, outs, evs, torch, graph=False)
     del warm
     occ_start = cache.views()["count"][0, :, 0].cpu().tolist()
+    planned = cache.plan(0) is not None
     torch.cuda.synchronize()
     ms = time_steps(cache, timed, outs, evs, torch, graph=not args.eager)
     ms = aggregate(ms, 0, dist)[0]
@@ -418,7 +419,7 @@ def bench_workload(args, torch, lf, stream_mod, peak, name, layers, steady, dist
         "prompt_remainder_steps": ({"sequences": sum(1 for x in overflow if x > 0),
                                     "max": max(overflow)} if max(overflow) > 0 else None),
         "launch_shape": {"cluster": lay.cluster, "stages": lay.stages,
-                         "split_units": lay.split_units},
+                         "planned_at_start": planned},
     }
 
 
@@ -475,7 +476,7 @@ def bench_rkv(args, torch, lf, stream_mod, peak):
         raise RuntimeError(f"device error word {bits} in the R-KV cycle")
     counts = cache.views()["count"].cpu()
     rlay = cache.layout
-    rkv_shape = {"cluster": rlay.cluster, "stages": rlay.stages, "split_units": rlay.split_units}
+    rkv_shape = {"cluster": rlay.cluster, "stages": rlay.stages}
     cache.close()
     del cache, gen, steps, qobs
     torch.cuda.empty_cache()
@@ -485,7 +486,8 @@ def bench_rkv(args, torch, lf, stream_mod, peak):
     lwl = wl.scaled(window=stream_mod.get_workload("r1-llama-8b").window, prefill=B)
     lcache, lgen = build_cache(lwl, torch, lf, stream_mod, seed=301)
     llay = lcache.layout
-    lf_shape = {"cluster": llay.cluster, "stages": llay.stages, "split_units": llay.split_units}
+    lf_shape = {"cluster": llay.cluster, "stages": llay.stages,
+                "planned_at_start": lcache.plan(0) is not None}
     lwarm = pregenerate(lgen, 3, torch)
     time_steps(lcache, lwarm, outs, evs, torch, graph=False)
     del lwarm
@@ -582,6 +584,7 @@ def bench_ours(args):
     if cache.check() != 0:
         raise RuntimeError("device error during warm-up")
     occ_start = cache.views()["count"][0, :, 0].cpu().tolist()  # occupied slots per sequence
+    planned = cache.plan(0) is not None
     clocks = ClockSampler(local)
     barrier()
     clocks.start()
@@ -783,7 +786,7 @@ def bench_ours(args):
                      "frac_of_nominal_8000": achieved / NOMINAL_HBM_GBS,
                      "traffic": stored_traffic(wl.name, wl.batch),
                      "kernel": (f"decode_step_tc_kernel<{wl.group}, "
-                                f"{'true' if lay.split_units else 'false'}>" if lay.kernel == 2 else
+                                f"{'true' if planned else 'false'}>" if lay.kernel == 2 else
                                 f"decode_step_simt_kernel<{wl.dtype},{wl.head_dim},{wl.group}>"),
                      "bytes_per_launch": bytes_per_launch,
                      "timing": "timed region / launches (includes launch gaps)"},

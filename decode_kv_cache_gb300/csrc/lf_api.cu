@@ -46,13 +46,15 @@ struct lf_cache {
   lf::KernelEntry kern;
   int threads;    // CTA size of the decode kernel
   int grid_y;     // tensor-core path: resident clusters (persistent grid)
-  int split_rem;  // tensor-core path: last-round units shared by two clusters (0: none)
-  // Per layer, a lower bound on every sequence's occupied slots (the shortest
-  // prompt plus the decode steps since, capped at fill_cap), which decides
-  // whether a step takes the split kernel; host state, ordered like the calls.
-  std::vector<long long> fill;
-  long long fill_cap;
-  float* split_stat;  // ... their exchanges through global memory (see TcArgs)
+  int plan_ok;    // tensor-core path: planned launches allowed (policy and kernel)
+  // Per layer and sequence, the host's count of occupied slots (the prompt plus
+  // the decode steps since, capped at the sequence's limit; cut back by an R-KV
+  // compression).  It only steers the launch plan: host state, ordered like the
+  // calls; a wrong count costs balance, never correctness.
+  std::vector<int32_t> occ;  // [layers][batch]
+  std::vector<int32_t> occ_limit;  // [batch]: budget (LongFlow) or capacity (append modes)
+  std::vector<int32_t> plan_n;     // scratch: one layer's counts per unit
+  float* split_stat;  // planned launches' exchanges through global memory (see TcArgs)
   float* split_fin;
   int32_t* split_cnt;
   CUtensorMap tmaps[4];  // tensor-core path: K and V as 2-D [rows][head_dim], two box heights
@@ -69,8 +71,104 @@ void clear_last() {
   g_last_status = LF_OK;
 }
 
-// Split launches only once every sequence of the layer holds this many tokens.
-constexpr long long kSplitMinSlots = 2048;
+// Planned launches only once every sequence of the layer holds this many tokens
+// (below it the exchanges through L2 cost more than the balance gains: measured
+// at batch 32 on 2-CTA clusters, two-part shared units were 4-9% slower from
+// 1408 slots down to 640, even at 1664, 7-9% faster from 2048 up).
+#ifndef LF_PLAN_MIN_SLOTS
+#define LF_PLAN_MIN_SLOTS 2048
+#endif
+constexpr int kPlanMinSlots = LF_PLAN_MIN_SLOTS;
+
+// Host cost model of one launch, in CTA slot rows (one row of K and V streamed
+// by one CTA, ~11.5 ns at the HBM rate): every item a CTA visits adds a unit
+// boundary, and every part of a shared unit adds its two exchanges through L2.
+#ifndef LF_PLAN_ITEM_COST
+#define LF_PLAN_ITEM_COST 64
+#endif
+#ifndef LF_PLAN_PART_COST
+#define LF_PLAN_PART_COST 192
+#endif
+constexpr long long kItemCost = LF_PLAN_ITEM_COST;
+constexpr long long kPartCost = LF_PLAN_PART_COST;
+
+// Cut one layer's (unit, slot) order into nc contiguous ranges of about equal
+// cost (n[u] = the unit's occupied slots, c = CTAs per cluster), at multiples
+// of `gran` slots inside a unit; parts shorter than `snap` go whole to one side.
+// Fills cut_unit / cut_slot [nc + 1].  Returns the largest range's cost, or -1
+// if some cluster would visit more than max_items items or a unit would be
+// shared by more than lf::kMaxSplitParts CTAs.
+long long make_plan(const std::vector<int32_t>& n, int c, int nc, int max_items, int* cut_unit,
+                    int* cut_slot) {
+  const int units = (int)n.size();
+  const long long gran = (long long)lf::kTcTile * c, snap = 2 * gran;
+  const long long ov = kItemCost * c;  // a unit boundary, in slots of the cluster
+  long long total = 0;
+  for (int u = 0; u < units; ++u) total += n[u] + ov;
+  cut_unit[0] = 0;
+  cut_slot[0] = 0;
+  cut_unit[nc] = units;
+  cut_slot[nc] = 0;
+  int u = 0;
+  long long before = 0;  // cost of units [0, u)
+  for (int j = 1; j < nc; ++j) {
+    const long long t = total * j / nc;
+    while (u < units && before + n[u] + ov <= t) before += n[u++] + ov;
+    int cu = u, cs = 0;
+    if (u < units) {
+      const long long off = ((t - before - ov) / gran) * gran;
+      if (off >= snap && n[u] - off >= snap) cs = (int)off;
+      else if (off >= snap) cu = u + 1;  // the unit's tail is short: it stays whole on the left
+    }
+    // cuts never go backwards
+    if (cu < cut_unit[j - 1] || (cu == cut_unit[j - 1] && cs < cut_slot[j - 1])) {
+      cu = cut_unit[j - 1];
+      cs = cut_slot[j - 1];
+    }
+    cut_unit[j] = cu;
+    cut_slot[j] = cs;
+  }
+  // Cost of every range, as the kernel will visit it.
+  long long worst = 0;
+  for (int j = 0; j < nc; ++j) {
+    const int u0 = cut_unit[j], s0 = cut_slot[j], u1 = cut_unit[j + 1], s1 = cut_slot[j + 1];
+    long long cost = 0;
+    int items = 0;
+    auto parts_of = [&](int uu) {  // clusters sharing unit uu: 1 + its inner cuts
+      int k = 1;
+      for (int q = 1; q < nc; ++q) k += (cut_unit[q] == uu && cut_slot[q] > 0) ? 1 : 0;
+      return k;
+    };
+    if (s0 > 0) {
+      const long long hi = (u1 == u0) ? s1 : n[u0];
+      cost += (std::max(0LL, hi - s0) + c - 1) / c + kItemCost + kPartCost;
+      ++items;
+      if (parts_of(u0) * c > lf::kMaxSplitParts) return -1;
+    }
+    if (s1 > 0 && !(s0 > 0 && u1 == u0)) {
+      cost += ((long long)std::min(s1, n[u1]) + c - 1) / c + kItemCost + kPartCost;
+      ++items;
+      if (parts_of(u1) * c > lf::kMaxSplitParts) return -1;
+    }
+    const int w0 = (s0 > 0) ? u0 + 1 : u0;
+    for (int w = w0; w < u1; ++w) cost += (n[w] + c - 1) / c + kItemCost;
+    items += std::max(0, u1 - w0);
+    if (items > max_items) return -1;
+    worst = std::max(worst, cost);
+  }
+  return worst;
+}
+
+// Cost of the whole-unit launch: cluster j visits units j, j + nc, ...
+long long round_robin_cost(const std::vector<int32_t>& n, int c, int nc) {
+  long long worst = 0;
+  for (int j = 0; j < nc; ++j) {
+    long long cost = 0;
+    for (int u = j; u < (int)n.size(); u += nc) cost += (n[u] + c - 1) / c + kItemCost;
+    worst = std::max(worst, cost);
+  }
+  return worst;
+}
 
 int fail(int code, const char* fmt, ...) {
   char buf[512];
@@ -144,6 +242,23 @@ int encode_tensor_maps(lf_cache* c, size_t n_rows) {
     if (r != CUDA_SUCCESS) return fail(LF_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
   }
   return LF_OK;
+}
+
+// The plan of the next decode step of `layer`: true, with cut_unit / cut_slot
+// [grid_y + 1] filled, when its ranges cost less than whole units (cost model
+// above) and every sequence is long enough for the exchanges to pay.
+bool plan_layer(lf_cache* c, int layer, int* cut_unit, int* cut_slot) {
+  if (!c->plan_ok) return false;
+  const int32_t* occ = c->occ.data() + (size_t)layer * c->batch;
+  int shortest = INT_MAX;
+  for (int b = 0; b < c->batch; ++b) {
+    shortest = std::min(shortest, occ[b]);
+    for (int g = 0; g < c->kv_heads; ++g) c->plan_n[(size_t)b * c->kv_heads + g] = occ[b];
+  }
+  if (shortest < kPlanMinSlots) return false;
+  const long long rr = round_robin_cost(c->plan_n, c->cluster, c->grid_y);
+  const long long pc = make_plan(c->plan_n, c->cluster, c->grid_y, c->items, cut_unit, cut_slot);
+  return pc >= 0 && pc < rr;
 }
 
 void destroy_memory(lf_cache* c) {
@@ -343,8 +458,9 @@ lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, i
       // The persistent grid visits ceil(units / resident clusters) units per
       // cluster; its item table is sized for that.  Start from the most
       // clusters the SMs could hold and grow the table if fewer are resident.
+      // (+ 2: a planned launch adds the parts of up to two shared units)
       const int most = std::max(1, num_sms / cl);
-      items = (units + most - 1) / most;
+      items = (units + most - 1) / most + 2;
       for (int pass = 0; pass < 4; ++pass) {
         smem = kern.smem_bytes(stages, chunk, cl, kevict, items);
         // The tensor-core kernel takes all of an SM's tensor memory: ask for more
@@ -353,7 +469,7 @@ lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, i
         fits = (smem <= max_optin) ? active_clusters(kern.decode, cl, 1, 1, smem, threads) : 0;
         if (fits <= 0) break;
         grid_y = std::min(fits, units);
-        const int need = (units + grid_y - 1) / grid_y;
+        const int need = (units + grid_y - 1) / grid_y + 2;
         if (need <= items) break;
         items = need;
         fits = 0;
@@ -442,19 +558,20 @@ lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, i
   cache->threads = threads;
   cache->grid_y = grid_y;
   cache->items = items;
-  cache->fill.assign((size_t)layers, 0);
-  cache->fill_cap = kevict ? min_budget : capacity;   // append modes fill the slab
-  // Split launches: when the units left over after the whole rounds fill at
-  // most half of the clusters, each of them is shared by two clusters, as the
-  // first item of both (the part-filled round then takes about half as long).  Only for the per-KV-head
-  // LongFlow score without the deferred order, and for the append modes.
+  cache->occ.assign((size_t)layers * batch, 0);
+  cache->occ_limit.resize((size_t)batch);
+  for (int b = 0; b < batch; ++b)  // append modes fill the slab to its capacity
+    cache->occ_limit[b] = (kevict && c.budgets) ? c.budgets[b] : capacity;
+  cache->plan_n.assign((size_t)units, 0);
+  // Planned launches: the layer's slots cut into equal contiguous ranges, one
+  // per cluster, when that balances better than whole units (decided per step
+  // on the host).  Only for the per-KV-head LongFlow score without the deferred
+  // order, and for the append modes.
   if (tc) {
-    const int rem = units % grid_y;
     const bool plain = !kevict || (c.score == LF_SCORE_LONGFLOW && c.scope == LF_SCOPE_KV_HEAD &&
                                    !c.deferred);
-    if (rem > 0 && 2 * rem <= grid_y && 2 * cluster <= lf::kMaxSplitParts && plain &&
-        kern.decode_split && cache->fill_cap >= kSplitMinSlots)
-      cache->split_rem = rem;
+    if (plain && kern.decode_split && grid_y <= lf::kTcMaxPlan && 2 * cluster <= lf::kMaxSplitParts)
+      cache->plan_ok = 1;
   }
   cache->score = c.score;
   cache->norm = c.norm;
@@ -483,13 +600,14 @@ lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, i
   size_t off_lws = round_up(off_pend + (c.deferred ? n_units * 4 : 0), 256);
   size_t off_lwr = round_up(off_lws + (layer ? lunits * cache->slot_stride * 4 : 0), 256);
   size_t off_lwa = round_up(off_lwr + (layer ? lunits * 4 : 0), 256);
-  // split launches: [rem][2C][2 kMaxGroup] statistics, [rem][2C][G d + 4] partial
-  // outputs, [rem][2] counters
-  const size_t nsp = (size_t)cache->split_rem * 2 * cluster;
+  // planned launches, per exchange slot (one per cluster): [kMaxSplitParts][2
+  // kMaxGroup] statistics, [kMaxSplitParts][G d + 4] partial outputs, [2] counters
+  const size_t nxs = cache->plan_ok ? (size_t)grid_y : 0;
+  const size_t nsp = nxs * lf::kMaxSplitParts;
   size_t off_sst = round_up(off_lwa + (layer ? lunits * 4 : 0), 256);
   size_t off_sfn = round_up(off_sst + nsp * 2 * lf::kMaxGroup * 4, 256);
   size_t off_scn = round_up(off_sfn + nsp * ((size_t)group * head_dim + 4) * 4, 256);
-  size_t small_bytes = round_up(off_scn + (size_t)cache->split_rem * 2 * 4, 256);
+  size_t small_bytes = round_up(off_scn + nxs * 2 * 4, 256);
 
   if ((e = cudaMalloc(&cache->K, kv_bytes)) != cudaSuccess ||
       (e = cudaMalloc(&cache->V, kv_bytes)) != cudaSuccess ||
@@ -512,9 +630,9 @@ lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, i
   cache->lw_score = layer ? reinterpret_cast<float*>(s + off_lws) : nullptr;
   cache->lw_req = layer ? reinterpret_cast<int32_t*>(s + off_lwr) : nullptr;
   cache->lw_anew = layer ? reinterpret_cast<float*>(s + off_lwa) : nullptr;
-  cache->split_stat = cache->split_rem ? reinterpret_cast<float*>(s + off_sst) : nullptr;
-  cache->split_fin = cache->split_rem ? reinterpret_cast<float*>(s + off_sfn) : nullptr;
-  cache->split_cnt = cache->split_rem ? reinterpret_cast<int32_t*>(s + off_scn) : nullptr;
+  cache->split_stat = cache->plan_ok ? reinterpret_cast<float*>(s + off_sst) : nullptr;
+  cache->split_fin = cache->plan_ok ? reinterpret_cast<float*>(s + off_sfn) : nullptr;
+  cache->split_cnt = cache->plan_ok ? reinterpret_cast<int32_t*>(s + off_scn) : nullptr;
 
   // Empty state: no occupied slot, positions -1, ||v||_1 0, K/V zero.
   int32_t* hb = new (std::nothrow) int32_t[batch];
@@ -635,9 +753,8 @@ int lf_prefill_fill(lf_cache* cache, int layer, const void* k, const void* v,
   e = cudaLaunchKernel(cache->kern.prefill, dim3(cache->kv_heads, cache->batch, 1),
                        dim3(lf::kThreads, 1, 1), args, 0, st);
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
-  long long shortest = cache->fill_cap;
-  for (int b = 0; b < cache->batch; ++b) shortest = std::min<long long>(shortest, prompt_len[b]);
-  cache->fill[layer] = shortest;
+  for (int b = 0; b < cache->batch; ++b)
+    cache->occ[(size_t)layer * cache->batch + b] = std::min(prompt_len[b], cache->occ_limit[b]);
   return LF_OK;
 }
 
@@ -715,22 +832,23 @@ int lf_decode_step(lf_cache* cache, int layer, const void* q, const void* k_new,
     ta.a = a;
     ta.row_base = (int)(layer * layer_slots);
     ta.max_items = cache->items;
-    // the split kernel pays for its exchanges only when every unit is long (measured at
-    // batch 32 on 2-CTA clusters: 9% faster at 3276 slots, 7% at 2048 and 2560, even at
-    // 1664, 4-9% slower from 1408 down to 640)
-    const bool split = cache->split_rem > 0 && cache->fill[layer] >= kSplitMinSlots;
-    ta.split_rem = cache->split_rem;
+    ta.plan_nc = 0;
     ta.split_stat = cache->split_stat;
     ta.split_fin = cache->split_fin;
     ta.split_cnt = cache->split_cnt;
+    const bool planned = plan_layer(cache, layer, ta.cut_unit, ta.cut_slot);
+    if (planned) ta.plan_nc = cache->grid_y;
     void* args[] = {&ta};
-    e = cudaLaunchKernelExC(&cfg, split ? cache->kern.decode_split : cache->kern.decode, args);
+    e = cudaLaunchKernelExC(&cfg, planned ? cache->kern.decode_split : cache->kern.decode, args);
   } else {
     void* args[] = {&a};
     e = cudaLaunchKernelExC(&cfg, cache->kern.decode, args);
   }
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
-  cache->fill[layer] = std::min(cache->fill[layer] + 1, cache->fill_cap);
+  for (int b = 0; b < cache->batch; ++b) {
+    int32_t& o = cache->occ[(size_t)layer * cache->batch + b];
+    o = std::min(o + 1, cache->occ_limit[b]);
+  }
   if (cache->scope == LF_SCOPE_LAYER) {
     // The shared victim of every sequence, once all its KV heads have scored.
     // Programmatic dependent launch: its CTAs are placed while the decode grid
@@ -787,7 +905,10 @@ int lf_rkv_compress(lf_cache* cache, int layer, const void* q_obs, lf_stream_t s
                                    static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "R-KV compression launch");
   // every sequence is back at the budget (or at most that: it was below it)
-  cache->fill[layer] = std::min(cache->fill[layer], (long long)ra.budget);
+  for (int b = 0; b < cache->batch; ++b) {
+    int32_t& o = cache->occ[(size_t)layer * cache->batch + b];
+    o = std::min(o, ra.budget);
+  }
   return LF_OK;
 }
 
@@ -804,12 +925,31 @@ int lf_cache_check(lf_cache* cache, lf_stream_t stream, int32_t* bits) {
   if ((e = cudaMemset(cache->err, 0, 4)) != cudaSuccess ||
       // an expired wait can leave a split launch's exchange counters mid-count
       ((word & LF_DEVERR_TIMEOUT) && cache->split_cnt &&
-       (e = cudaMemset(cache->split_cnt, 0, (size_t)cache->split_rem * 2 * 4)) != cudaSuccess) ||
+       (e = cudaMemset(cache->split_cnt, 0, (size_t)cache->grid_y * 2 * 4)) != cudaSuccess) ||
       (e = cudaDeviceSynchronize()) != cudaSuccess)
     return cuda_fail(e, "clearing the error word");
   if (bits) *bits = word;
   if (word != 0) return fail(LF_ERR_DEVICE, "device error word 0x%x", (unsigned)word);
   return LF_OK;
+}
+
+int lf_launch_plan(lf_cache* cache, int layer, int32_t* cut_unit, int32_t* cut_slot,
+                   int max_cuts) {
+  clear_last();
+  if (!cache) return fail(LF_ERR_ARG, "null cache");
+  if (layer < 0 || layer >= cache->layers)
+    return fail(LF_ERR_ARG, "layer %d outside [0, %d)", layer, cache->layers);
+  int cu[lf::kTcMaxPlan + 1], cs[lf::kTcMaxPlan + 1];
+  if (!plan_layer(cache, layer, cu, cs)) return 0;
+  const int nc = cache->grid_y;
+  if (cut_unit && cut_slot) {
+    if (max_cuts < nc + 1) return fail(LF_ERR_ARG, "max_cuts %d < %d", max_cuts, nc + 1);
+    for (int j = 0; j <= nc; ++j) {
+      cut_unit[j] = cu[j];
+      cut_slot[j] = cs[j];
+    }
+  }
+  return nc;
 }
 
 int lf_cache_layout(const lf_cache* cache, lf_layout* out) {
@@ -848,7 +988,7 @@ int lf_cache_layout(const lf_cache* cache, lf_layout* out) {
   out->rkv_beta = cache->rkv_beta;
   out->rkv_lambda = cache->rkv_lambda;
   out->rkv_tau = cache->rkv_tau;
-  out->split_units = cache->split_rem;
+  out->split_units = cache->plan_ok ? cache->grid_y : 0;
   out->split_cnt = cache->split_cnt;
   return LF_OK;
 }

@@ -62,23 +62,66 @@ constexpr int kTcPBufs = 4;       // P^T tiles in flight between the compute war
 // is resident per SM, so the allocation never waits.
 constexpr int kTcTmemCols = 512;
 constexpr int kTcMaxItems = 512;  // units one cluster may visit in one launch
+constexpr int kTcItemInts = 8;    // ints per entry of the shared-memory item table
+constexpr int kTcMaxPlan = 152;   // clusters a launch plan can describe (one per SM at most)
+
+// Planned launches: at most this many CTAs share a unit.
+constexpr int kMaxSplitParts = 16;
 
 struct TcArgs {
   CUtensorMap k64, k16, v64, v16;  // 2-D views [rows][128] of K and V, boxes {64,64} / {64,16}
   DecodeArgs a;
   int row_base;                    // tensor row of this layer's first slot
   int max_items;                   // units one cluster may visit (sizes the item table)
-  // Split launches (kernel instantiated with kSplit): the units left over after
-  // the whole rounds are each shared by two clusters, which exchange through
-  // global memory (they are co-resident: the grid is persistent).
-  int split_rem;                   // units shared by two clusters (units mod clusters)
-  float* split_stat;               // [split_rem][2C][2 kMaxGroup]: each piece's (m_h, l_h)
-  float* split_fin;                // [split_rem][2C][G D + 4]: partial output, score, slot, flag
-  int* split_cnt;                  // [split_rem][2]: arrivals at the two exchanges
+  // Planned launches (kernel instantiated with kSplit).  The host cuts the
+  // layer's (unit, slot) order, units in index order and slots in order within
+  // a unit, into one contiguous range per cluster: cluster j starts at slot
+  // cut_slot[j] of unit cut_unit[j] and ends where cluster j + 1 starts (cut
+  // plan_nc is (units, 0)).  A unit cut inside (cut_slot > 0) is shared by the
+  // clusters whose ranges meet it; they exchange through global memory (all are
+  // co-resident: the grid is persistent).  Its last range runs to the unit's
+  // occupied count at launch time, so any plan covers every slot.
+  int plan_nc;                     // clusters of the plan (gridDim.y); 0: whole units
+  float* split_stat;               // [plan_nc][kMaxSplitParts][2 kMaxGroup]: (m_h, l_h) per part
+  float* split_fin;                // [plan_nc][kMaxSplitParts][G D + 4]: partial output,
+                                   //   score, slot, flag per part
+  int* split_cnt;                  // [plan_nc][2]: arrivals at the two exchanges
+  int cut_unit[kTcMaxPlan + 1];
+  int cut_slot[kTcMaxPlan + 1];    // multiples of 4
 };
 
-// Split launches: at most this many CTAs share a unit (clusters of 1 or 2).
-constexpr int kMaxSplitParts = 4;
+// A shared unit's part held by one cluster of a planned launch.
+struct TcPiece {
+  int unit, lo, hi;  // slots [lo, hi) of the unit (hi = INT_MAX: to its occupied count)
+  int xi;            // exchange slot: the first cut inside the unit
+  int mc;            // this cluster's index among the unit's clusters (0 leads)
+  int ncl;           // clusters sharing the unit
+};
+
+// The parts of the units cut at cluster j's two range ends (start, then end),
+// and its whole units [*w0, *w1).  Returns the number of parts (0-2).
+__device__ __forceinline__ int plan_pieces(const TcArgs& ta, int j, TcPiece* pc, int* w0,
+                                           int* w1) {
+  const int nc = ta.plan_nc;
+  const int u0 = ta.cut_unit[j], s0 = ta.cut_slot[j];
+  const int u1 = ta.cut_unit[j + 1], s1 = ta.cut_slot[j + 1];
+  auto inner = [&](int c, int u) { return c >= 1 && c < nc && ta.cut_unit[c] == u && ta.cut_slot[c] > 0; };
+  int np = 0;
+  if (s0 > 0) {  // the range starts inside unit u0
+    int jmin = j, jmax = j;
+    while (inner(jmin - 1, u0)) --jmin;
+    while (inner(jmax + 1, u0)) ++jmax;
+    pc[np++] = {u0, s0, (u1 == u0) ? s1 : INT_MAX, jmin, j - jmin + 1, jmax - jmin + 2};
+  }
+  if (s1 > 0 && !(s0 > 0 && u1 == u0)) {  // it ends inside unit u1 and holds the unit's slot 0
+    int jmax = j + 1;
+    while (inner(jmax + 1, u1)) ++jmax;
+    pc[np++] = {u1, 0, s1, j + 1, 0, jmax - j + 1};
+  }
+  *w0 = (s0 > 0) ? u0 + 1 : u0;
+  *w1 = max(*w0, u1);
+  return np;
+}
 
 // Split launches: spin, with a bound, until another CTA of this persistent grid
 // (all of them are resident) has counted itself in.
@@ -113,9 +156,13 @@ struct TcPlan {
   static constexpr int kOffStats = 896;  // m_loc[2], l_loc[2], s_new[2], cmul, m_glb, l_glb
   static constexpr int kOffRed = kOffStats + 9 * kMaxGroup * 4;
   static constexpr int kOffMisc = kOffRed + 4 * kMaxGroup * 4 + 16;
-  static constexpr int kOffStatIn = 2048;                    // [2][kMaxCluster][2G] floats
+  // planned launches: the tail's copy of a shared unit's parts' (m, l)
+  static constexpr int kOffPieceStats = 2048;                // [kMaxSplitParts][2G] floats
+  static constexpr int kOffStatIn = 3072;                    // [2][kMaxCluster][2G] floats
   static constexpr int kOffOpart = kOffStatIn + 2 * kMaxCluster * 2 * kMaxGroup * 4;  // [2][G][D]
-  static_assert(kOffMisc + 64 <= kOffStatIn, "header overflow");
+  static_assert(kOffMisc + 64 <= kOffPieceStats, "header overflow");
+  static_assert(kOffPieceStats + kMaxSplitParts * 2 * kMaxGroup * 4 <= kOffStatIn,
+                "header overflow");
   static_assert(16 + 16 + 2 * kTcSBufs + 2 * kTcPBufs + 14 <= kOffStats / 8, "too many barriers");
   static constexpr int kOffQ = (kOffOpart + 2 * G * D * 4 + 1023) / 1024 * 1024;  // [2] buffers
   static constexpr int kOffRing = kOffQ + 2 * kQBytes;
@@ -135,14 +182,16 @@ struct TcPlan {
     return (off_lg(stages, cluster) + (evict ? 2 : 1) * chunk * G * 4 + 15) / 16 * 16;
   }
   // vn[2], pos[2] (raw, from the slab) then w[2] (candidate weights), each vn_bytes(chunk);
-  // then the item table: (count, next position, deferred choice, -) per unit visited.
+  // then the item table: (count, next position, deferred choice, budget, unit, first
+  // slot, end slot, part) per item visited.
   __host__ __device__ static constexpr int off_items(int stages, int chunk, int cluster,
                                                      int evict) {
     return off_vn(stages, chunk, cluster, evict) + (evict ? 6 * vn_bytes(chunk) : 0);
   }
   __host__ __device__ static constexpr int smem_bytes(int stages, int chunk, int cluster,
                                                       int evict, int items) {
-    return off_items(stages, chunk, cluster, evict) + items * 16 + 1024;  // + alignment slack
+    return off_items(stages, chunk, cluster, evict) + items * kTcItemInts * 4 +
+           1024;  // + alignment slack
   }
 };
 
@@ -167,21 +216,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int S = a.stages;
   const int chunk = a.chunk;
   const int units = a.batch * a.kv_heads;
-  // Whole units: cluster j takes j, j + NC, ...  Split launches: `rounds` whole
-  // rounds, and cluster j < 2 split_rem first takes half (j & 1) of unit
-  // rounds NC + j / 2, shared with cluster j ^ 1.  The shared unit comes first
-  // so that both halves start together and its exchanges through L2 overlap
-  // the stream of the whole units after it.
-  const int rounds = kSplit ? (units - ta.split_rem) / NC : 0;
-  const bool has_piece = kSplit && j < 2 * ta.split_rem;
-  const int pfirst = has_piece ? 1 : 0;  // items before the first whole unit
-  const int nitems = kSplit ? rounds + pfirst
-                            : ((j < units) ? (units - j + NC - 1) / NC : 0);
-  auto unit_of = [&](int k) {
-    return (has_piece && k == 0) ? rounds * NC + (j >> 1) : j + (k - pfirst) * NC;
-  };
-  auto is_piece = [&](int k) { return has_piece && k == 0; };
-  if (nitems > ta.max_items) {  // the host sized the item table for fewer units
+  // Whole-unit launches: cluster j takes units j, j + NC, ...  Planned
+  // launches: the parts of the units shared at its range ends first (so that
+  // every cluster sharing a unit starts on it together and the exchanges
+  // through L2 overlap the stream of the items after it), then its whole units
+  // in order.
+  TcPiece pcs[2];
+  int npc = 0, w0 = 0, w1 = 0;
+  if (kSplit && ta.plan_nc == NC) npc = plan_pieces(ta, j, pcs, &w0, &w1);
+  const bool planned = kSplit && ta.plan_nc == NC;
+  const int nitems = planned ? npc + (w1 - w0) : ((j < units) ? (units - j + NC - 1) / NC : 0);
+  if (nitems > ta.max_items || (kSplit && !planned) ||
+      (npc > 0 && pcs[0].ncl * C > kMaxSplitParts) ||
+      (npc > 1 && pcs[1].ncl * C > kMaxSplitParts)) {
+    // the host sized the item table for fewer units, or the plan does not fit
     if (threadIdx.x == 0 && cg::this_cluster().block_rank() == 0) atomicOr(ta.a.err, LF_DEVERR_STATE);
     return;
   }
@@ -222,7 +270,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   volatile int* uflag = reinterpret_cast<volatile int*>(smem + P::kOffMisc + 24);  // [2]
   volatile int* split_flag = reinterpret_cast<volatile int*>(smem + P::kOffMisc + 40);
   float* stat_in = reinterpret_cast<float*>(smem + P::kOffStatIn);  // [2][C][2G]
-  int* items = reinterpret_cast<int*>(smem + P::off_items(S, chunk, C, a.evict));  // [nitems][4]
+  int* items = reinterpret_cast<int*>(smem + P::off_items(S, chunk, C, a.evict));  // [nitems][8]
   float* opbase = reinterpret_cast<float*>(smem + P::kOffOpart);     // [2][G][D]
   unsigned char* qbuf = smem + P::kOffQ;
   unsigned char* ring = smem + P::kOffRing;
@@ -285,12 +333,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // Occupancy and position of every unit this cluster visits, read once: the
   // leaders update them during the launch, every role must see the old values.
+  // (A unit shared with other clusters is updated by its leader only after
+  // every part has sent its partial output, so all of them have read it.)
   for (int k = tid; k < nitems; k += kTcThreads) {
-    const int u = unit_of(k);
-    items[4 * k] = a.count[u];
-    items[4 * k + 1] = a.next_pos[u];
-    items[4 * k + 2] = (a.evict && a.deferred) ? a.pending[u] : -1;
-    items[4 * k + 3] = a.budget[u / a.kv_heads];
+    int u, lo = 0, hi = INT_MAX, part = 0;
+    if (!planned) {
+      u = j + k * NC;
+    } else if (k < npc) {
+      u = pcs[k].unit;
+      lo = pcs[k].lo;
+      hi = pcs[k].hi;
+      part = (pcs[k].xi << 16) | (pcs[k].mc << 8) | pcs[k].ncl;  // xi >= 1: never 0
+    } else {
+      u = w0 + (k - npc);
+    }
+    int* it = items + kTcItemInts * k;
+    it[0] = a.count[u];
+    it[1] = a.next_pos[u];
+    it[2] = (a.evict && a.deferred) ? a.pending[u] : -1;
+    it[3] = a.budget[u / a.kv_heads];
+    it[4] = u;
+    it[5] = lo;
+    it[6] = hi;
+    it[7] = part;
   }
   fence_proxy_async_smem();
   tc_fence_before();
@@ -301,19 +366,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const uint32_t tO = tmem + 16 * kTcSBufs;
 
-  // This CTA's share of unit k: the occupied slots are split evenly over the
-  // cluster (in multiples of 4), so a partly filled unit keeps every CTA busy.
-  // Returns the slot count and sets `base`, the first slot.
+  auto unit_of = [&](int k) { return items[kTcItemInts * k + 4]; };
+  auto is_piece = [&](int k) { return kSplit && items[kTcItemInts * k + 7] != 0; };
+  // This CTA's share of item k: the occupied slots of the unit (of a shared
+  // unit: of this cluster's range of it, clipped to the occupied count) are
+  // split evenly over the cluster, in multiples of 4 from a multiple of 4, so
+  // a partly filled unit keeps every CTA busy.  Returns the slot count and
+  // sets `base`, the first slot.
   auto unit_rows = [&](int k, int& n, int& p, bool& ok, int& base) {
-    n = items[4 * k];
-    p = items[4 * k + 1];
+    const int* it = items + kTcItemInts * k;
+    n = it[0];
+    p = it[1];
     ok = (n >= 0 && n <= a.capacity && p >= n);
-    // a split unit is shared by 2C CTAs: this cluster's half is the CTAs (j & 1) C ..
-    const int parts = is_piece(k) ? 2 * C : C;
-    const int sub = is_piece(k) ? (j & 1) * C + rank : rank;
-    const int per = ((n + parts - 1) / parts + 3) & ~3;  // <= chunk since n <= capacity
-    base = sub * per;
-    return ok ? max(0, min(per, n - base)) : 0;
+    const int lo = min(it[5], max(n, 0));
+    const int hi = min(it[6], max(n, 0));
+    const int per = ((hi - lo + C - 1) / C + 3) & ~3;  // <= chunk since n <= capacity
+    base = lo + rank * per;
+    return ok ? max(0, min(per, hi - base)) : 0;
   };
 
   // Tile order through the ring, shared by the producer and the MMA warp.  For
@@ -558,6 +627,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncwarp();
   } else if (warp < kTcTailWarp0) {
     // ---- epilogue warps 0-3 (thread i <-> TMEM lane i) ---------------------------
+    // A shared unit (planned launch): this CTA's (m_h, l_h) go to the unit's other
+    // parts through global memory as soon as they are final, from here rather
+    // than from the tail warps, so that no cluster's exchange waits for another
+    // cluster's tail to reach that unit.  Thread 0, after m_loc / l_loc are written.
+    auto publish_stats = [&](int k, int b2) {
+      const int part = items[kTcItemInts * k + 7];
+      const int xi = part >> 16;
+      const int me = ((part >> 8) & 0xff) * C + rank;
+      float* gst = ta.split_stat + ((size_t)xi * kMaxSplitParts + me) * 2 * kMaxGroup;
+#pragma unroll
+      for (int h = 0; h < kMaxGroup; ++h) {
+        gst[h] = h < G ? m_loc[b2 * kMaxGroup + h] : -INFINITY;
+        gst[kMaxGroup + h] = h < G ? l_loc[b2 * kMaxGroup + h] : 0.f;
+      }
+      __threadfence();
+      atomicAdd(ta.split_cnt + 2 * xi, 1);
+    };
     int kt = 0, ne = 0, pt = 0;
     for (int k = 0; k < nitems; ++k) {
       int n, p, base;
@@ -571,8 +657,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int32_t* pos_s =
           reinterpret_cast<const int32_t*>(vnbase + (2 + b2) * P::vn_bytes(chunk));
       float* w_s = reinterpret_cast<float*>(vnbase + (4 + b2) * P::vn_bytes(chunk));
-      const int bud = items[4 * k + 3];
-      const UnitRule rl = unit_rule(a, n, p, items[4 * k + 2], bud, state_ok);
+      const int bud = items[kTcItemInts * k + 3];
+      const UnitRule rl = unit_rule(a, n, p, items[kTcItemInts * k + 2], bud, state_ok);
       const int plim = rl.plim;  // a slot is a candidate iff sinks <= pos < plim (and not excl)
       const int excl = rl.excl - base;  // this CTA's row of the dropped slot (deferred)
 
@@ -684,7 +770,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // This CTA's (m, l), logits and candidate weights are final: the tail
         // warps exchange and score them while the unit's V tiles still stream.
         __syncwarp();
-        if (tid == 0) mbar_arrive(&statrdy[b2]);
+        if (tid == 0) {
+          if (is_piece(k)) publish_stats(k, b2);
+          mbar_arrive(&statrdy[b2]);
+        }
         // The output accumulator: thread e <-> TMEM lane e <-> output element e.
         if (!bad2 && __all_sync(0xffffffffu, mbar_wait_bounded(ofull, (uint32_t)(ne & 1)))) {
           tc_fence_after();
@@ -704,7 +793,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           l_loc[b2 * kMaxGroup + tid] = 0.f;
         }
         __syncwarp();
-        if (tid == 0) mbar_arrive(&statrdy[b2]);
+        if (tid == 0) {
+          if (is_piece(k)) publish_stats(k, b2);
+          mbar_arrive(&statrdy[b2]);
+        }
       }
       if (rows > 0) ne += 1;
       const bool failed = any_bad || named_bar_or(1, kTcCompute, bad2);
@@ -732,8 +824,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int u = unit_of(k);
       const int b = u / a.kv_heads;
       const int g = u - b * a.kv_heads;
-      const int bud = items[4 * k + 3];
-      const int pend = items[4 * k + 2];
+      const int bud = items[kTcItemInts * k + 3];
+      const int pend = items[kTcItemInts * k + 2];
       const UnitRule rl = unit_rule(a, n, p, pend, bud, state_ok);
       const bool h2o = a.evict && a.score == LF_SCORE_H2O;
       const bool layer = a.evict && a.scope == LF_SCOPE_LAYER;
@@ -773,27 +865,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
       if constexpr (kSplit) {
         if (is_piece(k)) {
-          // ---- a unit shared with cluster j ^ 1 (the first item of both): both
-          // exchanges go through global memory, counted by atomics.  Only the
-          // per-KV-head LongFlow score and append modes are split (host). ----
-          const int su = j >> 1;              // shared unit
-          const int np = 2 * C;               // CTAs sharing it (<= kMaxSplitParts: host)
-          const int me = (j & 1) * C + rank;  // this CTA's piece; piece 0 leads
-          constexpr int kFinF = G * D + 4;    // floats per piece: output, score, slot, flag
-          int* cnt = ta.split_cnt + 2 * su;
-          float* gst = ta.split_stat + (size_t)su * np * 2 * kMaxGroup;
-          float* gfn = ta.split_fin + (size_t)su * np * kFinF;
-          float* sst = stat_in + (size_t)b2 * kMaxCluster * 2 * kMaxGroup;  // local copy
-          // Exchange 1: every piece's (m_h, l_h).
-          if (tt_id < 2 * kMaxGroup) {
-            const int h = tt_id % kMaxGroup;
-            gst[me * 2 * kMaxGroup + tt_id] =
-                tt_id < kMaxGroup ? (h < G ? mlc[h] : -INFINITY) : (h < G ? llc[h] : 0.f);
-          }
-          __threadfence();
-          named_bar_sync(2, kTcTail);
+          // ---- a unit shared with other clusters (a planned launch): both
+          // exchanges go through global memory, counted by atomics.  The parts
+          // are the CTAs of the clusters whose ranges meet the unit, in cluster
+          // then rank order; part 0 leads.  Only the per-KV-head LongFlow score
+          // and the append modes are planned (host). ----
+          const int part = items[kTcItemInts * k + 7];
+          const int xi = part >> 16;                      // exchange slot
+          const int np = (part & 0xff) * C;               // parts (<= kMaxSplitParts)
+          const int me = ((part >> 8) & 0xff) * C + rank; // this CTA's part
+          constexpr int kFinF = G * D + 4;  // floats per part: output, score, slot, flag
+          int* cnt = ta.split_cnt + 2 * xi;
+          const float* gst = ta.split_stat + (size_t)xi * kMaxSplitParts * 2 * kMaxGroup;
+          float* gfn = ta.split_fin + (size_t)xi * kMaxSplitParts * kFinF;
+          // local copy (not stat_in: a cluster peer may already be sending the
+          // next whole unit's statistics there)
+          float* sst = reinterpret_cast<float*>(smem + P::kOffPieceStats);
+          // Exchange 1: every part's (m_h, l_h), published by the epilogue warps.
           if (tt_id == 0) {
-            atomicAdd(cnt, 1);
             split_flag[0] = wait_count_bounded(cnt, np) ? 1 : 0;
             __threadfence();
           }
@@ -856,7 +945,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           named_bar_sync(2, kTcTail);
           const bool unit_failed = unit_handoff();
-          // Exchange 2: partial output, lowest (score, slot) and failure flag to piece 0.
+          // Exchange 2: partial output, lowest (score, slot) and failure flag to part 0.
           for (int c = tt_id; c < G * D; c += kTcTail) gfn[(size_t)me * kFinF + c] = o_part[c];
           if (tt_id == 0) {
             float cs = red_t[0];
@@ -880,7 +969,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             named_bar_sync(2, kTcTail);
             const bool all_got = split_flag[0] != 0;
-            // Every piece's lowest (score, slot) and failure flag: one piece per
+            // Every part's lowest (score, slot) and failure flag: one part per
             // lane of warp 0, loaded together, then reduced.
             float fs = INFINITY;
             int fi = INT_MAX;
@@ -907,29 +996,43 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
               }
             }
-            // Output: the new token + every piece's partial output, in piece order.
-            // Each thread's elements (tt_id + 64 i) of every piece are loaded at once.
+            // Output: the new token + every part's partial output, in part order,
+            // four parts' elements loaded at a time.
             if (all_got && stats_ok) {
               constexpr int kEl = G * D / kTcTail;
               T* og = reinterpret_cast<T*>(a.out) + ((size_t)b * a.q_heads + (size_t)g * G) * D;
-              float part[kEl][kMaxSplitParts];
+              float acc[kEl];
 #pragma unroll
-              for (int i = 0; i < kEl; ++i)
+              for (int i = 0; i < kEl; ++i) {
+                const int h = (tt_id + i * kTcTail) / D;
+                const int e = (tt_id + i * kTcTail) - h * D;
+                acc[i] = exp2f(snw[h] - m_glb[h]) * to_f32(vn[e]);
+              }
+              for (int r0 = 0; r0 < np; r0 += 4) {
+                float part4[kEl][4];
 #pragma unroll
-                for (int r = 0; r < kMaxSplitParts; ++r)
-                  part[i][r] = (r < np) ? __ldcg(gfn + (size_t)r * kFinF + tt_id + i * kTcTail) : 0.f;
+                for (int i = 0; i < kEl; ++i)
+#pragma unroll
+                  for (int q = 0; q < 4; ++q)
+                    part4[i][q] = (r0 + q < np)
+                                      ? __ldcg(gfn + (size_t)(r0 + q) * kFinF + tt_id + i * kTcTail)
+                                      : 0.f;
+#pragma unroll
+                for (int i = 0; i < kEl; ++i) {
+                  const int h = (tt_id + i * kTcTail) / D;
+#pragma unroll
+                  for (int q = 0; q < 4; ++q) {
+                    const float mr = (r0 + q < np) ? sst[(r0 + q) * 2 * kMaxGroup + h] : -INFINITY;
+                    if (mr != -INFINITY) acc[i] += part4[i][q] * exp2f(mr - m_glb[h]);
+                  }
+                }
+              }
 #pragma unroll
               for (int i = 0; i < kEl; ++i) {
                 const int idx = tt_id + i * kTcTail;
                 const int h = idx / D;
                 const int e = idx - h * D;
-                float acc = exp2f(snw[h] - m_glb[h]) * to_f32(vn[e]);
-#pragma unroll
-                for (int r = 0; r < kMaxSplitParts; ++r) {
-                  const float mr = (r < np) ? sst[r * 2 * kMaxGroup + h] : -INFINITY;
-                  if (mr != -INFINITY) acc += part[i][r] * exp2f(mr - m_glb[h]);
-                }
-                from_f32(acc / l_glb[h], &og[(size_t)h * D + e]);
+                from_f32(acc[i] / l_glb[h], &og[(size_t)h * D + e]);
               }
             }
             float anew = 0.f;
@@ -939,7 +1042,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               const LeaderOut d =
                   leader_decide(a, u, n, p, pend, bud, state_ok, any_fail, rl, fi, anew);
               decision[0] = d.slot;
-              // every piece is through both exchanges: ready for the next launch
+              // every part is through both exchanges: ready for the next launch
               cnt[0] = 0;
               cnt[1] = 0;
             }
@@ -973,9 +1076,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             st_async_v4(ra + q4 * 4, v[q4], v[q4 + 1], v[q4 + 2], v[q4 + 3], rb);
         }
       }
-      // statb[b2] completes once per whole unit of parity b2 (a shared unit,
-      // item 0, does not use it).
-      const uint32_t stat_phase = (uint32_t)(((k >> 1) - ((pfirst && b2 == 0) ? 1 : 0)) & 1);
+      // statb[b2] completes once per whole unit of parity b2 (the shared units
+      // first in a planned launch do not use it).
+      const int npc_items = planned ? npc : 0;
+      const int k0 = npc_items + ((k - npc_items) & 1);  // first whole item of this parity
+      const uint32_t stat_phase = (uint32_t)(((k - k0) >> 1) & 1);
       const bool got_stats = __all_sync(
           0xffffffffu, mbar_wait_cluster_bounded(&statb[b2], stat_phase));
       if (tt_id < G) {
@@ -1074,7 +1179,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // Exchange 2: partial output and lowest (score, slot) to the unit's leader.
       // One receive buffer suffices: a peer can send the leader's next unit only
       // after the leader has sent its own statistics for it, i.e. finished this one.
-      const int leader = k % C;
+      const int leader = (k - npc_items) % C;
       unsigned char* fin = fin_in;
       if (rank == leader && tt_id == 0) mbar_arrive_expect_tx(finb, (uint32_t)(C * P::kFinBytes));
       {
@@ -1095,7 +1200,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       if (rank == leader) {
         // finb completes once per whole unit this CTA leads (not for a shared unit).
-        const uint32_t fin_phase = (uint32_t)(((k / C) - ((pfirst && leader == 0) ? 1 : 0)) & 1);
+        const uint32_t fin_phase = (uint32_t)(((k - npc_items) / C) & 1);
         const bool got = __all_sync(0xffffffffu, mbar_wait_cluster_bounded(finb, fin_phase));
         const bool all_got = !named_bar_or(2, kTcTail, !got);
         // Output: the new token + every CTA's partial output, in rank order.

@@ -27,7 +27,7 @@ __all__ = [
     "lf_cache_create", "lf_cache_create_ex", "lf_cache_destroy", "lf_prefill_fill",
     "lf_decode_step", "lf_cache_check", "lf_cache_layout", "lf_last_error", "lf_last_status",
     "lf_abi_version",
-    "lf_prefill_fill_noalloc", "lf_rkv_compress",
+    "lf_prefill_fill_noalloc", "lf_rkv_compress", "lf_launch_plan",
     "LFCache",
 ]
 
@@ -118,6 +118,9 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.lf_last_status.argtypes = []
     lib.lf_rkv_compress.restype = I
     lib.lf_rkv_compress.argtypes = [P, I, VP, VP]
+    lib.lf_launch_plan.restype = I
+    lib.lf_launch_plan.argtypes = [P, I, ctypes.POINTER(ctypes.c_int32),
+                                   ctypes.POINTER(ctypes.c_int32), I]
     lib.lf_prefill_fill_noalloc.restype = I
     lib.lf_prefill_fill_noalloc.argtypes = [ctypes.POINTER(LFLayout), I, VP, VP,
                                             ctypes.POINTER(ctypes.c_int32), I, VP]
@@ -237,6 +240,21 @@ def lf_rkv_compress(handle, layer, q_obs, stream=None) -> int:
     return _check(load_library().lf_rkv_compress(handle, layer, _ptr(q_obs), _stream(stream)))
 
 
+def lf_launch_plan(handle, layer):
+    """The next step's plan of `layer`: None (whole units per cluster) or a list
+    of (unit, slot) cuts, one per cluster plus the end."""
+    lib = load_library()
+    n = 256
+    cu = (ctypes.c_int32 * n)()
+    cs = (ctypes.c_int32 * n)()
+    nc = lib.lf_launch_plan(handle, layer, cu, cs, n)
+    if nc < 0:
+        raise LFError(nc, lf_last_error())
+    if nc == 0:
+        return None
+    return [(int(cu[j]), int(cs[j])) for j in range(nc + 1)]
+
+
 def lf_cache_layout(handle) -> LFLayout:
     lay = LFLayout()
     _check(load_library().lf_cache_layout(handle, ctypes.byref(lay)))
@@ -328,6 +346,10 @@ class LFCache:
         lay = self.layout
         self._expect(q_obs, (self.batch, lay.rkv_alpha, self.q_heads, self.head_dim), "q_obs")
         lf_rkv_compress(self.handle, layer, q_obs, stream)
+
+    def plan(self, layer: int):
+        """lf_launch_plan: None, or the (unit, slot) cuts of the next step of `layer`."""
+        return lf_launch_plan(self.handle, layer)
 
     def check(self, stream=None) -> int:
         return lf_cache_check(self.handle, stream)

@@ -72,7 +72,7 @@
 extern "C" {
 #endif
 
-#define LF_ABI_VERSION 5
+#define LF_ABI_VERSION 6
 
 typedef struct lf_cache lf_cache; /* opaque; owns the slab */
 
@@ -268,18 +268,42 @@ typedef struct lf_layout {
                        as count; -1 = none chosen), else NULL */
   int rkv_buffer, rkv_alpha, rkv_beta; /* R-KV parameters (evict = LF_EVICT_RKV) */
   float rkv_lambda, rkv_tau;
-  int split_units;  /* tensor-core kernel: units shared by two clusters (those left
-                       after the whole rounds, when they fill at most half of the
-                       clusters) at the steps where every sequence of the layer holds
-                       >= 2048 tokens,
-                       by the host's count of prompts and steps; 0: never split */
-  int32_t* split_cnt; /* split launches: [split_units][2] arrival counts of a shared
-                       unit's two exchanges through global memory.  Zero between
-                       launches; lf_cache_check zeroes them after an expired wait.
-                       NULL when split_units is 0 */
+  int split_units;  /* tensor-core kernel with planned launches possible (see
+                       lf_launch_plan): its resident clusters nc; 0 when steps never
+                       take a plan (the policy or the kernel does not allow it) */
+  int32_t* split_cnt; /* planned launches: [split_units][2] arrival counts of the two
+                       exchanges through global memory of a shared unit, at the row
+                       of its first inner cut.  Zero between launches; lf_cache_check
+                       zeroes them after an expired wait.  NULL when split_units is 0 */
 } lf_layout;
 
 int lf_cache_layout(const lf_cache* cache, lf_layout* out);
+
+/*
+ * The launch plan of the next lf_decode_step of `layer` (tensor-core kernel).
+ * (No counterpart on the pages: this reports how the work of a step is spread
+ * over the GPU, for tests and tuning.)
+ *
+ * A launch runs nc = lf_layout.split_units resident clusters.  Without a plan
+ * (return value 0) cluster j takes the whole units j, j + nc, j + 2 nc, ...
+ * of the layer (unit u = sequence u / kv_heads, KV head u % kv_heads).  With a
+ * plan (return value nc) the layer's slots, units in index order and slots in
+ * order within a unit, are cut into nc contiguous ranges: cluster j starts at
+ * slot cut_slot[j] of unit cut_unit[j] and ends where cluster j + 1 starts
+ * (cut 0 is (0, 0), cut nc is (units, 0)).  A unit cut inside (cut_slot > 0)
+ * is shared by the clusters whose ranges meet it; its last range runs to its
+ * occupied count, whatever that is at launch time.  The host takes a plan when
+ * its cost model says the ranges balance better than whole units and every
+ * sequence of the layer holds at least 2048 tokens by the host's count of
+ * prompts, decode steps and compressions (the counts only steer the plan, the
+ * results do not depend on it).
+ *   cut_unit, cut_slot  host [max_cuts], filled when a plan is returned (may be
+ *                       NULL: only the return value)
+ * Returns 0 or nc, or a negative lf_status (LF_ERR_ARG: bad layer, or
+ * max_cuts < nc + 1).  Reads host state only: no device work, no allocation.
+ */
+int lf_launch_plan(lf_cache* cache, int layer, int32_t* cut_unit, int32_t* cut_slot,
+                   int max_cuts);
 
 /*
  * Prefill without any device allocation.  (No counterpart on the pages: this

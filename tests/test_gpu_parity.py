@@ -229,70 +229,154 @@ def test_degenerate_budgets(kernel, budget, cluster):
     assert st.evictions == 40 * wl.kv_heads - (budget - 1) * wl.kv_heads
 
 
-def test_split_launch_choice():
-    """The units left after the whole rounds are shared by two clusters exactly
-    when they fill at most half of the resident clusters (one two-CTA cluster per two SMs at
-    budget 3276): batch 32 x 8 KV heads leaves 256 mod 76 = 28 units, batch 64
-    leaves 56 and is not split.  The parity tests at the r1-llama-8b shape run
-    through the split kernel."""
+def _plan_items(plan, units):
+    """Per cluster of a launch plan: its items in the kernel's order, each
+    (unit, is_shared), and each shared unit's clusters."""
+    nc = len(plan) - 1
+    inner = {}
+    for q in range(1, nc):
+        u, s = plan[q]
+        if s > 0:
+            inner.setdefault(u, []).append(q)
+    items = []
+    for j in range(nc):
+        (u0, s0), (u1, s1) = plan[j], plan[j + 1]
+        it = []
+        if s0 > 0:
+            it.append((u0, True))
+        if s1 > 0 and not (s0 > 0 and u1 == u0):
+            it.append((u1, True))
+        it += [(w, False) for w in range((u0 + 1) if s0 > 0 else u0, u1)]
+        items.append(it)
+    parts = {u: list(range(qs[0] - 1, qs[-1] + 1)) for u, qs in inner.items()}
+    return items, parts
+
+
+def _check_plan(plan, units, nc):
+    assert len(plan) == nc + 1 and plan[0] == (0, 0) and plan[-1] == (units, 0)
+    assert all(a <= b for a, b in zip(plan, plan[1:]))          # cuts never go back
+    assert all(s % 4 == 0 for _, s in plan)
+    items, parts = _plan_items(plan, units)
+    seen = sorted(u for it in items for u, _ in it)
+    assert set(seen) == set(range(units))                        # every unit visited
+    whole = [u for it in items for u, sh in it if not sh]
+    assert len(whole) == len(set(whole)) and not set(whole) & set(parts)
+    return items, parts
+
+
+def test_planned_launch_choice():
+    """A layer whose sequences all hold >= 2048 tokens takes a launch plan when
+    the host's cost model prefers it to whole units: batch 32 and batch 4 at
+    budget 3276 on two-CTA clusters do (units shared by two clusters, and by
+    three or more).  The plan cuts the layer into one contiguous range per
+    cluster that covers every unit.  An empty layer, and a cache with the
+    deferred order or the H2O score, never take one."""
     from decode_kv_cache_gb300.longflow import LFCache
     clusters = torch.cuda.get_device_properties(0).multi_processor_count // 2
-    for batch in (32, 64):
-        cache = LFCache(1, batch, 8, 32, 128, 3276, 64)
+    for batch in (32, 4):
+        cache = LFCache(2, batch, 8, 32, 128, 3276, 64)
         try:
             lay = cache.layout
-            assert lay.cluster == 2
-            rem = (batch * 8) % clusters
-            want = rem if 0 < rem and 2 * rem <= clusters else 0
-            assert lay.split_units == want, (batch, lay.split_units, want)
+            assert lay.cluster == 2 and lay.split_units == clusters
+            assert cache.plan(0) is None                          # empty
+            k = torch.zeros(batch, 8, 3276, 128, dtype=torch.bfloat16, device="cuda")
+            cache.prefill(0, k, k, [3276] * batch)
+            plan = cache.plan(0)
+            assert plan is not None and cache.plan(1) is None
+            items, parts = _check_plan(plan, batch * 8, clusters)
+            widest = max(len(p) for p in parts.values())
+            assert widest >= (3 if batch == 4 else 2), widest
+            assert max(sum(sh for _, sh in it) for it in items) <= 2
         finally:
             cache.close()
-    # the deferred order and the H2O score are never split
-    cache = LFCache(1, 32, 8, 32, 128, 3276, 64, deferred=True)
-    try:
-        assert cache.layout.split_units == 0
-    finally:
-        cache.close()
+    for kw in (dict(deferred=True), dict(score="h2o"), dict(scope="layer")):
+        cache = LFCache(1, 32, 8, 32, 128, 3276, 64, **kw)
+        try:
+            assert cache.layout.split_units == 0 and cache.plan(0) is None
+        finally:
+            cache.close()
 
 
-def test_split_launch_transition_with_policy():
-    """r1-llama-8b's launch shape (256 units; 28 are shared by two clusters at
-    the steps where every sequence holds >= 2048 tokens): a prompt of 2038, so
-    the first 10 steps run unsplit and the rest split, here with the l2 norm
-    and 4 sinks; sampled units among the shared ones and in whole rounds."""
+def test_planned_launch_transition_with_policy():
+    """r1-llama-8b's launch shape (256 units): a prompt of 2038, so the first
+    10 steps run whole units and the rest take a plan, here with the l2 norm
+    and 4 sinks; sampled units among the shared ones and whole ones."""
     import oracle
     wl = WORKLOADS["r1-llama-8b"].scaled(prefill=2038)
-    st = _run(wl, 60, layers=(1,), sample=[(0, 31, 7), (0, 29, 0), (0, 2, 3)],
-              policy=oracle.Policy(norm=2, sinks=4))
-    assert st.unit_steps == 60 * 3
+    run = ParityRun(wl, layers=(1,), sample=[(0, 31, 7), (0, 29, 0), (0, 2, 3), (0, 13, 4)],
+                    policy=oracle.Policy(norm=2, sinks=4))
+    try:
+        for t in range(60):
+            assert (run.cache.plan(0) is None) == (t < 10), t
+            run.step()
+        run.compare_state()
+        run.check_invariants()
+        run.stats.assert_ok()
+        assert run.stats.unit_steps == 60 * 4
+    finally:
+        run.close()
+
+
+@pytest.mark.parametrize("batch,budgets", [(4, None), (24, (2048, 3276, 2560))])
+def test_planned_launch_parity(batch, budgets):
+    """Planned launches at full head geometry: batch 4 (32 units on 76 clusters,
+    so every unit is shared by three or more clusters, up to 16 CTAs) and a
+    ragged batch of budgets 2048 / 3276 / 2560, all full, every step evicts.
+    Every unit is replayed by the oracle."""
+    wl = WORKLOADS["r1-llama-8b"].scaled(batch=batch, prefill=3276)
+    bud = [budgets[b % len(budgets)] for b in range(batch)] if budgets else None
+    run = ParityRun(wl, layers=(0,), budgets=bud)
+    try:
+        plan = run.cache.plan(0)
+        assert plan is not None
+        _check_plan(plan, batch * 8, len(plan) - 1)
+        run.run(40)
+        run.compare_state()
+        run.check_invariants()
+        st = run.stats
+        print(f"\nparity planned b{batch}: {st.unit_steps} unit-steps, {st.evictions} evictions, "
+              f"{st.near_ties} near-ties, {st.resyncs} resyncs, {len(st.hard_mismatches)} "
+              f"mismatches, max output error {st.max_out_violation:.3f} of tolerance")
+        st.assert_ok()
+        assert st.evictions == 40 * batch * 8
+    finally:
+        run.close()
 
 
 def test_split_exchange_timeout_recovers():
-    """A split launch whose exchange can never complete: the wait gives up after
-    its bound, the unit skips the step (state, count and position unchanged,
-    evicted = -1), LF_DEVERR_TIMEOUT is reported, lf_cache_check zeroes the
-    counters, and the context stays usable.  The failure is made on the host: the
-    first exchange's arrival count of shared unit 0 is set so low that the
-    arrivals never reach the target.  Batch 12 on 2-CTA clusters: 96 units on 76
-    clusters, the 20 left over shared.  Shared unit 0 is (sequence 9, KV head 4),
-    the first item of clusters 0 and 1.  A CTA whose wait ran out skips the rest
-    of its launch, so their second items, whole units 0 and 1, skip the step
-    too; every other unit matches the oracle."""
+    """A planned launch whose exchange through global memory can never
+    complete: the waits give up after their bound, the shared unit skips the
+    step (state, count and position unchanged, evicted = -1),
+    LF_DEVERR_TIMEOUT is reported, lf_cache_check zeroes the counters, and the
+    context stays usable.  The failure is made on the host: the first
+    exchange's arrival count of one shared unit is set so low that the arrivals
+    never reach the target.  Batch 12 at budget 3276 on 2-CTA clusters takes a
+    plan (96 units cut into one range per cluster).  A CTA whose wait ran out
+    skips the rest of its launch, so the items after the shared unit in its
+    cluster's list skip the step too; every other unit matches the oracle."""
     import time
     from decode_kv_cache_gb300.longflow import LF_DEVERR_TIMEOUT
     wl = WORKLOADS["r1-llama-8b"].scaled(layers=1, batch=12, prefill=3276)
-    nc = torch.cuda.get_device_properties(0).multi_processor_count // 2
     units = wl.batch * wl.kv_heads
-    rounds, rem = divmod(units, nc)
-    assert rounds >= 1 and 0 < 2 * rem <= nc
-    bad = divmod(rounds * nc, wl.kv_heads)  # shared unit 0
-    skipped = [bad] + [divmod(j + r * nc, wl.kv_heads) for j in (0, 1) for r in range(rounds)]
+    probe = ParityRun(wl, layers=(0,), sample=[(0, 0, 0)], cluster=2)
+    try:
+        plan = probe.cache.plan(0)
+    finally:
+        probe.close()
+    assert plan is not None
+    items, parts = _check_plan(plan, units, len(plan) - 1)
+    bad_unit = min(parts)                      # the first shared unit
+    xi = parts[bad_unit][1]                    # its exchange row: its first inner cut
+    skipped_units = {bad_unit}
+    for j in parts[bad_unit]:
+        it = [u for u, _ in items[j]]
+        skipped_units.update(it[it.index(bad_unit):])
+    skipped = [divmod(u, wl.kv_heads) for u in sorted(skipped_units)]
     sample = [(0, b, g) for b in range(wl.batch) for g in range(wl.kv_heads)
               if (b, g) not in skipped]
     run = ParityRun(wl, layers=(0,), sample=sample, cluster=2)
     try:
-        lay = run.cache.layout
-        assert lay.cluster == 2 and lay.split_units == rem
+        assert run.cache.layout.cluster == 2 and run.cache.plan(0) == plan
         run.run(3)
         assert run.cache.check() == 0
         vw = run.views
@@ -300,7 +384,7 @@ def test_split_exchange_timeout_recovers():
         assert int(cnt.abs().sum()) == 0
         names = ("k", "v", "vnorm", "pos", "count", "next_pos")
         before = {(bg, n): vw[n][0][bg].clone() for bg in skipped for n in names}
-        cnt[0, 0] = -(1 << 20)
+        cnt[xi, 0] = -(1 << 20)
         torch.cuda.synchronize()
         t0 = time.monotonic()
         run.step(check=True)  # every sampled unit against the oracle as usual

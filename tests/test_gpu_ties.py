@@ -1,6 +1,6 @@
 """The tie rule on the GPU: an exact tie of the lowest score goes to the lowest
 slot index, wherever the tied slots sit -- in one CTA, in different CTAs of a
-cluster, or in the two clusters that share a unit in a split launch.
+cluster, or in different clusters that share a unit in a planned launch.
 
 The rule comes from the guide ("LongFlow Guide: KV Cache Compression for
 Reasoning AI"), section "Static Memory Pre-Allocation and In-Place Eviction",
@@ -92,27 +92,42 @@ def test_exact_ties_go_to_the_lowest_slot(kernel, cluster):
         run.close()
 
 
-def test_exact_ties_split_launch():
-    """Batch 32 at budget 3276 on two-CTA clusters: the 28 units left after the
-    whole rounds are each shared by two clusters (four pieces), which exchange
-    their lowest (score, slot) through global memory.  Tied slots sit on both
-    sides of every piece boundary -- inside one CTA, across the two CTAs of a
-    cluster, and across the two clusters."""
+def test_exact_ties_planned_launch():
+    """Batch 32 at budget 3276 on two-CTA clusters takes a launch plan: the
+    layer is cut into one contiguous range per cluster, and a unit cut inside
+    is shared by the clusters whose ranges meet it, which exchange their lowest
+    (score, slot) through global memory.  Tied slots sit on both sides of the
+    cuts of three shared units and of the CTA boundaries inside their parts --
+    inside one CTA, across the CTAs of a cluster, and across clusters."""
+    from test_gpu_parity import _check_plan
     wl = WORKLOADS["r1-llama-8b"].scaled(layers=1, prefill=3276)
-    nc = torch.cuda.get_device_properties(0).multi_processor_count // 2
     units = wl.batch * wl.kv_heads
-    rem = units % nc
-    first_shared = units - rem
-    shared = [divmod(u, wl.kv_heads) for u in (first_shared, first_shared + 1, units - 1)]
-    whole = [(0, 0), (13, 6)]
-    slots = _tie_slots(wl.budget, 4, wl.window)
-    steps = len(slots) + 2
-    run, seen = _tie_run(wl, slots, steps, sample=[(0, b, g) for b, g in shared + whole])
+    probe = ParityRun(wl, layers=(0,), sample=[(0, 0, 0)])
     try:
-        lay = run.cache.layout
-        assert lay.cluster == 2 and lay.split_units == rem > 0
+        plan = probe.cache.plan(0)
+        C = probe.cache.layout.cluster
+    finally:
+        probe.close()
+    assert plan is not None
+    _, parts = _check_plan(plan, units, len(plan) - 1)
+    shared = sorted(parts)[:3]
+    slots = {3, 5}
+    for u in shared:
+        bounds = [0] + [plan[q][1] for q in parts[u][1:]] + [wl.budget]
+        for lo, hi in zip(bounds, bounds[1:]):
+            per = ((hi - lo + C - 1) // C + 3) & ~3
+            for x in (lo - 1, lo, lo + per - 1, lo + per):
+                slots.add(x)
+    top = wl.budget - wl.window - 1
+    slots = sorted(x for x in slots if 0 <= x < top)
+    steps = len(slots) + 2
+    sample = [(0,) + divmod(u, wl.kv_heads) for u in shared] + [(0, 0, 0), (0, 13, 6)]
+    run, seen = _tie_run(wl, slots, steps, sample=sample)
+    try:
+        assert run.cache.plan(0) == plan
         for t, s in enumerate(slots):
             assert bool((seen[t] == s).all()), (t, s, seen[t].unique().tolist())
+        assert run.stats.exact_ties == len(sample) * (len(slots) - 1)
     finally:
         run.close()
 

@@ -29,9 +29,11 @@ ClusterModel adds the exchanges between the CTAs of a cluster (clusters of 1,
 (m, l) to every CTA, then its partial output to the unit's leader.  Each
 transfer checks that it lands in the phase it is meant for and that the
 receiving buffer is no longer read; a planted single statistics buffer fails
-that check.  For split launches the model puts a shared unit first, exchanged
-through global memory (taken as immediate here: the other cluster is not
-modelled), and checks the whole units' corrected phase indices.
+that check.  For planned launches the model puts one or two shared units
+first, exchanged through global memory (taken as immediate here: the other
+clusters are not modelled, and a shared unit uses neither the statistics
+receive buffers nor their barriers), and checks the whole units' corrected
+phase indices.
 """
 import random
 
@@ -248,13 +250,14 @@ class ClusterModel:
     (finb, a single buffer).  Each transfer checks that the receiving buffer
     is free: the receiver has finished the unit that last used it."""
 
-    def __init__(self, occupied, cluster, stages, lookahead, mistake=None, shared_first=False):
+    def __init__(self, occupied, cluster, stages, lookahead, mistake=None, shared=0):
         self.n = occupied
         self.C = cluster
         self.mistake = mistake    # a planted protocol error (tests of the model itself)
-        # split launch: item 0 is a unit shared with another cluster, exchanged through
-        # global memory (modelled as immediate); it uses neither statb nor finb
-        self.shared = shared_first
+        # planned launch: items 0 .. shared-1 are units shared with other clusters,
+        # exchanged through global memory (modelled as immediate); they use neither
+        # statb nor finb nor the statistics receive buffers
+        self.shared = shared
         self.count = {}
         self.ctas = []
         for r in range(cluster):
@@ -277,33 +280,36 @@ class ClusterModel:
             for k in range(len(self.n)):
                 b2 = k & 1
                 yield ("statrdy", b2, k >> 1)
-                if self.shared and k == 0:
-                    yield ("handoff", 0, 0)
-                    self.stats_read[r] = 0
+                if k < self.shared:
+                    yield ("handoff", b2, k >> 1)
                     self.tail_done[r] += 1
-                    m.arrive("taildone", 0)
+                    m.arrive("taildone", b2)
                     continue
-                # the shared item completed no statb / finb phase: the phase index of
+                # the shared items completed no statb / finb phase: the phase index of
                 # a whole unit counts only the whole units before it
-                fix = self.shared and self.mistake != "uncorrected_phases"
+                npc = self.shared if self.mistake != "uncorrected_phases" else 0
                 # exchange 1: arm this parity's receive barrier, send (m, l) to all
                 if self.mistake == "one_statistics_buffer":
-                    sb, sp, gap = 0, k, 1      # (planted) one buffer for every unit
+                    sb, sp, prev = 0, k, k - 1      # (planted) one buffer for every unit
                 else:
-                    sb, sp, gap = b2, (k >> 1) - (1 if fix and b2 == 0 else 0), 2
+                    k0 = npc + ((k - npc) & 1)     # first whole item of this parity
+                    sb, sp, prev = b2, (k - k0) >> 1, k - 2
                 self.statb[(r, sb)].arm(sp)
                 for dst in range(C):
-                    assert self.stats_read[dst] >= k - gap, "statistics buffer still in use"
+                    # the buffer's previous user (a whole unit) has been read at dst
+                    assert prev < self.shared or self.stats_read[dst] >= prev, \
+                        "statistics buffer still in use"
                     self.statb[(dst, sb)].land(sp)
                 yield ("statb", sb, sp)
                 self.stats_read[r] = k
                 yield ("handoff", b2, k >> 1)          # the partial output is read
                 # exchange 2: partial output and lowest candidate to the leader
-                leader = k % C
-                fp = k // C - (1 if fix and leader == 0 else 0)
+                leader = (k - npc) % C
+                fp = (k - npc) // C
                 if r == leader:
                     self.finb[r].arm(fp)
-                assert k < C or self.tail_done[leader] >= k - C + 1, "output buffer still in use"
+                assert k - npc < C or self.tail_done[leader] >= k - C + 1, \
+                    "output buffer still in use"
                 self.finb[leader].land(fp)
                 if r == leader:
                     yield ("finb", 0, fp)
@@ -434,18 +440,22 @@ def test_cluster_model_catches_a_single_statistics_buffer():
     assert caught > 0
 
 
-@pytest.mark.parametrize("cluster", [1, 2])
-def test_split_launch_phase_indices(cluster):
-    """Split launches put a unit shared with another cluster first; it is
-    exchanged through global memory, so it completes no statb / finb phase.
-    The whole units' phase indices subtract it (the kernel's stat_phase and
-    fin_phase): the model runs clean with that correction, and without it a
-    transfer lands in the wrong phase."""
-    rng = random.Random(90 + cluster)
+@pytest.mark.parametrize("cluster,shared", [(1, 1), (2, 1), (2, 2), (4, 2)])
+def test_planned_launch_phase_indices(cluster, shared):
+    """Planned launches put the one or two units a cluster shares with other
+    clusters first; they are exchanged through global memory, so they complete
+    no statb / finb phase and use no statistics receive buffer.  The whole
+    units' phase indices and leaders count only the whole units (the kernel's
+    stat_phase, fin_phase and leader): the model runs clean with that, and
+    without it a transfer lands in the wrong phase."""
+    rng = random.Random(90 + 10 * cluster + shared)
     for _ in range(150):
-        occupied = [rng.randint(1, 3276) for _ in range(rng.randint(2, 9))]
-        m = ClusterModel(occupied, cluster, 3, 2, shared_first=True)
-        assert m.run(rng)[0] == "done", occupied
+        occupied = [rng.randint(1, 3276) for _ in range(rng.randint(shared + 1, 9))]
+        m = ClusterModel(occupied, cluster, 3, 2, shared=shared)
+        status, waits = m.run(rng)
+        assert status == "done", (occupied, waits)
+        assert m.tail_done == [len(occupied)] * cluster
     with pytest.raises(AssertionError):
-        ClusterModel([3276] * 5, cluster, 3, 2, shared_first=True,
-                     mistake="uncorrected_phases").run(random.Random(0))
+        for seed in range(20):
+            ClusterModel([3276] * 6, cluster, 3, 2, shared=shared,
+                         mistake="uncorrected_phases").run(random.Random(seed))
