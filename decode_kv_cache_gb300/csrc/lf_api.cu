@@ -92,70 +92,88 @@ constexpr int kPlanMinSlots = LF_PLAN_MIN_SLOTS;
 constexpr long long kItemCost = LF_PLAN_ITEM_COST;
 constexpr long long kPartCost = LF_PLAN_PART_COST;
 
-// Cut one layer's (unit, slot) order into nc contiguous ranges of about equal
-// cost (n[u] = the unit's occupied slots, c = CTAs per cluster), at multiples
-// of `gran` slots inside a unit; parts shorter than `snap` go whole to one side.
-// Fills cut_unit / cut_slot [nc + 1].  Returns the largest range's cost, or -1
-// if some cluster would visit more than max_items items or a unit would be
-// shared by more than lf::kMaxSplitParts CTAs.
-long long make_plan(const std::vector<int32_t>& n, int c, int nc, int max_items, int* cut_unit,
-                    int* cut_slot) {
+// A launch plan: every cluster takes `rounds` whole units round-robin (the
+// units below rounds * nc), and each unit past them is cut into parts, at most
+// one per cluster and as its first item, so that all parts of a unit start
+// together.  Its parts go to the clusters with the least whole-unit load, sized
+// to even out the clusters' loads (at least one tile per CTA each).
+struct Plan {
+  int rounds;
+  int unit[lf::kTcMaxPlan], lo[lf::kTcMaxPlan], hi[lf::kTcMaxPlan], info[lf::kTcMaxPlan];
+};
+
+// Fills `pl` for units of n[u] occupied slots on nc clusters of c CTAs; returns
+// the costliest cluster's cost (CTA slot rows), or -1 when no plan applies.
+long long make_plan(const std::vector<int32_t>& n, int c, int nc, int max_items, Plan* pl) {
   const int units = (int)n.size();
-  const long long gran = (long long)lf::kTcTile * c, snap = 2 * gran;
-  const long long ov = kItemCost * c;  // a unit boundary, in slots of the cluster
-  long long total = 0;
-  for (int u = 0; u < units; ++u) total += n[u] + ov;
-  cut_unit[0] = 0;
-  cut_slot[0] = 0;
-  cut_unit[nc] = units;
-  cut_slot[nc] = 0;
-  int u = 0;
-  long long before = 0;  // cost of units [0, u)
-  for (int j = 1; j < nc; ++j) {
-    const long long t = total * j / nc;
-    while (u < units && before + n[u] + ov <= t) before += n[u++] + ov;
-    int cu = u, cs = 0;
-    if (u < units) {
-      const long long off = ((t - before - ov) / gran) * gran;
-      if (off >= snap && n[u] - off >= snap) cs = (int)off;
-      else if (off >= snap) cu = u + 1;  // the unit's tail is short: it stays whole on the left
+  const int rounds = units / nc, rem = units - rounds * nc;
+  if (rem == 0 || nc > lf::kTcMaxPlan || rounds + 1 > max_items) return -1;
+  const long long gran = 32LL * c;  // cut points: multiples of 32 slots per CTA
+  const long long least = (long long)lf::kTcTile * c;  // a part: at least one tile per CTA
+  std::vector<long long> load((size_t)nc, 0);  // whole-unit cost per cluster
+  for (int j = 0; j < nc; ++j)
+    for (int k = 0; k < rounds; ++k) load[j] += (n[j + k * nc] + c - 1) / c + kItemCost;
+  // Parts per shared unit: the clusters shared out over the units (larger
+  // units first), each part at least one tile per CTA, at most
+  // kMaxSplitParts CTAs per unit.
+  std::vector<int> order((size_t)rem), parts((size_t)rem, 1);
+  for (int i = 0; i < rem; ++i) order[i] = i;
+  std::stable_sort(order.begin(), order.end(), [&](int a, int b) {
+    return n[rounds * nc + a] > n[rounds * nc + b];
+  });
+  int spare = nc - rem;
+  for (bool grew = true; spare > 0 && grew;) {
+    grew = false;
+    for (int x = 0; x < rem && spare > 0; ++x) {
+      const int i = order[x];
+      const long long nn = n[rounds * nc + i];
+      if ((parts[i] + 1) * c <= lf::kMaxSplitParts && nn >= (long long)(parts[i] + 1) * least) {
+        ++parts[i];
+        --spare;
+        grew = true;
+      }
     }
-    // cuts never go backwards
-    if (cu < cut_unit[j - 1] || (cu == cut_unit[j - 1] && cs < cut_slot[j - 1])) {
-      cu = cut_unit[j - 1];
-      cs = cut_slot[j - 1];
-    }
-    cut_unit[j] = cu;
-    cut_slot[j] = cs;
   }
-  // Cost of every range, as the kernel will visit it.
+  // Clusters by whole-unit load, least first; the largest units take them first.
+  std::vector<int> cl((size_t)nc);
+  for (int j = 0; j < nc; ++j) cl[j] = j;
+  std::stable_sort(cl.begin(), cl.end(), [&](int a, int b) { return load[a] < load[b]; });
+  pl->rounds = rounds;
+  for (int j = 0; j < nc; ++j) pl->unit[j] = -1;
   long long worst = 0;
-  for (int j = 0; j < nc; ++j) {
-    const int u0 = cut_unit[j], s0 = cut_slot[j], u1 = cut_unit[j + 1], s1 = cut_slot[j + 1];
-    long long cost = 0;
-    int items = 0;
-    auto parts_of = [&](int uu) {  // clusters sharing unit uu: 1 + its inner cuts
-      int k = 1;
-      for (int q = 1; q < nc; ++q) k += (cut_unit[q] == uu && cut_slot[q] > 0) ? 1 : 0;
-      return k;
-    };
-    if (s0 > 0) {
-      const long long hi = (u1 == u0) ? s1 : n[u0];
-      cost += (std::max(0LL, hi - s0) + c - 1) / c + kItemCost + kPartCost;
-      ++items;
-      if (parts_of(u0) * c > lf::kMaxSplitParts) return -1;
+  int next = 0;
+  for (int x = 0; x < rem; ++x) {
+    const int i = order[x];
+    const int u = rounds * nc + i;
+    const int k = parts[i];
+    std::vector<int> grp(cl.begin() + next, cl.begin() + next + k);
+    next += k;
+    std::sort(grp.begin(), grp.end());
+    // Level the loads: part sizes (in slots) so that load + part / c is equal.
+    long long sum = 0;
+    for (int j : grp) sum += load[j];
+    const double level = (double)(sum + (n[u] + c - 1) / c + k * (kItemCost + kPartCost)) / k;
+    long long lo = 0;
+    for (int q = 0; q < k; ++q) {
+      const int j = grp[q];
+      long long hi;
+      if (q == k - 1) {
+        hi = INT_MAX;
+      } else {
+        const double want = (level - load[j] - kItemCost - kPartCost) * c;
+        hi = lo + std::max(0LL, (long long)(want / gran) * gran);
+        hi = std::min(hi, (long long)n[u] / gran * gran);
+      }
+      pl->unit[j] = u;
+      pl->lo[j] = (int)lo;
+      pl->hi[j] = (int)hi;
+      pl->info[j] = (i << 16) | (q << 8) | k;
+      const long long len = std::max(0LL, std::min(hi, (long long)n[u]) - lo);
+      worst = std::max(worst, load[j] + (len + c - 1) / c + kItemCost + kPartCost);
+      lo = std::min(hi, (long long)n[u]);
     }
-    if (s1 > 0 && !(s0 > 0 && u1 == u0)) {
-      cost += ((long long)std::min(s1, n[u1]) + c - 1) / c + kItemCost + kPartCost;
-      ++items;
-      if (parts_of(u1) * c > lf::kMaxSplitParts) return -1;
-    }
-    const int w0 = (s0 > 0) ? u0 + 1 : u0;
-    for (int w = w0; w < u1; ++w) cost += (n[w] + c - 1) / c + kItemCost;
-    items += std::max(0, u1 - w0);
-    if (items > max_items) return -1;
-    worst = std::max(worst, cost);
   }
+  for (int j = 0; j < nc; ++j) worst = std::max(worst, load[j]);
   return worst;
 }
 
@@ -244,10 +262,10 @@ int encode_tensor_maps(lf_cache* c, size_t n_rows) {
   return LF_OK;
 }
 
-// The plan of the next decode step of `layer`: true, with cut_unit / cut_slot
-// [grid_y + 1] filled, when its ranges cost less than whole units (cost model
-// above) and every sequence is long enough for the exchanges to pay.
-bool plan_layer(lf_cache* c, int layer, int* cut_unit, int* cut_slot) {
+// The plan of the next decode step of `layer`: true, with `pl` filled, when it
+// costs less than whole units (cost model above) and every sequence is long
+// enough for the exchanges to pay.
+bool plan_layer(lf_cache* c, int layer, Plan* pl) {
   if (!c->plan_ok) return false;
   const int32_t* occ = c->occ.data() + (size_t)layer * c->batch;
   int shortest = INT_MAX;
@@ -257,7 +275,7 @@ bool plan_layer(lf_cache* c, int layer, int* cut_unit, int* cut_slot) {
   }
   if (shortest < kPlanMinSlots) return false;
   const long long rr = round_robin_cost(c->plan_n, c->cluster, c->grid_y);
-  const long long pc = make_plan(c->plan_n, c->cluster, c->grid_y, c->items, cut_unit, cut_slot);
+  const long long pc = make_plan(c->plan_n, c->cluster, c->grid_y, c->items, pl);
   return pc >= 0 && pc < rr;
 }
 
@@ -836,8 +854,18 @@ int lf_decode_step(lf_cache* cache, int layer, const void* q, const void* k_new,
     ta.split_stat = cache->split_stat;
     ta.split_fin = cache->split_fin;
     ta.split_cnt = cache->split_cnt;
-    const bool planned = plan_layer(cache, layer, ta.cut_unit, ta.cut_slot);
-    if (planned) ta.plan_nc = cache->grid_y;
+    Plan pl;
+    const bool planned = plan_layer(cache, layer, &pl);
+    if (planned) {
+      ta.plan_nc = cache->grid_y;
+      ta.plan_rounds = pl.rounds;
+      for (int j = 0; j < cache->grid_y; ++j) {
+        ta.piece_unit[j] = pl.unit[j];
+        ta.piece_lo[j] = pl.lo[j];
+        ta.piece_hi[j] = pl.hi[j];
+        ta.piece_info[j] = pl.info[j];
+      }
+    }
     void* args[] = {&ta};
     e = cudaLaunchKernelExC(&cfg, planned ? cache->kern.decode_split : cache->kern.decode, args);
   } else {
@@ -933,22 +961,25 @@ int lf_cache_check(lf_cache* cache, lf_stream_t stream, int32_t* bits) {
   return LF_OK;
 }
 
-int lf_launch_plan(lf_cache* cache, int layer, int32_t* cut_unit, int32_t* cut_slot,
-                   int max_cuts) {
+int lf_launch_plan(lf_cache* cache, int layer, int32_t* rounds, int32_t* part_unit,
+                   int32_t* part_lo, int32_t* part_hi, int max_clusters) {
   clear_last();
   if (!cache) return fail(LF_ERR_ARG, "null cache");
   if (layer < 0 || layer >= cache->layers)
     return fail(LF_ERR_ARG, "layer %d outside [0, %d)", layer, cache->layers);
-  int cu[lf::kTcMaxPlan + 1], cs[lf::kTcMaxPlan + 1];
-  if (!plan_layer(cache, layer, cu, cs)) return 0;
+  Plan pl;
+  if (!plan_layer(cache, layer, &pl)) return 0;
   const int nc = cache->grid_y;
-  if (cut_unit && cut_slot) {
-    if (max_cuts < nc + 1) return fail(LF_ERR_ARG, "max_cuts %d < %d", max_cuts, nc + 1);
-    for (int j = 0; j <= nc; ++j) {
-      cut_unit[j] = cu[j];
-      cut_slot[j] = cs[j];
+  if (part_unit || part_lo || part_hi) {
+    if (!part_unit || !part_lo || !part_hi || max_clusters < nc)
+      return fail(LF_ERR_ARG, "need part_unit, part_lo, part_hi of >= %d entries", nc);
+    for (int j = 0; j < nc; ++j) {
+      part_unit[j] = pl.unit[j];
+      part_lo[j] = pl.lo[j];
+      part_hi[j] = pl.hi[j];
     }
   }
+  if (rounds) *rounds = pl.rounds;
   return nc;
 }
 

@@ -73,55 +73,26 @@ struct TcArgs {
   DecodeArgs a;
   int row_base;                    // tensor row of this layer's first slot
   int max_items;                   // units one cluster may visit (sizes the item table)
-  // Planned launches (kernel instantiated with kSplit).  The host cuts the
-  // layer's (unit, slot) order, units in index order and slots in order within
-  // a unit, into one contiguous range per cluster: cluster j starts at slot
-  // cut_slot[j] of unit cut_unit[j] and ends where cluster j + 1 starts (cut
-  // plan_nc is (units, 0)).  A unit cut inside (cut_slot > 0) is shared by the
-  // clusters whose ranges meet it; they exchange through global memory (all are
-  // co-resident: the grid is persistent).  Its last range runs to the unit's
-  // occupied count at launch time, so any plan covers every slot.
+  // Planned launches (kernel instantiated with kSplit).  Cluster j takes the
+  // whole units j, j + plan_nc, ... below plan_rounds * plan_nc, and first, if
+  // piece_unit[j] >= 0, the slots [piece_lo[j], piece_hi[j]) of that unit (one
+  // of the units past the whole rounds), clipped to its occupied count at
+  // launch time.  A unit cut into parts is shared by the clusters holding them;
+  // every part is its cluster's first item, so all of them start together, and
+  // they exchange through global memory (all clusters are co-resident: the grid
+  // is persistent).
   int plan_nc;                     // clusters of the plan (gridDim.y); 0: whole units
+  int plan_rounds;                 // whole units per cluster
   float* split_stat;               // [plan_nc][kMaxSplitParts][2 kMaxGroup]: (m_h, l_h) per part
   float* split_fin;                // [plan_nc][kMaxSplitParts][G D + 4]: partial output,
                                    //   score, slot, flag per part
   int* split_cnt;                  // [plan_nc][2]: arrivals at the two exchanges
-  int cut_unit[kTcMaxPlan + 1];
-  int cut_slot[kTcMaxPlan + 1];    // multiples of 4
+  int piece_unit[kTcMaxPlan];      // -1: no part
+  int piece_lo[kTcMaxPlan];        // multiples of 4
+  int piece_hi[kTcMaxPlan];        // INT_MAX: to the occupied count
+  int piece_info[kTcMaxPlan];      // exchange row << 16 | index among the unit's clusters
+                                   //   << 8 | clusters sharing the unit
 };
-
-// A shared unit's part held by one cluster of a planned launch.
-struct TcPiece {
-  int unit, lo, hi;  // slots [lo, hi) of the unit (hi = INT_MAX: to its occupied count)
-  int xi;            // exchange slot: the first cut inside the unit
-  int mc;            // this cluster's index among the unit's clusters (0 leads)
-  int ncl;           // clusters sharing the unit
-};
-
-// The parts of the units cut at cluster j's two range ends (start, then end),
-// and its whole units [*w0, *w1).  Returns the number of parts (0-2).
-__device__ __forceinline__ int plan_pieces(const TcArgs& ta, int j, TcPiece* pc, int* w0,
-                                           int* w1) {
-  const int nc = ta.plan_nc;
-  const int u0 = ta.cut_unit[j], s0 = ta.cut_slot[j];
-  const int u1 = ta.cut_unit[j + 1], s1 = ta.cut_slot[j + 1];
-  auto inner = [&](int c, int u) { return c >= 1 && c < nc && ta.cut_unit[c] == u && ta.cut_slot[c] > 0; };
-  int np = 0;
-  if (s0 > 0) {  // the range starts inside unit u0
-    int jmin = j, jmax = j;
-    while (inner(jmin - 1, u0)) --jmin;
-    while (inner(jmax + 1, u0)) ++jmax;
-    pc[np++] = {u0, s0, (u1 == u0) ? s1 : INT_MAX, jmin, j - jmin + 1, jmax - jmin + 2};
-  }
-  if (s1 > 0 && !(s0 > 0 && u1 == u0)) {  // it ends inside unit u1 and holds the unit's slot 0
-    int jmax = j + 1;
-    while (inner(jmax + 1, u1)) ++jmax;
-    pc[np++] = {u1, 0, s1, j + 1, 0, jmax - j + 1};
-  }
-  *w0 = (s0 > 0) ? u0 + 1 : u0;
-  *w1 = max(*w0, u1);
-  return np;
-}
 
 // Split launches: spin, with a bound, until another CTA of this persistent grid
 // (all of them are resident) has counted itself in.
@@ -217,18 +188,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int chunk = a.chunk;
   const int units = a.batch * a.kv_heads;
   // Whole-unit launches: cluster j takes units j, j + NC, ...  Planned
-  // launches: the parts of the units shared at its range ends first (so that
-  // every cluster sharing a unit starts on it together and the exchanges
-  // through L2 overlap the stream of the items after it), then its whole units
-  // in order.
-  TcPiece pcs[2];
-  int npc = 0, w0 = 0, w1 = 0;
-  if (kSplit && ta.plan_nc == NC) npc = plan_pieces(ta, j, pcs, &w0, &w1);
+  // launches: its part of a shared unit first (so that every cluster sharing
+  // the unit starts on it together and the exchanges through L2 overlap the
+  // stream of the whole units after it), then plan_rounds whole units.
   const bool planned = kSplit && ta.plan_nc == NC;
-  const int nitems = planned ? npc + (w1 - w0) : ((j < units) ? (units - j + NC - 1) / NC : 0);
+  const int npc = (planned && ta.piece_unit[j] >= 0) ? 1 : 0;  // a shared unit's part first
+  const int nitems = planned ? npc + ta.plan_rounds
+                             : ((j < units) ? (units - j + NC - 1) / NC : 0);
   if (nitems > ta.max_items || (kSplit && !planned) ||
-      (npc > 0 && pcs[0].ncl * C > kMaxSplitParts) ||
-      (npc > 1 && pcs[1].ncl * C > kMaxSplitParts)) {
+      (npc > 0 && (ta.piece_info[j] & 0xff) * C > kMaxSplitParts)) {
     // the host sized the item table for fewer units, or the plan does not fit
     if (threadIdx.x == 0 && cg::this_cluster().block_rank() == 0) atomicOr(ta.a.err, LF_DEVERR_STATE);
     return;
@@ -337,15 +305,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // every part has sent its partial output, so all of them have read it.)
   for (int k = tid; k < nitems; k += kTcThreads) {
     int u, lo = 0, hi = INT_MAX, part = 0;
-    if (!planned) {
-      u = j + k * NC;
-    } else if (k < npc) {
-      u = pcs[k].unit;
-      lo = pcs[k].lo;
-      hi = pcs[k].hi;
-      part = (pcs[k].xi << 16) | (pcs[k].mc << 8) | pcs[k].ncl;  // xi >= 1: never 0
+    if (k < npc) {
+      u = ta.piece_unit[j];
+      lo = ta.piece_lo[j];
+      hi = ta.piece_hi[j];
+      part = ta.piece_info[j];  // the low byte (clusters sharing the unit) is >= 1: never 0
     } else {
-      u = w0 + (k - npc);
+      u = j + (k - npc) * NC;
     }
     int* it = items + kTcItemInts * k;
     it[0] = a.count[u];
@@ -867,9 +833,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (is_piece(k)) {
           // ---- a unit shared with other clusters (a planned launch): both
           // exchanges go through global memory, counted by atomics.  The parts
-          // are the CTAs of the clusters whose ranges meet the unit, in cluster
-          // then rank order; part 0 leads.  Only the per-KV-head LongFlow score
-          // and the append modes are planned (host). ----
+          // are the CTAs of the clusters sharing the unit, in the order of the
+          // clusters' parts then rank; part 0 leads.  Only the per-KV-head
+          // LongFlow score and the append modes are planned (host). ----
           const int part = items[kTcItemInts * k + 7];
           const int xi = part >> 16;                      // exchange slot
           const int np = (part & 0xff) * C;               // parts (<= kMaxSplitParts)

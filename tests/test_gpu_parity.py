@@ -229,39 +229,30 @@ def test_degenerate_budgets(kernel, budget, cluster):
     assert st.evictions == 40 * wl.kv_heads - (budget - 1) * wl.kv_heads
 
 
-def _plan_items(plan, units):
-    """Per cluster of a launch plan: its items in the kernel's order, each
-    (unit, is_shared), and each shared unit's clusters."""
-    nc = len(plan) - 1
-    inner = {}
-    for q in range(1, nc):
-        u, s = plan[q]
-        if s > 0:
-            inner.setdefault(u, []).append(q)
-    items = []
-    for j in range(nc):
-        (u0, s0), (u1, s1) = plan[j], plan[j + 1]
-        it = []
-        if s0 > 0:
-            it.append((u0, True))
-        if s1 > 0 and not (s0 > 0 and u1 == u0):
-            it.append((u1, True))
-        it += [(w, False) for w in range((u0 + 1) if s0 > 0 else u0, u1)]
-        items.append(it)
-    parts = {u: list(range(qs[0] - 1, qs[-1] + 1)) for u, qs in inner.items()}
-    return items, parts
+INT32_MAX = 2**31 - 1
 
 
 def _check_plan(plan, units, nc):
-    assert len(plan) == nc + 1 and plan[0] == (0, 0) and plan[-1] == (units, 0)
-    assert all(a <= b for a, b in zip(plan, plan[1:]))          # cuts never go back
-    assert all(s % 4 == 0 for _, s in plan)
-    items, parts = _plan_items(plan, units)
-    seen = sorted(u for it in items for u, _ in it)
-    assert set(seen) == set(range(units))                        # every unit visited
-    whole = [u for it in items for u, sh in it if not sh]
-    assert len(whole) == len(set(whole)) and not set(whole) & set(parts)
-    return items, parts
+    """A launch plan (lf_launch_plan) covers the layer: every cluster takes
+    `rounds` whole units round-robin, every unit past them is cut into parts
+    held by distinct clusters that cover it in order.  Returns the clusters
+    holding each shared unit's parts, in part order."""
+    rounds, parts = plan
+    assert len(parts) == nc and rounds * nc < units
+    held = {}
+    for j, p in enumerate(parts):
+        if p is not None:
+            u, lo, hi = p
+            assert rounds * nc <= u < units and lo % 4 == 0 and lo <= hi
+            held.setdefault(u, []).append((lo, hi, j))
+    assert set(held) == set(range(rounds * nc, units))          # every unit past the rounds
+    out = {}
+    for u, ps in held.items():
+        ps.sort()
+        assert ps[0][0] == 0 and ps[-1][1] == INT32_MAX            # from slot 0 to the end
+        assert all(a[1] == b[0] for a, b in zip(ps, ps[1:]))       # contiguous
+        out[u] = [j for _, _, j in ps]
+    return out
 
 
 def test_planned_launch_choice():
@@ -274,7 +265,7 @@ def test_planned_launch_choice():
     from decode_kv_cache_gb300.longflow import LFCache
     clusters = torch.cuda.get_device_properties(0).multi_processor_count // 2
     for batch in (32, 4):
-        cache = LFCache(2, batch, 8, 32, 128, 3276, 64)
+        cache = LFCache(2, batch, 8, 32, 128, 3276, 64, cluster=2)
         try:
             lay = cache.layout
             assert lay.cluster == 2 and lay.split_units == clusters
@@ -283,12 +274,20 @@ def test_planned_launch_choice():
             cache.prefill(0, k, k, [3276] * batch)
             plan = cache.plan(0)
             assert plan is not None and cache.plan(1) is None
-            items, parts = _check_plan(plan, batch * 8, clusters)
-            widest = max(len(p) for p in parts.values())
-            assert widest >= (3 if batch == 4 else 2), widest
-            assert max(sum(sh for _, sh in it) for it in items) <= 2
+            shared = _check_plan(plan, batch * 8, clusters)
+            widest = max(len(p) for p in shared.values())
+            assert widest >= 3, widest
         finally:
             cache.close()
+    # 64 sequences: 512 units on 76 clusters; with at most one part per cluster
+    # no plan beats 7 whole units on the busiest cluster
+    cache = LFCache(1, 64, 8, 32, 128, 3276, 64)
+    try:
+        k = torch.zeros(64, 8, 3276, 128, dtype=torch.bfloat16, device="cuda")
+        cache.prefill(0, k, k, [3276] * 64)
+        assert cache.plan(0) is None
+    finally:
+        cache.close()
     for kw in (dict(deferred=True), dict(score="h2o"), dict(scope="layer")):
         cache = LFCache(1, 32, 8, 32, 128, 3276, 64, **kw)
         try:
@@ -325,11 +324,12 @@ def test_planned_launch_parity(batch, budgets):
     Every unit is replayed by the oracle."""
     wl = WORKLOADS["r1-llama-8b"].scaled(batch=batch, prefill=3276)
     bud = [budgets[b % len(budgets)] for b in range(batch)] if budgets else None
-    run = ParityRun(wl, layers=(0,), budgets=bud)
+    run = ParityRun(wl, layers=(0,), budgets=bud, cluster=2)
     try:
         plan = run.cache.plan(0)
         assert plan is not None
-        _check_plan(plan, batch * 8, len(plan) - 1)
+        shared = _check_plan(plan, batch * 8, len(plan[1]))
+        assert max(len(p) for p in shared.values()) >= (3 if batch == 4 else 2)
         run.run(40)
         run.compare_state()
         run.check_invariants()
@@ -351,9 +351,10 @@ def test_split_exchange_timeout_recovers():
     context stays usable.  The failure is made on the host: the first
     exchange's arrival count of one shared unit is set so low that the arrivals
     never reach the target.  Batch 12 at budget 3276 on 2-CTA clusters takes a
-    plan (96 units cut into one range per cluster).  A CTA whose wait ran out
-    skips the rest of its launch, so the items after the shared unit in its
-    cluster's list skip the step too; every other unit matches the oracle."""
+    plan (one whole round of 76 units, the other 20 units each cut into parts
+    held by three or four clusters).  A CTA whose wait ran out skips the rest
+    of its launch, so the whole units after the shared unit in its
+    cluster skip the step too; every other unit matches the oracle."""
     import time
     from decode_kv_cache_gb300.longflow import LF_DEVERR_TIMEOUT
     wl = WORKLOADS["r1-llama-8b"].scaled(layers=1, batch=12, prefill=3276)
@@ -361,16 +362,17 @@ def test_split_exchange_timeout_recovers():
     probe = ParityRun(wl, layers=(0,), sample=[(0, 0, 0)], cluster=2)
     try:
         plan = probe.cache.plan(0)
+        nc = probe.cache.layout.split_units
     finally:
         probe.close()
     assert plan is not None
-    items, parts = _check_plan(plan, units, len(plan) - 1)
-    bad_unit = min(parts)                      # the first shared unit
-    xi = parts[bad_unit][1]                    # its exchange row: its first inner cut
+    rounds = plan[0]
+    shared = _check_plan(plan, units, nc)
+    bad_unit = rounds * nc                     # the first shared unit
+    xi = bad_unit - rounds * nc                # its exchange row
     skipped_units = {bad_unit}
-    for j in parts[bad_unit]:
-        it = [u for u, _ in items[j]]
-        skipped_units.update(it[it.index(bad_unit):])
+    for j in shared[bad_unit]:                 # the clusters holding its parts skip their
+        skipped_units.update(j + k * nc for k in range(rounds))   # whole units after it
     skipped = [divmod(u, wl.kv_heads) for u in sorted(skipped_units)]
     sample = [(0, b, g) for b in range(wl.batch) for g in range(wl.kv_heads)
               if (b, g) not in skipped]

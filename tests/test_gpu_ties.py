@@ -93,12 +93,13 @@ def test_exact_ties_go_to_the_lowest_slot(kernel, cluster):
 
 
 def test_exact_ties_planned_launch():
-    """Batch 32 at budget 3276 on two-CTA clusters takes a launch plan: the
-    layer is cut into one contiguous range per cluster, and a unit cut inside
-    is shared by the clusters whose ranges meet it, which exchange their lowest
-    (score, slot) through global memory.  Tied slots sit on both sides of the
-    cuts of three shared units and of the CTA boundaries inside their parts --
-    inside one CTA, across the CTAs of a cluster, and across clusters."""
+    """Batch 32 at budget 3276 on two-CTA clusters takes a launch plan: three
+    whole rounds, and each of the 28 units past them cut into two or three
+    parts held by different clusters, which exchange their lowest (score,
+    slot) through global memory.  Tied slots sit on both sides of the part
+    boundaries of three shared units and of the CTA boundaries inside their
+    parts -- inside one CTA, across the CTAs of a cluster, and across
+    clusters."""
     from test_gpu_parity import _check_plan
     wl = WORKLOADS["r1-llama-8b"].scaled(layers=1, prefill=3276)
     units = wl.batch * wl.kv_heads
@@ -106,22 +107,24 @@ def test_exact_ties_planned_launch():
     try:
         plan = probe.cache.plan(0)
         C = probe.cache.layout.cluster
+        nc = probe.cache.layout.split_units
     finally:
         probe.close()
     assert plan is not None
-    _, parts = _check_plan(plan, units, len(plan) - 1)
-    shared = sorted(parts)[:3]
+    held = _check_plan(plan, units, nc)
+    chosen = sorted(held, key=lambda u: -len(held[u]))[:2] + [max(held)]
     slots = {3, 5}
-    for u in shared:
-        bounds = [0] + [plan[q][1] for q in parts[u][1:]] + [wl.budget]
-        for lo, hi in zip(bounds, bounds[1:]):
+    for u in chosen:
+        for j in held[u]:
+            _, lo, hi = plan[1][j]
+            hi = min(hi, wl.budget)
             per = ((hi - lo + C - 1) // C + 3) & ~3
             for x in (lo - 1, lo, lo + per - 1, lo + per):
                 slots.add(x)
     top = wl.budget - wl.window - 1
     slots = sorted(x for x in slots if 0 <= x < top)
     steps = len(slots) + 2
-    sample = [(0,) + divmod(u, wl.kv_heads) for u in shared] + [(0, 0, 0), (0, 13, 6)]
+    sample = [(0,) + divmod(u, wl.kv_heads) for u in chosen] + [(0, 0, 0), (0, 13, 6)]
     run, seen = _tie_run(wl, slots, steps, sample=sample)
     try:
         assert run.cache.plan(0) == plan

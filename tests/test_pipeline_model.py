@@ -29,11 +29,11 @@ ClusterModel adds the exchanges between the CTAs of a cluster (clusters of 1,
 (m, l) to every CTA, then its partial output to the unit's leader.  Each
 transfer checks that it lands in the phase it is meant for and that the
 receiving buffer is no longer read; a planted single statistics buffer fails
-that check.  For planned launches the model puts one or two shared units
-first, exchanged through global memory (taken as immediate here: the other
-clusters are not modelled, and a shared unit uses neither the statistics
-receive buffers nor their barriers), and checks the whole units' corrected
-phase indices.
+that check.  For planned launches the model puts a cluster's part of a shared
+unit first, exchanged through global memory (taken as immediate here: the
+other clusters are not modelled, and a shared unit uses neither the
+statistics receive buffers nor their barriers), and checks the whole units'
+corrected phase indices.
 """
 import random
 
@@ -440,14 +440,15 @@ def test_cluster_model_catches_a_single_statistics_buffer():
     assert caught > 0
 
 
-@pytest.mark.parametrize("cluster,shared", [(1, 1), (2, 1), (2, 2), (4, 2)])
+@pytest.mark.parametrize("cluster,shared", [(1, 1), (2, 1), (4, 1), (2, 2)])
 def test_planned_launch_phase_indices(cluster, shared):
-    """Planned launches put the one or two units a cluster shares with other
-    clusters first; they are exchanged through global memory, so they complete
-    no statb / finb phase and use no statistics receive buffer.  The whole
-    units' phase indices and leaders count only the whole units (the kernel's
-    stat_phase, fin_phase and leader): the model runs clean with that, and
-    without it a transfer lands in the wrong phase."""
+    """Planned launches put a cluster's part of a shared unit first; it is
+    exchanged through global memory, so it completes no statb / finb phase
+    and uses no statistics receive buffer.  The whole units' phase indices
+    and leaders count only the whole units (the kernel's stat_phase,
+    fin_phase and leader): the model runs clean with that, and without it a
+    transfer lands in the wrong phase.  (Two shared items, which the host
+    never plans, are covered too: the indices are written for any count.)"""
     rng = random.Random(90 + 10 * cluster + shared)
     for _ in range(150):
         occupied = [rng.randint(1, 3276) for _ in range(rng.randint(shared + 1, 9))]
