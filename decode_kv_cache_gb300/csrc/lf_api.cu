@@ -167,9 +167,9 @@ long long make_plan(const std::vector<int32_t>& n, int c, int nc, int max_items,
       pl->unit[j] = u;
       pl->lo[j] = (int)lo;
       pl->hi[j] = (int)hi;
-      pl->info[j] = (i << 16) | (q << 8) | k;
+      pl->info[j] = (i << 16) | (q << 8) | k;  // k = 1: a whole unit, first
       const long long len = std::max(0LL, std::min(hi, (long long)n[u]) - lo);
-      worst = std::max(worst, load[j] + (len + c - 1) / c + kItemCost + kPartCost);
+      worst = std::max(worst, load[j] + (len + c - 1) / c + kItemCost + (k > 1 ? kPartCost : 0));
       lo = std::min(hi, (long long)n[u]);
     }
   }
@@ -468,7 +468,7 @@ lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, i
   const int stages = c.stages ? c.stages : (tc ? 3 : 4);
   // The shared memory, resident clusters and item-table size of one cluster size;
   // false if it does not fit.
-  int chunk = 0, smem = 0, grid_y = 0, items = 0;
+  int chunk = 0, smem = 0, grid_y = 0, items = 0, resident = 0;
   auto try_shape = [&](int cl) -> bool {
     chunk = (int)round_up((size_t)((capacity + cl - 1) / cl), 4);
     int fits = 0;
@@ -486,6 +486,7 @@ lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, i
         smem = std::max(smem, max_sm_smem / 2 + 1024);
         fits = (smem <= max_optin) ? active_clusters(kern.decode, cl, 1, 1, smem, threads) : 0;
         if (fits <= 0) break;
+        resident = fits;
         grid_y = std::min(fits, units);
         const int need = (units + grid_y - 1) / grid_y + 2;
         if (need <= items) break;
@@ -588,8 +589,13 @@ lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, i
   if (tc) {
     const bool plain = !kevict || (c.score == LF_SCORE_LONGFLOW && c.scope == LF_SCOPE_KV_HEAD &&
                                    !c.deferred);
-    if (plain && kern.decode_split && grid_y <= lf::kTcMaxPlan && 2 * cluster <= lf::kMaxSplitParts)
+    if (plain && kern.decode_split && resident <= lf::kTcMaxPlan &&
+        2 * cluster <= lf::kMaxSplitParts) {
       cache->plan_ok = 1;
+      // every resident cluster, also when there are fewer units: a plan cuts
+      // units into parts for the clusters a whole-unit launch would leave idle
+      cache->grid_y = resident;
+    }
   }
   cache->score = c.score;
   cache->norm = c.norm;

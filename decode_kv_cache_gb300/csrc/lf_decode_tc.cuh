@@ -192,8 +192,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // the unit starts on it together and the exchanges through L2 overlap the
   // stream of the whole units after it), then plan_rounds whole units.
   const bool planned = kSplit && ta.plan_nc == NC;
-  const int npc = (planned && ta.piece_unit[j] >= 0) ? 1 : 0;  // a shared unit's part first
-  const int nitems = planned ? npc + ta.plan_rounds
+  // a unit past the whole rounds, first: shared (a part), or whole (one part)
+  const int nfirst = (planned && ta.piece_unit[j] >= 0) ? 1 : 0;
+  const int npc = (nfirst && (ta.piece_info[j] & 0xff) > 1) ? 1 : 0;  // items exchanged via L2
+  const int nitems = planned ? nfirst + ta.plan_rounds
                              : ((j < units) ? (units - j + NC - 1) / NC : 0);
   if (nitems > ta.max_items || (kSplit && !planned) ||
       (npc > 0 && (ta.piece_info[j] & 0xff) * C > kMaxSplitParts)) {
@@ -305,13 +307,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // every part has sent its partial output, so all of them have read it.)
   for (int k = tid; k < nitems; k += kTcThreads) {
     int u, lo = 0, hi = INT_MAX, part = 0;
-    if (k < npc) {
+    if (k < nfirst) {
       u = ta.piece_unit[j];
-      lo = ta.piece_lo[j];
-      hi = ta.piece_hi[j];
-      part = ta.piece_info[j];  // the low byte (clusters sharing the unit) is >= 1: never 0
+      if (npc) {
+        lo = ta.piece_lo[j];
+        hi = ta.piece_hi[j];
+        part = ta.piece_info[j];  // the low byte (clusters sharing the unit) is >= 2: never 0
+      }
     } else {
-      u = j + (k - npc) * NC;
+      u = j + (k - nfirst) * NC;
     }
     int* it = items + kTcItemInts * k;
     it[0] = a.count[u];
