@@ -81,99 +81,121 @@ void clear_last() {
 constexpr int kPlanMinSlots = LF_PLAN_MIN_SLOTS;
 
 // Host cost model of one launch, in CTA slot rows (one row of K and V streamed
-// by one CTA, ~11.5 ns at the HBM rate): every item a CTA visits adds a unit
+// by one CTA, ~12.5 ns in a steady launch): every item a CTA visits adds a unit
 // boundary, and every part of a shared unit adds its two exchanges through L2.
+// Measured at batch 64 on 2-CTA clusters (512 units of 3276 slots on 76
+// clusters): a plan of 6.74 units and two parts per cluster took 146.6 us per
+// launch against 149.5 us for 7 whole units, about 1.3 us (~100 rows) per part.
 #ifndef LF_PLAN_ITEM_COST
-#define LF_PLAN_ITEM_COST 64
+#define LF_PLAN_ITEM_COST 32
 #endif
 #ifndef LF_PLAN_PART_COST
-#define LF_PLAN_PART_COST 192
+#define LF_PLAN_PART_COST 64
 #endif
 constexpr long long kItemCost = LF_PLAN_ITEM_COST;
 constexpr long long kPartCost = LF_PLAN_PART_COST;
 
 // A launch plan: every cluster takes `rounds` whole units round-robin (the
-// units below rounds * nc), and each unit past them is cut into parts, at most
-// one per cluster and as its first item, so that all parts of a unit start
-// together.  Its parts go to the clusters with the least whole-unit load, sized
-// to even out the clusters' loads (at least one tile per CTA each).
+// units below rounds * nc), and before them one contiguous range of the units
+// past the whole rounds, cut so that the clusters' loads come out level (parts
+// first, so every cluster's parts start together and take about as long).
+// When those units are few, only as many clusters take ranges as keep every
+// shared unit within lf::kMaxSplitParts CTAs.
 struct Plan {
   int rounds;
-  int unit[lf::kTcMaxPlan], lo[lf::kTcMaxPlan], hi[lf::kTcMaxPlan], info[lf::kTcMaxPlan];
+  int cut_unit[lf::kTcMaxPlan + 1], cut_slot[lf::kTcMaxPlan + 1];
 };
 
 // Fills `pl` for units of n[u] occupied slots on nc clusters of c CTAs; returns
 // the costliest cluster's cost (CTA slot rows), or -1 when no plan applies.
 long long make_plan(const std::vector<int32_t>& n, int c, int nc, int max_items, Plan* pl) {
   const int units = (int)n.size();
-  const int rounds = units / nc, rem = units - rounds * nc;
-  if (rem == 0 || nc > lf::kTcMaxPlan || rounds + 1 > max_items) return -1;
-  const long long gran = 32LL * c;  // cut points: multiples of 32 slots per CTA
-  const long long least = (long long)lf::kTcTile * c;  // a part: at least one tile per CTA
-  std::vector<long long> load((size_t)nc, 0);  // whole-unit cost per cluster
+  const int rounds = units / nc, first = rounds * nc;
+  if (first == units || nc > lf::kTcMaxPlan) return -1;
+  const long long gran = 32LL * c;                      // cut points: 32 slots per CTA
+  const long long least = (long long)lf::kTcTile * c;   // parts: one tile per CTA at least
+  std::vector<long long> load((size_t)nc, 0);           // whole-unit cost per cluster
   for (int j = 0; j < nc; ++j)
     for (int k = 0; k < rounds; ++k) load[j] += (n[j + k * nc] + c - 1) / c + kItemCost;
-  // Parts per shared unit: the clusters shared out over the units (larger
-  // units first), each part at least one tile per CTA, at most
-  // kMaxSplitParts CTAs per unit.
-  std::vector<int> order((size_t)rem), parts((size_t)rem, 1);
-  for (int i = 0; i < rem; ++i) order[i] = i;
-  std::stable_sort(order.begin(), order.end(), [&](int a, int b) {
-    return n[rounds * nc + a] > n[rounds * nc + b];
-  });
-  int spare = nc - rem;
-  for (bool grew = true; spare > 0 && grew;) {
-    grew = false;
-    for (int x = 0; x < rem && spare > 0; ++x) {
-      const int i = order[x];
-      const long long nn = n[rounds * nc + i];
-      if ((parts[i] + 1) * c <= lf::kMaxSplitParts && nn >= (long long)(parts[i] + 1) * least) {
-        ++parts[i];
-        --spare;
-        grew = true;
-      }
-    }
+  long long total = 0, longest = 1;                     // slots past the whole rounds
+  for (int u = first; u < units; ++u) {
+    total += n[u];
+    longest = std::max(longest, (long long)n[u]);
   }
-  // Clusters by whole-unit load, least first; the largest units take them first.
-  std::vector<int> cl((size_t)nc);
-  for (int j = 0; j < nc; ++j) cl[j] = j;
-  std::stable_sort(cl.begin(), cl.end(), [&](int a, int b) { return load[a] < load[b]; });
+  // Ranges of at least `span` slots keep a unit within kMaxSplitParts / c clusters.
+  const int most = lf::kMaxSplitParts / c;
+  if (most < 2) return -1;
+  const long long span = (longest + most - 2) / (most - 1) + 2 * gran;
+  const int ncp = (int)std::max(1LL, std::min<long long>(nc, total / span));
+  // Level: range lengths f_j = c (level - load_j), at least 0, summing to `total`
+  // over the first ncp clusters.
+  double lo_l = 0, hi_l = 1e18;
+  for (int it = 0; it < 100; ++it) {
+    const double mid = 0.5 * (lo_l + hi_l);
+    double sum = 0;
+    for (int j = 0; j < ncp; ++j) sum += std::max(0.0, (mid - load[j]) * c);
+    (sum < total ? lo_l : hi_l) = mid;
+  }
+  // Cut points at the running sums, rounded to the grid and moved off short parts.
   pl->rounds = rounds;
-  for (int j = 0; j < nc; ++j) pl->unit[j] = -1;
-  long long worst = 0;
-  int next = 0;
-  for (int x = 0; x < rem; ++x) {
-    const int i = order[x];
-    const int u = rounds * nc + i;
-    const int k = parts[i];
-    std::vector<int> grp(cl.begin() + next, cl.begin() + next + k);
-    next += k;
-    std::sort(grp.begin(), grp.end());
-    // Level the loads: part sizes (in slots) so that load + part / c is equal.
-    long long sum = 0;
-    for (int j : grp) sum += load[j];
-    const double level = (double)(sum + (n[u] + c - 1) / c + k * (kItemCost + kPartCost)) / k;
-    long long lo = 0;
-    for (int q = 0; q < k; ++q) {
-      const int j = grp[q];
-      long long hi;
-      if (q == k - 1) {
-        hi = INT_MAX;
-      } else {
-        const double want = (level - load[j] - kItemCost - kPartCost) * c;
-        hi = lo + std::max(0LL, (long long)(want / gran) * gran);
-        hi = std::min(hi, (long long)n[u] / gran * gran);
-      }
-      pl->unit[j] = u;
-      pl->lo[j] = (int)lo;
-      pl->hi[j] = (int)hi;
-      pl->info[j] = (i << 16) | (q << 8) | k;  // k = 1: a whole unit, first
-      const long long len = std::max(0LL, std::min(hi, (long long)n[u]) - lo);
-      worst = std::max(worst, load[j] + (len + c - 1) / c + kItemCost + (k > 1 ? kPartCost : 0));
-      lo = std::min(hi, (long long)n[u]);
+  pl->cut_unit[0] = first;
+  pl->cut_slot[0] = 0;
+  double at = 0;
+  int u = first;
+  long long before = 0;  // slots of the units [first, u)
+  for (int j = 1; j <= nc; ++j) {
+    if (j >= ncp) {
+      pl->cut_unit[j] = units;
+      pl->cut_slot[j] = 0;
+      continue;
     }
+    at += std::max(0.0, (hi_l - load[j - 1]) * c);
+    const long long t = std::min((long long)at, total);
+    while (u < units && before + n[u] <= t) before += n[u++];
+    int cu = u, cs = 0;
+    if (u < units) {
+      const long long off = (t - before) / gran * gran;
+      if (off >= least && n[u] - off >= least) cs = (int)off;
+      else if (off >= least) cu = u + 1;  // the unit's tail is short: it stays on the left
+    }
+    if (cu < pl->cut_unit[j - 1] ||
+        (cu == pl->cut_unit[j - 1] && cs < pl->cut_slot[j - 1])) {  // never go back
+      cu = pl->cut_unit[j - 1];
+      cs = pl->cut_slot[j - 1];
+    }
+    pl->cut_unit[j] = cu;
+    pl->cut_slot[j] = cs;
   }
-  for (int j = 0; j < nc; ++j) worst = std::max(worst, load[j]);
+  // Check and cost every cluster as the kernel will run it.
+  auto parts_of = [&](int uu) {  // clusters sharing unit uu: 1 + its inner cuts
+    int k = 1;
+    for (int q = 1; q < nc; ++q) k += (pl->cut_unit[q] == uu && pl->cut_slot[q] > 0) ? 1 : 0;
+    return k;
+  };
+  long long worst = 0;
+  for (int j = 0; j < nc; ++j) {
+    const int u0 = pl->cut_unit[j], s0 = pl->cut_slot[j];
+    const int u1 = pl->cut_unit[j + 1], s1 = pl->cut_slot[j + 1];
+    long long cost = load[j];
+    int items = rounds;
+    if (s0 > 0) {
+      const long long hi = (u1 == u0) ? s1 : n[u0];
+      cost += (std::max(0LL, hi - s0) + c - 1) / c + kItemCost + kPartCost;
+      ++items;
+      if (parts_of(u0) * c > lf::kMaxSplitParts) return -1;
+    }
+    if (s1 > 0 && !(s0 > 0 && u1 == u0)) {
+      cost += ((long long)std::min(s1, n[u1]) + c - 1) / c + kItemCost + kPartCost;
+      ++items;
+      if (parts_of(u1) * c > lf::kMaxSplitParts) return -1;
+    }
+    for (int w = (s0 > 0) ? u0 + 1 : u0; w < u1; ++w) {  // units wholly inside the range
+      cost += (n[w] + c - 1) / c + kItemCost;
+      ++items;
+    }
+    if (items > max_items) return -1;
+    worst = std::max(worst, cost);
+  }
   return worst;
 }
 
@@ -865,11 +887,9 @@ int lf_decode_step(lf_cache* cache, int layer, const void* q, const void* k_new,
     if (planned) {
       ta.plan_nc = cache->grid_y;
       ta.plan_rounds = pl.rounds;
-      for (int j = 0; j < cache->grid_y; ++j) {
-        ta.piece_unit[j] = pl.unit[j];
-        ta.piece_lo[j] = pl.lo[j];
-        ta.piece_hi[j] = pl.hi[j];
-        ta.piece_info[j] = pl.info[j];
+      for (int j = 0; j <= cache->grid_y; ++j) {
+        ta.cut_unit[j] = pl.cut_unit[j];
+        ta.cut_slot[j] = pl.cut_slot[j];
       }
     }
     void* args[] = {&ta};
@@ -967,8 +987,8 @@ int lf_cache_check(lf_cache* cache, lf_stream_t stream, int32_t* bits) {
   return LF_OK;
 }
 
-int lf_launch_plan(lf_cache* cache, int layer, int32_t* rounds, int32_t* part_unit,
-                   int32_t* part_lo, int32_t* part_hi, int max_clusters) {
+int lf_launch_plan(lf_cache* cache, int layer, int32_t* rounds, int32_t* cut_unit,
+                   int32_t* cut_slot, int max_cuts) {
   clear_last();
   if (!cache) return fail(LF_ERR_ARG, "null cache");
   if (layer < 0 || layer >= cache->layers)
@@ -976,13 +996,12 @@ int lf_launch_plan(lf_cache* cache, int layer, int32_t* rounds, int32_t* part_un
   Plan pl;
   if (!plan_layer(cache, layer, &pl)) return 0;
   const int nc = cache->grid_y;
-  if (part_unit || part_lo || part_hi) {
-    if (!part_unit || !part_lo || !part_hi || max_clusters < nc)
-      return fail(LF_ERR_ARG, "need part_unit, part_lo, part_hi of >= %d entries", nc);
-    for (int j = 0; j < nc; ++j) {
-      part_unit[j] = pl.unit[j];
-      part_lo[j] = pl.lo[j];
-      part_hi[j] = pl.hi[j];
+  if (cut_unit || cut_slot) {
+    if (!cut_unit || !cut_slot || max_cuts < nc + 1)
+      return fail(LF_ERR_ARG, "need cut_unit and cut_slot of >= %d entries", nc + 1);
+    for (int j = 0; j <= nc; ++j) {
+      cut_unit[j] = pl.cut_unit[j];
+      cut_slot[j] = pl.cut_slot[j];
     }
   }
   if (rounds) *rounds = pl.rounds;

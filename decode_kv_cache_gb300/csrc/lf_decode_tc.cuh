@@ -74,25 +74,61 @@ struct TcArgs {
   int row_base;                    // tensor row of this layer's first slot
   int max_items;                   // units one cluster may visit (sizes the item table)
   // Planned launches (kernel instantiated with kSplit).  Cluster j takes the
-  // whole units j, j + plan_nc, ... below plan_rounds * plan_nc, and first, if
-  // piece_unit[j] >= 0, the slots [piece_lo[j], piece_hi[j]) of that unit (one
-  // of the units past the whole rounds), clipped to its occupied count at
-  // launch time.  A unit cut into parts is shared by the clusters holding them;
-  // every part is its cluster's first item, so all of them start together, and
-  // they exchange through global memory (all clusters are co-resident: the grid
-  // is persistent).
+  // whole units j, j + plan_nc, ... below plan_rounds * plan_nc, and before them
+  // one contiguous range of the units past the whole rounds (units in order,
+  // slots in order within a unit): from slot cut_slot[j] of unit cut_unit[j] to
+  // where cluster j + 1 starts (cut plan_nc is (units, 0)).  A unit cut inside
+  // (cut_slot > 0) is shared by the clusters whose ranges meet it; they exchange
+  // through global memory (all clusters are co-resident: the grid is
+  // persistent).  A cluster's parts (at most two: of the unit its range starts
+  // inside, then of the unit it ends inside) are its first items, then the
+  // units wholly inside its range, then its whole rounds.  The last part of a
+  // unit runs to the unit's occupied count at launch time.
   int plan_nc;                     // clusters of the plan (gridDim.y); 0: whole units
   int plan_rounds;                 // whole units per cluster
   float* split_stat;               // [plan_nc][kMaxSplitParts][2 kMaxGroup]: (m_h, l_h) per part
   float* split_fin;                // [plan_nc][kMaxSplitParts][G D + 4]: partial output,
                                    //   score, slot, flag per part
   int* split_cnt;                  // [plan_nc][2]: arrivals at the two exchanges
-  int piece_unit[kTcMaxPlan];      // -1: no part
-  int piece_lo[kTcMaxPlan];        // multiples of 4
-  int piece_hi[kTcMaxPlan];        // INT_MAX: to the occupied count
-  int piece_info[kTcMaxPlan];      // exchange row << 16 | index among the unit's clusters
-                                   //   << 8 | clusters sharing the unit
+  int cut_unit[kTcMaxPlan + 1];
+  int cut_slot[kTcMaxPlan + 1];    // multiples of 4
 };
+
+// One cluster's part of a shared unit in a planned launch.
+struct TcPiece {
+  int unit, lo, hi;  // slots [lo, hi) of the unit (hi = INT_MAX: to its occupied count)
+  int info;          // exchange row (its first inner cut) << 16 | index among the
+                     //   unit's clusters (0 leads) << 8 | clusters sharing the unit
+};
+
+// The parts of cluster j's range: of the unit it starts inside, then of the
+// unit it ends inside (one part when it lies inside a single unit); and the
+// units wholly inside it, [*w0, *w1).  Returns the number of parts (0-2).
+__device__ __forceinline__ int plan_pieces(const TcArgs& ta, int j, TcPiece* pc, int* w0,
+                                           int* w1) {
+  const int nc = ta.plan_nc;
+  const int u0 = ta.cut_unit[j], s0 = ta.cut_slot[j];
+  const int u1 = ta.cut_unit[j + 1], s1 = ta.cut_slot[j + 1];
+  auto inner = [&](int c, int u) {
+    return c >= 1 && c < nc && ta.cut_unit[c] == u && ta.cut_slot[c] > 0;
+  };
+  int np = 0;
+  if (s0 > 0) {  // the range starts inside unit u0
+    int jmin = j, jmax = j;
+    while (inner(jmin - 1, u0)) --jmin;
+    while (inner(jmax + 1, u0)) ++jmax;
+    pc[np++] = {u0, s0, (u1 == u0) ? s1 : INT_MAX,
+                (jmin << 16) | ((j - jmin + 1) << 8) | (jmax - jmin + 2)};
+  }
+  if (s1 > 0 && !(s0 > 0 && u1 == u0)) {  // it ends inside unit u1 and holds slot 0
+    int jmax = j + 1;
+    while (inner(jmax + 1, u1)) ++jmax;
+    pc[np++] = {u1, 0, s1, ((j + 1) << 16) | (jmax - j + 1)};
+  }
+  *w0 = (s0 > 0) ? u0 + 1 : u0;  // units wholly inside the range
+  *w1 = max(*w0, u1);
+  return np;
+}
 
 // Split launches: spin, with a bound, until another CTA of this persistent grid
 // (all of them are resident) has counted itself in.
@@ -188,17 +224,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int chunk = a.chunk;
   const int units = a.batch * a.kv_heads;
   // Whole-unit launches: cluster j takes units j, j + NC, ...  Planned
-  // launches: its part of a shared unit first (so that every cluster sharing
-  // the unit starts on it together and the exchanges through L2 overlap the
-  // stream of the whole units after it), then plan_rounds whole units.
+  // launches: its parts of shared units first (every cluster's range takes
+  // about as long, so the parts of a unit finish about together and the
+  // exchanges through L2 overlap the stream of the whole units after them),
+  // then the units wholly inside its range, then plan_rounds whole units.
   const bool planned = kSplit && ta.plan_nc == NC;
-  // a unit past the whole rounds, first: shared (a part), or whole (one part)
-  const int nfirst = (planned && ta.piece_unit[j] >= 0) ? 1 : 0;
-  const int npc = (nfirst && (ta.piece_info[j] & 0xff) > 1) ? 1 : 0;  // items exchanged via L2
-  const int nitems = planned ? nfirst + ta.plan_rounds
+  TcPiece pcs[2];
+  int w0 = 0, w1 = 0;
+  const int npc = planned ? plan_pieces(ta, j, pcs, &w0, &w1) : 0;  // parts, exchanged via L2
+  const int nitems = planned ? npc + (w1 - w0) + ta.plan_rounds
                              : ((j < units) ? (units - j + NC - 1) / NC : 0);
   if (nitems > ta.max_items || (kSplit && !planned) ||
-      (npc > 0 && (ta.piece_info[j] & 0xff) * C > kMaxSplitParts)) {
+      (npc > 0 && (pcs[0].info & 0xff) * C > kMaxSplitParts) ||
+      (npc > 1 && (pcs[1].info & 0xff) * C > kMaxSplitParts)) {
     // the host sized the item table for fewer units, or the plan does not fit
     if (threadIdx.x == 0 && cg::this_cluster().block_rank() == 0) atomicOr(ta.a.err, LF_DEVERR_STATE);
     return;
@@ -307,15 +345,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // every part has sent its partial output, so all of them have read it.)
   for (int k = tid; k < nitems; k += kTcThreads) {
     int u, lo = 0, hi = INT_MAX, part = 0;
-    if (k < nfirst) {
-      u = ta.piece_unit[j];
-      if (npc) {
-        lo = ta.piece_lo[j];
-        hi = ta.piece_hi[j];
-        part = ta.piece_info[j];  // the low byte (clusters sharing the unit) is >= 2: never 0
-      }
+    if (k < npc) {
+      u = pcs[k].unit;
+      lo = pcs[k].lo;
+      hi = pcs[k].hi;
+      part = pcs[k].info;  // the low byte (clusters sharing the unit) is >= 2: never 0
+    } else if (k < npc + (w1 - w0)) {
+      u = w0 + (k - npc);  // a unit wholly inside the range
     } else {
-      u = j + (k - nfirst) * NC;
+      u = j + (k - npc - (w1 - w0)) * NC;
     }
     int* it = items + kTcItemInts * k;
     it[0] = a.count[u];
@@ -837,8 +875,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (is_piece(k)) {
           // ---- a unit shared with other clusters (a planned launch): both
           // exchanges go through global memory, counted by atomics.  The parts
-          // are the CTAs of the clusters sharing the unit, in the order of the
-          // clusters' parts then rank; part 0 leads.  Only the per-KV-head
+          // are the CTAs of the clusters whose ranges meet the unit, in
+          // cluster then rank order; part 0 leads.  Only the per-KV-head
           // LongFlow score and the append modes are planned (host). ----
           const int part = items[kTcItemInts * k + 7];
           const int xi = part >> 16;                      // exchange slot

@@ -119,7 +119,7 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.lf_rkv_compress.restype = I
     lib.lf_rkv_compress.argtypes = [P, I, VP, VP]
     lib.lf_launch_plan.restype = I
-    lib.lf_launch_plan.argtypes = [P, I] + [ctypes.POINTER(ctypes.c_int32)] * 4 + [I]
+    lib.lf_launch_plan.argtypes = [P, I] + [ctypes.POINTER(ctypes.c_int32)] * 3 + [I]
     lib.lf_prefill_fill_noalloc.restype = I
     lib.lf_prefill_fill_noalloc.argtypes = [ctypes.POINTER(LFLayout), I, VP, VP,
                                             ctypes.POINTER(ctypes.c_int32), I, VP]
@@ -241,19 +241,18 @@ def lf_rkv_compress(handle, layer, q_obs, stream=None) -> int:
 
 def lf_launch_plan(handle, layer):
     """The next step's plan of `layer`: None (whole units j, j + nc, ... per
-    cluster), or (rounds, parts) with parts[j] = (unit, lo, hi) of cluster j's
-    part of a shared unit, or None (hi = 2**31 - 1: to the occupied count)."""
+    cluster), or (rounds, cuts) with cuts[j] = (unit, slot) where cluster j's
+    range of the units past the whole rounds starts (cuts[nc] = (units, 0))."""
     lib = load_library()
     n = 256
     rounds = ctypes.c_int32(0)
-    pu, plo, phi = ((ctypes.c_int32 * n)() for _ in range(3))
-    nc = lib.lf_launch_plan(handle, layer, ctypes.byref(rounds), pu, plo, phi, n)
+    cu, cs = ((ctypes.c_int32 * n)() for _ in range(2))
+    nc = lib.lf_launch_plan(handle, layer, ctypes.byref(rounds), cu, cs, n)
     if nc < 0:
         raise LFError(nc, lf_last_error())
     if nc == 0:
         return None
-    parts = [(int(pu[j]), int(plo[j]), int(phi[j])) if pu[j] >= 0 else None for j in range(nc)]
-    return int(rounds.value), parts
+    return int(rounds.value), [(int(cu[j]), int(cs[j])) for j in range(nc + 1)]
 
 
 def lf_cache_layout(handle) -> LFLayout:

@@ -272,8 +272,8 @@ typedef struct lf_layout {
                        lf_launch_plan): its resident clusters nc; 0 when steps never
                        take a plan (the policy or the kernel does not allow it) */
   int32_t* split_cnt; /* planned launches: [split_units][2] arrival counts of the two
-                       exchanges through global memory of a shared unit, at row
-                       (unit - rounds * nc) (see lf_launch_plan).  Zero between
+                       exchanges through global memory of a shared unit, at the row
+                       of its first inner cut (see lf_launch_plan).  Zero between
                        launches; lf_cache_check zeroes them after an expired wait.
                        NULL when split_units is 0 */
 } lf_layout;
@@ -289,23 +289,24 @@ int lf_cache_layout(const lf_cache* cache, lf_layout* out);
  * (return value 0) cluster j takes the whole units j, j + nc, j + 2 nc, ... of
  * the layer (unit u = sequence u / kv_heads, KV head u % kv_heads).  With a plan
  * (return value nc) cluster j takes the whole units j, j + nc, ... below
- * *rounds * nc and first, if part_unit[j] >= 0, the slots [part_lo[j],
- * part_hi[j]) of that unit (part_hi = INT32_MAX: to its occupied count at
- * launch time).  Such a unit, one of those from *rounds * nc on, is shared by
- * the clusters holding its parts, which cover it in cluster order and
- * exchange through global memory.  The host takes a plan when its cost model
- * says it balances the clusters better than whole units and every sequence of
- * the layer holds at least 2048 tokens by the host's count of prompts, decode
- * steps and compressions (the counts only steer the plan; results never depend
- * on it).
- *   rounds                       host, may be NULL
- *   part_unit, part_lo, part_hi  host [max_clusters], filled when a plan is
- *                                returned (all three NULL: not filled)
+ * *rounds * nc and, before them, one contiguous range of the units from
+ * *rounds * nc on (units in order, slots in order within a unit): from slot
+ * cut_slot[j] of unit cut_unit[j] to where cluster j + 1 starts (cut nc is
+ * (units, 0)).  A unit cut inside (cut_slot > 0) is shared by the clusters whose
+ * ranges meet it; they exchange through global memory, and its last range runs
+ * to its occupied count at launch time.  The host takes a plan when its cost
+ * model says it balances the clusters better than whole units and every
+ * sequence of the layer holds at least 2048 tokens by the host's count of
+ * prompts, decode steps and compressions (the counts only steer the plan;
+ * results never depend on it).
+ *   rounds              host, may be NULL
+ *   cut_unit, cut_slot  host [max_cuts], filled when a plan is returned (both
+ *                       NULL: not filled)
  * Returns 0 or nc, or a negative lf_status (LF_ERR_ARG: bad layer, or arrays
- * shorter than nc).  Reads host state only: no device work, no allocation.
+ * shorter than nc + 1).  Reads host state only: no device work, no allocation.
  */
-int lf_launch_plan(lf_cache* cache, int layer, int32_t* rounds, int32_t* part_unit,
-                   int32_t* part_lo, int32_t* part_hi, int max_clusters);
+int lf_launch_plan(lf_cache* cache, int layer, int32_t* rounds, int32_t* cut_unit,
+                   int32_t* cut_slot, int max_cuts);
 
 /*
  * Prefill without any device allocation.  (No counterpart on the pages: this

@@ -155,7 +155,7 @@ def test_null_handles(lib):
     assert lib.lf_prefill_fill(None, 0, None, None, None, 0, None) == lf.LF_ERR_ARG
     assert lib.lf_cache_layout(None, None) == lf.LF_ERR_ARG
     assert lib.lf_cache_check(None, None, None) == lf.LF_ERR_ARG
-    assert lib.lf_launch_plan(None, 0, None, None, None, None, 0) == lf.LF_ERR_ARG
+    assert lib.lf_launch_plan(None, 0, None, None, None, 0) == lf.LF_ERR_ARG
 
 
 def test_create_without_gpu_fails_cleanly(lib):

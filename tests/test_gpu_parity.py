@@ -229,39 +229,55 @@ def test_degenerate_budgets(kernel, budget, cluster):
     assert st.evictions == 40 * wl.kv_heads - (budget - 1) * wl.kv_heads
 
 
-INT32_MAX = 2**31 - 1
+def _plan_items(plan, units, nc):
+    """The items of every cluster of a launch plan (lf_launch_plan), in the
+    kernel's order: its parts of shared units (of the unit its range starts
+    inside, then of the unit it ends inside), the units wholly inside its
+    range, then its whole rounds.  Each item is (unit, shared)."""
+    rounds, cuts = plan
+    items = []
+    for j in range(nc):
+        (u0, s0), (u1, s1) = cuts[j], cuts[j + 1]
+        it = []
+        if s0 > 0:
+            it.append((u0, True))
+        if s1 > 0 and not (s0 > 0 and u1 == u0):
+            it.append((u1, True))
+        it += [(w, False) for w in range(u0 + 1 if s0 > 0 else u0, u1)]
+        it += [(j + k * nc, False) for k in range(rounds)]
+        items.append(it)
+    return items
 
 
 def _check_plan(plan, units, nc):
-    """A launch plan (lf_launch_plan) covers the layer: every cluster takes
-    `rounds` whole units round-robin, every unit past them is cut into parts
-    held by distinct clusters that cover it in order.  Returns the clusters
-    holding each shared unit's parts, in part order."""
-    rounds, parts = plan
-    assert len(parts) == nc and rounds * nc < units
-    held = {}
-    for j, p in enumerate(parts):
-        if p is not None:
-            u, lo, hi = p
-            assert rounds * nc <= u < units and lo % 4 == 0 and lo <= hi
-            held.setdefault(u, []).append((lo, hi, j))
-    assert set(held) == set(range(rounds * nc, units))          # every unit past the rounds
-    out = {}
-    for u, ps in held.items():
-        ps.sort()
-        assert ps[0][0] == 0 and ps[-1][1] == INT32_MAX            # from slot 0 to the end
-        assert all(a[1] == b[0] for a, b in zip(ps, ps[1:]))       # contiguous
-        out[u] = [j for _, _, j in ps]
-    return out
+    """A launch plan covers the layer once: whole rounds round-robin, then
+    contiguous ranges over the units past them, with cut points on 4-slot
+    boundaries.  Returns, per shared unit, the clusters holding its parts."""
+    rounds, cuts = plan
+    first = rounds * nc
+    assert len(cuts) == nc + 1 and cuts[0] == (first, 0) and cuts[-1] == (units, 0)
+    assert all(a <= b for a, b in zip(cuts, cuts[1:]))           # cuts never go back
+    assert all(s % 4 == 0 for _, s in cuts)
+    items = _plan_items(plan, units, nc)
+    whole = sorted(u for it in items for u, sh in it if not sh)
+    shared = {}
+    for j, it in enumerate(items):
+        for u, sh in it:
+            if sh:
+                shared.setdefault(u, []).append(j)
+    assert len(whole) == len(set(whole)) and not set(whole) & set(shared)
+    assert set(whole) | set(shared) == set(range(units))          # every unit, once
+    assert all(len(js) >= 2 and js == list(range(js[0], js[-1] + 1)) for js in shared.values())
+    return shared
 
 
 def test_planned_launch_choice():
     """A layer whose sequences all hold >= 2048 tokens takes a launch plan when
-    the host's cost model prefers it to whole units: batch 32 and batch 4 at
+    the host's cost model prefers it to whole units: batches 64, 32 and 4 at
     budget 3276 on two-CTA clusters do (units shared by two clusters, and by
-    three or more).  The plan cuts the layer into one contiguous range per
-    cluster that covers every unit.  An empty layer, and a cache with the
-    deferred order or the H2O score, never take one."""
+    three or more).  The plan covers every unit once.  An empty layer, and a
+    cache with the deferred order, the H2O score or the layer scope, never
+    takes one."""
     from decode_kv_cache_gb300.longflow import LFCache
     clusters = torch.cuda.get_device_properties(0).multi_processor_count // 2
     for batch in (32, 4):
@@ -279,13 +295,15 @@ def test_planned_launch_choice():
             assert widest >= 3, widest
         finally:
             cache.close()
-    # 64 sequences: 512 units on 76 clusters; with at most one part per cluster
-    # no plan beats 7 whole units on the busiest cluster
+    # 64 sequences: 512 units on 76 clusters, six whole rounds and the 56
+    # units past them cut into 76 ranges
     cache = LFCache(1, 64, 8, 32, 128, 3276, 64)
     try:
         k = torch.zeros(64, 8, 3276, 128, dtype=torch.bfloat16, device="cuda")
         cache.prefill(0, k, k, [3276] * 64)
-        assert cache.plan(0) is None
+        plan = cache.plan(0)
+        assert plan is not None and plan[0] == 6
+        _check_plan(plan, 512, clusters)
     finally:
         cache.close()
     for kw in (dict(deferred=True), dict(score="h2o"), dict(scope="layer")):
@@ -328,8 +346,8 @@ def test_planned_launch_parity(batch, budgets):
     try:
         plan = run.cache.plan(0)
         assert plan is not None
-        shared = _check_plan(plan, batch * 8, len(plan[1]))
-        assert max(len(p) for p in shared.values()) >= (3 if batch == 4 else 2)
+        shared = _check_plan(plan, batch * 8, len(plan[1]) - 1)
+        assert max(len(p) for p in shared.values()) >= 3
         run.run(40)
         run.compare_state()
         run.check_invariants()
@@ -351,10 +369,11 @@ def test_split_exchange_timeout_recovers():
     context stays usable.  The failure is made on the host: the first
     exchange's arrival count of one shared unit is set so low that the arrivals
     never reach the target.  Batch 12 at budget 3276 on 2-CTA clusters takes a
-    plan (one whole round of 76 units, the other 20 units each cut into parts
-    held by three or four clusters).  A CTA whose wait ran out skips the rest
-    of its launch, so the whole units after the shared unit in its
-    cluster skip the step too; every other unit matches the oracle."""
+    plan (one whole round of 76 units, the other 20 cut into 76 ranges, so
+    every one of them is shared by three to five clusters).  A CTA whose wait
+    ran out skips the rest of its launch, so the items after the shared unit
+    in its cluster's list skip the step too; every other unit matches the
+    oracle."""
     import time
     from decode_kv_cache_gb300.longflow import LF_DEVERR_TIMEOUT
     wl = WORKLOADS["r1-llama-8b"].scaled(layers=1, batch=12, prefill=3276)
@@ -366,13 +385,14 @@ def test_split_exchange_timeout_recovers():
     finally:
         probe.close()
     assert plan is not None
-    rounds = plan[0]
     shared = _check_plan(plan, units, nc)
-    bad_unit = rounds * nc                     # the first shared unit
-    xi = bad_unit - rounds * nc                # its exchange row
+    items = _plan_items(plan, units, nc)
+    bad_unit = min(shared)                     # the first shared unit
+    xi = shared[bad_unit][1]                   # its exchange row: its first inner cut
     skipped_units = {bad_unit}
-    for j in shared[bad_unit]:                 # the clusters holding its parts skip their
-        skipped_units.update(j + k * nc for k in range(rounds))   # whole units after it
+    for j in shared[bad_unit]:                 # the clusters holding its parts skip
+        it = [u for u, _ in items[j]]          # every item after it
+        skipped_units.update(it[it.index(bad_unit):])
     skipped = [divmod(u, wl.kv_heads) for u in sorted(skipped_units)]
     sample = [(0, b, g) for b in range(wl.batch) for g in range(wl.kv_heads)
               if (b, g) not in skipped]

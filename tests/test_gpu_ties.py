@@ -94,12 +94,11 @@ def test_exact_ties_go_to_the_lowest_slot(kernel, cluster):
 
 def test_exact_ties_planned_launch():
     """Batch 32 at budget 3276 on two-CTA clusters takes a launch plan: three
-    whole rounds, and each of the 28 units past them cut into two or three
-    parts held by different clusters, which exchange their lowest (score,
-    slot) through global memory.  Tied slots sit on both sides of the part
-    boundaries of three shared units and of the CTA boundaries inside their
-    parts -- inside one CTA, across the CTAs of a cluster, and across
-    clusters."""
+    whole rounds, and the 28 units past them cut into 76 ranges, so each is
+    shared by two to four clusters, which exchange their lowest (score, slot)
+    through global memory.  Tied slots sit on both sides of the cut points of
+    three shared units and of the CTA boundaries inside their parts -- inside
+    one CTA, across the CTAs of a cluster, and across clusters."""
     from test_gpu_parity import _check_plan
     wl = WORKLOADS["r1-llama-8b"].scaled(layers=1, prefill=3276)
     units = wl.batch * wl.kv_heads
@@ -111,13 +110,13 @@ def test_exact_ties_planned_launch():
     finally:
         probe.close()
     assert plan is not None
-    held = _check_plan(plan, units, nc)
-    chosen = sorted(held, key=lambda u: -len(held[u]))[:2] + [max(held)]
+    shared = _check_plan(plan, units, nc)
+    cuts = plan[1]
+    chosen = sorted(shared, key=lambda u: -len(shared[u]))[:2] + [max(shared)]
     slots = {3, 5}
     for u in chosen:
-        for j in held[u]:
-            _, lo, hi = plan[1][j]
-            hi = min(hi, wl.budget)
+        bounds = [0] + [cuts[q][1] for q in shared[u][1:]] + [wl.budget]
+        for lo, hi in zip(bounds, bounds[1:]):
             per = ((hi - lo + C - 1) // C + 3) & ~3
             for x in (lo - 1, lo, lo + per - 1, lo + per):
                 slots.add(x)
