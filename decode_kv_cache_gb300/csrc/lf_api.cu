@@ -648,7 +648,8 @@ lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, i
   size_t off_lwa = round_up(off_lwr + (layer ? lunits * 4 : 0), 256);
   // planned launches, per exchange slot (one per cluster): [kMaxSplitParts][2
   // kMaxGroup] statistics, [kMaxSplitParts][G d + 4] partial outputs, [2] counters
-  const size_t nxs = cache->plan_ok ? (size_t)grid_y : 0;
+  // (one row per cut point: cache->grid_y, every resident cluster)
+  const size_t nxs = cache->plan_ok ? (size_t)cache->grid_y : 0;
   const size_t nsp = nxs * lf::kMaxSplitParts;
   size_t off_sst = round_up(off_lwa + (layer ? lunits * 4 : 0), 256);
   size_t off_sfn = round_up(off_sst + nsp * 2 * lf::kMaxGroup * 4, 256);
@@ -1006,6 +1007,26 @@ int lf_launch_plan(lf_cache* cache, int layer, int32_t* rounds, int32_t* cut_uni
   }
   if (rounds) *rounds = pl.rounds;
   return nc;
+}
+
+int lf_launch_plan_for(const int32_t* occupancy, int units, int cluster, int clusters,
+                       int max_items, int32_t* rounds, int32_t* cut_unit, int32_t* cut_slot) {
+  clear_last();
+  if (!occupancy || units < 1 || cluster < 1 || clusters < 1 || clusters > lf::kTcMaxPlan ||
+      max_items < 1 || !rounds || !cut_unit || !cut_slot)
+    return fail(LF_ERR_ARG, "bad plan arguments (clusters <= %d)", lf::kTcMaxPlan);
+  std::vector<int32_t> n(occupancy, occupancy + units);
+  for (int u = 0; u < units; ++u)
+    if (n[u] < 0) return fail(LF_ERR_ARG, "occupancy[%d] < 0", u);
+  Plan pl;
+  const long long pc = make_plan(n, cluster, clusters, max_items, &pl);
+  if (pc < 0 || pc >= round_robin_cost(n, cluster, clusters)) return 0;
+  *rounds = pl.rounds;
+  for (int j = 0; j <= clusters; ++j) {
+    cut_unit[j] = pl.cut_unit[j];
+    cut_slot[j] = pl.cut_slot[j];
+  }
+  return clusters;
 }
 
 int lf_cache_layout(const lf_cache* cache, lf_layout* out) {

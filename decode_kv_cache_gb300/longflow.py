@@ -27,7 +27,7 @@ __all__ = [
     "lf_cache_create", "lf_cache_create_ex", "lf_cache_destroy", "lf_prefill_fill",
     "lf_decode_step", "lf_cache_check", "lf_cache_layout", "lf_last_error", "lf_last_status",
     "lf_abi_version",
-    "lf_prefill_fill_noalloc", "lf_rkv_compress", "lf_launch_plan",
+    "lf_prefill_fill_noalloc", "lf_rkv_compress", "lf_launch_plan", "lf_launch_plan_for",
     "LFCache",
 ]
 
@@ -120,6 +120,9 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.lf_rkv_compress.argtypes = [P, I, VP, VP]
     lib.lf_launch_plan.restype = I
     lib.lf_launch_plan.argtypes = [P, I] + [ctypes.POINTER(ctypes.c_int32)] * 3 + [I]
+    lib.lf_launch_plan_for.restype = I
+    lib.lf_launch_plan_for.argtypes = ([ctypes.POINTER(ctypes.c_int32)] + [I] * 4 +
+                                       [ctypes.POINTER(ctypes.c_int32)] * 3)
     lib.lf_prefill_fill_noalloc.restype = I
     lib.lf_prefill_fill_noalloc.argtypes = [ctypes.POINTER(LFLayout), I, VP, VP,
                                             ctypes.POINTER(ctypes.c_int32), I, VP]
@@ -248,6 +251,22 @@ def lf_launch_plan(handle, layer):
     rounds = ctypes.c_int32(0)
     cu, cs = ((ctypes.c_int32 * n)() for _ in range(2))
     nc = lib.lf_launch_plan(handle, layer, ctypes.byref(rounds), cu, cs, n)
+    if nc < 0:
+        raise LFError(nc, lf_last_error())
+    if nc == 0:
+        return None
+    return int(rounds.value), [(int(cu[j]), int(cs[j])) for j in range(nc + 1)]
+
+
+def lf_launch_plan_for(occupancy: Sequence[int], cluster: int, clusters: int, max_items: int):
+    """The planner on given per-unit occupancies: None or (rounds, cuts), as
+    lf_launch_plan returns them."""
+    lib = load_library()
+    occ = (ctypes.c_int32 * len(occupancy))(*[int(x) for x in occupancy])
+    rounds = ctypes.c_int32(0)
+    cu, cs = ((ctypes.c_int32 * (clusters + 1))() for _ in range(2))
+    nc = lib.lf_launch_plan_for(occ, len(occupancy), cluster, clusters, max_items,
+                                ctypes.byref(rounds), cu, cs)
     if nc < 0:
         raise LFError(nc, lf_last_error())
     if nc == 0:

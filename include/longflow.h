@@ -309,6 +309,19 @@ int lf_launch_plan(lf_cache* cache, int layer, int32_t* rounds, int32_t* cut_uni
                    int32_t* cut_slot, int max_cuts);
 
 /*
+ * The planner behind lf_launch_plan on given occupancies, without a cache or a
+ * GPU (no counterpart on the pages; for tests and tuning).  occupancy [units]
+ * host: the occupied slots of units 0..units-1; cluster: CTAs per cluster;
+ * clusters: resident clusters (<= 152); max_items: units one cluster may
+ * visit.  Returns `clusters` and fills *rounds, cut_unit and cut_slot [clusters
+ * + 1] as lf_launch_plan does when a plan is taken (whatever the occupancies,
+ * without the 2048-token rule), 0 when whole units are the cheaper launch, or
+ * LF_ERR_ARG.
+ */
+int lf_launch_plan_for(const int32_t* occupancy, int units, int cluster, int clusters,
+                       int max_items, int32_t* rounds, int32_t* cut_unit, int32_t* cut_slot);
+
+/*
  * Prefill without any device allocation.  (No counterpart on the pages: this
  * is an integration entry point, not part of the method.)
  *
