@@ -150,6 +150,30 @@ __device__ __forceinline__ bool wait_count_bounded(const int* cnt, int target) {
   }
 }
 
+// sum_h row[h] cm[h], the FMAs in head order (vector loads of the logit row).
+template <int G>
+__device__ __forceinline__ float group_dot(const float* row, const float* cm) {
+  float as = 0.f;
+  if constexpr (G % 4 == 0) {
+#pragma unroll
+    for (int h = 0; h < G; h += 4) {
+      const float4 x = *reinterpret_cast<const float4*>(row + h);
+      as = fmaf(x.x, cm[h], as);
+      as = fmaf(x.y, cm[h + 1], as);
+      as = fmaf(x.z, cm[h + 2], as);
+      as = fmaf(x.w, cm[h + 3], as);
+    }
+  } else if constexpr (G == 2) {
+    const float2 x = *reinterpret_cast<const float2*>(row);
+    as = fmaf(x.x, cm[0], as);
+    as = fmaf(x.y, cm[1], as);
+  } else {
+#pragma unroll
+    for (int h = 0; h < G; ++h) as = fmaf(row[h], cm[h], as);
+  }
+  return as;
+}
+
 template <int G>
 struct TcPlan {
   static constexpr int D = 128;
@@ -163,15 +187,21 @@ struct TcPlan {
   static constexpr int kOffStats = 896;  // m_loc[2], l_loc[2], s_new[2], cmul, m_glb, l_glb
   static constexpr int kOffRed = kOffStats + 9 * kMaxGroup * 4;
   static constexpr int kOffMisc = kOffRed + 4 * kMaxGroup * 4 + 16;
+  // the leader's output scales: 2^(m_r - M) / L per part r and head, and the new token's
+  static constexpr int kOffOutScale = 1408;  // [kMaxSplitParts + 1][kMaxGroup] floats
   // planned launches: the tail's copy of a shared unit's parts' (m, l)
   static constexpr int kOffPieceStats = 2048;                // [kMaxSplitParts][2G] floats
   static constexpr int kOffStatIn = 3072;                    // [2][kMaxCluster][2G] floats
   static constexpr int kOffOpart = kOffStatIn + 2 * kMaxCluster * 2 * kMaxGroup * 4;  // [2][G][D]
-  static_assert(kOffMisc + 64 <= kOffPieceStats, "header overflow");
+  static_assert(kOffMisc + 64 <= kOffOutScale, "header overflow");
+  static_assert(kOffOutScale + (kMaxSplitParts + 1) * kMaxGroup * 4 <= kOffPieceStats,
+                "header overflow");
+  static_assert(kMaxCluster <= kMaxSplitParts, "output scales sized for the larger count");
   static_assert(kOffPieceStats + kMaxSplitParts * 2 * kMaxGroup * 4 <= kOffStatIn,
                 "header overflow");
   static_assert(16 + 16 + 2 * kTcSBufs + 2 * kTcPBufs + 14 <= kOffStats / 8, "too many barriers");
-  static constexpr int kOffQ = (kOffOpart + 2 * G * D * 4 + 1023) / 1024 * 1024;  // [2] buffers
+  static constexpr int kOffNew = kOffOpart + 2 * G * D * 4;  // [2][k | v][D] the new token
+  static constexpr int kOffQ = (kOffNew + 2 * 2 * D * 2 + 1023) / 1024 * 1024;  // [2] buffers
   static constexpr int kOffRing = kOffQ + 2 * kQBytes;
 
   __host__ __device__ static constexpr int off_p(int stages) { return kOffRing + stages * kStage; }
@@ -269,6 +299,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   float* cmul = s_new + 2 * kMaxGroup;
   float* m_glb = cmul + kMaxGroup;
   float* l_glb = m_glb + kMaxGroup;
+  float* osc = reinterpret_cast<float*>(smem + P::kOffOutScale);  // [parts + 1][kMaxGroup]
   float* red = reinterpret_cast<float*>(smem + P::kOffRed);  // epilogue: [4][kMaxGroup]
   float* red_t = red + 4 * kMaxGroup;                        // tail: [2] scores
   int* red_ti = reinterpret_cast<int*>(red_t + 2);           // tail: [2] slots
@@ -318,6 +349,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     mbar_init(drain, 1);
     fence_mbar_init();
+    // The tensor maps are kernel parameters: fetch them before the wait below.
+    tma_prefetch_desc(&ta.k64);
+    tma_prefetch_desc(&ta.k16);
+    tma_prefetch_desc(&ta.v64);
+    tma_prefetch_desc(&ta.v16);
   }
   if (tid == 0) *fail_any = 0;
   // Operand buffers start at zero (padding rows of q^T and P^T stay zero).
@@ -848,6 +884,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       float* snw = s_new + b2 * kMaxGroup;
       const float* mlc = m_loc + b2 * kMaxGroup;
       const float* llc = l_loc + b2 * kMaxGroup;
+      // The new token's k and v in shared memory for the leader's output and slot
+      // write: loaded here, their latency passes while the tail waits for the
+      // unit's statistics, not after the last exchange (the barrier after that
+      // wait orders the copy for both tail warps).
+      T* nkv = reinterpret_cast<T*>(smem + P::kOffNew) + (size_t)b2 * 2 * D;  // [k | v]
+      for (int e = tt_id; e < D; e += kTcTail) {
+        nkv[e] = kn[e];
+        nkv[D + e] = vn[e];
+      }
 
       // The new token's logits (every CTA computes them), before the waits.
       for (int h = twarp; h < G; h += 2) {
@@ -910,6 +955,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             m_glb[h] = M;
             l_glb[h] = L;
             cmul[h] = (mlc[h] != -INFINITY) ? exp2f(mlc[h] - M) / L : 0.f;
+            // the leader's output scales: each part's, then the new token's
+            for (int r = 0; r < np; ++r) {
+              const float mr = sst[r * 2 * kMaxGroup + h];
+              osc[r * kMaxGroup + h] = (mr != -INFINITY) ? exp2f(mr - M) / L : 0.f;
+            }
+            osc[np * kMaxGroup + h] = exp2f(snw[h] - M) / L;
             if (!(isfinite(M) && isfinite(L) && L > 0.f)) atomicOr(a.err, LF_DEVERR_NONFINITE);
           }
           const bool stats_ok = !named_bar_or(2, kTcTail, !got_stats);
@@ -928,9 +979,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               const int slot = base + i;
               if (slot == rl.excl) continue;
               const float w = w_s[i];
-              float as = 0.f;
-#pragma unroll
-              for (int h = 0; h < G; ++h) as = fmaf(lg[(size_t)i * G + h], cm[h], as);
+              const float as = group_dot<G>(lg + (size_t)i * G, cm);
               const float sc = fabsf(w) * as;
               if (is_candidate(w) && better(sc, slot, bs, bi)) {
                 bs = sc;
@@ -1004,59 +1053,52 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
               }
             }
-            // Output: the new token + every part's partial output, in part order,
-            // four parts' elements loaded at a time.
-            if (all_got && stats_ok) {
-              constexpr int kEl = G * D / kTcTail;
-              T* og = reinterpret_cast<T*>(a.out) + ((size_t)b * a.q_heads + (size_t)g * G) * D;
-              float acc[kEl];
-#pragma unroll
-              for (int i = 0; i < kEl; ++i) {
-                const int h = (tt_id + i * kTcTail) / D;
-                const int e = (tt_id + i * kTcTail) - h * D;
-                acc[i] = exp2f(snw[h] - m_glb[h]) * to_f32(vn[e]);
-              }
-              for (int r0 = 0; r0 < np; r0 += 4) {
-                float part4[kEl][4];
-#pragma unroll
-                for (int i = 0; i < kEl; ++i)
-#pragma unroll
-                  for (int q = 0; q < 4; ++q)
-                    part4[i][q] = (r0 + q < np)
-                                      ? __ldcg(gfn + (size_t)(r0 + q) * kFinF + tt_id + i * kTcTail)
-                                      : 0.f;
+            if (twarp == 1) {
+              // Output (warp 1): the new token + every part's partial output, in part
+              // order; each part's elements of this lane loaded together.
+              if (all_got && stats_ok) {
+                constexpr int kEl = G * D / 32;
+                T* og = reinterpret_cast<T*>(a.out) + ((size_t)b * a.q_heads + (size_t)g * G) * D;
+                float acc[kEl];
 #pragma unroll
                 for (int i = 0; i < kEl; ++i) {
-                  const int h = (tt_id + i * kTcTail) / D;
+                  const int h = (lane + 32 * i) / D;
+                  const int e = (lane + 32 * i) - h * D;
+                  acc[i] = to_f32(nkv[D + e]) * osc[np * kMaxGroup + h];
+                }
+                for (int r = 0; r < np; ++r) {
+                  float part[kEl];
 #pragma unroll
-                  for (int q = 0; q < 4; ++q) {
-                    const float mr = (r0 + q < np) ? sst[(r0 + q) * 2 * kMaxGroup + h] : -INFINITY;
-                    if (mr != -INFINITY) acc[i] += part4[i][q] * exp2f(mr - m_glb[h]);
-                  }
+                  for (int i = 0; i < kEl; ++i)
+                    part[i] = __ldcg(gfn + (size_t)r * kFinF + lane + 32 * i);
+#pragma unroll
+                  for (int i = 0; i < kEl; ++i)
+                    acc[i] = fmaf(part[i], osc[r * kMaxGroup + (lane + 32 * i) / D], acc[i]);
+                }
+#pragma unroll
+                for (int i = 0; i < kEl; ++i) {
+                  const int idx = lane + 32 * i;
+                  const int h = idx / D;
+                  from_f32(acc[i], &og[(size_t)h * D + (idx - h * D)]);
                 }
               }
+            } else {
+              // The decision and the slot write (warp 0), beside the output.
+              float anew = 0.f;
+              if (lane == 0) {
 #pragma unroll
-              for (int i = 0; i < kEl; ++i) {
-                const int idx = tt_id + i * kTcTail;
-                const int h = idx / D;
-                const int e = idx - h * D;
-                from_f32(acc[i] / l_glb[h], &og[(size_t)h * D + e]);
+                for (int h = 0; h < G; ++h) anew += osc[np * kMaxGroup + h];
+                const LeaderOut d =
+                    leader_decide(a, u, n, p, pend, bud, state_ok, any_fail, rl, fi, anew);
+                decision[0] = d.slot;
+                // every part is through both exchanges: ready for the next launch
+                cnt[0] = 0;
+                cnt[1] = 0;
               }
+              __syncwarp();
+              const int slot = decision[0];
+              if (slot >= 0) write_slot<T, D>(a, ubase, slot, nkv, nkv + D, p, anew, lane, 32);
             }
-            float anew = 0.f;
-            if (tt_id == 0) {
-#pragma unroll
-              for (int h = 0; h < G; ++h) anew += exp2f(snw[h] - m_glb[h]) / l_glb[h];
-              const LeaderOut d =
-                  leader_decide(a, u, n, p, pend, bud, state_ok, any_fail, rl, fi, anew);
-              decision[0] = d.slot;
-              // every part is through both exchanges: ready for the next launch
-              cnt[0] = 0;
-              cnt[1] = 0;
-            }
-            named_bar_sync(2, kTcTail);
-            const int slot = decision[0];
-            if (slot >= 0) write_slot<T, D>(a, ubase, slot, kn, vn, p, anew, tt_id, kTcTail);
           }
           named_bar_sync(2, kTcTail);
           if (lane == 0) mbar_arrive(&taildone[b2]);
@@ -1103,6 +1145,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         m_glb[h] = M;
         l_glb[h] = L;
         cmul[h] = (mlc[h] != -INFINITY) ? exp2f(mlc[h] - M) / L : 0.f;
+        // the leader's output scales: each CTA's, then the new token's
+        for (int r = 0; r < C; ++r) {
+          const float mr = sin[r * 2 * kMaxGroup + h];
+          osc[r * kMaxGroup + h] = (mr != -INFINITY) ? exp2f(mr - M) / L : 0.f;
+        }
+        osc[C * kMaxGroup + h] = exp2f(snw[h] - M) / L;
         if (!(isfinite(M) && isfinite(L) && L > 0.f)) atomicOr(a.err, LF_DEVERR_NONFINITE);
       }
       const bool stats_ok = !named_bar_or(2, kTcTail, !got_stats);
@@ -1135,9 +1183,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           const float w = w_s[i];
           const float val = fabsf(w);
-          float as = 0.f;
-#pragma unroll
-          for (int h = 0; h < G; ++h) as = fmaf(lg[(size_t)i * G + h], cm[h], as);
+          const float as = group_dot<G>(lg + (size_t)i * G, cm);
           const float sc = h2o ? val + as : val * as;
           if (layer) {
             if (h2o) a.acc[ubase + slot] = sc;
@@ -1177,9 +1223,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int i = tt_id; i < rows; i += kTcTail) {
           const int slot = base + i;
           if (slot == rl.excl || slot == ci) continue;
-          float as = 0.f;
-#pragma unroll
-          for (int h = 0; h < G; ++h) as = fmaf(lg[(size_t)i * G + h], cm[h], as);
+          const float as = group_dot<G>(lg + (size_t)i * G, cm);
           a.acc[ubase + slot] = fabsf(w_s[i]) + as;
         }
       }
@@ -1211,55 +1255,57 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t fin_phase = (uint32_t)(((k - npc_items) / C) & 1);
         const bool got = __all_sync(0xffffffffu, mbar_wait_cluster_bounded(finb, fin_phase));
         const bool all_got = !named_bar_or(2, kTcTail, !got);
-        // Output: the new token + every CTA's partial output, in rank order.
-        if (all_got && stats_ok) {
-          T* og = reinterpret_cast<T*>(a.out) + ((size_t)b * a.q_heads + (size_t)g * G) * D;
-          for (int idx = tt_id; idx < G * D; idx += kTcTail) {
-            const int h = idx / D;
-            const int e = idx - h * D;
-            float acc = exp2f(snw[h] - m_glb[h]) * to_f32(vn[e]);
-            for (int r = 0; r < C; ++r) {
-              const float mr = sin[r * 2 * kMaxGroup + h];
-              if (mr != -INFINITY)
-                acc += reinterpret_cast<const float*>(fin + (size_t)r * P::kFinBytes)[idx] *
-                       exp2f(mr - m_glb[h]);
-            }
-            from_f32(acc / l_glb[h], &og[(size_t)h * D + e]);
-          }
-        }
-        float anew = 0.f;  // the new token's attention mass (tt_id 0)
-        if (tt_id == 0) {
-          bool any_fail = !all_got || !stats_ok;
-          float fs = INFINITY;
-          int fi = INT_MAX;
-          for (int r = 0; r < C; ++r) {
-            const uint32_t* tail =
-                reinterpret_cast<const uint32_t*>(fin + (size_t)r * P::kFinBytes + G * D * 4);
-            any_fail = any_fail || tail[2] != 0;
-            const float rs = __uint_as_float(tail[0]);
-            const int ri = (int)tail[1];
-            if (better(rs, ri, fs, fi)) {
-              fs = rs;
-              fi = ri;
+        if (twarp == 1) {
+          // Output (warp 1): the new token + every CTA's partial output, in rank order.
+          if (all_got && stats_ok) {
+            T* og = reinterpret_cast<T*>(a.out) + ((size_t)b * a.q_heads + (size_t)g * G) * D;
+            for (int idx = lane; idx < G * D; idx += 32) {
+              const int h = idx / D;
+              const int e = idx - h * D;
+              float acc = to_f32(nkv[D + e]) * osc[C * kMaxGroup + h];
+              for (int r = 0; r < C; ++r)
+                acc = fmaf(reinterpret_cast<const float*>(fin + (size_t)r * P::kFinBytes)[idx],
+                           osc[r * kMaxGroup + h], acc);
+              from_f32(acc, &og[(size_t)h * D + e]);
             }
           }
-#pragma unroll
-          for (int h = 0; h < G; ++h) anew += exp2f(snw[h] - m_glb[h]) / l_glb[h];
-          const LeaderOut d = leader_decide(a, u, n, p, pend, bud, state_ok, any_fail, rl, fi, anew);
-          decision[0] = d.slot;
-          // H2O: the accumulators of the CTAs' lowest candidates (their scores),
-          // except the slot the new token takes.
-          if (h2o && !layer && state_ok && !any_fail)
+        } else {
+          // The decision and the slot write (warp 0), beside the output.
+          float anew = 0.f;  // the new token's attention mass (lane 0)
+          if (lane == 0) {
+            bool any_fail = !all_got || !stats_ok;
+            float fs = INFINITY;
+            int fi = INT_MAX;
             for (int r = 0; r < C; ++r) {
               const uint32_t* tail =
                   reinterpret_cast<const uint32_t*>(fin + (size_t)r * P::kFinBytes + G * D * 4);
+              any_fail = any_fail || tail[2] != 0;
+              const float rs = __uint_as_float(tail[0]);
               const int ri = (int)tail[1];
-              if (ri != INT_MAX && ri != d.slot) a.acc[ubase + ri] = __uint_as_float(tail[0]);
+              if (better(rs, ri, fs, fi)) {
+                fs = rs;
+                fi = ri;
+              }
             }
+#pragma unroll
+            for (int h = 0; h < G; ++h) anew += osc[C * kMaxGroup + h];
+            const LeaderOut d =
+                leader_decide(a, u, n, p, pend, bud, state_ok, any_fail, rl, fi, anew);
+            decision[0] = d.slot;
+            // H2O: the accumulators of the CTAs' lowest candidates (their scores),
+            // except the slot the new token takes.
+            if (h2o && !layer && state_ok && !any_fail)
+              for (int r = 0; r < C; ++r) {
+                const uint32_t* tail =
+                    reinterpret_cast<const uint32_t*>(fin + (size_t)r * P::kFinBytes + G * D * 4);
+                const int ri = (int)tail[1];
+                if (ri != INT_MAX && ri != d.slot) a.acc[ubase + ri] = __uint_as_float(tail[0]);
+              }
+          }
+          __syncwarp();
+          const int slot = decision[0];
+          if (slot >= 0) write_slot<T, D>(a, ubase, slot, nkv, nkv + D, p, anew, lane, 32);
         }
-        named_bar_sync(2, kTcTail);
-        const int slot = decision[0];
-        if (slot >= 0) write_slot<T, D>(a, ubase, slot, kn, vn, p, anew, tt_id, kTcTail);
       }
       // Release this parity's buffers (logits, partial output, statistics).
       named_bar_sync(2, kTcTail);
