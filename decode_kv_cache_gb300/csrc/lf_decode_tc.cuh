@@ -57,6 +57,7 @@ constexpr int kTcTile = 128;      // slots per tile (the MMA M of phase A)
 constexpr int kTcSBufs = 16;      // logit accumulators in flight between MMA and epilogue
 constexpr int kTcLookahead = 2;   // K tiles of the next unit issued before V of this one
 constexpr int kTcPBufs = 4;       // P^T tiles in flight between the compute warps and MMA
+constexpr int kScoreRows = 4;     // rows a tail thread scores per pass (loads issued together)
 // kTcSBufs x 16 columns of S + 16 columns of O, rounded to a power of two.  All
 // 512 columns of the SM: the host sizes shared memory so that exactly one CTA
 // is resident per SM, so the allocation never waits.
@@ -975,15 +976,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             float cm[G];
 #pragma unroll
             for (int h = 0; h < G; ++h) cm[h] = cmul[h];
-            for (int i = tt_id; i < rows; i += kTcTail) {
-              const int slot = base + i;
-              if (slot == rl.excl) continue;
-              const float w = w_s[i];
-              const float as = group_dot<G>(lg + (size_t)i * G, cm);
-              const float sc = fabsf(w) * as;
-              if (is_candidate(w) && better(sc, slot, bs, bi)) {
-                bs = sc;
-                bi = slot;
+            for (int i0 = tt_id; i0 < rows; i0 += kScoreRows * kTcTail) {
+              float wv[kScoreRows], asv[kScoreRows];
+#pragma unroll
+              for (int jr = 0; jr < kScoreRows; ++jr) {
+                const int i = i0 + jr * kTcTail;
+                wv[jr] = 0.f;
+                asv[jr] = 0.f;
+                if (i < rows) {
+                  wv[jr] = w_s[i];
+                  asv[jr] = group_dot<G>(lg + (size_t)i * G, cm);
+                }
+              }
+#pragma unroll
+              for (int jr = 0; jr < kScoreRows; ++jr) {
+                const int i = i0 + jr * kTcTail;
+                const int slot = base + i;
+                if (i >= rows) break;
+                if (slot == rl.excl) continue;
+                const float sc = fabsf(wv[jr]) * asv[jr];
+                if (is_candidate(wv[jr]) && better(sc, slot, bs, bi)) {
+                  bs = sc;
+                  bi = slot;
+                }
               }
             }
           }
@@ -1175,22 +1190,39 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         float cm[G];
 #pragma unroll
         for (int h = 0; h < G; ++h) cm[h] = cmul[h];
-        for (int i = tt_id; i < rows; i += kTcTail) {
-          const int slot = base + i;
-          if (slot == rl.excl) {
-            if (layer && rl.choosing) a.lw_score[ubase + slot] = INFINITY;
-            continue;
+        // kScoreRows rows per pass, their loads issued together (the lowest
+        // (score, slot) does not depend on the order rows are visited in).
+        for (int i0 = tt_id; i0 < rows; i0 += kScoreRows * kTcTail) {
+          float wv[kScoreRows], asv[kScoreRows];
+#pragma unroll
+          for (int jr = 0; jr < kScoreRows; ++jr) {
+            const int i = i0 + jr * kTcTail;
+            wv[jr] = 0.f;
+            asv[jr] = 0.f;
+            if (i < rows) {
+              wv[jr] = w_s[i];
+              asv[jr] = group_dot<G>(lg + (size_t)i * G, cm);
+            }
           }
-          const float w = w_s[i];
-          const float val = fabsf(w);
-          const float as = group_dot<G>(lg + (size_t)i * G, cm);
-          const float sc = h2o ? val + as : val * as;
-          if (layer) {
-            if (h2o) a.acc[ubase + slot] = sc;
-            if (rl.choosing) a.lw_score[ubase + slot] = is_candidate(w) ? sc : INFINITY;
-          } else if (rl.choosing && is_candidate(w) && better(sc, slot, bs, bi)) {
-            bs = sc;
-            bi = slot;
+#pragma unroll
+          for (int jr = 0; jr < kScoreRows; ++jr) {
+            const int i = i0 + jr * kTcTail;
+            const int slot = base + i;
+            if (i >= rows) break;
+            if (slot == rl.excl) {
+              if (layer && rl.choosing) a.lw_score[ubase + slot] = INFINITY;
+              continue;
+            }
+            const float w = wv[jr];
+            const float val = fabsf(w);
+            const float sc = h2o ? val + asv[jr] : val * asv[jr];
+            if (layer) {
+              if (h2o) a.acc[ubase + slot] = sc;
+              if (rl.choosing) a.lw_score[ubase + slot] = is_candidate(w) ? sc : INFINITY;
+            } else if (rl.choosing && is_candidate(w) && better(sc, slot, bs, bi)) {
+              bs = sc;
+              bi = slot;
+            }
           }
         }
       }
