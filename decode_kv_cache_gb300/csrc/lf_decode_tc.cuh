@@ -194,13 +194,13 @@ struct TcPlan {
   static constexpr int kOffPieceStats = 2048;                // [kMaxSplitParts][2G] floats
   static constexpr int kOffStatIn = 3072;                    // [2][kMaxCluster][2G] floats
   static constexpr int kOffOpart = kOffStatIn + 2 * kMaxCluster * 2 * kMaxGroup * 4;  // [2][G][D]
-  static_assert(kOffMisc + 64 <= kOffOutScale, "header overflow");
+  static_assert(kOffMisc + 80 <= kOffOutScale, "header overflow");
   static_assert(kOffOutScale + (kMaxSplitParts + 1) * kMaxGroup * 4 <= kOffPieceStats,
                 "header overflow");
   static_assert(kMaxCluster <= kMaxSplitParts, "output scales sized for the larger count");
   static_assert(kOffPieceStats + kMaxSplitParts * 2 * kMaxGroup * 4 <= kOffStatIn,
                 "header overflow");
-  static_assert(16 + 16 + 2 * kTcSBufs + 2 * kTcPBufs + 14 <= kOffStats / 8, "too many barriers");
+  static_assert(16 + 16 + 2 * kTcSBufs + 2 * kTcPBufs + 16 <= kOffStats / 8, "too many barriers");
   static constexpr int kOffNew = kOffOpart + 2 * G * D * 4;  // [2][k | v][D] the new token
   static constexpr int kOffQ = (kOffNew + 2 * 2 * D * 2 + 1023) / 1024 * 1024;  // [2] buffers
   static constexpr int kOffRing = kOffQ + 2 * kQBytes;
@@ -294,6 +294,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* taildone = handoff + 2;        // [2] tail -> epilogue: that state is consumed
   uint64_t* drain = taildone + 2;          // every MMA complete
   uint64_t* statrdy = drain + 1;           // [2] epilogue -> tail: (m, l), logits, weights
+  uint64_t* gstat = statrdy + 2;           // tail -> epilogue: the last unit's scales (once)
+  uint64_t* escore = gstat + 1;            // epilogue -> tail: its share of the last unit's scores
   float* m_loc = reinterpret_cast<float*>(smem + P::kOffStats);  // [2][kMaxGroup]
   float* l_loc = m_loc + 2 * kMaxGroup;                          // [2][kMaxGroup]
   float* s_new = l_loc + 2 * kMaxGroup;                          // [2][kMaxGroup]
@@ -309,6 +311,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   volatile int* fail_any = reinterpret_cast<volatile int*>(smem + P::kOffMisc + 16);
   volatile int* uflag = reinterpret_cast<volatile int*>(smem + P::kOffMisc + 24);  // [2]
   volatile int* split_flag = reinterpret_cast<volatile int*>(smem + P::kOffMisc + 40);
+  volatile int* gscore_ok = reinterpret_cast<volatile int*>(smem + P::kOffMisc + 44);
+  float* esc_s = reinterpret_cast<float*>(smem + P::kOffMisc + 48);  // [4] epilogue warps' lowest
+  int* esc_i = reinterpret_cast<int*>(smem + P::kOffMisc + 64);      // [4]
   float* stat_in = reinterpret_cast<float*>(smem + P::kOffStatIn);  // [2][C][2G]
   int* items = reinterpret_cast<int*>(smem + P::off_items(S, chunk, C, a.evict));  // [nitems][8]
   float* opbase = reinterpret_cast<float*>(smem + P::kOffOpart);     // [2][G][D]
@@ -349,6 +354,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&statrdy[i], 1);
     }
     mbar_init(drain, 1);
+    mbar_init(gstat, 1);
+    mbar_init(escore, 4);  // the four epilogue warps
     fence_mbar_init();
     // The tensor maps are kernel parameters: fetch them before the wait below.
     tma_prefetch_desc(&ta.k64);
@@ -412,6 +419,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t tO = tmem + 16 * kTcSBufs;
 
   auto unit_of = [&](int k) { return items[kTcItemInts * k + 4]; };
+  // The launch's last item, a whole unit with the plain LongFlow score: the
+  // epilogue warps, idle after it, score the rows from `split` on while the tail
+  // warps score the rows before it, so that the launch ends sooner.
+  auto last_shared_scoring = [&](int k, const UnitRule& rl) {
+    return k == nitems - 1 && items[kTcItemInts * k + 7] == 0 && rl.choosing &&
+           a.score != LF_SCORE_H2O && a.scope != LF_SCOPE_LAYER;
+  };
+  auto score_split = [](int rows) { return (rows / 3) & ~3; };
   auto is_piece = [&](int k) { return kSplit && items[kTcItemInts * k + 7] != 0; };
   // This CTA's share of item k: the occupied slots of the unit (of a shared
   // unit: of this cluster's range of it, clipped to the occupied count) are
@@ -689,6 +704,63 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       __threadfence();
       atomicAdd(ta.split_cnt + 2 * xi, 1);
     };
+    // The epilogue warps' share of the last unit's scores (rows from score_split
+    // on), once the tail warps have the unit's scales; the lowest (score, slot)
+    // of each warp goes to the tail warps.  Every path arrives on `escore`.
+    auto epilogue_scores = [&](int rows, int base, const UnitRule& rl, const float* lg,
+                               const float* w_s, bool have) {
+      const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(gstat, 0));
+      float bs = INFINITY;
+      int bi = INT_MAX;
+      if (ok && have && gscore_ok[0]) {
+        float cm[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) cm[h] = cmul[h];
+        for (int i0 = score_split(rows) + tid; i0 < rows; i0 += kScoreRows * kTcCompute) {
+          float wv[kScoreRows], asv[kScoreRows];
+#pragma unroll
+          for (int jr = 0; jr < kScoreRows; ++jr) {
+            const int i = i0 + jr * kTcCompute;
+            wv[jr] = 0.f;
+            asv[jr] = 0.f;
+            if (i < rows) {
+              wv[jr] = w_s[i];
+              asv[jr] = group_dot<G>(lg + (size_t)i * G, cm);
+            }
+          }
+#pragma unroll
+          for (int jr = 0; jr < kScoreRows; ++jr) {
+            const int i = i0 + jr * kTcCompute;
+            const int slot = base + i;
+            if (i >= rows) break;
+            if (slot == rl.excl) continue;
+            const float sc = fabsf(wv[jr]) * asv[jr];
+            if (is_candidate(wv[jr]) && better(sc, slot, bs, bi)) {
+              bs = sc;
+              bi = slot;
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float os = __shfl_xor_sync(0xffffffffu, bs, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (better(os, oi, bs, bi)) {
+          bs = os;
+          bi = oi;
+        }
+      }
+      if (lane == 0) {
+        esc_s[warp] = bs;
+        esc_i[warp] = bi;
+        mbar_arrive(escore);
+      }
+      if (!ok && tid == 0) {
+        *fail_any = 1;
+        atomicOr(a.err, LF_DEVERR_TIMEOUT);
+      }
+    };
     int kt = 0, ne = 0, pt = 0;
     for (int k = 0; k < nitems; ++k) {
       int n, p, base;
@@ -819,6 +891,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (is_piece(k)) publish_stats(k, b2);
           mbar_arrive(&statrdy[b2]);
         }
+        if (last_shared_scoring(k, rl)) epilogue_scores(rows, base, rl, lg, w_s, !bad2);
         // The output accumulator: thread e <-> TMEM lane e <-> output element e.
         if (!bad2 && __all_sync(0xffffffffu, mbar_wait_bounded(ofull, (uint32_t)(ne & 1)))) {
           tc_fence_after();
@@ -842,6 +915,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (is_piece(k)) publish_stats(k, b2);
           mbar_arrive(&statrdy[b2]);
         }
+        if (last_shared_scoring(k, rl)) epilogue_scores(rows, base, rl, lg, w_s, false);
       }
       if (rows > 0) ne += 1;
       const bool failed = any_bad || named_bar_or(1, kTcCompute, bad2);
@@ -1186,20 +1260,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       float bs = INFINITY;
       int bi = INT_MAX;
       const bool scoring = (rl.choosing || h2o) && !unit_failed && got_loc && stats_ok;
+      // The launch's last unit: the epilogue warps score the rows from `srows` on.
+      const bool shared_last = last_shared_scoring(k, rl);
+      const int srows = shared_last ? score_split(rows) : rows;
+      if (shared_last && tt_id == 0) {
+        gscore_ok[0] = scoring ? 1 : 0;
+        mbar_arrive(gstat);  // the scales (cmul) are final: the named barrier above
+      }
       if (scoring) {
         float cm[G];
 #pragma unroll
         for (int h = 0; h < G; ++h) cm[h] = cmul[h];
         // kScoreRows rows per pass, their loads issued together (the lowest
         // (score, slot) does not depend on the order rows are visited in).
-        for (int i0 = tt_id; i0 < rows; i0 += kScoreRows * kTcTail) {
+        for (int i0 = tt_id; i0 < srows; i0 += kScoreRows * kTcTail) {
           float wv[kScoreRows], asv[kScoreRows];
 #pragma unroll
           for (int jr = 0; jr < kScoreRows; ++jr) {
             const int i = i0 + jr * kTcTail;
             wv[jr] = 0.f;
             asv[jr] = 0.f;
-            if (i < rows) {
+            if (i < srows) {
               wv[jr] = w_s[i];
               asv[jr] = group_dot<G>(lg + (size_t)i * G, cm);
             }
@@ -1208,7 +1289,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           for (int jr = 0; jr < kScoreRows; ++jr) {
             const int i = i0 + jr * kTcTail;
             const int slot = base + i;
-            if (i >= rows) break;
+            if (i >= srows) break;
             if (slot == rl.excl) {
               if (layer && rl.choosing) a.lw_score[ubase + slot] = INFINITY;
               continue;
@@ -1277,6 +1358,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (better(red_t[1], red_ti[1], bs, bi)) {
             bs = red_t[1];
             bi = red_ti[1];
+          }
+          if (shared_last) {  // the epilogue warps' share
+            if (!mbar_wait_bounded(escore, 0)) {
+              *fail_any = 1;
+              atomicOr(a.err, LF_DEVERR_TIMEOUT);
+            }
+            for (int w = 0; w < 4; ++w)
+              if (better(esc_s[w], esc_i[w], bs, bi)) {
+                bs = esc_s[w];
+                bi = esc_i[w];
+              }
           }
           const uint32_t flag = (unit_failed || !stats_ok || *fail_any) ? 1u : 0u;
           st_async_v4(dst + G * D * 4, __float_as_uint(bs), (uint32_t)bi, flag, 0u, rb);
