@@ -58,6 +58,11 @@ constexpr int kTcSBufs = 16;      // logit accumulators in flight between MMA an
 constexpr int kTcLookahead = 2;   // K tiles of the next unit issued before V of this one
 constexpr int kTcPBufs = 4;       // P^T tiles in flight between the compute warps and MMA
 constexpr int kScoreRows = 4;     // rows a tail thread scores per pass (loads issued together)
+#ifndef LF_PREFETCH_TILES
+#define LF_PREFETCH_TILES 8
+#endif
+// K tiles of a CTA's first unit brought into L2 before the grid dependency wait.
+constexpr int kPrefetchTiles = LF_PREFETCH_TILES;
 // kTcSBufs x 16 columns of S + 16 columns of O, rounded to a power of two.  All
 // 512 columns of the SM: the host sizes shared memory so that exactly one CTA
 // is resident per SM, so the allocation never waits.
@@ -362,6 +367,49 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tma_prefetch_desc(&ta.k16);
     tma_prefetch_desc(&ta.v64);
     tma_prefetch_desc(&ta.v16);
+    // While the previous grid on the stream finishes (its last units leave HBM
+    // mostly idle), bring the first K tiles of this CTA's first unit, its norms
+    // and positions and its queries into L2.  A hint only: the copies proper
+    // come after the wait below and read memory again, and the occupancy is
+    // read without ordering, so a stale value costs bandwidth and nothing else.
+    if (nitems > 0 && kPrefetchTiles > 0) {
+      int u = j, lo = 0, hi = INT_MAX;
+      if (npc > 0) {
+        u = pcs[0].unit;
+        lo = pcs[0].lo;
+        hi = pcs[0].hi;
+      } else if (w1 > w0) {
+        u = w0;
+      }
+      const int n = min(max(ld_relaxed(a.count + u), 0), a.capacity);
+      const int lo2 = min(lo, n);
+      const int hi2 = min(hi, n);
+      const int per = ((hi2 - lo2 + C - 1) / C + 3) & ~3;
+      const int base = lo2 + rank * per;
+      const int rows = max(0, min(per, hi2 - base));
+      const int row0 = ta.row_base + u * a.slot_stride + base;
+      // The boxes of the copies proper: 64-row boxes, then 16-row granules.
+      const int lim = min((rows + 15) & ~15, kPrefetchTiles * kTcTile);
+      int r = 0;
+      for (; r + 64 <= lim; r += 64) {
+        tma_prefetch_l2_2d(&ta.k64, 0, row0 + r);
+        tma_prefetch_l2_2d(&ta.k64, 64, row0 + r);
+      }
+      for (; r < lim; r += 16) {
+        tma_prefetch_l2_2d(&ta.k16, 0, row0 + r);
+        tma_prefetch_l2_2d(&ta.k16, 64, row0 + r);
+      }
+      if (rows > 0 && a.evict) {
+        const size_t ub = (size_t)u * a.slot_stride + base;
+        const uint32_t small = (uint32_t)(((rows + 3) & ~3) * 4);
+        bulk_prefetch_l2((a.score == LF_SCORE_H2O ? a.acc : a.vnorm) + ub, small);
+        bulk_prefetch_l2(a.pos + ub, small);
+      }
+      const int bb = u / a.kv_heads;
+      bulk_prefetch_l2(reinterpret_cast<const T*>(a.q) +
+                           ((size_t)bb * a.q_heads + (size_t)(u - bb * a.kv_heads) * G) * D,
+                       (uint32_t)(G * D * sizeof(T)));
+    }
   }
   if (tid == 0) *fail_any = 0;
   // Operand buffers start at zero (padding rows of q^T and P^T stay zero).
@@ -1380,18 +1428,38 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const bool got = __all_sync(0xffffffffu, mbar_wait_cluster_bounded(finb, fin_phase));
         const bool all_got = !named_bar_or(2, kTcTail, !got);
         if (twarp == 1) {
-          // Output (warp 1): the new token + every CTA's partial output, in rank order.
+          // Output (warp 1): the new token + every CTA's partial output, in rank
+          // order.  Lane l takes elements [4l, 4l + 4) of every head row, each
+          // CTA's rows loaded together as 16-byte vectors.
           if (all_got && stats_ok) {
+            static_assert(D == 32 * 4, "four elements of a head row per lane");
             T* og = reinterpret_cast<T*>(a.out) + ((size_t)b * a.q_heads + (size_t)g * G) * D;
-            for (int idx = lane; idx < G * D; idx += 32) {
-              const int h = idx / D;
-              const int e = idx - h * D;
-              float acc = to_f32(nkv[D + e]) * osc[C * kMaxGroup + h];
-              for (int r = 0; r < C; ++r)
-                acc = fmaf(reinterpret_cast<const float*>(fin + (size_t)r * P::kFinBytes)[idx],
-                           osc[r * kMaxGroup + h], acc);
-              from_f32(acc, &og[(size_t)h * D + e]);
+            const int e0 = lane * 4;
+            float acc[G][4];
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+              const float sn = osc[C * kMaxGroup + h];
+#pragma unroll
+              for (int x = 0; x < 4; ++x) acc[h][x] = to_f32(nkv[D + e0 + x]) * sn;
             }
+            for (int r = 0; r < C; ++r) {
+              const float* fr = reinterpret_cast<const float*>(fin + (size_t)r * P::kFinBytes);
+              float4 pr[G];
+#pragma unroll
+              for (int h = 0; h < G; ++h) pr[h] = *reinterpret_cast<const float4*>(fr + h * D + e0);
+#pragma unroll
+              for (int h = 0; h < G; ++h) {
+                const float sc = osc[r * kMaxGroup + h];
+                acc[h][0] = fmaf(pr[h].x, sc, acc[h][0]);
+                acc[h][1] = fmaf(pr[h].y, sc, acc[h][1]);
+                acc[h][2] = fmaf(pr[h].z, sc, acc[h][2]);
+                acc[h][3] = fmaf(pr[h].w, sc, acc[h][3]);
+              }
+            }
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+#pragma unroll
+              for (int x = 0; x < 4; ++x) from_f32(acc[h][x], &og[(size_t)h * D + e0 + x]);
           }
         } else {
           // The decision and the slot write (warp 0), beside the output.

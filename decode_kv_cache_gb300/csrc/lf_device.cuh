@@ -162,6 +162,25 @@ __device__ __forceinline__ bool better(float s, int i, float bs, int bi) {
 
 namespace lf {
 
+// Bring the box of a 2-D tensor map at {x, y} into L2 only (no shared memory,
+// no barrier).  A box past the tensor's edge is clipped.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y) : "memory");
+}
+
+// Bring [src, src + bytes) into L2 only: src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// A load not ordered against other threads' writes: the value may be stale.
+__device__ __forceinline__ int ld_relaxed(const int* p) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 // 2-D tiled TMA load of box {x .. x+box0, y .. y+box1} into this CTA's smem.
 __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, int y,
                                             uint64_t* bar, uint64_t policy) {

@@ -79,12 +79,6 @@ static_assert(kOffMisc + 16 <= kOffStats && kOffStats + 2 * kRkQRows * 4 <= kOff
 // the sort reuses the ring: 64-bit keys then 16-bit slot indices
 static_assert(kRkvMaxSlots * 10 <= kRkStages * kRkStage, "sort space");
 
-// Bring a tile of a 2-D tensor map into L2 only (no shared memory, no barrier).
-__device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int x, int y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                   reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y) : "memory");
-}
-
 __device__ __forceinline__ uint32_t orderable(float z) {
   const uint32_t u = __float_as_uint(z);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
