@@ -106,8 +106,103 @@ struct Plan {
   int cut_unit[lf::kTcMaxPlan + 1], cut_slot[lf::kTcMaxPlan + 1];
 };
 
+// Costs every cluster of `pl` as the kernel will run it: false when a shared
+// unit needs more than lf::kMaxSplitParts CTAs or a cluster more items than
+// the table holds.  `worst` is the costliest cluster's cost and fixed[j] the
+// part of cluster j's cost that its range adds beyond its slots (items, parts).
+bool cost_plan(const Plan& pl, const std::vector<int32_t>& n, int c, int nc, int max_items,
+               const std::vector<long long>& load, long long* worst,
+               std::vector<long long>* fixed) {
+  auto parts_of = [&](int uu) {  // clusters sharing unit uu: 1 + its inner cuts
+    int k = 1;
+    for (int q = 1; q < nc; ++q) k += (pl.cut_unit[q] == uu && pl.cut_slot[q] > 0) ? 1 : 0;
+    return k;
+  };
+  *worst = 0;
+  for (int j = 0; j < nc; ++j) {
+    const int u0 = pl.cut_unit[j], s0 = pl.cut_slot[j];
+    const int u1 = pl.cut_unit[j + 1], s1 = pl.cut_slot[j + 1];
+    long long cost = load[j], fx = 0;
+    int items = pl.rounds;
+    if (s0 > 0) {
+      const long long hi = (u1 == u0) ? s1 : n[u0];
+      cost += (std::max(0LL, hi - s0) + c - 1) / c;
+      fx += kItemCost + kPartCost;
+      ++items;
+      if (parts_of(u0) * c > lf::kMaxSplitParts) return false;
+    }
+    if (s1 > 0 && !(s0 > 0 && u1 == u0)) {
+      cost += ((long long)std::min(s1, n[u1]) + c - 1) / c;
+      fx += kItemCost + kPartCost;
+      ++items;
+      if (parts_of(u1) * c > lf::kMaxSplitParts) return false;
+    }
+    for (int w = (s0 > 0) ? u0 + 1 : u0; w < u1; ++w) {  // units wholly inside the range
+      cost += (n[w] + c - 1) / c;
+      fx += kItemCost;
+      ++items;
+    }
+    if (items > max_items) return false;
+    (*fixed)[j] = fx;
+    *worst = std::max(*worst, cost + fx);
+  }
+  return true;
+}
+
+// Cuts for level `level`: clusters 0, 1, ... take, in turn, the units past the
+// whole rounds from where the last range ended, each as far as its cost stays
+// within the level, every part and unit of the range paying its fixed cost
+// where it falls.  False when the ranges end before the last unit does.
+bool walk_plan(const std::vector<int32_t>& n, int c, int ncp, int nc, int first,
+               const std::vector<long long>& load, double level, long long gran, long long least,
+               Plan* pl) {
+  const int units = (int)n.size();
+  int u = first;
+  long long s = 0;  // the walk's position: slot s of unit u
+  pl->cut_unit[0] = first;
+  pl->cut_slot[0] = 0;
+  for (int j = 0; j < nc; ++j) {
+    if (j < ncp && u < units) {
+      double cap = (level - (double)load[j]) * c;  // slots left to this cluster
+      while (u < units) {
+        const long long rest = n[u] - s;
+        const double fixed = (double)(kItemCost + (s > 0 ? kPartCost : 0)) * c;
+        if ((double)rest + fixed <= cap) {  // the rest of unit u fits
+          cap -= (double)rest + fixed;
+          ++u;
+          s = 0;
+          continue;
+        }
+        // A part of unit u: from s, as many slots as the level leaves, on the grid.
+        const double room = cap - (double)(kItemCost + kPartCost) * c;
+        const long long x = room > 0 ? (long long)(room / (double)gran) * gran : 0;
+        if (x >= least && rest - x >= least) {
+          s += x;
+        } else if (x >= least) {
+          // The unit's tail would be short: leave the next range a part of
+          // `least` slots, or take the whole unit when that leaves too little.
+          const long long x2 = (rest - least) / gran * gran;
+          if (x2 >= least) {
+            s += x2;
+          } else {
+            ++u;
+            s = 0;
+          }
+        }
+        break;
+      }
+    }
+    pl->cut_unit[j + 1] = (u < units) ? u : units;
+    pl->cut_slot[j + 1] = (u < units) ? (int)s : 0;
+  }
+  return u >= units;
+}
+
 // Fills `pl` for units of n[u] occupied slots on nc clusters of c CTAs; returns
 // the costliest cluster's cost (CTA slot rows), or -1 when no plan applies.
+// Two ways to cut the ranges, the cheaper kept: lengths levelled on the
+// clusters' loads alone (the fixed costs of parts and units fall where the
+// cuts do), and the walk above at the lowest level that covers every unit.
 long long make_plan(const std::vector<int32_t>& n, int c, int nc, int max_items, Plan* pl) {
   const int units = (int)n.size();
   const int rounds = units / nc, first = rounds * nc;
@@ -127,8 +222,12 @@ long long make_plan(const std::vector<int32_t>& n, int c, int nc, int max_items,
   if (most < 2) return -1;
   const long long span = (longest + most - 2) / (most - 1) + 2 * gran;
   const int ncp = (int)std::max(1LL, std::min<long long>(nc, total / span));
-  // Level: range lengths f_j = c (level - load_j), at least 0, summing to `total`
-  // over the first ncp clusters.
+  std::vector<long long> fixed((size_t)nc, 0);
+  long long best = -1, worst = 0;
+  Plan trial;
+  // Level: range lengths f_j = c (level - load_j), at least 0, summing to
+  // `total` over the first ncp clusters; cut points at the running sums,
+  // rounded to the grid and moved off short parts.
   double lo_l = 0, hi_l = 1e18;
   for (int it = 0; it < 100; ++it) {
     const double mid = 0.5 * (lo_l + hi_l);
@@ -136,17 +235,16 @@ long long make_plan(const std::vector<int32_t>& n, int c, int nc, int max_items,
     for (int j = 0; j < ncp; ++j) sum += std::max(0.0, (mid - load[j]) * c);
     (sum < total ? lo_l : hi_l) = mid;
   }
-  // Cut points at the running sums, rounded to the grid and moved off short parts.
-  pl->rounds = rounds;
-  pl->cut_unit[0] = first;
-  pl->cut_slot[0] = 0;
+  trial.rounds = rounds;
+  trial.cut_unit[0] = first;
+  trial.cut_slot[0] = 0;
   double at = 0;
   int u = first;
   long long before = 0;  // slots of the units [first, u)
   for (int j = 1; j <= nc; ++j) {
     if (j >= ncp) {
-      pl->cut_unit[j] = units;
-      pl->cut_slot[j] = 0;
+      trial.cut_unit[j] = units;
+      trial.cut_slot[j] = 0;
       continue;
     }
     at += std::max(0.0, (hi_l - load[j - 1]) * c);
@@ -158,45 +256,36 @@ long long make_plan(const std::vector<int32_t>& n, int c, int nc, int max_items,
       if (off >= least && n[u] - off >= least) cs = (int)off;
       else if (off >= least) cu = u + 1;  // the unit's tail is short: it stays on the left
     }
-    if (cu < pl->cut_unit[j - 1] ||
-        (cu == pl->cut_unit[j - 1] && cs < pl->cut_slot[j - 1])) {  // never go back
-      cu = pl->cut_unit[j - 1];
-      cs = pl->cut_slot[j - 1];
+    if (cu < trial.cut_unit[j - 1] ||
+        (cu == trial.cut_unit[j - 1] && cs < trial.cut_slot[j - 1])) {  // never go back
+      cu = trial.cut_unit[j - 1];
+      cs = trial.cut_slot[j - 1];
     }
-    pl->cut_unit[j] = cu;
-    pl->cut_slot[j] = cs;
+    trial.cut_unit[j] = cu;
+    trial.cut_slot[j] = cs;
   }
-  // Check and cost every cluster as the kernel will run it.
-  auto parts_of = [&](int uu) {  // clusters sharing unit uu: 1 + its inner cuts
-    int k = 1;
-    for (int q = 1; q < nc; ++q) k += (pl->cut_unit[q] == uu && pl->cut_slot[q] > 0) ? 1 : 0;
-    return k;
-  };
-  long long worst = 0;
-  for (int j = 0; j < nc; ++j) {
-    const int u0 = pl->cut_unit[j], s0 = pl->cut_slot[j];
-    const int u1 = pl->cut_unit[j + 1], s1 = pl->cut_slot[j + 1];
-    long long cost = load[j];
-    int items = rounds;
-    if (s0 > 0) {
-      const long long hi = (u1 == u0) ? s1 : n[u0];
-      cost += (std::max(0LL, hi - s0) + c - 1) / c + kItemCost + kPartCost;
-      ++items;
-      if (parts_of(u0) * c > lf::kMaxSplitParts) return -1;
-    }
-    if (s1 > 0 && !(s0 > 0 && u1 == u0)) {
-      cost += ((long long)std::min(s1, n[u1]) + c - 1) / c + kItemCost + kPartCost;
-      ++items;
-      if (parts_of(u1) * c > lf::kMaxSplitParts) return -1;
-    }
-    for (int w = (s0 > 0) ? u0 + 1 : u0; w < u1; ++w) {  // units wholly inside the range
-      cost += (n[w] + c - 1) / c + kItemCost;
-      ++items;
-    }
-    if (items > max_items) return -1;
-    worst = std::max(worst, cost);
+  if (cost_plan(trial, n, c, nc, max_items, load, &worst, &fixed)) {
+    *pl = trial;
+    best = worst;
   }
-  return worst;
+  // The walk: the lowest level (bisection) at which the ranges cover every unit.
+  double lo_w = 0, hi_w = 0;
+  for (int j = 0; j < ncp; ++j) hi_w = std::max(hi_w, (double)load[j]);
+  hi_w += (double)total / c + (double)(units - first + 2) * (kItemCost + kPartCost) + 1;
+  trial.rounds = rounds;
+  if (walk_plan(n, c, ncp, nc, first, load, hi_w, gran, least, &trial)) {
+    for (int it = 0; it < 60; ++it) {
+      const double mid = 0.5 * (lo_w + hi_w);
+      (walk_plan(n, c, ncp, nc, first, load, mid, gran, least, &trial) ? hi_w : lo_w) = mid;
+    }
+    if (walk_plan(n, c, ncp, nc, first, load, hi_w, gran, least, &trial) &&
+        cost_plan(trial, n, c, nc, max_items, load, &worst, &fixed) &&
+        (best < 0 || worst < best)) {
+      *pl = trial;
+      best = worst;
+    }
+  }
+  return best;
 }
 
 // Cost of the whole-unit launch: cluster j visits units j, j + nc, ...

@@ -130,7 +130,9 @@ def test_plans_of_random_occupancies():
 def test_batch_64_and_32_take_plans():
     """The two steady shapes at budget 3276 on 76 two-CTA clusters: batch 64
     (six whole rounds, 56 units past them) and batch 32 (three rounds, 28)
-    take plans that give every cluster about the same work."""
+    take plans in which no cluster streams much more than the average (the
+    planner levels cost, so a range that meets two shared units is shorter,
+    and the last ranges may come out short or empty)."""
     for batch, rounds in ((64, 6), (32, 3)):
         n = [3276] * (batch * 8)
         plan = lf.lf_launch_plan_for(n, 2, 76, math.ceil(len(n) / 76) + 2)
@@ -141,7 +143,7 @@ def test_batch_64_and_32_take_plans():
             for x in it:
                 w += n[x[0]] if len(x) == 1 else (x[2] if x[2] is not None else n[x[0]]) - x[1]
             work.append(w)
-        assert max(work) - min(work) <= 2 * 64 * 2 + 3276 // 4, (max(work), min(work))
+        assert max(work) - sum(work) / len(work) <= 3276 // 4, (max(work), min(work))
         assert max(work) < (rounds + 1) * 3276
 
 
