@@ -19,6 +19,17 @@
 #include "lf_rkv.h"
 #include "longflow.h"
 
+// A launch plan: every cluster takes `rounds` whole units round-robin (the
+// units below rounds * nc), and before them one contiguous range of the units
+// past the whole rounds, cut so that the clusters' loads come out level (parts
+// first, so every cluster's parts start together and take about as long).
+// When those units are few, only as many clusters take ranges as keep every
+// shared unit within lf::kMaxSplitParts CTAs.
+struct Plan {
+  int rounds;
+  int cut_unit[lf::kTcMaxPlan + 1], cut_slot[lf::kTcMaxPlan + 1];
+};
+
 struct lf_cache {
   int layers, batch, kv_heads, q_heads, head_dim, capacity, slot_stride, window;
   int dtype, evict, cluster, stages, chunk, smem, device;
@@ -54,6 +65,11 @@ struct lf_cache {
   std::vector<int32_t> occ;  // [layers][batch]
   std::vector<int32_t> occ_limit;  // [batch]: budget (LongFlow) or capacity (append modes)
   std::vector<int32_t> plan_n;     // scratch: one layer's counts per unit
+  // Per layer, the occupancies of its last planning and the outcome: the same
+  // counts give the same plan, so a layer in steady state plans once.
+  std::vector<int32_t> memo_occ;       // [layers][batch]; -1: not planned yet
+  std::vector<signed char> memo_used;  // [layers]: the plan was taken
+  std::vector<Plan> memo_plan;         // [layers]
   float* split_stat;  // planned launches' exchanges through global memory (see TcArgs)
   float* split_fin;
   int32_t* split_cnt;
@@ -95,17 +111,6 @@ constexpr int kPlanMinSlots = LF_PLAN_MIN_SLOTS;
 constexpr long long kItemCost = LF_PLAN_ITEM_COST;
 constexpr long long kPartCost = LF_PLAN_PART_COST;
 
-// A launch plan: every cluster takes `rounds` whole units round-robin (the
-// units below rounds * nc), and before them one contiguous range of the units
-// past the whole rounds, cut so that the clusters' loads come out level (parts
-// first, so every cluster's parts start together and take about as long).
-// When those units are few, only as many clusters take ranges as keep every
-// shared unit within lf::kMaxSplitParts CTAs.
-struct Plan {
-  int rounds;
-  int cut_unit[lf::kTcMaxPlan + 1], cut_slot[lf::kTcMaxPlan + 1];
-};
-
 // Costs every cluster of `pl` as the kernel will run it: false when a shared
 // unit needs more than lf::kMaxSplitParts CTAs or a cluster more items than
 // the table holds.  `worst` is the costliest cluster's cost and fixed[j] the
@@ -113,11 +118,15 @@ struct Plan {
 bool cost_plan(const Plan& pl, const std::vector<int32_t>& n, int c, int nc, int max_items,
                const std::vector<long long>& load, long long* worst,
                std::vector<long long>* fixed) {
-  auto parts_of = [&](int uu) {  // clusters sharing unit uu: 1 + its inner cuts
-    int k = 1;
-    for (int q = 1; q < nc; ++q) k += (pl.cut_unit[q] == uu && pl.cut_slot[q] > 0) ? 1 : 0;
-    return k;
+  // Clusters sharing the unit of inner cut q: 1 + the unit's inner cuts, which
+  // are consecutive (cuts never go back).
+  int pos[lf::kTcMaxPlan + 1], tot[lf::kTcMaxPlan + 1];
+  auto same = [&](int q, int r) {  // cuts q and r: inner cuts of one unit
+    return pl.cut_slot[q] > 0 && pl.cut_slot[r] > 0 && pl.cut_unit[q] == pl.cut_unit[r];
   };
+  for (int q = 1; q < nc; ++q) pos[q] = (q > 1 && same(q - 1, q)) ? pos[q - 1] + 1 : 1;
+  for (int q = nc - 1; q >= 1; --q) tot[q] = (q + 1 < nc && same(q, q + 1)) ? tot[q + 1] : pos[q];
+  auto parts_of = [&](int q) { return 1 + tot[q]; };
   *worst = 0;
   for (int j = 0; j < nc; ++j) {
     const int u0 = pl.cut_unit[j], s0 = pl.cut_slot[j];
@@ -129,13 +138,13 @@ bool cost_plan(const Plan& pl, const std::vector<int32_t>& n, int c, int nc, int
       cost += (std::max(0LL, hi - s0) + c - 1) / c;
       fx += kItemCost + kPartCost;
       ++items;
-      if (parts_of(u0) * c > lf::kMaxSplitParts) return false;
+      if (parts_of(j) * c > lf::kMaxSplitParts) return false;
     }
     if (s1 > 0 && !(s0 > 0 && u1 == u0)) {
       cost += ((long long)std::min(s1, n[u1]) + c - 1) / c;
       fx += kItemCost + kPartCost;
       ++items;
-      if (parts_of(u1) * c > lf::kMaxSplitParts) return false;
+      if (parts_of(j + 1) * c > lf::kMaxSplitParts) return false;
     }
     for (int w = (s0 > 0) ? u0 + 1 : u0; w < u1; ++w) {  // units wholly inside the range
       cost += (n[w] + c - 1) / c;
@@ -228,8 +237,9 @@ long long make_plan(const std::vector<int32_t>& n, int c, int nc, int max_items,
   // Level: range lengths f_j = c (level - load_j), at least 0, summing to
   // `total` over the first ncp clusters; cut points at the running sums,
   // rounded to the grid and moved off short parts.
-  double lo_l = 0, hi_l = 1e18;
-  for (int it = 0; it < 100; ++it) {
+  double lo_l = 0, hi_l = (double)total / c + 1;
+  for (int j = 0; j < ncp; ++j) hi_l = std::max(hi_l, (double)load[j] + (double)total / c + 1);
+  for (int it = 0; it < 48; ++it) {
     const double mid = 0.5 * (lo_l + hi_l);
     double sum = 0;
     for (int j = 0; j < ncp; ++j) sum += std::max(0.0, (mid - load[j]) * c);
@@ -274,7 +284,7 @@ long long make_plan(const std::vector<int32_t>& n, int c, int nc, int max_items,
   hi_w += (double)total / c + (double)(units - first + 2) * (kItemCost + kPartCost) + 1;
   trial.rounds = rounds;
   if (walk_plan(n, c, ncp, nc, first, load, hi_w, gran, least, &trial)) {
-    for (int it = 0; it < 60; ++it) {
+    for (int it = 0; it < 40; ++it) {
       const double mid = 0.5 * (lo_w + hi_w);
       (walk_plan(n, c, ncp, nc, first, load, mid, gran, least, &trial) ? hi_w : lo_w) = mid;
     }
@@ -379,15 +389,26 @@ int encode_tensor_maps(lf_cache* c, size_t n_rows) {
 bool plan_layer(lf_cache* c, int layer, Plan* pl) {
   if (!c->plan_ok) return false;
   const int32_t* occ = c->occ.data() + (size_t)layer * c->batch;
+  int32_t* memo = c->memo_occ.data() + (size_t)layer * c->batch;
+  if (std::equal(occ, occ + c->batch, memo)) {
+    if (c->memo_used[layer]) *pl = c->memo_plan[layer];
+    return c->memo_used[layer] != 0;
+  }
   int shortest = INT_MAX;
   for (int b = 0; b < c->batch; ++b) {
     shortest = std::min(shortest, occ[b]);
     for (int g = 0; g < c->kv_heads; ++g) c->plan_n[(size_t)b * c->kv_heads + g] = occ[b];
   }
-  if (shortest < kPlanMinSlots) return false;
-  const long long rr = round_robin_cost(c->plan_n, c->cluster, c->grid_y);
-  const long long pc = make_plan(c->plan_n, c->cluster, c->grid_y, c->items, pl);
-  return pc >= 0 && pc < rr;
+  bool used = false;
+  if (shortest >= kPlanMinSlots) {
+    const long long rr = round_robin_cost(c->plan_n, c->cluster, c->grid_y);
+    const long long pc = make_plan(c->plan_n, c->cluster, c->grid_y, c->items, pl);
+    used = pc >= 0 && pc < rr;
+  }
+  std::copy(occ, occ + c->batch, memo);
+  c->memo_used[layer] = used ? 1 : 0;
+  if (used) c->memo_plan[layer] = *pl;
+  return used;
 }
 
 void destroy_memory(lf_cache* c) {
@@ -693,6 +714,8 @@ lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, i
   for (int b = 0; b < batch; ++b)  // append modes fill the slab to its capacity
     cache->occ_limit[b] = (kevict && c.budgets) ? c.budgets[b] : capacity;
   cache->plan_n.assign((size_t)units, 0);
+  cache->memo_occ.assign((size_t)layers * batch, -1);
+  cache->memo_used.assign((size_t)layers, 0);
   // Planned launches: the layer's slots cut into equal contiguous ranges, one
   // per cluster, when that balances better than whole units (decided per step
   // on the host).  Only for the per-KV-head LongFlow score without the deferred
@@ -703,6 +726,7 @@ lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, i
     if (plain && kern.decode_split && resident <= lf::kTcMaxPlan &&
         2 * cluster <= lf::kMaxSplitParts) {
       cache->plan_ok = 1;
+      cache->memo_plan.resize((size_t)layers);
       // every resident cluster, also when there are fewer units: a plan cuts
       // units into parts for the clusters a whole-unit launch would leave idle
       cache->grid_y = resident;
