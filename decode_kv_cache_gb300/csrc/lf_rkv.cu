@@ -25,7 +25,11 @@
 //           TMEM accumulators; a stage is refilled as soon as its MMAs
 //           complete, so the stream runs ahead of the epilogue; each pair
 //           (i, j) is looked at once and a near-duplicate pair counts for the
-//           older token.  The B x B cosine matrix never leaves the chip;
+//           older token.  The column tiles of row block I come in the order
+//           I+2, ..., then I+1, and the stage that holds tile I+1 becomes the
+//           next row block's buffer (the old one takes its place in the ring),
+//           so no row block is loaded twice and none waits for its load.  The
+//           B x B cosine matrix never leaves the chip;
 //   select  a radix select of the (Z, position) keys for the budget-th largest,
 //           observation tokens first;
 //   move    kept buffer tokens into the freed retained slots.
@@ -47,8 +51,8 @@ namespace {
 constexpr int kRkEpiWarps = 8;               // epilogue warps 0-7
 constexpr int kRkEpi = kRkEpiWarps * 32;
 constexpr int kRkProducerWarp = 8;
-constexpr int kRkMmaWarp = 9;
-constexpr int kRkThreads = 320;
+constexpr int kRkMmaWarp = 9;                // MMA warps 9 and 10: even and odd blocks
+constexpr int kRkThreads = 352;
 constexpr int kRkTile = 128;
 constexpr int kRkStages = 3;
 constexpr int kRkStage = kRkTile * 256;     // one K tile [128 rows][128 d] bf16: 32 KB
@@ -59,10 +63,34 @@ constexpr int kRkAcc = 3;                   // key dot-product accumulators, 128
 constexpr int kRkImpCol = kRkAcc * 128;     // two importance accumulators, 64 columns each
 constexpr int kRkPrefetch = 6;              // ring tiles requested into L2 ahead of their load
 
+// A position in the tile walk (see the kernel): pass 1 tile k, then column
+// tile J of row block I; `last` marks the row block's final tile.
+struct Walk {
+  int k, I, J;
+  bool last;
+};
+
+// Shared-memory buffers behind the ring stages and the row block.
+struct Bufs {
+  unsigned char* stage[kRkStages];
+  unsigned char* a;
+  __device__ void swap(int st) {
+    unsigned char* t = stage[st];
+    stage[st] = a;
+    a = t;
+  }
+};
+
+// Column block of the k-th key dot-product block of row block I: the diagonal,
+// then I+2, ..., nb-1, then I+1.
+__device__ __forceinline__ int col_block(int I, int k, int nb) {
+  return k == 0 ? I : (k < nb - I - 1 ? I + 1 + k : I + 1);
+}
+
 // Shared-memory plan (offsets from a 1024-byte aligned base).
 constexpr int kOffBars = 0;        // 19 mbarriers (see the kernel)
 constexpr int kOffTmem = 256;
-constexpr int kOffMisc = 272;      // [0] fail flag, [1] move count
+constexpr int kOffMisc = 272;      // [0] fail flag, [1] move count, [2] row blocks landed
 constexpr int kOffStats = 512;     // m[64], l[64]
 constexpr int kOffRed = 1024;      // [4 quarters][64 columns][2]
 constexpr int kOffNmin = 3072;     // per 32-slot chunk: smallest ||k|| (128 chunks)
@@ -104,14 +132,14 @@ __global__ void __launch_bounds__(kRkThreads, 1) rkv_compress_kernel(const __gri
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBars);
   uint64_t* full = bars;            // [3] ring stage landed
-  uint64_t* empty = bars + 3;       // [3] ring stage read (pass 1: by the epilogue; pass 2: MMAs)
+  uint64_t* empty = bars + 3;       // [3] ring stage read (both passes: by the epilogue)
   uint64_t* afull = bars + 6;       // row block landed
-  uint64_t* afree = bars + 7;       // every MMA reading the row block complete
   uint64_t* impfull = bars + 8;     // [2] importance logits ready
   uint64_t* impfree = bars + 10;    // [2] ... loaded by every epilogue warp
   uint64_t* accfull = bars + 12;    // [3] key dot products of a block ready
   uint64_t* accfree = bars + 15;    // [3] ... loaded by every epilogue warp
-  uint64_t* drain = bars + 18;      // every MMA complete
+  uint64_t* drain = bars + 18;      // every MMA of the first MMA warp complete
+  uint64_t* drain2 = bars + 7;      // ... of the second
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmem);
   volatile int* misc = reinterpret_cast<volatile int*>(smem + kOffMisc);
   float* m_col = reinterpret_cast<float*>(smem + kOffStats);
@@ -141,6 +169,7 @@ __global__ void __launch_bounds__(kRkThreads, 1) rkv_compress_kernel(const __gri
       mbar_init(&bars[i], ((i >= 10 && i < 12) || (i >= 15 && i < 18)) ? kRkEpiWarps : 1);
     fence_mbar_init();
     misc[0] = 0;
+    misc[2] = 0;
   }
   if (warp == 0) {
     __syncwarp();  // warp-collective allocation (thread 0 initialised the barriers alone)
@@ -184,26 +213,40 @@ __global__ void __launch_bounds__(kRkThreads, 1) rkv_compress_kernel(const __gri
                     bar, pol);
   };
 
+  // The tile walk shared by the producer (loads, L2 requests) and the MMA warp:
+  // pass 1 tiles 0..nb-1, then per row block I the column tiles I+2..nb-1 and
+  // I+1 (`last` set on I+1); -1 at the end.
+  auto next = [&](Walk& w) -> int {
+    w.last = false;
+    if (w.k < nb) return w.k++;
+    for (;;) {
+      if (w.I >= nb - 1) return -1;   // the last row block has no column tiles
+      if (w.J < nb) return w.J++;
+      if (w.J == nb) {
+        w.J = nb + 1;
+        w.last = true;
+        return w.I + 1;
+      }
+      ++w.I;
+      w.J = w.I + 2;
+    }
+  };
+  // The buffers behind the ring's stages and the row block, as the producer
+  // and the MMA warp both track them (the same swaps at the same tiles).
+  auto initial_bufs = [&]() {
+    Bufs b;
+    for (int i = 0; i < kRkStages; ++i) b.stage[i] = ring + i * kRkStage;
+    b.a = abuf;
+    return b;
+  };
+
   if (warp == kRkProducerWarp) {
     // ---- producer: the ring's tile sequence, pass 1 tiles 0..nb-1, then for
-    // each row block I the column tiles I+1..nb-1.  The ring is latency-bound
-    // (the tiles mostly come from L2), so every tile is also requested into L2
-    // kRkPrefetch places ahead of its load. ---------------------------------------
+    // each row block I the column tiles I+2..nb-1 and I+1.  The ring is
+    // latency-bound (the tiles mostly come from L2), so every tile is also
+    // requested into L2 kRkPrefetch places ahead of its load. ----------------------
     if (lane == 0) {
-      // walks the sequence: returns the next tile index, or -1 at the end
-      struct Walk {
-        int k, I, J;
-      };
-      auto next = [&](Walk& w) -> int {
-        if (w.k < nb) return w.k++;
-        for (;;) {
-          if (w.I >= nb) return -1;
-          if (w.J < nb) return w.J++;
-          ++w.I;
-          w.J = w.I + 1;
-        }
-      };
-      Walk ahead{0, 0, 1};
+      Walk ahead{0, 0, 2, false};
       for (int q = 0; q < kRkPrefetch; ++q) {
         const int t = next(ahead);
         if (t < 0) break;
@@ -211,7 +254,8 @@ __global__ void __launch_bounds__(kRkThreads, 1) rkv_compress_kernel(const __gri
           for (int blk = 0; blk < 2; ++blk)
             tma_prefetch_l2_2d(&ra.kmap, blk * 64, row0 + t * kRkTile + ro);
       }
-      Walk cur{0, 0, 1};
+      Walk cur{0, 0, 2, false};
+      Bufs bf = initial_bufs();
       int tt = 0;       // ring tiles issued
       for (int t = next(cur); t >= 0; t = next(cur), ++tt) {
         const int st = tt % kRkStages;
@@ -220,7 +264,8 @@ __global__ void __launch_bounds__(kRkThreads, 1) rkv_compress_kernel(const __gri
           misc[0] = 1;
           break;
         }
-        load_tile(ring + st * kRkStage, t, &full[st]);
+        load_tile(bf.stage[st], t, &full[st]);
+        if (cur.last) bf.swap(st);  // tile I+1: the next row block's buffer
         const int tp = next(ahead);
         if (tp >= 0)
           for (int ro = 0; ro < kRkTile; ro += 64)
@@ -232,92 +277,124 @@ __global__ void __launch_bounds__(kRkThreads, 1) rkv_compress_kernel(const __gri
         (void)mbar_wait_bounded(&full[t % kRkStages], (uint32_t)((t / kRkStages) & 1));
     }
     __syncwarp();
-  } else if (warp == kRkMmaWarp) {
-    // ---- MMA warp (lane 0): the same tile order as the producer; it also loads
-    // each row block into its own buffer once the previous block's MMAs are done,
-    // so the producer's stream runs on across row blocks --------------------------
+  } else if (warp == kRkMmaWarp || warp == kRkMmaWarp + 1) {
+    // ---- MMA warps (lane 0 of each): the same tile order as the producer.  The
+    // two warps take turns, item by item (a tile's importance in pass 1, and in
+    // pass 2 a row block's importance and its key dot-product blocks), so that
+    // one issues while the other waits on its barriers: a single issuing thread
+    // left the tensor cores idle between blocks.  Both walk every item to keep
+    // the same counters; each waits only for what its own MMAs read. ----------
     if (lane == 0) {
+      const int par = warp - kRkMmaWarp;
       const uint32_t id_imp = idesc_bf16_f32(128, QN16, false, false);
       const uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
       const uint32_t q0 = smem_u32(qop);
       bool fail = false;
       int rt = 0;   // ring tiles consumed
-      int it = 0;   // importance accumulators used
-      int at = 0;   // key dot-product accumulators used
-      int na = 0;   // row blocks requested
+      int it = 0;   // importance items (accumulator it % 2 = the warp that takes it)
+      int at = 0;   // key dot-product blocks (accumulator at % kRkAcc)
       auto wait = [&](uint64_t* bar, uint32_t parity) {
         if (!fail && (misc[0] || !mbar_wait_bounded(bar, parity))) fail = true;
         return !fail;
       };
-      // S = tile . Q^T into importance accumulator it % 2
+      // S = tile . Q^T into importance accumulator it % 2, by warp it % 2
       auto mma_imp = [&](uint32_t a0) {
         const int ib = it & 1;
-        if (it >= 2 && !wait(&impfree[ib], (uint32_t)(((it >> 1) - 1) & 1))) return;
-        tc_fence_after();
+        if (ib == par && !fail) {
+          if (it >= 2 && !wait(&impfree[ib], (uint32_t)(((it >> 1) - 1) & 1))) return;
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          tc_mma_bf16(tm + (uint32_t)(kRkImpCol + ib * 64),
-                      sw128_desc(a0 + (kk >> 2) * kRkBlock + (kk & 3) * 32, 16, 1024),
-                      sw128_desc(q0 + (kk >> 2) * kRkQBlock + (kk & 3) * 32, 16, 1024), id_imp,
-                      kk > 0 ? 1u : 0u);
-        tc_commit(&impfull[ib]);
+          for (int kk = 0; kk < D / 16; ++kk)
+            tc_mma_bf16(tm + (uint32_t)(kRkImpCol + ib * 64),
+                        sw128_desc(a0 + (kk >> 2) * kRkBlock + (kk & 3) * 32, 16, 1024),
+                        sw128_desc(q0 + (kk >> 2) * kRkQBlock + (kk & 3) * 32, 16, 1024),
+                        id_imp, kk > 0 ? 1u : 0u);
+          tc_commit(&impfull[ib]);
+        }
         ++it;
       };
-      // row block 0 is not used in pass 1: request it now
-      load_tile(abuf, 0, afull);
-      na = 1;
+      // row block 0 (the others come through the ring): request it now
+      if (par == 0) load_tile(abuf, 0, afull);
       // pass 1: the stage is released by the epilogue (it also reads ||k|| there)
       for (int t = 0; t < nb && !fail; ++t) {
         const int st = rt % kRkStages;
-        if (!wait(&full[st], (uint32_t)((rt / kRkStages) & 1))) break;
-        tc_fence_after();
+        if ((it & 1) == par) {
+          if (!wait(&full[st], (uint32_t)((rt / kRkStages) & 1))) break;
+          tc_fence_after();
+        }
         mma_imp(smem_u32(ring + st * kRkStage));
         ++rt;
       }
       // pass 2
-      const uint32_t a0 = smem_u32(abuf);
+      Bufs bf = initial_bufs();
+      volatile int* landed = misc + 2;   // row blocks known to have landed, besides 0
       for (int I = 0; I < nb && !fail; ++I) {
-        if (!wait(afull, (uint32_t)(I & 1))) break;
+        const uint32_t a0 = smem_u32(bf.a);
+        // The row block has landed: row block 0 by its own copy; row block I > 0
+        // as row block I - 1's last column tile, which one of the two warps
+        // waited for.  That warp raises a counter (the stage's barrier may have
+        // moved on to its next tile by the time the other warp gets here).
+        if (I == 0) {
+          if (!wait(afull, 0)) break;
+        } else if (*landed < I) {
+          const unsigned long long t0 = global_ns();
+          while (*landed < I && !misc[0]) {
+            __nanosleep(32);
+            if (global_ns() - t0 > kWaitLimitNs) {
+              fail = true;
+              break;
+            }
+          }
+          if (fail || misc[0]) {
+            fail = true;
+            break;
+          }
+        }
+        __threadfence_block();
         tc_fence_after();
         mma_imp(a0);
-        for (int J = I; J < nb && !fail; ++J) {
+        for (int k = 0; k < nb - I && !fail; ++k) {
           const int acc = at % kRkAcc;
-          if (at >= kRkAcc && !wait(&accfree[acc], (uint32_t)(((at / kRkAcc) - 1) & 1))) break;
-          int st = -1;
-          uint32_t b0 = a0;   // the diagonal block: K_I . K_I^T
-          if (J > I) {
-            st = rt % kRkStages;
-            if (!wait(&full[st], (uint32_t)((rt / kRkStages) & 1))) break;
-            b0 = smem_u32(ring + st * kRkStage);
-          }
-          tc_fence_after();
+          const int st = (k > 0) ? rt % kRkStages : -1;
+          if ((at & 1) == par) {
+            if (at >= kRkAcc && !wait(&accfree[acc], (uint32_t)(((at / kRkAcc) - 1) & 1))) break;
+            uint32_t b0 = a0;   // the diagonal block: K_I . K_I^T
+            if (st >= 0) {
+              if (!wait(&full[st], (uint32_t)((rt / kRkStages) & 1))) break;
+              b0 = smem_u32(bf.stage[st]);
+              if (k == nb - I - 1) {   // tile I + 1, the next row block, has landed
+                __threadfence_block();
+                *landed = I + 1;
+              }
+            }
+            tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            tc_mma_bf16(tm + (uint32_t)(acc * 128),
-                        sw128_desc(a0 + (kk >> 2) * kRkBlock + (kk & 3) * 32, 16, 1024),
-                        sw128_desc(b0 + (kk >> 2) * kRkBlock + (kk & 3) * 32, 16, 1024), id_s,
-                        kk > 0 ? 1u : 0u);
-          tc_commit(&accfull[acc]);
+            for (int kk = 0; kk < D / 16; ++kk)
+              tc_mma_bf16(tm + (uint32_t)(acc * 128),
+                          sw128_desc(a0 + (kk >> 2) * kRkBlock + (kk & 3) * 32, 16, 1024),
+                          sw128_desc(b0 + (kk >> 2) * kRkBlock + (kk & 3) * 32, 16, 1024), id_s,
+                          kk > 0 ? 1u : 0u);
+            tc_commit(&accfull[acc]);
+          }
           if (st >= 0) {
-            tc_commit(&empty[st]);
+            // The epilogue hands the stage back once it sees the block's
+            // products, in block order, so after every earlier block's: for the
+            // row block's last tile (I + 1, kept as the next row block) that
+            // covers every MMA on the old row block, whose buffer takes its
+            // place in the ring.
+            if (k == nb - I - 1) bf.swap(st);
             ++rt;
           }
           ++at;
         }
-        // the next row block goes into the buffer once these MMAs have read it
-        if (!fail && I + 1 < nb) {
-          tc_commit(afree);
-          if (!wait(afree, (uint32_t)(I & 1))) break;
-          load_tile(abuf, I + 1, afull);
-          ++na;
-        }
       }
       if (fail) misc[0] = 1;
-      // every MMA issued completes before tensor memory is released, and the
-      // last row block requested lands before the CTA may exit
-      tc_commit(drain);
-      (void)mbar_wait_bounded(drain, 0);
-      (void)mbar_wait_bounded(afull, (uint32_t)((na - 1) & 1));
+      // every MMA issued completes before tensor memory is released, and row
+      // block 0 lands before the CTA may exit
+      uint64_t* dr = par == 0 ? drain : drain2;
+      tc_commit(dr);
+      (void)mbar_wait_bounded(dr, 0);
+      if (par == 0) (void)mbar_wait_bounded(afull, 0);
     }
     __syncwarp();
   } else {
@@ -450,6 +527,7 @@ __global__ void __launch_bounds__(kRkThreads, 1) rkv_compress_kernel(const __gri
 
     // ---- pass 2: importance, then near-duplicate counts over blocks J >= I ---------
     int at = 0;
+    int rt = nb;   // ring tiles consumed (pass 1 took nb)
     for (int I = 0; I < nb; ++I) {
       const int row = I * kRkTile + r;   // this thread's token
       {
@@ -468,9 +546,13 @@ __global__ void __launch_bounds__(kRkThreads, 1) rkv_compress_kernel(const __gri
       const float thr_i = (inv_i > 0.f) ? ra.tau / inv_i : INFINITY;   // tau * ||k_i||
       const int pos_i = pos_s[min(row, kRkvMaxSlots - 1)];
       int cnt = 0;
-      for (int J = I; J < nb; ++J, ++at) {
+      for (int k = 0; k < nb - I; ++k, ++at) {
+        const int J = col_block(I, k, nb);
         const int acc = at % kRkAcc;
+        const int st = (k > 0) ? (rt++) % kRkStages : -1;   // the block's column tile's stage
         if (!wait(&accfull[acc], (uint32_t)((at / kRkAcc) & 1))) continue;
+        // that tile has been read: its stage may be refilled
+        if (st >= 0 && tid == 0) mbar_arrive(&empty[st]);
         tc_fence_after();
         // columns 64*half .. +63 of block J: both warp-collective loads first, then
         // hand the accumulator back, then each thread's own (divergent) tests
@@ -489,15 +571,34 @@ __global__ void __launch_bounds__(kRkThreads, 1) rkv_compress_kernel(const __gri
 #pragma unroll
           for (int c = 0; c < 32; ++c) mx = fmaxf(mx, v[cc][c]);
           // quick rejection: cos >= tau needs S_ij >= tau ||k_i|| ||k_j|| >= thr_i * min ||k_j||
-          if (mx < thr_i * nmin[j0 >> 5]) continue;
+          const bool rejected = mx < thr_i * nmin[j0 >> 5];
+          if (__all_sync(0xffffffffu, rejected)) continue;
+          // The exact test on every column, the same instructions for every lane
+          // (the chunk's 1/||k_j|| are broadcast loads), as a mask of hits.
+          uint32_t hits = 0;
+          const float4* iv4 = reinterpret_cast<const float4*>(inv_s + j0);
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const int j = j0 + c;
-            const bool valid = row < n && j < n && (J != I || j > row);
-            if (valid && v[cc][c] * inv_s[j] >= thr_i) {
-              if (pos_s[j] > pos_i) ++cnt;                 // a later near-duplicate of i
-              else atomicAdd(&cnt_s[j], 1);                 // i is the later one: j is older
-            }
+          for (int q = 0; q < 8; ++q) {
+            const float4 w = iv4[q];
+            hits |= (v[cc][4 * q] * w.x >= thr_i ? 1u : 0u) << (4 * q);
+            hits |= (v[cc][4 * q + 1] * w.y >= thr_i ? 1u : 0u) << (4 * q + 1);
+            hits |= (v[cc][4 * q + 2] * w.z >= thr_i ? 1u : 0u) << (4 * q + 2);
+            hits |= (v[cc][4 * q + 3] * w.w >= thr_i ? 1u : 0u) << (4 * q + 3);
+          }
+          // only tokens (j < n), and on the diagonal block only j > row
+          const int lim = n - j0;
+          if (rejected || row >= n || lim <= 0) hits = 0;
+          else if (lim < 32) hits &= (1u << lim) - 1u;
+          if (J == I) {
+            const int d = row - j0 + 1;   // columns c >= d have j > row
+            if (d >= 32) hits = 0;
+            else if (d > 0) hits &= ~((1u << d) - 1u);
+          }
+          while (hits) {
+            const int j = j0 + __ffs(hits) - 1;
+            hits &= hits - 1u;
+            if (pos_s[j] > pos_i) ++cnt;                 // a later near-duplicate of i
+            else atomicAdd(&cnt_s[j], 1);                 // i is the later one: j is older
           }
         }
       }
