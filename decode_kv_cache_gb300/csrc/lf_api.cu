@@ -96,6 +96,9 @@ void clear_last() {
 #endif
 constexpr int kPlanMinSlots = LF_PLAN_MIN_SLOTS;
 
+// Slot rows per CTA below which a decode launch gets no prefetch hints.
+constexpr long long kPrefetchMinRows = 2048;
+
 // Host cost model of one launch, in CTA slot rows (one row of K and V streamed
 // by one CTA, ~12.5 ns in a steady launch): every item a CTA visits adds a unit
 // boundary, and every part of a shared unit adds its two exchanges through L2.
@@ -575,29 +578,33 @@ lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, i
     cuda_fail(e, "cudaDeviceGetAttribute");
     return nullptr;
   }
-  if ((e = cudaFuncSetAttribute(kern.decode, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                max_optin)) != cudaSuccess ||
-      (e = cudaFuncSetAttribute(kern.decode, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) !=
-          cudaSuccess ||
-      (kern.decode_split &&
-       ((e = cudaFuncSetAttribute(kern.decode_split, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  auto set_attributes = [&](const lf::KernelEntry& k) -> bool {
+    if ((e = cudaFuncSetAttribute(k.decode, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   max_optin)) != cudaSuccess ||
-        (e = cudaFuncSetAttribute(kern.decode_split,
-                                  cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) !=
-            cudaSuccess))) {
-    cuda_fail(e, "cudaFuncSetAttribute");
-    return nullptr;
-  }
+        (e = cudaFuncSetAttribute(k.decode, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) !=
+            cudaSuccess ||
+        (k.decode_split &&
+         ((e = cudaFuncSetAttribute(k.decode_split, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    max_optin)) != cudaSuccess ||
+          (e = cudaFuncSetAttribute(k.decode_split,
+                                    cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) !=
+              cudaSuccess))) {
+      cuda_fail(e, "cudaFuncSetAttribute");
+      return false;
+    }
+    return true;
+  };
+  if (!set_attributes(kern)) return nullptr;
 
   // Launch shape.  CUDA-core kernel: one cluster of C CTAs per unit; prefer
   // the smallest C giving at least 8 CTAs per SM with >= 128 slots per CTA.
   // Tensor-core kernel: persistent, one CTA per SM; prefer the smallest C
   // whose per-CTA chunk fits next to a ring of `stages` 32 KB tiles.  The
   // caller may force C and the ring depth.
-  const bool tc = (kern.kind == lf::kTensorCore);
-  const int threads = tc ? lf::kTcThreads : lf::kThreads;
+  bool tc = (kern.kind == lf::kTensorCore);
+  int threads = tc ? lf::kTcThreads : lf::kThreads;
   const int units = batch * kv_heads;
-  const int stages = c.stages ? c.stages : (tc ? 3 : 4);
+  int stages = c.stages ? c.stages : (tc ? 3 : 4);
   // The shared memory, resident clusters and item-table size of one cluster size;
   // false if it does not fit.
   int chunk = 0, smem = 0, grid_y = 0, items = 0, resident = 0;
@@ -633,17 +640,36 @@ lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, i
     }
     return fits > 0;
   };
-  int cluster = c.cluster;
-  if (cluster == 0) {
-    cluster = 1;
-    if (!tc)
-      while (cluster < lf::kMaxCluster && (long long)units * cluster < 8LL * num_sms &&
-             (capacity + 2 * cluster - 1) / (2 * cluster) >= 128)
-        cluster *= 2;
-  }
+  auto first_cluster = [&]() {
+    int cl = c.cluster;
+    if (cl == 0) {
+      cl = 1;
+      if (!tc)
+        while (cl < lf::kMaxCluster && (long long)units * cl < 8LL * num_sms &&
+               (capacity + 2 * cl - 1) / (2 * cl) >= 128)
+          cl *= 2;
+    }
+    return cl;
+  };
+  int cluster = first_cluster();
   for (;;) {
     if (try_shape(cluster)) break;
     if (c.cluster != 0 || cluster >= lf::kMaxCluster) {
+      // The tensor-core kernel chosen by default may not take a very large
+      // layer (its per-cluster item table holds kTcMaxItems units, and long
+      // units need large clusters): the CUDA-core kernel, one cluster per unit,
+      // takes any number of units.
+      lf::KernelEntry simt;
+      if (tc && c.kernel == LF_KERNEL_AUTO && c.cluster == 0 &&
+          lf::find_kernels_bf16(head_dim, group, &simt)) {
+        if (!set_attributes(simt)) return nullptr;
+        kern = simt;
+        tc = false;
+        threads = lf::kThreads;
+        stages = c.stages ? c.stages : 4;
+        cluster = first_cluster();
+        continue;
+      }
       fail(LF_ERR_UNSUPPORTED, "launch does not fit: cluster %d, %d stages, %d slots per CTA need "
            "%d bytes of shared memory (max %d)", cluster, stages, chunk, smem, max_optin);
       return nullptr;
@@ -1005,6 +1031,32 @@ int lf_decode_step(lf_cache* cache, int layer, const void* q, const void* k_new,
         ta.cut_unit[j] = pl.cut_unit[j];
         ta.cut_slot[j] = pl.cut_slot[j];
       }
+    }
+    // Each cluster's first unit (the kernel's item order: the part its range
+    // starts inside, else the part it ends inside, else a whole unit of the
+    // range, else its first round) and the host's count of its slots, for the
+    // kernel's L2 prefetch before its grid dependency wait.  Only for launches
+    // of at least kPrefetchMinRows slot rows per CTA: a short launch's CTAs
+    // start as the previous grid ends, and the prefetch then delays them
+    // (measured on qwen3-0.6b, 215 rows per CTA: 11.2 -> 12.1 us per launch).
+    const int units = cache->batch * cache->kv_heads;
+    const int32_t* occ = cache->occ.data() + (size_t)layer * cache->batch;
+    long long slots = 0;
+    for (int b = 0; b < cache->batch; ++b) slots += (long long)occ[b] * cache->kv_heads;
+    const bool hint = slots >= (long long)kPrefetchMinRows * cache->grid_y * cache->cluster;
+    for (int j = 0; j < lf::kTcMaxPlan; ++j) {
+      int u = -1;
+      if (hint && j < cache->grid_y) {
+        if (!planned) {
+          u = j < units ? j : -1;
+        } else {
+          const int u0 = pl.cut_unit[j], s0 = pl.cut_slot[j];
+          const int u1 = pl.cut_unit[j + 1], s1 = pl.cut_slot[j + 1];
+          u = s0 > 0 ? u0 : s1 > 0 ? u1 : u1 > u0 ? u0 : (pl.rounds > 0 ? j : -1);
+        }
+      }
+      ta.hint_unit[j] = u;
+      ta.hint_n[j] = (u >= 0 && u < units) ? occ[u / cache->kv_heads] : 0;
     }
     void* args[] = {&ta};
     e = cudaLaunchKernelExC(&cfg, planned ? cache->kern.decode_split : cache->kern.decode, args);

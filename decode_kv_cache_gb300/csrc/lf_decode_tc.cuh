@@ -98,6 +98,11 @@ struct TcArgs {
   int* split_cnt;                  // [plan_nc][2]: arrivals at the two exchanges
   int cut_unit[kTcMaxPlan + 1];
   int cut_slot[kTcMaxPlan + 1];    // multiples of 4
+  // The host's guess at cluster j's first unit and its occupied slots, for the
+  // L2 prefetch before the grid dependency wait (a hint: the copies proper read
+  // the counts from memory); hint_n[j] <= 0 or another first unit: no prefetch.
+  int hint_unit[kTcMaxPlan];
+  int hint_n[kTcMaxPlan];
 };
 
 // One cluster's part of a shared unit in a planned launch.
@@ -238,6 +243,45 @@ struct TcPlan {
   }
 };
 
+// The L2 prefetch of a CTA's first unit before the grid dependency wait (see
+// the kernel): rows [lo, hi) of unit u clipped to its n occupied slots, this
+// CTA's share of them, as the copies proper will read them (64-row boxes, then
+// 16-row granules, up to kPrefetchTiles tiles), its norms and positions, and
+// the group's queries.  Out of line: a launch without hints pays nothing for it.
+template <int G>
+__device__ __noinline__ void prefetch_first_unit(const TcArgs& ta, int u, int lo, int hi, int n,
+                                                 int C, int rank) {
+  constexpr int D = 128;
+  using T = __nv_bfloat16;
+  const DecodeArgs& a = ta.a;
+  const int lo2 = min(lo, n);
+  const int hi2 = min(hi, n);
+  const int per = ((hi2 - lo2 + C - 1) / C + 3) & ~3;
+  const int base = lo2 + rank * per;
+  const int rows = max(0, min(per, hi2 - base));
+  const int row0 = ta.row_base + u * a.slot_stride + base;
+  const int lim = min((rows + 15) & ~15, kPrefetchTiles * kTcTile);
+  int r = 0;
+  for (; r + 64 <= lim; r += 64) {
+    tma_prefetch_l2_2d(&ta.k64, 0, row0 + r);
+    tma_prefetch_l2_2d(&ta.k64, 64, row0 + r);
+  }
+  for (; r < lim; r += 16) {
+    tma_prefetch_l2_2d(&ta.k16, 0, row0 + r);
+    tma_prefetch_l2_2d(&ta.k16, 64, row0 + r);
+  }
+  if (rows > 0 && a.evict) {
+    const size_t ub = (size_t)u * a.slot_stride + base;
+    const uint32_t small = (uint32_t)(((rows + 3) & ~3) * 4);
+    bulk_prefetch_l2((a.score == LF_SCORE_H2O ? a.acc : a.vnorm) + ub, small);
+    bulk_prefetch_l2(a.pos + ub, small);
+  }
+  const int bb = u / a.kv_heads;
+  bulk_prefetch_l2(reinterpret_cast<const T*>(a.q) +
+                       ((size_t)bb * a.q_heads + (size_t)(u - bb * a.kv_heads) * G) * D,
+                   (uint32_t)(G * D * sizeof(T)));
+}
+
 template <int G, bool kSplit = false>
 __global__ void __launch_bounds__(kTcThreads, 1)
     decode_step_tc_kernel(const __grid_constant__ TcArgs ta) {
@@ -370,46 +414,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // While the previous grid on the stream finishes (its last units leave HBM
     // mostly idle), bring the first K tiles of this CTA's first unit, its norms
     // and positions and its queries into L2.  A hint only: the copies proper
-    // come after the wait below and read memory again, and the occupancy is
-    // read without ordering, so a stale value costs bandwidth and nothing else.
-    if (nitems > 0 && kPrefetchTiles > 0) {
-      int u = j, lo = 0, hi = INT_MAX;
-      if (npc > 0) {
-        u = pcs[0].unit;
-        lo = pcs[0].lo;
-        hi = pcs[0].hi;
-      } else if (w1 > w0) {
-        u = w0;
-      }
-      const int n = min(max(ld_relaxed(a.count + u), 0), a.capacity);
-      const int lo2 = min(lo, n);
-      const int hi2 = min(hi, n);
-      const int per = ((hi2 - lo2 + C - 1) / C + 3) & ~3;
-      const int base = lo2 + rank * per;
-      const int rows = max(0, min(per, hi2 - base));
-      const int row0 = ta.row_base + u * a.slot_stride + base;
-      // The boxes of the copies proper: 64-row boxes, then 16-row granules.
-      const int lim = min((rows + 15) & ~15, kPrefetchTiles * kTcTile);
-      int r = 0;
-      for (; r + 64 <= lim; r += 64) {
-        tma_prefetch_l2_2d(&ta.k64, 0, row0 + r);
-        tma_prefetch_l2_2d(&ta.k64, 64, row0 + r);
-      }
-      for (; r < lim; r += 16) {
-        tma_prefetch_l2_2d(&ta.k16, 0, row0 + r);
-        tma_prefetch_l2_2d(&ta.k16, 64, row0 + r);
-      }
-      if (rows > 0 && a.evict) {
-        const size_t ub = (size_t)u * a.slot_stride + base;
-        const uint32_t small = (uint32_t)(((rows + 3) & ~3) * 4);
-        bulk_prefetch_l2((a.score == LF_SCORE_H2O ? a.acc : a.vnorm) + ub, small);
-        bulk_prefetch_l2(a.pos + ub, small);
-      }
-      const int bb = u / a.kv_heads;
-      bulk_prefetch_l2(reinterpret_cast<const T*>(a.q) +
-                           ((size_t)bb * a.q_heads + (size_t)(u - bb * a.kv_heads) * G) * D,
-                       (uint32_t)(G * D * sizeof(T)));
+    // come after the wait below and read memory again; the occupancy is the
+    // host's (a kernel parameter: no global load holds up the set-up), so a
+    // wrong value costs bandwidth and nothing else.
+    int u = j, lo = 0, hi = INT_MAX;
+    if (npc > 0) {
+      u = pcs[0].unit;
+      lo = pcs[0].lo;
+      hi = pcs[0].hi;
+    } else if (w1 > w0) {
+      u = w0;
     }
+    if (nitems > 0 && kPrefetchTiles > 0 && j < kTcMaxPlan && ta.hint_unit[j] == u &&
+        ta.hint_n[j] > 0)
+      prefetch_first_unit<G>(ta, u, lo, hi, min(ta.hint_n[j], a.capacity), C, rank);
   }
   if (tid == 0) *fail_any = 0;
   // Operand buffers start at zero (padding rows of q^T and P^T stay zero).

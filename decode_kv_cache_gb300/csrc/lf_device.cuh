@@ -174,13 +174,6 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
-// A load not ordered against other threads' writes: the value may be stale.
-__device__ __forceinline__ int ld_relaxed(const int* p) {
-  int v;
-  asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
 // 2-D tiled TMA load of box {x .. x+box0, y .. y+box1} into this CTA's smem.
 __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, int y,
                                             uint64_t* bar, uint64_t policy) {

@@ -100,7 +100,8 @@ typedef enum lf_evict {
 
 /* Which decode kernel to build the cache for. */
 typedef enum lf_kernel {
-  LF_KERNEL_AUTO = 0,        /* tensor cores where supported, else CUDA cores */
+  LF_KERNEL_AUTO = 0,        /* tensor cores where supported and the layer fits their
+                                launch shape (per-cluster item table), else CUDA cores */
   LF_KERNEL_SIMT = 1,        /* CUDA-core dot products (every dtype / head_dim) */
   LF_KERNEL_TENSOR_CORE = 2  /* tcgen05 MMAs: bf16, head_dim 128, group 1/2/4/8 */
 } lf_kernel;

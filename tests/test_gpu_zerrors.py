@@ -28,9 +28,9 @@ def test_slab_larger_than_the_device_is_refused():
     # has a launch shape) for 2000 layers: K alone is 2000 x 432 MB = 858 GB.
     with pytest.raises(lf.LFError, match="out of memory|does not fit"):
         lf.lf_cache_create_ex(2000, 64, 8, 32, 128, 3276, 64)
-    # 8192 units of 16384 slots: no tensor-core launch shape fits (checked before
-    # any allocation)
-    with pytest.raises(lf.LFError, match="does not fit"):
+    # 8192 units of 16384 slots for 64 layers (4.4 TB): no tensor-core launch
+    # shape fits, and the CUDA-core kernel's slab does not fit the device
+    with pytest.raises(lf.LFError, match="out of memory|does not fit"):
         lf.lf_cache_create_ex(64, 1024, 8, 32, 128, 16384, 64)
     with lf.LFCache(1, 2, 2, 4, 128, 64, 4) as cache:   # the context still works
         _small_step(cache)
