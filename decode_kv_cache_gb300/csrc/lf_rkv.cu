@@ -54,7 +54,7 @@ constexpr int kRkProducerWarp = 8;
 constexpr int kRkMmaWarp = 9;                // MMA warps 9 and 10: even and odd blocks
 constexpr int kRkThreads = 352;
 constexpr int kRkTile = 128;
-constexpr int kRkStages = 3;
+constexpr int kRkStages = 4;
 constexpr int kRkStage = kRkTile * 256;     // one K tile [128 rows][128 d] bf16: 32 KB
 constexpr int kRkBlock = kRkTile * 128;     // one 64-column half of it: 16 KB
 constexpr int kRkQRows = 64;                // observation query rows (alpha * G <= 64)
@@ -88,7 +88,8 @@ __device__ __forceinline__ int col_block(int I, int k, int nb) {
 }
 
 // Shared-memory plan (offsets from a 1024-byte aligned base).
-constexpr int kOffBars = 0;        // 19 mbarriers (see the kernel)
+constexpr int kRkBars = 2 * kRkStages + 13;   // mbarriers (see the kernel)
+constexpr int kOffBars = 0;
 constexpr int kOffTmem = 256;
 constexpr int kOffMisc = 272;      // [0] fail flag, [1] move count, [2] row blocks landed
 constexpr int kOffStats = 512;     // m[64], l[64]
@@ -97,15 +98,15 @@ constexpr int kOffNmin = 3072;     // per 32-slot chunk: smallest ||k|| (128 chu
 constexpr int kOffA = 4096;        // the row block of pass 2
 constexpr int kOffRing = kOffA + kRkStage;
 constexpr int kOffQ = kOffRing + kRkStages * kRkStage;
-constexpr int kOffPos = kOffQ + 2 * kRkQBlock;
-constexpr int kOffInv = kOffPos + kRkvMaxSlots * 4;
-constexpr int kOffCnt = kOffInv + kRkvMaxSlots * 4;
-constexpr int kOffZ = kOffCnt + kRkvMaxSlots * 4;
+constexpr int kOffInv = kOffQ + 2 * kRkQBlock;
+constexpr int kOffCnt = kOffInv + kRkvMaxSlots * 4;       // 16-bit counts, two per word
+constexpr int kOffZ = kOffCnt + kRkvMaxSlots * 2;
 constexpr int kSmem = kOffZ + kRkvMaxSlots * 4 + 1024;  // + alignment slack
 static_assert(kOffA % 1024 == 0 && kOffRing % 1024 == 0 && kOffQ % 1024 == 0, "alignment");
 static_assert(kOffMisc + 16 <= kOffStats && kOffStats + 2 * kRkQRows * 4 <= kOffRed, "header");
 // the sort reuses the ring: 64-bit keys then 16-bit slot indices
 static_assert(kRkvMaxSlots * 10 <= kRkStages * kRkStage, "sort space");
+static_assert(kOffBars + kRkBars * 8 <= kOffTmem, "barriers");
 
 __device__ __forceinline__ uint32_t orderable(float z) {
   const uint32_t u = __float_as_uint(z);
@@ -131,15 +132,17 @@ __global__ void __launch_bounds__(kRkThreads, 1) rkv_compress_kernel(const __gri
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBars);
-  uint64_t* full = bars;            // [3] ring stage landed
-  uint64_t* empty = bars + 3;       // [3] ring stage read (both passes: by the epilogue)
-  uint64_t* afull = bars + 6;       // row block landed
-  uint64_t* impfull = bars + 8;     // [2] importance logits ready
-  uint64_t* impfree = bars + 10;    // [2] ... loaded by every epilogue warp
-  uint64_t* accfull = bars + 12;    // [3] key dot products of a block ready
-  uint64_t* accfree = bars + 15;    // [3] ... loaded by every epilogue warp
-  uint64_t* drain = bars + 18;      // every MMA of the first MMA warp complete
-  uint64_t* drain2 = bars + 7;      // ... of the second
+  // barriers: full / empty per ring stage, then the fixed ones
+  uint64_t* full = bars;                      // [kRkStages] ring stage landed
+  uint64_t* empty = bars + kRkStages;         // [kRkStages] ring stage read (by the epilogue)
+  uint64_t* fixed = bars + 2 * kRkStages;
+  uint64_t* afull = fixed;                    // row block 0 landed
+  uint64_t* drain2 = fixed + 1;               // every MMA of the second MMA warp complete
+  uint64_t* impfull = fixed + 2;              // [2] importance logits ready
+  uint64_t* impfree = fixed + 4;              // [2] ... loaded by every epilogue warp
+  uint64_t* accfull = fixed + 6;              // [3] key dot products of a block ready
+  uint64_t* accfree = fixed + 9;              // [3] ... loaded by every epilogue warp
+  uint64_t* drain = fixed + 12;               // every MMA of the first MMA warp complete
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmem);
   volatile int* misc = reinterpret_cast<volatile int*>(smem + kOffMisc);
   float* m_col = reinterpret_cast<float*>(smem + kOffStats);
@@ -149,9 +152,13 @@ __global__ void __launch_bounds__(kRkThreads, 1) rkv_compress_kernel(const __gri
   unsigned char* abuf = smem + kOffA;
   unsigned char* ring = smem + kOffRing;
   unsigned char* qop = smem + kOffQ;
-  int32_t* pos_s = reinterpret_cast<int32_t*>(smem + kOffPos);
+  const int32_t* posg = ra.pos + ubase;   // positions, read from global memory (L2)
   float* inv_s = reinterpret_cast<float*>(smem + kOffInv);
-  int* cnt_s = reinterpret_cast<int*>(smem + kOffCnt);
+  // Near-duplicate counts, 16 bits per token (at most n - 1 < 65536: no carry
+  // into the neighbour), added with 32-bit atomics on the word holding them.
+  uint32_t* cnt_w = reinterpret_cast<uint32_t*>(smem + kOffCnt);
+  auto cnt_add = [&](int i, int v) { atomicAdd(&cnt_w[i >> 1], (uint32_t)v << ((i & 1) * 16)); };
+  auto cnt_get = [&](int i) { return (int)((cnt_w[i >> 1] >> ((i & 1) * 16)) & 0xFFFFu); };
   float* z_s = reinterpret_cast<float*>(smem + kOffZ);
 
   const int n = ra.count[unit];
@@ -165,8 +172,11 @@ __global__ void __launch_bounds__(kRkThreads, 1) rkv_compress_kernel(const __gri
 
   // ---- set-up: barriers, tensor memory, positions, the query operand -------------
   if (tid == 0) {
-    for (int i = 0; i < 19; ++i)   // impfree, accfree: one arrival per epilogue warp
-      mbar_init(&bars[i], ((i >= 10 && i < 12) || (i >= 15 && i < 18)) ? kRkEpiWarps : 1);
+    for (int i = 0; i < kRkBars; ++i) {  // impfree, accfree: one arrival per epilogue warp
+      const bool per_warp = (&bars[i] >= impfree && &bars[i] < impfree + 2) ||
+                            (&bars[i] >= accfree && &bars[i] < accfree + kRkAcc);
+      mbar_init(&bars[i], per_warp ? kRkEpiWarps : 1);
+    }
     fence_mbar_init();
     misc[0] = 0;
     misc[2] = 0;
@@ -177,8 +187,7 @@ __global__ void __launch_bounds__(kRkThreads, 1) rkv_compress_kernel(const __gri
     tmem_relinquish();
   }
   for (int i = tid; i < kRkvMaxSlots; i += kRkThreads) {
-    pos_s[i] = (i < n) ? ra.pos[ubase + i] : INT_MIN;
-    cnt_s[i] = 0;
+    if (i < kRkvMaxSlots / 2) cnt_w[i] = 0u;
     z_s[i] = 0.f;
     inv_s[i] = 0.f;   // ||k_i||^2 accumulates here in pass 1, then becomes 1/||k_i||
   }
@@ -544,7 +553,7 @@ __global__ void __launch_bounds__(kRkThreads, 1) rkv_compress_kernel(const __gri
       }
       const float inv_i = (row < n) ? inv_s[row] : 0.f;
       const float thr_i = (inv_i > 0.f) ? ra.tau / inv_i : INFINITY;   // tau * ||k_i||
-      const int pos_i = pos_s[min(row, kRkvMaxSlots - 1)];
+      const int pos_i = (row < n) ? posg[row] : INT_MIN;
       int cnt = 0;
       for (int k = 0; k < nb - I; ++k, ++at) {
         const int J = col_block(I, k, nb);
@@ -597,12 +606,12 @@ __global__ void __launch_bounds__(kRkThreads, 1) rkv_compress_kernel(const __gri
           while (hits) {
             const int j = j0 + __ffs(hits) - 1;
             hits &= hits - 1u;
-            if (pos_s[j] > pos_i) ++cnt;                 // a later near-duplicate of i
-            else atomicAdd(&cnt_s[j], 1);                 // i is the later one: j is older
+            if (posg[j] > pos_i) ++cnt;                  // a later near-duplicate of i
+            else cnt_add(j, 1);                           // i is the later one: j is older
           }
         }
       }
-      if (row < n && cnt) atomicAdd(&cnt_s[row], cnt);
+      if (row < n && cnt) cnt_add(row, cnt);
     }
   }
   const bool ok = __syncthreads_and(misc[0] == 0);
@@ -616,16 +625,17 @@ __global__ void __launch_bounds__(kRkThreads, 1) rkv_compress_kernel(const __gri
   if (ok) {
     // every count is in: Z_i = lambda I_i - (1 - lambda) R_i
     for (int i = tid; i < n; i += kRkThreads)
-      z_s[i] = ra.lam * z_s[i] - (1.f - ra.lam) * ((cnt_s[i] >= ra.beta) ? 1.f : 0.f);
+      z_s[i] = ra.lam * z_s[i] - (1.f - ra.lam) * ((cnt_get(i) >= ra.beta) ? 1.f : 0.f);
     __syncthreads();
     unsigned long long* key = reinterpret_cast<unsigned long long*>(ring);   // [n]
     int* hist = reinterpret_cast<int*>(ring + kRkvMaxSlots * 8);            // [256]
     unsigned long long* sel_prefix = reinterpret_cast<unsigned long long*>(smem + kOffMisc + 16);
     int* sel_rank = reinterpret_cast<int*>(smem + kOffMisc + 24);
     for (int i = tid; i < n; i += kRkThreads) {
-      const bool obs = pos_s[i] >= pnext - ra.alpha;
+      const int pi = posg[i];
+      const bool obs = pi >= pnext - ra.alpha;
       const uint32_t hi = obs ? 0xFFFFFFFFu : orderable(z_s[i]);
-      key[i] = ((unsigned long long)hi << 32) | (uint32_t)pos_s[i];
+      key[i] = ((unsigned long long)hi << 32) | (uint32_t)pi;
     }
     if (tid == 0) {
       *sel_prefix = 0ull;
@@ -683,9 +693,10 @@ __global__ void __launch_bounds__(kRkThreads, 1) rkv_compress_kernel(const __gri
       }
       __syncthreads();
     }
-    // kept flags (reuse the counts): every key above the largest dropped one
+    // kept flags: every key above the largest dropped one
     const unsigned long long kcut = *sel_prefix;
-    for (int i = tid; i < kRkvMaxSlots; i += kRkThreads) cnt_s[i] = (i < n && key[i] > kcut) ? 1 : 0;
+    int* kept = reinterpret_cast<int*>(z_s);   // Z is in the keys now: reuse its space
+    for (int i = tid; i < kRkvMaxSlots; i += kRkThreads) kept[i] = (i < n && key[i] > kcut) ? 1 : 0;
     __syncthreads();
     // ---- move: kept buffer tokens into the freed retained slots, in slot order ----
     int* freed = reinterpret_cast<int*>(ring);                  // reuse the ring
@@ -694,8 +705,8 @@ __global__ void __launch_bounds__(kRkThreads, 1) rkv_compress_kernel(const __gri
       int nf = 0, nm = 0;
       for (int s0 = 0; s0 < n; s0 += 32) {
         const int sl = s0 + lane;
-        const bool is_freed = sl < ra.budget && !cnt_s[sl];
-        const bool is_mover = sl >= ra.budget && sl < n && cnt_s[sl];
+        const bool is_freed = sl < ra.budget && !kept[sl];
+        const bool is_mover = sl >= ra.budget && sl < n && kept[sl];
         const unsigned fb = __ballot_sync(0xffffffffu, is_freed);
         const unsigned mb = __ballot_sync(0xffffffffu, is_mover);
         const unsigned below = (1u << lane) - 1u;
@@ -720,7 +731,7 @@ __global__ void __launch_bounds__(kRkThreads, 1) rkv_compress_kernel(const __gri
         uint4* to = reinterpret_cast<uint4*>(lane < 16 ? Kw + (size_t)dst * D : Vw + (size_t)dst * D);
         to[lane & 15] = from[lane & 15];
         if (lane == 0) {
-          ra.pos[ubase + dst] = pos_s[src];
+          ra.pos[ubase + dst] = posg[src];   // src >= budget > dst: never a moved slot
           ra.vnorm[ubase + dst] = ra.vnorm[ubase + src];
         }
       }
