@@ -54,7 +54,7 @@ constexpr int kRkProducerWarp = 8;
 constexpr int kRkMmaWarp = 9;                // MMA warps 9 and 10: even and odd blocks
 constexpr int kRkThreads = 352;
 constexpr int kRkTile = 128;
-constexpr int kRkStages = 4;
+constexpr int kRkStages = 3;
 constexpr int kRkStage = kRkTile * 256;     // one K tile [128 rows][128 d] bf16: 32 KB
 constexpr int kRkBlock = kRkTile * 128;     // one 64-column half of it: 16 KB
 constexpr int kRkQRows = 64;                // observation query rows (alpha * G <= 64)
@@ -63,29 +63,33 @@ constexpr int kRkAcc = 3;                   // key dot-product accumulators, 128
 constexpr int kRkImpCol = kRkAcc * 128;     // two importance accumulators, 64 columns each
 constexpr int kRkPrefetch = 6;              // ring tiles requested into L2 ahead of their load
 
-// A position in the tile walk (see the kernel): pass 1 tile k, then column
-// tile J of row block I; `last` marks the row block's final tile.
+// Pass 2 takes the row blocks in pairs p: I0 = 2p and I1 = 2p + 1 (when below
+// nb), and streams each column tile J > I1 once for both: first I1+3 .. nb-1,
+// then I1+2, then I1+1.  The last two become the next pair's row blocks.
+__device__ __forceinline__ int pair_tiles(int I1, int nb) { return I1 < nb ? nb - I1 - 1 : 0; }
+__device__ __forceinline__ int pair_kept(int m) { return m < 2 ? m : 2; }
+__device__ __forceinline__ int pair_tile(int I1, int k, int m) {
+  if (k < m - pair_kept(m)) return I1 + 3 + k;
+  return k == m - 1 ? I1 + 1 : I1 + 2;
+}
+
+// A position in the producer's tile walk: pass 1 tile k, then column tile j of
+// pair p; `keep` marks a tile that becomes the next pair's row block 1 (I1+2)
+// or 0 (I1+1), else -1.
 struct Walk {
-  int k, I, J;
-  bool last;
+  int k, p, j, keep;
 };
 
-// Shared-memory buffers behind the ring stages and the row block.
+// Shared-memory buffers behind the ring stages and the pair's two row blocks.
 struct Bufs {
   unsigned char* stage[kRkStages];
-  unsigned char* a;
-  __device__ void swap(int st) {
+  unsigned char* a[2];
+  __device__ void swap(int st, int which) {
     unsigned char* t = stage[st];
-    stage[st] = a;
-    a = t;
+    stage[st] = a[which];
+    a[which] = t;
   }
 };
-
-// Column block of the k-th key dot-product block of row block I: the diagonal,
-// then I+2, ..., nb-1, then I+1.
-__device__ __forceinline__ int col_block(int I, int k, int nb) {
-  return k == 0 ? I : (k < nb - I - 1 ? I + 1 + k : I + 1);
-}
 
 // Shared-memory plan (offsets from a 1024-byte aligned base).
 constexpr int kRkBars = 2 * kRkStages + 13;   // mbarriers (see the kernel)
@@ -95,8 +99,8 @@ constexpr int kOffMisc = 272;      // [0] fail flag, [1] move count, [2] row blo
 constexpr int kOffStats = 512;     // m[64], l[64]
 constexpr int kOffRed = 1024;      // [4 quarters][64 columns][2]
 constexpr int kOffNmin = 3072;     // per 32-slot chunk: smallest ||k|| (128 chunks)
-constexpr int kOffA = 4096;        // the row block of pass 2
-constexpr int kOffRing = kOffA + kRkStage;
+constexpr int kOffA = 4096;        // the two row blocks of pass 2
+constexpr int kOffRing = kOffA + 2 * kRkStage;
 constexpr int kOffQ = kOffRing + kRkStages * kRkStage;
 constexpr int kOffInv = kOffQ + 2 * kRkQBlock;
 constexpr int kOffCnt = kOffInv + kRkvMaxSlots * 4;       // 16-bit counts, two per word
@@ -214,48 +218,55 @@ __global__ void __launch_bounds__(kRkThreads, 1) rkv_compress_kernel(const __gri
 
   // K tiles are read again for every row block: ask L2 to keep them
   const uint64_t pol = l2_evict_last_policy();
-  auto load_tile = [&](unsigned char* dst, int t, uint64_t* bar) {
-    mbar_arrive_expect_tx(bar, (uint32_t)kRkStage);
+  auto load_tile_tx = [&](unsigned char* dst, int t, uint64_t* bar) {  // bytes announced by the caller
     for (int blk = 0; blk < 2; ++blk)
       for (int ro = 0; ro < kRkTile; ro += 64)
         tma_load_2d(dst + blk * kRkBlock + ro * 128, &ra.kmap, blk * 64, row0 + t * kRkTile + ro,
                     bar, pol);
   };
+  auto load_tile = [&](unsigned char* dst, int t, uint64_t* bar) {
+    mbar_arrive_expect_tx(bar, (uint32_t)kRkStage);
+    load_tile_tx(dst, t, bar);
+  };
 
-  // The tile walk shared by the producer (loads, L2 requests) and the MMA warp:
-  // pass 1 tiles 0..nb-1, then per row block I the column tiles I+2..nb-1 and
-  // I+1 (`last` set on I+1); -1 at the end.
+  // The producer's tile walk (loads, L2 requests), in the order the MMA warps
+  // and the epilogue take the tiles: pass 1 tiles 0..nb-1, then per pair its
+  // column tiles in pair_tile order; -1 at the end.
   auto next = [&](Walk& w) -> int {
-    w.last = false;
+    w.keep = -1;
     if (w.k < nb) return w.k++;
     for (;;) {
-      if (w.I >= nb - 1) return -1;   // the last row block has no column tiles
-      if (w.J < nb) return w.J++;
-      if (w.J == nb) {
-        w.J = nb + 1;
-        w.last = true;
-        return w.I + 1;
+      const int I1 = 2 * w.p + 1;
+      if (I1 >= nb) return -1;   // no pair from here on has column tiles
+      const int m = pair_tiles(I1, nb);
+      if (w.j < m) {
+        const int k = w.j++;
+        if (k == m - 1) w.keep = 0;
+        else if (pair_kept(m) == 2 && k == m - 2) w.keep = 1;
+        return pair_tile(I1, k, m);
       }
-      ++w.I;
-      w.J = w.I + 2;
+      ++w.p;
+      w.j = 0;
     }
   };
-  // The buffers behind the ring's stages and the row block, as the producer
-  // and the MMA warp both track them (the same swaps at the same tiles).
+  // The buffers behind the ring's stages and the row blocks (the producer and
+  // the MMA warps make the same swaps: the producer when it loads a kept tile,
+  // the MMA warps when the pair is done with the old row blocks).
   auto initial_bufs = [&]() {
     Bufs b;
     for (int i = 0; i < kRkStages; ++i) b.stage[i] = ring + i * kRkStage;
-    b.a = abuf;
+    b.a[0] = abuf;
+    b.a[1] = abuf + kRkStage;
     return b;
   };
 
   if (warp == kRkProducerWarp) {
     // ---- producer: the ring's tile sequence, pass 1 tiles 0..nb-1, then for
-    // each row block I the column tiles I+2..nb-1 and I+1.  The ring is
+    // each pair of row blocks its column tiles.  The ring is
     // latency-bound (the tiles mostly come from L2), so every tile is also
     // requested into L2 kRkPrefetch places ahead of its load. ----------------------
     if (lane == 0) {
-      Walk ahead{0, 0, 2, false};
+      Walk ahead{0, 0, 0, -1};
       for (int q = 0; q < kRkPrefetch; ++q) {
         const int t = next(ahead);
         if (t < 0) break;
@@ -263,7 +274,7 @@ __global__ void __launch_bounds__(kRkThreads, 1) rkv_compress_kernel(const __gri
           for (int blk = 0; blk < 2; ++blk)
             tma_prefetch_l2_2d(&ra.kmap, blk * 64, row0 + t * kRkTile + ro);
       }
-      Walk cur{0, 0, 2, false};
+      Walk cur{0, 0, 0, -1};
       Bufs bf = initial_bufs();
       int tt = 0;       // ring tiles issued
       for (int t = next(cur); t >= 0; t = next(cur), ++tt) {
@@ -274,7 +285,7 @@ __global__ void __launch_bounds__(kRkThreads, 1) rkv_compress_kernel(const __gri
           break;
         }
         load_tile(bf.stage[st], t, &full[st]);
-        if (cur.last) bf.swap(st);  // tile I+1: the next row block's buffer
+        if (cur.keep >= 0) bf.swap(st, cur.keep);  // the next pair's row block
         const int tp = next(ahead);
         if (tp >= 0)
           for (int ro = 0; ro < kRkTile; ro += 64)
@@ -322,8 +333,12 @@ __global__ void __launch_bounds__(kRkThreads, 1) rkv_compress_kernel(const __gri
         }
         ++it;
       };
-      // row block 0 (the others come through the ring): request it now
-      if (par == 0) load_tile(abuf, 0, afull);
+      // row blocks 0 and 1 (the others come through the ring): request them now
+      if (par == 0) {
+        mbar_arrive_expect_tx(afull, (uint32_t)((nb > 1 ? 2 : 1) * kRkStage));
+        load_tile_tx(abuf, 0, afull);
+        if (nb > 1) load_tile_tx(abuf + kRkStage, 1, afull);
+      }
       // pass 1: the stage is released by the epilogue (it also reads ||k|| there)
       for (int t = 0; t < nb && !fail; ++t) {
         const int st = rt % kRkStages;
@@ -334,68 +349,80 @@ __global__ void __launch_bounds__(kRkThreads, 1) rkv_compress_kernel(const __gri
         mma_imp(smem_u32(ring + st * kRkStage));
         ++rt;
       }
-      // pass 2
+      // pass 2, in pairs of row blocks
       Bufs bf = initial_bufs();
-      volatile int* landed = misc + 2;   // row blocks known to have landed, besides 0
-      for (int I = 0; I < nb && !fail; ++I) {
-        const uint32_t a0 = smem_u32(bf.a);
-        // The row block has landed: row block 0 by its own copy; row block I > 0
-        // as row block I - 1's last column tile, which one of the two warps
-        // waited for.  That warp raises a counter (the stage's barrier may have
-        // moved on to its next tile by the time the other warp gets here).
-        if (I == 0) {
-          if (!wait(afull, 0)) break;
-        } else if (*landed < I) {
-          const unsigned long long t0 = global_ns();
-          while (*landed < I && !misc[0]) {
-            __nanosleep(32);
-            if (global_ns() - t0 > kWaitLimitNs) {
-              fail = true;
-              break;
-            }
+      volatile int* landed = misc + 2;   // kept tiles known to have landed
+      int kept_before = 0;               // kept tiles of the pairs so far
+      // One key dot-product block into accumulator at % kRkAcc, by warp at % 2:
+      // A = aop's 128 keys, B = bop's; st >= 0: bop is ring stage st.  `mark`:
+      // the tile becomes a row block of the next pair, count it as landed.
+      auto block = [&](uint32_t aop, uint32_t bop, int st, bool mark) {
+        const int acc = at % kRkAcc;
+        if ((at & 1) == par && !fail) {
+          if (at >= kRkAcc && !wait(&accfree[acc], (uint32_t)(((at / kRkAcc) - 1) & 1))) return;
+          if (st >= 0 && !wait(&full[st], (uint32_t)((rt / kRkStages) & 1))) return;
+          if (mark) {
+            __threadfence_block();
+            atomicAdd(const_cast<int*>(landed), 1);
           }
-          if (fail || misc[0]) {
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            tc_mma_bf16(tm + (uint32_t)(acc * 128),
+                        sw128_desc(aop + (kk >> 2) * kRkBlock + (kk & 3) * 32, 16, 1024),
+                        sw128_desc(bop + (kk >> 2) * kRkBlock + (kk & 3) * 32, 16, 1024), id_s,
+                        kk > 0 ? 1u : 0u);
+          tc_commit(&accfull[acc]);
+        }
+        ++at;
+      };
+      for (int p = 0; 2 * p < nb && !fail; ++p) {
+        const int I1 = 2 * p + 1;
+        const bool has1 = I1 < nb;
+        const int m = pair_tiles(I1, nb);
+        // The pair's row blocks have landed: rows 0 and 1 by their own copy, the
+        // others as the previous pair's kept tiles, which one of the two warps
+        // waited for and counted (a stage's barrier may have moved on to its
+        // next tile by the time the other warp gets here).
+        if (p == 0) {
+          if (!wait(afull, 0)) break;
+        } else if (*landed < kept_before) {
+          const unsigned long long t0 = global_ns();
+          while (*landed < kept_before && !misc[0]) {
+            __nanosleep(32);
+            if (global_ns() - t0 > kWaitLimitNs) break;
+          }
+          if (*landed < kept_before) {
             fail = true;
             break;
           }
         }
         __threadfence_block();
         tc_fence_after();
+        const uint32_t a0 = smem_u32(bf.a[0]), a1 = smem_u32(bf.a[1]);
         mma_imp(a0);
-        for (int k = 0; k < nb - I && !fail; ++k) {
-          const int acc = at % kRkAcc;
-          const int st = (k > 0) ? rt % kRkStages : -1;
-          if ((at & 1) == par) {
-            if (at >= kRkAcc && !wait(&accfree[acc], (uint32_t)(((at / kRkAcc) - 1) & 1))) break;
-            uint32_t b0 = a0;   // the diagonal block: K_I . K_I^T
-            if (st >= 0) {
-              if (!wait(&full[st], (uint32_t)((rt / kRkStages) & 1))) break;
-              b0 = smem_u32(bf.stage[st]);
-              if (k == nb - I - 1) {   // tile I + 1, the next row block, has landed
-                __threadfence_block();
-                *landed = I + 1;
-              }
-            }
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-              tc_mma_bf16(tm + (uint32_t)(acc * 128),
-                          sw128_desc(a0 + (kk >> 2) * kRkBlock + (kk & 3) * 32, 16, 1024),
-                          sw128_desc(b0 + (kk >> 2) * kRkBlock + (kk & 3) * 32, 16, 1024), id_s,
-                          kk > 0 ? 1u : 0u);
-            tc_commit(&accfull[acc]);
-          }
-          if (st >= 0) {
-            // The epilogue hands the stage back once it sees the block's
-            // products, in block order, so after every earlier block's: for the
-            // row block's last tile (I + 1, kept as the next row block) that
-            // covers every MMA on the old row block, whose buffer takes its
-            // place in the ring.
-            if (k == nb - I - 1) bf.swap(st);
-            ++rt;
-          }
-          ++at;
+        if (has1) mma_imp(a1);
+        block(a0, a0, -1, false);        // K_I0 . K_I0^T
+        if (has1) {
+          block(a0, a1, -1, false);      // K_I0 . K_I1^T
+          block(a1, a1, -1, false);      // K_I1 . K_I1^T
         }
+        int keep_st[2] = {-1, -1};
+        for (int k = 0; k < m && !fail; ++k) {
+          const int st = rt % kRkStages;
+          const int keep = (k == m - 1) ? 0 : (pair_kept(m) == 2 && k == m - 2) ? 1 : -1;
+          const uint32_t b0 = smem_u32(bf.stage[st]);
+          block(a0, b0, st, keep >= 0);
+          block(a1, b0, st, false);
+          if (keep >= 0) keep_st[keep] = st;
+          ++rt;
+        }
+        // The epilogue hands the kept tiles' stages back after the pair's last
+        // block, so after every MMA on the old row blocks, whose buffers take
+        // their places in the ring.
+        if (keep_st[1] >= 0) bf.swap(keep_st[1], 1);
+        if (keep_st[0] >= 0) bf.swap(keep_st[0], 0);
+        kept_before += pair_kept(m);
       }
       if (fail) misc[0] = 1;
       // every MMA issued completes before tensor memory is released, and row
@@ -534,84 +561,125 @@ __global__ void __launch_bounds__(kRkThreads, 1) rkv_compress_kernel(const __gri
     }
     named_bar_sync(1, kRkEpi);
 
-    // ---- pass 2: importance, then near-duplicate counts over blocks J >= I ---------
+    // ---- pass 2: importance, then near-duplicate counts over blocks J >= I, ----
+    // in the MMA warps' order: per pair, both row blocks' importance, the blocks
+    // (I0, I0), (I0, I1), (I1, I1), then (I0, J), (I1, J) per column tile.
     int at = 0;
     int rt = nb;   // ring tiles consumed (pass 1 took nb)
-    for (int I = 0; I < nb; ++I) {
-      const int row = I * kRkTile + r;   // this thread's token
-      {
-        float s[32];
-        if (imp_logits(row, s)) {
-          float part = 0.f;
+    // This thread's token of a row block: its importance, then its state.
+    struct RowState {
+      int row, pos;
+      float thr;
+      int cnt;
+    };
+    auto row_start = [&](int I) -> RowState {
+      RowState rs;
+      rs.row = I * kRkTile + r;
+      float s[32];
+      if (imp_logits(rs.row, s)) {
+        float part = 0.f;
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const int col = half * 32 + c;
-            if (col < QN && s[c] != -INFINITY) part += exp2f(s[c] - m_col[col]) / l_col[col];
-          }
-          if (row < n) atomicAdd(&z_s[row], part / (float)QN);
+        for (int c = 0; c < 32; ++c) {
+          const int col = half * 32 + c;
+          if (col < QN && s[c] != -INFINITY) part += exp2f(s[c] - m_col[col]) / l_col[col];
+        }
+        if (rs.row < n) atomicAdd(&z_s[rs.row], part / (float)QN);
+      }
+      const float inv_i = (rs.row < n) ? inv_s[rs.row] : 0.f;
+      rs.thr = (inv_i > 0.f) ? ra.tau / inv_i : INFINITY;   // tau * ||k_i||
+      rs.pos = (rs.row < n) ? posg[rs.row] : INT_MIN;
+      rs.cnt = 0;
+      return rs;
+    };
+    // Block `at` (row block of rs, column block J; diag: J is rs's own row
+    // block, only j > row counts); release: ring stage to hand back once its
+    // products are read (-1: none), release2 a second one.
+    auto take_block = [&](RowState& rs, int J, bool diag, int release, int release2) {
+      const int acc = at % kRkAcc;
+      const bool got = wait(&accfull[acc], (uint32_t)((at / kRkAcc) & 1));
+      ++at;
+      if (!got) return;
+      // every block so far is complete: those stages may be refilled
+      if (tid == 0) {
+        if (release >= 0) mbar_arrive(&empty[release]);
+        if (release2 >= 0) mbar_arrive(&empty[release2]);
+      }
+      tc_fence_after();
+      // columns 64*half .. +63 of block J: both warp-collective loads first, then
+      // hand the accumulator back, then each thread's own tests
+      float v[2][32];
+      __syncwarp();
+      tmem_ld32(tm + (uint32_t)(acc * 128) + lanes + (uint32_t)(half * 64), v[0]);
+      tmem_ld32(tm + (uint32_t)(acc * 128) + lanes + (uint32_t)(half * 64 + 32), v[1]);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&accfree[acc]);
+      const int row = rs.row;
+      const float thr_i = rs.thr;
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int j0 = J * kRkTile + half * 64 + cc * 32;   // first column token
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 32; ++c) mx = fmaxf(mx, v[cc][c]);
+        // quick rejection: cos >= tau needs S_ij >= tau ||k_i|| ||k_j|| >= thr_i * min ||k_j||
+        const bool rejected = mx < thr_i * nmin[j0 >> 5];
+        if (__all_sync(0xffffffffu, rejected)) continue;
+        // The exact test on every column, the same instructions for every lane
+        // (the chunk's 1/||k_j|| are broadcast loads), as a mask of hits.
+        uint32_t hits = 0;
+        const float4* iv4 = reinterpret_cast<const float4*>(inv_s + j0);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float4 w = iv4[q];
+          hits |= (v[cc][4 * q] * w.x >= thr_i ? 1u : 0u) << (4 * q);
+          hits |= (v[cc][4 * q + 1] * w.y >= thr_i ? 1u : 0u) << (4 * q + 1);
+          hits |= (v[cc][4 * q + 2] * w.z >= thr_i ? 1u : 0u) << (4 * q + 2);
+          hits |= (v[cc][4 * q + 3] * w.w >= thr_i ? 1u : 0u) << (4 * q + 3);
+        }
+        // only tokens (j < n), and on a diagonal block only j > row
+        const int lim = n - j0;
+        if (rejected || row >= n || lim <= 0) hits = 0;
+        else if (lim < 32) hits &= (1u << lim) - 1u;
+        if (diag) {
+          const int d = row - j0 + 1;   // columns c >= d have j > row
+          if (d >= 32) hits = 0;
+          else if (d > 0) hits &= ~((1u << d) - 1u);
+        }
+        while (hits) {
+          const int j = j0 + __ffs(hits) - 1;
+          hits &= hits - 1u;
+          if (posg[j] > rs.pos) ++rs.cnt;               // a later near-duplicate of i
+          else cnt_add(j, 1);                           // i is the later one: j is older
         }
       }
-      const float inv_i = (row < n) ? inv_s[row] : 0.f;
-      const float thr_i = (inv_i > 0.f) ? ra.tau / inv_i : INFINITY;   // tau * ||k_i||
-      const int pos_i = (row < n) ? posg[row] : INT_MIN;
-      int cnt = 0;
-      for (int k = 0; k < nb - I; ++k, ++at) {
-        const int J = col_block(I, k, nb);
-        const int acc = at % kRkAcc;
-        const int st = (k > 0) ? (rt++) % kRkStages : -1;   // the block's column tile's stage
-        if (!wait(&accfull[acc], (uint32_t)((at / kRkAcc) & 1))) continue;
-        // that tile has been read: its stage may be refilled
-        if (st >= 0 && tid == 0) mbar_arrive(&empty[st]);
-        tc_fence_after();
-        // columns 64*half .. +63 of block J: both warp-collective loads first, then
-        // hand the accumulator back, then each thread's own (divergent) tests
-        float v[2][32];
-        __syncwarp();
-        tmem_ld32(tm + (uint32_t)(acc * 128) + lanes + (uint32_t)(half * 64), v[0]);
-        tmem_ld32(tm + (uint32_t)(acc * 128) + lanes + (uint32_t)(half * 64 + 32), v[1]);
-        tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&accfree[acc]);
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const int j0 = J * kRkTile + half * 64 + cc * 32;   // first column token
-          float mx = -INFINITY;
-#pragma unroll
-          for (int c = 0; c < 32; ++c) mx = fmaxf(mx, v[cc][c]);
-          // quick rejection: cos >= tau needs S_ij >= tau ||k_i|| ||k_j|| >= thr_i * min ||k_j||
-          const bool rejected = mx < thr_i * nmin[j0 >> 5];
-          if (__all_sync(0xffffffffu, rejected)) continue;
-          // The exact test on every column, the same instructions for every lane
-          // (the chunk's 1/||k_j|| are broadcast loads), as a mask of hits.
-          uint32_t hits = 0;
-          const float4* iv4 = reinterpret_cast<const float4*>(inv_s + j0);
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const float4 w = iv4[q];
-            hits |= (v[cc][4 * q] * w.x >= thr_i ? 1u : 0u) << (4 * q);
-            hits |= (v[cc][4 * q + 1] * w.y >= thr_i ? 1u : 0u) << (4 * q + 1);
-            hits |= (v[cc][4 * q + 2] * w.z >= thr_i ? 1u : 0u) << (4 * q + 2);
-            hits |= (v[cc][4 * q + 3] * w.w >= thr_i ? 1u : 0u) << (4 * q + 3);
-          }
-          // only tokens (j < n), and on the diagonal block only j > row
-          const int lim = n - j0;
-          if (rejected || row >= n || lim <= 0) hits = 0;
-          else if (lim < 32) hits &= (1u << lim) - 1u;
-          if (J == I) {
-            const int d = row - j0 + 1;   // columns c >= d have j > row
-            if (d >= 32) hits = 0;
-            else if (d > 0) hits &= ~((1u << d) - 1u);
-          }
-          while (hits) {
-            const int j = j0 + __ffs(hits) - 1;
-            hits &= hits - 1u;
-            if (posg[j] > pos_i) ++cnt;                  // a later near-duplicate of i
-            else cnt_add(j, 1);                           // i is the later one: j is older
-          }
-        }
+    };
+    for (int p = 0; 2 * p < nb; ++p) {
+      const int I0 = 2 * p, I1 = I0 + 1;
+      const bool has1 = I1 < nb;
+      const int m = pair_tiles(I1, nb);
+      RowState r0 = row_start(I0);
+      RowState r1 = has1 ? row_start(I1) : r0;
+      take_block(r0, I0, true, -1, -1);
+      if (has1) {
+        take_block(r0, I1, false, -1, -1);
+        take_block(r1, I1, true, -1, -1);
       }
-      if (row < n && cnt) cnt_add(row, cnt);
+      // A tile's stage goes back after its second block, but the tile kept as
+      // the next pair's row block 1 only with the last block of the pair: the
+      // old row block 1, whose buffer refills that stage, is read until then.
+      int held = -1;
+      for (int k = 0; k < m; ++k) {
+        const int J = pair_tile(I1, k, m);
+        const int st = (rt++) % kRkStages;
+        const bool keep1 = pair_kept(m) == 2 && k == m - 2;
+        take_block(r0, J, false, -1, -1);
+        take_block(r1, J, false, keep1 ? -1 : st, k == m - 1 ? held : -1);
+        if (keep1) held = st;
+      }
+      if (r0.row < n && r0.cnt) cnt_add(r0.row, r0.cnt);
+      if (has1 && r1.row < n && r1.cnt) cnt_add(r1.row, r1.cnt);
     }
   }
   const bool ok = __syncthreads_and(misc[0] == 0);
