@@ -1063,7 +1063,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           // exchanges go through global memory, counted by atomics.  The parts
           // are the CTAs of the clusters whose ranges meet the unit, in
           // cluster then rank order; part 0 leads.  Only the per-KV-head
-          // LongFlow score and the append modes are planned (host). ----
+          // LongFlow score (either victim order) and the append modes are
+          // planned (host). ----
           const int part = items[kTcItemInts * k + 7];
           const int xi = part >> 16;                      // exchange slot
           const int np = (part & 0xff) * C;               // parts (<= kMaxSplitParts)

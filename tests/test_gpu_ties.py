@@ -134,6 +134,48 @@ def test_exact_ties_planned_launch():
         run.close()
 
 
+def test_exact_ties_planned_launch_deferred():
+    """The same planned launch (batch 32 at budget 3276, two-CTA clusters)
+    with the deferred victim: the step that fills each buffer chooses the
+    lowest tied slot, and every later step overwrites the slot chosen one step
+    before, across the cut points of shared units and the CTA boundaries
+    inside their parts."""
+    from test_gpu_parity import _check_plan
+    pol = oracle.Policy(deferred=True)
+    wl = WORKLOADS["r1-llama-8b"].scaled(layers=1, prefill=3275)
+    units = wl.batch * wl.kv_heads
+    probe = ParityRun(wl, layers=(0,), sample=[(0, 0, 0)], policy=pol)
+    try:
+        plan = probe.cache.plan(0)
+        C = probe.cache.layout.cluster
+        nc = probe.cache.layout.split_units
+    finally:
+        probe.close()
+    assert plan is not None
+    shared = _check_plan(plan, units, nc)
+    cuts = plan[1]
+    chosen = sorted(shared, key=lambda u: -len(shared[u]))[:2] + [max(shared)]
+    slots = {3, 5}
+    for u in chosen:
+        bounds = [0] + [cuts[q][1] for q in shared[u][1:]] + [wl.budget]
+        for lo, hi in zip(bounds, bounds[1:]):
+            per = ((hi - lo + C - 1) // C + 3) & ~3
+            for x in (lo - 1, lo, lo + per - 1, lo + per):
+                slots.add(x)
+    top = wl.budget - wl.window - 1
+    slots = sorted(x for x in slots if 0 <= x < top)
+    steps = len(slots) + 2
+    sample = [(0,) + divmod(u, wl.kv_heads) for u in chosen] + [(0, 0, 0), (0, 13, 6)]
+    run, seen = _tie_run(wl, slots, steps, sample=sample, policy=pol)
+    try:
+        assert run.cache.plan(0) is not None
+        for t, s in enumerate(slots):
+            assert bool((seen[t + 1] == s).all()), (t, s, seen[t + 1].unique().tolist())
+        assert run.stats.exact_ties >= len(slots) - 1
+    finally:
+        run.close()
+
+
 POLICIES = {
     "deferred": oracle.Policy(deferred=True),
     "layer": oracle.Policy(scope="layer"),
