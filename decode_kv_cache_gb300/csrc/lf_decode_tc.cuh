@@ -1110,10 +1110,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             *fail_any = 1;
             atomicOr(a.err, LF_DEVERR_TIMEOUT);
           }
-          // Exact scores of this CTA's slots, its lowest candidate.
+          // Exact scores of this CTA's slots, its lowest candidate (LongFlow:
+          // ||v_i|| sum_h alpha_{h,i}; H2O: the slot's accumulator plus this
+          // step's sum_h alpha_{h,i}, scored on every step to update it).
           float bs = INFINITY;
           int bi = INT_MAX;
-          if (rl.choosing && got_loc && stats_ok) {
+          const bool pscoring = (rl.choosing || h2o) && got_loc && stats_ok;
+          if (pscoring && rl.choosing) {
             float cm[G];
 #pragma unroll
             for (int h = 0; h < G; ++h) cm[h] = cmul[h];
@@ -1135,7 +1138,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const int slot = base + i;
                 if (i >= rows) break;
                 if (slot == rl.excl) continue;
-                const float sc = fabsf(wv[jr]) * asv[jr];
+                const float sc = h2o ? fabsf(wv[jr]) + asv[jr] : fabsf(wv[jr]) * asv[jr];
                 if (is_candidate(wv[jr]) && better(sc, slot, bs, bi)) {
                   bs = sc;
                   bi = slot;
@@ -1158,6 +1161,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           named_bar_sync(2, kTcTail);
           const bool unit_failed = unit_handoff();
+          // H2O: write back the accumulators of this part's slots except the
+          // dropped slot and the part's lowest candidate, which the leader
+          // writes (it may be the victim, which takes the new token's).
+          if (pscoring && h2o && !unit_failed) {
+            int ci = red_ti[0];
+            if (better(red_t[1], red_ti[1], red_t[0], red_ti[0])) ci = red_ti[1];
+            float cm[G];
+#pragma unroll
+            for (int h = 0; h < G; ++h) cm[h] = cmul[h];
+            for (int i = tt_id; i < rows; i += kTcTail) {
+              const int slot = base + i;
+              if (slot == rl.excl || slot == ci) continue;
+              a.acc[ubase + slot] = fabsf(w_s[i]) + group_dot<G>(lg + (size_t)i * G, cm);
+            }
+          }
           // Exchange 2: partial output, lowest (score, slot) and failure flag to part 0.
           for (int c = tt_id; c < G * D; c += kTcTail) gfn[(size_t)me * kFinF + c] = o_part[c];
           if (tt_id == 0) {
@@ -1187,9 +1205,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             float fs = INFINITY;
             int fi = INT_MAX;
             bool any_fail = !all_got || !stats_ok;
+            float rs = INFINITY;   // warp 0, lane r < np: part r's lowest (score, slot)
+            int ri = INT_MAX;
             if (twarp == 0) {
-              float rs = INFINITY, rf = 0.f;
-              int ri = INT_MAX;
+              float rf = 0.f;
               if (lane < np) {
                 const float* tl = gfn + (size_t)lane * kFinF + G * D;
                 rs = __ldcg(tl);
@@ -1253,6 +1272,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               }
               __syncwarp();
               const int slot = decision[0];
+              // H2O: the accumulators of the parts' lowest candidates (their
+              // scores), except the slot the new token takes.
+              if (h2o && state_ok && !__any_sync(0xffffffffu, any_fail) && lane < np &&
+                  ri != INT_MAX && ri != slot)
+                a.acc[ubase + ri] = rs;
               if (slot >= 0) write_slot<T, D>(a, ubase, slot, nkv, nkv + D, p, anew, lane, 32);
             }
           }

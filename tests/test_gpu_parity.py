@@ -276,8 +276,8 @@ def test_planned_launch_choice():
     the host's cost model prefers it to whole units: batches 64, 32 and 4 at
     budget 3276 on two-CTA clusters do (units shared by two clusters, and by
     three or more).  The plan covers every unit once.  An empty layer, and a
-    cache with the H2O score or the layer scope, never takes one; the
-    deferred order does."""
+    cache with the layer scope, never takes one; the deferred order and the
+    H2O score do."""
     from decode_kv_cache_gb300.longflow import LFCache
     clusters = torch.cuda.get_device_properties(0).multi_processor_count // 2
     for batch in (32, 4):
@@ -306,22 +306,22 @@ def test_planned_launch_choice():
         _check_plan(plan, 512, clusters)
     finally:
         cache.close()
-    for kw in (dict(score="h2o"), dict(scope="layer")):
-        cache = LFCache(1, 32, 8, 32, 128, 3276, 64, **kw)
-        try:
-            assert cache.layout.split_units == 0 and cache.plan(0) is None
-        finally:
-            cache.close()
-    cache = LFCache(1, 32, 8, 32, 128, 3276, 64, deferred=True)
+    cache = LFCache(1, 32, 8, 32, 128, 3276, 64, scope="layer")
     try:
-        k = torch.zeros(32, 8, 3276, 128, dtype=torch.bfloat16, device="cuda")
-        cache.prefill(0, k, k, [3275] * 32)    # deferred: at most budget - 1
-        assert cache.layout.split_units == clusters
-        plan = cache.plan(0)
-        assert plan is not None
-        _check_plan(plan, 256, clusters)
+        assert cache.layout.split_units == 0 and cache.plan(0) is None
     finally:
         cache.close()
+    for kw, prompt in ((dict(deferred=True), 3275), (dict(score="h2o"), 3276)):
+        cache = LFCache(1, 32, 8, 32, 128, 3276, 64, **kw)
+        try:
+            k = torch.zeros(32, 8, 3276, 128, dtype=torch.bfloat16, device="cuda")
+            cache.prefill(0, k, k, [prompt] * 32)    # deferred: at most budget - 1
+            assert cache.layout.split_units == clusters
+            plan = cache.plan(0)
+            assert plan is not None
+            _check_plan(plan, 256, clusters)
+        finally:
+            cache.close()
 
 
 def test_planned_launch_transition_with_policy():
