@@ -744,12 +744,9 @@ lf_cache* lf_cache_create_ex(int layers, int batch, int kv_heads, int q_heads, i
   cache->memo_used.assign((size_t)layers, 0);
   // Planned launches: the layer's slots cut into equal contiguous ranges, one
   // per cluster, when that balances better than whole units (decided per step
-  // on the host).  For the per-KV-head scores (LongFlow or H2O, either victim
-  // order) and the append modes: the layer scope hands each slot's score to a
-  // second launch, which the parts of a shared unit do not.
+  // on the host), for every policy.
   if (tc) {
-    const bool plain = !kevict || c.scope == LF_SCOPE_KV_HEAD;
-    if (plain && kern.decode_split && resident <= lf::kTcMaxPlan &&
+    if (kern.decode_split && resident <= lf::kTcMaxPlan &&
         2 * cluster <= lf::kMaxSplitParts) {
       cache->plan_ok = 1;
       cache->memo_plan.resize((size_t)layers);

@@ -1062,9 +1062,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           // ---- a unit shared with other clusters (a planned launch): both
           // exchanges go through global memory, counted by atomics.  The parts
           // are the CTAs of the clusters whose ranges meet the unit, in
-          // cluster then rank order; part 0 leads.  Only the per-KV-head
-          // LongFlow score (either victim order) and the append modes are
-          // planned (host). ----
+          // cluster then rank order; part 0 leads. ----
           const int part = items[kTcItemInts * k + 7];
           const int xi = part >> 16;                      // exchange slot
           const int np = (part & 0xff) * C;               // parts (<= kMaxSplitParts)
@@ -1112,11 +1110,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           // Exact scores of this CTA's slots, its lowest candidate (LongFlow:
           // ||v_i|| sum_h alpha_{h,i}; H2O: the slot's accumulator plus this
-          // step's sum_h alpha_{h,i}, scored on every step to update it).
+          // step's sum_h alpha_{h,i}, scored on every step to update it).  Layer
+          // scope: every score goes to the scratch for the selection kernel,
+          // after the hand-off, so that a failed unit leaves it alone.
+          const bool early = !layer;
+          bool unit_failed = early ? false : unit_handoff();
           float bs = INFINITY;
           int bi = INT_MAX;
-          const bool pscoring = (rl.choosing || h2o) && got_loc && stats_ok;
-          if (pscoring && rl.choosing) {
+          const bool pscoring = (rl.choosing || h2o) && !unit_failed && got_loc && stats_ok;
+          if (pscoring && (rl.choosing || layer)) {
             float cm[G];
 #pragma unroll
             for (int h = 0; h < G; ++h) cm[h] = cmul[h];
@@ -1137,9 +1139,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const int i = i0 + jr * kTcTail;
                 const int slot = base + i;
                 if (i >= rows) break;
-                if (slot == rl.excl) continue;
+                if (slot == rl.excl) {
+                  if (layer && rl.choosing) a.lw_score[ubase + slot] = INFINITY;
+                  continue;
+                }
                 const float sc = h2o ? fabsf(wv[jr]) + asv[jr] : fabsf(wv[jr]) * asv[jr];
-                if (is_candidate(wv[jr]) && better(sc, slot, bs, bi)) {
+                if (layer) {
+                  if (h2o) a.acc[ubase + slot] = sc;
+                  if (rl.choosing) a.lw_score[ubase + slot] = is_candidate(wv[jr]) ? sc : INFINITY;
+                } else if (rl.choosing && is_candidate(wv[jr]) && better(sc, slot, bs, bi)) {
                   bs = sc;
                   bi = slot;
                 }
@@ -1160,11 +1168,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             red_ti[twarp] = bi;
           }
           named_bar_sync(2, kTcTail);
-          const bool unit_failed = unit_handoff();
-          // H2O: write back the accumulators of this part's slots except the
-          // dropped slot and the part's lowest candidate, which the leader
-          // writes (it may be the victim, which takes the new token's).
-          if (pscoring && h2o && !unit_failed) {
+          if (early) unit_failed = unit_handoff();
+          // H2O, per-KV-head scope: write back the accumulators of this part's
+          // slots except the dropped slot and the part's lowest candidate, which
+          // the leader writes (it may be the victim, which takes the new token's).
+          if (pscoring && h2o && !layer && !unit_failed) {
             int ci = red_ti[0];
             if (better(red_t[1], red_ti[1], red_t[0], red_ti[0])) ci = red_ti[1];
             float cm[G];
@@ -1272,9 +1280,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               }
               __syncwarp();
               const int slot = decision[0];
-              // H2O: the accumulators of the parts' lowest candidates (their
-              // scores), except the slot the new token takes.
-              if (h2o && state_ok && !__any_sync(0xffffffffu, any_fail) && lane < np &&
+              // H2O, per-KV-head scope: the accumulators of the parts' lowest
+              // candidates (their scores), except the slot the new token takes.
+              if (h2o && !layer && state_ok && !__any_sync(0xffffffffu, any_fail) && lane < np &&
                   ri != INT_MAX && ri != slot)
                 a.acc[ubase + ri] = rs;
               if (slot >= 0) write_slot<T, D>(a, ubase, slot, nkv, nkv + D, p, anew, lane, 32);

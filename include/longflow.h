@@ -271,7 +271,8 @@ typedef struct lf_layout {
   float rkv_lambda, rkv_tau;
   int split_units;  /* tensor-core kernel with planned launches possible (see
                        lf_launch_plan): its resident clusters nc; 0 when steps never
-                       take a plan (the policy or the kernel does not allow it) */
+                       take a plan (the CUDA-core kernel, or more resident clusters
+                       than a plan can describe) */
   int32_t* split_cnt; /* planned launches: [split_units][2] arrival counts of the two
                        exchanges through global memory of a shared unit, at the row
                        of its first inner cut (see lf_launch_plan).  Zero between

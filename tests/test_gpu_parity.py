@@ -275,9 +275,8 @@ def test_planned_launch_choice():
     """A layer whose sequences all hold >= 2048 tokens takes a launch plan when
     the host's cost model prefers it to whole units: batches 64, 32 and 4 at
     budget 3276 on two-CTA clusters do (units shared by two clusters, and by
-    three or more).  The plan covers every unit once.  An empty layer, and a
-    cache with the layer scope, never takes one; the deferred order and the
-    H2O score do."""
+    three or more).  The plan covers every unit once.  An empty layer never
+    takes one; the deferred order, the H2O score and the layer scope do."""
     from decode_kv_cache_gb300.longflow import LFCache
     clusters = torch.cuda.get_device_properties(0).multi_processor_count // 2
     for batch in (32, 4):
@@ -306,12 +305,8 @@ def test_planned_launch_choice():
         _check_plan(plan, 512, clusters)
     finally:
         cache.close()
-    cache = LFCache(1, 32, 8, 32, 128, 3276, 64, scope="layer")
-    try:
-        assert cache.layout.split_units == 0 and cache.plan(0) is None
-    finally:
-        cache.close()
-    for kw, prompt in ((dict(deferred=True), 3275), (dict(score="h2o"), 3276)):
+    for kw, prompt in ((dict(deferred=True), 3275), (dict(score="h2o"), 3276),
+                       (dict(scope="layer"), 3276)):
         cache = LFCache(1, 32, 8, 32, 128, 3276, 64, **kw)
         try:
             k = torch.zeros(32, 8, 3276, 128, dtype=torch.bfloat16, device="cuda")
