@@ -948,7 +948,8 @@ int lf_decode_step(lf_cache* cache, int layer, const void* q, const void* k_new,
     return fail(LF_ERR_ARG, "layer %d outside [0, %d)", layer, cache->layers);
   if (!q || !k_new || !v_new || !out || !evicted_slot)
     return fail(LF_ERR_ARG, "null q, k_new, v_new, out or evicted_slot");
-  if (!aligned16(q)) return fail(LF_ERR_ARG, "q must be 16-byte aligned");
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new))
+    return fail(LF_ERR_ARG, "q, k_new and v_new must be 16-byte aligned");
   const size_t layer_units = (size_t)cache->batch * cache->kv_heads;
   const size_t layer_slots = layer_units * cache->slot_stride;
   lf::DecodeArgs a;

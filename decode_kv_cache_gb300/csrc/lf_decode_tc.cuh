@@ -1002,6 +1002,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ---- tail warps 6-7: exchange, exact scores, leader's output and eviction -----
     const int tt_id = tid - kTcTailWarp0 * 32;  // 0..63
     const int twarp = tt_id >> 5;
+    // The new token's k and v and the group's queries of an item, in 16-byte
+    // chunks, loaded into registers one item ahead: under a saturated HBM their
+    // latency is microseconds, and it passes while the tail works on the
+    // previous unit.  Tail thread t holds query chunks c = t + 64 i (head c / 16,
+    // elements 8 (c mod 16) ...), key chunk t mod 16 and, for t < 16, value chunk t.
+    constexpr int kNq = (G * 16 + kTcTail - 1) / kTcTail;
+    uint4 nq[kNq], nk = make_uint4(0, 0, 0, 0), nv = make_uint4(0, 0, 0, 0);
+    auto load_new = [&](int kk) {
+      const int uu = unit_of(kk);
+      const int bb = uu / a.kv_heads;
+      const uint4* qs = reinterpret_cast<const uint4*>(
+          reinterpret_cast<const T*>(a.q) + ((size_t)bb * a.q_heads + (size_t)(uu - bb * a.kv_heads) * G) * D);
+#pragma unroll
+      for (int i = 0; i < kNq; ++i) {
+        const int c = tt_id + kTcTail * i;
+        nq[i] = (c < G * 16) ? qs[c] : make_uint4(0, 0, 0, 0);
+      }
+      nk = reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(a.k_new) + (size_t)uu * D)[tt_id & 15];
+      if (tt_id < 16)
+        nv = reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(a.v_new) + (size_t)uu * D)[tt_id];
+    };
+    if (nitems > 0) load_new(0);
     for (int k = 0; k < nitems; ++k) {
       int n, p, base;
       bool state_ok;
@@ -1019,30 +1041,38 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const float* o_part = opbase + (size_t)b2 * G * D;
       const float* w_s = reinterpret_cast<const float*>(vnbase + (4 + b2) * P::vn_bytes(chunk));
       const size_t ubase = (size_t)u * a.slot_stride;
-      const T* qg = reinterpret_cast<const T*>(a.q) + ((size_t)b * a.q_heads + (size_t)g * G) * D;
-      const T* kn = reinterpret_cast<const T*>(a.k_new) + (size_t)u * D;
-      const T* vn = reinterpret_cast<const T*>(a.v_new) + (size_t)u * D;
       float* snw = s_new + b2 * kMaxGroup;
       const float* mlc = m_loc + b2 * kMaxGroup;
       const float* llc = l_loc + b2 * kMaxGroup;
       // The new token's k and v in shared memory for the leader's output and slot
-      // write: loaded here, their latency passes while the tail waits for the
-      // unit's statistics, not after the last exchange (the barrier after that
-      // wait orders the copy for both tail warps).
+      // write (the barrier after the statistics wait below orders the copy for
+      // both tail warps), and its logits (every CTA computes them): the dot
+      // products of this thread's query chunks with the key chunk, summed over
+      // the 16 threads of a head.
       T* nkv = reinterpret_cast<T*>(smem + P::kOffNew) + (size_t)b2 * 2 * D;  // [k | v]
-      for (int e = tt_id; e < D; e += kTcTail) {
-        nkv[e] = kn[e];
-        nkv[D + e] = vn[e];
+      if (tt_id < 16) {
+        reinterpret_cast<uint4*>(nkv)[tt_id] = nk;
+        reinterpret_cast<uint4*>(nkv + D)[tt_id] = nv;
       }
-
-      // The new token's logits (every CTA computes them), before the waits.
-      for (int h = twarp; h < G; h += 2) {
+#pragma unroll
+      for (int i = 0; i < kNq; ++i) {
+        const int c = tt_id + kTcTail * i;
+        const uint32_t qw[4] = {nq[i].x, nq[i].y, nq[i].z, nq[i].w};
+        const uint32_t kw[4] = {nk.x, nk.y, nk.z, nk.w};
         float s = 0.f;
-        for (int e = lane; e < D; e += 32)
-          s = fmaf(to_f32(qg[(size_t)h * D + e]), to_f32(kn[e]), s);
-        s = warp_sum(s);
-        if (lane == 0) snw[h] = s * a.scale_log2;
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          const float2 qf = bf2_to_f2(qw[x]);
+          const float2 kf = bf2_to_f2(kw[x]);
+          s = fmaf(qf.x, kf.x, s);
+          s = fmaf(qf.y, kf.y, s);
+        }
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if ((tt_id & 15) == 0 && c < G * 16) snw[c >> 4] = s * a.scale_log2;
       }
+      // The next item's, in the background.
+      if (k + 1 < nitems) load_new(k + 1);
       // This CTA's (m, l), logits and weights: exchanged and scored while the
       // unit's V tiles still stream.
       const bool got_loc = __all_sync(

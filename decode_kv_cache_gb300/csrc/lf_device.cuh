@@ -131,6 +131,11 @@ __device__ __forceinline__ void load4_f32(const __nv_bfloat16* src, float* dst) 
   dst[3] = __uint_as_float(x.y & 0xffff0000u);
 }
 
+// Two packed bf16 (the lower address in the low half) as floats.
+__device__ __forceinline__ float2 bf2_to_f2(uint32_t x) {
+  return make_float2(__uint_as_float(x << 16), __uint_as_float(x & 0xffff0000u));
+}
+
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
 __device__ __forceinline__ void from_f32(float v, float* dst) { *dst = v; }

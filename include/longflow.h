@@ -201,7 +201,8 @@ int lf_prefill_fill(lf_cache* cache, int layer, const void* k, const void* v,
 /*
  * One fused decode step of one layer for every sequence (see the top of the
  * file).  All buffers are caller-owned, contiguous device memory that must
- * stay valid until the stream reaches the call:
+ * stay valid until the stream reaches the call (q, k_new and v_new 16-byte
+ * aligned):
  *   q             [batch][q_heads][head_dim]   cache dtype
  *   k_new, v_new  [batch][kv_heads][head_dim]  cache dtype (the token's stored values)
  *   out           [batch][q_heads][head_dim]   cache dtype (fp32 accumulation, RNE rounding)

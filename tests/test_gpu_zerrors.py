@@ -1,5 +1,5 @@
 """Host-detected errors on a real device: a slab larger than the GPU, a prompt
-longer than the buffer, a misaligned query and a layer out of range are each
+longer than the buffer, a misaligned query, key or value and a layer out of range are each
 refused with a message, nothing is launched, and the context stays usable
 (GPU; no fault is provoked)."""
 import pytest
@@ -46,6 +46,13 @@ def test_bad_calls_are_refused_before_any_launch():
         kn = torch.zeros(2, 2, 128, dtype=cache.dtype, device="cuda")
         with pytest.raises(lf.LFError, match="16-byte aligned"):
             cache.decode_step(0, q_mis, kn, kn)
+        m = 2 * 2 * 128
+        kn_mis = torch.zeros(m + 1, dtype=cache.dtype, device="cuda")[1:].view(2, 2, 128)
+        q = torch.zeros(2, 4, 128, dtype=cache.dtype, device="cuda")
+        with pytest.raises(lf.LFError, match="16-byte aligned"):
+            cache.decode_step(0, q, kn_mis, kn)
+        with pytest.raises(lf.LFError, match="16-byte aligned"):
+            cache.decode_step(0, q, kn, kn_mis)
         with pytest.raises(lf.LFError, match="outside"):
             cache.decode_step(2, torch.zeros(2, 4, 128, dtype=cache.dtype, device="cuda"), kn, kn)
         # nothing was written by the refused calls; a normal step still works
