@@ -527,77 +527,95 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint64_t pol = l2_evict_first_policy();
       bool fail = false;
       int tt = 0;  // tiles produced
-      // Issue tiles [t0, t1) of unit k (K when isK) into the ring.
-      auto emit = [&](int k, int rows, int base, bool isK, int t0, int t1) {
-        const int u = unit_of(k);
-        const int unit_row = ta.row_base + u * a.slot_stride + base;
-        const void* m64 = isK ? (const void*)&ta.k64 : (const void*)&ta.v64;
-        const void* m16 = isK ? (const void*)&ta.k16 : (const void*)&ta.v16;
-        for (int t = t0; t < t1 && !fail; ++t, ++tt) {
-          const int st = tt % S;
-          if (tt >= S && !mbar_wait_bounded(&empty[st], (uint32_t)(((tt / S) - 1) & 1))) {
-            fail = true;
-            break;
-          }
-          const int r0 = t * kTcTile;
-          const int rr = (min(kTcTile, rows - r0) + 15) & ~15;  // 16-row granules
-          unsigned char* dst = ring + (size_t)st * P::kStage;
-          mbar_arrive_expect_tx(&full[st], (uint32_t)(rr * D * 2));
-          for (int blk = 0; blk < 2; ++blk) {
-            int ro = 0;
-            for (; ro + 64 <= rr; ro += 64)
-              tma_load_2d(dst + blk * P::kBlock + ro * 128, m64, blk * 64, unit_row + r0 + ro,
-                          &full[st], pol);
-            for (; ro < rr; ro += 16)
-              tma_load_2d(dst + blk * P::kBlock + ro * 128, m16, blk * 64, unit_row + r0 + ro,
-                          &full[st], pol);
-          }
-        }
-      };
+      // Each step of the walk is up to five segments in ring order, issued by one
+      // loop (one copy of the issue code): 0, a pending V(prev) that the walk has
+      // passed; 1, unit k's norms and positions; 2, its first K tiles (all of them
+      // when nothing is pending); 3, V(prev); 4, the rest of its K tiles.  Step
+      // nitems only flushes.
       int prev = -1, prev_rows = 0, prev_base = 0;
-      for (int k = 0; k < nitems && !fail; ++k) {
-        if (prev >= 0 && prev <= k - 2) {
-          emit(prev, prev_rows, prev_base, false, 0, (prev_rows + kTcTile - 1) / kTcTile);
-          prev = -1;
+      for (int k = 0; k <= nitems && !fail; ++k) {
+        const bool flush = prev >= 0 && (k == nitems || prev <= k - 2);
+        const int fk = prev, frows = prev_rows, fbase = prev_base;
+        if (flush) prev = -1;
+        int rows = 0, base = 0, ntile = 0, L = 0;
+        if (k < nitems) {
+          int n, p;
+          bool ok;
+          rows = unit_rows(k, n, p, ok, base);
+          ntile = (rows + kTcTile - 1) / kTcTile;
+          L = (prev < 0) ? ntile : min(ntile, kTcLookahead);
         }
-        int n, p, base;
-        bool ok;
-        const int rows = unit_rows(k, n, p, ok, base);
-        const int u = unit_of(k);
-        const size_t ubase = (size_t)u * a.slot_stride;
-        const int b2 = k & 1;
-        if (k >= 2 && !mbar_wait_bounded(&auxfree[b2], (uint32_t)(((k >> 1) - 1) & 1))) {
-          fail = true;
-          break;
+        const bool pend = prev >= 0 && rows > 0;  // V(prev) between this unit's K tiles
+#pragma unroll 1
+        for (int si = 0; si < 5 && !fail; ++si) {
+          // this segment: unit item gk (rows, first slot), kind, tiles [t0, t1)
+          int gk = k, grows = rows, gbase = base, t0 = 0, t1 = 0;
+          bool isK = true;
+          if (si == 0 || si == 3) {
+            if (si == 0 ? !flush : !pend) continue;
+            gk = (si == 0) ? fk : prev;
+            grows = (si == 0) ? frows : prev_rows;
+            gbase = (si == 0) ? fbase : prev_base;
+            isK = false;
+            t1 = (grows + kTcTile - 1) / kTcTile;
+          } else if (si == 1) {
+            if (k == nitems) continue;
+            // unit k's ||v||_1 (H2O: accumulators) and positions, once the
+            // epilogue has read this parity's buffers (unit k - 2)
+            const int b2 = k & 1;
+            if (k >= 2 && !mbar_wait_bounded(&auxfree[b2], (uint32_t)(((k >> 1) - 1) & 1))) {
+              fail = true;
+              break;
+            }
+            if (rows > 0 && a.evict) {
+              const size_t ub = (size_t)unit_of(k) * a.slot_stride + base;
+              const uint32_t small = (uint32_t)(((rows + 3) & ~3) * 4);
+              unsigned char* vdst = vnbase + b2 * P::vn_bytes(chunk);
+              unsigned char* pdst = vnbase + (2 + b2) * P::vn_bytes(chunk);
+              mbar_arrive_expect_tx(&aux[b2], 2u * small);
+              bulk_g2s(vdst, (a.score == LF_SCORE_H2O ? a.acc : a.vnorm) + ub, small, &aux[b2],
+                       pol);
+              bulk_g2s(pdst, a.pos + ub, small, &aux[b2], pol);
+            } else {
+              mbar_arrive(&aux[b2]);  // nothing to load: complete the phase
+            }
+            continue;
+          } else {
+            t0 = (si == 2) ? 0 : L;
+            t1 = (si == 2) ? L : ntile;
+          }
+          // Tiles [t0, t1) of the unit (K or V) into the ring.
+          const int unit_row = ta.row_base + unit_of(gk) * a.slot_stride + gbase;
+          const void* m64 = isK ? (const void*)&ta.k64 : (const void*)&ta.v64;
+          const void* m16 = isK ? (const void*)&ta.k16 : (const void*)&ta.v16;
+#pragma unroll 1
+          for (int t = t0; t < t1; ++t, ++tt) {
+            const int st = tt % S;
+            if (tt >= S && !mbar_wait_bounded(&empty[st], (uint32_t)(((tt / S) - 1) & 1))) {
+              fail = true;
+              break;
+            }
+            const int r0 = t * kTcTile;
+            const int rr = (min(kTcTile, grows - r0) + 15) & ~15;  // 16-row granules
+            unsigned char* dst = ring + (size_t)st * P::kStage;
+            mbar_arrive_expect_tx(&full[st], (uint32_t)(rr * D * 2));
+            for (int blk = 0; blk < 2; ++blk) {
+              int ro = 0;
+              for (; ro + 64 <= rr; ro += 64)
+                tma_load_2d(dst + blk * P::kBlock + ro * 128, m64, blk * 64, unit_row + r0 + ro,
+                            &full[st], pol);
+              for (; ro < rr; ro += 16)
+                tma_load_2d(dst + blk * P::kBlock + ro * 128, m16, blk * 64, unit_row + r0 + ro,
+                            &full[st], pol);
+            }
+          }
         }
-        if (rows > 0 && a.evict) {
-          const uint32_t small = (uint32_t)(((rows + 3) & ~3) * 4);
-          unsigned char* vdst = vnbase + b2 * P::vn_bytes(chunk);
-          unsigned char* pdst = vnbase + (2 + b2) * P::vn_bytes(chunk);
-          mbar_arrive_expect_tx(&aux[b2], 2u * small);
-          bulk_g2s(vdst, (a.score == LF_SCORE_H2O ? a.acc : a.vnorm) + ubase + base, small,
-                   &aux[b2], pol);
-          bulk_g2s(pdst, a.pos + ubase + base, small, &aux[b2], pol);
-        } else {
-          mbar_arrive(&aux[b2]);  // nothing to load: complete the phase
+        if (k < nitems && rows > 0) {
+          prev = k;
+          prev_rows = rows;
+          prev_base = base;
         }
-        if (rows == 0) continue;
-        const int ntile = (rows + kTcTile - 1) / kTcTile;
-        if (prev < 0) {
-          emit(k, rows, base, true, 0, ntile);
-        } else {
-          const int L = min(ntile, kTcLookahead);
-          const int pnt = (prev_rows + kTcTile - 1) / kTcTile;
-          emit(k, rows, base, true, 0, L);
-          emit(prev, prev_rows, prev_base, false, 0, pnt);
-          emit(k, rows, base, true, L, ntile);
-        }
-        prev = k;
-        prev_rows = rows;
-        prev_base = base;
       }
-      if (prev >= 0 && !fail)
-        emit(prev, prev_rows, prev_base, false, 0, (prev_rows + kTcTile - 1) / kTcTile);
       // Every copy issued lands before the CTA may exit.
       for (int t = max(0, tt - S); t < tt; ++t)
         (void)mbar_wait_bounded(&full[t % S], (uint32_t)((t / S) & 1));
@@ -616,6 +634,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     int nq[2] = {0, 0};
     // K tiles [t0, t1) of a unit: S^T = K . q^T into the next free logit accumulator.
     auto mma_k = [&](int t0, int t1, uint32_t qaddr) {
+#pragma unroll 1
       for (int t = t0; t < t1 && !fail; ++t, ++tt, ++kt) {
         const int st = tt % S;
         const int buf = kt % kTcSBufs;
@@ -641,6 +660,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // All V tiles of a unit: O^T += V^T . P^T, then signal the output.
     auto mma_v = [&](int rows) {
       const int ntile = (rows + kTcTile - 1) / kTcTile;
+#pragma unroll 1
       for (int vt = 0; vt < ntile && !fail; ++vt, ++tt, ++pt) {
         const int st = tt % S;
         const int pb = pt % kTcPBufs;
@@ -684,63 +704,72 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       qreg_item = kk;
     };
     if (nitems > 0) load_q(0);
+    // The producer's walk, step by step: its tile segments in ring order (0, a
+    // pending V(prev); 2, unit k's first K tiles; 3, V(prev); 4, the rest of its
+    // K tiles), issued by lane 0 through one copy of each MMA loop.
     int prev = -1, prev_rows = 0;
-    for (int k = 0; k < nitems && !fail; ++k) {
-      if (prev >= 0 && prev <= k - 2) {  // same flush rule as the producer
-        if (lane == 0) mma_v(prev_rows);
-        prev = -1;
-        fail = __shfl_sync(0xffffffffu, fail ? 1 : 0, 0) != 0;
-        if (fail) break;
+    for (int k = 0; k <= nitems && !fail; ++k) {
+      const bool flush = prev >= 0 && (k == nitems || prev <= k - 2);
+      const int frows = prev_rows;
+      if (flush) prev = -1;
+      int rows = 0, qb = 0, ntile = 0, L = 0;
+      uint32_t qaddr = 0;
+      if (k < nitems) {
+        int n, p, base;
+        bool ok;
+        rows = unit_rows(k, n, p, ok, base);
       }
-      int n, p, base;
-      bool ok;
-      const int rows = unit_rows(k, n, p, ok, base);
-      if (rows == 0) continue;
-      const int ntile = (rows + kTcTile - 1) / kTcTile;
-      const int qb = nn & 1;
-      unsigned char* qdst = qbuf + qb * P::kQBytes;
-      // The buffer's previous contents (two units ago) must have been read.
-      bool okq = true;
-      if (lane == 0 && nq[qb] > 0)
-        okq = mbar_wait_bounded(&qfree[qb], (uint32_t)((nq[qb] - 1) & 1));
-      if (__shfl_sync(0xffffffffu, okq ? 1 : 0, 0) == 0) {
-        fail = true;
-        break;
-      }
-      // q^T rows h < G: the group's queries (16-byte chunks, 128-byte swizzle).
-      if (qreg_item != k) load_q(k);   // not fetched ahead (an empty unit came between)
+      if (rows > 0) {
+        ntile = (rows + kTcTile - 1) / kTcTile;
+        L = (prev < 0) ? ntile : min(ntile, kTcLookahead);
+        qb = nn & 1;
+        unsigned char* qdst = qbuf + qb * P::kQBytes;
+        // The buffer's previous contents (two units ago) must have been read.
+        bool okq = true;
+        if (lane == 0 && nq[qb] > 0)
+          okq = mbar_wait_bounded(&qfree[qb], (uint32_t)((nq[qb] - 1) & 1));
+        if (__shfl_sync(0xffffffffu, okq ? 1 : 0, 0) == 0) {
+          fail = true;
+          break;
+        }
+        // q^T rows h < G: the group's queries (16-byte chunks, 128-byte swizzle).
+        if (qreg_item != k) load_q(k);   // not fetched ahead (an empty unit came between)
 #pragma unroll
-      for (int i = 0; i < kQChunks; ++i) {
-        const int c = lane + 32 * i;
-        if (c < G * 16) {
-          const int h = c >> 4;
-          const int ch = c & 15;
-          *reinterpret_cast<uint4*>(qdst + (ch >> 3) * 2048 + h * 128 + (((ch & 7) ^ (h & 7)) << 4)) =
-              qreg[i];
+        for (int i = 0; i < kQChunks; ++i) {
+          const int c = lane + 32 * i;
+          if (c < G * 16) {
+            const int h = c >> 4;
+            const int ch = c & 15;
+            *reinterpret_cast<uint4*>(qdst + (ch >> 3) * 2048 + h * 128 + (((ch & 7) ^ (h & 7)) << 4)) =
+                qreg[i];
+          }
         }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (k + 1 < nitems) load_q(k + 1);   // the next unit's queries, in the background
+        qaddr = smem_u32(qdst);
       }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (k + 1 < nitems) load_q(k + 1);   // the next unit's queries, in the background
+      const bool pend = prev >= 0 && rows > 0;
       if (lane == 0) {
-        const uint32_t qaddr = smem_u32(qdst);
-        if (prev < 0) {
-          mma_k(0, ntile, qaddr);
-        } else {
-          const int L = min(ntile, kTcLookahead);
-          mma_k(0, L, qaddr);
-          mma_v(prev_rows);
-          mma_k(L, ntile, qaddr);
+#pragma unroll 1
+        for (int si = 0; si < 5 && !fail; ++si) {
+          if (si == 0 || si == 3) {
+            if (si == 0 ? !flush : !pend) continue;
+            mma_v(si == 0 ? frows : prev_rows);
+          } else if (si != 1 && rows > 0) {
+            mma_k(si == 2 ? 0 : L, si == 2 ? L : ntile, qaddr);
+          }
         }
-        tc_commit(&qfree[qb]);
+        if (rows > 0) tc_commit(&qfree[qb]);
       }
-      nq[qb] += 1;
-      nn += 1;
-      prev = k;
-      prev_rows = rows;
+      if (rows > 0) {
+        nq[qb] += 1;
+        nn += 1;
+        prev = k;
+        prev_rows = rows;
+      }
       fail = __shfl_sync(0xffffffffu, fail ? 1 : 0, 0) != 0;
     }
-    if (lane == 0 && prev >= 0 && !fail) mma_v(prev_rows);
     if (lane == 0) {
       // Every MMA issued completes before tensor memory is released.
       tc_commit(drain);
@@ -782,6 +811,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         float cm[G];
 #pragma unroll
         for (int h = 0; h < G; ++h) cm[h] = cmul[h];
+#pragma unroll 1
         for (int i0 = score_split(rows) + tid; i0 < rows; i0 += kScoreRows * kTcCompute) {
           float wv[kScoreRows], asv[kScoreRows];
 #pragma unroll
@@ -857,6 +887,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       float mx[G];
 #pragma unroll
       for (int h = 0; h < G; ++h) mx[h] = -INFINITY;
+#pragma unroll 1
       for (int t = 0; t < ntile && !bad; ++t, ++kt) {
         const int buf = kt % kTcSBufs;
         if (!__all_sync(0xffffffffu,
@@ -908,6 +939,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         // p = 2^(s - m) (kept in fp32 for the score) and the bf16 hi/lo P^T operand,
         // ahead of the MMAs in a ring of kTcPBufs tiles; slots past `rows` are zero.
+#pragma unroll 1
         for (int vt = 0; vt < ntile; ++vt, ++pt) {
           const int pb = pt % kTcPBufs;
           if (pt >= kTcPBufs &&
@@ -1116,8 +1148,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (tt_id < G) {
             const int h = tt_id;
             float M = snw[h];
+#pragma unroll 1
             for (int r = 0; r < np; ++r) M = fmaxf(M, sst[r * 2 * kMaxGroup + h]);
             float L = exp2f(snw[h] - M);
+#pragma unroll 1
             for (int r = 0; r < np; ++r) {
               const float mr = sst[r * 2 * kMaxGroup + h];
               if (mr != -INFINITY) L += sst[r * 2 * kMaxGroup + kMaxGroup + h] * exp2f(mr - M);
@@ -1126,6 +1160,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             l_glb[h] = L;
             cmul[h] = (mlc[h] != -INFINITY) ? exp2f(mlc[h] - M) / L : 0.f;
             // the leader's output scales: each part's, then the new token's
+#pragma unroll 1
             for (int r = 0; r < np; ++r) {
               const float mr = sst[r * 2 * kMaxGroup + h];
               osc[r * kMaxGroup + h] = (mr != -INFINITY) ? exp2f(mr - M) / L : 0.f;
@@ -1152,6 +1187,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             float cm[G];
 #pragma unroll
             for (int h = 0; h < G; ++h) cm[h] = cmul[h];
+#pragma unroll 1
             for (int i0 = tt_id; i0 < rows; i0 += kScoreRows * kTcTail) {
               float wv[kScoreRows], asv[kScoreRows];
 #pragma unroll
@@ -1208,6 +1244,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             float cm[G];
 #pragma unroll
             for (int h = 0; h < G; ++h) cm[h] = cmul[h];
+#pragma unroll 1
             for (int i = tt_id; i < rows; i += kTcTail) {
               const int slot = base + i;
               if (slot == rl.excl || slot == ci) continue;
@@ -1279,6 +1316,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                   const int e = (lane + 32 * i) - h * D;
                   acc[i] = to_f32(nkv[D + e]) * osc[np * kMaxGroup + h];
                 }
+#pragma unroll 1
                 for (int r = 0; r < np; ++r) {
                   float part[kEl];
 #pragma unroll
@@ -1336,6 +1374,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           v[h] = __float_as_uint(h < G ? mlc[h] : -INFINITY);
           v[kMaxGroup + h] = __float_as_uint(h < G ? llc[h] : 0.f);
         }
+#pragma unroll 1
         for (int r = 0; r < C; ++r) {
           const uint32_t ra = mapa_u32(src, (uint32_t)r);
           const uint32_t rb = mapa_u32(bar, (uint32_t)r);
@@ -1354,8 +1393,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (tt_id < G) {
         const int h = tt_id;
         float M = snw[h];
+#pragma unroll 1
         for (int r = 0; r < C; ++r) M = fmaxf(M, sin[r * 2 * kMaxGroup + h]);
         float L = exp2f(snw[h] - M);
+#pragma unroll 1
         for (int r = 0; r < C; ++r) {
           const float mr = sin[r * 2 * kMaxGroup + h];
           if (mr != -INFINITY) L += sin[r * 2 * kMaxGroup + kMaxGroup + h] * exp2f(mr - M);
@@ -1364,6 +1405,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         l_glb[h] = L;
         cmul[h] = (mlc[h] != -INFINITY) ? exp2f(mlc[h] - M) / L : 0.f;
         // the leader's output scales: each CTA's, then the new token's
+#pragma unroll 1
         for (int r = 0; r < C; ++r) {
           const float mr = sin[r * 2 * kMaxGroup + h];
           osc[r * kMaxGroup + h] = (mr != -INFINITY) ? exp2f(mr - M) / L : 0.f;
@@ -1402,6 +1444,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int h = 0; h < G; ++h) cm[h] = cmul[h];
         // kScoreRows rows per pass, their loads issued together (the lowest
         // (score, slot) does not depend on the order rows are visited in).
+#pragma unroll 1
         for (int i0 = tt_id; i0 < srows; i0 += kScoreRows * kTcTail) {
           float wv[kScoreRows], asv[kScoreRows];
 #pragma unroll
@@ -1462,6 +1505,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         float cm[G];
 #pragma unroll
         for (int h = 0; h < G; ++h) cm[h] = cmul[h];
+#pragma unroll 1
         for (int i = tt_id; i < rows; i += kTcTail) {
           const int slot = base + i;
           if (slot == rl.excl || slot == ci) continue;
@@ -1523,6 +1567,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
               for (int x = 0; x < 4; ++x) acc[h][x] = to_f32(nkv[D + e0 + x]) * sn;
             }
+#pragma unroll 1
             for (int r = 0; r < C; ++r) {
               const float* fr = reinterpret_cast<const float*>(fin + (size_t)r * P::kFinBytes);
               float4 pr[G];
@@ -1549,6 +1594,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             bool any_fail = !all_got || !stats_ok;
             float fs = INFINITY;
             int fi = INT_MAX;
+#pragma unroll 1
             for (int r = 0; r < C; ++r) {
               const uint32_t* tail =
                   reinterpret_cast<const uint32_t*>(fin + (size_t)r * P::kFinBytes + G * D * 4);
@@ -1568,6 +1614,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // H2O: the accumulators of the CTAs' lowest candidates (their scores),
             // except the slot the new token takes.
             if (h2o && !layer && state_ok && !any_fail)
+#pragma unroll 1
               for (int r = 0; r < C; ++r) {
                 const uint32_t* tail =
                     reinterpret_cast<const uint32_t*>(fin + (size_t)r * P::kFinBytes + G * D * 4);
