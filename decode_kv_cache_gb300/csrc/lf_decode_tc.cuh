@@ -1187,36 +1187,46 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             float cm[G];
 #pragma unroll
             for (int h = 0; h < G; ++h) cm[h] = cmul[h];
+            if (!layer) {
 #pragma unroll 1
-            for (int i0 = tt_id; i0 < rows; i0 += kScoreRows * kTcTail) {
-              float wv[kScoreRows], asv[kScoreRows];
+              for (int i0 = tt_id; i0 < rows; i0 += kScoreRows * kTcTail) {
+                float wv[kScoreRows], asv[kScoreRows];
 #pragma unroll
-              for (int jr = 0; jr < kScoreRows; ++jr) {
-                const int i = i0 + jr * kTcTail;
-                wv[jr] = 0.f;
-                asv[jr] = 0.f;
-                if (i < rows) {
-                  wv[jr] = w_s[i];
-                  asv[jr] = group_dot<G>(lg + (size_t)i * G, cm);
+                for (int jr = 0; jr < kScoreRows; ++jr) {
+                  const int i = i0 + jr * kTcTail;
+                  wv[jr] = 0.f;
+                  asv[jr] = 0.f;
+                  if (i < rows) {
+                    wv[jr] = w_s[i];
+                    asv[jr] = group_dot<G>(lg + (size_t)i * G, cm);
+                  }
+                }
+#pragma unroll
+                for (int jr = 0; jr < kScoreRows; ++jr) {
+                  const int i = i0 + jr * kTcTail;
+                  const int slot = base + i;
+                  if (i >= rows) break;
+                  const float w = wv[jr];
+                  const float sc = h2o ? fabsf(w) + asv[jr] : fabsf(w) * asv[jr];
+                  if (slot != rl.excl && rl.choosing && is_candidate(w) && better(sc, slot, bs, bi)) {
+                    bs = sc;
+                    bi = slot;
+                  }
                 }
               }
-#pragma unroll
-              for (int jr = 0; jr < kScoreRows; ++jr) {
-                const int i = i0 + jr * kTcTail;
+            } else {
+#pragma unroll 1
+              for (int i = tt_id; i < rows; i += kTcTail) {
                 const int slot = base + i;
-                if (i >= rows) break;
                 if (slot == rl.excl) {
-                  if (layer && rl.choosing) a.lw_score[ubase + slot] = INFINITY;
+                  if (rl.choosing) a.lw_score[ubase + slot] = INFINITY;
                   continue;
                 }
-                const float sc = h2o ? fabsf(wv[jr]) + asv[jr] : fabsf(wv[jr]) * asv[jr];
-                if (layer) {
-                  if (h2o) a.acc[ubase + slot] = sc;
-                  if (rl.choosing) a.lw_score[ubase + slot] = is_candidate(wv[jr]) ? sc : INFINITY;
-                } else if (rl.choosing && is_candidate(wv[jr]) && better(sc, slot, bs, bi)) {
-                  bs = sc;
-                  bi = slot;
-                }
+                const float w = w_s[i];
+                const float as = group_dot<G>(lg + (size_t)i * G, cm);
+                const float sc = h2o ? fabsf(w) + as : fabsf(w) * as;
+                if (h2o) a.acc[ubase + slot] = sc;
+                if (rl.choosing) a.lw_score[ubase + slot] = is_candidate(w) ? sc : INFINITY;
               }
             }
           }
@@ -1442,40 +1452,51 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         float cm[G];
 #pragma unroll
         for (int h = 0; h < G; ++h) cm[h] = cmul[h];
-        // kScoreRows rows per pass, their loads issued together (the lowest
-        // (score, slot) does not depend on the order rows are visited in).
+        if (!layer) {
+          // The lowest (score, slot) of this CTA's candidates, kScoreRows rows per
+          // pass with their loads issued together (the result does not depend on
+          // the order rows are visited in).
 #pragma unroll 1
-        for (int i0 = tt_id; i0 < srows; i0 += kScoreRows * kTcTail) {
-          float wv[kScoreRows], asv[kScoreRows];
+          for (int i0 = tt_id; i0 < srows; i0 += kScoreRows * kTcTail) {
+            float wv[kScoreRows], asv[kScoreRows];
 #pragma unroll
-          for (int jr = 0; jr < kScoreRows; ++jr) {
-            const int i = i0 + jr * kTcTail;
-            wv[jr] = 0.f;
-            asv[jr] = 0.f;
-            if (i < srows) {
-              wv[jr] = w_s[i];
-              asv[jr] = group_dot<G>(lg + (size_t)i * G, cm);
+            for (int jr = 0; jr < kScoreRows; ++jr) {
+              const int i = i0 + jr * kTcTail;
+              wv[jr] = 0.f;
+              asv[jr] = 0.f;
+              if (i < srows) {
+                wv[jr] = w_s[i];
+                asv[jr] = group_dot<G>(lg + (size_t)i * G, cm);
+              }
+            }
+#pragma unroll
+            for (int jr = 0; jr < kScoreRows; ++jr) {
+              const int i = i0 + jr * kTcTail;
+              const int slot = base + i;
+              if (i >= srows) break;
+              const float w = wv[jr];
+              const float sc = h2o ? fabsf(w) + asv[jr] : fabsf(w) * asv[jr];
+              if (slot != rl.excl && rl.choosing && is_candidate(w) && better(sc, slot, bs, bi)) {
+                bs = sc;
+                bi = slot;
+              }
             }
           }
-#pragma unroll
-          for (int jr = 0; jr < kScoreRows; ++jr) {
-            const int i = i0 + jr * kTcTail;
+        } else {
+          // Layer scope: every score to the scratch (+inf for a non-candidate),
+          // and the H2O accumulators written back.
+#pragma unroll 1
+          for (int i = tt_id; i < srows; i += kTcTail) {
             const int slot = base + i;
-            if (i >= srows) break;
             if (slot == rl.excl) {
-              if (layer && rl.choosing) a.lw_score[ubase + slot] = INFINITY;
+              if (rl.choosing) a.lw_score[ubase + slot] = INFINITY;
               continue;
             }
-            const float w = wv[jr];
-            const float val = fabsf(w);
-            const float sc = h2o ? val + asv[jr] : val * asv[jr];
-            if (layer) {
-              if (h2o) a.acc[ubase + slot] = sc;
-              if (rl.choosing) a.lw_score[ubase + slot] = is_candidate(w) ? sc : INFINITY;
-            } else if (rl.choosing && is_candidate(w) && better(sc, slot, bs, bi)) {
-              bs = sc;
-              bi = slot;
-            }
+            const float w = w_s[i];
+            const float as = group_dot<G>(lg + (size_t)i * G, cm);
+            const float sc = h2o ? fabsf(w) + as : fabsf(w) * as;
+            if (h2o) a.acc[ubase + slot] = sc;
+            if (rl.choosing) a.lw_score[ubase + slot] = is_candidate(w) ? sc : INFINITY;
           }
         }
       }
